@@ -1,0 +1,422 @@
+"""Pins for the CPU fp64 oracle, against facts that do not come from the oracle itself.
+
+Each pin names the page passage (or the mathematical fact) it rests on:
+  * brute-force loops over the definition (Flash attention page, "Why attention is
+    memory-bound": softmax(QK^T/sqrt(d)) V);
+  * online softmax = two-pass softmax in exact arithmetic (same page, "Online softmax
+    recurrence");
+  * probability rows sum to one; a per-row constant in S changes nothing;
+  * exact dS rows sum to zero and dQ ignores a common shift of all keys (GProj page,
+    "How the zero sum turns into a false gradient");
+  * central finite differences of the forward (first backward) and of the first
+    backward (second backward, a Hessian-vector product), and of O along the
+    cotangent direction (gdO is that directional derivative);
+  * symbolic differentiation (sympy) and fp64 autograd on tiny cases, both of
+    which know nothing of the hand-derived closed form;
+  * closed-form special cases (N = 1; Q = 0 gives uniform causal attention);
+  * the streaming row/column-pass form of BoB (FlashBoB page, "Two scalar states
+    replace quadratic tensors") equals the closed form.
+A final group plants mistakes in the oracle and checks that these pins catch them.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import attention as A
+
+
+def rel(x, y):
+    x, y = np.asarray(x, np.float64), np.asarray(y, np.float64)
+    n = np.linalg.norm(y)
+    return np.linalg.norm(x - y) / (n if n > 0 else 1.0)
+
+
+def rnd(seed, *shape):
+    return np.random.default_rng(seed).standard_normal(shape)
+
+
+def slice_set(N, d, seed=0):
+    r = np.random.default_rng(seed)
+    return [r.standard_normal((N, d)) for _ in range(7)]  # Q K V dO a b c
+
+
+# ---------------------------------------------------------------- forward ----
+
+def brute_forward(Q, K, V, scale):
+    """Pure-Python loops over the definition: no NumPy linear algebra."""
+    N, d = len(Q), len(Q[0])
+    O = [[0.0] * d for _ in range(N)]
+    L = [0.0] * N
+    for i in range(N):
+        s = [scale * sum(Q[i][t] * K[j][t] for t in range(d)) for j in range(i + 1)]
+        m = max(s)
+        e = [math.exp(x - m) for x in s]
+        tot = sum(e)
+        L[i] = m + math.log(tot)
+        for t in range(d):
+            O[i][t] = sum(e[j] / tot * V[j][t] for j in range(i + 1))
+    return O, L
+
+
+@pytest.mark.parametrize("N,d", [(1, 4), (2, 3), (7, 5), (16, 8)])
+def test_forward_brute_force(N, d):
+    Q, K, V = rnd(1, N, d), rnd(2, N, d), rnd(3, N, d)
+    s = 0.37
+    Ob, Lb = brute_forward(Q.tolist(), K.tolist(), V.tolist(), s)
+    O, L = oracle.forward(Q, K, V, scale=s)
+    assert rel(O, Ob) <= 1e-13
+    assert rel(L, Lb) <= 1e-13
+
+
+@pytest.mark.parametrize("Br,Bc", [(1, 1), (3, 3), (16, 16), (37, 37), (16, 3), (3, 16), (5, 37)])
+def test_online_softmax_equals_two_pass(Br, Bc):
+    N, d = 37, 8
+    Q, K, V = rnd(4, N, d) * 2, rnd(5, N, d) * 2, rnd(6, N, d)
+    O2, L2 = oracle.forward(Q, K, V)
+    O1, L1 = oracle.forward_online(Q, K, V, Br, Bc)
+    assert rel(O1, O2) <= 1e-13
+    assert rel(L1, L2) <= 1e-13
+
+
+def test_probability_rows_sum_to_one_and_are_causal():
+    N, d = 50, 16
+    Q, K = rnd(7, N, d) * 3, rnd(8, N, d) * 3
+    P, L = oracle.softmax_rows(oracle.scores(Q, K, np.arange(N), 0.25))
+    assert np.max(np.abs(P.sum(axis=1) - 1.0)) <= 1e-14
+    assert np.all(P[np.triu_indices(N, 1)] == 0.0)
+    assert np.all(P[np.tril_indices(N)] > 0.0)
+
+
+def test_forward_invariant_to_common_key_shift():
+    N, d = 40, 8
+    Q, K, V = rnd(9, N, d), rnd(10, N, d), rnd(11, N, d)
+    v = rnd(12, d) * 5
+    O0, L0 = oracle.forward(Q, K, V)
+    O1, L1 = oracle.forward(Q, K + v[None, :], V)
+    assert rel(O1, O0) <= 1e-12
+    # L moves by exactly s q_i . v
+    assert np.allclose(L1 - L0, oracle.default_scale(d) * Q @ v, rtol=0, atol=1e-12)
+
+
+def test_forward_uniform_attention_closed_form():
+    """Q = 0: every allowed score is 0, so P_ij = 1/(i+1) for j <= i, O_i is the running
+    mean of V and L_i = log(i+1)."""
+    N, d = 33, 6
+    K, V = rnd(13, N, d), rnd(14, N, d)
+    O, L = oracle.forward(np.zeros((N, d)), K, V)
+    cum = np.cumsum(V, axis=0) / np.arange(1, N + 1)[:, None]
+    assert rel(O, cum) <= 1e-14
+    assert np.allclose(L, np.log(np.arange(1, N + 1)), rtol=0, atol=1e-14)
+
+
+def test_forward_row_blocking_and_sampling_agree():
+    N, d = 70, 8
+    Q, K, V = rnd(15, N, d), rnd(16, N, d), rnd(17, N, d)
+    O, L = oracle.forward(Q, K, V)
+    Ob, Lb = oracle.forward(Q, K, V, block=9)
+    assert rel(Ob, O) <= 1e-15 and rel(Lb, L) <= 1e-15
+    rows = np.array([69, 0, 33, 5])
+    Or, Lr = oracle.forward_rows(Q, K, V, rows)
+    assert rel(Or, O[rows]) <= 1e-15 and rel(Lr, L[rows]) <= 1e-15
+
+
+# --------------------------------------------------------------- backward ----
+
+def loss(Q, K, V, dO, s):
+    O, _ = oracle.forward(Q, K, V, scale=s)
+    return float((O * dO).sum())
+
+
+def fd_grad(f, X, h=1e-5):
+    g = np.zeros_like(X)
+    for idx in np.ndindex(X.shape):
+        e = np.zeros_like(X)
+        e[idx] = h
+        g[idx] = (f(X + e) - f(X - e)) / (2 * h)
+    return g
+
+
+@pytest.mark.parametrize("N,d", [(1, 3), (6, 3), (11, 4)])
+def test_backward_matches_finite_differences(N, d):
+    Q, K, V, dO = (x * 0.8 for x in slice_set(N, d, 20)[:4])
+    s = 0.6
+    g = oracle.backward(Q, K, V, dO, scale=s)
+    gQ = fd_grad(lambda X: loss(X, K, V, dO, s), Q)
+    gK = fd_grad(lambda X: loss(Q, X, V, dO, s), K)
+    gV = fd_grad(lambda X: loss(Q, K, X, dO, s), V)
+    top = max(np.abs(gQ).max(), np.abs(gK).max(), np.abs(gV).max(), 1e-3)
+    assert np.abs(g["dQ"] - gQ).max() <= 1e-8 * top
+    assert np.abs(g["dK"] - gK).max() <= 1e-8 * top
+    assert np.abs(g["dV"] - gV).max() <= 1e-8 * top
+
+
+def test_dS_rows_sum_to_zero():
+    N, d = 60, 16
+    Q, K, V, dO = slice_set(N, d, 21)[:4]
+    t = A._row_terms(Q * 2, K * 2, V, dO, np.arange(N), 0.25)
+    l1 = np.abs(t["dS"]).sum(axis=1)
+    assert np.all(np.abs(t["dS"].sum(axis=1)) <= 1e-13 * np.maximum(l1, 1e-300))
+
+
+def test_backward_invariant_to_common_key_shift():
+    N, d = 45, 8
+    Q, K, V, dO = slice_set(N, d, 22)[:4]
+    v = rnd(23, d) * 7
+    g0 = oracle.backward(Q, K, V, dO)
+    g1 = oracle.backward(Q, K + v[None, :], V, dO)
+    for k in ("dQ", "dK", "dV"):
+        assert rel(g1[k], g0[k]) <= 1e-12, k
+
+
+def test_backward_single_token_closed_form():
+    """N = 1: P = 1, O = V, dV = dO and dS = 0, so dQ = dK = 0."""
+    q, k, v, do = (rnd(i, 1, 5) for i in range(30, 34))
+    g = oracle.backward(q, k, v, do)
+    assert np.all(g["dQ"] == 0) and np.all(g["dK"] == 0)
+    assert np.allclose(g["dV"], do, rtol=0, atol=1e-15)
+
+
+def test_backward_uniform_attention_dV_closed_form():
+    """Q = 0: dV_j = sum_{i >= j} dO_i / (i + 1) and dK = s dS^T Q = 0."""
+    N, d = 29, 5
+    K, V, dO = rnd(34, N, d), rnd(35, N, d), rnd(36, N, d)
+    g = oracle.backward(np.zeros((N, d)), K, V, dO)
+    w = dO / np.arange(1, N + 1)[:, None]
+    want = np.cumsum(w[::-1], axis=0)[::-1]
+    assert rel(g["dV"], want) <= 1e-14
+    assert np.abs(g["dK"]).max() == 0.0
+
+
+def test_backward_sampling_agrees():
+    N, d = 64, 8
+    Q, K, V, dO = slice_set(N, d, 37)[:4]
+    g = oracle.backward(Q, K, V, dO)
+    rows, cols = np.array([63, 3, 40]), np.array([50, 63, 7])
+    assert rel(oracle.backward_rows(Q, K, V, dO, rows), g["dQ"][rows]) <= 1e-14
+    dK, dV = oracle.backward_cols(Q, K, V, dO, cols)
+    assert rel(dK, g["dK"][cols]) <= 1e-14 and rel(dV, g["dV"][cols]) <= 1e-14
+
+
+# ----------------------------------------------------------------- GProj ----
+
+def test_gproj_projected_rows_sum_to_zero_and_rounding_leaves_residual():
+    N, d = 96, 16
+    Q, K, V, dO = slice_set(N, d, 40)[:4]
+    K = K + 10.0  # large common key: the residual then shows up in dQ
+    plain = oracle.backward_bf16_dS(Q, K, V, dO, gproj=False)
+    proj = oracle.backward_bf16_dS(Q, K, V, dO, gproj=True)
+    exact = oracle.backward(Q, K, V, dO)
+    assert proj["dS_proj_rowsum_rel"] <= 1e-13
+    assert plain["dS_proj_rowsum_rel"] > 1e-5          # bf16 rounding leaves a row mass
+    assert rel(proj["dQ"], exact["dQ"]) < rel(plain["dQ"], exact["dQ"])
+
+
+def test_bf16_round_is_round_to_nearest_even():
+    # 1 + 2^-8 is halfway between 1 and 1 + 2^-7: ties to even gives 1.
+    x = np.array([1.0, 1 + 2 ** -8, 1 + 3 * 2 ** -8, -2.5 + 2 ** -9, 3.0e-39])
+    y = A.bf16_round(x)
+    assert y[0] == 1.0 and y[1] == 1.0 and y[2] == 1 + 2 ** -6
+    assert abs(y[3] - x[3]) <= 2 ** -8 * 2.5
+    import torch
+    t = torch.tensor(x, dtype=torch.float32).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(t, y)
+
+
+# -------------------------------------------------------------------- BoB ----
+
+def grads(Q, K, V, dO, s):
+    g = oracle.backward(Q, K, V, dO, scale=s)
+    return g["dQ"], g["dK"], g["dV"]
+
+
+@pytest.mark.parametrize("N,d", [(1, 3), (5, 3), (12, 4), (16, 2)])
+def test_bob_is_hessian_vector_product(N, d):
+    """(gQ, gK, gV) = d/dh grad l(X + h U) at h = 0, U = (a, b, c): central differences."""
+    Q, K, V, dO, a, b, c = slice_set(N, d, 50)
+    s, h = 0.55, 1e-5
+    out = oracle.bob(Q, K, V, dO, a, b, c, scale=s)
+    gp = grads(Q + h * a, K + h * b, V + h * c, dO, s)
+    gm = grads(Q - h * a, K - h * b, V - h * c, dO, s)
+    fd = [(p - m) / (2 * h) for p, m in zip(gp, gm)]
+    top = max(np.abs(x).max() for x in fd)
+    for name, want in zip(("gQ", "gK", "gV"), fd):
+        assert np.abs(out[name] - want).max() <= 1e-8 * max(top, 1e-3), name
+
+
+@pytest.mark.parametrize("N,d", [(1, 3), (9, 4), (16, 8)])
+def test_bob_gdO_is_forward_jvp(N, d):
+    Q, K, V, dO, a, b, c = slice_set(N, d, 51)
+    s, h = 0.4, 1e-5
+    out = oracle.bob(Q, K, V, dO, a, b, c, scale=s)
+    Op, _ = oracle.forward(Q + h * a, K + h * b, V + h * c, scale=s)
+    Om, _ = oracle.forward(Q - h * a, K - h * b, V - h * c, scale=s)
+    fd = (Op - Om) / (2 * h)
+    assert np.abs(out["gdO"] - fd).max() <= 1e-8 * max(np.abs(fd).max(), 1e-3)
+
+
+def test_bob_gdO_independent_of_dO():
+    Q, K, V, dO, a, b, c = slice_set(20, 6, 52)
+    g1 = oracle.bob(Q, K, V, dO, a, b, c)["gdO"]
+    g2 = oracle.bob(Q, K, V, 3 * dO + 1, a, b, c)["gdO"]
+    assert rel(g2, g1) <= 1e-13
+
+
+def test_bob_hvp_symmetry():
+    """<U', H U> = <U, H U'> for the Hessian of l = <O, dO> in (Q, K, V)."""
+    Q, K, V, dO, a, b, c = slice_set(24, 6, 53)
+    a2, b2, c2 = slice_set(24, 6, 54)[:3]
+    h1 = oracle.bob(Q, K, V, dO, a, b, c)
+    h2 = oracle.bob(Q, K, V, dO, a2, b2, c2)
+    lhs = (a2 * h1["gQ"]).sum() + (b2 * h1["gK"]).sum() + (c2 * h1["gV"]).sum()
+    rhs = (a * h2["gQ"]).sum() + (b * h2["gK"]).sum() + (c * h2["gV"]).sum()
+    assert abs(lhs - rhs) <= 1e-12 * max(abs(lhs), 1.0)
+
+
+def test_bob_row_sums_of_sbar_and_dpbar_vanish():
+    N, d = 40, 8
+    Q, K, V, dO, a, b, c = slice_set(N, d, 55)
+    t = A._row_terms(Q, K, V, dO, np.arange(N), 0.3, a, b, c)
+    for k in ("Sbar", "dPbar"):
+        l1 = np.abs(t[k]).sum(axis=1)
+        assert np.all(np.abs(t[k].sum(axis=1)) <= 1e-13 * np.maximum(l1, 1e-300)), k
+
+
+def test_bob_invariant_to_common_key_shift():
+    Q, K, V, dO, a, b, c = slice_set(30, 8, 56)
+    v = rnd(57, 8) * 6
+    o0 = oracle.bob(Q, K, V, dO, a, b, c)
+    o1 = oracle.bob(Q, K + v[None, :], V, dO, a, b, c)
+    for k in ("gQ", "gK", "gV", "gdO"):
+        assert rel(o1[k], o0[k]) <= 1e-11, k
+
+
+def test_bob_single_token_closed_form():
+    """N = 1: gQ = gK = gV = 0 and gdO = c (gdO = P c + dPbar V with P = 1, dPbar = 0)."""
+    Q, K, V, dO, a, b, c = slice_set(1, 5, 58)
+    o = oracle.bob(Q, K, V, dO, a, b, c)
+    for k in ("gQ", "gK", "gV"):
+        assert np.abs(o[k]).max() <= 1e-15, k
+    assert np.allclose(o["gdO"], c, rtol=0, atol=1e-15)
+
+
+@pytest.mark.parametrize("Bc,Br", [(1, 1), (4, 7), (16, 16), (64, 64)])
+def test_bob_streaming_passes_equal_closed_form(Bc, Br):
+    N, d = 53, 8
+    Q, K, V, dO, a, b, c = slice_set(N, d, 59)
+    ref = oracle.bob(Q, K, V, dO, a, b, c)
+    O, L = oracle.forward(Q, K, V)
+    rp = oracle.bob_row_pass(Q, K, V, dO, a, b, c, O, L, Bc)
+    for k in ("gQ", "gdO", "E", "F"):
+        assert rel(rp[k], ref[k]) <= 1e-12, k
+    gK, gV = oracle.bob_col_pass(Q, K, V, dO, a, b, c, L, rp["D"], rp["E"], rp["F"], Br)
+    assert rel(gK, ref["gK"]) <= 1e-12 and rel(gV, ref["gV"]) <= 1e-12
+
+
+def test_bob_sampling_agrees():
+    N, d = 64, 8
+    Q, K, V, dO, a, b, c = slice_set(N, d, 60)
+    ref = oracle.bob(Q, K, V, dO, a, b, c, block=11)
+    rows, cols = np.array([0, 63, 17]), np.array([60, 2, 63])
+    r = oracle.bob_rows(Q, K, V, dO, a, b, c, rows)
+    assert rel(r["gQ"], ref["gQ"][rows]) <= 1e-13 and rel(r["gdO"], ref["gdO"][rows]) <= 1e-13
+    gK, gV = oracle.bob_cols(Q, K, V, dO, a, b, c, cols)
+    assert rel(gK, ref["gK"][cols]) <= 1e-13 and rel(gV, ref["gV"][cols]) <= 1e-13
+
+
+def test_bob_against_fp64_autograd():
+    """Independent check: PyTorch's fp64 CPU double backward of the same loss."""
+    torch = pytest.importorskip("torch")
+    N, d = 13, 8
+    arrs = slice_set(N, d, 61)
+    s = 1 / math.sqrt(d)
+    Q, K, V, dO, a, b, c = (torch.tensor(x, dtype=torch.float64, requires_grad=i < 4)
+                            for i, x in enumerate(arrs))
+    S = (Q @ K.T) * s
+    S = S.masked_fill(torch.triu(torch.ones(N, N, dtype=torch.bool), 1), float("-inf"))
+    O = torch.softmax(S, dim=-1) @ V
+    dQ, dK, dV = torch.autograd.grad((O * dO).sum(), (Q, K, V), create_graph=True)
+    psi = (a * dQ).sum() + (b * dK).sum() + (c * dV).sum()
+    gQ, gK, gV, gdO = torch.autograd.grad(psi, (Q, K, V, dO))
+    ref = oracle.bob(*arrs)
+    for k, t in zip(("gQ", "gK", "gV", "gdO"), (gQ, gK, gV, gdO)):
+        assert rel(ref[k], t.numpy()) <= 1e-13, k
+    fb = oracle.backward(*arrs[:4])
+    assert rel(fb["dQ"], dQ.detach().numpy()) <= 1e-13
+
+
+def test_bob_against_symbolic_second_derivative():
+    """Independent check: sympy differentiates the causal attention loss twice."""
+    sp = pytest.importorskip("sympy")
+    N, d = 3, 2
+    vals = slice_set(N, d, 62)
+    s = sp.Rational(7, 10)
+    sym = {n: sp.Matrix(N, d, lambda i, j, n=n: sp.Symbol(f"{n}{i}{j}")) for n in ("q", "k", "v", "o")}
+    q, k, v, o = (sym[n] for n in ("q", "k", "v", "o"))
+    loss_expr = 0
+    for i in range(N):
+        w = [sp.exp(s * (q.row(i).dot(k.row(j)))) for j in range(i + 1)]
+        z = sum(w)
+        for t in range(d):
+            loss_expr += o[i, t] * sum(w[j] * v[j, t] for j in range(i + 1)) / z
+    a_, b_, c_ = (sp.Matrix(vals[4 + i]) for i in range(3))
+    psi = 0
+    for i in range(N):
+        for t in range(d):
+            psi += a_[i, t] * sp.diff(loss_expr, q[i, t]) + b_[i, t] * sp.diff(loss_expr, k[i, t]) \
+                + c_[i, t] * sp.diff(loss_expr, v[i, t])
+    point = {}
+    for n, arr in zip(("q", "k", "v", "o"), vals[:4]):
+        for i in range(N):
+            for t in range(d):
+                point[sym[n][i, t]] = float(arr[i, t])
+    syms = [sym[n][i, t] for n in ("q", "k", "v", "o") for i in range(N) for t in range(d)]
+    f = sp.lambdify(syms, [sp.diff(psi, x) for x in syms], "math")
+    g = np.array(f(*[point[x] for x in syms])).reshape(4, N, d)
+    ref = oracle.bob(*vals, scale=0.7)
+    for idx, key in enumerate(("gQ", "gK", "gV", "gdO")):
+        assert rel(ref[key], g[idx]) <= 1e-12, key
+
+
+# ------------------------------------------------------ planted mistakes ----
+
+MUTATIONS = {
+    "drop_H": lambda t: t.update(Hm=t["Hm"] * 0),
+    "sign_E": lambda t: t.update(dPbar=t["P"] * (t["G"] + t["E"][:, None])),
+    "drop_F": lambda t: t.update(Sbar=t["P"] * t["Pbar"]),
+    "transpose_b": lambda t: None,  # handled below: b and a swapped in G
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistakes_are_caught(name, monkeypatch):
+    """Plant a plausible mistake in the oracle's BoB and check the FD pin fails."""
+    orig = A._row_terms
+
+    def mutated(Q, K, V, dO, rows, scale, a=None, b=None, c=None):
+        if name == "transpose_b" and a is not None:
+            return orig(Q, K, V, dO, rows, scale, b, a, c)
+        t = orig(Q, K, V, dO, rows, scale, a, b, c)
+        if a is not None:
+            MUTATIONS[name](t)
+            # re-derive the dependants of the mutated tile as the real code would
+            if name == "drop_H":
+                t["Pbar"] = t["G"] * (t["dP"] - t["D"][:, None]) - t["E"][:, None] * t["dP"]
+                t["F"] = (t["P"] * t["Pbar"]).sum(axis=1)
+                t["Sbar"] = t["P"] * (t["Pbar"] - t["F"][:, None])
+        return t
+
+    N, d = 8, 3
+    Q, K, V, dO, a, b, c = slice_set(N, d, 70)
+    s, h = 0.5, 1e-5
+    gp = grads(Q + h * a, K + h * b, V + h * c, dO, s)
+    gm = grads(Q - h * a, K - h * b, V - h * c, dO, s)
+    fd = [(p - m) / (2 * h) for p, m in zip(gp, gm)]
+    Op, _ = oracle.forward(Q + h * a, K + h * b, V + h * c, scale=s)
+    Om, _ = oracle.forward(Q - h * a, K - h * b, V - h * c, scale=s)
+    fd.append((Op - Om) / (2 * h))
+    monkeypatch.setattr(A, "_row_terms", mutated)
+    out = A.bob(Q, K, V, dO, a, b, c, scale=s)
+    errs = [rel(out[k], w) for k, w in zip(("gQ", "gK", "gV", "gdO"), fd)]
+    assert max(errs) > 1e-4, (name, errs)
