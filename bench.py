@@ -1,0 +1,318 @@
+"""Benchmark: one step = attention forward + recompute backward + backward-over-backward
+on one batch of synthetic inputs, through the C ABI of libfbd.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--n-seq S] [--batch B] [--heads H] [--gproj 0|1]
+
+Workload: the GPT-2 Small layer shape at N = 8192 (B=4, H=12, d=64, causal, bf16
+inputs, fp32 accumulation), the shape the throughput targets are stated on.
+Metric: dense-definition TFLOP/s of the whole step (causal halves the count):
+fwd 4 BHN^2 d/2, bwd 10 BHN^2 d/2, BoB 24 BHN^2 d/2.
+
+--impl reference times the CPU fp64 oracle (the only reference this method has)
+on the host cores, on a bounded sample of the same workload (one slice, shorter N),
+converted to the same unit.
+Multi-GPU: the (batch, head) slices are independent, so each rank runs its own
+copy of the workload (weak scaling, no collective); value = sum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+L2_BYTES = 129 * 2 ** 20
+LAUNCHES_PER_STEP = {"fwd": 1, "bwd": 2, "bob": 2}
+
+
+def dense_flops(w, op):
+    unit = w.B * w.H * w.N * w.N * w.d / 2.0
+    return {"fwd": 4, "bwd": 10, "bob": 24}[op] * unit
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"bf16_tflops": d["bf16_tflops"], "bf16_tflops_sustained": d.get("bf16_tflops_sustained"),
+                "hbm_gbs": d["hbm_gbs"], "source": "measured"}
+    return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0):
+        self.index, self.rows, self.proc = index, [], None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+def make_inputs(w, device):
+    import torch
+    x = W.inputs(w)
+    pinned = {k: torch.from_numpy(v).to(torch.bfloat16).pin_memory() for k, v in x.items()}
+    dev = {k: v.to(device, non_blocking=True) for k, v in pinned.items()}
+    return pinned, dev
+
+
+def run_ours(args, w, rank, world):
+    import torch
+
+    import fwd_bwd_double_gb300 as fbd
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    pinned, x = make_inputs(w, dev)
+    torch.cuda.synchronize()
+    desc = fbd.make_desc(x["Q"], w.scale)
+    bf = torch.bfloat16
+    shp = x["Q"].shape
+    out = {k: torch.empty(shp, dtype=bf, device=dev) for k in ("O", "dQ", "dK", "dV", "gQ", "gK", "gV", "gdO")}
+    lse = torch.empty(shp[:3], dtype=torch.float32, device=dev)
+    ws = torch.empty(max(fbd.attn_bob_workspace_bytes(desc), fbd.attn_bwd_workspace_bytes(desc, 1)),
+                     dtype=torch.uint8, device=dev)
+
+    def step(xx, gproj=args.gproj, ev=None):
+        if ev: ev[0].record(stream)
+        fbd.attn_fwd(xx["Q"], xx["K"], xx["V"], O=out["O"], lse=lse, stream=stream, desc=desc)
+        if ev: ev[1].record(stream)
+        fbd.attn_bwd(xx["Q"], xx["K"], xx["V"], out["O"], xx["dO"], lse, gproj=gproj, dQ=out["dQ"], dK=out["dK"],
+                     dV=out["dV"], workspace=ws, stream=stream, desc=desc)
+        if ev: ev[2].record(stream)
+        fbd.attn_bob(xx["Q"], xx["K"], xx["V"], out["O"], xx["dO"], lse, xx["gdQ"], xx["gdK"], xx["gdV"],
+                     gQ=out["gQ"], gK=out["gK"], gV=out["gV"], gdO=out["gdO"], workspace=ws, stream=stream,
+                     desc=desc)
+        if ev: ev[3].record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step(x)
+    torch.cuda.synchronize()
+    fbd.attn_device_status(stream)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for k in range(args.steps):
+                step(x, ev=evs[k])
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    barrier()
+    fbd.attn_device_status(stream)
+    per_op = {op: [evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps)]
+              for i, op in enumerate(("fwd", "bwd", "bob"))}
+    step_ms = [sum(per_op[op][k] for op in per_op) for k in range(args.steps)]
+    ms = statistics.mean(step_ms)
+    ms_max = ms
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    flops_step = sum(dense_flops(w, op) for op in per_op)
+
+    # GProj overhead on the backward alone (same inputs), reported beside the step.
+    def time_bwd(gp, reps=max(3, args.steps)):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        with torch.cuda.stream(stream):
+            fbd.attn_bwd(x["Q"], x["K"], x["V"], out["O"], x["dO"], lse, gproj=gp, dQ=out["dQ"], dK=out["dK"],
+                         dV=out["dV"], workspace=ws, stream=stream, desc=desc)
+            e[0].record(stream)
+            for _ in range(reps):
+                fbd.attn_bwd(x["Q"], x["K"], x["V"], out["O"], x["dO"], lse, gproj=gp, dQ=out["dQ"],
+                             dK=out["dK"], dV=out["dV"], workspace=ws, stream=stream, desc=desc)
+            e[1].record(stream)
+        torch.cuda.synchronize()
+        return e[0].elapsed_time(e[1]) / reps
+
+    bwd0, bwd1 = time_bwd(0), time_bwd(1)
+
+    # End to end: pinned host inputs -> device, the step, all outputs -> host, every step.
+    host_out = {k: torch.empty(shp, dtype=bf).pin_memory() for k in out}
+    host_lse = torch.empty(shp[:3], dtype=torch.float32).pin_memory()
+    e2e_steps = max(2, min(args.steps, 5))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    xin = {k: torch.empty_like(v) for k, v in x.items()}
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            for k in xin:
+                xin[k].copy_(pinned[k], non_blocking=True)
+            step(xin)
+            for k in out:
+                host_out[k].copy_(out[k], non_blocking=True)
+            host_lse.copy_(lse, non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    h2d = sum(v.numel() * v.element_size() for v in pinned.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values()) + host_lse.numel() * 4
+    return dict(ms=ms, ms_max=ms_max, per_op={op: statistics.mean(v) for op, v in per_op.items()},
+                flops_step=flops_step, wall=wall, clocks=clk.summary(), bwd_gproj_ms=(bwd0, bwd1),
+                e2e_ms=e2e_ms, h2d=h2d, d2h=d2h)
+
+
+def cpu_baseline(w, budget_s=20.0):
+    """The oracle as it stands, on host cores, on one slice of the workload at a shorter N."""
+    import oracle
+    N = min(w.N, 2048)
+    ws = W.Workload(w.name + "@cpu_sample", 1, 1, N, w.d, w.dtype)
+    x = {k: v[0, 0].astype(np.float64) for k, v in W.inputs(ws).items()}
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.forward(x["Q"], x["K"], x["V"], scale=w.scale)
+        oracle.backward(x["Q"], x["K"], x["V"], x["dO"], scale=w.scale)
+        oracle.bob(x["Q"], x["K"], x["V"], x["dO"], x["gdQ"], x["gdK"], x["gdV"], scale=w.scale)
+        reps += 1
+        if time.perf_counter() - t0 > budget_s or reps >= 50:
+            break
+    dt = (time.perf_counter() - t0) / reps
+    flops = sum(dense_flops(ws, op) for op in ("fwd", "bwd", "bob"))
+    cores = len(os.sched_getaffinity(0))
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"fwd+bwd+BoB of one (b,h) slice at N={N}, d={w.d}, fp64 NumPy, {reps} reps, "
+                      f"{dt:.2f} s each"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--n-seq", type=int, default=8192)
+    ap.add_argument("--batch", type=int, default=4)
+    ap.add_argument("--heads", type=int, default=12)
+    ap.add_argument("--gproj", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    w = W.Workload(f"gpt2small_B{args.batch}H{args.heads}N{args.n_seq}d64", args.batch, args.heads, args.n_seq,
+                   64, "bf16")
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    config = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": 64, "causal": True,
+              "ops": "fwd + bwd(gproj=%d) + BoB" % args.gproj,
+              "l2": "inputs larger than L2 (each input tensor %.0f MB; 7 inputs)" % (w.rows * 64 * 2 / 1e6),
+              "parallelism": f"independent replicas x{world}"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        times = []
+        for _ in range(args.warmup):
+            pass
+        base = None
+        for _ in range(args.steps):
+            base = cpu_baseline(w, budget_s=max(2.0, 60.0 / max(args.steps, 1)))
+            times.append(base["value"])
+        v = statistics.mean(times)
+        flops = sum(dense_flops(w, op) for op in ("fwd", "bwd", "bob"))
+        print(json.dumps({"impl": "reference", "metric": "fwd+bwd+BoB attention TFLOP/s (dense definition)",
+                          "value": v, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+                          "warmup": args.warmup, "ms_per_step": flops / (v * 1e12) * 1e3,
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                          "data": "synthetic", "config": config, "cpu_baseline": base,
+                          "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}))
+        return
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    import __graft_entry__
+    __graft_entry__.build()
+    r = run_ours(args, w, rank, world)
+    pk = peaks()
+    value = r["flops_step"] * world / (r["ms_max"] * 1e-3) / 1e12
+    # Dominant op: the longest of fwd / bwd / BoB.
+    dom = max(r["per_op"], key=lambda op: r["per_op"][op])
+    ach = dense_flops(w, dom) / (r["per_op"][dom] * 1e-3) / 1e12
+    line = {
+        "metric": "fwd+bwd+BoB attention TFLOP/s (dense definition, causal-halved)",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": r["ms_max"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic", "config": config,
+        "ops": {op: {"ms": r["per_op"][op], "tflops_dense": dense_flops(w, op) / (r["per_op"][op] * 1e-3) / 1e12,
+                     "frac_of_peak": dense_flops(w, op) / (r["per_op"][op] * 1e-3) / 1e12 / pk["bf16_tflops"]}
+                for op in r["per_op"]},
+        "gproj_bwd_ms": {"off": r["bwd_gproj_ms"][0], "on": r["bwd_gproj_ms"][1],
+                         "overhead_pct": 100.0 * (r["bwd_gproj_ms"][1] / r["bwd_gproj_ms"][0] - 1.0)},
+        "roofline": {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": pk["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops"], "traffic": None,
+                     "peak_source": pk["source"] + " burst bf16"},
+        "e2e": {"value": r["flops_step"] / (r["e2e_ms"] * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["e2e_ms"]},
+        "gpu_launches": sum(LAUNCHES_PER_STEP.values()) * args.steps,
+        "clocks": r["clocks"],
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,153 @@
+"""Python binding of libfbd: exact causal attention forward, backward (GProj) and
+backward-over-backward on GB300.
+
+Argument marshalling only.  Every computation runs in the CUDA kernels of
+``libfbd.so`` behind the C ABI declared in ``include/fbd.h``; PyTorch is used for
+device memory and streams.  Importing the package loads the library and raises
+if it is missing: there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import _lib
+from ._lib import (ATTN_BF16, ATTN_F32, AttnDesc, FbdError, lib, status_name)  # noqa: F401
+
+__all__ = [
+    "attn_fwd", "attn_bwd", "attn_bob", "attn_bwd_workspace_bytes", "attn_bob_workspace_bytes",
+    "attn_bwd_projected_dS", "attn_device_status", "attn_status_string", "attn_version", "make_desc",
+    "FbdError", "AttnDesc", "ATTN_F32", "ATTN_BF16", "lib",
+]
+
+LIB_PATH = _lib.LIB_PATH
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return ATTN_F32
+    if t.dtype == torch.bfloat16:
+        return ATTN_BF16
+    raise FbdError(2, f"unsupported tensor dtype {t.dtype} (float32 or bfloat16)")
+
+
+def make_desc(Q, scale: float = 0.0, causal: int = 1) -> AttnDesc:
+    """Descriptor from a [B, H, N, d] tensor."""
+    if Q.dim() != 4:
+        raise FbdError(1, "tensors must be [B, H, N, d]")
+    B, H, N, d = Q.shape
+    return AttnDesc(B, H, N, d, float(scale), int(causal), _dtype_code(Q))
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise FbdError(1, "tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    torch = _torch()
+    if stream is None:
+        if torch.cuda.is_available():
+            stream = torch.cuda.current_stream()
+        else:
+            return None
+    return ctypes.c_void_p(int(getattr(stream, "cuda_stream", stream)))
+
+
+def _check(status: int):
+    if status != 0:
+        raise FbdError(status, lib.attn_last_error().decode())
+
+
+def attn_fwd(Q, K, V, O=None, lse=None, scale: float = 0.0, stream=None, desc=None):
+    """O, lse = attention forward (allocates O and lse with torch when not given)."""
+    torch = _torch()
+    desc = desc or make_desc(Q, scale)
+    if O is None:
+        O = torch.empty_like(Q)
+    if lse is None:
+        lse = torch.empty(Q.shape[:3], dtype=torch.float32, device=Q.device)
+    _check(lib.attn_fwd(ctypes.byref(desc), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(lse), _stream(stream)))
+    return O, lse
+
+
+def attn_bwd_workspace_bytes(desc: AttnDesc, gproj: int = 0) -> int:
+    return int(lib.attn_bwd_workspace_bytes(ctypes.byref(desc), int(gproj)))
+
+
+def attn_bob_workspace_bytes(desc: AttnDesc) -> int:
+    return int(lib.attn_bob_workspace_bytes(ctypes.byref(desc)))
+
+
+def _workspace(nbytes, like, workspace):
+    torch = _torch()
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=like.device)
+    return workspace
+
+
+def attn_bwd(Q, K, V, O, dO, lse, gproj: int = 0, dQ=None, dK=None, dV=None, workspace=None,
+             scale: float = 0.0, stream=None, desc=None):
+    """dQ, dK, dV = recompute backward (GProj when gproj != 0, bf16 only)."""
+    torch = _torch()
+    desc = desc or make_desc(Q, scale)
+    dQ = torch.empty_like(Q) if dQ is None else dQ
+    dK = torch.empty_like(K) if dK is None else dK
+    dV = torch.empty_like(V) if dV is None else dV
+    need = attn_bwd_workspace_bytes(desc, gproj)
+    workspace = _workspace(need, Q, workspace)
+    _check(lib.attn_bwd(ctypes.byref(desc), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(lse),
+                        _ptr(dQ), _ptr(dK), _ptr(dV), int(gproj), _ptr(workspace),
+                        ctypes.c_size_t(workspace.numel() * workspace.element_size()), _stream(stream)))
+    return dQ, dK, dV
+
+
+def attn_bob(Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ=None, gK=None, gV=None, gdO=None, workspace=None,
+             scale: float = 0.0, stream=None, desc=None):
+    """gQ, gK, gV, gdO = backward over backward against cotangents (gdQ, gdK, gdV)."""
+    torch = _torch()
+    desc = desc or make_desc(Q, scale)
+    gQ = torch.empty_like(Q) if gQ is None else gQ
+    gK = torch.empty_like(K) if gK is None else gK
+    gV = torch.empty_like(V) if gV is None else gV
+    gdO = torch.empty_like(dO) if gdO is None else gdO
+    workspace = _workspace(attn_bob_workspace_bytes(desc), Q, workspace)
+    _check(lib.attn_bob(ctypes.byref(desc), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(lse),
+                        _ptr(gdQ), _ptr(gdK), _ptr(gdV), _ptr(gQ), _ptr(gK), _ptr(gV), _ptr(gdO),
+                        _ptr(workspace), ctypes.c_size_t(workspace.numel() * workspace.element_size()),
+                        _stream(stream)))
+    return gQ, gK, gV, gdO
+
+
+def attn_bwd_projected_dS(Q, K, V, O, dO, lse, dS=None, scale: float = 0.0, stream=None, desc=None):
+    """Diagnostic: the GProj-projected dS [B, H, N, N] float32 (small N only)."""
+    torch = _torch()
+    desc = desc or make_desc(Q, scale)
+    B, H, N, _ = Q.shape
+    dS = torch.empty((B, H, N, N), dtype=torch.float32, device=Q.device) if dS is None else dS
+    _check(lib.attn_bwd_projected_dS(ctypes.byref(desc), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO),
+                                     _ptr(lse), _ptr(dS), _stream(stream)))
+    return dS
+
+
+def attn_device_status(stream=None) -> int:
+    """Synchronise the stream; raise FbdError if a device-side wait timed out."""
+    _check(lib.attn_device_status(_stream(stream)))
+    return 0
+
+
+def attn_status_string(status: int) -> str:
+    return lib.attn_status_string(int(status)).decode()
+
+
+def attn_version() -> str:
+    return lib.attn_version().decode()

@@ -1,0 +1,266 @@
+// C ABI of libfbd (declared in include/fbd.h): argument validation, dispatch to
+// the float32 CUDA-core kernels or the bf16 tcgen05/TMA kernels, and status
+// reporting.  No entry point allocates device memory or falls back to another
+// implementation: an unsupported request is an error.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "fbd.h"
+#include "internal.h"
+
+namespace {
+
+thread_local char g_last_error[256] = "";
+
+attn_status_t fail(attn_status_t s, const char* fmt, const char* what = "") {
+  std::snprintf(g_last_error, sizeof(g_last_error), fmt, what);
+  return s;
+}
+
+struct Span {
+  const char* name;
+  uintptr_t lo, hi;  // [lo, hi)
+};
+
+bool overlap(const Span& a, const Span& b) { return a.lo < b.hi && b.lo < a.hi; }
+
+// Shape/type checks shared by every entry point.  Fills `p` on success.
+attn_status_t check_desc(const attn_desc_t* desc, fbd::Problem& p) {
+  if (desc == nullptr) return fail(ATTN_ERR_INVALID_ARG, "desc is NULL%s");
+  if (desc->B < 0 || desc->H < 0 || desc->N < 0 || desc->d <= 0)
+    return fail(ATTN_ERR_INVALID_ARG, "negative B/H/N or non-positive d%s");
+  if (desc->causal != 1) return fail(ATTN_ERR_UNSUPPORTED, "only causal attention (causal=1) is supported%s");
+  if (desc->d != 64 && desc->d != 128) return fail(ATTN_ERR_UNSUPPORTED, "head dim must be 64 or 128%s");
+  if (desc->dtype != ATTN_F32 && desc->dtype != ATTN_BF16) return fail(ATTN_ERR_UNSUPPORTED, "unknown dtype%s");
+  if (!std::isfinite(desc->scale) || desc->scale < 0.f)
+    return fail(ATTN_ERR_INVALID_ARG, "scale must be finite and >= 0 (0 selects 1/sqrt(d))%s");
+  // Overflow guards: element counts of one tensor must fit comfortably in int64,
+  // the sequence length in a TMA coordinate (int32), slices in a 1-D grid.
+  const int64_t lim = int64_t(1) << 31;
+  if (desc->N >= lim || desc->B >= lim || desc->H >= lim)
+    return fail(ATTN_ERR_INVALID_ARG, "B, H and N must each be < 2^31%s");
+  const long double elems = (long double)desc->B * desc->H * desc->N * desc->d;
+  if (elems > 9.0e18L / 8) return fail(ATTN_ERR_INVALID_ARG, "tensor too large%s");
+  p.B = desc->B;
+  p.H = desc->H;
+  p.N = desc->N;
+  p.d = desc->d;
+  p.BH = desc->B * desc->H;
+  p.scale = desc->scale == 0.f ? 1.0f / std::sqrt(static_cast<float>(desc->d)) : desc->scale;
+  p.dtype = desc->dtype;
+  if (p.BH >= lim) return fail(ATTN_ERR_INVALID_ARG, "B*H must be < 2^31%s");
+  if (((p.N + 7) / 8) * p.BH >= lim) return fail(ATTN_ERR_INVALID_ARG, "B*H*N too large for one launch%s");
+  return ATTN_OK;
+}
+
+size_t elem_size(const fbd::Problem& p) { return p.dtype == ATTN_F32 ? 4 : 2; }
+
+// Non-NULL, 16-byte aligned, pairwise non-overlapping outputs vs everything.
+attn_status_t check_ptrs(const Span* in, int nin, const Span* out, int nout) {
+  for (int k = 0; k < nin + nout; ++k) {
+    const Span& s = k < nin ? in[k] : out[k - nin];
+    if (s.lo == 0) return fail(ATTN_ERR_INVALID_ARG, "pointer %s is NULL", s.name);
+    if (s.lo % 16 != 0) return fail(ATTN_ERR_ALIGNMENT, "pointer %s is not 16-byte aligned", s.name);
+  }
+  for (int k = 0; k < nout; ++k) {
+    for (int m = 0; m < nin; ++m)
+      if (overlap(out[k], in[m])) return fail(ATTN_ERR_INVALID_ARG, "output %s overlaps an input", out[k].name);
+    for (int m = k + 1; m < nout; ++m)
+      if (overlap(out[k], out[m])) return fail(ATTN_ERR_INVALID_ARG, "output %s overlaps another output", out[k].name);
+  }
+  return ATTN_OK;
+}
+
+Span span(const char* name, const void* ptr, size_t bytes) {
+  const uintptr_t lo = reinterpret_cast<uintptr_t>(ptr);
+  return Span{name, lo, lo + bytes};
+}
+
+attn_status_t launch_status(cudaError_t e) {
+  if (e == cudaSuccess) return ATTN_OK;
+  (void)cudaGetLastError();  // clear the sticky-free launch error
+  return fail(ATTN_ERR_LAUNCH, "CUDA: %s", cudaGetErrorString(e));
+}
+
+bool tc_path(const fbd::Problem& p, int op) { return p.dtype == ATTN_BF16 && fbd::tc_supports(op, p.d); }
+
+}  // namespace
+
+namespace fbd {
+// bf16 kernels by operation: forward and backward for d in {64, 128};
+// backward-over-backward for d = 64 (its row pass keeps four d-wide accumulators
+// and four score-sized tiles in the 512 TMEM columns).
+bool tc_supports(int op, int64_t d) {
+  if (op == 2) return d == 64;
+  return d == 64 || d == 128;
+}
+}  // namespace fbd
+
+namespace {
+
+}  // namespace
+
+extern "C" {
+
+attn_status_t attn_fwd(const attn_desc_t* desc, const void* Q, const void* K, const void* V, void* O, float* lse,
+                       void* stream) {
+  fbd::Problem p;
+  attn_status_t s = check_desc(desc, p);
+  if (s != ATTN_OK) return s;
+  if (p.BH * p.N == 0) return ATTN_OK;
+  const size_t tb = static_cast<size_t>(p.BH * p.N * p.d) * elem_size(p), sb = p.BH * p.N * sizeof(float);
+  const Span in[] = {span("Q", Q, tb), span("K", K, tb), span("V", V, tb)};
+  const Span out[] = {span("O", O, tb), span("lse", lse, sb)};
+  if ((s = check_ptrs(in, 3, out, 2)) != ATTN_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (p.dtype == ATTN_F32) return launch_status(fbd::simt_fwd(p, Q, K, V, O, lse, st));
+  if (!tc_path(p, 0)) return fail(ATTN_ERR_UNSUPPORTED, "no bf16 forward kernel for this head dim%s");
+  return launch_status(fbd::tc_fwd(p, Q, K, V, O, lse, st));
+}
+
+size_t attn_bwd_workspace_bytes(const attn_desc_t* desc, int gproj) {
+  (void)gproj;
+  if (desc == nullptr || desc->B < 0 || desc->H < 0 || desc->N < 0) return 0;
+  return static_cast<size_t>(desc->B) * desc->H * desc->N * 16;
+}
+
+size_t attn_bob_workspace_bytes(const attn_desc_t* desc) {
+  if (desc == nullptr || desc->B < 0 || desc->H < 0 || desc->N < 0) return 0;
+  return static_cast<size_t>(desc->B) * desc->H * desc->N * 16;
+}
+
+attn_status_t attn_bwd(const attn_desc_t* desc, const void* Q, const void* K, const void* V, const void* O,
+                       const void* dO, const float* lse, void* dQ, void* dK, void* dV, int gproj, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  fbd::Problem p;
+  attn_status_t s = check_desc(desc, p);
+  if (s != ATTN_OK) return s;
+  if (p.BH * p.N == 0) return ATTN_OK;
+  const size_t need = attn_bwd_workspace_bytes(desc, gproj);
+  if (workspace == nullptr || workspace_bytes < need)
+    return fail(ATTN_ERR_WORKSPACE, "workspace NULL or smaller than attn_bwd_workspace_bytes()%s");
+  const size_t tb = static_cast<size_t>(p.BH * p.N * p.d) * elem_size(p), sb = p.BH * p.N * sizeof(float);
+  const Span in[] = {span("Q", Q, tb), span("K", K, tb), span("V", V, tb),
+                     span("O", O, tb), span("dO", dO, tb), span("lse", lse, sb)};
+  const Span out[] = {span("dQ", dQ, tb), span("dK", dK, tb), span("dV", dV, tb),
+                      span("workspace", workspace, need)};
+  if ((s = check_ptrs(in, 6, out, 4)) != ATTN_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  float4* ws = static_cast<float4*>(workspace);
+  if (p.dtype == ATTN_F32) return launch_status(fbd::simt_bwd(p, Q, K, V, O, dO, lse, dQ, dK, dV, 0, ws, st));
+  if (!tc_path(p, 1)) return fail(ATTN_ERR_UNSUPPORTED, "no bf16 backward kernel for this head dim%s");
+  return launch_status(fbd::simt_bwd(p, Q, K, V, O, dO, lse, dQ, dK, dV, gproj != 0, ws, st));
+}
+
+attn_status_t attn_bob(const attn_desc_t* desc, const void* Q, const void* K, const void* V, const void* O,
+                       const void* dO, const float* lse, const void* gdQ, const void* gdK, const void* gdV,
+                       void* gQ, void* gK, void* gV, void* gdO, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  fbd::Problem p;
+  attn_status_t s = check_desc(desc, p);
+  if (s != ATTN_OK) return s;
+  if (p.dtype == ATTN_BF16 && !fbd::tc_supports(2, p.d))
+    return fail(ATTN_ERR_UNSUPPORTED, "bf16 backward-over-backward supports d = 64 only%s");
+  if (p.BH * p.N == 0) return ATTN_OK;
+  const size_t need = attn_bob_workspace_bytes(desc);
+  if (workspace == nullptr || workspace_bytes < need)
+    return fail(ATTN_ERR_WORKSPACE, "workspace NULL or smaller than attn_bob_workspace_bytes()%s");
+  const size_t tb = static_cast<size_t>(p.BH * p.N * p.d) * elem_size(p), sb = p.BH * p.N * sizeof(float);
+  const Span in[] = {span("Q", Q, tb),     span("K", K, tb),     span("V", V, tb),
+                     span("O", O, tb),     span("dO", dO, tb),   span("lse", lse, sb),
+                     span("gdQ", gdQ, tb), span("gdK", gdK, tb), span("gdV", gdV, tb)};
+  const Span out[] = {span("gQ", gQ, tb), span("gK", gK, tb), span("gV", gV, tb), span("gdO", gdO, tb),
+                      span("workspace", workspace, need)};
+  if ((s = check_ptrs(in, 9, out, 5)) != ATTN_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  float4* ws = static_cast<float4*>(workspace);
+  if (p.dtype == ATTN_F32)
+    return launch_status(fbd::simt_bob(p, Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ, gK, gV, gdO, ws, st));
+  return launch_status(fbd::simt_bob(p, Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ, gK, gV, gdO, ws, st));
+}
+
+attn_status_t attn_bwd_projected_dS(const attn_desc_t* desc, const void* Q, const void* K, const void* V,
+                                    const void* O, const void* dO, const float* lse, float* dS_out,
+                                    void* stream) {
+  fbd::Problem p;
+  attn_status_t s = check_desc(desc, p);
+  if (s != ATTN_OK) return s;
+  if (p.dtype != ATTN_BF16) return fail(ATTN_ERR_UNSUPPORTED, "the GProj projection applies to bf16 only%s");
+  if (p.BH * p.N == 0) return ATTN_OK;
+  const size_t tb = static_cast<size_t>(p.BH * p.N * p.d) * 2, sb = p.BH * p.N * sizeof(float);
+  const size_t ob = static_cast<size_t>(p.BH) * p.N * p.N * sizeof(float);
+  const Span in[] = {span("Q", Q, tb), span("K", K, tb), span("V", V, tb),
+                     span("O", O, tb), span("dO", dO, tb), span("lse", lse, sb)};
+  const Span out[] = {span("dS_out", dS_out, ob)};
+  if ((s = check_ptrs(in, 6, out, 1)) != ATTN_OK) return s;
+  return launch_status(fbd::simt_projected_dS(p, Q, K, V, O, dO, lse, dS_out, static_cast<cudaStream_t>(stream)));
+}
+
+attn_status_t attn_device_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "CUDA: %s", cudaGetErrorString(e));
+  const uint32_t flags = fbd::tc_fwd_take_error();
+  if (flags != 0) return fail(ATTN_ERR_TIMEOUT, "a device-side bounded wait gave up%s");
+  return ATTN_OK;
+}
+
+const char* attn_status_string(attn_status_t status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case ATTN_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case ATTN_ERR_WORKSPACE: return "workspace missing or too small";
+    case ATTN_ERR_LAUNCH: return "CUDA launch or tensor-map error";
+    case ATTN_ERR_TIMEOUT: return "device-side wait timed out";
+    case ATTN_ERR_DEVICE: return "no usable CUDA device";
+  }
+  return "unknown status";
+}
+
+const char* attn_last_error(void) { return g_last_error; }
+
+const char* attn_version(void) { return "libfbd 0.1 (sm_103a: tcgen05/TMA bf16 path, CUDA-core fp32 path)"; }
+
+}  // extern "C"
+
+// ------------------------------------------------------------- tensor maps
+namespace fbd {
+
+namespace {
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeFn encode_fn() {
+  static EncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &f, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(f);
+  });
+  return fn;
+}
+}  // namespace
+
+bool make_tmap_bf16(void* map_out, const void* base, int64_t N, int64_t d, int64_t BH, int box_rows) {
+  EncodeFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N * d) * 2};
+  const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows), 1u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = fn(static_cast<CUtensorMap*>(map_out), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
+                  dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace fbd

@@ -1,0 +1,56 @@
+// Internal launch interface between the C ABI (api.cu) and the kernel
+// translation units.  Every launcher validates nothing: api.cu has already
+// checked pointers, sizes, alignment and workspace.
+#pragma once
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "fbd.h"
+
+namespace fbd {
+
+struct Problem {
+  int64_t B, H, N, d;
+  int64_t BH;     // B * H independent (batch, head) slices
+  float scale;    // s, already resolved (1/sqrt(d) when the caller passed 0)
+  int dtype;      // attn_dtype_t
+};
+
+// Float32 path: CUDA-core kernels with float32 inputs/outputs (exact fp32 arithmetic).
+cudaError_t simt_fwd(const Problem& p, const void* Q, const void* K, const void* V, void* O, float* lse,
+                     cudaStream_t st);
+cudaError_t simt_bwd(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
+                     const void* dO, const float* lse, void* dQ, void* dK, void* dV, int gproj, float4* ws,
+                     cudaStream_t st);
+cudaError_t simt_bob(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
+                     const void* dO, const float* lse, const void* a, const void* b, const void* c, void* gQ,
+                     void* gK, void* gV, void* gdO, float4* ws, cudaStream_t st);
+cudaError_t simt_projected_dS(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
+                              const void* dO, const float* lse, float* dS, cudaStream_t st);
+
+// bf16 tensor-core path (tcgen05 + TMA).  Return cudaErrorInvalidValue if a
+// tensor map could not be encoded.
+cudaError_t tc_fwd(const Problem& p, const void* Q, const void* K, const void* V, void* O, float* lse,
+                   cudaStream_t st);
+cudaError_t tc_bwd(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
+                   const void* dO, const float* lse, void* dQ, void* dK, void* dV, int gproj, float4* ws,
+                   cudaStream_t st);
+cudaError_t tc_bob(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
+                   const void* dO, const float* lse, const void* a, const void* b, const void* c, void* gQ,
+                   void* gK, void* gV, void* gdO, float4* ws, cudaStream_t st);
+
+// Which kernels exist for a given (op, dtype, d): false means ATTN_ERR_UNSUPPORTED.
+bool tc_supports(int op, int64_t d);  // op: 0 fwd, 1 bwd, 2 bob
+
+// Device status words (bit FBD_ERR_TIMEOUT), read-and-cleared per translation unit.
+uint32_t tc_fwd_take_error();
+uint32_t tc_bwd_take_error();
+uint32_t tc_bob_take_error();
+
+// Tensor maps: 3-D bf16 view (d, N, B*H) of a [B,H,N,d] tensor, box (64, rows, 1),
+// 128-byte swizzle.  Returns false if the driver entry point is missing or the
+// encode fails.
+bool make_tmap_bf16(void* map_out /* CUtensorMap* */, const void* base, int64_t N, int64_t d, int64_t BH,
+                    int box_rows);
+
+}  // namespace fbd

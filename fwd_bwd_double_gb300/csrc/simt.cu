@@ -1,0 +1,617 @@
+// Float32 path: forward, backward (GProj emulation for bf16 debugging), BoB and
+// the GProj projected-dS export, on CUDA cores in exact fp32 arithmetic.
+//
+// Work split: one warp per query row (row passes) or per key (column passes);
+// a warp's 32 lanes each hold d/32 consecutive elements of the row's vectors, so
+// every global row read is one coalesced 128/256/512-byte access.  The CTA's 8
+// warps share a shared-memory staging tile of 32 partner rows (keys for row
+// passes, queries for column passes), converted to fp32 once.  Dot products are
+// warp butterfly reductions; all lanes then hold the same value, so the softmax
+// bookkeeping is warp-uniform.
+//
+// These kernels follow the same decomposition as the tensor-core path:
+//   forward: online softmax ("Flash attention for trading models", "Online
+//            softmax recurrence"), max subtracted before scaling ("FlashAttention
+//            bf16 gradient and GProj", "Why the error appears late");
+//   backward: recompute P from lse ("Backward pass: recompute instead of store");
+//   BoB: row pass with the two scalar states, column pass re-reading them
+//        ("FlashBoB: second-order attention", "Two scalar states replace
+//        quadratic tensors").
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include <type_traits>
+
+#include "internal.h"
+
+namespace fbd {
+namespace {
+
+constexpr int kWarps = 8;       // rows (or keys) per CTA
+constexpr int kThreads = kWarps * 32;
+constexpr int kTile = 32;       // partner rows staged per step
+constexpr unsigned kFull = 0xffffffffu;
+
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T>
+__device__ __forceinline__ T from_f(float x);
+template <>
+__device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+__device__ __forceinline__ int64_t lmin(int64_t a, int64_t b) { return a < b ? a : b; }
+__device__ __forceinline__ int64_t lmax(int64_t a, int64_t b) { return a > b ? a : b; }
+
+__device__ __forceinline__ float bf16r(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
+template <int V, typename T>
+__device__ __forceinline__ void load_vec(const T* __restrict__ row, int lane, float (&v)[V]) {
+#pragma unroll
+  for (int t = 0; t < V; ++t) v[t] = to_f(row[lane * V + t]);
+}
+template <int V, typename T>
+__device__ __forceinline__ void store_vec(T* __restrict__ row, int lane, const float (&v)[V]) {
+#pragma unroll
+  for (int t = 0; t < V; ++t) row[lane * V + t] = from_f<T>(v[t]);
+}
+template <int V>
+__device__ __forceinline__ void load_smem(const float* __restrict__ row, int lane, float (&v)[V]) {
+#pragma unroll
+  for (int t = 0; t < V; ++t) v[t] = row[lane * V + t];
+}
+
+template <int K>
+__device__ __forceinline__ void warp_sum(float (&x)[K]) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+    for (int k = 0; k < K; ++k) x[k] += __shfl_xor_sync(kFull, x[k], off);
+}
+
+template <int V>
+__device__ __forceinline__ float dot(const float (&x)[V], const float (&y)[V]) {
+  float s = 0.f;
+#pragma unroll
+  for (int t = 0; t < V; ++t) s = fmaf(x[t], y[t], s);
+  return s;
+}
+
+// Stage rows [r0, r0 + kTile) of a [N, D] slice into shared memory as fp32 (0 past N).
+template <typename T, int D>
+__device__ __forceinline__ void stage(float* __restrict__ dst, const T* __restrict__ src, int64_t r0, int64_t N) {
+  for (int e = threadIdx.x; e < kTile * D; e += kThreads) {
+    const int r = e / D;
+    const int64_t gr = r0 + r;
+    dst[e] = gr < N ? to_f(src[gr * D + (e % D)]) : 0.f;
+  }
+}
+
+// Slice/row-block decode of the 1-D grid: blockIdx.x = blk * BH + bh, heaviest
+// causal blocks (largest blk for row passes) first.
+struct Tile {
+  int64_t bh, blk;
+};
+__device__ __forceinline__ Tile decode(int64_t BH, int64_t nblk, bool heavy_last_rows) {
+  const int64_t x = blockIdx.x;
+  Tile t;
+  t.bh = x % BH;
+  const int64_t k = x / BH;
+  t.blk = heavy_last_rows ? (nblk - 1 - k) : k;
+  return t;
+}
+
+// ---------------------------------------------------------------- forward
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads) fwd_kernel(const T* __restrict__ Q, const T* __restrict__ K,
+                                                       const T* __restrict__ Vt, T* __restrict__ O,
+                                                       float* __restrict__ lse, int64_t N, int64_t BH,
+                                                       float scale) {
+  constexpr int V = D / 32;
+  extern __shared__ float sm[];
+  float* Ks = sm;
+  float* Vs = sm + kTile * D;
+  const int64_t nblk = (N + kWarps - 1) / kWarps;
+  const Tile tl = decode(BH, nblk, true);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int64_t row0 = tl.blk * kWarps, i = row0 + warp;
+  const bool live = i < N;
+  const size_t base = static_cast<size_t>(tl.bh) * N * D;
+  float q[V], o[V];
+#pragma unroll
+  for (int t = 0; t < V; ++t) o[t] = 0.f;
+  if (live) load_vec(Q + base + i * D, lane, q);
+  float m = -CUDART_INF_F, l = 0.f;  // running max of raw dot products, running sum
+  const int64_t last = min(row0 + kWarps, N) - 1;
+  for (int64_t k0 = 0; k0 <= last; k0 += kTile) {
+    __syncthreads();
+    stage<T, D>(Ks, K + base, k0, N);
+    stage<T, D>(Vs, Vt + base, k0, N);
+    __syncthreads();
+    if (!live) continue;
+    const int jn = static_cast<int>(lmin(kTile, i - k0 + 1));
+    for (int jj = 0; jj < jn; ++jj) {
+      float kv[V], vv[V];
+      load_smem(Ks + jj * D, lane, kv);
+      load_smem(Vs + jj * D, lane, vv);
+      float s[1] = {dot(q, kv)};
+      warp_sum(s);
+      if (s[0] > m) {  // the running max moves: rescale what was accumulated
+        const float al = expf((m - s[0]) * scale);
+        l *= al;
+#pragma unroll
+        for (int t = 0; t < V; ++t) o[t] *= al;
+        m = s[0];
+      }
+      const float p = expf((s[0] - m) * scale);  // subtract the max, then scale
+      l += p;
+#pragma unroll
+      for (int t = 0; t < V; ++t) o[t] = fmaf(p, vv[t], o[t]);
+    }
+  }
+  if (!live) return;
+  const float inv = 1.f / l;
+#pragma unroll
+  for (int t = 0; t < V; ++t) o[t] *= inv;
+  store_vec(O + base + i * D, lane, o);
+  if (lane == 0) lse[tl.bh * N + i] = m * scale + logf(l);
+}
+
+// --------------------------------------------------------- backward, rows
+// dQ and the row statistics (lse, D, rho, 0).  GPROJ rounds dS and P to bf16 as
+// the bf16 tensor-core path does and applies the GProj projection.
+template <typename T, int D, bool GPROJ>
+__global__ void __launch_bounds__(kThreads) bwd_row_kernel(const T* __restrict__ Q, const T* __restrict__ K,
+                                                           const T* __restrict__ Vt, const T* __restrict__ O,
+                                                           const T* __restrict__ dO, const float* __restrict__ lse,
+                                                           T* __restrict__ dQ, float4* __restrict__ ws, int64_t N,
+                                                           int64_t BH, float scale) {
+  constexpr int V = D / 32;
+  extern __shared__ float sm[];
+  float* Ks = sm;
+  float* Vs = sm + kTile * D;
+  const int64_t nblk = (N + kWarps - 1) / kWarps;
+  const Tile tl = decode(BH, nblk, true);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int64_t row0 = tl.blk * kWarps, i = row0 + warp;
+  const bool live = i < N;
+  const size_t base = static_cast<size_t>(tl.bh) * N * D;
+  float q[V], g[V], acc[V], pk[V];
+  float Di = 0.f, Li = 0.f, r = 0.f, sp = 0.f;
+#pragma unroll
+  for (int t = 0; t < V; ++t) acc[t] = pk[t] = 0.f;
+  if (live) {
+    float o[V];
+    load_vec(Q + base + i * D, lane, q);
+    load_vec(dO + base + i * D, lane, g);
+    load_vec(O + base + i * D, lane, o);
+    float x[1] = {dot(g, o)};
+    warp_sum(x);
+    Di = x[0];
+    Li = lse[tl.bh * N + i];
+  }
+  const int64_t last = min(row0 + kWarps, N) - 1;
+  for (int64_t k0 = 0; k0 <= last; k0 += kTile) {
+    __syncthreads();
+    stage<T, D>(Ks, K + base, k0, N);
+    stage<T, D>(Vs, Vt + base, k0, N);
+    __syncthreads();
+    if (!live) continue;
+    const int jn = static_cast<int>(lmin(kTile, i - k0 + 1));
+    for (int jj = 0; jj < jn; ++jj) {
+      float kv[V], vv[V];
+      load_smem(Ks + jj * D, lane, kv);
+      load_smem(Vs + jj * D, lane, vv);
+      float x[2] = {dot(q, kv), dot(g, vv)};
+      warp_sum(x);
+      const float p = expf(x[0] * scale - Li);
+      const float ds = p * (x[1] - Di);
+      if constexpr (GPROJ) {
+        const float dsh = bf16r(ds), ph = bf16r(p);
+        r += dsh;
+        sp += ph;
+#pragma unroll
+        for (int t = 0; t < V; ++t) {
+          acc[t] = fmaf(dsh, kv[t], acc[t]);
+          pk[t] = fmaf(ph, kv[t], pk[t]);
+        }
+      } else {
+#pragma unroll
+        for (int t = 0; t < V; ++t) acc[t] = fmaf(ds, kv[t], acc[t]);
+      }
+    }
+  }
+  if (!live) return;
+  const float rho = GPROJ ? r / sp : 0.f;
+#pragma unroll
+  for (int t = 0; t < V; ++t) acc[t] = scale * (acc[t] - rho * pk[t]);
+  store_vec(dQ + base + i * D, lane, acc);
+  if (lane == 0) ws[tl.bh * N + i] = make_float4(Li, Di, rho, 0.f);
+}
+
+// ------------------------------------------------------- backward, columns
+template <typename T, int D, bool GPROJ>
+__global__ void __launch_bounds__(kThreads) bwd_col_kernel(const T* __restrict__ Q, const T* __restrict__ K,
+                                                           const T* __restrict__ Vt, const T* __restrict__ dO,
+                                                           const float4* __restrict__ ws, T* __restrict__ dK,
+                                                           T* __restrict__ dV, int64_t N, int64_t BH,
+                                                           float scale) {
+  constexpr int V = D / 32;
+  extern __shared__ float sm[];
+  float* Qs = sm;
+  float* Gs = sm + kTile * D;
+  float4* Ss = reinterpret_cast<float4*>(sm + 2 * kTile * D);
+  const int64_t nblk = (N + kWarps - 1) / kWarps;
+  const Tile tl = decode(BH, nblk, false);  // smallest key index = most rows: first
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int64_t col0 = tl.blk * kWarps, j = col0 + warp;
+  const bool live = j < N;
+  const size_t base = static_cast<size_t>(tl.bh) * N * D;
+  float kv[V], vv[V], ak[V], av[V];
+#pragma unroll
+  for (int t = 0; t < V; ++t) ak[t] = av[t] = 0.f;
+  if (live) {
+    load_vec(K + base + j * D, lane, kv);
+    load_vec(Vt + base + j * D, lane, vv);
+  }
+  for (int64_t i0 = col0; i0 < N; i0 += kTile) {
+    __syncthreads();
+    stage<T, D>(Qs, Q + base, i0, N);
+    stage<T, D>(Gs, dO + base, i0, N);
+    if (threadIdx.x < kTile)
+      Ss[threadIdx.x] = (i0 + threadIdx.x < N) ? ws[tl.bh * N + i0 + threadIdx.x] : make_float4(0, 0, 0, 0);
+    __syncthreads();
+    if (!live) continue;
+    const int ib = static_cast<int>(lmax(0, j - i0));  // rows i >= j only
+    const int ie = static_cast<int>(lmin(kTile, N - i0));
+    for (int ii = ib; ii < ie; ++ii) {
+      float qv[V], gv[V];
+      load_smem(Qs + ii * D, lane, qv);
+      load_smem(Gs + ii * D, lane, gv);
+      const float4 st = Ss[ii];
+      float x[2] = {dot(qv, kv), dot(gv, vv)};
+      warp_sum(x);
+      const float p = expf(x[0] * scale - st.x);
+      const float ds = p * (x[1] - st.y);
+      float cq, cv;
+      if constexpr (GPROJ) {
+        const float ph = bf16r(p);
+        cq = bf16r(ds) - st.z * ph;
+        cv = ph;
+      } else {
+        cq = ds;
+        cv = p;
+      }
+#pragma unroll
+      for (int t = 0; t < V; ++t) {
+        ak[t] = fmaf(cq, qv[t], ak[t]);
+        av[t] = fmaf(cv, gv[t], av[t]);
+      }
+    }
+  }
+  if (!live) return;
+#pragma unroll
+  for (int t = 0; t < V; ++t) ak[t] *= scale;
+  store_vec(dK + base + j * D, lane, ak);
+  store_vec(dV + base + j * D, lane, av);
+}
+
+// ------------------------------------------------------------- BoB, rows
+// Streams keys past each query row; accumulates E, F' and X, Y, Z, U, and at the
+// end applies the corrections that need the finished row:
+//   gdO = X - E O,  gQ = s (Y - E Z - F' U),  F = F' - E D.
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads) bob_row_kernel(
+    const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ Vt, const T* __restrict__ O,
+    const T* __restrict__ dO, const float* __restrict__ lse, const T* __restrict__ A, const T* __restrict__ Bm,
+    const T* __restrict__ C, T* __restrict__ gQ, T* __restrict__ gdO, float4* __restrict__ ws, int64_t N,
+    int64_t BH, float scale) {
+  constexpr int V = D / 32;
+  extern __shared__ float sm[];
+  float* Ks = sm;
+  float* Vs = sm + kTile * D;
+  float* Bs = sm + 2 * kTile * D;
+  float* Cs = sm + 3 * kTile * D;
+  const int64_t nblk = (N + kWarps - 1) / kWarps;
+  const Tile tl = decode(BH, nblk, true);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int64_t row0 = tl.blk * kWarps, i = row0 + warp;
+  const bool live = i < N;
+  const size_t base = static_cast<size_t>(tl.bh) * N * D;
+  float q[V], g[V], av[V], o[V], X[V], Y[V], Z[V], U[V];
+  float Di = 0.f, Li = 0.f, E = 0.f, Fp = 0.f;
+#pragma unroll
+  for (int t = 0; t < V; ++t) X[t] = Y[t] = Z[t] = U[t] = 0.f;
+  if (live) {
+    load_vec(Q + base + i * D, lane, q);
+    load_vec(dO + base + i * D, lane, g);
+    load_vec(A + base + i * D, lane, av);
+    load_vec(O + base + i * D, lane, o);
+    float x[1] = {dot(g, o)};
+    warp_sum(x);
+    Di = x[0];
+    Li = lse[tl.bh * N + i];
+  }
+  const int64_t last = min(row0 + kWarps, N) - 1;
+  for (int64_t k0 = 0; k0 <= last; k0 += kTile) {
+    __syncthreads();
+    stage<T, D>(Ks, K + base, k0, N);
+    stage<T, D>(Vs, Vt + base, k0, N);
+    stage<T, D>(Bs, Bm + base, k0, N);
+    stage<T, D>(Cs, C + base, k0, N);
+    __syncthreads();
+    if (!live) continue;
+    const int jn = static_cast<int>(lmin(kTile, i - k0 + 1));
+    for (int jj = 0; jj < jn; ++jj) {
+      float kv[V], vv[V], bv[V], cv[V];
+      load_smem(Ks + jj * D, lane, kv);
+      load_smem(Vs + jj * D, lane, vv);
+      load_smem(Bs + jj * D, lane, bv);
+      load_smem(Cs + jj * D, lane, cv);
+      float x[4] = {dot(q, kv), dot(g, vv), dot(av, kv) + dot(q, bv), dot(g, cv)};
+      warp_sum(x);
+      const float p = expf(x[0] * scale - Li);
+      const float dp = x[1];
+      const float G = scale * x[2];
+      const float Hh = x[3];
+      const float ds = p * (dp - Di);
+      const float pg = p * G;
+      const float w = G * ds + p * Hh;
+      E += pg;
+      Fp += w;
+#pragma unroll
+      for (int t = 0; t < V; ++t) {
+        X[t] = fmaf(p, cv[t], fmaf(pg, vv[t], X[t]));
+        Y[t] = fmaf(ds, bv[t], fmaf(w, kv[t], Y[t]));
+        Z[t] = fmaf(ds, kv[t], Z[t]);
+        U[t] = fmaf(p, kv[t], U[t]);
+      }
+    }
+  }
+  if (!live) return;
+  float go[V], gq[V];
+#pragma unroll
+  for (int t = 0; t < V; ++t) {
+    go[t] = X[t] - E * o[t];
+    gq[t] = scale * (Y[t] - E * Z[t] - Fp * U[t]);
+  }
+  store_vec(gdO + base + i * D, lane, go);
+  store_vec(gQ + base + i * D, lane, gq);
+  if (lane == 0) ws[tl.bh * N + i] = make_float4(Li, Di, E, Fp - E * Di);
+}
+
+// ---------------------------------------------------------- BoB, columns
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads) bob_col_kernel(
+    const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ Vt, const T* __restrict__ dO,
+    const T* __restrict__ A, const T* __restrict__ Bm, const T* __restrict__ C, const float4* __restrict__ ws,
+    T* __restrict__ gK, T* __restrict__ gV, int64_t N, int64_t BH, float scale) {
+  constexpr int V = D / 32;
+  extern __shared__ float sm[];
+  float* Qs = sm;
+  float* Gs = sm + kTile * D;
+  float* As = sm + 2 * kTile * D;
+  float4* Ss = reinterpret_cast<float4*>(sm + 3 * kTile * D);
+  const int64_t nblk = (N + kWarps - 1) / kWarps;
+  const Tile tl = decode(BH, nblk, false);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int64_t col0 = tl.blk * kWarps, j = col0 + warp;
+  const bool live = j < N;
+  const size_t base = static_cast<size_t>(tl.bh) * N * D;
+  float kv[V], vv[V], bv[V], cv[V], aK[V], aV[V];
+#pragma unroll
+  for (int t = 0; t < V; ++t) aK[t] = aV[t] = 0.f;
+  if (live) {
+    load_vec(K + base + j * D, lane, kv);
+    load_vec(Vt + base + j * D, lane, vv);
+    load_vec(Bm + base + j * D, lane, bv);
+    load_vec(C + base + j * D, lane, cv);
+  }
+  for (int64_t i0 = col0; i0 < N; i0 += kTile) {
+    __syncthreads();
+    stage<T, D>(Qs, Q + base, i0, N);
+    stage<T, D>(Gs, dO + base, i0, N);
+    stage<T, D>(As, A + base, i0, N);
+    if (threadIdx.x < kTile)
+      Ss[threadIdx.x] = (i0 + threadIdx.x < N) ? ws[tl.bh * N + i0 + threadIdx.x] : make_float4(0, 0, 0, 0);
+    __syncthreads();
+    if (!live) continue;
+    const int ib = static_cast<int>(lmax(0, j - i0));
+    const int ie = static_cast<int>(lmin(kTile, N - i0));
+    for (int ii = ib; ii < ie; ++ii) {
+      float qv[V], gv[V], a2[V];
+      load_smem(Qs + ii * D, lane, qv);
+      load_smem(Gs + ii * D, lane, gv);
+      load_smem(As + ii * D, lane, a2);
+      const float4 st = Ss[ii];  // (lse, D, E, F) of row i
+      float x[4] = {dot(qv, kv), dot(gv, vv), dot(a2, kv) + dot(qv, bv), dot(gv, cv)};
+      warp_sum(x);
+      const float p = expf(x[0] * scale - st.x);
+      const float dp = x[1];
+      const float G = scale * x[2];
+      const float Hh = x[3];
+      const float ds = p * (dp - st.y);
+      const float dpbar = p * (G - st.z);
+      const float sbar = p * (G * (dp - st.y) - st.z * dp + Hh - st.w);
+#pragma unroll
+      for (int t = 0; t < V; ++t) {
+        aV[t] = fmaf(dpbar, gv[t], aV[t]);
+        aK[t] = fmaf(ds, a2[t], fmaf(sbar, qv[t], aK[t]));
+      }
+    }
+  }
+  if (!live) return;
+#pragma unroll
+  for (int t = 0; t < V; ++t) aK[t] *= scale;
+  store_vec(gK + base + j * D, lane, aK);
+  store_vec(gV + base + j * D, lane, aV);
+}
+
+// ------------------------------------------- GProj projected dS (diagnostic)
+// One warp per row: sweep 1 accumulates r = sum bf16(dS) and sum bf16(P);
+// sweep 2 writes dS~ = bf16(dS) - rho bf16(P) for j <= i and 0 beyond.
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads) projected_dS_kernel(const T* __restrict__ Q, const T* __restrict__ K,
+                                                                const T* __restrict__ Vt, const T* __restrict__ O,
+                                                                const T* __restrict__ dO,
+                                                                const float* __restrict__ lse,
+                                                                float* __restrict__ out, int64_t N, int64_t BH,
+                                                                float scale) {
+  constexpr int V = D / 32;
+  const int64_t nblk = (N + kWarps - 1) / kWarps;
+  const Tile tl = decode(BH, nblk, true);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int64_t i = tl.blk * kWarps + warp;
+  if (i >= N) return;
+  const size_t base = static_cast<size_t>(tl.bh) * N * D;
+  float q[V], g[V], o[V];
+  load_vec(Q + base + i * D, lane, q);
+  load_vec(dO + base + i * D, lane, g);
+  load_vec(O + base + i * D, lane, o);
+  float x0[1] = {dot(g, o)};
+  warp_sum(x0);
+  const float Di = x0[0], Li = lse[tl.bh * N + i];
+  float r = 0.f, sp = 0.f;
+  for (int pass = 0; pass < 2; ++pass) {
+    const float rho = r / sp;
+    for (int64_t j = 0; j < N; ++j) {
+      float* dst = out + (static_cast<size_t>(tl.bh) * N + i) * N + j;
+      if (j > i) {
+        if (pass == 1 && lane == 0) *dst = 0.f;
+        continue;
+      }
+      float kv[V], vv[V];
+      load_vec(K + base + j * D, lane, kv);
+      load_vec(Vt + base + j * D, lane, vv);
+      float x[2] = {dot(q, kv), dot(g, vv)};
+      warp_sum(x);
+      const float p = expf(x[0] * scale - Li);
+      const float dsh = bf16r(p * (x[1] - Di)), ph = bf16r(p);
+      if (pass == 0) {
+        r += dsh;
+        sp += ph;
+      } else if (lane == 0) {
+        *dst = dsh - rho * ph;
+      }
+    }
+  }
+}
+
+template <typename Kern>
+cudaError_t allow_smem(Kern k, size_t bytes) {
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+}
+
+inline unsigned grid_for(const Problem& p) {
+  return static_cast<unsigned>(((p.N + kWarps - 1) / kWarps) * p.BH);
+}
+
+template <typename T, int D>
+cudaError_t fwd_t(const Problem& p, const void* Q, const void* K, const void* V, void* O, float* lse,
+                  cudaStream_t st) {
+  const size_t sm = 2 * kTile * D * sizeof(float);
+  auto k = fwd_kernel<T, D>;
+  cudaError_t e = allow_smem(k, sm);
+  if (e != cudaSuccess) return e;
+  k<<<grid_for(p), kThreads, sm, st>>>(static_cast<const T*>(Q), static_cast<const T*>(K),
+                                        static_cast<const T*>(V), static_cast<T*>(O), lse, p.N, p.BH, p.scale);
+  return cudaGetLastError();
+}
+
+template <typename T, int D, bool GP>
+cudaError_t bwd_t(const Problem& p, const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                  const float* lse, void* dQ, void* dK, void* dV, float4* ws, cudaStream_t st) {
+  const size_t sm_row = 2 * kTile * D * sizeof(float);
+  const size_t sm_col = 2 * kTile * D * sizeof(float) + kTile * sizeof(float4);
+  auto kr = bwd_row_kernel<T, D, GP>;
+  auto kc = bwd_col_kernel<T, D, GP>;
+  cudaError_t e = allow_smem(kr, sm_row);
+  if (e == cudaSuccess) e = allow_smem(kc, sm_col);
+  if (e != cudaSuccess) return e;
+  kr<<<grid_for(p), kThreads, sm_row, st>>>(static_cast<const T*>(Q), static_cast<const T*>(K),
+                                             static_cast<const T*>(V), static_cast<const T*>(O),
+                                             static_cast<const T*>(dO), lse, static_cast<T*>(dQ), ws, p.N, p.BH,
+                                             p.scale);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  kc<<<grid_for(p), kThreads, sm_col, st>>>(static_cast<const T*>(Q), static_cast<const T*>(K),
+                                             static_cast<const T*>(V), static_cast<const T*>(dO), ws,
+                                             static_cast<T*>(dK), static_cast<T*>(dV), p.N, p.BH, p.scale);
+  return cudaGetLastError();
+}
+
+template <typename T, int D>
+cudaError_t bob_t(const Problem& p, const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                  const float* lse, const void* a, const void* b, const void* c, void* gQ, void* gK, void* gV,
+                  void* gdO, float4* ws, cudaStream_t st) {
+  const size_t sm_row = 4 * kTile * D * sizeof(float);
+  const size_t sm_col = 3 * kTile * D * sizeof(float) + kTile * sizeof(float4);
+  auto kr = bob_row_kernel<T, D>;
+  auto kc = bob_col_kernel<T, D>;
+  cudaError_t e = allow_smem(kr, sm_row);
+  if (e == cudaSuccess) e = allow_smem(kc, sm_col);
+  if (e != cudaSuccess) return e;
+  using CT = const T*;
+  kr<<<grid_for(p), kThreads, sm_row, st>>>(
+      static_cast<CT>(Q), static_cast<CT>(K), static_cast<CT>(V), static_cast<CT>(O), static_cast<CT>(dO), lse,
+      static_cast<CT>(a), static_cast<CT>(b), static_cast<CT>(c), static_cast<T*>(gQ), static_cast<T*>(gdO), ws,
+      p.N, p.BH, p.scale);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  kc<<<grid_for(p), kThreads, sm_col, st>>>(static_cast<CT>(Q), static_cast<CT>(K), static_cast<CT>(V),
+                                             static_cast<CT>(dO), static_cast<CT>(a), static_cast<CT>(b),
+                                             static_cast<CT>(c), ws, static_cast<T*>(gK), static_cast<T*>(gV),
+                                             p.N, p.BH, p.scale);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t simt_fwd(const Problem& p, const void* Q, const void* K, const void* V, void* O, float* lse,
+                     cudaStream_t st) {
+  if (p.dtype == ATTN_F32) return p.d == 64 ? fwd_t<float, 64>(p, Q, K, V, O, lse, st)
+                                            : fwd_t<float, 128>(p, Q, K, V, O, lse, st);
+  return p.d == 64 ? fwd_t<__nv_bfloat16, 64>(p, Q, K, V, O, lse, st)
+                   : fwd_t<__nv_bfloat16, 128>(p, Q, K, V, O, lse, st);
+}
+
+cudaError_t simt_bwd(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
+                     const void* dO, const float* lse, void* dQ, void* dK, void* dV, int gproj, float4* ws,
+                     cudaStream_t st) {
+  if (p.dtype == ATTN_F32)
+    return p.d == 64 ? bwd_t<float, 64, false>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, st)
+                     : bwd_t<float, 128, false>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, st);
+  if (gproj)
+    return p.d == 64 ? bwd_t<__nv_bfloat16, 64, true>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, st)
+                     : bwd_t<__nv_bfloat16, 128, true>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, st);
+  return p.d == 64 ? bwd_t<__nv_bfloat16, 64, false>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, st)
+                   : bwd_t<__nv_bfloat16, 128, false>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, st);
+}
+
+cudaError_t simt_bob(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
+                     const void* dO, const float* lse, const void* a, const void* b, const void* c, void* gQ,
+                     void* gK, void* gV, void* gdO, float4* ws, cudaStream_t st) {
+  if (p.dtype == ATTN_F32)
+    return p.d == 64 ? bob_t<float, 64>(p, Q, K, V, O, dO, lse, a, b, c, gQ, gK, gV, gdO, ws, st)
+                     : bob_t<float, 128>(p, Q, K, V, O, dO, lse, a, b, c, gQ, gK, gV, gdO, ws, st);
+  return p.d == 64 ? bob_t<__nv_bfloat16, 64>(p, Q, K, V, O, dO, lse, a, b, c, gQ, gK, gV, gdO, ws, st)
+                   : bob_t<__nv_bfloat16, 128>(p, Q, K, V, O, dO, lse, a, b, c, gQ, gK, gV, gdO, ws, st);
+}
+
+cudaError_t simt_projected_dS(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
+                              const void* dO, const float* lse, float* dS, cudaStream_t st) {
+  using T = __nv_bfloat16;
+  if (p.d == 64)
+    projected_dS_kernel<T, 64><<<grid_for(p), kThreads, 0, st>>>(
+        static_cast<const T*>(Q), static_cast<const T*>(K), static_cast<const T*>(V), static_cast<const T*>(O),
+        static_cast<const T*>(dO), lse, dS, p.N, p.BH, p.scale);
+  else
+    projected_dS_kernel<T, 128><<<grid_for(p), kThreads, 0, st>>>(
+        static_cast<const T*>(Q), static_cast<const T*>(K), static_cast<const T*>(V), static_cast<const T*>(O),
+        static_cast<const T*>(dO), lse, dS, p.N, p.BH, p.scale);
+  return cudaGetLastError();
+}
+
+}  // namespace fbd

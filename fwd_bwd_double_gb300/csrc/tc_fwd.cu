@@ -1,0 +1,301 @@
+// bf16 causal attention forward on sm_103a: TMA-fed shared-memory tiles, tcgen05
+// MMAs accumulating in tensor memory, online softmax on CUDA cores.
+//
+// "Flash attention for trading models", sections "The Flash Attention algorithm"
+// and "Online softmax recurrence": one CTA owns a block of BM = 128 query rows and
+// streams key/value blocks of BN = 128 keys (only blocks j <= i: section "Causal
+// masking ...": future blocks are never loaded).  Per block:
+//   S = Q K_j^T            tcgen05.mma, A = Q and B = K_j from shared memory,
+//                          accumulator in TMEM (128 lanes = query rows)
+//   m_new = max(m, rowmax S); p = 2^((S - m_new) s log2 e)   (subtract, then scale:
+//                          "FlashAttention bf16 gradient and GProj", "Why the error
+//                          appears late", so the row max maps to exactly 1)
+//   O <- O 2^((m - m_new) s log2 e) only for rows whose max moved (FA2's deferred
+//                          rescaling; O stays unnormalised until the end)
+//   O += P V_j             tcgen05.mma, A = P (bf16, written to shared memory in the
+//                          128-byte-swizzled K-major layout), B = V_j (MN-major)
+// and at the end O / l is written once and lse = m s + ln l.
+//
+// Warp roles (192 threads): warps 0-3 own TMEM lanes 0-127, one query row per
+// thread (softmax, rescale, epilogue); warp 4 issues TMA loads (Q once, K/V
+// through a 2-stage ring); warp 5 allocates TMEM and issues the MMAs.  With d = 64
+// two CTAs fit on an SM, so one CTA's softmax overlaps the other's MMAs.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fbd {
+namespace {
+
+__device__ unsigned int g_err = 0;
+
+constexpr int BM = 128;
+constexpr int BN = 128;
+constexpr int NS = 2;
+constexpr int kThreads = 192;
+
+template <int D>
+struct Layout {
+  static constexpr int kQ = BM * D * 2;   // bytes of the Q tile
+  static constexpr int kKV = BN * D * 2;  // bytes of one K (or V) tile
+  static constexpr int kP = BM * BN * 2;  // bytes of the P tile
+  static constexpr int oQ = 0;
+  static constexpr int oK = oQ + kQ;
+  static constexpr int oV = oK + NS * kKV;
+  static constexpr int oP = oV + NS * kKV;
+  static constexpr int oBar = oP + kP;
+  static constexpr int bytes = oBar + 128;
+  static constexpr int kTmemCols = 256;    // S: 128 columns, O: D columns
+};
+
+// Shared-memory descriptor of a K-major operand tile stored as 64-element
+// (128-byte) column slabs of `rows` rows each, advanced to K-step k (16 elements).
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int rows, int k) {
+  return ptx::sdesc_sw128(base + (k >> 2) * rows * 128 + (k & 3) * 32, 16, 1024);
+}
+// MN-major operand (rows = K index, 64-element slabs along MN of `rows` rows),
+// advanced to K-step k (16 rows).
+__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int rows, int k) {
+  return ptx::sdesc_sw128(base + k * 16 * 128, rows * 128, 1024);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
+    fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+               const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O, float* __restrict__ lse,
+               int N, int nrb, int BH, float scale, float scale_log2) {
+  using Lay = Layout<D>;
+  extern __shared__ __align__(1024) uint8_t sm[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Lay::oBar);
+  uint64_t* q_full = bars + 0;
+  uint64_t* full = bars + 1;            // [NS]
+  uint64_t* empty = bars + 1 + NS;      // [NS]
+  uint64_t* s_full = bars + 1 + 2 * NS;
+  uint64_t* p_ready = s_full + 1;
+  uint64_t* o_full = s_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 3);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = static_cast<int>(blockIdx.x % BH);
+  const int rb = nrb - 1 - static_cast<int>(blockIdx.x / BH);  // heaviest row blocks first
+  const int nkv = rb + 1;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(q_full, 1);
+    for (int s = 0; s < NS; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    ptx::mbar_init(s_full, 1);
+    ptx::mbar_init(p_ready, 128);
+    ptx::mbar_init(o_full, 1);
+    // The swizzled operand layout needs 1024-byte aligned tiles.
+    *abort_flag = (ptx::smem_u32(sm) & 1023u) ? 1 : 0;
+    if (*abort_flag) atomicOr(&g_err, FBD_ERR_TIMEOUT);
+    ptx::fence_mbar_init();
+  }
+  if (warp == 5) {
+    ptx::tmem_alloc(tmem_slot, Lay::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS = tmem;         // S accumulator: columns [0, 128)
+  const uint32_t tO = tmem + BN;    // O accumulator: columns [128, 128 + D)
+  const ptx::BoundedWait wait{abort_flag, &g_err};
+  const bool ok = *abort_flag == 0;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0 && ok) {
+      ptx::prefetch_tmap(&tmQ);
+      ptx::prefetch_tmap(&tmK);
+      ptx::prefetch_tmap(&tmV);
+      ptx::mbar_expect_tx(q_full, Lay::kQ);
+      for (int c = 0; c < D / 64; ++c) ptx::tma_load_3d(sm + Lay::oQ + c * BM * 128, &tmQ, q_full, c * 64, rb * BM, bh);
+      for (int j = 0; j < nkv; ++j) {
+        const int s = j % NS;
+        if (j >= NS) wait(&empty[s], ((j / NS) - 1) & 1);
+        ptx::mbar_expect_tx(&full[s], 2 * Lay::kKV);
+        for (int c = 0; c < D / 64; ++c) {
+          ptx::tma_load_3d(sm + Lay::oK + s * Lay::kKV + c * BN * 128, &tmK, &full[s], c * 64, j * BN, bh);
+          ptx::tma_load_3d(sm + Lay::oV + s * Lay::kKV + c * BN * 128, &tmV, &full[s], c * 64, j * BN, bh);
+        }
+      }
+      // Drain: the last NS stages must have been consumed before the CTA exits.
+      for (int j = (nkv > NS ? nkv - NS : 0); j < nkv; ++j) wait(&empty[j % NS], (j / NS) & 1);
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------- MMA issuer
+    if (lane == 0 && ok) {
+      constexpr uint32_t idS = ptx::idesc_bf16(BM, BN, 0, 0);
+      constexpr uint32_t idO = ptx::idesc_bf16(BM, D, 0, 1);
+      const uint32_t sQ = ptx::smem_u32(sm + Lay::oQ);
+      const uint32_t sK = ptx::smem_u32(sm + Lay::oK);
+      const uint32_t sV = ptx::smem_u32(sm + Lay::oV);
+      const uint32_t sP = ptx::smem_u32(sm + Lay::oP);
+      auto issue_pv = [&](int j) {
+        const uint32_t v = sV + (j % NS) * Lay::kKV;
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k)
+          ptx::mma_ss(tO, kmajor_desc(sP, BM, k), mnmajor_desc(v, BN, k), idO, (j > 0 || k > 0) ? 1u : 0u);
+        ptx::mma_commit(&empty[j % NS]);
+      };
+      wait(q_full, 0);
+      for (int j = 0; j < nkv; ++j) {
+        const int s = j % NS;
+        wait(&full[s], (j / NS) & 1);
+        if (j > 0) {
+          wait(p_ready, (j - 1) & 1);  // P_{j-1} written, S free, O rescaled
+          ptx::tc_fence_after();
+          issue_pv(j - 1);
+        }
+        ptx::tc_fence_after();
+        const uint32_t k = sK + s * Lay::kKV;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          ptx::mma_ss(tS, kmajor_desc(sQ, BM, kk), kmajor_desc(k, BN, kk), idS, kk > 0 ? 1u : 0u);
+        ptx::mma_commit(s_full);
+      }
+      wait(p_ready, (nkv - 1) & 1);
+      ptx::tc_fence_after();
+      issue_pv(nkv - 1);
+      ptx::mma_commit(o_full);
+    }
+  } else {
+    // ---------------------------------------- softmax: thread r owns query row r
+    const int r = threadIdx.x;                       // TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int64_t row = static_cast<int64_t>(rb) * BM + r;
+    uint8_t* P = sm + Lay::oP;
+    float m = -INFINITY, l = 0.f;
+    for (int j = 0; j < nkv; ++j) {
+      wait(s_full, j & 1);
+      ptx::tc_fence_after();
+      const bool diag = (j == rb);  // the only block holding keys after some rows
+      float mx = -INFINITY;
+#pragma unroll
+      for (int ch = 0; ch < BN / 32; ++ch) {
+        uint32_t v[32];
+        ptx::tmem_ld32(tS + lane_off + ch * 32, v);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int t = 0; t < 32; ++t) {
+          const float s = (diag && ch * 32 + t > r) ? -INFINITY : __uint_as_float(v[t]);
+          mx = fmaxf(mx, s);
+        }
+      }
+      const float m_new = fmaxf(m, mx);
+      const bool moved = (j > 0) && (m_new > m);
+      const float alpha = moved ? ptx::ex2((m - m_new) * scale_log2) : 1.f;
+      if (__any_sync(0xffffffffu, moved)) {
+#pragma unroll
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t v[32];
+          ptx::tmem_ld32(tO + lane_off + ch * 32, v);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * alpha);
+          ptx::tmem_st32(tO + lane_off + ch * 32, v);
+        }
+        ptx::tmem_wait_st();
+      }
+      l *= alpha;
+      m = m_new;
+      float rs = 0.f;
+#pragma unroll
+      for (int ch = 0; ch < BN / 32; ++ch) {
+        uint32_t v[32];
+        ptx::tmem_ld32(tS + lane_off + ch * 32, v);
+        ptx::tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int t = 0; t < 32; t += 2) {
+          const bool k0 = diag && ch * 32 + t > r, k1 = diag && ch * 32 + t + 1 > r;
+          const float p0 = k0 ? 0.f : ptx::ex2((__uint_as_float(v[t]) - m) * scale_log2);
+          const float p1 = k1 ? 0.f : ptx::ex2((__uint_as_float(v[t + 1]) - m) * scale_log2);
+          rs += p0 + p1;
+          pk[t >> 1] = ptx::pack_bf16(p0, p1);
+        }
+        // keys ch*32 .. ch*32+31 -> four 16-byte chunks of the swizzled K-major P tile
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int kk = ch * 32 + u * 8;
+          const int slab = kk >> 6, chunk = (kk & 63) >> 3;
+          uint4* dst = reinterpret_cast<uint4*>(P + slab * BM * 128 + r * 128 + ((chunk ^ (r & 7)) << 4));
+          *dst = make_uint4(pk[u * 4], pk[u * 4 + 1], pk[u * 4 + 2], pk[u * 4 + 3]);
+        }
+      }
+      l += rs;
+      ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(p_ready);
+    }
+    // ------------------------------------------------------------------ epilogue
+    wait(o_full, 0);
+    ptx::tc_fence_after();
+    const float inv = 1.f / l;
+#pragma unroll
+    for (int ch = 0; ch < D / 32; ++ch) {
+      uint32_t v[32];
+      ptx::tmem_ld32(tO + lane_off + ch * 32, v);
+      ptx::tmem_wait_ld();
+      if (row < N) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int t = 0; t < 32; t += 2)
+          pk[t >> 1] = ptx::pack_bf16(__uint_as_float(v[t]) * inv, __uint_as_float(v[t + 1]) * inv);
+        uint4* dst = reinterpret_cast<uint4*>(O + (static_cast<int64_t>(bh) * N + row) * D + ch * 32);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) dst[u] = make_uint4(pk[u * 4], pk[u * 4 + 1], pk[u * 4 + 2], pk[u * 4 + 3]);
+      }
+    }
+    if (row < N) lse[static_cast<int64_t>(bh) * N + row] = m * scale + logf(l);
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, Lay::kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch(const Problem& p, const void* Q, const void* K, const void* V, void* O, float* lse,
+                   cudaStream_t st) {
+  alignas(64) CUtensorMap mq, mk, mv;
+  if (!make_tmap_bf16(&mq, Q, p.N, D, p.BH, BM) || !make_tmap_bf16(&mk, K, p.N, D, p.BH, BN) ||
+      !make_tmap_bf16(&mv, V, p.N, D, p.BH, BN))
+    return cudaErrorInvalidValue;
+  const int nrb = static_cast<int>((p.N + BM - 1) / BM);
+  const size_t smem = Layout<D>::bytes;
+  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const float log2e = 1.4426950408889634f;
+  fwd_kernel<D><<<static_cast<unsigned>(nrb * p.BH), kThreads, smem, st>>>(
+      mq, mk, mv, static_cast<__nv_bfloat16*>(O), lse, static_cast<int>(p.N), nrb, static_cast<int>(p.BH),
+      p.scale, p.scale * log2e);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t tc_fwd(const Problem& p, const void* Q, const void* K, const void* V, void* O, float* lse,
+                   cudaStream_t st) {
+  return p.d == 64 ? launch<64>(p, Q, K, V, O, lse, st) : launch<128>(p, Q, K, V, O, lse, st);
+}
+
+uint32_t tc_fwd_take_error() {
+  uint32_t v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, g_err, sizeof(v)) != cudaSuccess) return 0;
+  if (v) cudaMemcpyToSymbol(g_err, &z, sizeof(z));
+  return v;
+}
+
+}  // namespace fbd

@@ -1,0 +1,170 @@
+/*
+ * fbd.h -- C ABI of libfbd: exact causal softmax attention on GB300 (sm_103a):
+ * forward, recompute backward (optional GProj), and backward-over-backward.
+ *
+ * The N x N score matrix is never written to device memory.  All entry points
+ * take plain device pointers owned by the caller; the library allocates and
+ * frees nothing.
+ *
+ * Sources (cited by page title and section):
+ *   [FA]   "Flash attention for trading models": "Why attention is memory-bound"
+ *          (S = Q K^T / sqrt(d), softmax, O = P V), "The Flash Attention
+ *          algorithm" (tiling into row and column blocks), "Online softmax
+ *          recurrence", "Backward pass: recompute instead of store" (only O and
+ *          the softmax statistics are kept), "Causal masking is where trading
+ *          gets a discount", "Eight-line integration" (q, k, v shaped
+ *          (batch, heads, seq, head_dim)).
+ *   [GP]   "FlashAttention bf16 gradient and GProj": "Why the error appears late"
+ *          (subtract the row max before scaling), "How the zero sum turns into a
+ *          false gradient" (bf16 rounding of dS, GProj).
+ *   [BoB]  "FlashBoB: second-order attention": "Why go backward through an
+ *          already computed gradient" (definition of backward-over-backward),
+ *          "Two scalar states replace quadratic tensors" (row pass, column pass).
+ *
+ * Conventions shared by every entry point
+ *   Layout:     every [B,H,N,d] tensor is contiguous row-major (d fastest), the
+ *               (batch, heads, seq, head_dim) order of [FA] "Eight-line
+ *               integration".  Statistics are [B,H,N] float32, contiguous.
+ *   Types:      desc->dtype selects the element type of every [B,H,N,d] tensor
+ *               (inputs and outputs alike): ATTN_F32 = float, ATTN_BF16 =
+ *               bfloat16.  Arithmetic is float32 throughout (bf16 tensor-core
+ *               products accumulate in float32).
+ *   Supported:  causal == 1; d in {64, 128}; dtype in {ATTN_F32, ATTN_BF16};
+ *               for attn_bob with ATTN_BF16, d == 64.  Anything else returns
+ *               ATTN_ERR_UNSUPPORTED before any launch; there is no fallback.
+ *   Scale:      desc->scale == 0 means 1/sqrt(d); otherwise it must be finite.
+ *   Pointers:   device pointers, 16-byte aligned (ATTN_ERR_ALIGNMENT otherwise),
+ *               non-NULL whenever B*H*N > 0 (ATTN_ERR_INVALID_ARG).  Outputs must
+ *               not overlap inputs, each other, or the workspace
+ *               (ATTN_ERR_INVALID_ARG).  Empty problems (B*H*N == 0) return
+ *               ATTN_OK without touching memory.
+ *   Streams:    `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *               Calls are asynchronous: argument errors are returned at once;
+ *               a launch failure returns ATTN_ERR_LAUNCH; a device-side wait that
+ *               gave up (bounded waits; never expected) is reported by
+ *               attn_device_status().  Outputs are valid once the stream is
+ *               synchronised.  Each output element is written exactly once.
+ *   Ragged N:   any N >= 1 is accepted; tiles past N are zero-filled on load and
+ *               never stored.
+ */
+#ifndef FBD_H
+#define FBD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,  /* NULL/negative/overlapping arguments, non-finite scale */
+  ATTN_ERR_UNSUPPORTED = 2,  /* causal != 1, d not supported, unknown dtype */
+  ATTN_ERR_ALIGNMENT = 3,    /* a pointer is not 16-byte aligned */
+  ATTN_ERR_WORKSPACE = 4,    /* workspace NULL or smaller than the *_workspace_bytes query */
+  ATTN_ERR_LAUNCH = 5,       /* CUDA rejected a launch or a tensor-map encode */
+  ATTN_ERR_TIMEOUT = 6,      /* a bounded device-side wait gave up (see attn_device_status) */
+  ATTN_ERR_DEVICE = 7        /* no usable CUDA device / driver entry point */
+} attn_status_t;
+
+typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1 } attn_dtype_t;
+
+typedef struct {
+  int64_t B, H, N, d;  /* batch, heads, sequence length, head dimension */
+  float scale;         /* softmax scale s; 0 means 1/sqrt(d) */
+  int32_t causal;      /* must be 1: key j is visible to query i iff j <= i */
+  int32_t dtype;       /* attn_dtype_t */
+} attn_desc_t;
+
+/* Forward.  [FA] "The Flash Attention algorithm", "Online softmax recurrence",
+ * causal masking; [GP] "Why the error appears late" (max subtracted before the
+ * scale is applied, so the row max maps to exactly exp(0) = 1).
+ *   In:  Q, K, V [B,H,N,d].
+ *   Out: O [B,H,N,d] = softmax(s Q K^T + causal mask) V;
+ *        lse [B,H,N] float32, lse_i = log sum_{j<=i} exp(s q_i.k_j) (natural log),
+ *        the single-number form of the softmax statistics (m, l) kept for the
+ *        recompute backward ([FA] "Backward pass: recompute instead of store"). */
+attn_status_t attn_fwd(const attn_desc_t* desc, const void* Q, const void* K, const void* V,
+                       void* O, float* lse, void* stream);
+
+/* Workspace for attn_bwd: 16 bytes per (b,h,row) = one float4 of row statistics
+ * (lse, D, GProj coefficient, 0) written by the row pass and read by the column
+ * pass. */
+size_t attn_bwd_workspace_bytes(const attn_desc_t* desc, int gproj);
+
+/* Recompute backward.  [FA] "Backward pass: recompute instead of store": P is
+ * rebuilt from Q, K and lse; nothing N x N is stored.  With
+ *   dP = dO V^T, D_i = sum_k dO_ik O_ik, dS = P * (dP - D):
+ *   dQ = s dS K,  dK = s dS^T Q,  dV = P^T dO          (all [B,H,N,d]).
+ * Two launches on `stream`: a row pass (dQ and the row statistics) and a column
+ * pass (dK, dV).
+ * gproj != 0 (bf16 only; ignored for ATTN_F32, whose dS is never rounded):
+ *   [GP] "How the zero sum turns into a false gradient".  The row of dS is rounded
+ *   to bf16 (dS^) before the dS K and dS^T Q products; its remaining mass
+ *   r_i = sum_j dS^_ij is removed by subtracting r_i * P^_ij / sum_k P^_ik, where
+ *   P^ is the bf16 probability row the kernel feeds to its products, so that the
+ *   row the products see sums to zero.  The query correction is applied inside
+ *   the row pass; the key correction needs r_i of complete rows and is applied in
+ *   the column pass.
+ *   workspace: >= attn_bwd_workspace_bytes(desc, gproj) bytes of device memory,
+ *   16-byte aligned, contents ignored on entry; it holds row statistics after. */
+attn_status_t attn_bwd(const attn_desc_t* desc, const void* Q, const void* K, const void* V,
+                       const void* O, const void* dO, const float* lse,
+                       void* dQ, void* dK, void* dV, int gproj,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace for attn_bob: 16 bytes per (b,h,row) = float4 (lse, D, E, F). */
+size_t attn_bob_workspace_bytes(const attn_desc_t* desc);
+
+/* Backward over backward.  [BoB] "Why go backward through an already computed
+ * gradient": with Phi(Q,K,V,dO) = (dQ,dK,dV) the first backward and cotangents
+ * gdQ, gdK, gdV of its outputs, returns the vector-Jacobian product
+ *   (gQ, gK, gV, gdO) = d/d(Q,K,V,dO) [ <gdQ,dQ> + <gdK,dK> + <gdV,dV> ].
+ * With a = gdQ, b = gdK, c = gdV, G = s(a K^T + Q b^T), H = dO c^T and the two
+ * per-row scalar states ([BoB] "Two scalar states replace quadratic tensors")
+ *   E_i = sum_j P_ij G_ij,  F_i = sum_j P_ij (G_ij (dP_ij - D_i) - E_i dP_ij + H_ij):
+ *   gQ  = s (dS b + Sbar K),   gK = s (dS^T a + Sbar^T Q),
+ *   gV  = dPbar^T dO,          gdO = P c + dPbar V,
+ *   dPbar = P (G - E),  Sbar = P (G (dP - D) - E dP + H - F).
+ * Two launches: the row pass holds a block of query rows, streams keys, writes
+ * gQ, gdO and (lse, D, E, F) per row; the column pass holds a block of keys,
+ * streams rows, re-reads those states and writes gK, gV.
+ *   O, lse: the forward's outputs for the same Q, K, V (attn_fwd).
+ *   workspace: >= attn_bob_workspace_bytes(desc) bytes; holds (lse, D, E, F). */
+attn_status_t attn_bob(const attn_desc_t* desc, const void* Q, const void* K, const void* V,
+                       const void* O, const void* dO, const float* lse,
+                       const void* gdQ, const void* gdK, const void* gdV,
+                       void* gQ, void* gK, void* gV, void* gdO,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* Diagnostic export of the GProj-projected score gradient (bf16 only).
+ * Writes dS_out [B,H,N,N] float32 with dS_out[i][j] = dS^_ij - rho_i P^_ij for
+ * j <= i (and 0 for j > i), where dS^, P^ and rho_i = r_i / sum_k P^_ik are the
+ * very values the GProj row pass feeds to its products.  Meant for small N:
+ * the output is N x N per slice.  [GP] "How the zero sum turns into a false
+ * gradient". */
+attn_status_t attn_bwd_projected_dS(const attn_desc_t* desc, const void* Q, const void* K,
+                                    const void* V, const void* O, const void* dO,
+                                    const float* lse, float* dS_out, void* stream);
+
+/* Synchronises `stream` and reports (then clears) the device-side status word:
+ * ATTN_ERR_TIMEOUT if any kernel's bounded wait gave up since the last call,
+ * ATTN_ERR_LAUNCH if the stream holds a CUDA error, else ATTN_OK. */
+attn_status_t attn_device_status(void* stream);
+
+/* Static description of a status code (never NULL). */
+const char* attn_status_string(attn_status_t status);
+
+/* Human-readable detail of the most recent non-OK status on the calling thread
+ * (e.g. which argument was rejected); empty string if none. */
+const char* attn_last_error(void);
+
+/* Library build identification string. */
+const char* attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FBD_H */

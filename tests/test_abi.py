@@ -1,0 +1,131 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports every
+function include/fbd.h declares, and rejects bad arguments synchronously (before
+any CUDA call, so fake non-NULL pointers are never dereferenced)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import __graft_entry__
+
+__graft_entry__.build()
+import fwd_bwd_double_gb300 as fbd  # noqa: E402
+from fwd_bwd_double_gb300 import AttnDesc, lib  # noqa: E402
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "fbd.h")
+
+OK, INVALID, UNSUP, ALIGN, WS = 0, 1, 2, 3, 4
+FAKE = 1 << 40  # a 16-byte aligned address that is never dereferenced
+
+
+def declared_functions():
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_\w+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_function():
+    names = declared_functions()
+    assert "attn_fwd" in names and "attn_bwd" in names and "attn_bob" in names
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in fbd._lib.PROTOTYPES, f"binding lacks a prototype for {n}"
+
+
+def desc(B=1, H=2, N=64, d=64, scale=0.0, causal=1, dtype=1):
+    return AttnDesc(B, H, N, d, scale, causal, dtype)
+
+
+def ptrs(n, base=FAKE, stride=1 << 30):
+    return [ctypes.c_void_p(base + i * stride) for i in range(n)]
+
+
+def fwd(dsc, p=None):
+    p = p or ptrs(5)
+    return lib.attn_fwd(ctypes.byref(dsc), *p, None)
+
+
+def bwd(dsc, p=None, gproj=0, ws_bytes=None):
+    p = p or ptrs(10)
+    wsb = lib.attn_bwd_workspace_bytes(ctypes.byref(dsc), gproj) if ws_bytes is None else ws_bytes
+    return lib.attn_bwd(ctypes.byref(dsc), *p[:9], gproj, p[9], wsb, None)
+
+
+def bob(dsc, p=None, ws_bytes=None):
+    p = p or ptrs(14)
+    wsb = lib.attn_bob_workspace_bytes(ctypes.byref(dsc)) if ws_bytes is None else ws_bytes
+    return lib.attn_bob(ctypes.byref(dsc), *p[:13], p[13], wsb, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(causal=0), UNSUP), (dict(d=32), UNSUP), (dict(d=256), UNSUP), (dict(dtype=7), UNSUP),
+    (dict(B=-1), INVALID), (dict(N=-5), INVALID), (dict(d=0), INVALID),
+    (dict(scale=float("nan")), INVALID), (dict(scale=float("inf")), INVALID), (dict(scale=-1.0), INVALID),
+    (dict(N=1 << 31), INVALID),
+])
+def test_rejects_bad_descriptors(kw, code):
+    d = desc(**kw)
+    assert fwd(d) == code
+    assert bwd(d) == code
+    assert bob(d) == code
+    assert lib.attn_last_error()  # a detail message is recorded
+
+
+def test_bob_bf16_head_dim_128_is_unsupported_but_f32_is_checked_further():
+    assert bob(desc(d=128, dtype=1)) == UNSUP
+    # fp32 d=128 passes the descriptor check and fails on the NULL workspace instead
+    p = ptrs(14)
+    p[13] = ctypes.c_void_p(0)
+    assert bob(desc(d=128, dtype=0), p) == WS
+
+
+def test_null_misaligned_and_overlapping_pointers():
+    d = desc()
+    p = ptrs(5)
+    p[2] = ctypes.c_void_p(0)
+    assert fwd(d, p) == INVALID
+    p = ptrs(5)
+    p[1] = ctypes.c_void_p(FAKE + (1 << 30) + 8)
+    assert fwd(d, p) == ALIGN
+    p = ptrs(5)
+    p[3] = ctypes.c_void_p(FAKE + 1024)  # O inside Q
+    assert fwd(d, p) == INVALID
+    p = ptrs(10)
+    p[7] = p[6]                           # dK == dQ
+    assert bwd(d, p) == INVALID
+
+
+def test_workspace_checks():
+    d = desc(B=2, H=3, N=100)
+    assert lib.attn_bwd_workspace_bytes(ctypes.byref(d), 0) == 2 * 3 * 100 * 16
+    assert lib.attn_bwd_workspace_bytes(ctypes.byref(d), 1) == 2 * 3 * 100 * 16
+    assert lib.attn_bob_workspace_bytes(ctypes.byref(d)) == 2 * 3 * 100 * 16
+    assert bwd(d, ws_bytes=2 * 3 * 100 * 16 - 1) == WS
+    assert bob(d, ws_bytes=0) == WS
+    p = ptrs(14)
+    p[13] = ctypes.c_void_p(0)
+    assert bob(d, p) == WS
+
+
+def test_empty_problems_are_ok_without_touching_memory():
+    for kw in (dict(N=0), dict(B=0), dict(H=0)):
+        d = desc(**kw)
+        nulls = [ctypes.c_void_p(0)] * 14
+        assert fwd(d, nulls[:5]) == OK
+        assert bwd(d, nulls[:10]) == OK
+        assert bob(d, nulls) == OK
+
+
+def test_status_strings_and_version():
+    for code in range(8):
+        assert fbd.attn_status_string(code)
+    assert fbd.attn_status_string(99) == "unknown status"
+    assert "sm_103a" in fbd.attn_version()
+
+
+def test_python_binding_raises_on_error():
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(1, 1, 4, 32)  # d = 32 is unsupported: rejected before any device use
+    with pytest.raises(fbd.FbdError) as e:
+        fbd.attn_fwd(q, q, q, O=torch.zeros_like(q), lse=torch.zeros(1, 1, 4))
+    assert e.value.status == UNSUP

@@ -1,0 +1,229 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU fp64 oracle on the
+same seeded inputs.
+
+Tolerances (relative Frobenius error per output tensor over all slices checked):
+1e-5 for float32 inputs, 2e-2 for bf16 inputs with fp32 accumulation.  At long
+sequence lengths the oracle checks sampled rows (row-pass outputs) and late
+columns (column-pass outputs, which need only the rows after them)."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from gpu_util import host, inputs, oracle_full, rel_fro, row_rel_errors, run_ops, to_device
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-5, "bf16": 2e-2}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def check_full(w, got, ops):
+    tol = TOL[w.dtype]
+    errs = {}
+    f = oracle_full(w, "fwd")
+    errs["O"], errs["L"] = rel_fro(host(got["O"]), f["O"]), rel_fro(host(got["L"]), f["L"])
+    if "bwd" in ops:
+        b = oracle_full(w, "bwd")
+        for k in ("dQ", "dK", "dV"):
+            errs[k] = rel_fro(host(got[k]), b[k])
+    if "bob" in ops:
+        b = oracle_full(w, "bob")
+        for k in ("gQ", "gK", "gV", "gdO"):
+            errs[k] = rel_fro(host(got[k]), b[k])
+    bad = {k: v for k, v in errs.items() if not v <= tol}
+    assert not bad, f"{w.name}: errors above {tol}: {bad} (all: {errs})"
+    return errs
+
+
+def test_tiny_f32_all_ops():
+    w = W.TINY_F32
+    got = run_ops(w, to_device(inputs(w), w))
+    errs = check_full(w, got, ("bwd", "bob"))
+    print(w.name, {k: f"{v:.2e}" for k, v in errs.items()})
+
+
+@pytest.mark.parametrize("gproj", [0, 1])
+def test_gpt2_layer_bf16(gproj):
+    w = W.GPT2_LAYER
+    got = run_ops(w, to_device(inputs(w), w), ops=("bwd", "bob") if gproj == 0 else ("bwd",), gproj=gproj)
+    errs = check_full(w, got, ("bwd", "bob") if gproj == 0 else ("bwd",))
+    print(w.name, gproj, {k: f"{v:.2e}" for k, v in errs.items()})
+
+
+def test_long_sweep_n4096_all_heads():
+    w = W.LONG_SWEEP[0]
+    got = run_ops(w, to_device(inputs(w), w))
+    errs = check_full(w, got, ("bwd", "bob"))
+    print(w.name, {k: f"{v:.2e}" for k, v in errs.items()})
+
+
+def sampled_check(w, got, ops, heads, rows, cols):
+    """Oracle on sampled rows (row outputs) and columns (column outputs) of given heads."""
+    tol = TOL[w.dtype]
+    errs = {}
+    x = W.inputs(w, heads=heads, batches=[0])
+    acc = {k: ([], []) for k in ("O", "L", "dQ", "dK", "dV", "gQ", "gK", "gV", "gdO")}
+    for hi, h in enumerate(heads):
+        s = {k: v[0, hi].astype(np.float64) for k, v in x.items()}
+        O, L = oracle.forward_rows(s["Q"], s["K"], s["V"], rows, scale=w.scale)
+        acc["O"][0].append(host(got["O"][0, h])[rows]); acc["O"][1].append(O)
+        acc["L"][0].append(host(got["L"][0, h])[rows]); acc["L"][1].append(L)
+        if "bwd" in ops:
+            acc["dQ"][0].append(host(got["dQ"][0, h])[rows])
+            acc["dQ"][1].append(oracle.backward_rows(s["Q"], s["K"], s["V"], s["dO"], rows, scale=w.scale))
+            dK, dV = oracle.backward_cols(s["Q"], s["K"], s["V"], s["dO"], cols, scale=w.scale)
+            acc["dK"][0].append(host(got["dK"][0, h])[cols]); acc["dK"][1].append(dK)
+            acc["dV"][0].append(host(got["dV"][0, h])[cols]); acc["dV"][1].append(dV)
+        if "bob" in ops:
+            r = oracle.bob_rows(s["Q"], s["K"], s["V"], s["dO"], s["gdQ"], s["gdK"], s["gdV"], rows, scale=w.scale)
+            acc["gQ"][0].append(host(got["gQ"][0, h])[rows]); acc["gQ"][1].append(r["gQ"])
+            acc["gdO"][0].append(host(got["gdO"][0, h])[rows]); acc["gdO"][1].append(r["gdO"])
+            gK, gV = oracle.bob_cols(s["Q"], s["K"], s["V"], s["dO"], s["gdQ"], s["gdK"], s["gdV"], cols,
+                                     scale=w.scale)
+            acc["gK"][0].append(host(got["gK"][0, h])[cols]); acc["gK"][1].append(gK)
+            acc["gV"][0].append(host(got["gV"][0, h])[cols]); acc["gV"][1].append(gV)
+    for k, (g, r) in acc.items():
+        if g:
+            errs[k] = rel_fro(np.concatenate(g), np.concatenate(r))
+    bad = {k: v for k, v in errs.items() if not v <= tol}
+    assert not bad, f"{w.name}: sampled errors above {tol}: {bad} (all: {errs})"
+    return errs
+
+
+def sample_rows_cols(N, rng, n_rows=48, n_tail_cols=96):
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, N - 1], rng.integers(0, N, n_rows), np.arange(N - 40, N)]))
+    cols = np.unique(np.concatenate([np.arange(N - n_tail_cols, N), rng.integers(N - 4096, N, 16)]))
+    return rows[(rows >= 0) & (rows < N)], cols[(cols >= 0) & (cols < N)]
+
+
+@pytest.mark.parametrize("N", [16384])
+def test_long_sweep_sampled(N):
+    w = W.LONG_SWEEP[0].with_n(N)
+    x = to_device(W.inputs(w), w)
+    got = run_ops(w, x)
+    rows, cols = sample_rows_cols(N, np.random.default_rng(N))
+    errs = sampled_check(w, got, ("bwd", "bob"), heads=[0, 11], rows=rows, cols=cols)
+    print(w.name, {k: f"{v:.2e}" for k, v in errs.items()})
+
+
+def test_full_day_ragged_tail():
+    w = W.FULL_DAY
+    x = to_device(W.inputs(w), w)
+    got = run_ops(w, x, ops=("bwd",))
+    # The batch-0 heads checked; rows include the whole ragged last tile (104 rows).
+    rows, cols = sample_rows_cols(w.N, np.random.default_rng(3))
+    rows = np.unique(np.concatenate([rows, np.arange(w.N - 104, w.N)]))
+    errs = sampled_check(w, got, ("bwd",), heads=[0, 7], rows=rows, cols=cols)
+    print(w.name, {k: f"{v:.2e}" for k, v in errs.items()})
+    # batch 1 (a different slice offset) and no NaN anywhere
+    for k in ("O", "dQ", "dK", "dV"):
+        assert not np.isnan(host(got[k])).any(), k
+
+
+def test_large_key_gproj_reduces_dQ_error():
+    """GProj page, "How the zero sum turns into a false gradient": large shared key
+    mean + near-copy queries.  Reports the median per-row relative dQ error with and
+    without GProj on batches 0-1 (16 slices) against the exact fp64 dQ."""
+    import fwd_bwd_double_gb300 as fbd
+    w = W.LARGE_KEY
+    x = W.inputs(w)
+    xd = to_device(x, w)
+    O, lse = fbd.attn_fwd(xd["Q"], xd["K"], xd["V"], scale=w.scale)
+    dQ0, dK0, _ = fbd.attn_bwd(xd["Q"], xd["K"], xd["V"], O, xd["dO"], lse, gproj=0, scale=w.scale)
+    dQ1, dK1, dV1 = fbd.attn_bwd(xd["Q"], xd["K"], xd["V"], O, xd["dO"], lse, gproj=1, scale=w.scale)
+    fbd.attn_device_status()
+    e0, e1, maxp = [], [], []
+    for b in range(2):
+        for h in range(w.H):
+            s = {k: x[k][b, h].astype(np.float64) for k in ("Q", "K", "V", "dO")}
+            ref = oracle.backward(s["Q"], s["K"], s["V"], s["dO"], scale=w.scale)
+            e0.append(row_rel_errors(host(dQ0[b, h]), ref["dQ"]))
+            e1.append(row_rel_errors(host(dQ1[b, h]), ref["dQ"]))
+            P, _ = oracle.softmax_rows(oracle.scores(s["Q"], s["K"], np.arange(256, 2048, 64), w.scale))
+            maxp.append(P.max(axis=1))
+    m0, m1 = float(np.median(np.concatenate(e0))), float(np.median(np.concatenate(e1)))
+    print(f"{w.name}: median row dQ rel err no-GProj {m0:.4e}, GProj {m1:.4e}; "
+          f"median row max P {float(np.median(np.concatenate(maxp))):.3f}")
+    assert m1 < m0
+
+
+def test_large_key_projected_rows_sum_to_zero():
+    """The projected dS rows fed to the products sum to zero within 1e-6 of their L1 norm."""
+    import fwd_bwd_double_gb300 as fbd
+    w = W.LARGE_KEY
+    x = W.inputs(w, batches=[0], heads=[0, 5])
+    xd = to_device(x, w)
+    O, lse = fbd.attn_fwd(xd["Q"], xd["K"], xd["V"], scale=w.scale)
+    dS = host(fbd.attn_bwd_projected_dS(xd["Q"], xd["K"], xd["V"], O, xd["dO"], lse, scale=w.scale))
+    rs = np.abs(dS.sum(axis=-1))
+    l1 = np.abs(dS).sum(axis=-1)
+    keep = l1 > 0
+    worst = float(np.max(rs[keep] / l1[keep]))
+    print(f"{w.name}: max |row sum| / L1 of projected dS = {worst:.3e}")
+    assert worst <= 1e-6
+    assert np.all(np.triu(dS[0, 0], 1) == 0)
+
+
+EDGE_N = [1, 2, 15, 17, 127, 128, 129, 255, 300]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", EDGE_N)
+def test_edge_sizes(N, d, dtype):
+    w = W.Workload(f"edge_B1H2N{N}d{d}_{dtype}", 1, 2, N, d, dtype)
+    ops = ("bwd", "bob") if (dtype == "f32" or d == 64) else ("bwd",)
+    got = run_ops(w, to_device(inputs(w), w), ops=ops)
+    check_full(w, got, ops)
+
+
+def test_outputs_written_once_and_nothing_outside():
+    """Outputs live inside NaN-filled guard buffers: every output element is written
+    (no NaN left) and no guard element is touched."""
+    import torch
+
+    import fwd_bwd_double_gb300 as fbd
+    w = W.Workload("guard_B1H3N200d64", 1, 3, 200, 64, "bf16")
+    xd = to_device(inputs(w), w)
+    n = xd["Q"].numel()
+    pad = 4096
+
+    def guarded():
+        buf = torch.full((n + 2 * pad,), float("nan"), dtype=torch.bfloat16, device="cuda")
+        return buf, buf[pad:pad + n].view_as(xd["Q"])
+
+    def lse_guarded():
+        buf = torch.full((3 * 200 + 2 * pad,), float("nan"), dtype=torch.float32, device="cuda")
+        return buf, buf[pad:pad + 600].view(1, 3, 200)
+
+    bufs = {k: guarded() for k in ("O", "dQ", "dK", "dV", "gQ", "gK", "gV", "gdO")}
+    lb, lse = lse_guarded()
+    O = bufs["O"][1]
+    fbd.attn_fwd(xd["Q"], xd["K"], xd["V"], O=O, lse=lse)
+    fbd.attn_bwd(xd["Q"], xd["K"], xd["V"], O, xd["dO"], lse, gproj=1, dQ=bufs["dQ"][1], dK=bufs["dK"][1],
+                 dV=bufs["dV"][1])
+    fbd.attn_bob(xd["Q"], xd["K"], xd["V"], O, xd["dO"], lse, xd["gdQ"], xd["gdK"], xd["gdV"], gQ=bufs["gQ"][1],
+                 gK=bufs["gK"][1], gV=bufs["gV"][1], gdO=bufs["gdO"][1])
+    fbd.attn_device_status()
+    for k, (buf, view) in list(bufs.items()) + [("lse", (lb, lse))]:
+        b = buf.float().cpu().numpy()
+        assert np.isnan(b[:pad]).all() and np.isnan(b[-pad:]).all(), f"{k}: guard touched"
+        assert not np.isnan(view.float().cpu().numpy()).any(), f"{k}: element not written"
+
+
+def test_deterministic():
+    w = W.GPT2_LAYER.with_n(512)
+    xd = to_device(inputs(w), w)
+    a = run_ops(w, xd)
+    b = run_ops(w, xd)
+    for k in a:
+        assert np.array_equal(host(a[k]), host(b[k])), k
