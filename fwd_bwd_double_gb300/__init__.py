@@ -16,7 +16,7 @@ from ._lib import (ATTN_BF16, ATTN_F32, AttnDesc, FbdError, lib, status_name)  #
 
 __all__ = [
     "attn_fwd", "attn_bwd", "attn_bob", "attn_bwd_workspace_bytes", "attn_bob_workspace_bytes",
-    "attn_bwd_projected_dS", "attn_device_status", "attn_status_string", "attn_version", "make_desc",
+    "attn_bob_static", "attn_bwd_projected_dS", "attn_device_status", "attn_status_string", "attn_version", "make_desc",
     "FbdError", "AttnDesc", "ATTN_F32", "ATTN_BF16", "lib",
 ]
 
@@ -125,6 +125,22 @@ def attn_bob(Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ=None, gK=None, gV=None, gdO=
                         _ptr(gdQ), _ptr(gdK), _ptr(gdV), _ptr(gQ), _ptr(gK), _ptr(gV), _ptr(gdO),
                         _ptr(workspace), ctypes.c_size_t(workspace.numel() * workspace.element_size()),
                         _stream(stream)))
+    return gQ, gK, gV, gdO
+
+
+def attn_bob_static(Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ=None, gK=None, gV=None, gdO=None,
+                    scale: float = 0.0, stream=None, desc=None):
+    """attn_bob without a workspace argument: the library's static scratch array is used
+    (for callers that cannot allocate device memory; B*H*N <= 1,048,576)."""
+    torch = _torch()
+    desc = desc or make_desc(Q, scale)
+    gQ = torch.empty_like(Q) if gQ is None else gQ
+    gK = torch.empty_like(K) if gK is None else gK
+    gV = torch.empty_like(V) if gV is None else gV
+    gdO = torch.empty_like(dO) if gdO is None else gdO
+    _check(lib.attn_bob_static(ctypes.byref(desc), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(lse),
+                               _ptr(gdQ), _ptr(gdK), _ptr(gdV), _ptr(gQ), _ptr(gK), _ptr(gV), _ptr(gdO),
+                               _stream(stream)))
     return gQ, gK, gV, gdO
 
 

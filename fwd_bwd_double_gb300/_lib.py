@@ -38,6 +38,7 @@ PROTOTYPES = {
     "attn_bwd": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int, _P, ctypes.c_size_t, _P]),
     "attn_bob_workspace_bytes": (ctypes.c_size_t, [_D]),
     "attn_bob": (ctypes.c_int, [_D] + [_P] * 13 + [_P, ctypes.c_size_t, _P]),
+    "attn_bob_static": (ctypes.c_int, [_D] + [_P] * 13 + [_P]),
     "attn_bwd_projected_dS": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, _P]),
     "attn_device_status": (ctypes.c_int, [_P]),
     "attn_status_string": (ctypes.c_char_p, [ctypes.c_int]),

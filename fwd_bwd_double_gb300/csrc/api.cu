@@ -101,9 +101,9 @@ bool tc_supports(int op, int64_t d) {
 }
 }  // namespace fbd
 
-namespace {
-
-}  // namespace
+namespace fbd {
+attn_status_t set_last_error(attn_status_t s, const char* msg) { return fail(s, "%s", msg); }
+}  // namespace fbd
 
 extern "C" {
 

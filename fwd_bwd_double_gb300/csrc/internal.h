@@ -47,6 +47,12 @@ uint32_t tc_fwd_take_error();
 uint32_t tc_bwd_take_error();
 uint32_t tc_bob_take_error();
 
+// Record `msg` as the calling thread's attn_last_error() detail; returns s.
+attn_status_t set_last_error(attn_status_t s, const char* msg);
+
+// Size of the file-scope scratch array behind attn_bob_static.
+size_t static_bob_scratch_bytes();
+
 // Tensor maps: 3-D bf16 view (d, N, B*H) of a [B,H,N,d] tensor, box (64, rows, 1),
 // 128-byte swizzle.  Returns false if the driver entry point is missing or the
 // encode fails.

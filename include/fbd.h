@@ -138,6 +138,28 @@ attn_status_t attn_bob(const attn_desc_t* desc, const void* Q, const void* K, co
                        void* gQ, void* gK, void* gV, void* gdO,
                        void* workspace, size_t workspace_bytes, void* stream);
 
+/* attn_bob for callers that cannot allocate device memory.  The source pages have
+ * no counterpart of this entry point.  Some callers cannot obtain device memory
+ * of their own (for example a plugin inside a host application whose memory
+ * manager owns the device, or a deployment with a fixed memory plan that forbids
+ * allocation after start-up), so this variant takes no workspace: the row
+ * statistics live in a file-scope device array of 16 MiB, enough for
+ * B*H*N <= 1,048,576 rows.  Larger problems return ATTN_ERR_WORKSPACE without
+ * launching anything (use attn_bob with a caller workspace instead).
+ *   Arguments, outputs and errors are those of attn_bob minus the workspace.
+ *   The array is held by every GPU that loads the library until process exit.
+ *   The first call on each device looks up the array's device address with
+ *   cudaGetSymbolAddress (that device must be current) and caches it; make that
+ *   first call before any stream capture.  No call allocates or frees memory.
+ *   All calls share the one array, which keeps the last call's contents; nothing
+ *   in it needs clearing (the row pass writes every entry the column pass reads).
+ *   Calls whose executions overlap on the GPU (other streams, or other host
+ *   threads) race on the array: serialise them. */
+attn_status_t attn_bob_static(const attn_desc_t* desc, const void* Q, const void* K, const void* V,
+                              const void* O, const void* dO, const float* lse,
+                              const void* gdQ, const void* gdK, const void* gdV,
+                              void* gQ, void* gK, void* gV, void* gdO, void* stream);
+
 /* Diagnostic export of the GProj-projected score gradient (bf16 only).
  * Writes dS_out [B,H,N,N] float32 with dS_out[i][j] = dS^_ij - rho_i P^_ij for
  * j <= i (and 0 for j > i), where dS^, P^ and rho_i = r_i / sum_k P^_ik are the
