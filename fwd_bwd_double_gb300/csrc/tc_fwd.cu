@@ -12,14 +12,15 @@
 //                          appears late", so the row max maps to exactly 1)
 //   O <- O 2^((m - m_new) s log2 e) only for rows whose max moved (FA2's deferred
 //                          rescaling; O stays unnormalised until the end)
-//   O += P V_j             tcgen05.mma, A = P (bf16, written to shared memory in the
-//                          128-byte-swizzled K-major layout), B = V_j (MN-major)
+//   O += P V_j             tcgen05.mma, A = P (bf16, two values per 32-bit TMEM
+//                          column, lane = query row), B = V_j (MN-major, shared)
 // and at the end O / l is written once and lse = m s + ln l.
 //
 // Warp roles (192 threads): warps 0-3 own TMEM lanes 0-127, one query row per
 // thread (softmax, rescale, epilogue); warp 4 issues TMA loads (Q once, K/V
 // through a 2-stage ring); warp 5 allocates TMEM and issues the MMAs.  With d = 64
-// two CTAs fit on an SM, so one CTA's softmax overlaps the other's MMAs.
+// two CTAs fit on an SM (80 KB shared, 256 TMEM columns each), so one CTA's
+// softmax overlaps the other's MMAs.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -39,14 +40,13 @@ template <int D>
 struct Layout {
   static constexpr int kQ = BM * D * 2;   // bytes of the Q tile
   static constexpr int kKV = BN * D * 2;  // bytes of one K (or V) tile
-  static constexpr int kP = BM * BN * 2;  // bytes of the P tile
   static constexpr int oQ = 0;
   static constexpr int oK = oQ + kQ;
   static constexpr int oV = oK + NS * kKV;
-  static constexpr int oP = oV + NS * kKV;
-  static constexpr int oBar = oP + kP;
+  static constexpr int oBar = oV + NS * kKV;
   static constexpr int bytes = oBar + 128;
-  static constexpr int kTmemCols = 256;    // S: 128 columns, O: D columns
+  // TMEM columns: S fp32 [0, 128), P bf16 pairs [128, 192), O fp32 [192, 192 + D).
+  static constexpr int kTmemCols = (192 + D <= 256) ? 256 : 512;
 };
 
 // Shared-memory descriptor of a K-major operand tile stored as 64-element
@@ -104,8 +104,9 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem;         // S accumulator: columns [0, 128)
-  const uint32_t tO = tmem + BN;    // O accumulator: columns [128, 128 + D)
+  const uint32_t tS = tmem;                 // S accumulator
+  const uint32_t tP = tmem + BN;            // P, bf16 A operand of P V
+  const uint32_t tO = tmem + BN + BN / 2;   // O accumulator
   const ptx::BoundedWait wait{abort_flag, &g_err};
   const bool ok = *abort_flag == 0;
 
@@ -137,12 +138,11 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
       const uint32_t sQ = ptx::smem_u32(sm + Lay::oQ);
       const uint32_t sK = ptx::smem_u32(sm + Lay::oK);
       const uint32_t sV = ptx::smem_u32(sm + Lay::oV);
-      const uint32_t sP = ptx::smem_u32(sm + Lay::oP);
       auto issue_pv = [&](int j) {
         const uint32_t v = sV + (j % NS) * Lay::kKV;
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k)
-          ptx::mma_ss(tO, kmajor_desc(sP, BM, k), mnmajor_desc(v, BN, k), idO, (j > 0 || k > 0) ? 1u : 0u);
+          ptx::mma_ts(tO, tP + k * 8, mnmajor_desc(v, BN, k), idO, (j > 0 || k > 0) ? 1u : 0u);
         ptx::mma_commit(&empty[j % NS]);
       };
       wait(q_full, 0);
@@ -171,7 +171,6 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
     const int r = threadIdx.x;                       // TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     const int64_t row = static_cast<int64_t>(rb) * BM + r;
-    uint8_t* P = sm + Lay::oP;
     float m = -INFINITY, l = 0.f;
     for (int j = 0; j < nkv; ++j) {
       wait(s_full, j & 1);
@@ -221,17 +220,10 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
           rs += p0 + p1;
           pk[t >> 1] = ptx::pack_bf16(p0, p1);
         }
-        // keys ch*32 .. ch*32+31 -> four 16-byte chunks of the swizzled K-major P tile
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int kk = ch * 32 + u * 8;
-          const int slab = kk >> 6, chunk = (kk & 63) >> 3;
-          uint4* dst = reinterpret_cast<uint4*>(P + slab * BM * 128 + r * 128 + ((chunk ^ (r & 7)) << 4));
-          *dst = make_uint4(pk[u * 4], pk[u * 4 + 1], pk[u * 4 + 2], pk[u * 4 + 3]);
-        }
+        ptx::tmem_st16(tP + lane_off + ch * 16, pk);  // keys ch*32 .. ch*32+31
       }
+      ptx::tmem_wait_st();
       l += rs;
-      ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
       ptx::mbar_arrive(p_ready);
     }
