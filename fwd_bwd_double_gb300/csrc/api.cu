@@ -154,7 +154,7 @@ attn_status_t attn_bwd(const attn_desc_t* desc, const void* Q, const void* K, co
   float4* ws = static_cast<float4*>(workspace);
   if (p.dtype == ATTN_F32) return launch_status(fbd::simt_bwd(p, Q, K, V, O, dO, lse, dQ, dK, dV, 0, ws, st));
   if (!tc_path(p, 1)) return fail(ATTN_ERR_UNSUPPORTED, "no bf16 backward kernel for this head dim%s");
-  return launch_status(fbd::simt_bwd(p, Q, K, V, O, dO, lse, dQ, dK, dV, gproj != 0, ws, st));
+  return launch_status(fbd::tc_bwd(p, Q, K, V, O, dO, lse, dQ, dK, dV, gproj != 0, ws, st));
 }
 
 attn_status_t attn_bob(const attn_desc_t* desc, const void* Q, const void* K, const void* V, const void* O,
@@ -204,7 +204,7 @@ attn_status_t attn_bwd_projected_dS(const attn_desc_t* desc, const void* Q, cons
 attn_status_t attn_device_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "CUDA: %s", cudaGetErrorString(e));
-  const uint32_t flags = fbd::tc_fwd_take_error();
+  const uint32_t flags = fbd::tc_fwd_take_error() | fbd::tc_bwd_take_error();
   if (flags != 0) return fail(ATTN_ERR_TIMEOUT, "a device-side bounded wait gave up%s");
   return ATTN_OK;
 }
@@ -260,6 +260,19 @@ bool make_tmap_bf16(void* map_out, const void* base, int64_t N, int64_t d, int64
   CUresult r = fn(static_cast<CUtensorMap*>(map_out), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
                   dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool make_tmap_stats(void* map_out, const void* base, int64_t N, int64_t BH, int box_rows) {
+  EncodeFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {4u, static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {16u, static_cast<cuuint64_t>(N) * 16u};
+  const cuuint32_t box[3] = {4u, static_cast<cuuint32_t>(box_rows), 1u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = fn(static_cast<CUtensorMap*>(map_out), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base),
+                  dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 

@@ -59,4 +59,8 @@ size_t static_bob_scratch_bytes();
 bool make_tmap_bf16(void* map_out /* CUtensorMap* */, const void* base, int64_t N, int64_t d, int64_t BH,
                     int box_rows);
 
+// Tensor map of the float4 row-statistics workspace [B*H, N]: 3-D fp32 view
+// (4, N, B*H), box (4, rows, 1), no swizzle; rows past N read as zero.
+bool make_tmap_stats(void* map_out, const void* base, int64_t N, int64_t BH, int box_rows);
+
 }  // namespace fbd

@@ -1,0 +1,522 @@
+// bf16 causal attention backward on sm_103a (tcgen05 + TMA), written once per
+// output block: a row pass for dQ and a column pass for dK, dV.
+//
+// "Flash attention for trading models", "Backward pass: recompute instead of
+// store": P is rebuilt from Q, K and the stored log-sum-exp; nothing N x N is
+// stored.  With dP = dO V^T, D_i = dO_i . O_i and dS = P * (dP - D):
+//   row pass    (CTA holds 128 query rows, streams 64-key blocks j <= i)
+//               S = Q K_j^T, dP = dO V_j^T           (A, B from shared memory)
+//               dQ += dS K_j                          (A = dS from TMEM, B = K_j MN-major)
+//               writes dQ = s dQ once and the row statistics (L log2 e, D, rho, 0)
+//   column pass (CTA holds 128 keys, streams 64-query blocks i >= j)
+//               S^T = K Q_i^T, dP^T = V dO_i^T        (transposed tiles: lanes = keys)
+//               dV += P^T dO_i, dK += dS^T Q_i        (A from TMEM, B MN-major)
+//               writes dK = s dK, dV once.
+// GProj ("FlashAttention bf16 gradient and GProj", "How the zero sum turns into a
+// false gradient"): the products see dS^ = bf16(dS) whose rows no longer sum to
+// zero.  The row pass accumulates r_i = sum_j dS^_ij and sum_j P^_ij of the bf16
+// values it feeds to the products, plus PK_i = P^ K; it writes
+//   dQ_i = s (dS^ K - rho_i PK_i),  rho_i = r_i / sum_j P^_ij,
+// i.e. the products of the projected row dS^_ij - rho_i P^_ij, which sums to zero.
+// The key correction needs rho_i of complete rows, hence the separate column pass:
+// it adds (-rho_i P^_ji) as a third A operand to the dK product.
+//
+// Roles: warps 0-7 compute (warp w owns TMEM lanes 32(w%4).., i.e. 32 rows, and
+// half of each tile's 64 columns); warp 8 issues TMA loads; warp 9 allocates TMEM
+// and issues the MMAs.  Score tiles are NB-buffered in TMEM so the MMAs of tile
+// t+1 run while the compute warps turn tile t into dS.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "tc_common.cuh"
+
+namespace fbd {
+namespace {
+
+__device__ unsigned int g_err = 0;
+
+constexpr int BM = 128;        // rows held by a CTA (queries, or keys in the column pass)
+constexpr int BN = 64;         // rows of a streamed block
+constexpr int NS = 3;          // shared-memory stages of streamed tiles
+constexpr int kCompute = 256;  // 8 compute warps
+constexpr int kThreads = kCompute + 64;
+constexpr float kLog2e = 1.4426950408889634f;
+
+using tc::bf16_hi;
+using tc::bf16_lo;
+using tc::f;
+
+// ================================================================ row pass
+template <int D, int NB, bool GP>
+struct RowLay {
+  static constexpr int kHeld = BM * D * 2;
+  static constexpr int kStream = BN * D * 2;
+  static constexpr int oQ = 0, odO = kHeld, oK = 2 * kHeld, oV = oK + NS * kStream;
+  static constexpr int oRed = oV + NS * kStream;  // float [6][BM]
+  static constexpr int oBar = oRed + 6 * BM * 4;
+  static constexpr int bytes = oBar + 256;
+  static constexpr int cS = 0, cdP = NB * BN, cdS = 2 * NB * BN, cP = cdS + NB * BN / 2;
+  static constexpr int cdQ = cP + (GP ? NB * BN / 2 : 0), cPK = cdQ + D;
+  static constexpr int cols = cPK + (GP ? D : 0);
+  static_assert(cols <= 512, "TMEM budget");
+};
+
+template <int D, int NB, bool GP>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_row_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
+                   const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                   const __nv_bfloat16* __restrict__ O, const __nv_bfloat16* __restrict__ dO,
+                   const float* __restrict__ lse, __nv_bfloat16* __restrict__ dQ, float4* __restrict__ ws, int N,
+                   int nrb, int BH, float scale, float c) {
+  using Lay = RowLay<D, NB, GP>;
+  extern __shared__ __align__(1024) uint8_t sm[];
+  uint64_t* q_full = reinterpret_cast<uint64_t*>(sm + Lay::oBar);
+  uint64_t* full = q_full + 1;
+  uint64_t* empty = full + NS;
+  uint64_t* s_full = empty + NS;
+  uint64_t* ds_ready = s_full + NB;
+  uint64_t* acc_full = ds_ready + NB;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* red = reinterpret_cast<float*>(sm + Lay::oRed);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = static_cast<int>(blockIdx.x % BH);
+  const int rb = nrb - 1 - static_cast<int>(blockIdx.x / BH);  // heaviest first
+  const int nkv = ((rb + 1) * BM + BN - 1) / BN;                 // key blocks touching rows <= last row
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(q_full, 1);
+    for (int s = 0; s < NS; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < NB; ++b) {
+      ptx::mbar_init(&s_full[b], 1);
+      ptx::mbar_init(&ds_ready[b], kCompute);
+    }
+    ptx::mbar_init(acc_full, 1);
+    *abort_flag = (ptx::smem_u32(sm) & 1023u) ? 1 : 0;
+    if (*abort_flag) atomicOr(&g_err, FBD_ERR_TIMEOUT);
+    ptx::fence_mbar_init();
+  }
+  if (warp == 9) {
+    ptx::tmem_alloc(tmem_slot, 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const ptx::BoundedWait wait{abort_flag, &g_err};
+  const bool ok = *abort_flag == 0;
+
+  if (warp == 8) {
+    // ---------------------------------------------------------------- TMA
+    if (lane == 0 && ok) {
+      ptx::prefetch_tmap(&tmK);
+      ptx::prefetch_tmap(&tmV);
+      ptx::mbar_expect_tx(q_full, 2 * Lay::kHeld);
+      for (int cc = 0; cc < D / 64; ++cc) {
+        ptx::tma_load_3d(sm + Lay::oQ + cc * BM * 128, &tmQ, q_full, cc * 64, rb * BM, bh);
+        ptx::tma_load_3d(sm + Lay::odO + cc * BM * 128, &tmdO, q_full, cc * 64, rb * BM, bh);
+      }
+      for (int j = 0; j < nkv; ++j) {
+        const int s = j % NS;
+        if (j >= NS) wait(&empty[s], ((j / NS) - 1) & 1);
+        ptx::mbar_expect_tx(&full[s], 2 * Lay::kStream);
+        for (int cc = 0; cc < D / 64; ++cc) {
+          ptx::tma_load_3d(sm + Lay::oK + s * Lay::kStream + cc * BN * 128, &tmK, &full[s], cc * 64, j * BN, bh);
+          ptx::tma_load_3d(sm + Lay::oV + s * Lay::kStream + cc * BN * 128, &tmV, &full[s], cc * 64, j * BN, bh);
+        }
+      }
+      for (int j = (nkv > NS ? nkv - NS : 0); j < nkv; ++j) wait(&empty[j % NS], (j / NS) & 1);
+    }
+  } else if (warp == 9) {
+    // ---------------------------------------------------------------- MMA
+    if (lane == 0 && ok) {
+      constexpr uint32_t idS = ptx::idesc_bf16(BM, BN, 0, 0);
+      constexpr uint32_t idQ = ptx::idesc_bf16(BM, D, 0, 1);
+      const uint32_t sQ = ptx::smem_u32(sm + Lay::oQ), sdO = ptx::smem_u32(sm + Lay::odO);
+      const uint32_t sK = ptx::smem_u32(sm + Lay::oK), sV = ptx::smem_u32(sm + Lay::oV);
+      auto products = [&](int t) {  // dQ (+ P^ K) of tile t, then release its stage
+        const int b = t % NB, s = t % NS;
+        wait(&ds_ready[b], (t / NB) & 1);
+        ptx::tc_fence_after();
+        const uint32_t kt = sK + s * Lay::kStream;
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k) {
+          const uint64_t bd = tc::mnmajor_desc(kt, BN, k);
+          ptx::mma_ts(tmem + Lay::cdQ, tmem + Lay::cdS + b * (BN / 2) + k * 8, bd, idQ, (t > 0 || k > 0));
+          if constexpr (GP)
+            ptx::mma_ts(tmem + Lay::cPK, tmem + Lay::cP + b * (BN / 2) + k * 8, bd, idQ, (t > 0 || k > 0));
+        }
+        ptx::mma_commit(&empty[s]);
+      };
+      wait(q_full, 0);
+      for (int j = 0; j < nkv; ++j) {
+        const int s = j % NS, b = j % NB;
+        wait(&full[s], (j / NS) & 1);
+        if (j >= NB) products(j - NB);  // frees score buffer b
+        ptx::tc_fence_after();
+        const uint32_t kt = sK + s * Lay::kStream, vt = sV + s * Lay::kStream;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          ptx::mma_ss(tmem + Lay::cS + b * BN, tc::kmajor_desc(sQ, BM, kk), tc::kmajor_desc(kt, BN, kk), idS, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          ptx::mma_ss(tmem + Lay::cdP + b * BN, tc::kmajor_desc(sdO, BM, kk), tc::kmajor_desc(vt, BN, kk), idS,
+                      kk > 0);
+        ptx::mma_commit(&s_full[b]);
+      }
+      for (int t = (nkv > NB ? nkv - NB : 0); t < nkv; ++t) products(t);
+      ptx::mma_commit(acc_full);
+    }
+  } else {
+    // ------------------------------------------------------------- compute
+    const int qd = warp & 3, hf = warp >> 2;
+    const int r = qd * 32 + lane;
+    const uint32_t lo = static_cast<uint32_t>(qd * 32) << 16;
+    const int64_t row = static_cast<int64_t>(rb) * BM + r;
+    const bool live = row < N;
+    const size_t rowoff = (static_cast<size_t>(bh) * N + row) * D;
+    float part = 0.f;
+    if (live) {  // this thread's half of D_r = dO_r . O_r
+      const uint4* po = reinterpret_cast<const uint4*>(O + rowoff + hf * (D / 2));
+      const uint4* pg = reinterpret_cast<const uint4*>(dO + rowoff + hf * (D / 2));
+#pragma unroll
+      for (int u = 0; u < D / 16; ++u) {
+        const uint4 a = po[u], g = pg[u];
+        const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) part += bf16_lo(aw[e]) * bf16_lo(gw[e]) + bf16_hi(aw[e]) * bf16_hi(gw[e]);
+      }
+    }
+    red[hf * BM + r] = part;
+    tc::named_sync(1, kCompute);
+    const float Dr = red[r] + red[BM + r];
+    const float L2 = live ? lse[static_cast<size_t>(bh) * N + row] * kLog2e : 0.f;
+    float racc = 0.f, sp = 0.f;
+    const int c0 = hf * (BN / 2);
+    for (int j = 0; j < nkv; ++j) {
+      const int b = j % NB;
+      wait(&s_full[b], (j / NB) & 1);
+      ptx::tc_fence_after();
+      uint32_t sv[32], pv[32];
+      ptx::tmem_ld32(tmem + Lay::cS + b * BN + c0 + lo, sv);
+      ptx::tmem_ld32(tmem + Lay::cdP + b * BN + c0 + lo, pv);
+      ptx::tmem_wait_ld();
+      const int krel = j * BN + c0 - rb * BM;  // key of my column 0 minus the block's first row
+      uint32_t dsk[16], pk[16];
+#pragma unroll
+      for (int t = 0; t < 32; t += 2) {
+        const float p0 = (krel + t > r) ? 0.f : ptx::ex2(fmaf(f(sv[t]), c, -L2));
+        const float p1 = (krel + t + 1 > r) ? 0.f : ptx::ex2(fmaf(f(sv[t + 1]), c, -L2));
+        dsk[t >> 1] = ptx::pack_bf16(p0 * (f(pv[t]) - Dr), p1 * (f(pv[t + 1]) - Dr));
+        if constexpr (GP) {
+          pk[t >> 1] = ptx::pack_bf16(p0, p1);
+          racc += bf16_lo(dsk[t >> 1]) + bf16_hi(dsk[t >> 1]);
+          sp += bf16_lo(pk[t >> 1]) + bf16_hi(pk[t >> 1]);
+        }
+      }
+      ptx::tmem_st16(tmem + Lay::cdS + b * (BN / 2) + c0 / 2 + lo, dsk);
+      if constexpr (GP) ptx::tmem_st16(tmem + Lay::cP + b * (BN / 2) + c0 / 2 + lo, pk);
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&ds_ready[b]);
+    }
+    float rho = 0.f;
+    if constexpr (GP) {
+      red[2 * BM + hf * BM + r] = racc;
+      red[4 * BM + hf * BM + r] = sp;
+      tc::named_sync(1, kCompute);
+      rho = (red[2 * BM + r] + red[3 * BM + r]) / (red[4 * BM + r] + red[5 * BM + r]);
+    }
+    wait(acc_full, 0);
+    ptx::tc_fence_after();
+#pragma unroll
+    for (int cc = 0; cc < D / 2; cc += 32) {
+      uint32_t a[32], pkv[32];
+      ptx::tmem_ld32(tmem + Lay::cdQ + hf * (D / 2) + cc + lo, a);
+      if constexpr (GP) ptx::tmem_ld32(tmem + Lay::cPK + hf * (D / 2) + cc + lo, pkv);
+      ptx::tmem_wait_ld();
+      if (live) {
+        uint32_t o[16];
+#pragma unroll
+        for (int t = 0; t < 32; t += 2) {
+          float v0 = f(a[t]), v1 = f(a[t + 1]);
+          if constexpr (GP) {
+            v0 -= rho * f(pkv[t]);
+            v1 -= rho * f(pkv[t + 1]);
+          }
+          o[t >> 1] = ptx::pack_bf16(scale * v0, scale * v1);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(dQ + rowoff + hf * (D / 2) + cc);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) dst[u] = make_uint4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
+      }
+    }
+    if (live && hf == 0) ws[static_cast<size_t>(bh) * N + row] = make_float4(L2, Dr, rho, 0.f);
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+// ============================================================= column pass
+template <int D, int NB, bool GP>
+struct ColLay {
+  static constexpr int kHeld = BM * D * 2;
+  static constexpr int kStream = BN * D * 2;
+  static constexpr int kStat = BN * 16;
+  static constexpr int oK = 0, oV = kHeld, oQ = 2 * kHeld, odO = oQ + NS * kStream, oSt = odO + NS * kStream;
+  static constexpr int oBar = oSt + NS * kStat;
+  static constexpr int bytes = oBar + 256;
+  static constexpr int cS = 0, cdP = NB * BN, cP = 2 * NB * BN, cdS = cP + NB * BN / 2, cG = cdS + NB * BN / 2;
+  static constexpr int cdV = cG + (GP ? NB * BN / 2 : 0), cdK = cdV + D;
+  static constexpr int cols = cdK + D;
+  static_assert(cols <= 512, "TMEM budget");
+};
+
+template <int D, int NB, bool GP>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_col_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                   const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
+                   const __grid_constant__ CUtensorMap tmSt, __nv_bfloat16* __restrict__ dK,
+                   __nv_bfloat16* __restrict__ dV, int N, int BH, float scale, float c) {
+  using Lay = ColLay<D, NB, GP>;
+  extern __shared__ __align__(1024) uint8_t sm[];
+  uint64_t* k_full = reinterpret_cast<uint64_t*>(sm + Lay::oBar);
+  uint64_t* full = k_full + 1;
+  uint64_t* empty = full + NS;
+  uint64_t* s_full = empty + NS;
+  uint64_t* ds_ready = s_full + NB;
+  uint64_t* acc_full = ds_ready + NB;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = static_cast<int>(blockIdx.x % BH);
+  const int kb = static_cast<int>(blockIdx.x / BH);  // first key blocks have the most rows: first
+  const int nq = (N + BN - 1) / BN;
+  const int i0 = (kb * BM) / BN;                      // first query block with a query >= first key
+  const int ntile = nq - i0;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(k_full, 1);
+    for (int s = 0; s < NS; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < NB; ++b) {
+      ptx::mbar_init(&s_full[b], 1);
+      ptx::mbar_init(&ds_ready[b], kCompute);
+    }
+    ptx::mbar_init(acc_full, 1);
+    *abort_flag = (ptx::smem_u32(sm) & 1023u) ? 1 : 0;
+    if (*abort_flag) atomicOr(&g_err, FBD_ERR_TIMEOUT);
+    ptx::fence_mbar_init();
+  }
+  if (warp == 9) {
+    ptx::tmem_alloc(tmem_slot, 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const ptx::BoundedWait wait{abort_flag, &g_err};
+  const bool ok = *abort_flag == 0;
+
+  if (warp == 8) {
+    if (lane == 0 && ok) {
+      ptx::prefetch_tmap(&tmQ);
+      ptx::prefetch_tmap(&tmdO);
+      ptx::prefetch_tmap(&tmSt);
+      ptx::mbar_expect_tx(k_full, 2 * Lay::kHeld);
+      for (int cc = 0; cc < D / 64; ++cc) {
+        ptx::tma_load_3d(sm + Lay::oK + cc * BM * 128, &tmK, k_full, cc * 64, kb * BM, bh);
+        ptx::tma_load_3d(sm + Lay::oV + cc * BM * 128, &tmV, k_full, cc * 64, kb * BM, bh);
+      }
+      for (int t = 0; t < ntile; ++t) {
+        const int s = t % NS, i = i0 + t;
+        if (t >= NS) wait(&empty[s], ((t / NS) - 1) & 1);
+        ptx::mbar_expect_tx(&full[s], 2 * Lay::kStream + Lay::kStat);
+        for (int cc = 0; cc < D / 64; ++cc) {
+          ptx::tma_load_3d(sm + Lay::oQ + s * Lay::kStream + cc * BN * 128, &tmQ, &full[s], cc * 64, i * BN, bh);
+          ptx::tma_load_3d(sm + Lay::odO + s * Lay::kStream + cc * BN * 128, &tmdO, &full[s], cc * 64, i * BN, bh);
+        }
+        ptx::tma_load_3d(sm + Lay::oSt + s * Lay::kStat, &tmSt, &full[s], 0, i * BN, bh);
+      }
+      for (int t = (ntile > NS ? ntile - NS : 0); t < ntile; ++t) wait(&empty[t % NS], (t / NS) & 1);
+    }
+  } else if (warp == 9) {
+    if (lane == 0 && ok) {
+      constexpr uint32_t idS = ptx::idesc_bf16(BM, BN, 0, 0);
+      constexpr uint32_t idKV = ptx::idesc_bf16(BM, D, 0, 1);
+      const uint32_t sK = ptx::smem_u32(sm + Lay::oK), sV = ptx::smem_u32(sm + Lay::oV);
+      const uint32_t sQ = ptx::smem_u32(sm + Lay::oQ), sdO = ptx::smem_u32(sm + Lay::odO);
+      auto products = [&](int t) {
+        const int b = t % NB, s = t % NS;
+        wait(&ds_ready[b], (t / NB) & 1);
+        ptx::tc_fence_after();
+        const uint32_t qt = sQ + s * Lay::kStream, gt = sdO + s * Lay::kStream;
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k) {
+          ptx::mma_ts(tmem + Lay::cdV, tmem + Lay::cP + b * (BN / 2) + k * 8, tc::mnmajor_desc(gt, BN, k), idKV,
+                      (t > 0 || k > 0));
+          const uint64_t bq = tc::mnmajor_desc(qt, BN, k);
+          ptx::mma_ts(tmem + Lay::cdK, tmem + Lay::cdS + b * (BN / 2) + k * 8, bq, idKV, (t > 0 || k > 0));
+          if constexpr (GP) ptx::mma_ts(tmem + Lay::cdK, tmem + Lay::cG + b * (BN / 2) + k * 8, bq, idKV, 1u);
+        }
+        ptx::mma_commit(&empty[s]);
+      };
+      wait(k_full, 0);
+      for (int t = 0; t < ntile; ++t) {
+        const int s = t % NS, b = t % NB;
+        wait(&full[s], (t / NS) & 1);
+        if (t >= NB) products(t - NB);
+        ptx::tc_fence_after();
+        const uint32_t qt = sQ + s * Lay::kStream, gt = sdO + s * Lay::kStream;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          ptx::mma_ss(tmem + Lay::cS + b * BN, tc::kmajor_desc(sK, BM, kk), tc::kmajor_desc(qt, BN, kk), idS, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          ptx::mma_ss(tmem + Lay::cdP + b * BN, tc::kmajor_desc(sV, BM, kk), tc::kmajor_desc(gt, BN, kk), idS,
+                      kk > 0);
+        ptx::mma_commit(&s_full[b]);
+      }
+      for (int t = (ntile > NB ? ntile - NB : 0); t < ntile; ++t) products(t);
+      ptx::mma_commit(acc_full);
+    }
+  } else {
+    const int qd = warp & 3, hf = warp >> 2;
+    const int r = qd * 32 + lane;  // key row within the block (TMEM lane)
+    const uint32_t lo = static_cast<uint32_t>(qd * 32) << 16;
+    const int key = kb * BM + r;
+    const int c0 = hf * (BN / 2);
+    for (int t = 0; t < ntile; ++t) {
+      const int s = t % NS, b = t % NB, i = i0 + t;
+      wait(&s_full[b], (t / NB) & 1);
+      ptx::tc_fence_after();
+      uint32_t sv[32], pv[32];
+      ptx::tmem_ld32(tmem + Lay::cS + b * BN + c0 + lo, sv);
+      ptx::tmem_ld32(tmem + Lay::cdP + b * BN + c0 + lo, pv);
+      ptx::tmem_wait_ld();
+      const float4* st = reinterpret_cast<const float4*>(sm + Lay::oSt + s * Lay::kStat) + c0;
+      const int qbase = i * BN + c0;
+      uint32_t pk[16], dk[16], gk[16];
+#pragma unroll
+      for (int u = 0; u < 32; u += 2) {
+        const float4 a0 = st[u], a1 = st[u + 1];  // (L log2 e, D, rho, 0) of queries qbase+u, +u+1
+        const bool m0 = (qbase + u < key) || (qbase + u >= N);
+        const bool m1 = (qbase + u + 1 < key) || (qbase + u + 1 >= N);
+        const float p0 = m0 ? 0.f : ptx::ex2(fmaf(f(sv[u]), c, -a0.x));
+        const float p1 = m1 ? 0.f : ptx::ex2(fmaf(f(sv[u + 1]), c, -a1.x));
+        pk[u >> 1] = ptx::pack_bf16(p0, p1);
+        dk[u >> 1] = ptx::pack_bf16(p0 * (f(pv[u]) - a0.y), p1 * (f(pv[u + 1]) - a1.y));
+        if constexpr (GP) gk[u >> 1] = ptx::pack_bf16(-a0.z * bf16_lo(pk[u >> 1]), -a1.z * bf16_hi(pk[u >> 1]));
+      }
+      ptx::tmem_st16(tmem + Lay::cP + b * (BN / 2) + c0 / 2 + lo, pk);
+      ptx::tmem_st16(tmem + Lay::cdS + b * (BN / 2) + c0 / 2 + lo, dk);
+      if constexpr (GP) ptx::tmem_st16(tmem + Lay::cG + b * (BN / 2) + c0 / 2 + lo, gk);
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&ds_ready[b]);
+    }
+    wait(acc_full, 0);
+    ptx::tc_fence_after();
+    const bool live = key < N;
+    const size_t rowoff = (static_cast<size_t>(bh) * N + key) * D;
+#pragma unroll
+    for (int cc = 0; cc < D / 2; cc += 32) {
+      uint32_t a[32], g[32];
+      ptx::tmem_ld32(tmem + Lay::cdV + hf * (D / 2) + cc + lo, a);
+      ptx::tmem_ld32(tmem + Lay::cdK + hf * (D / 2) + cc + lo, g);
+      ptx::tmem_wait_ld();
+      if (live) {
+        uint32_t ov[16], ok2[16];
+#pragma unroll
+        for (int u = 0; u < 32; u += 2) {
+          ov[u >> 1] = ptx::pack_bf16(f(a[u]), f(a[u + 1]));
+          ok2[u >> 1] = ptx::pack_bf16(scale * f(g[u]), scale * f(g[u + 1]));
+        }
+        uint4* dv = reinterpret_cast<uint4*>(dV + rowoff + hf * (D / 2) + cc);
+        uint4* dk2 = reinterpret_cast<uint4*>(dK + rowoff + hf * (D / 2) + cc);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          dv[u] = make_uint4(ov[4 * u], ov[4 * u + 1], ov[4 * u + 2], ov[4 * u + 3]);
+          dk2[u] = make_uint4(ok2[4 * u], ok2[4 * u + 1], ok2[4 * u + 2], ok2[4 * u + 3]);
+        }
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, int NBR, int NBC, bool GP>
+cudaError_t launch(const Problem& p, const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                   const float* lse, void* dQ, void* dK, void* dV, float4* ws, cudaStream_t st) {
+  alignas(64) CUtensorMap q128, do128, k64, v64, k128, v128, q64, do64, s64;
+  const int64_t N = p.N, BH = p.BH;
+  if (!make_tmap_bf16(&q128, Q, N, D, BH, BM) || !make_tmap_bf16(&do128, dO, N, D, BH, BM) ||
+      !make_tmap_bf16(&k64, K, N, D, BH, BN) || !make_tmap_bf16(&v64, V, N, D, BH, BN) ||
+      !make_tmap_bf16(&k128, K, N, D, BH, BM) || !make_tmap_bf16(&v128, V, N, D, BH, BM) ||
+      !make_tmap_bf16(&q64, Q, N, D, BH, BN) || !make_tmap_bf16(&do64, dO, N, D, BH, BN) ||
+      !make_tmap_stats(&s64, ws, N, BH, BN))
+    return cudaErrorInvalidValue;
+  const float c = p.scale * kLog2e;
+  const int nrb = static_cast<int>((N + BM - 1) / BM);
+  {
+    using Lay = RowLay<D, NBR, GP>;
+    auto kern = bwd_row_kernel<D, NBR, GP>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::bytes);
+    if (e != cudaSuccess) return e;
+    kern<<<static_cast<unsigned>(nrb * BH), kThreads, Lay::bytes, st>>>(
+        q128, do128, k64, v64, static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), lse,
+        static_cast<__nv_bfloat16*>(dQ), ws, static_cast<int>(N), nrb, static_cast<int>(BH), p.scale, c);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  {
+    using Lay = ColLay<D, NBC, GP>;
+    auto kern = bwd_col_kernel<D, NBC, GP>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::bytes);
+    if (e != cudaSuccess) return e;
+    kern<<<static_cast<unsigned>(nrb * BH), kThreads, Lay::bytes, st>>>(
+        k128, v128, q64, do64, s64, static_cast<__nv_bfloat16*>(dK), static_cast<__nv_bfloat16*>(dV),
+        static_cast<int>(N), static_cast<int>(BH), p.scale, c);
+    return cudaGetLastError();
+  }
+}
+
+}  // namespace
+
+cudaError_t tc_bwd(const Problem& p, const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                   const float* lse, void* dQ, void* dK, void* dV, int gproj, float4* ws, cudaStream_t st) {
+  if (p.d == 64)
+    return gproj ? launch<64, 2, 1, true>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, st)
+                 : launch<64, 2, 2, false>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, st);
+  return gproj ? launch<128, 1, 1, true>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, st)
+               : launch<128, 2, 1, false>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, st);
+}
+
+uint32_t tc_bwd_take_error() {
+  uint32_t v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, g_err, sizeof(v)) != cudaSuccess) return 0;
+  if (v) cudaMemcpyToSymbol(g_err, &z, sizeof(z));
+  return v;
+}
+
+}  // namespace fbd

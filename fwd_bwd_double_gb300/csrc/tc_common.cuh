@@ -1,0 +1,37 @@
+// Helpers shared by the tcgen05 kernels: operand descriptors for TMA-written
+// 128-byte-swizzled tiles, named barriers, bf16 packing.
+#pragma once
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace fbd {
+namespace tc {
+
+// A tile of `rows` rows x D bf16 columns is stored as D/64 slabs; slab c holds
+// columns [64c, 64c + 64) as `rows` lines of 128 bytes, 128-byte swizzled (the
+// layout a TMA box of (64, rows) writes).  The tile base is 1024-byte aligned.
+
+// K-major operand (rows = M or N index, columns = K), advanced to K-step k (16 columns).
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int rows, int k) {
+  return ptx::sdesc_sw128(base + (k >> 2) * rows * 128 + (k & 3) * 32, 16, 1024);
+}
+// MN-major operand (rows = K index, columns = M or N), advanced to K-step k (16 rows).
+// Leading byte offset = slab stride (next 64 columns), stride byte offset = 8 rows.
+__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int rows, int k) {
+  return ptx::sdesc_sw128(base + k * 16 * 128, rows * 128, 1024);
+}
+
+// Barrier among the first `n` threads (the compute warps), id 1 (id 0 is __syncthreads).
+__device__ __forceinline__ void named_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// The two floats held by a packed bf16x2 word (low half = even element).
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ float f(uint32_t u) { return __uint_as_float(u); }
+
+}  // namespace tc
+}  // namespace fbd
