@@ -181,7 +181,7 @@ attn_status_t attn_bob(const attn_desc_t* desc, const void* Q, const void* K, co
   float4* ws = static_cast<float4*>(workspace);
   if (p.dtype == ATTN_F32)
     return launch_status(fbd::simt_bob(p, Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ, gK, gV, gdO, ws, st));
-  return launch_status(fbd::simt_bob(p, Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ, gK, gV, gdO, ws, st));
+  return launch_status(fbd::tc_bob(p, Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ, gK, gV, gdO, ws, st));
 }
 
 attn_status_t attn_bwd_projected_dS(const attn_desc_t* desc, const void* Q, const void* K, const void* V,
@@ -204,7 +204,7 @@ attn_status_t attn_bwd_projected_dS(const attn_desc_t* desc, const void* Q, cons
 attn_status_t attn_device_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "CUDA: %s", cudaGetErrorString(e));
-  const uint32_t flags = fbd::tc_fwd_take_error() | fbd::tc_bwd_take_error();
+  const uint32_t flags = fbd::tc_fwd_take_error() | fbd::tc_bwd_take_error() | fbd::tc_bob_take_error();
   if (flags != 0) return fail(ATTN_ERR_TIMEOUT, "a device-side bounded wait gave up%s");
   return ATTN_OK;
 }

@@ -1,0 +1,574 @@
+// bf16 backward-over-backward (FlashBoB) on sm_103a, d = 64: a row pass and a
+// column pass, every output block written once, nothing N x N in HBM.
+//
+// "FlashBoB: second-order attention", "Two scalar states replace quadratic
+// tensors".  With a = gdQ, b = gdK, c = gdV, G = s(a K^T + Q b^T), H = dO c^T,
+// dS = P * (dP - D), W = G * dS + P * H, the two per-row scalar states are
+//   E_i = sum_j P_ij G_ij   and   F_i = F'_i - E_i D_i,  F'_i = sum_j W_ij.
+// Row pass (CTA holds 128 query rows; 64-key blocks j <= i stream past):
+//   tiles   [S | Q b^T] = Q [K_j; b_j]^T,  G += a K_j^T,  [dP | H] = dO [V_j; c_j]^T
+//   outputs X += P c_j + (P G) V_j,  Y += dS b_j + W K_j,  Z += dS K_j,  U += P K_j
+//   end     gdO = X - E O,  gQ = s (Y - E Z - F' U); row states (L log2 e, D, E, F)
+// (the corrections after the finished row are linear in E and F', so they are
+// applied once per row: "partial sums accumulated early, corrected after").
+// Column pass (CTA holds 128 keys; 64-query blocks i >= j stream past, with the
+// row states re-read): transposed tiles, lanes = keys,
+//   tiles   [S^T | K a^T] = K [Q_i; a_i]^T,  G^T += b Q_i^T,  dP^T = V dO_i^T,
+//           H^T = c dO_i^T
+//   dPbar = P (G - E),  Sbar = P (G (dP - D) - E dP + H - F)
+//   outputs gV += dPbar^T dO_i,  gK += dS^T a_i + Sbar^T Q_i;  end gK *= s.
+// All tile products take A and B from 128-byte-swizzled shared memory (TMA);
+// all output products take the bf16 tile (P, P G, dS, W, dPbar, Sbar) from TMEM
+// as the A operand and the streamed block, MN-major, as B.
+//
+// Rounding: the output products see bf16 copies P^, (PG)^, dS^, W^ of the tiles.
+// The corrections use scalars taken from those same copies,
+//   E_i = sum_j (PG)^_ij,  F'_i = (sum_j W^_ij - E_i sum_j dS^_ij) / sum_j P^_ij,
+// so that the row of Sbar the products effectively see, W^ - E dS^ - F' P^, sums
+// to exactly zero (as the exact Sbar does).  In exact arithmetic these are the
+// definitions above (sum dS = 0, sum P = 1); in bf16 they keep the rounding of W
+// from being multiplied by the mean key, the same mechanism GProj removes from dQ
+// ("FlashAttention bf16 gradient and GProj", "How the zero sum turns into a false
+// gradient").  The stored state F_i = sum_j W_ij - E_i D_i uses the fp32 sums.
+//
+// Row-pass TMEM: [S | G] 128 columns, [dP | H] 128, X, Y, Z, U 64 each = 512.
+// The bf16 operands are written over the fp32 tile columns their own thread has
+// read, so the next block's tile MMAs wait until this block's output MMAs
+// complete (explicit commit + wait: MMAs with different accumulators carry no
+// ordering guarantee).  Column-pass TMEM: tiles 256, operands 96, gV, gK 128.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "tc_common.cuh"
+
+namespace fbd {
+namespace {
+
+__device__ unsigned int g_err = 0;
+
+constexpr int D = 64;
+constexpr int BM = 128;
+constexpr int BN = 64;
+constexpr int NS = 3;
+constexpr int kCompute = 256;
+constexpr int kThreads = kCompute + 64;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kTile = BN * D * 2;  // 8 KB: one streamed 64-row tile
+constexpr int kHeld = BM * D * 2;  // 16 KB: one held 128-row tile
+
+using tc::bf16_hi;
+using tc::bf16_lo;
+using tc::f;
+
+// TMEM column of the bf16 operand for K-step k (16 keys) when a thread half hf
+// stores its 32 keys as [first operand: 16 columns | second operand: 16 columns]
+// inside its own 32 fp32 columns: keys 32 hf .. 32 hf + 31 -> columns 32 hf ...
+__device__ __forceinline__ uint32_t op_col(int k, int second) {
+  return static_cast<uint32_t>(32 * (k >> 1) + 8 * (k & 1) + 16 * second);
+}
+
+// ================================================================ row pass
+struct RowLay {
+  static constexpr int oQ = 0, odO = kHeld, oA = 2 * kHeld, oStage = 3 * kHeld;
+  static constexpr int kStage = 4 * kTile;  // [K_j; b_j] then [V_j; c_j]
+  static constexpr int oRed = oStage + NS * kStage;
+  static constexpr int oBar = oRed + 12 * BM * 4;
+  static constexpr int bytes = oBar + 256;
+  static constexpr int cSG = 0, cPH = 128, cX = 256, cY = 320, cZ = 384, cU = 448;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    bob_row_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
+                   const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, const __nv_bfloat16* __restrict__ O,
+                   const __nv_bfloat16* __restrict__ dO, const float* __restrict__ lse,
+                   __nv_bfloat16* __restrict__ gQ, __nv_bfloat16* __restrict__ gdO, float4* __restrict__ ws, int N,
+                   int nrb, int BH, float scale, float c) {
+  using Lay = RowLay;
+  extern __shared__ __align__(1024) uint8_t sm[];
+  uint64_t* q_full = reinterpret_cast<uint64_t*>(sm + Lay::oBar);
+  uint64_t* full = q_full + 1;
+  uint64_t* empty = full + NS;
+  uint64_t* s_full = empty + NS;
+  uint64_t* ready = s_full + 1;
+  uint64_t* out_done = ready + 1;
+  uint64_t* acc_full = out_done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* red = reinterpret_cast<float*>(sm + Lay::oRed);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = static_cast<int>(blockIdx.x % BH);
+  const int rb = nrb - 1 - static_cast<int>(blockIdx.x / BH);
+  const int nkv = ((rb + 1) * BM + BN - 1) / BN;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(q_full, 1);
+    for (int s = 0; s < NS; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    ptx::mbar_init(s_full, 1);
+    ptx::mbar_init(ready, kCompute);
+    ptx::mbar_init(out_done, 1);
+    ptx::mbar_init(acc_full, 1);
+    *abort_flag = (ptx::smem_u32(sm) & 1023u) ? 1 : 0;
+    if (*abort_flag) atomicOr(&g_err, FBD_ERR_TIMEOUT);
+    ptx::fence_mbar_init();
+  }
+  if (warp == 9) {
+    ptx::tmem_alloc(tmem_slot, 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const ptx::BoundedWait wait{abort_flag, &g_err};
+  const bool ok = *abort_flag == 0;
+
+  if (warp == 8) {
+    if (lane == 0 && ok) {
+      ptx::prefetch_tmap(&tmK);
+      ptx::prefetch_tmap(&tmV);
+      ptx::prefetch_tmap(&tmB);
+      ptx::prefetch_tmap(&tmC);
+      ptx::mbar_expect_tx(q_full, 3 * kHeld);
+      ptx::tma_load_3d(sm + Lay::oQ, &tmQ, q_full, 0, rb * BM, bh);
+      ptx::tma_load_3d(sm + Lay::odO, &tmdO, q_full, 0, rb * BM, bh);
+      ptx::tma_load_3d(sm + Lay::oA, &tmA, q_full, 0, rb * BM, bh);
+      for (int j = 0; j < nkv; ++j) {
+        const int s = j % NS;
+        if (j >= NS) wait(&empty[s], ((j / NS) - 1) & 1);
+        uint8_t* st = sm + Lay::oStage + s * Lay::kStage;
+        ptx::mbar_expect_tx(&full[s], 4 * kTile);
+        ptx::tma_load_3d(st, &tmK, &full[s], 0, j * BN, bh);
+        ptx::tma_load_3d(st + kTile, &tmB, &full[s], 0, j * BN, bh);
+        ptx::tma_load_3d(st + 2 * kTile, &tmV, &full[s], 0, j * BN, bh);
+        ptx::tma_load_3d(st + 3 * kTile, &tmC, &full[s], 0, j * BN, bh);
+      }
+      for (int j = (nkv > NS ? nkv - NS : 0); j < nkv; ++j) wait(&empty[j % NS], (j / NS) & 1);
+    }
+  } else if (warp == 9) {
+    if (lane == 0 && ok) {
+      constexpr uint32_t id128 = ptx::idesc_bf16(BM, 2 * BN, 0, 0);
+      constexpr uint32_t id64 = ptx::idesc_bf16(BM, BN, 0, 0);
+      constexpr uint32_t idO = ptx::idesc_bf16(BM, D, 0, 1);
+      const uint32_t sQ = ptx::smem_u32(sm + Lay::oQ), sdO = ptx::smem_u32(sm + Lay::odO);
+      const uint32_t sA = ptx::smem_u32(sm + Lay::oA), sSt = ptx::smem_u32(sm + Lay::oStage);
+      wait(q_full, 0);
+      for (int j = 0; j < nkv; ++j) {
+        const int s = j % NS;
+        const uint32_t kb = sSt + s * Lay::kStage;  // [K_j; b_j]
+        const uint32_t vc = kb + 2 * kTile;          // [V_j; c_j]
+        wait(&full[s], (j / NS) & 1);
+        if (j > 0) wait(out_done, (j - 1) & 1);  // block j-1's products have read the tile columns
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          ptx::mma_ss(tmem + Lay::cSG, tc::kmajor_desc(sQ, BM, kk), tc::kmajor_desc(kb, 2 * BN, kk), id128, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          ptx::mma_ss(tmem + Lay::cSG + BN, tc::kmajor_desc(sA, BM, kk), tc::kmajor_desc(kb, BN, kk), id64, 1u);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          ptx::mma_ss(tmem + Lay::cPH, tc::kmajor_desc(sdO, BM, kk), tc::kmajor_desc(vc, 2 * BN, kk), id128, kk > 0);
+        ptx::mma_commit(s_full);
+        wait(ready, j & 1);
+        ptx::tc_fence_after();
+        const uint32_t kt = kb, bt = kb + kTile, vt = vc, ct = vc + kTile;
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k) {
+          const uint32_t acc = (j > 0 || k > 0) ? 1u : 0u;
+          const uint32_t aP = tmem + Lay::cSG + op_col(k, 0), aPG = tmem + Lay::cSG + op_col(k, 1);
+          const uint32_t adS = tmem + Lay::cPH + op_col(k, 0), aW = tmem + Lay::cPH + op_col(k, 1);
+          const uint64_t dK = tc::mnmajor_desc(kt, BN, k), dB = tc::mnmajor_desc(bt, BN, k);
+          const uint64_t dV = tc::mnmajor_desc(vt, BN, k), dC = tc::mnmajor_desc(ct, BN, k);
+          ptx::mma_ts(tmem + Lay::cX, aP, dC, idO, acc);
+          ptx::mma_ts(tmem + Lay::cX, aPG, dV, idO, 1u);
+          ptx::mma_ts(tmem + Lay::cY, adS, dB, idO, acc);
+          ptx::mma_ts(tmem + Lay::cY, aW, dK, idO, 1u);
+          ptx::mma_ts(tmem + Lay::cZ, adS, dK, idO, acc);
+          ptx::mma_ts(tmem + Lay::cU, aP, dK, idO, acc);
+        }
+        ptx::mma_commit(&empty[s]);
+        ptx::mma_commit(out_done);
+      }
+      ptx::mma_commit(acc_full);
+    }
+  } else {
+    const int qd = warp & 3, hf = warp >> 2;
+    const int r = qd * 32 + lane;
+    const uint32_t lo = static_cast<uint32_t>(qd * 32) << 16;
+    const int64_t row = static_cast<int64_t>(rb) * BM + r;
+    const bool live = row < N;
+    const size_t rowoff = (static_cast<size_t>(bh) * N + row) * D;
+    float part = 0.f;
+    uint4 oh[4];  // this thread's half of the O row (32 bf16), reused in the epilogue
+#pragma unroll
+    for (int u = 0; u < 4; ++u) oh[u] = make_uint4(0, 0, 0, 0);
+    if (live) {
+      const uint4* po = reinterpret_cast<const uint4*>(O + rowoff + hf * 32);
+      const uint4* pg = reinterpret_cast<const uint4*>(dO + rowoff + hf * 32);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        oh[u] = po[u];
+        const uint4 g = pg[u];
+        const uint32_t aw[4] = {oh[u].x, oh[u].y, oh[u].z, oh[u].w}, gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) part += bf16_lo(aw[e]) * bf16_lo(gw[e]) + bf16_hi(aw[e]) * bf16_hi(gw[e]);
+      }
+    }
+    red[hf * BM + r] = part;
+    tc::named_sync(1, kCompute);
+    const float Dr = red[r] + red[BM + r];
+    const float L2 = live ? lse[static_cast<size_t>(bh) * N + row] * kLog2e : 0.f;
+    float E = 0.f, Fp = 0.f, sW = 0.f, sdS = 0.f, sP = 0.f;
+    const int c0 = hf * 32;
+    for (int j = 0; j < nkv; ++j) {
+      wait(s_full, j & 1);
+      ptx::tc_fence_after();
+      const int krel = j * BN + c0 - rb * BM;
+      uint32_t pP[16], pG[16], pS[16], pW[16];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {  // two sub-chunks of 16 keys
+        uint32_t sv[16], gv[16], dv[16], hv[16];
+        ptx::tmem_ld16(tmem + Lay::cSG + c0 + 16 * h + lo, sv);
+        ptx::tmem_ld16(tmem + Lay::cSG + BN + c0 + 16 * h + lo, gv);
+        ptx::tmem_ld16(tmem + Lay::cPH + c0 + 16 * h + lo, dv);
+        ptx::tmem_ld16(tmem + Lay::cPH + BN + c0 + 16 * h + lo, hv);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int t = 0; t < 16; t += 2) {
+          float p[2], pg[2], ds[2], w[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int tt = t + e;
+            p[e] = (krel + 16 * h + tt > r) ? 0.f : ptx::ex2(fmaf(f(sv[tt]), c, -L2));
+            const float G = scale * f(gv[tt]);
+            ds[e] = p[e] * (f(dv[tt]) - Dr);
+            pg[e] = p[e] * G;
+            w[e] = fmaf(G, ds[e], p[e] * f(hv[tt]));
+            Fp += w[e];
+          }
+          const int idx = 8 * h + (t >> 1);
+          pP[idx] = ptx::pack_bf16(p[0], p[1]);
+          pG[idx] = ptx::pack_bf16(pg[0], pg[1]);
+          pS[idx] = ptx::pack_bf16(ds[0], ds[1]);
+          pW[idx] = ptx::pack_bf16(w[0], w[1]);
+          E += bf16_lo(pG[idx]) + bf16_hi(pG[idx]);
+          sW += bf16_lo(pW[idx]) + bf16_hi(pW[idx]);
+          sdS += bf16_lo(pS[idx]) + bf16_hi(pS[idx]);
+          sP += bf16_lo(pP[idx]) + bf16_hi(pP[idx]);
+        }
+      }
+      // Over this thread's own (already read) fp32 columns: [P | P G] and [dS | W].
+      ptx::tmem_st16(tmem + Lay::cSG + c0 + lo, pP);
+      ptx::tmem_st16(tmem + Lay::cSG + c0 + 16 + lo, pG);
+      ptx::tmem_st16(tmem + Lay::cPH + c0 + lo, pS);
+      ptx::tmem_st16(tmem + Lay::cPH + c0 + 16 + lo, pW);
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(ready);
+    }
+    red[2 * BM + hf * BM + r] = E;
+    red[4 * BM + hf * BM + r] = Fp;
+    red[6 * BM + hf * BM + r] = sW;
+    red[8 * BM + hf * BM + r] = sdS;
+    red[10 * BM + hf * BM + r] = sP;
+    tc::named_sync(1, kCompute);
+    E = red[2 * BM + r] + red[3 * BM + r];
+    Fp = red[4 * BM + r] + red[5 * BM + r];
+    sW = red[6 * BM + r] + red[7 * BM + r];
+    sdS = red[8 * BM + r] + red[9 * BM + r];
+    sP = red[10 * BM + r] + red[11 * BM + r];
+    const float Fq = (sW - E * sdS) / sP;  // F' as seen through the bf16 operands
+    wait(acc_full, 0);
+    ptx::tc_fence_after();
+    uint32_t xv[32], yv[32], zv[32], uv[32];
+    ptx::tmem_ld32(tmem + Lay::cX + c0 + lo, xv);
+    ptx::tmem_ld32(tmem + Lay::cY + c0 + lo, yv);
+    ptx::tmem_ld32(tmem + Lay::cZ + c0 + lo, zv);
+    ptx::tmem_ld32(tmem + Lay::cU + c0 + lo, uv);
+    ptx::tmem_wait_ld();
+    if (live) {
+      const uint32_t ow[16] = {oh[0].x, oh[0].y, oh[0].z, oh[0].w, oh[1].x, oh[1].y, oh[1].z, oh[1].w,
+                               oh[2].x, oh[2].y, oh[2].z, oh[2].w, oh[3].x, oh[3].y, oh[3].z, oh[3].w};
+      uint32_t go[16], gq[16];
+#pragma unroll
+      for (int t = 0; t < 32; t += 2) {
+        const float o0 = bf16_lo(ow[t >> 1]), o1 = bf16_hi(ow[t >> 1]);
+        go[t >> 1] = ptx::pack_bf16(f(xv[t]) - E * o0, f(xv[t + 1]) - E * o1);
+        gq[t >> 1] = ptx::pack_bf16(scale * (f(yv[t]) - E * f(zv[t]) - Fq * f(uv[t])),
+                                    scale * (f(yv[t + 1]) - E * f(zv[t + 1]) - Fq * f(uv[t + 1])));
+      }
+      uint4* d0 = reinterpret_cast<uint4*>(gdO + rowoff + c0);
+      uint4* d1 = reinterpret_cast<uint4*>(gQ + rowoff + c0);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        d0[u] = make_uint4(go[4 * u], go[4 * u + 1], go[4 * u + 2], go[4 * u + 3]);
+        d1[u] = make_uint4(gq[4 * u], gq[4 * u + 1], gq[4 * u + 2], gq[4 * u + 3]);
+      }
+      if (hf == 0) ws[static_cast<size_t>(bh) * N + row] = make_float4(L2, Dr, E, Fp - E * Dr);
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+// ============================================================= column pass
+struct ColLay {
+  static constexpr int oK = 0, oB = kHeld, oV = 2 * kHeld, oC = 3 * kHeld, oStage = 4 * kHeld;
+  static constexpr int kStat = BN * 16;
+  static constexpr int kStage = 3 * kTile + 2048;  // [Q_i; a_i], dO_i, stats (padded to 1 KB multiple)
+  static constexpr int oBar = oStage + NS * kStage;
+  static constexpr int bytes = oBar + 256;
+  static constexpr int cSG = 0, cPH = 128, cOp = 256, cgV = 352, cgK = 416;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    bob_col_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmC,
+                   const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmA,
+                   const __grid_constant__ CUtensorMap tmdO, const __grid_constant__ CUtensorMap tmSt,
+                   __nv_bfloat16* __restrict__ gK, __nv_bfloat16* __restrict__ gV, int N, int BH, float scale,
+                   float c) {
+  using Lay = ColLay;
+  extern __shared__ __align__(1024) uint8_t sm[];
+  uint64_t* k_full = reinterpret_cast<uint64_t*>(sm + Lay::oBar);
+  uint64_t* full = k_full + 1;
+  uint64_t* empty = full + NS;
+  uint64_t* s_full = empty + NS;
+  uint64_t* ready = s_full + 1;
+  uint64_t* acc_full = ready + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = static_cast<int>(blockIdx.x % BH);
+  const int kb = static_cast<int>(blockIdx.x / BH);
+  const int nq = (N + BN - 1) / BN;
+  const int i0 = (kb * BM) / BN;
+  const int ntile = nq - i0;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(k_full, 1);
+    for (int s = 0; s < NS; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    ptx::mbar_init(s_full, 1);
+    ptx::mbar_init(ready, kCompute);
+    ptx::mbar_init(acc_full, 1);
+    *abort_flag = (ptx::smem_u32(sm) & 1023u) ? 1 : 0;
+    if (*abort_flag) atomicOr(&g_err, FBD_ERR_TIMEOUT);
+    ptx::fence_mbar_init();
+  }
+  if (warp == 9) {
+    ptx::tmem_alloc(tmem_slot, 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const ptx::BoundedWait wait{abort_flag, &g_err};
+  const bool ok = *abort_flag == 0;
+
+  if (warp == 8) {
+    if (lane == 0 && ok) {
+      ptx::prefetch_tmap(&tmQ);
+      ptx::prefetch_tmap(&tmA);
+      ptx::prefetch_tmap(&tmdO);
+      ptx::prefetch_tmap(&tmSt);
+      ptx::mbar_expect_tx(k_full, 4 * kHeld);
+      ptx::tma_load_3d(sm + Lay::oK, &tmK, k_full, 0, kb * BM, bh);
+      ptx::tma_load_3d(sm + Lay::oB, &tmB, k_full, 0, kb * BM, bh);
+      ptx::tma_load_3d(sm + Lay::oV, &tmV, k_full, 0, kb * BM, bh);
+      ptx::tma_load_3d(sm + Lay::oC, &tmC, k_full, 0, kb * BM, bh);
+      for (int t = 0; t < ntile; ++t) {
+        const int s = t % NS, i = i0 + t;
+        if (t >= NS) wait(&empty[s], ((t / NS) - 1) & 1);
+        uint8_t* st = sm + Lay::oStage + s * Lay::kStage;
+        ptx::mbar_expect_tx(&full[s], 3 * kTile + Lay::kStat);
+        ptx::tma_load_3d(st, &tmQ, &full[s], 0, i * BN, bh);
+        ptx::tma_load_3d(st + kTile, &tmA, &full[s], 0, i * BN, bh);
+        ptx::tma_load_3d(st + 2 * kTile, &tmdO, &full[s], 0, i * BN, bh);
+        ptx::tma_load_3d(st + 3 * kTile, &tmSt, &full[s], 0, i * BN, bh);
+      }
+      for (int t = (ntile > NS ? ntile - NS : 0); t < ntile; ++t) wait(&empty[t % NS], (t / NS) & 1);
+    }
+  } else if (warp == 9) {
+    if (lane == 0 && ok) {
+      constexpr uint32_t id128 = ptx::idesc_bf16(BM, 2 * BN, 0, 0);
+      constexpr uint32_t id64 = ptx::idesc_bf16(BM, BN, 0, 0);
+      constexpr uint32_t idO = ptx::idesc_bf16(BM, D, 0, 1);
+      const uint32_t sK = ptx::smem_u32(sm + Lay::oK), sB = ptx::smem_u32(sm + Lay::oB);
+      const uint32_t sV = ptx::smem_u32(sm + Lay::oV), sC = ptx::smem_u32(sm + Lay::oC);
+      const uint32_t sSt = ptx::smem_u32(sm + Lay::oStage);
+      wait(k_full, 0);
+      for (int t = 0; t < ntile; ++t) {
+        const int s = t % NS;
+        const uint32_t qa = sSt + s * Lay::kStage;  // [Q_i; a_i]
+        const uint32_t gt = qa + 2 * kTile;          // dO_i
+        wait(&full[s], (t / NS) & 1);
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          ptx::mma_ss(tmem + Lay::cSG, tc::kmajor_desc(sK, BM, kk), tc::kmajor_desc(qa, 2 * BN, kk), id128, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          ptx::mma_ss(tmem + Lay::cSG + BN, tc::kmajor_desc(sB, BM, kk), tc::kmajor_desc(qa, BN, kk), id64, 1u);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          ptx::mma_ss(tmem + Lay::cPH, tc::kmajor_desc(sV, BM, kk), tc::kmajor_desc(gt, BN, kk), id64, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          ptx::mma_ss(tmem + Lay::cPH + BN, tc::kmajor_desc(sC, BM, kk), tc::kmajor_desc(gt, BN, kk), id64, kk > 0);
+        ptx::mma_commit(s_full);
+        wait(ready, t & 1);
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k) {
+          const uint32_t acc = (t > 0 || k > 0) ? 1u : 0u;
+          ptx::mma_ts(tmem + Lay::cgV, tmem + Lay::cOp + k * 8, tc::mnmajor_desc(gt, BN, k), idO, acc);
+          ptx::mma_ts(tmem + Lay::cgK, tmem + Lay::cOp + 32 + k * 8, tc::mnmajor_desc(qa + kTile, BN, k), idO, acc);
+          ptx::mma_ts(tmem + Lay::cgK, tmem + Lay::cOp + 64 + k * 8, tc::mnmajor_desc(qa, BN, k), idO, 1u);
+        }
+        ptx::mma_commit(&empty[s]);
+      }
+      ptx::mma_commit(acc_full);
+    }
+  } else {
+    const int qd = warp & 3, hf = warp >> 2;
+    const int r = qd * 32 + lane;
+    const uint32_t lo = static_cast<uint32_t>(qd * 32) << 16;
+    const int key = kb * BM + r;
+    const int c0 = hf * 32;
+    for (int t = 0; t < ntile; ++t) {
+      const int s = t % NS, i = i0 + t;
+      wait(s_full, t & 1);
+      ptx::tc_fence_after();
+      const float4* stat =
+          reinterpret_cast<const float4*>(sm + Lay::oStage + s * Lay::kStage + 3 * kTile) + c0;
+      const int qbase = i * BN + c0;
+      uint32_t pDP[16], pDS[16], pSB[16];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t sv[16], gv[16], dv[16], hv[16];
+        ptx::tmem_ld16(tmem + Lay::cSG + c0 + 16 * h + lo, sv);
+        ptx::tmem_ld16(tmem + Lay::cSG + BN + c0 + 16 * h + lo, gv);
+        ptx::tmem_ld16(tmem + Lay::cPH + c0 + 16 * h + lo, dv);
+        ptx::tmem_ld16(tmem + Lay::cPH + BN + c0 + 16 * h + lo, hv);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int u = 0; u < 16; u += 2) {
+          float dpb[2], dsv[2], sbv[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int uu = u + e, qi = qbase + 16 * h + uu;
+            const float4 a = stat[16 * h + uu];  // (L log2 e, D, E, F) of query qi
+            const bool masked = (qi < key) || (qi >= N);
+            const float p = masked ? 0.f : ptx::ex2(fmaf(f(sv[uu]), c, -a.x));
+            const float G = scale * f(gv[uu]);
+            const float dp = f(dv[uu]);
+            const float dmd = dp - a.y;
+            dsv[e] = p * dmd;
+            dpb[e] = p * (G - a.z);
+            sbv[e] = p * (fmaf(G, dmd, -a.z * dp) + f(hv[uu]) - a.w);
+          }
+          const int idx = 8 * h + (u >> 1);
+          pDP[idx] = ptx::pack_bf16(dpb[0], dpb[1]);
+          pDS[idx] = ptx::pack_bf16(dsv[0], dsv[1]);
+          pSB[idx] = ptx::pack_bf16(sbv[0], sbv[1]);
+        }
+      }
+      ptx::tmem_st16(tmem + Lay::cOp + hf * 16 + lo, pDP);
+      ptx::tmem_st16(tmem + Lay::cOp + 32 + hf * 16 + lo, pDS);
+      ptx::tmem_st16(tmem + Lay::cOp + 64 + hf * 16 + lo, pSB);
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(ready);
+    }
+    wait(acc_full, 0);
+    ptx::tc_fence_after();
+    uint32_t av[32], bv[32];
+    ptx::tmem_ld32(tmem + Lay::cgV + c0 + lo, av);
+    ptx::tmem_ld32(tmem + Lay::cgK + c0 + lo, bv);
+    ptx::tmem_wait_ld();
+    if (key < N) {
+      const size_t rowoff = (static_cast<size_t>(bh) * N + key) * D;
+      uint32_t ov[16], ok2[16];
+#pragma unroll
+      for (int u = 0; u < 32; u += 2) {
+        ov[u >> 1] = ptx::pack_bf16(f(av[u]), f(av[u + 1]));
+        ok2[u >> 1] = ptx::pack_bf16(scale * f(bv[u]), scale * f(bv[u + 1]));
+      }
+      uint4* dv = reinterpret_cast<uint4*>(gV + rowoff + c0);
+      uint4* dk = reinterpret_cast<uint4*>(gK + rowoff + c0);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        dv[u] = make_uint4(ov[4 * u], ov[4 * u + 1], ov[4 * u + 2], ov[4 * u + 3]);
+        dk[u] = make_uint4(ok2[4 * u], ok2[4 * u + 1], ok2[4 * u + 2], ok2[4 * u + 3]);
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+cudaError_t tc_bob(const Problem& p, const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                   const float* lse, const void* a, const void* b, const void* cc, void* gQ, void* gK, void* gV,
+                   void* gdO, float4* ws, cudaStream_t st) {
+  if (p.d != D) return cudaErrorInvalidValue;
+  alignas(64) CUtensorMap q128, do128, a128, k64, v64, b64, c64;
+  alignas(64) CUtensorMap k128, b128, v128, c128, q64, a64, do64, s64;
+  const int64_t N = p.N, BH = p.BH;
+  if (!make_tmap_bf16(&q128, Q, N, D, BH, BM) || !make_tmap_bf16(&do128, dO, N, D, BH, BM) ||
+      !make_tmap_bf16(&a128, a, N, D, BH, BM) || !make_tmap_bf16(&k64, K, N, D, BH, BN) ||
+      !make_tmap_bf16(&v64, V, N, D, BH, BN) || !make_tmap_bf16(&b64, b, N, D, BH, BN) ||
+      !make_tmap_bf16(&c64, cc, N, D, BH, BN) || !make_tmap_bf16(&k128, K, N, D, BH, BM) ||
+      !make_tmap_bf16(&b128, b, N, D, BH, BM) || !make_tmap_bf16(&v128, V, N, D, BH, BM) ||
+      !make_tmap_bf16(&c128, cc, N, D, BH, BM) || !make_tmap_bf16(&q64, Q, N, D, BH, BN) ||
+      !make_tmap_bf16(&a64, a, N, D, BH, BN) || !make_tmap_bf16(&do64, dO, N, D, BH, BN) ||
+      !make_tmap_stats(&s64, ws, N, BH, BN))
+    return cudaErrorInvalidValue;
+  const float c = p.scale * kLog2e;
+  const int nrb = static_cast<int>((N + BM - 1) / BM);
+  cudaError_t e = cudaFuncSetAttribute(bob_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, RowLay::bytes);
+  if (e != cudaSuccess) return e;
+  bob_row_kernel<<<static_cast<unsigned>(nrb * BH), kThreads, RowLay::bytes, st>>>(
+      q128, do128, a128, k64, v64, b64, c64, static_cast<const __nv_bfloat16*>(O),
+      static_cast<const __nv_bfloat16*>(dO), lse, static_cast<__nv_bfloat16*>(gQ), static_cast<__nv_bfloat16*>(gdO),
+      ws, static_cast<int>(N), nrb, static_cast<int>(BH), p.scale, c);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(bob_col_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ColLay::bytes);
+  if (e != cudaSuccess) return e;
+  bob_col_kernel<<<static_cast<unsigned>(nrb * BH), kThreads, ColLay::bytes, st>>>(
+      k128, b128, v128, c128, q64, a64, do64, s64, static_cast<__nv_bfloat16*>(gK), static_cast<__nv_bfloat16*>(gV),
+      static_cast<int>(N), static_cast<int>(BH), p.scale, c);
+  return cudaGetLastError();
+}
+
+uint32_t tc_bob_take_error() {
+  uint32_t v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, g_err, sizeof(v)) != cudaSuccess) return 0;
+  if (v) cudaMemcpyToSymbol(g_err, &z, sizeof(z));
+  return v;
+}
+
+}  // namespace fbd
