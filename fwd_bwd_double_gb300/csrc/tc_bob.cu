@@ -50,7 +50,7 @@ __device__ unsigned int g_err = 0;
 constexpr int D = 64;
 constexpr int BM = 128;
 constexpr int BN = 64;
-constexpr int NS = 3;
+constexpr int NS = 5;  // stages of streamed tiles (requested several tile-times ahead)
 constexpr int kCompute = 256;
 constexpr int kThreads = kCompute + 64;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::named_sync(1, kCompute);
     const float Dr = red[r] + red[BM + r];
     const float L2 = live ? lse[static_cast<size_t>(bh) * N + row] * kLog2e : 0.f;
-    float E = 0.f, Fp = 0.f, sW = 0.f, sdS = 0.f, sP = 0.f;
+    float E2[2] = {0.f, 0.f}, Fp2[2] = {0.f, 0.f}, sW2[2] = {0.f, 0.f}, sdS2[2] = {0.f, 0.f}, sP2[2] = {0.f, 0.f};
     const int c0 = hf * 32;
     for (int j = 0; j < nkv; ++j) {
       wait(s_full, j & 1);
@@ -251,17 +251,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             ds[e] = p[e] * (f(dv[tt]) - Dr);
             pg[e] = p[e] * G;
             w[e] = fmaf(G, ds[e], p[e] * f(hv[tt]));
-            Fp += w[e];
+            Fp2[e] += w[e];
           }
           const int idx = 8 * h + (t >> 1);
           pP[idx] = ptx::pack_bf16(p[0], p[1]);
           pG[idx] = ptx::pack_bf16(pg[0], pg[1]);
           pS[idx] = ptx::pack_bf16(ds[0], ds[1]);
           pW[idx] = ptx::pack_bf16(w[0], w[1]);
-          E += bf16_lo(pG[idx]) + bf16_hi(pG[idx]);
-          sW += bf16_lo(pW[idx]) + bf16_hi(pW[idx]);
-          sdS += bf16_lo(pS[idx]) + bf16_hi(pS[idx]);
-          sP += bf16_lo(pP[idx]) + bf16_hi(pP[idx]);
+          const int a2 = (t >> 1) & 1;
+          E2[a2] += bf16_lo(pG[idx]) + bf16_hi(pG[idx]);
+          sW2[a2] += bf16_lo(pW[idx]) + bf16_hi(pW[idx]);
+          sdS2[a2] += bf16_lo(pS[idx]) + bf16_hi(pS[idx]);
+          sP2[a2] += bf16_lo(pP[idx]) + bf16_hi(pP[idx]);
         }
       }
       // Over this thread's own (already read) fp32 columns: [P | P G] and [dS | W].
@@ -273,17 +274,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_before();
       ptx::mbar_arrive(ready);
     }
-    red[2 * BM + hf * BM + r] = E;
-    red[4 * BM + hf * BM + r] = Fp;
-    red[6 * BM + hf * BM + r] = sW;
-    red[8 * BM + hf * BM + r] = sdS;
-    red[10 * BM + hf * BM + r] = sP;
+    red[2 * BM + hf * BM + r] = E2[0] + E2[1];
+    red[4 * BM + hf * BM + r] = Fp2[0] + Fp2[1];
+    red[6 * BM + hf * BM + r] = sW2[0] + sW2[1];
+    red[8 * BM + hf * BM + r] = sdS2[0] + sdS2[1];
+    red[10 * BM + hf * BM + r] = sP2[0] + sP2[1];
     tc::named_sync(1, kCompute);
-    E = red[2 * BM + r] + red[3 * BM + r];
-    Fp = red[4 * BM + r] + red[5 * BM + r];
-    sW = red[6 * BM + r] + red[7 * BM + r];
-    sdS = red[8 * BM + r] + red[9 * BM + r];
-    sP = red[10 * BM + r] + red[11 * BM + r];
+    const float E = red[2 * BM + r] + red[3 * BM + r];
+    const float Fp = red[4 * BM + r] + red[5 * BM + r];
+    const float sW = red[6 * BM + r] + red[7 * BM + r];
+    const float sdS = red[8 * BM + r] + red[9 * BM + r];
+    const float sP = red[10 * BM + r] + red[11 * BM + r];
     const float Fq = (sW - E * sdS) / sP;  // F' as seen through the bf16 operands
     wait(acc_full, 0);
     ptx::tc_fence_after();

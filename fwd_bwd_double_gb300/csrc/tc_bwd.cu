@@ -38,7 +38,10 @@ __device__ unsigned int g_err = 0;
 
 constexpr int BM = 128;        // rows held by a CTA (queries, or keys in the column pass)
 constexpr int BN = 64;         // rows of a streamed block
-constexpr int NS = 3;          // shared-memory stages of streamed tiles
+// Shared-memory stages of streamed tiles: deep enough that a tile is requested
+// several tile-times before its MMA needs it (L2/HBM latency under load).
+template <int D>
+constexpr int stages() { return D == 64 ? 6 : 4; }
 constexpr int kCompute = 256;  // 8 compute warps
 constexpr int kThreads = kCompute + 64;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -50,6 +53,7 @@ using tc::f;
 // ================================================================ row pass
 template <int D, int NB, bool GP>
 struct RowLay {
+  static constexpr int NS = stages<D>();
   static constexpr int kHeld = BM * D * 2;
   static constexpr int kStream = BN * D * 2;
   static constexpr int oQ = 0, odO = kHeld, oK = 2 * kHeld, oV = oK + NS * kStream;
@@ -70,6 +74,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const float* __restrict__ lse, __nv_bfloat16* __restrict__ dQ, float4* __restrict__ ws, int N,
                    int nrb, int BH, float scale, float c) {
   using Lay = RowLay<D, NB, GP>;
+  constexpr int NS = Lay::NS;
   extern __shared__ __align__(1024) uint8_t sm[];
   uint64_t* q_full = reinterpret_cast<uint64_t*>(sm + Lay::oBar);
   uint64_t* full = q_full + 1;
@@ -197,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::named_sync(1, kCompute);
     const float Dr = red[r] + red[BM + r];
     const float L2 = live ? lse[static_cast<size_t>(bh) * N + row] * kLog2e : 0.f;
-    float racc = 0.f, sp = 0.f;
+    float racc2[2] = {0.f, 0.f}, sp2[2] = {0.f, 0.f};
     const int c0 = hf * (BN / 2);
     for (int j = 0; j < nkv; ++j) {
       const int b = j % NB;
@@ -216,8 +221,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         dsk[t >> 1] = ptx::pack_bf16(p0 * (f(pv[t]) - Dr), p1 * (f(pv[t + 1]) - Dr));
         if constexpr (GP) {
           pk[t >> 1] = ptx::pack_bf16(p0, p1);
-          racc += bf16_lo(dsk[t >> 1]) + bf16_hi(dsk[t >> 1]);
-          sp += bf16_lo(pk[t >> 1]) + bf16_hi(pk[t >> 1]);
+          racc2[(t >> 1) & 1] += bf16_lo(dsk[t >> 1]) + bf16_hi(dsk[t >> 1]);
+          sp2[(t >> 1) & 1] += bf16_lo(pk[t >> 1]) + bf16_hi(pk[t >> 1]);
         }
       }
       ptx::tmem_st16(tmem + Lay::cdS + b * (BN / 2) + c0 / 2 + lo, dsk);
@@ -228,8 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     float rho = 0.f;
     if constexpr (GP) {
-      red[2 * BM + hf * BM + r] = racc;
-      red[4 * BM + hf * BM + r] = sp;
+      red[2 * BM + hf * BM + r] = racc2[0] + racc2[1];
+      red[4 * BM + hf * BM + r] = sp2[0] + sp2[1];
       tc::named_sync(1, kCompute);
       rho = (red[2 * BM + r] + red[3 * BM + r]) / (red[4 * BM + r] + red[5 * BM + r]);
     }
@@ -271,6 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ============================================================= column pass
 template <int D, int NB, bool GP>
 struct ColLay {
+  static constexpr int NS = stages<D>();
   static constexpr int kHeld = BM * D * 2;
   static constexpr int kStream = BN * D * 2;
   static constexpr int kStat = BN * 16;
@@ -290,6 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tmSt, __nv_bfloat16* __restrict__ dK,
                    __nv_bfloat16* __restrict__ dV, int N, int BH, float scale, float c) {
   using Lay = ColLay<D, NB, GP>;
+  constexpr int NS = Lay::NS;
   extern __shared__ __align__(1024) uint8_t sm[];
   uint64_t* k_full = reinterpret_cast<uint64_t*>(sm + Lay::oBar);
   uint64_t* full = k_full + 1;

@@ -33,7 +33,7 @@ __device__ unsigned int g_err = 0;
 
 constexpr int BM = 128;
 constexpr int BN = 128;
-constexpr int NS = 2;
+constexpr int NS = 3;  // K/V stages (2 CTAs per SM at d = 64 still fit)
 constexpr int kThreads = 192;
 
 template <int D>
@@ -176,51 +176,63 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
       wait(s_full, j & 1);
       ptx::tc_fence_after();
       const bool diag = (j == rb);  // the only block holding keys after some rows
-      float mx = -INFINITY;
+      // The whole 128-column S row in registers: four loads, one wait.
+      uint32_t v[4][32];
 #pragma unroll
-      for (int ch = 0; ch < BN / 32; ++ch) {
-        uint32_t v[32];
-        ptx::tmem_ld32(tS + lane_off + ch * 32, v);
-        ptx::tmem_wait_ld();
+      for (int ch = 0; ch < 4; ++ch) ptx::tmem_ld32(tS + lane_off + ch * 32, v[ch]);
+      ptx::tmem_wait_ld();
+      if (diag) {
 #pragma unroll
-        for (int t = 0; t < 32; ++t) {
-          const float s = (diag && ch * 32 + t > r) ? -INFINITY : __uint_as_float(v[t]);
-          mx = fmaxf(mx, s);
-        }
+        for (int ch = 0; ch < 4; ++ch)
+#pragma unroll
+          for (int t = 0; t < 32; ++t)
+            if (ch * 32 + t > r) v[ch][t] = __float_as_uint(-INFINITY);
       }
-      const float m_new = fmaxf(m, mx);
+      // Row max over 8 independent partial maxima (short dependency chains).
+      float mx8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) mx8[u] = -INFINITY;
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch)
+#pragma unroll
+        for (int t = 0; t < 32; ++t) mx8[t & 7] = fmaxf(mx8[t & 7], __uint_as_float(v[ch][t]));
+#pragma unroll
+      for (int u = 1; u < 8; ++u) mx8[0] = fmaxf(mx8[0], mx8[u]);
+      const float m_new = fmaxf(m, mx8[0]);
       const bool moved = (j > 0) && (m_new > m);
       const float alpha = moved ? ptx::ex2((m - m_new) * scale_log2) : 1.f;
-      if (__any_sync(0xffffffffu, moved)) {
-#pragma unroll
-        for (int ch = 0; ch < D / 32; ++ch) {
-          uint32_t v[32];
-          ptx::tmem_ld32(tO + lane_off + ch * 32, v);
-          ptx::tmem_wait_ld();
-#pragma unroll
-          for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * alpha);
-          ptx::tmem_st32(tO + lane_off + ch * 32, v);
-        }
-        ptx::tmem_wait_st();
-      }
       l *= alpha;
       m = m_new;
-      float rs = 0.f;
+      // p = 2^((s - m) s log2 e): subtract first, then scale (masked entries are -inf -> 0).
+      float rs8[8];
 #pragma unroll
-      for (int ch = 0; ch < BN / 32; ++ch) {
-        uint32_t v[32];
-        ptx::tmem_ld32(tS + lane_off + ch * 32, v);
-        ptx::tmem_wait_ld();
+      for (int u = 0; u < 8; ++u) rs8[u] = 0.f;
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
         uint32_t pk[16];
 #pragma unroll
         for (int t = 0; t < 32; t += 2) {
-          const bool k0 = diag && ch * 32 + t > r, k1 = diag && ch * 32 + t + 1 > r;
-          const float p0 = k0 ? 0.f : ptx::ex2((__uint_as_float(v[t]) - m) * scale_log2);
-          const float p1 = k1 ? 0.f : ptx::ex2((__uint_as_float(v[t + 1]) - m) * scale_log2);
-          rs += p0 + p1;
+          const float p0 = ptx::ex2((__uint_as_float(v[ch][t]) - m) * scale_log2);
+          const float p1 = ptx::ex2((__uint_as_float(v[ch][t + 1]) - m) * scale_log2);
+          rs8[t & 7] += p0;
+          rs8[(t + 1) & 7] += p1;
           pk[t >> 1] = ptx::pack_bf16(p0, p1);
         }
         ptx::tmem_st16(tP + lane_off + ch * 16, pk);  // keys ch*32 .. ch*32+31
+      }
+      float rs = 0.f;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) rs += rs8[u];
+      if (__any_sync(0xffffffffu, moved)) {  // rescale O for rows whose max moved
+#pragma unroll
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t o[32];
+          ptx::tmem_ld32(tO + lane_off + ch * 32, o);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
+          ptx::tmem_st32(tO + lane_off + ch * 32, o);
+        }
       }
       ptx::tmem_wait_st();
       l += rs;
