@@ -32,7 +32,8 @@
  *   Supported:  causal == 1; d in {64, 128}; dtype in {ATTN_F32, ATTN_BF16};
  *               for attn_bob with ATTN_BF16, d == 64.  Anything else returns
  *               ATTN_ERR_UNSUPPORTED before any launch; there is no fallback.
- *   Scale:      desc->scale == 0 means 1/sqrt(d); otherwise it must be finite.
+ *   Scale:      desc->scale == 0 means 1/sqrt(d); otherwise it must be finite and
+ *               positive (the row max is subtracted before scaling).
  *   Pointers:   device pointers, 16-byte aligned (ATTN_ERR_ALIGNMENT otherwise),
  *               non-NULL whenever B*H*N > 0 (ATTN_ERR_INVALID_ARG).  Outputs must
  *               not overlap inputs, each other, or the workspace
