@@ -18,8 +18,9 @@
 //   dPbar = P (G - E),  Sbar = P (G (dP - D) - E dP + H - F)
 //   outputs gV += dPbar^T dO_i,  gK += dS^T a_i + Sbar^T Q_i;  end gK *= s.
 // All tile products take A and B from 128-byte-swizzled shared memory (TMA);
-// all output products take the bf16 tile (P, P G, dS, W, dPbar, Sbar) from TMEM
-// as the A operand and the streamed block, MN-major, as B.
+// the output products take the bf16 tiles (P, P G, dS, W from shared memory in
+// the row pass; dPbar, dS, Sbar from TMEM in the column pass) as the A operand
+// and the streamed block, MN-major, as B.
 //
 // Rounding: the output products see bf16 copies P^, (PG)^, dS^, W^ of the tiles.
 // The corrections use scalars taken from those same copies,
@@ -31,11 +32,13 @@
 // ("FlashAttention bf16 gradient and GProj", "How the zero sum turns into a false
 // gradient").  The stored state F_i = sum_j W_ij - E_i D_i uses the fp32 sums.
 //
-// Row-pass TMEM: [S | G] 128 columns, [dP | H] 128, X, Y, Z, U 64 each = 512.
-// The bf16 operands are written over the fp32 tile columns their own thread has
-// read, so the next block's tile MMAs wait until this block's output MMAs
-// complete (explicit commit + wait: MMAs with different accumulators carry no
-// ordering guarantee).  Column-pass TMEM: tiles 256, operands 96, gV, gK 128.
+// Row-pass TMEM: [S | G] 128 columns, [dP | H] 128, X, Y, Z, U 64 each = 512; its
+// four bf16 operands go to 128-byte-swizzled shared memory (A operand of the
+// output products).  Column-pass TMEM: tiles 256, operands 96, gV, gK 128.
+// In both passes the compute warps copy a block's tiles into registers and
+// release the tile columns at once, so the next block's tile MMAs overlap this
+// block's CUDA-core work; no TMEM region is read by one MMA while a later MMA
+// with a different accumulator writes it (such MMAs carry no ordering guarantee).
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -50,7 +53,6 @@ __device__ unsigned int g_err = 0;
 constexpr int D = 64;
 constexpr int BM = 128;
 constexpr int BN = 64;
-constexpr int NS = 5;  // stages of streamed tiles (requested several tile-times ahead)
 constexpr int kCompute = 256;
 constexpr int kThreads = kCompute + 64;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -61,17 +63,19 @@ using tc::bf16_hi;
 using tc::bf16_lo;
 using tc::f;
 
-// TMEM column of the bf16 operand for K-step k (16 keys) when a thread half hf
-// stores its 32 keys as [first operand: 16 columns | second operand: 16 columns]
-// inside its own 32 fp32 columns: keys 32 hf .. 32 hf + 31 -> columns 32 hf ...
-__device__ __forceinline__ uint32_t op_col(int k, int second) {
-  return static_cast<uint32_t>(32 * (k >> 1) + 8 * (k & 1) + 16 * second);
-}
-
 // ================================================================ row pass
+// Per 64-key block j the MMA warp issues tiles(j) as soon as the compute warps
+// have copied tiles(j-1) out of TMEM (barrier `consumed`), then outputs(j-1) once
+// the bf16 operands of block j-1 are in shared memory (`ready`).  The tensor pipe
+// thus computes tiles(j) while the CUDA cores turn tiles(j-1) into operands.  The
+// operands live in one shared buffer, rewritten only after outputs(j-1) finished
+// reading it (`out_done`).
 struct RowLay {
-  static constexpr int oQ = 0, odO = kHeld, oA = 2 * kHeld, oStage = 3 * kHeld;
-  static constexpr int kStage = 4 * kTile;  // [K_j; b_j] then [V_j; c_j]
+  static constexpr int NS = 3;
+  static constexpr int oQ = 0, odO = kHeld, oA = 2 * kHeld;
+  static constexpr int oOp = 3 * kHeld;          // P^, (PG)^, dS^, W^: 4 x (128 rows x 64 keys) bf16
+  static constexpr int oStage = oOp + 4 * kHeld;
+  static constexpr int kStage = 4 * kTile;       // [K_j; b_j] then [V_j; c_j]
   static constexpr int oRed = oStage + NS * kStage;
   static constexpr int oBar = oRed + 12 * BM * 4;
   static constexpr int bytes = oBar + 256;
@@ -87,12 +91,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                    __nv_bfloat16* __restrict__ gQ, __nv_bfloat16* __restrict__ gdO, float4* __restrict__ ws, int N,
                    int nrb, int BH, float scale, float c) {
   using Lay = RowLay;
+  constexpr int NS = Lay::NS;
   extern __shared__ __align__(1024) uint8_t sm[];
   uint64_t* q_full = reinterpret_cast<uint64_t*>(sm + Lay::oBar);
   uint64_t* full = q_full + 1;
   uint64_t* empty = full + NS;
   uint64_t* s_full = empty + NS;
-  uint64_t* ready = s_full + 1;
+  uint64_t* consumed = s_full + 1;
+  uint64_t* ready = consumed + 1;
   uint64_t* out_done = ready + 1;
   uint64_t* acc_full = out_done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
@@ -111,6 +117,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&empty[s], 1);
     }
     ptx::mbar_init(s_full, 1);
+    ptx::mbar_init(consumed, kCompute);
     ptx::mbar_init(ready, kCompute);
     ptx::mbar_init(out_done, 1);
     ptx::mbar_init(acc_full, 1);
@@ -158,13 +165,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idO = ptx::idesc_bf16(BM, D, 0, 1);
       const uint32_t sQ = ptx::smem_u32(sm + Lay::oQ), sdO = ptx::smem_u32(sm + Lay::odO);
       const uint32_t sA = ptx::smem_u32(sm + Lay::oA), sSt = ptx::smem_u32(sm + Lay::oStage);
+      const uint32_t sOp = ptx::smem_u32(sm + Lay::oOp);
+      auto outputs = [&](int j) {  // X, Y, Z, U += block j's operands x its streamed tiles
+        const int s = j % NS;
+        const uint32_t kt = sSt + s * Lay::kStage, bt = kt + kTile, vt = kt + 2 * kTile, ct = kt + 3 * kTile;
+        wait(ready, j & 1);
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k) {
+          const uint32_t acc = (j > 0 || k > 0) ? 1u : 0u;
+          const uint64_t aP = tc::kmajor_desc(sOp, BM, k), aPG = tc::kmajor_desc(sOp + kHeld, BM, k);
+          const uint64_t adS = tc::kmajor_desc(sOp + 2 * kHeld, BM, k), aW = tc::kmajor_desc(sOp + 3 * kHeld, BM, k);
+          const uint64_t dK = tc::mnmajor_desc(kt, BN, k), dB = tc::mnmajor_desc(bt, BN, k);
+          const uint64_t dV = tc::mnmajor_desc(vt, BN, k), dC = tc::mnmajor_desc(ct, BN, k);
+          ptx::mma_ss(tmem + Lay::cX, aP, dC, idO, acc);
+          ptx::mma_ss(tmem + Lay::cX, aPG, dV, idO, 1u);
+          ptx::mma_ss(tmem + Lay::cY, adS, dB, idO, acc);
+          ptx::mma_ss(tmem + Lay::cY, aW, dK, idO, 1u);
+          ptx::mma_ss(tmem + Lay::cZ, adS, dK, idO, acc);
+          ptx::mma_ss(tmem + Lay::cU, aP, dK, idO, acc);
+        }
+        ptx::mma_commit(&empty[s]);
+        ptx::mma_commit(out_done);
+      };
       wait(q_full, 0);
       for (int j = 0; j < nkv; ++j) {
         const int s = j % NS;
         const uint32_t kb = sSt + s * Lay::kStage;  // [K_j; b_j]
         const uint32_t vc = kb + 2 * kTile;          // [V_j; c_j]
         wait(&full[s], (j / NS) & 1);
-        if (j > 0) wait(out_done, (j - 1) & 1);  // block j-1's products have read the tile columns
+        if (j > 0) wait(consumed, (j - 1) & 1);  // tiles of block j-1 copied out of TMEM
         ptx::tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
@@ -176,26 +206,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < D / 16; ++kk)
           ptx::mma_ss(tmem + Lay::cPH, tc::kmajor_desc(sdO, BM, kk), tc::kmajor_desc(vc, 2 * BN, kk), id128, kk > 0);
         ptx::mma_commit(s_full);
-        wait(ready, j & 1);
-        ptx::tc_fence_after();
-        const uint32_t kt = kb, bt = kb + kTile, vt = vc, ct = vc + kTile;
-#pragma unroll
-        for (int k = 0; k < BN / 16; ++k) {
-          const uint32_t acc = (j > 0 || k > 0) ? 1u : 0u;
-          const uint32_t aP = tmem + Lay::cSG + op_col(k, 0), aPG = tmem + Lay::cSG + op_col(k, 1);
-          const uint32_t adS = tmem + Lay::cPH + op_col(k, 0), aW = tmem + Lay::cPH + op_col(k, 1);
-          const uint64_t dK = tc::mnmajor_desc(kt, BN, k), dB = tc::mnmajor_desc(bt, BN, k);
-          const uint64_t dV = tc::mnmajor_desc(vt, BN, k), dC = tc::mnmajor_desc(ct, BN, k);
-          ptx::mma_ts(tmem + Lay::cX, aP, dC, idO, acc);
-          ptx::mma_ts(tmem + Lay::cX, aPG, dV, idO, 1u);
-          ptx::mma_ts(tmem + Lay::cY, adS, dB, idO, acc);
-          ptx::mma_ts(tmem + Lay::cY, aW, dK, idO, 1u);
-          ptx::mma_ts(tmem + Lay::cZ, adS, dK, idO, acc);
-          ptx::mma_ts(tmem + Lay::cU, aP, dK, idO, acc);
-        }
-        ptx::mma_commit(&empty[s]);
-        ptx::mma_commit(out_done);
+        if (j > 0) outputs(j - 1);
       }
+      outputs(nkv - 1);
       ptx::mma_commit(acc_full);
     }
   } else {
@@ -227,51 +240,57 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float L2 = live ? lse[static_cast<size_t>(bh) * N + row] * kLog2e : 0.f;
     float E2[2] = {0.f, 0.f}, Fp2[2] = {0.f, 0.f}, sW2[2] = {0.f, 0.f}, sdS2[2] = {0.f, 0.f}, sP2[2] = {0.f, 0.f};
     const int c0 = hf * 32;
+    uint8_t* op = sm + Lay::oOp;
     for (int j = 0; j < nkv; ++j) {
       wait(s_full, j & 1);
       ptx::tc_fence_after();
+      uint32_t sv[32], gv[32], dv[32], hv[32];
+      ptx::tmem_ld32(tmem + Lay::cSG + c0 + lo, sv);
+      ptx::tmem_ld32(tmem + Lay::cSG + BN + c0 + lo, gv);
+      ptx::tmem_ld32(tmem + Lay::cPH + c0 + lo, dv);
+      ptx::tmem_ld32(tmem + Lay::cPH + BN + c0 + lo, hv);
+      ptx::tmem_wait_ld();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(consumed);  // the MMA warp may now overwrite the tile columns
       const int krel = j * BN + c0 - rb * BM;
       uint32_t pP[16], pG[16], pS[16], pW[16];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {  // two sub-chunks of 16 keys
-        uint32_t sv[16], gv[16], dv[16], hv[16];
-        ptx::tmem_ld16(tmem + Lay::cSG + c0 + 16 * h + lo, sv);
-        ptx::tmem_ld16(tmem + Lay::cSG + BN + c0 + 16 * h + lo, gv);
-        ptx::tmem_ld16(tmem + Lay::cPH + c0 + 16 * h + lo, dv);
-        ptx::tmem_ld16(tmem + Lay::cPH + BN + c0 + 16 * h + lo, hv);
-        ptx::tmem_wait_ld();
+      for (int t = 0; t < 32; t += 2) {
+        float p[2], pg[2], ds[2], w[2];
 #pragma unroll
-        for (int t = 0; t < 16; t += 2) {
-          float p[2], pg[2], ds[2], w[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int tt = t + e;
-            p[e] = (krel + 16 * h + tt > r) ? 0.f : ptx::ex2(fmaf(f(sv[tt]), c, -L2));
-            const float G = scale * f(gv[tt]);
-            ds[e] = p[e] * (f(dv[tt]) - Dr);
-            pg[e] = p[e] * G;
-            w[e] = fmaf(G, ds[e], p[e] * f(hv[tt]));
-            Fp2[e] += w[e];
-          }
-          const int idx = 8 * h + (t >> 1);
-          pP[idx] = ptx::pack_bf16(p[0], p[1]);
-          pG[idx] = ptx::pack_bf16(pg[0], pg[1]);
-          pS[idx] = ptx::pack_bf16(ds[0], ds[1]);
-          pW[idx] = ptx::pack_bf16(w[0], w[1]);
-          const int a2 = (t >> 1) & 1;
-          E2[a2] += bf16_lo(pG[idx]) + bf16_hi(pG[idx]);
-          sW2[a2] += bf16_lo(pW[idx]) + bf16_hi(pW[idx]);
-          sdS2[a2] += bf16_lo(pS[idx]) + bf16_hi(pS[idx]);
-          sP2[a2] += bf16_lo(pP[idx]) + bf16_hi(pP[idx]);
+        for (int e = 0; e < 2; ++e) {
+          const int tt = t + e;
+          p[e] = (krel + tt > r) ? 0.f : ptx::ex2(fmaf(f(sv[tt]), c, -L2));
+          const float G = scale * f(gv[tt]);
+          ds[e] = p[e] * (f(dv[tt]) - Dr);
+          pg[e] = p[e] * G;
+          w[e] = fmaf(G, ds[e], p[e] * f(hv[tt]));
+          Fp2[e] += w[e];
         }
+        const int idx = t >> 1, a2 = idx & 1;
+        pP[idx] = ptx::pack_bf16(p[0], p[1]);
+        pG[idx] = ptx::pack_bf16(pg[0], pg[1]);
+        pS[idx] = ptx::pack_bf16(ds[0], ds[1]);
+        pW[idx] = ptx::pack_bf16(w[0], w[1]);
+        E2[a2] += bf16_lo(pG[idx]) + bf16_hi(pG[idx]);
+        sW2[a2] += bf16_lo(pW[idx]) + bf16_hi(pW[idx]);
+        sdS2[a2] += bf16_lo(pS[idx]) + bf16_hi(pS[idx]);
+        sP2[a2] += bf16_lo(pP[idx]) + bf16_hi(pP[idx]);
       }
-      // Over this thread's own (already read) fp32 columns: [P | P G] and [dS | W].
-      ptx::tmem_st16(tmem + Lay::cSG + c0 + lo, pP);
-      ptx::tmem_st16(tmem + Lay::cSG + c0 + 16 + lo, pG);
-      ptx::tmem_st16(tmem + Lay::cPH + c0 + lo, pS);
-      ptx::tmem_st16(tmem + Lay::cPH + c0 + 16 + lo, pW);
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
+      if (j > 0) wait(out_done, (j - 1) & 1);  // block j-1's products have read the operands
+      // Keys 32 hf .. 32 hf + 31 of row r = 16-byte chunks 4 hf .. 4 hf + 3, 128-byte swizzled.
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int chunk = (4 * hf + u) ^ (r & 7);
+        uint8_t* dst = op + r * 128 + chunk * 16;
+        *reinterpret_cast<uint4*>(dst) = make_uint4(pP[4 * u], pP[4 * u + 1], pP[4 * u + 2], pP[4 * u + 3]);
+        *reinterpret_cast<uint4*>(dst + kHeld) = make_uint4(pG[4 * u], pG[4 * u + 1], pG[4 * u + 2], pG[4 * u + 3]);
+        *reinterpret_cast<uint4*>(dst + 2 * kHeld) =
+            make_uint4(pS[4 * u], pS[4 * u + 1], pS[4 * u + 2], pS[4 * u + 3]);
+        *reinterpret_cast<uint4*>(dst + 3 * kHeld) =
+            make_uint4(pW[4 * u], pW[4 * u + 1], pW[4 * u + 2], pW[4 * u + 3]);
+      }
+      ptx::fence_proxy_async_smem();
       ptx::mbar_arrive(ready);
     }
     red[2 * BM + hf * BM + r] = E2[0] + E2[1];
@@ -324,8 +343,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+
 // ============================================================= column pass
+// Same hand-off as the row pass (`consumed` releases the tile columns early,
+// `out_done` guards the operand columns); the three bf16 operands stay in TMEM.
 struct ColLay {
+  static constexpr int NS = 5;
   static constexpr int oK = 0, oB = kHeld, oV = 2 * kHeld, oC = 3 * kHeld, oStage = 4 * kHeld;
   static constexpr int kStat = BN * 16;
   static constexpr int kStage = 3 * kTile + 2048;  // [Q_i; a_i], dO_i, stats (padded to 1 KB multiple)
@@ -342,13 +365,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                    __nv_bfloat16* __restrict__ gK, __nv_bfloat16* __restrict__ gV, int N, int BH, float scale,
                    float c) {
   using Lay = ColLay;
+  constexpr int NS = Lay::NS;
   extern __shared__ __align__(1024) uint8_t sm[];
   uint64_t* k_full = reinterpret_cast<uint64_t*>(sm + Lay::oBar);
   uint64_t* full = k_full + 1;
   uint64_t* empty = full + NS;
   uint64_t* s_full = empty + NS;
-  uint64_t* ready = s_full + 1;
-  uint64_t* acc_full = ready + 1;
+  uint64_t* consumed = s_full + 1;
+  uint64_t* ready = consumed + 1;
+  uint64_t* out_done = ready + 1;
+  uint64_t* acc_full = out_done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -366,7 +392,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&empty[s], 1);
     }
     ptx::mbar_init(s_full, 1);
+    ptx::mbar_init(consumed, kCompute);
     ptx::mbar_init(ready, kCompute);
+    ptx::mbar_init(out_done, 1);
     ptx::mbar_init(acc_full, 1);
     *abort_flag = (ptx::smem_u32(sm) & 1023u) ? 1 : 0;
     if (*abort_flag) atomicOr(&g_err, FBD_ERR_TIMEOUT);
@@ -414,12 +442,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sK = ptx::smem_u32(sm + Lay::oK), sB = ptx::smem_u32(sm + Lay::oB);
       const uint32_t sV = ptx::smem_u32(sm + Lay::oV), sC = ptx::smem_u32(sm + Lay::oC);
       const uint32_t sSt = ptx::smem_u32(sm + Lay::oStage);
+      auto outputs = [&](int t) {
+        const int s = t % NS;
+        const uint32_t qa = sSt + s * Lay::kStage, gt = qa + 2 * kTile;
+        wait(ready, t & 1);
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k) {
+          const uint32_t acc = (t > 0 || k > 0) ? 1u : 0u;
+          ptx::mma_ts(tmem + Lay::cgV, tmem + Lay::cOp + k * 8, tc::mnmajor_desc(gt, BN, k), idO, acc);
+          ptx::mma_ts(tmem + Lay::cgK, tmem + Lay::cOp + 32 + k * 8, tc::mnmajor_desc(qa + kTile, BN, k), idO, acc);
+          ptx::mma_ts(tmem + Lay::cgK, tmem + Lay::cOp + 64 + k * 8, tc::mnmajor_desc(qa, BN, k), idO, 1u);
+        }
+        ptx::mma_commit(&empty[s]);
+        ptx::mma_commit(out_done);
+      };
       wait(k_full, 0);
       for (int t = 0; t < ntile; ++t) {
         const int s = t % NS;
         const uint32_t qa = sSt + s * Lay::kStage;  // [Q_i; a_i]
         const uint32_t gt = qa + 2 * kTile;          // dO_i
         wait(&full[s], (t / NS) & 1);
+        if (t > 0) wait(consumed, (t - 1) & 1);
         ptx::tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
@@ -434,17 +478,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < D / 16; ++kk)
           ptx::mma_ss(tmem + Lay::cPH + BN, tc::kmajor_desc(sC, BM, kk), tc::kmajor_desc(gt, BN, kk), id64, kk > 0);
         ptx::mma_commit(s_full);
-        wait(ready, t & 1);
-        ptx::tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < BN / 16; ++k) {
-          const uint32_t acc = (t > 0 || k > 0) ? 1u : 0u;
-          ptx::mma_ts(tmem + Lay::cgV, tmem + Lay::cOp + k * 8, tc::mnmajor_desc(gt, BN, k), idO, acc);
-          ptx::mma_ts(tmem + Lay::cgK, tmem + Lay::cOp + 32 + k * 8, tc::mnmajor_desc(qa + kTile, BN, k), idO, acc);
-          ptx::mma_ts(tmem + Lay::cgK, tmem + Lay::cOp + 64 + k * 8, tc::mnmajor_desc(qa, BN, k), idO, 1u);
-        }
-        ptx::mma_commit(&empty[s]);
+        if (t > 0) outputs(t - 1);
       }
+      outputs(ntile - 1);
       ptx::mma_commit(acc_full);
     }
   } else {
@@ -457,40 +493,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int s = t % NS, i = i0 + t;
       wait(s_full, t & 1);
       ptx::tc_fence_after();
+      uint32_t sv[32], gv[32], dv[32], hv[32];
+      ptx::tmem_ld32(tmem + Lay::cSG + c0 + lo, sv);
+      ptx::tmem_ld32(tmem + Lay::cSG + BN + c0 + lo, gv);
+      ptx::tmem_ld32(tmem + Lay::cPH + c0 + lo, dv);
+      ptx::tmem_ld32(tmem + Lay::cPH + BN + c0 + lo, hv);
+      ptx::tmem_wait_ld();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(consumed);
       const float4* stat =
           reinterpret_cast<const float4*>(sm + Lay::oStage + s * Lay::kStage + 3 * kTile) + c0;
       const int qbase = i * BN + c0;
       uint32_t pDP[16], pDS[16], pSB[16];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t sv[16], gv[16], dv[16], hv[16];
-        ptx::tmem_ld16(tmem + Lay::cSG + c0 + 16 * h + lo, sv);
-        ptx::tmem_ld16(tmem + Lay::cSG + BN + c0 + 16 * h + lo, gv);
-        ptx::tmem_ld16(tmem + Lay::cPH + c0 + 16 * h + lo, dv);
-        ptx::tmem_ld16(tmem + Lay::cPH + BN + c0 + 16 * h + lo, hv);
-        ptx::tmem_wait_ld();
+      for (int u = 0; u < 32; u += 2) {
+        float dpb[2], dsv[2], sbv[2];
 #pragma unroll
-        for (int u = 0; u < 16; u += 2) {
-          float dpb[2], dsv[2], sbv[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int uu = u + e, qi = qbase + 16 * h + uu;
-            const float4 a = stat[16 * h + uu];  // (L log2 e, D, E, F) of query qi
-            const bool masked = (qi < key) || (qi >= N);
-            const float p = masked ? 0.f : ptx::ex2(fmaf(f(sv[uu]), c, -a.x));
-            const float G = scale * f(gv[uu]);
-            const float dp = f(dv[uu]);
-            const float dmd = dp - a.y;
-            dsv[e] = p * dmd;
-            dpb[e] = p * (G - a.z);
-            sbv[e] = p * (fmaf(G, dmd, -a.z * dp) + f(hv[uu]) - a.w);
-          }
-          const int idx = 8 * h + (u >> 1);
-          pDP[idx] = ptx::pack_bf16(dpb[0], dpb[1]);
-          pDS[idx] = ptx::pack_bf16(dsv[0], dsv[1]);
-          pSB[idx] = ptx::pack_bf16(sbv[0], sbv[1]);
+        for (int e = 0; e < 2; ++e) {
+          const int uu = u + e, qi = qbase + uu;
+          const float4 a = stat[uu];  // (L log2 e, D, E, F) of query qi
+          const bool masked = (qi < key) || (qi >= N);
+          const float p = masked ? 0.f : ptx::ex2(fmaf(f(sv[uu]), c, -a.x));
+          const float G = scale * f(gv[uu]);
+          const float dp = f(dv[uu]);
+          const float dmd = dp - a.y;
+          dsv[e] = p * dmd;
+          dpb[e] = p * (G - a.z);
+          sbv[e] = p * (fmaf(G, dmd, -a.z * dp) + f(hv[uu]) - a.w);
         }
+        pDP[u >> 1] = ptx::pack_bf16(dpb[0], dpb[1]);
+        pDS[u >> 1] = ptx::pack_bf16(dsv[0], dsv[1]);
+        pSB[u >> 1] = ptx::pack_bf16(sbv[0], sbv[1]);
       }
+      if (t > 0) wait(out_done, (t - 1) & 1);  // block t-1's products have read the operand columns
       ptx::tmem_st16(tmem + Lay::cOp + hf * 16 + lo, pDP);
       ptx::tmem_st16(tmem + Lay::cOp + 32 + hf * 16 + lo, pDS);
       ptx::tmem_st16(tmem + Lay::cOp + 64 + hf * 16 + lo, pSB);
