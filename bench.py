@@ -35,11 +35,39 @@ import workloads as W  # noqa: E402
 
 L2_BYTES = 129 * 2 ** 20
 LAUNCHES_PER_STEP = {"fwd": 1, "bwd": 2, "bob": 2}
+KERNELS = ("fwd", "bwd_row", "bwd_col", "bob_row", "bob_col")
+# Contractions (N^2 d products) per kernel: the dense definition's share (each of
+# the pages' contractions counted once; tiles recomputed by a column pass are not
+# counted) and what the kernel executes.  Flops = 2 x count x B H N^2 d / 2.
+DENSE_CONTRACTIONS = {"fwd": 2, "bwd_row": 3, "bwd_col": 2, "bob_row": 9, "bob_col": 3}
+EXECUTED_CONTRACTIONS = {"fwd": 2, "bwd_row": 3, "bwd_col": 4, "bob_row": 11, "bob_col": 8}
 
 
 def dense_flops(w, op):
     unit = w.B * w.H * w.N * w.N * w.d / 2.0
     return {"fwd": 4, "bwd": 10, "bob": 24}[op] * unit
+
+
+def kernel_flops(w, kn, table):
+    return 2 * table[kn] * w.B * w.H * w.N * w.N * w.d / 2.0
+
+
+def traffic_for(kernel, w):
+    """DRAM bytes per launch from the committed ncu capture of this kernel at this
+    workload, or None when there is none or the kernel source changed since."""
+    import hashlib
+    rec = MEASURED_TRAFFIC.get((kernel, w.name))
+    if rec is None:
+        return None
+    src = os.path.join(ROOT, "fwd_bwd_double_gb300", "csrc", rec["source"])
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return rec["bytes"] if sha == rec["sha"] else None
+
+
+# dram__bytes_read.sum + dram__bytes_write.sum per launch (ncu, one-pass capture of
+# the bench command; see profiles/), keyed by (kernel, workload), with the source
+# hash of the kernel file the counters were taken on.
+MEASURED_TRAFFIC = {}
 
 
 def peaks():
@@ -118,20 +146,28 @@ def run_ours(args, w, rank, world):
     shp = x["Q"].shape
     out = {k: torch.empty(shp, dtype=bf, device=dev) for k in ("O", "dQ", "dK", "dV", "gQ", "gK", "gV", "gdO")}
     lse = torch.empty(shp[:3], dtype=torch.float32, device=dev)
-    ws = torch.empty(max(fbd.attn_bob_workspace_bytes(desc), fbd.attn_bwd_workspace_bytes(desc, 1)),
-                     dtype=torch.uint8, device=dev)
+    ws = torch.empty(fbd.attn_bwd_workspace_bytes(desc, 1), dtype=torch.uint8, device=dev)
+    ws2 = torch.empty(fbd.attn_bob_workspace_bytes(desc), dtype=torch.uint8, device=dev)
+
+    R, C = fbd.ATTN_ROW_PASS, fbd.ATTN_COL_PASS
 
     def step(xx, gproj=args.gproj, ev=None):
-        if ev: ev[0].record(stream)
+        """fwd, bwd row pass, bwd column pass, BoB row pass, BoB column pass: one launch each."""
+        def mark(i):
+            if ev:
+                ev[i].record(stream)
+        mark(0)
         fbd.attn_fwd(xx["Q"], xx["K"], xx["V"], O=out["O"], lse=lse, stream=stream, desc=desc)
-        if ev: ev[1].record(stream)
-        fbd.attn_bwd(xx["Q"], xx["K"], xx["V"], out["O"], xx["dO"], lse, gproj=gproj, dQ=out["dQ"], dK=out["dK"],
-                     dV=out["dV"], workspace=ws, stream=stream, desc=desc)
-        if ev: ev[2].record(stream)
-        fbd.attn_bob(xx["Q"], xx["K"], xx["V"], out["O"], xx["dO"], lse, xx["gdQ"], xx["gdK"], xx["gdV"],
-                     gQ=out["gQ"], gK=out["gK"], gV=out["gV"], gdO=out["gdO"], workspace=ws, stream=stream,
-                     desc=desc)
-        if ev: ev[3].record(stream)
+        mark(1)
+        for i, ps in enumerate((R, C)):
+            fbd.attn_bwd_passes(xx["Q"], xx["K"], xx["V"], out["O"], xx["dO"], lse, ps, gproj=gproj, dQ=out["dQ"],
+                                dK=out["dK"], dV=out["dV"], workspace=ws, stream=stream, desc=desc)
+            mark(2 + i)
+        for i, ps in enumerate((R, C)):
+            fbd.attn_bob_passes(xx["Q"], xx["K"], xx["V"], out["O"], xx["dO"], lse, xx["gdQ"], xx["gdK"], xx["gdV"],
+                                ps, gQ=out["gQ"], gK=out["gK"], gV=out["gV"], gdO=out["gdO"], workspace=ws2,
+                                stream=stream, desc=desc)
+            mark(4 + i)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -144,7 +180,7 @@ def run_ours(args, w, rank, world):
             import torch.distributed as dist
             dist.barrier()
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
     barrier()
     torch.cuda.synchronize()
     with ClockSampler(dev.index) as clk:
@@ -156,8 +192,11 @@ def run_ours(args, w, rank, world):
         wall = time.perf_counter() - t0
     barrier()
     fbd.attn_device_status(stream)
-    per_op = {op: [evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps)]
-              for i, op in enumerate(("fwd", "bwd", "bob"))}
+    per_kernel = {kn: [evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps)]
+                  for i, kn in enumerate(KERNELS)}
+    per_op = {"fwd": per_kernel["fwd"],
+              "bwd": [x + y for x, y in zip(per_kernel["bwd_row"], per_kernel["bwd_col"])],
+              "bob": [x + y for x, y in zip(per_kernel["bob_row"], per_kernel["bob_col"])]}
     step_ms = [sum(per_op[op][k] for op in per_op) for k in range(args.steps)]
     ms = statistics.mean(step_ms)
     ms_max = ms
@@ -206,6 +245,7 @@ def run_ours(args, w, rank, world):
     h2d = sum(v.numel() * v.element_size() for v in pinned.values())
     d2h = sum(v.numel() * v.element_size() for v in host_out.values()) + host_lse.numel() * 4
     return dict(ms=ms, ms_max=ms_max, per_op={op: statistics.mean(v) for op, v in per_op.items()},
+                per_kernel={kn: statistics.mean(v) for kn, v in per_kernel.items()},
                 flops_step=flops_step, wall=wall, clocks=clk.summary(), bwd_gproj_ms=(bwd0, bwd1),
                 e2e_ms=e2e_ms, h2d=h2d, d2h=d2h)
 
@@ -233,6 +273,73 @@ def cpu_baseline(w, budget_s=20.0):
                       f"{dt:.2f} s each"}
 
 
+def max_n(args):
+    """Largest N (multiple of 2^16) whose full buffer set for BoB / backward allocates at
+    B=1, H=12, d=64, bf16; then one timed run of each op at N = 2^20 on device-drawn inputs."""
+    import torch
+
+    import fwd_bwd_double_gb300 as fbd
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    H, d = 12, 64
+    row = H * d * 2  # bytes of one token of one [B,H,N,d] bf16 tensor
+    per_token = {"bob": 12 * row + 4 * H + 16 * H, "bwd": 8 * row + 4 * H + 16 * H}
+    ntensor = {"bob": 12, "bwd": 8}
+    free, total = torch.cuda.mem_get_info(dev)
+    out = {"metric": "max N in HBM (B=1, H=12, d=64, bf16)", "hbm_total_bytes": total, "hbm_free_bytes": free}
+
+    def fits(op, N):
+        bufs = []
+        try:
+            for _ in range(ntensor[op]):
+                bufs.append(torch.empty((1, H, N, d), dtype=torch.bfloat16, device=dev))
+            bufs.append(torch.empty((1, H, N), dtype=torch.float32, device=dev))
+            bufs.append(torch.empty((1, H, N, 4), dtype=torch.float32, device=dev))
+            return True
+        except torch.OutOfMemoryError:
+            return False
+        finally:
+            del bufs
+            torch.cuda.empty_cache()
+
+    step = 1 << 16
+    for op in ("bob", "bwd"):
+        lo, hi = 0, (free // per_token[op]) // step + 2  # in units of step
+        while hi - lo > 1:
+            mid = (lo + hi) // 2
+            if fits(op, mid * step):
+                lo = mid
+            else:
+                hi = mid
+        nmax = lo * step
+        bound = free / per_token[op]
+        out[op] = {"max_n_alloc": nmax, "bytes_per_token": per_token[op], "linear_bound_tokens": int(bound),
+                   "fraction_of_bound": nmax / bound}
+    # one execution per op at N = 2^20 (device-drawn N(0,1) inputs: a timing run, not parity)
+    N = 1 << 20
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    x = {k: torch.randn((1, H, N, d), generator=g, device=dev).to(torch.bfloat16)
+         for k in ("Q", "K", "V", "dO", "gdQ", "gdK", "gdV")}
+    O, lse = fbd.attn_fwd(x["Q"], x["K"], x["V"])
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    torch.cuda.synchronize()
+    ev[0].record()
+    fbd.attn_bwd(x["Q"], x["K"], x["V"], O, x["dO"], lse)
+    ev[1].record()
+    fbd.attn_bob(x["Q"], x["K"], x["V"], O, x["dO"], lse, x["gdQ"], x["gdK"], x["gdV"])
+    ev[2].record()
+    torch.cuda.synchronize()
+    fbd.attn_device_status()
+    w = W.Workload("maxn", 1, H, N, d, "bf16")
+    for i, op in enumerate(("bwd", "bob")):
+        ms = ev[i].elapsed_time(ev[i + 1])
+        out[op]["executed_n"] = N
+        out[op]["executed_ms"] = ms
+        out[op]["executed_tflops_dense"] = dense_flops(w, op) / (ms * 1e-3) / 1e12
+    print(json.dumps(out))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -244,7 +351,13 @@ def main():
     ap.add_argument("--heads", type=int, default=12)
     ap.add_argument("--gproj", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--max-n", action="store_true", help="report the largest N that fits in HBM instead")
     args = ap.parse_args()
+    if args.max_n:
+        import __graft_entry__
+        __graft_entry__.build()
+        max_n(args)
+        return
     args.warmup = max(args.warmup, 3)
     w = W.Workload(f"gpt2small_B{args.batch}H{args.heads}N{args.n_seq}d64", args.batch, args.heads, args.n_seq,
                    64, "bf16")
@@ -284,22 +397,33 @@ def main():
     r = run_ours(args, w, rank, world)
     pk = peaks()
     value = r["flops_step"] * world / (r["ms_max"] * 1e-3) / 1e12
-    # Dominant op: the longest of fwd / bwd / BoB.
-    dom = max(r["per_op"], key=lambda op: r["per_op"][op])
-    ach = dense_flops(w, dom) / (r["per_op"][dom] * 1e-3) / 1e12
+    # Dominant kernel: the longest of the five launches of a step.
+    dom = max(r["per_kernel"], key=lambda kn: r["per_kernel"][kn])
+    ach = kernel_flops(w, dom, DENSE_CONTRACTIONS) / (r["per_kernel"][dom] * 1e-3) / 1e12
+
+    def tf(flops, ms):
+        return flops / (ms * 1e-3) / 1e12
+
     line = {
         "metric": "fwd+bwd+BoB attention TFLOP/s (dense definition, causal-halved)",
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": r["ms_max"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic", "config": config,
-        "ops": {op: {"ms": r["per_op"][op], "tflops_dense": dense_flops(w, op) / (r["per_op"][op] * 1e-3) / 1e12,
-                     "frac_of_peak": dense_flops(w, op) / (r["per_op"][op] * 1e-3) / 1e12 / pk["bf16_tflops"]}
+        "ops": {op: {"ms": r["per_op"][op], "tflops_dense": tf(dense_flops(w, op), r["per_op"][op]),
+                     "frac_of_peak": tf(dense_flops(w, op), r["per_op"][op]) / pk["bf16_tflops"]}
                 for op in r["per_op"]},
+        "kernels": {kn: {"ms": r["per_kernel"][kn],
+                         "tflops_dense_share": tf(kernel_flops(w, kn, DENSE_CONTRACTIONS), r["per_kernel"][kn]),
+                         "tflops_executed": tf(kernel_flops(w, kn, EXECUTED_CONTRACTIONS), r["per_kernel"][kn])}
+                    for kn in KERNELS},
         "gproj_bwd_ms": {"off": r["bwd_gproj_ms"][0], "on": r["bwd_gproj_ms"][1],
                          "overhead_pct": 100.0 * (r["bwd_gproj_ms"][1] / r["bwd_gproj_ms"][0] - 1.0)},
         "roofline": {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": pk["bf16_tflops"],
-                     "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops"], "traffic": None,
-                     "peak_source": pk["source"] + " burst bf16"},
+                     "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops"], "traffic": traffic_for(dom, w),
+                     "peak_source": pk["source"] + " burst bf16",
+                     "achieved_basis": "dense-definition contractions of this kernel / its CUDA-event time",
+                     "executed_frac": tf(kernel_flops(w, dom, EXECUTED_CONTRACTIONS), r["per_kernel"][dom])
+                     / pk["bf16_tflops"]},
         "e2e": {"value": r["flops_step"] / (r["e2e_ms"] * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["e2e_ms"]},
         "gpu_launches": sum(LAUNCHES_PER_STEP.values()) * args.steps,

@@ -12,10 +12,11 @@ import ctypes
 import os
 
 from . import _lib
-from ._lib import (ATTN_BF16, ATTN_F32, AttnDesc, FbdError, lib, status_name)  # noqa: F401
+from ._lib import (ATTN_BF16, ATTN_COL_PASS, ATTN_F32, ATTN_ROW_PASS, AttnDesc, FbdError, lib,  # noqa: F401
+                   status_name)
 
 __all__ = [
-    "attn_fwd", "attn_bwd", "attn_bob", "attn_bwd_workspace_bytes", "attn_bob_workspace_bytes",
+    "attn_fwd", "attn_bwd", "attn_bob", "attn_bwd_passes", "attn_bob_passes", "ATTN_ROW_PASS", "ATTN_COL_PASS", "attn_bwd_workspace_bytes", "attn_bob_workspace_bytes",
     "attn_bob_static", "attn_bwd_projected_dS", "attn_device_status", "attn_status_string", "attn_version", "make_desc",
     "FbdError", "AttnDesc", "ATTN_F32", "ATTN_BF16", "lib",
 ]
@@ -98,6 +99,13 @@ def _workspace(nbytes, like, workspace):
 def attn_bwd(Q, K, V, O, dO, lse, gproj: int = 0, dQ=None, dK=None, dV=None, workspace=None,
              scale: float = 0.0, stream=None, desc=None):
     """dQ, dK, dV = recompute backward (GProj when gproj != 0, bf16 only)."""
+    return attn_bwd_passes(Q, K, V, O, dO, lse, ATTN_ROW_PASS | ATTN_COL_PASS, gproj, dQ, dK, dV, workspace,
+                           scale, stream, desc)
+
+
+def attn_bwd_passes(Q, K, V, O, dO, lse, passes, gproj: int = 0, dQ=None, dK=None, dV=None, workspace=None,
+                    scale: float = 0.0, stream=None, desc=None):
+    """The backward's row pass (dQ) and/or column pass (dK, dV); see attn_bwd_passes in fbd.h."""
     torch = _torch()
     desc = desc or make_desc(Q, scale)
     dQ = torch.empty_like(Q) if dQ is None else dQ
@@ -105,15 +113,23 @@ def attn_bwd(Q, K, V, O, dO, lse, gproj: int = 0, dQ=None, dK=None, dV=None, wor
     dV = torch.empty_like(V) if dV is None else dV
     need = attn_bwd_workspace_bytes(desc, gproj)
     workspace = _workspace(need, Q, workspace)
-    _check(lib.attn_bwd(ctypes.byref(desc), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(lse),
-                        _ptr(dQ), _ptr(dK), _ptr(dV), int(gproj), _ptr(workspace),
-                        ctypes.c_size_t(workspace.numel() * workspace.element_size()), _stream(stream)))
+    _check(lib.attn_bwd_passes(ctypes.byref(desc), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(lse),
+                               _ptr(dQ), _ptr(dK), _ptr(dV), int(gproj), _ptr(workspace),
+                               ctypes.c_size_t(workspace.numel() * workspace.element_size()), int(passes),
+                               _stream(stream)))
     return dQ, dK, dV
 
 
 def attn_bob(Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ=None, gK=None, gV=None, gdO=None, workspace=None,
              scale: float = 0.0, stream=None, desc=None):
     """gQ, gK, gV, gdO = backward over backward against cotangents (gdQ, gdK, gdV)."""
+    return attn_bob_passes(Q, K, V, O, dO, lse, gdQ, gdK, gdV, ATTN_ROW_PASS | ATTN_COL_PASS, gQ, gK, gV, gdO,
+                           workspace, scale, stream, desc)
+
+
+def attn_bob_passes(Q, K, V, O, dO, lse, gdQ, gdK, gdV, passes, gQ=None, gK=None, gV=None, gdO=None,
+                    workspace=None, scale: float = 0.0, stream=None, desc=None):
+    """BoB's row pass (gQ, gdO, row states) and/or column pass (gK, gV); see fbd.h."""
     torch = _torch()
     desc = desc or make_desc(Q, scale)
     gQ = torch.empty_like(Q) if gQ is None else gQ
@@ -121,10 +137,10 @@ def attn_bob(Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ=None, gK=None, gV=None, gdO=
     gV = torch.empty_like(V) if gV is None else gV
     gdO = torch.empty_like(dO) if gdO is None else gdO
     workspace = _workspace(attn_bob_workspace_bytes(desc), Q, workspace)
-    _check(lib.attn_bob(ctypes.byref(desc), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(lse),
-                        _ptr(gdQ), _ptr(gdK), _ptr(gdV), _ptr(gQ), _ptr(gK), _ptr(gV), _ptr(gdO),
-                        _ptr(workspace), ctypes.c_size_t(workspace.numel() * workspace.element_size()),
-                        _stream(stream)))
+    _check(lib.attn_bob_passes(ctypes.byref(desc), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(lse),
+                               _ptr(gdQ), _ptr(gdK), _ptr(gdV), _ptr(gQ), _ptr(gK), _ptr(gV), _ptr(gdO),
+                               _ptr(workspace), ctypes.c_size_t(workspace.numel() * workspace.element_size()),
+                               int(passes), _stream(stream)))
     return gQ, gK, gV, gdO
 
 

@@ -8,6 +8,8 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfbd.so")
 
 ATTN_F32 = 0
 ATTN_BF16 = 1
+ATTN_ROW_PASS = 1
+ATTN_COL_PASS = 2
 
 STATUS_NAMES = {
     0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_ALIGNMENT",
@@ -38,6 +40,9 @@ PROTOTYPES = {
     "attn_bwd": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int, _P, ctypes.c_size_t, _P]),
     "attn_bob_workspace_bytes": (ctypes.c_size_t, [_D]),
     "attn_bob": (ctypes.c_int, [_D] + [_P] * 13 + [_P, ctypes.c_size_t, _P]),
+    "attn_bwd_passes": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int, _P, ctypes.c_size_t,
+                                        ctypes.c_int, _P]),
+    "attn_bob_passes": (ctypes.c_int, [_D] + [_P] * 13 + [_P, ctypes.c_size_t, ctypes.c_int, _P]),
     "attn_bob_static": (ctypes.c_int, [_D] + [_P] * 13 + [_P]),
     "attn_bwd_projected_dS": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, _P]),
     "attn_device_status": (ctypes.c_int, [_P]),

@@ -134,12 +134,13 @@ size_t attn_bob_workspace_bytes(const attn_desc_t* desc) {
   return static_cast<size_t>(desc->B) * desc->H * desc->N * 16;
 }
 
-attn_status_t attn_bwd(const attn_desc_t* desc, const void* Q, const void* K, const void* V, const void* O,
-                       const void* dO, const float* lse, void* dQ, void* dK, void* dV, int gproj, void* workspace,
-                       size_t workspace_bytes, void* stream) {
+attn_status_t attn_bwd_passes(const attn_desc_t* desc, const void* Q, const void* K, const void* V, const void* O,
+                              const void* dO, const float* lse, void* dQ, void* dK, void* dV, int gproj,
+                              void* workspace, size_t workspace_bytes, int passes, void* stream) {
   fbd::Problem p;
   attn_status_t s = check_desc(desc, p);
   if (s != ATTN_OK) return s;
+  if (passes < 1 || passes > 3) return fail(ATTN_ERR_INVALID_ARG, "passes must be ATTN_ROW_PASS, ATTN_COL_PASS or both%s");
   if (p.BH * p.N == 0) return ATTN_OK;
   const size_t need = attn_bwd_workspace_bytes(desc, gproj);
   if (workspace == nullptr || workspace_bytes < need)
@@ -152,20 +153,29 @@ attn_status_t attn_bwd(const attn_desc_t* desc, const void* Q, const void* K, co
   if ((s = check_ptrs(in, 6, out, 4)) != ATTN_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   float4* ws = static_cast<float4*>(workspace);
-  if (p.dtype == ATTN_F32) return launch_status(fbd::simt_bwd(p, Q, K, V, O, dO, lse, dQ, dK, dV, 0, ws, st));
+  if (p.dtype == ATTN_F32)
+    return launch_status(fbd::simt_bwd(p, Q, K, V, O, dO, lse, dQ, dK, dV, 0, ws, passes, st));
   if (!tc_path(p, 1)) return fail(ATTN_ERR_UNSUPPORTED, "no bf16 backward kernel for this head dim%s");
-  return launch_status(fbd::tc_bwd(p, Q, K, V, O, dO, lse, dQ, dK, dV, gproj != 0, ws, st));
+  return launch_status(fbd::tc_bwd(p, Q, K, V, O, dO, lse, dQ, dK, dV, gproj != 0, ws, passes, st));
 }
 
-attn_status_t attn_bob(const attn_desc_t* desc, const void* Q, const void* K, const void* V, const void* O,
-                       const void* dO, const float* lse, const void* gdQ, const void* gdK, const void* gdV,
-                       void* gQ, void* gK, void* gV, void* gdO, void* workspace, size_t workspace_bytes,
-                       void* stream) {
+attn_status_t attn_bwd(const attn_desc_t* desc, const void* Q, const void* K, const void* V, const void* O,
+                       const void* dO, const float* lse, void* dQ, void* dK, void* dV, int gproj, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  return attn_bwd_passes(desc, Q, K, V, O, dO, lse, dQ, dK, dV, gproj, workspace, workspace_bytes,
+                         ATTN_ROW_PASS | ATTN_COL_PASS, stream);
+}
+
+attn_status_t attn_bob_passes(const attn_desc_t* desc, const void* Q, const void* K, const void* V, const void* O,
+                              const void* dO, const float* lse, const void* gdQ, const void* gdK, const void* gdV,
+                              void* gQ, void* gK, void* gV, void* gdO, void* workspace, size_t workspace_bytes,
+                              int passes, void* stream) {
   fbd::Problem p;
   attn_status_t s = check_desc(desc, p);
   if (s != ATTN_OK) return s;
   if (p.dtype == ATTN_BF16 && !fbd::tc_supports(2, p.d))
     return fail(ATTN_ERR_UNSUPPORTED, "bf16 backward-over-backward supports d = 64 only%s");
+  if (passes < 1 || passes > 3) return fail(ATTN_ERR_INVALID_ARG, "passes must be ATTN_ROW_PASS, ATTN_COL_PASS or both%s");
   if (p.BH * p.N == 0) return ATTN_OK;
   const size_t need = attn_bob_workspace_bytes(desc);
   if (workspace == nullptr || workspace_bytes < need)
@@ -180,8 +190,16 @@ attn_status_t attn_bob(const attn_desc_t* desc, const void* Q, const void* K, co
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   float4* ws = static_cast<float4*>(workspace);
   if (p.dtype == ATTN_F32)
-    return launch_status(fbd::simt_bob(p, Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ, gK, gV, gdO, ws, st));
-  return launch_status(fbd::tc_bob(p, Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ, gK, gV, gdO, ws, st));
+    return launch_status(fbd::simt_bob(p, Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ, gK, gV, gdO, ws, passes, st));
+  return launch_status(fbd::tc_bob(p, Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ, gK, gV, gdO, ws, passes, st));
+}
+
+attn_status_t attn_bob(const attn_desc_t* desc, const void* Q, const void* K, const void* V, const void* O,
+                       const void* dO, const float* lse, const void* gdQ, const void* gdK, const void* gdV,
+                       void* gQ, void* gK, void* gV, void* gdO, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  return attn_bob_passes(desc, Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ, gK, gV, gdO, workspace, workspace_bytes,
+                         ATTN_ROW_PASS | ATTN_COL_PASS, stream);
 }
 
 attn_status_t attn_bwd_projected_dS(const attn_desc_t* desc, const void* Q, const void* K, const void* V,

@@ -21,10 +21,10 @@ cudaError_t simt_fwd(const Problem& p, const void* Q, const void* K, const void*
                      cudaStream_t st);
 cudaError_t simt_bwd(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
                      const void* dO, const float* lse, void* dQ, void* dK, void* dV, int gproj, float4* ws,
-                     cudaStream_t st);
+                     int passes, cudaStream_t st);
 cudaError_t simt_bob(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
                      const void* dO, const float* lse, const void* a, const void* b, const void* c, void* gQ,
-                     void* gK, void* gV, void* gdO, float4* ws, cudaStream_t st);
+                     void* gK, void* gV, void* gdO, float4* ws, int passes, cudaStream_t st);
 cudaError_t simt_projected_dS(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
                               const void* dO, const float* lse, float* dS, cudaStream_t st);
 
@@ -34,10 +34,12 @@ cudaError_t tc_fwd(const Problem& p, const void* Q, const void* K, const void* V
                    cudaStream_t st);
 cudaError_t tc_bwd(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
                    const void* dO, const float* lse, void* dQ, void* dK, void* dV, int gproj, float4* ws,
-                   cudaStream_t st);
+                   int passes, cudaStream_t st);
 cudaError_t tc_bob(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
                    const void* dO, const float* lse, const void* a, const void* b, const void* c, void* gQ,
-                   void* gK, void* gV, void* gdO, float4* ws, cudaStream_t st);
+                   void* gK, void* gV, void* gdO, float4* ws, int passes, cudaStream_t st);
+
+// passes: bit 0 = the row pass, bit 1 = the column pass (ATTN_ROW_PASS / ATTN_COL_PASS).
 
 // Which kernels exist for a given (op, dtype, d): false means ATTN_ERR_UNSUPPORTED.
 bool tc_supports(int op, int64_t d);  // op: 0 fwd, 1 bwd, 2 bob

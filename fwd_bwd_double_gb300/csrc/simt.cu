@@ -1,5 +1,5 @@
-// Float32 path: forward, backward (GProj emulation for bf16 debugging), BoB and
-// the GProj projected-dS export, on CUDA cores in exact fp32 arithmetic.
+// Float32 path: forward, backward and BoB on CUDA cores in exact fp32 arithmetic,
+// plus the GProj projected-dS diagnostic export (bf16 inputs).
 //
 // Work split: one warp per query row (row passes) or per key (column passes);
 // a warp's 32 lanes each hold d/32 consecutive elements of the row's vectors, so
@@ -522,7 +522,7 @@ cudaError_t fwd_t(const Problem& p, const void* Q, const void* K, const void* V,
 
 template <typename T, int D, bool GP>
 cudaError_t bwd_t(const Problem& p, const void* Q, const void* K, const void* V, const void* O, const void* dO,
-                  const float* lse, void* dQ, void* dK, void* dV, float4* ws, cudaStream_t st) {
+                  const float* lse, void* dQ, void* dK, void* dV, float4* ws, int passes, cudaStream_t st) {
   const size_t sm_row = 2 * kTile * D * sizeof(float);
   const size_t sm_col = 2 * kTile * D * sizeof(float) + kTile * sizeof(float4);
   auto kr = bwd_row_kernel<T, D, GP>;
@@ -530,12 +530,15 @@ cudaError_t bwd_t(const Problem& p, const void* Q, const void* K, const void* V,
   cudaError_t e = allow_smem(kr, sm_row);
   if (e == cudaSuccess) e = allow_smem(kc, sm_col);
   if (e != cudaSuccess) return e;
-  kr<<<grid_for(p), kThreads, sm_row, st>>>(static_cast<const T*>(Q), static_cast<const T*>(K),
-                                             static_cast<const T*>(V), static_cast<const T*>(O),
-                                             static_cast<const T*>(dO), lse, static_cast<T*>(dQ), ws, p.N, p.BH,
-                                             p.scale);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  if (passes & 1) {
+    kr<<<grid_for(p), kThreads, sm_row, st>>>(static_cast<const T*>(Q), static_cast<const T*>(K),
+                                               static_cast<const T*>(V), static_cast<const T*>(O),
+                                               static_cast<const T*>(dO), lse, static_cast<T*>(dQ), ws, p.N, p.BH,
+                                               p.scale);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (!(passes & 2)) return cudaSuccess;
   kc<<<grid_for(p), kThreads, sm_col, st>>>(static_cast<const T*>(Q), static_cast<const T*>(K),
                                              static_cast<const T*>(V), static_cast<const T*>(dO), ws,
                                              static_cast<T*>(dK), static_cast<T*>(dV), p.N, p.BH, p.scale);
@@ -545,7 +548,7 @@ cudaError_t bwd_t(const Problem& p, const void* Q, const void* K, const void* V,
 template <typename T, int D>
 cudaError_t bob_t(const Problem& p, const void* Q, const void* K, const void* V, const void* O, const void* dO,
                   const float* lse, const void* a, const void* b, const void* c, void* gQ, void* gK, void* gV,
-                  void* gdO, float4* ws, cudaStream_t st) {
+                  void* gdO, float4* ws, int passes, cudaStream_t st) {
   const size_t sm_row = 4 * kTile * D * sizeof(float);
   const size_t sm_col = 3 * kTile * D * sizeof(float) + kTile * sizeof(float4);
   auto kr = bob_row_kernel<T, D>;
@@ -554,12 +557,15 @@ cudaError_t bob_t(const Problem& p, const void* Q, const void* K, const void* V,
   if (e == cudaSuccess) e = allow_smem(kc, sm_col);
   if (e != cudaSuccess) return e;
   using CT = const T*;
-  kr<<<grid_for(p), kThreads, sm_row, st>>>(
-      static_cast<CT>(Q), static_cast<CT>(K), static_cast<CT>(V), static_cast<CT>(O), static_cast<CT>(dO), lse,
-      static_cast<CT>(a), static_cast<CT>(b), static_cast<CT>(c), static_cast<T*>(gQ), static_cast<T*>(gdO), ws,
-      p.N, p.BH, p.scale);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  if (passes & 1) {
+    kr<<<grid_for(p), kThreads, sm_row, st>>>(
+        static_cast<CT>(Q), static_cast<CT>(K), static_cast<CT>(V), static_cast<CT>(O), static_cast<CT>(dO), lse,
+        static_cast<CT>(a), static_cast<CT>(b), static_cast<CT>(c), static_cast<T*>(gQ), static_cast<T*>(gdO), ws,
+        p.N, p.BH, p.scale);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (!(passes & 2)) return cudaSuccess;
   kc<<<grid_for(p), kThreads, sm_col, st>>>(static_cast<CT>(Q), static_cast<CT>(K), static_cast<CT>(V),
                                              static_cast<CT>(dO), static_cast<CT>(a), static_cast<CT>(b),
                                              static_cast<CT>(c), ws, static_cast<T*>(gK), static_cast<T*>(gV),
@@ -579,25 +585,17 @@ cudaError_t simt_fwd(const Problem& p, const void* Q, const void* K, const void*
 
 cudaError_t simt_bwd(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
                      const void* dO, const float* lse, void* dQ, void* dK, void* dV, int gproj, float4* ws,
-                     cudaStream_t st) {
-  if (p.dtype == ATTN_F32)
-    return p.d == 64 ? bwd_t<float, 64, false>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, st)
-                     : bwd_t<float, 128, false>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, st);
-  if (gproj)
-    return p.d == 64 ? bwd_t<__nv_bfloat16, 64, true>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, st)
-                     : bwd_t<__nv_bfloat16, 128, true>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, st);
-  return p.d == 64 ? bwd_t<__nv_bfloat16, 64, false>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, st)
-                   : bwd_t<__nv_bfloat16, 128, false>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, st);
+                     int passes, cudaStream_t st) {
+  (void)gproj;  // fp32 dS is never rounded, so there is nothing to project
+  return p.d == 64 ? bwd_t<float, 64, false>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st)
+                   : bwd_t<float, 128, false>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st);
 }
 
 cudaError_t simt_bob(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
                      const void* dO, const float* lse, const void* a, const void* b, const void* c, void* gQ,
-                     void* gK, void* gV, void* gdO, float4* ws, cudaStream_t st) {
-  if (p.dtype == ATTN_F32)
-    return p.d == 64 ? bob_t<float, 64>(p, Q, K, V, O, dO, lse, a, b, c, gQ, gK, gV, gdO, ws, st)
-                     : bob_t<float, 128>(p, Q, K, V, O, dO, lse, a, b, c, gQ, gK, gV, gdO, ws, st);
-  return p.d == 64 ? bob_t<__nv_bfloat16, 64>(p, Q, K, V, O, dO, lse, a, b, c, gQ, gK, gV, gdO, ws, st)
-                   : bob_t<__nv_bfloat16, 128>(p, Q, K, V, O, dO, lse, a, b, c, gQ, gK, gV, gdO, ws, st);
+                     void* gK, void* gV, void* gdO, float4* ws, int passes, cudaStream_t st) {
+  return p.d == 64 ? bob_t<float, 64>(p, Q, K, V, O, dO, lse, a, b, c, gQ, gK, gV, gdO, ws, passes, st)
+                   : bob_t<float, 128>(p, Q, K, V, O, dO, lse, a, b, c, gQ, gK, gV, gdO, ws, passes, st);
 }
 
 cudaError_t simt_projected_dS(const Problem& p, const void* Q, const void* K, const void* V, const void* O,

@@ -569,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 cudaError_t tc_bob(const Problem& p, const void* Q, const void* K, const void* V, const void* O, const void* dO,
                    const float* lse, const void* a, const void* b, const void* cc, void* gQ, void* gK, void* gV,
-                   void* gdO, float4* ws, cudaStream_t st) {
+                   void* gdO, float4* ws, int passes, cudaStream_t st) {
   if (p.d != D) return cudaErrorInvalidValue;
   alignas(64) CUtensorMap q128, do128, a128, k64, v64, b64, c64;
   alignas(64) CUtensorMap k128, b128, v128, c128, q64, a64, do64, s64;
@@ -585,13 +585,17 @@ cudaError_t tc_bob(const Problem& p, const void* Q, const void* K, const void* V
     return cudaErrorInvalidValue;
   const float c = p.scale * kLog2e;
   const int nrb = static_cast<int>((N + BM - 1) / BM);
-  cudaError_t e = cudaFuncSetAttribute(bob_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, RowLay::bytes);
+  cudaError_t e = cudaSuccess;
+  if (passes & 1) {
+  e = cudaFuncSetAttribute(bob_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, RowLay::bytes);
   if (e != cudaSuccess) return e;
   bob_row_kernel<<<static_cast<unsigned>(nrb * BH), kThreads, RowLay::bytes, st>>>(
       q128, do128, a128, k64, v64, b64, c64, static_cast<const __nv_bfloat16*>(O),
       static_cast<const __nv_bfloat16*>(dO), lse, static_cast<__nv_bfloat16*>(gQ), static_cast<__nv_bfloat16*>(gdO),
       ws, static_cast<int>(N), nrb, static_cast<int>(BH), p.scale, c);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (!(passes & 2)) return cudaSuccess;
   e = cudaFuncSetAttribute(bob_col_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ColLay::bytes);
   if (e != cudaSuccess) return e;
   bob_col_kernel<<<static_cast<unsigned>(nrb * BH), kThreads, ColLay::bytes, st>>>(

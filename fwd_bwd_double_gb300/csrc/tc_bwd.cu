@@ -475,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, int NBR, int NBC, bool GP>
 cudaError_t launch(const Problem& p, const void* Q, const void* K, const void* V, const void* O, const void* dO,
-                   const float* lse, void* dQ, void* dK, void* dV, float4* ws, cudaStream_t st) {
+                   const float* lse, void* dQ, void* dK, void* dV, float4* ws, int passes, cudaStream_t st) {
   alignas(64) CUtensorMap q128, do128, k64, v64, k128, v128, q64, do64, s64;
   const int64_t N = p.N, BH = p.BH;
   if (!make_tmap_bf16(&q128, Q, N, D, BH, BM) || !make_tmap_bf16(&do128, dO, N, D, BH, BM) ||
@@ -486,7 +486,7 @@ cudaError_t launch(const Problem& p, const void* Q, const void* K, const void* V
     return cudaErrorInvalidValue;
   const float c = p.scale * kLog2e;
   const int nrb = static_cast<int>((N + BM - 1) / BM);
-  {
+  if (passes & 1) {
     using Lay = RowLay<D, NBR, GP>;
     auto kern = bwd_row_kernel<D, NBR, GP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::bytes);
@@ -496,7 +496,7 @@ cudaError_t launch(const Problem& p, const void* Q, const void* K, const void* V
         static_cast<__nv_bfloat16*>(dQ), ws, static_cast<int>(N), nrb, static_cast<int>(BH), p.scale, c);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  {
+  if (passes & 2) {
     using Lay = ColLay<D, NBC, GP>;
     auto kern = bwd_col_kernel<D, NBC, GP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::bytes);
@@ -506,17 +506,19 @@ cudaError_t launch(const Problem& p, const void* Q, const void* K, const void* V
         static_cast<int>(N), static_cast<int>(BH), p.scale, c);
     return cudaGetLastError();
   }
+  return cudaSuccess;
 }
 
 }  // namespace
 
 cudaError_t tc_bwd(const Problem& p, const void* Q, const void* K, const void* V, const void* O, const void* dO,
-                   const float* lse, void* dQ, void* dK, void* dV, int gproj, float4* ws, cudaStream_t st) {
+                   const float* lse, void* dQ, void* dK, void* dV, int gproj, float4* ws, int passes,
+                   cudaStream_t st) {
   if (p.d == 64)
-    return gproj ? launch<64, 2, 1, true>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, st)
-                 : launch<64, 2, 2, false>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, st);
-  return gproj ? launch<128, 1, 1, true>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, st)
-               : launch<128, 2, 1, false>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, st);
+    return gproj ? launch<64, 2, 1, true>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st)
+                 : launch<64, 2, 2, false>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st);
+  return gproj ? launch<128, 1, 1, true>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st)
+               : launch<128, 2, 1, false>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st);
 }
 
 uint32_t tc_bwd_take_error() {

@@ -161,6 +161,28 @@ attn_status_t attn_bob_static(const attn_desc_t* desc, const void* Q, const void
                               const void* gdQ, const void* gdK, const void* gdV,
                               void* gQ, void* gK, void* gV, void* gdO, void* stream);
 
+/* The two launches of attn_bwd / attn_bob, issued separately (for callers that
+ * schedule or time the passes themselves).  passes = ATTN_ROW_PASS (backward: dQ
+ * and the row statistics; BoB: gQ, gdO and the row states), ATTN_COL_PASS
+ * (backward: dK, dV; BoB: gK, gV, both from the statistics the row pass left in
+ * `workspace`), or both, which is exactly attn_bwd / attn_bob.  A column pass
+ * must follow, in stream order, a row pass over the same inputs and workspace.
+ * Arguments and checks are those of attn_bwd / attn_bob (all pointers are
+ * validated whichever pass runs); any other `passes` is ATTN_ERR_INVALID_ARG.
+ * [BoB] "Two scalar states replace quadratic tensors" (row pass, then column pass);
+ * [GP] "How the zero sum ..." (the key correction needs the finished rows). */
+#define ATTN_ROW_PASS 1
+#define ATTN_COL_PASS 2
+attn_status_t attn_bwd_passes(const attn_desc_t* desc, const void* Q, const void* K, const void* V,
+                              const void* O, const void* dO, const float* lse,
+                              void* dQ, void* dK, void* dV, int gproj,
+                              void* workspace, size_t workspace_bytes, int passes, void* stream);
+attn_status_t attn_bob_passes(const attn_desc_t* desc, const void* Q, const void* K, const void* V,
+                              const void* O, const void* dO, const float* lse,
+                              const void* gdQ, const void* gdK, const void* gdV,
+                              void* gQ, void* gK, void* gV, void* gdO,
+                              void* workspace, size_t workspace_bytes, int passes, void* stream);
+
 /* Diagnostic export of the GProj-projected score gradient (bf16 only).
  * Writes dS_out [B,H,N,N] float32 with dS_out[i][j] = dS^_ij - rho_i P^_ij for
  * j <= i (and 0 for j > i), where dS^, P^ and rho_i = r_i / sum_k P^_ik are the

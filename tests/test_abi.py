@@ -129,3 +129,16 @@ def test_python_binding_raises_on_error():
     with pytest.raises(fbd.FbdError) as e:
         fbd.attn_fwd(q, q, q, O=torch.zeros_like(q), lse=torch.zeros(1, 1, 4))
     assert e.value.status == UNSUP
+
+
+def test_pass_masks_are_validated():
+    d = desc()
+    p = ptrs(10)
+    wsb = lib.attn_bwd_workspace_bytes(ctypes.byref(d), 0)
+    for bad in (0, 4, -1):
+        assert lib.attn_bwd_passes(ctypes.byref(d), *p[:9], 0, p[9], wsb, bad, None) == INVALID
+    q = ptrs(14)
+    wsb = lib.attn_bob_workspace_bytes(ctypes.byref(d))
+    for bad in (0, 7):
+        assert lib.attn_bob_passes(ctypes.byref(d), *q[:13], q[13], wsb, bad, None) == INVALID
+    assert fbd.ATTN_ROW_PASS == 1 and fbd.ATTN_COL_PASS == 2

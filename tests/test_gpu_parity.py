@@ -222,6 +222,30 @@ def test_outputs_written_once_and_nothing_outside():
         assert not np.isnan(view.float().cpu().numpy()).any(), f"{k}: element not written"
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_separate_passes_equal_the_fused_call(dtype):
+    """attn_*_passes(ROW) then attn_*_passes(COL) is exactly attn_bwd / attn_bob."""
+    import fwd_bwd_double_gb300 as fbd
+    w = W.Workload(f"passes_B2H3N300d64_{dtype}", 2, 3, 300, 64, dtype)
+    x = to_device(inputs(w), w)
+    O, lse = fbd.attn_fwd(x["Q"], x["K"], x["V"])
+    ref_b = fbd.attn_bwd(x["Q"], x["K"], x["V"], O, x["dO"], lse, gproj=1)
+    ref_g = fbd.attn_bob(x["Q"], x["K"], x["V"], O, x["dO"], lse, x["gdQ"], x["gdK"], x["gdV"])
+    import torch
+    outs = [torch.empty_like(x["Q"]) for _ in range(3)]
+    ws = torch.empty(fbd.attn_bwd_workspace_bytes(fbd.make_desc(x["Q"]), 1), dtype=torch.uint8, device="cuda")
+    for ps in (fbd.ATTN_ROW_PASS, fbd.ATTN_COL_PASS):
+        fbd.attn_bwd_passes(x["Q"], x["K"], x["V"], O, x["dO"], lse, ps, gproj=1, dQ=outs[0], dK=outs[1],
+                            dV=outs[2], workspace=ws)
+    gouts = [torch.empty_like(x["Q"]) for _ in range(4)]
+    for ps in (fbd.ATTN_ROW_PASS, fbd.ATTN_COL_PASS):
+        fbd.attn_bob_passes(x["Q"], x["K"], x["V"], O, x["dO"], lse, x["gdQ"], x["gdK"], x["gdV"], ps,
+                            gQ=gouts[0], gK=gouts[1], gV=gouts[2], gdO=gouts[3], workspace=ws)
+    fbd.attn_device_status()
+    for a, b in zip(outs + gouts, list(ref_b) + list(ref_g)):
+        assert torch.equal(a, b)
+
+
 def test_deterministic():
     w = W.GPT2_LAYER.with_n(512)
     xd = to_device(inputs(w), w)
