@@ -87,8 +87,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* red = reinterpret_cast<float*>(sm + Lay::oRed);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = static_cast<int>(blockIdx.x % BH);
-  const int rb = nrb - 1 - static_cast<int>(blockIdx.x / BH);  // heaviest first
+  const tc::Order ord = tc::grid_order(BH, nrb);
+  const int bh = ord.bh;
+  const int rb = nrb - 1 - ord.k;  // heaviest row blocks first (within a group of slices)
   const int nkv = ((rb + 1) * BM + BN - 1) / BN;                 // key blocks touching rows <= last row
 
   if (threadIdx.x == 0) {
@@ -308,8 +309,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = static_cast<int>(blockIdx.x % BH);
-  const int kb = static_cast<int>(blockIdx.x / BH);  // first key blocks have the most rows: first
+  const int nkb = (N + BM - 1) / BM;
+  const tc::Order ord = tc::grid_order(BH, nkb);
+  const int bh = ord.bh;
+  const int kb = ord.k;  // first key blocks have the most rows: first
   const int nq = (N + BN - 1) / BN;
   const int i0 = (kb * BM) / BN;                      // first query block with a query >= first key
   const int ntile = nq - i0;

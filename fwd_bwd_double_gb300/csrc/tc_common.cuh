@@ -27,6 +27,26 @@ __device__ __forceinline__ void named_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
+// Grid order of the 1-D grids: slices (batch, head) go in groups of 8, so the
+// streamed tiles of one group (K, V, ... of 8 heads) stay resident in L2 while its
+// CTAs run; within a group, block index k = 0 (the heaviest causal block) comes
+// first, interleaved across the group's slices.
+struct Order {
+  int bh, k;
+};
+__device__ __forceinline__ Order grid_order(int BH, int nblk) {
+  constexpr int G = 8;
+  const int x = static_cast<int>(blockIdx.x);
+  const int group = x / (G * nblk);
+  const int base = group * G;
+  const int gsize = min(G, BH - base);
+  const int within = x - base * nblk;
+  Order o;
+  o.k = within / gsize;
+  o.bh = base + within % gsize;
+  return o;
+}
+
 // The two floats held by a packed bf16x2 word (low half = even element).
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }

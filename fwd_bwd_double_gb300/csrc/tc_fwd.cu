@@ -25,6 +25,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "tc_common.cuh"
 
 namespace fbd {
 namespace {
@@ -78,8 +79,9 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = static_cast<int>(blockIdx.x % BH);
-  const int rb = nrb - 1 - static_cast<int>(blockIdx.x / BH);  // heaviest row blocks first
+  const tc::Order ord = tc::grid_order(BH, nrb);
+  const int bh = ord.bh;
+  const int rb = nrb - 1 - ord.k;  // heaviest row blocks first (within a group of slices)
   const int nkv = rb + 1;
 
   if (threadIdx.x == 0) {
