@@ -131,7 +131,9 @@ size_t attn_bwd_workspace_bytes(const attn_desc_t* desc, int gproj) {
 
 size_t attn_bob_workspace_bytes(const attn_desc_t* desc) {
   if (desc == nullptr || desc->B < 0 || desc->H < 0 || desc->N < 0) return 0;
-  return static_cast<size_t>(desc->B) * desc->H * desc->N * 16;
+  // 16 bytes per row, rows of each slice rounded up to an even count (the bf16
+  // column pass reads the row states two rows at a time).
+  return static_cast<size_t>(desc->B) * desc->H * ((desc->N + 1) & ~static_cast<int64_t>(1)) * 16;
 }
 
 attn_status_t attn_bwd_passes(const attn_desc_t* desc, const void* Q, const void* K, const void* V, const void* O,

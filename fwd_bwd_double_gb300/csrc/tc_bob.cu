@@ -23,10 +23,10 @@
 // and the streamed block, MN-major, as B.
 //
 // Rounding: the output products see bf16 copies P^, (PG)^, dS^, W^ of the tiles.
-// The corrections use scalars taken from those same copies,
-//   E_i = sum_j (PG)^_ij,  F'_i = (sum_j W^_ij - E_i sum_j dS^_ij) / sum_j P^_ij,
+// The corrections use E_i = sum_j (PG)_ij (fp32) and a second state taken from
+// those same copies,  F'_i = (sum_j W^_ij - E_i sum_j dS^_ij) / sum_j P^_ij,
 // so that the row of Sbar the products effectively see, W^ - E dS^ - F' P^, sums
-// to exactly zero (as the exact Sbar does).  In exact arithmetic these are the
+// to exactly zero (as the exact Sbar does) whatever the rounding of E.  In exact arithmetic these are the
 // definitions above (sum dS = 0, sum P = 1); in bf16 they keep the rounding of W
 // from being multiplied by the mean key, the same mechanism GProj removes from dQ
 // ("FlashAttention bf16 gradient and GProj", "How the zero sum turns into a false
@@ -40,6 +40,8 @@
 // block's CUDA-core work; no TMEM region is read by one MMA while a later MMA
 // with a different accumulator writes it (such MMAs carry no ordering guarantee).
 #include <cuda_bf16.h>
+
+#include <type_traits>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -89,7 +91,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tmC, const __nv_bfloat16* __restrict__ O,
                    const __nv_bfloat16* __restrict__ dO, const float* __restrict__ lse,
                    __nv_bfloat16* __restrict__ gQ, __nv_bfloat16* __restrict__ gdO, float4* __restrict__ ws, int N,
-                   int nrb, int BH, float scale, float c) {
+                   int Np, int nrb, int BH, float scale, float c) {
   using Lay = RowLay;
   constexpr int NS = Lay::NS;
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -239,7 +241,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::named_sync(1, kCompute);
     const float Dr = red[r] + red[BM + r];
     const float L2 = live ? lse[static_cast<size_t>(bh) * N + row] * kLog2e : 0.f;
-    float E2[2] = {0.f, 0.f}, Fp2[2] = {0.f, 0.f}, sW2[2] = {0.f, 0.f}, sdS2[2] = {0.f, 0.f}, sP2[2] = {0.f, 0.f};
+    // Per-row sums as fp32 pairs (two keys per f32x2 instruction).
+    uint64_t accE = 0, accF = 0, accW = 0, accdS = 0, accP = 0;
+    const uint64_t c2 = tc::pk2f(c, c), s2 = tc::pk2f(scale, scale);
+    const uint64_t nL2 = tc::pk2f(-L2, -L2), nD2 = tc::pk2f(-Dr, -Dr);
     const int c0 = hf * 32;
     uint8_t* op = sm + Lay::oOp;
     for (int j = 0; j < nkv; ++j) {
@@ -255,29 +260,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_arrive(consumed);  // the MMA warp may now overwrite the tile columns
       const int krel = j * BN + c0 - rb * BM;
       uint32_t pP[16], pG[16], pS[16], pW[16];
+      auto block = [&](auto masked) {
 #pragma unroll
-      for (int t = 0; t < 32; t += 2) {
-        float p[2], pg[2], ds[2], w[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int tt = t + e;
-          p[e] = (krel + tt > r) ? 0.f : ptx::ex2(fmaf(f(sv[tt]), c, -L2));
-          const float G = scale * f(gv[tt]);
-          ds[e] = p[e] * (f(dv[tt]) - Dr);
-          pg[e] = p[e] * G;
-          w[e] = fmaf(G, ds[e], p[e] * f(hv[tt]));
-          Fp2[e] += w[e];
+        for (int t = 0; t < 32; t += 2) {
+          const float2 arg = tc::unpk2(tc::fma2(tc::pk2(sv[t], sv[t + 1]), c2, nL2));
+          float p0 = ptx::ex2(arg.x), p1 = ptx::ex2(arg.y);
+          if constexpr (decltype(masked)::value) {
+            if (krel + t > r) p0 = 0.f;
+            if (krel + t + 1 > r) p1 = 0.f;
+          }
+          const uint64_t P2 = tc::pk2f(p0, p1);
+          const uint64_t G2 = tc::mul2(tc::pk2(gv[t], gv[t + 1]), s2);
+          const uint64_t ds2 = tc::mul2(P2, tc::add2(tc::pk2(dv[t], dv[t + 1]), nD2));
+          const uint64_t pg2 = tc::mul2(P2, G2);
+          const uint64_t w2 = tc::fma2(G2, ds2, tc::mul2(P2, tc::pk2(hv[t], hv[t + 1])));
+          accF = tc::add2(accF, w2);
+          accE = tc::add2(accE, pg2);
+          const float2 ds = tc::unpk2(ds2), pg = tc::unpk2(pg2), w = tc::unpk2(w2);
+          const int idx = t >> 1;
+          pP[idx] = ptx::pack_bf16(p0, p1);
+          pG[idx] = ptx::pack_bf16(pg.x, pg.y);
+          pS[idx] = ptx::pack_bf16(ds.x, ds.y);
+          pW[idx] = ptx::pack_bf16(w.x, w.y);
+          accW = tc::add2(accW, tc::bf2_to_f2(pW[idx]));
+          accdS = tc::add2(accdS, tc::bf2_to_f2(pS[idx]));
+          accP = tc::add2(accP, tc::bf2_to_f2(pP[idx]));
         }
-        const int idx = t >> 1, a2 = idx & 1;
-        pP[idx] = ptx::pack_bf16(p[0], p[1]);
-        pG[idx] = ptx::pack_bf16(pg[0], pg[1]);
-        pS[idx] = ptx::pack_bf16(ds[0], ds[1]);
-        pW[idx] = ptx::pack_bf16(w[0], w[1]);
-        E2[a2] += bf16_lo(pG[idx]) + bf16_hi(pG[idx]);
-        sW2[a2] += bf16_lo(pW[idx]) + bf16_hi(pW[idx]);
-        sdS2[a2] += bf16_lo(pS[idx]) + bf16_hi(pS[idx]);
-        sP2[a2] += bf16_lo(pP[idx]) + bf16_hi(pP[idx]);
-      }
+      };
+      if (krel + 31 > 0)  // a block reaching past the first row of this CTA: causal mask needed
+        block(std::true_type{});
+      else
+        block(std::false_type{});
       if (j > 0) wait(out_done, (j - 1) & 1);  // block j-1's products have read the operands
       // Keys 32 hf .. 32 hf + 31 of row r = 16-byte chunks 4 hf .. 4 hf + 3, 128-byte swizzled.
 #pragma unroll
@@ -294,11 +307,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::fence_proxy_async_smem();
       ptx::mbar_arrive(ready);
     }
-    red[2 * BM + hf * BM + r] = E2[0] + E2[1];
-    red[4 * BM + hf * BM + r] = Fp2[0] + Fp2[1];
-    red[6 * BM + hf * BM + r] = sW2[0] + sW2[1];
-    red[8 * BM + hf * BM + r] = sdS2[0] + sdS2[1];
-    red[10 * BM + hf * BM + r] = sP2[0] + sP2[1];
+    auto hsum = [](uint64_t x) {
+      const float2 v = tc::unpk2(x);
+      return v.x + v.y;
+    };
+    red[2 * BM + hf * BM + r] = hsum(accE);
+    red[4 * BM + hf * BM + r] = hsum(accF);
+    red[6 * BM + hf * BM + r] = hsum(accW);
+    red[8 * BM + hf * BM + r] = hsum(accdS);
+    red[10 * BM + hf * BM + r] = hsum(accP);
     tc::named_sync(1, kCompute);
     const float E = red[2 * BM + r] + red[3 * BM + r];
     const float Fp = red[4 * BM + r] + red[5 * BM + r];
@@ -332,7 +349,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         d0[u] = make_uint4(go[4 * u], go[4 * u + 1], go[4 * u + 2], go[4 * u + 3]);
         d1[u] = make_uint4(gq[4 * u], gq[4 * u + 1], gq[4 * u + 2], gq[4 * u + 3]);
       }
-      if (hf == 0) ws[static_cast<size_t>(bh) * N + row] = make_float4(L2, Dr, E, Fp - E * Dr);
+      if (hf == 0) {  // row states, negated, pair-interleaved (see the column pass)
+        float* wf = reinterpret_cast<float*>(ws) + static_cast<size_t>(bh) * Np * 4;
+        const int64_t k2 = row & ~static_cast<int64_t>(1);
+        const int odd = static_cast<int>(row & 1);
+        wf[k2 * 4 + odd] = -L2;
+        wf[k2 * 4 + 2 + odd] = -Dr;
+        wf[(k2 + 1) * 4 + odd] = -E;
+        wf[(k2 + 1) * 4 + 2 + odd] = -(Fp - E * Dr);
+      }
     }
   }
 
@@ -504,30 +529,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tmem_wait_ld();
       ptx::tc_fence_before();
       ptx::mbar_arrive(consumed);
+      // Row states of the 64 queries, pair-interleaved: float4 2m = (-L2, -L2', -D, -D'),
+      // float4 2m+1 = (-E, -E', -F, -F') of queries 2m, 2m+1 of the block.
       const float4* stat =
           reinterpret_cast<const float4*>(sm + Lay::oStage + s * Lay::kStage + 3 * kTile) + c0;
       const int qbase = i * BN + c0;
+      const uint64_t c2 = tc::pk2f(c, c), s2 = tc::pk2f(scale, scale);
       uint32_t pDP[16], pDS[16], pSB[16];
+      auto block = [&](auto masked) {
 #pragma unroll
-      for (int u = 0; u < 32; u += 2) {
-        float dpb[2], dsv[2], sbv[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int uu = u + e, qi = qbase + uu;
-          const float4 a = stat[uu];  // (L log2 e, D, E, F) of query qi
-          const bool masked = (qi < key) || (qi >= N);
-          const float p = masked ? 0.f : ptx::ex2(fmaf(f(sv[uu]), c, -a.x));
-          const float G = scale * f(gv[uu]);
-          const float dp = f(dv[uu]);
-          const float dmd = dp - a.y;
-          dsv[e] = p * dmd;
-          dpb[e] = p * (G - a.z);
-          sbv[e] = p * (fmaf(G, dmd, -a.z * dp) + f(hv[uu]) - a.w);
+        for (int u = 0; u < 32; u += 2) {
+          const float4 A = stat[u], Bs = stat[u + 1];
+          const uint64_t nL = tc::pk2f(A.x, A.y), nD = tc::pk2f(A.z, A.w);
+          const uint64_t nE = tc::pk2f(Bs.x, Bs.y), nF = tc::pk2f(Bs.z, Bs.w);
+          const float2 arg = tc::unpk2(tc::fma2(tc::pk2(sv[u], sv[u + 1]), c2, nL));
+          float p0 = ptx::ex2(arg.x), p1 = ptx::ex2(arg.y);
+          if constexpr (decltype(masked)::value) {
+            const int q0 = qbase + u;
+            if (q0 < key || q0 >= N) p0 = 0.f;
+            if (q0 + 1 < key || q0 + 1 >= N) p1 = 0.f;
+          }
+          const uint64_t P2 = tc::pk2f(p0, p1);
+          const uint64_t G2 = tc::mul2(tc::pk2(gv[u], gv[u + 1]), s2);
+          const uint64_t dP2 = tc::pk2(dv[u], dv[u + 1]);
+          const uint64_t dmd = tc::add2(dP2, nD);                          // dP - D
+          const uint64_t ds2 = tc::mul2(P2, dmd);
+          const uint64_t dpb2 = tc::mul2(P2, tc::add2(G2, nE));            // P (G - E)
+          const uint64_t t2 = tc::fma2(G2, dmd, tc::mul2(nE, dP2));        // G (dP - D) - E dP
+          const uint64_t sb2 = tc::mul2(P2, tc::add2(tc::add2(t2, tc::pk2(hv[u], hv[u + 1])), nF));
+          const float2 vdp = tc::unpk2(dpb2), vds = tc::unpk2(ds2), vsb = tc::unpk2(sb2);
+          pDP[u >> 1] = ptx::pack_bf16(vdp.x, vdp.y);
+          pDS[u >> 1] = ptx::pack_bf16(vds.x, vds.y);
+          pSB[u >> 1] = ptx::pack_bf16(vsb.x, vsb.y);
         }
-        pDP[u >> 1] = ptx::pack_bf16(dpb[0], dpb[1]);
-        pDS[u >> 1] = ptx::pack_bf16(dsv[0], dsv[1]);
-        pSB[u >> 1] = ptx::pack_bf16(sbv[0], sbv[1]);
-      }
+      };
+      // Causal mask only in the first blocks (queries before this CTA's last key) and
+      // past N only in the last block.
+      if (qbase < kb * BM + BM || qbase + 32 > N)
+        block(std::true_type{});
+      else
+        block(std::false_type{});
       if (t > 0) wait(out_done, (t - 1) & 1);  // block t-1's products have read the operand columns
       ptx::tmem_st16(tmem + Lay::cOp + hf * 16 + lo, pDP);
       ptx::tmem_st16(tmem + Lay::cOp + 32 + hf * 16 + lo, pDS);
@@ -576,7 +617,7 @@ cudaError_t tc_bob(const Problem& p, const void* Q, const void* K, const void* V
   if (p.d != D) return cudaErrorInvalidValue;
   alignas(64) CUtensorMap q128, do128, a128, k64, v64, b64, c64;
   alignas(64) CUtensorMap k128, b128, v128, c128, q64, a64, do64, s64;
-  const int64_t N = p.N, BH = p.BH;
+  const int64_t N = p.N, BH = p.BH, Np = (p.N + 1) & ~static_cast<int64_t>(1);
   if (!make_tmap_bf16(&q128, Q, N, D, BH, BM) || !make_tmap_bf16(&do128, dO, N, D, BH, BM) ||
       !make_tmap_bf16(&a128, a, N, D, BH, BM) || !make_tmap_bf16(&k64, K, N, D, BH, BN) ||
       !make_tmap_bf16(&v64, V, N, D, BH, BN) || !make_tmap_bf16(&b64, b, N, D, BH, BN) ||
@@ -584,7 +625,7 @@ cudaError_t tc_bob(const Problem& p, const void* Q, const void* K, const void* V
       !make_tmap_bf16(&b128, b, N, D, BH, BM) || !make_tmap_bf16(&v128, V, N, D, BH, BM) ||
       !make_tmap_bf16(&c128, cc, N, D, BH, BM) || !make_tmap_bf16(&q64, Q, N, D, BH, BN) ||
       !make_tmap_bf16(&a64, a, N, D, BH, BN) || !make_tmap_bf16(&do64, dO, N, D, BH, BN) ||
-      !make_tmap_stats(&s64, ws, N, BH, BN))
+      !make_tmap_stats(&s64, ws, Np, BH, BN))
     return cudaErrorInvalidValue;
   const float c = p.scale * kLog2e;
   const int nrb = static_cast<int>((N + BM - 1) / BM);
@@ -595,7 +636,7 @@ cudaError_t tc_bob(const Problem& p, const void* Q, const void* K, const void* V
   bob_row_kernel<<<static_cast<unsigned>(nrb * BH), kThreads, RowLay::bytes, st>>>(
       q128, do128, a128, k64, v64, b64, c64, static_cast<const __nv_bfloat16*>(O),
       static_cast<const __nv_bfloat16*>(dO), lse, static_cast<__nv_bfloat16*>(gQ), static_cast<__nv_bfloat16*>(gdO),
-      ws, static_cast<int>(N), nrb, static_cast<int>(BH), p.scale, c);
+      ws, static_cast<int>(N), static_cast<int>(Np), nrb, static_cast<int>(BH), p.scale, c);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (!(passes & 2)) return cudaSuccess;

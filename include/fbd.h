@@ -115,7 +115,9 @@ attn_status_t attn_bwd(const attn_desc_t* desc, const void* Q, const void* K, co
                        void* dQ, void* dK, void* dV, int gproj,
                        void* workspace, size_t workspace_bytes, void* stream);
 
-/* Workspace for attn_bob: 16 bytes per (b,h,row) = float4 (lse, D, E, F). */
+/* Workspace for attn_bob: 16 bytes per (b,h,row), the rows of each slice rounded
+ * up to an even count: the per-row states (lse, D, E, F) written by the row pass
+ * for the column pass (layout internal to the library). */
 size_t attn_bob_workspace_bytes(const attn_desc_t* desc);
 
 /* Backward over backward.  [BoB] "Why go backward through an already computed
