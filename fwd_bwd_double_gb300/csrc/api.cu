@@ -126,7 +126,9 @@ attn_status_t attn_fwd(const attn_desc_t* desc, const void* Q, const void* K, co
 size_t attn_bwd_workspace_bytes(const attn_desc_t* desc, int gproj) {
   (void)gproj;
   if (desc == nullptr || desc->B < 0 || desc->H < 0 || desc->N < 0) return 0;
-  return static_cast<size_t>(desc->B) * desc->H * desc->N * 16;
+  // 16 bytes per row, the rows of each slice rounded up to an even count (the bf16
+  // column pass reads the row statistics two rows at a time).
+  return static_cast<size_t>(desc->B) * desc->H * ((desc->N + 1) & ~static_cast<int64_t>(1)) * 16;
 }
 
 size_t attn_bob_workspace_bytes(const attn_desc_t* desc) {

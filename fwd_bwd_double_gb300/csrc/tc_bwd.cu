@@ -7,7 +7,8 @@
 //   row pass    (CTA holds 128 query rows, streams 64-key blocks j <= i)
 //               S = Q K_j^T, dP = dO V_j^T           (A, B from shared memory)
 //               dQ += dS K_j                          (A = dS from TMEM, B = K_j MN-major)
-//               writes dQ = s dQ once and the row statistics (L log2 e, D, rho, 0)
+//               writes dQ = s dQ once and the row statistics (L log2 e, D, rho), stored
+//               negated and interleaved by row pairs for the column pass
 //   column pass (CTA holds 128 keys, streams 64-query blocks i >= j)
 //               S^T = K Q_i^T, dP^T = V dO_i^T        (transposed tiles: lanes = keys)
 //               dV += P^T dO_i, dK += dS^T Q_i        (A from TMEM, B MN-major)
@@ -26,6 +27,8 @@
 // and issues the MMAs.  Score tiles are NB-buffered in TMEM so the MMAs of tile
 // t+1 run while the compute warps turn tile t into dS.
 #include <cuda_bf16.h>
+
+#include <type_traits>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -53,7 +56,12 @@ using tc::f;
 // ================================================================ row pass
 template <int D, int NB, bool GP>
 struct RowLay {
-  static constexpr int NS = stages<D>();
+  // TMEM columns used (see below); at most 256 lets two CTAs share an SM, in which
+  // case the ring is shortened so that both fit in shared memory.
+  static constexpr int kCols = 2 * NB * BN + NB * BN / 2 + (GP ? NB * BN / 2 : 0) + D + (GP ? D : 0);
+  static constexpr int kTmem = kCols <= 256 ? 256 : 512;
+  static constexpr int kMinBlocks = kTmem == 256 ? 2 : 1;
+  static constexpr int NS = kTmem == 256 ? 4 : stages<D>();
   static constexpr int kHeld = BM * D * 2;
   static constexpr int kStream = BN * D * 2;
   static constexpr int oQ = 0, odO = kHeld, oK = 2 * kHeld, oV = oK + NS * kStream;
@@ -63,16 +71,16 @@ struct RowLay {
   static constexpr int cS = 0, cdP = NB * BN, cdS = 2 * NB * BN, cP = cdS + NB * BN / 2;
   static constexpr int cdQ = cP + (GP ? NB * BN / 2 : 0), cPK = cdQ + D;
   static constexpr int cols = cPK + (GP ? D : 0);
-  static_assert(cols <= 512, "TMEM budget");
+  static_assert(cols == kCols && cols <= 512, "TMEM budget");
 };
 
 template <int D, int NB, bool GP>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
     bwd_row_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                    const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const __nv_bfloat16* __restrict__ O, const __nv_bfloat16* __restrict__ dO,
                    const float* __restrict__ lse, __nv_bfloat16* __restrict__ dQ, float4* __restrict__ ws, int N,
-                   int nrb, int BH, float scale, float c) {
+                   int Np, int nrb, int BH, float scale, float c) {
   using Lay = RowLay<D, NB, GP>;
   constexpr int NS = Lay::NS;
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -108,7 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::fence_mbar_init();
   }
   if (warp == 9) {
-    ptx::tmem_alloc(tmem_slot, 512);
+    ptx::tmem_alloc(tmem_slot, Lay::kTmem);
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
@@ -203,7 +211,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::named_sync(1, kCompute);
     const float Dr = red[r] + red[BM + r];
     const float L2 = live ? lse[static_cast<size_t>(bh) * N + row] * kLog2e : 0.f;
-    float racc2[2] = {0.f, 0.f}, sp2[2] = {0.f, 0.f};
+    uint64_t accR = 0, accP = 0;  // GProj: sums of the bf16 dS and P fed to the products
+    const uint64_t c2 = tc::pk2f(c, c), nL2 = tc::pk2f(-L2, -L2), nD2 = tc::pk2f(-Dr, -Dr);
     const int c0 = hf * (BN / 2);
     for (int j = 0; j < nkv; ++j) {
       const int b = j % NB;
@@ -215,17 +224,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tmem_wait_ld();
       const int krel = j * BN + c0 - rb * BM;  // key of my column 0 minus the block's first row
       uint32_t dsk[16], pk[16];
+      auto block = [&](auto masked) {
 #pragma unroll
-      for (int t = 0; t < 32; t += 2) {
-        const float p0 = (krel + t > r) ? 0.f : ptx::ex2(fmaf(f(sv[t]), c, -L2));
-        const float p1 = (krel + t + 1 > r) ? 0.f : ptx::ex2(fmaf(f(sv[t + 1]), c, -L2));
-        dsk[t >> 1] = ptx::pack_bf16(p0 * (f(pv[t]) - Dr), p1 * (f(pv[t + 1]) - Dr));
-        if constexpr (GP) {
-          pk[t >> 1] = ptx::pack_bf16(p0, p1);
-          racc2[(t >> 1) & 1] += bf16_lo(dsk[t >> 1]) + bf16_hi(dsk[t >> 1]);
-          sp2[(t >> 1) & 1] += bf16_lo(pk[t >> 1]) + bf16_hi(pk[t >> 1]);
+        for (int t = 0; t < 32; t += 2) {
+          const float2 arg = tc::unpk2(tc::fma2(tc::pk2(sv[t], sv[t + 1]), c2, nL2));
+          float p0 = ptx::ex2(arg.x), p1 = ptx::ex2(arg.y);
+          if constexpr (decltype(masked)::value) {
+            if (krel + t > r) p0 = 0.f;
+            if (krel + t + 1 > r) p1 = 0.f;
+          }
+          const float2 ds = tc::unpk2(tc::mul2(tc::pk2f(p0, p1), tc::add2(tc::pk2(pv[t], pv[t + 1]), nD2)));
+          dsk[t >> 1] = ptx::pack_bf16(ds.x, ds.y);
+          if constexpr (GP) {
+            pk[t >> 1] = ptx::pack_bf16(p0, p1);
+            accR = tc::add2(accR, tc::bf2_to_f2(dsk[t >> 1]));
+            accP = tc::add2(accP, tc::bf2_to_f2(pk[t >> 1]));
+          }
         }
-      }
+      };
+      if (krel + 31 > 0)  // the causal mask reaches into this thread's columns
+        block(std::true_type{});
+      else
+        block(std::false_type{});
       ptx::tmem_st16(tmem + Lay::cdS + b * (BN / 2) + c0 / 2 + lo, dsk);
       if constexpr (GP) ptx::tmem_st16(tmem + Lay::cP + b * (BN / 2) + c0 / 2 + lo, pk);
       ptx::tmem_wait_st();
@@ -234,8 +254,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     float rho = 0.f;
     if constexpr (GP) {
-      red[2 * BM + hf * BM + r] = racc2[0] + racc2[1];
-      red[4 * BM + hf * BM + r] = sp2[0] + sp2[1];
+      const float2 vr = tc::unpk2(accR), vp = tc::unpk2(accP);
+      red[2 * BM + hf * BM + r] = vr.x + vr.y;
+      red[4 * BM + hf * BM + r] = vp.x + vp.y;
       tc::named_sync(1, kCompute);
       rho = (red[2 * BM + r] + red[3 * BM + r]) / (red[4 * BM + r] + red[5 * BM + r]);
     }
@@ -263,14 +284,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int u = 0; u < 4; ++u) dst[u] = make_uint4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
       }
     }
-    if (live && hf == 0) ws[static_cast<size_t>(bh) * N + row] = make_float4(L2, Dr, rho, 0.f);
+    if (live && hf == 0) {  // row statistics, negated, pair-interleaved (see the column pass)
+      float* wf = reinterpret_cast<float*>(ws) + static_cast<size_t>(bh) * Np * 4;
+      const int64_t k2 = row & ~static_cast<int64_t>(1);
+      const int odd = static_cast<int>(row & 1);
+      wf[k2 * 4 + odd] = -L2;
+      wf[k2 * 4 + 2 + odd] = -Dr;
+      wf[(k2 + 1) * 4 + odd] = -rho;
+      wf[(k2 + 1) * 4 + 2 + odd] = 0.f;
+    }
   }
 
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 9) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, 512);
+    ptx::tmem_dealloc(tmem, Lay::kTmem);
   }
 }
 
@@ -411,6 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lo = static_cast<uint32_t>(qd * 32) << 16;
     const int key = kb * BM + r;
     const int c0 = hf * (BN / 2);
+    const uint64_t c2 = tc::pk2f(c, c);
     for (int t = 0; t < ntile; ++t) {
       const int s = t % NS, b = t % NB, i = i0 + t;
       wait(&s_full[b], (t / NB) & 1);
@@ -419,20 +449,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tmem_ld32(tmem + Lay::cS + b * BN + c0 + lo, sv);
       ptx::tmem_ld32(tmem + Lay::cdP + b * BN + c0 + lo, pv);
       ptx::tmem_wait_ld();
+      // Row statistics of the 64 queries, pair-interleaved: float4 2m = (-L2, -L2', -D, -D'),
+      // float4 2m+1 = (-rho, -rho', 0, 0) of queries 2m, 2m+1 of the block.
       const float4* st = reinterpret_cast<const float4*>(sm + Lay::oSt + s * Lay::kStat) + c0;
       const int qbase = i * BN + c0;
       uint32_t pk[16], dk[16], gk[16];
+      auto block = [&](auto masked) {
 #pragma unroll
-      for (int u = 0; u < 32; u += 2) {
-        const float4 a0 = st[u], a1 = st[u + 1];  // (L log2 e, D, rho, 0) of queries qbase+u, +u+1
-        const bool m0 = (qbase + u < key) || (qbase + u >= N);
-        const bool m1 = (qbase + u + 1 < key) || (qbase + u + 1 >= N);
-        const float p0 = m0 ? 0.f : ptx::ex2(fmaf(f(sv[u]), c, -a0.x));
-        const float p1 = m1 ? 0.f : ptx::ex2(fmaf(f(sv[u + 1]), c, -a1.x));
-        pk[u >> 1] = ptx::pack_bf16(p0, p1);
-        dk[u >> 1] = ptx::pack_bf16(p0 * (f(pv[u]) - a0.y), p1 * (f(pv[u + 1]) - a1.y));
-        if constexpr (GP) gk[u >> 1] = ptx::pack_bf16(-a0.z * bf16_lo(pk[u >> 1]), -a1.z * bf16_hi(pk[u >> 1]));
-      }
+        for (int u = 0; u < 32; u += 2) {
+          const float4 A = st[u];
+          const float2 arg = tc::unpk2(tc::fma2(tc::pk2(sv[u], sv[u + 1]), c2, tc::pk2f(A.x, A.y)));
+          float p0 = ptx::ex2(arg.x), p1 = ptx::ex2(arg.y);
+          if constexpr (decltype(masked)::value) {
+            const int q0 = qbase + u;
+            if (q0 < key || q0 >= N) p0 = 0.f;
+            if (q0 + 1 < key || q0 + 1 >= N) p1 = 0.f;
+          }
+          const float2 ds =
+              tc::unpk2(tc::mul2(tc::pk2f(p0, p1), tc::add2(tc::pk2(pv[u], pv[u + 1]), tc::pk2f(A.z, A.w))));
+          pk[u >> 1] = ptx::pack_bf16(p0, p1);
+          dk[u >> 1] = ptx::pack_bf16(ds.x, ds.y);
+          if constexpr (GP) {
+            const float4 Bs = st[u + 1];
+            const float2 g = tc::unpk2(tc::mul2(tc::pk2f(Bs.x, Bs.y), tc::bf2_to_f2(pk[u >> 1])));
+            gk[u >> 1] = ptx::pack_bf16(g.x, g.y);
+          }
+        }
+      };
+      if (qbase < kb * BM + BM || qbase + 32 > N)  // causal mask (first blocks) or past N (last block)
+        block(std::true_type{});
+      else
+        block(std::false_type{});
       ptx::tmem_st16(tmem + Lay::cP + b * (BN / 2) + c0 / 2 + lo, pk);
       ptx::tmem_st16(tmem + Lay::cdS + b * (BN / 2) + c0 / 2 + lo, dk);
       if constexpr (GP) ptx::tmem_st16(tmem + Lay::cG + b * (BN / 2) + c0 / 2 + lo, gk);
@@ -480,12 +527,12 @@ template <int D, int NBR, int NBC, bool GP>
 cudaError_t launch(const Problem& p, const void* Q, const void* K, const void* V, const void* O, const void* dO,
                    const float* lse, void* dQ, void* dK, void* dV, float4* ws, int passes, cudaStream_t st) {
   alignas(64) CUtensorMap q128, do128, k64, v64, k128, v128, q64, do64, s64;
-  const int64_t N = p.N, BH = p.BH;
+  const int64_t N = p.N, BH = p.BH, Np = (p.N + 1) & ~static_cast<int64_t>(1);
   if (!make_tmap_bf16(&q128, Q, N, D, BH, BM) || !make_tmap_bf16(&do128, dO, N, D, BH, BM) ||
       !make_tmap_bf16(&k64, K, N, D, BH, BN) || !make_tmap_bf16(&v64, V, N, D, BH, BN) ||
       !make_tmap_bf16(&k128, K, N, D, BH, BM) || !make_tmap_bf16(&v128, V, N, D, BH, BM) ||
       !make_tmap_bf16(&q64, Q, N, D, BH, BN) || !make_tmap_bf16(&do64, dO, N, D, BH, BN) ||
-      !make_tmap_stats(&s64, ws, N, BH, BN))
+      !make_tmap_stats(&s64, ws, Np, BH, BN))
     return cudaErrorInvalidValue;
   const float c = p.scale * kLog2e;
   const int nrb = static_cast<int>((N + BM - 1) / BM);
@@ -496,7 +543,8 @@ cudaError_t launch(const Problem& p, const void* Q, const void* K, const void* V
     if (e != cudaSuccess) return e;
     kern<<<static_cast<unsigned>(nrb * BH), kThreads, Lay::bytes, st>>>(
         q128, do128, k64, v64, static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), lse,
-        static_cast<__nv_bfloat16*>(dQ), ws, static_cast<int>(N), nrb, static_cast<int>(BH), p.scale, c);
+        static_cast<__nv_bfloat16*>(dQ), ws, static_cast<int>(N), static_cast<int>(Np), nrb, static_cast<int>(BH),
+        p.scale, c);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (passes & 2) {
@@ -519,7 +567,7 @@ cudaError_t tc_bwd(const Problem& p, const void* Q, const void* K, const void* V
                    cudaStream_t st) {
   if (p.d == 64)
     return gproj ? launch<64, 2, 1, true>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st)
-                 : launch<64, 2, 2, false>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st);
+                 : launch<64, 1, 2, false>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st);
   return gproj ? launch<128, 1, 1, true>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st)
                : launch<128, 2, 1, false>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st);
 }

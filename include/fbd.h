@@ -89,9 +89,9 @@ typedef struct {
 attn_status_t attn_fwd(const attn_desc_t* desc, const void* Q, const void* K, const void* V,
                        void* O, float* lse, void* stream);
 
-/* Workspace for attn_bwd: 16 bytes per (b,h,row) = one float4 of row statistics
- * (lse, D, GProj coefficient, 0) written by the row pass and read by the column
- * pass. */
+/* Workspace for attn_bwd: 16 bytes per (b,h,row), the rows of each slice rounded
+ * up to an even count: the row statistics (lse, D, GProj coefficient) written by
+ * the row pass and read by the column pass (layout internal to the library). */
 size_t attn_bwd_workspace_bytes(const attn_desc_t* desc, int gproj);
 
 /* Recompute backward.  [FA] "Backward pass: recompute instead of store": P is
