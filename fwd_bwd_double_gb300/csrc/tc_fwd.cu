@@ -206,25 +206,24 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
       l *= alpha;
       m = m_new;
       // p = 2^((s - m) s log2 e): subtract first, then scale (masked entries are -inf -> 0).
-      float rs8[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) rs8[u] = 0.f;
+      // Packed f32x2: (s - m) then * s log2 e for two keys per instruction.
+      const uint64_t nm2 = tc::pk2f(-m, -m), c2 = tc::pk2f(scale_log2, scale_log2);
+      uint64_t rs4[4] = {0, 0, 0, 0};
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
         uint32_t pk[16];
 #pragma unroll
         for (int t = 0; t < 32; t += 2) {
-          const float p0 = ptx::ex2((__uint_as_float(v[ch][t]) - m) * scale_log2);
-          const float p1 = ptx::ex2((__uint_as_float(v[ch][t + 1]) - m) * scale_log2);
-          rs8[t & 7] += p0;
-          rs8[(t + 1) & 7] += p1;
+          const float2 arg = tc::unpk2(tc::mul2(tc::add2(tc::pk2(v[ch][t], v[ch][t + 1]), nm2), c2));
+          const float p0 = ptx::ex2(arg.x), p1 = ptx::ex2(arg.y);
+          const uint64_t P2 = tc::pk2f(p0, p1);
+          rs4[(t >> 1) & 3] = tc::add2(rs4[(t >> 1) & 3], P2);
           pk[t >> 1] = ptx::pack_bf16(p0, p1);
         }
         ptx::tmem_st16(tP + lane_off + ch * 16, pk);  // keys ch*32 .. ch*32+31
       }
-      float rs = 0.f;
-#pragma unroll
-      for (int u = 0; u < 8; ++u) rs += rs8[u];
+      const float2 rsa = tc::unpk2(tc::add2(tc::add2(rs4[0], rs4[1]), tc::add2(rs4[2], rs4[3])));
+      const float rs = rsa.x + rsa.y;
       if (__any_sync(0xffffffffu, moved)) {  // rescale O for rows whose max moved
 #pragma unroll
         for (int ch = 0; ch < D / 32; ++ch) {
