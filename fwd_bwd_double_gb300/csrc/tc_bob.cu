@@ -6,8 +6,9 @@
 // dS = P * (dP - D), W = G * dS + P * H, the two per-row scalar states are
 //   E_i = sum_j P_ij G_ij   and   F_i = F'_i - E_i D_i,  F'_i = sum_j W_ij.
 // Row pass (CTA holds 128 query rows; 64-key blocks j <= i stream past):
-//   tiles   [S | Q b^T] = Q [K_j; b_j]^T,  G += a K_j^T,  [dP | H] = dO [V_j; c_j]^T
-//   outputs X += P c_j + (P G) V_j,  Y += dS b_j + W K_j,  Z += dS K_j,  U += P K_j
+//   tiles   [Q b^T | S] = Q [b_j; K_j]^T,  G += a K_j^T,  [H | dP] = dO [c_j; V_j]^T
+//   outputs [X | U] += P [c_j | K_j],  X += (P G) V_j,  [Y | Z] += dS [b_j | K_j],
+//           Y += W K_j   (128-wide products wherever two share an A operand)
 //   end     gdO = X - E O,  gQ = s (Y - E Z - F' U); row states (L log2 e, D, E, F)
 // (the corrections after the finished row are linear in E and F', so they are
 // applied once per row: "partial sums accumulated early, corrected after").
@@ -77,11 +78,17 @@ struct RowLay {
   static constexpr int oQ = 0, odO = kHeld, oA = 2 * kHeld;
   static constexpr int oOp = 3 * kHeld;          // P^, (PG)^, dS^, W^: 4 x (128 rows x 64 keys) bf16
   static constexpr int oStage = oOp + 4 * kHeld;
-  static constexpr int kStage = 4 * kTile;       // [K_j; b_j] then [V_j; c_j]
+  // One stage: c_j, V_j, b_j, K_j (8 KB each).  [c_j; V_j] and [b_j; K_j] are the
+  // 128-row B operands of the tile products; K_j sits at a fixed positive offset
+  // from c_j and from b_j, so [c_j | K_j] and [b_j | K_j] are 128-wide MN-major B
+  // operands of the output products (two 64-column slabs, leading offset = gap).
+  static constexpr int kStage = 4 * kTile;
+  static constexpr int oc = 0, oV = kTile, ob = 2 * kTile, oKs = 3 * kTile;
   static constexpr int oRed = oStage + NS * kStage;
   static constexpr int oBar = oRed + 12 * BM * 4;
   static constexpr int bytes = oBar + 256;
-  static constexpr int cSG = 0, cPH = 128, cX = 256, cY = 320, cZ = 384, cU = 448;
+  // TMEM: [G | S] (Q b^T + a K^T, then Q K^T), [H | dP], [X | U], [Y | Z].
+  static constexpr int cG = 0, cS = 64, cH = 128, cdP = 192, cX = 256, cU = 320, cY = 384, cZ = 448;
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -154,10 +161,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j >= NS) wait(&empty[s], ((j / NS) - 1) & 1);
         uint8_t* st = sm + Lay::oStage + s * Lay::kStage;
         ptx::mbar_expect_tx(&full[s], 4 * kTile);
-        ptx::tma_load_3d(st, &tmK, &full[s], 0, j * BN, bh);
-        ptx::tma_load_3d(st + kTile, &tmB, &full[s], 0, j * BN, bh);
-        ptx::tma_load_3d(st + 2 * kTile, &tmV, &full[s], 0, j * BN, bh);
-        ptx::tma_load_3d(st + 3 * kTile, &tmC, &full[s], 0, j * BN, bh);
+        ptx::tma_load_3d(st + Lay::oc, &tmC, &full[s], 0, j * BN, bh);
+        ptx::tma_load_3d(st + Lay::oV, &tmV, &full[s], 0, j * BN, bh);
+        ptx::tma_load_3d(st + Lay::ob, &tmB, &full[s], 0, j * BN, bh);
+        ptx::tma_load_3d(st + Lay::oKs, &tmK, &full[s], 0, j * BN, bh);
       }
       for (int j = (nkv > NS ? nkv - NS : 0); j < nkv; ++j) wait(&empty[j % NS], (j / NS) & 1);
     }
@@ -166,12 +173,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id128 = ptx::idesc_bf16(BM, 2 * BN, 0, 0);
       constexpr uint32_t id64 = ptx::idesc_bf16(BM, BN, 0, 0);
       constexpr uint32_t idO = ptx::idesc_bf16(BM, D, 0, 1);
+      constexpr uint32_t idO2 = ptx::idesc_bf16(BM, 2 * D, 0, 1);
       const uint32_t sQ = ptx::smem_u32(sm + Lay::oQ), sdO = ptx::smem_u32(sm + Lay::odO);
       const uint32_t sA = ptx::smem_u32(sm + Lay::oA), sSt = ptx::smem_u32(sm + Lay::oStage);
       const uint32_t sOp = ptx::smem_u32(sm + Lay::oOp);
       auto outputs = [&](int j) {  // X, Y, Z, U += block j's operands x its streamed tiles
         const int s = j % NS;
-        const uint32_t kt = sSt + s * Lay::kStage, bt = kt + kTile, vt = kt + 2 * kTile, ct = kt + 3 * kTile;
+        const uint32_t st = sSt + s * Lay::kStage;
+        const uint32_t ct = st + Lay::oc, vt = st + Lay::oV, bt = st + Lay::ob, kt = st + Lay::oKs;
         wait(ready, j & 1);
         ptx::tc_fence_after();
 #pragma unroll
@@ -179,14 +188,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t acc = (j > 0 || k > 0) ? 1u : 0u;
           const uint64_t aP = tc::kmajor_desc(sOp, BM, k), aPG = tc::kmajor_desc(sOp + kHeld, BM, k);
           const uint64_t adS = tc::kmajor_desc(sOp + 2 * kHeld, BM, k), aW = tc::kmajor_desc(sOp + 3 * kHeld, BM, k);
-          const uint64_t dK = tc::mnmajor_desc(kt, BN, k), dB = tc::mnmajor_desc(bt, BN, k);
-          const uint64_t dV = tc::mnmajor_desc(vt, BN, k), dC = tc::mnmajor_desc(ct, BN, k);
-          ptx::mma_ss(tmem + Lay::cX, aP, dC, idO, acc);
-          ptx::mma_ss(tmem + Lay::cX, aPG, dV, idO, 1u);
-          ptx::mma_ss(tmem + Lay::cY, adS, dB, idO, acc);
-          ptx::mma_ss(tmem + Lay::cY, aW, dK, idO, 1u);
-          ptx::mma_ss(tmem + Lay::cZ, adS, dK, idO, acc);
-          ptx::mma_ss(tmem + Lay::cU, aP, dK, idO, acc);
+          // [X | U] += P [c | K],  X += (PG) V,  [Y | Z] += dS [b | K],  Y += W K
+          ptx::mma_ss(tmem + Lay::cX, aP, ptx::sdesc_sw128(ct + k * 16 * 128, Lay::oKs - Lay::oc, 1024), idO2, acc);
+          ptx::mma_ss(tmem + Lay::cX, aPG, tc::mnmajor_desc(vt, BN, k), idO, 1u);
+          ptx::mma_ss(tmem + Lay::cY, adS, ptx::sdesc_sw128(bt + k * 16 * 128, Lay::oKs - Lay::ob, 1024), idO2, acc);
+          ptx::mma_ss(tmem + Lay::cY, aW, tc::mnmajor_desc(kt, BN, k), idO, 1u);
         }
         ptx::mma_commit(&empty[s]);
         ptx::mma_commit(out_done);
@@ -194,20 +200,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait(q_full, 0);
       for (int j = 0; j < nkv; ++j) {
         const int s = j % NS;
-        const uint32_t kb = sSt + s * Lay::kStage;  // [K_j; b_j]
-        const uint32_t vc = kb + 2 * kTile;          // [V_j; c_j]
+        const uint32_t st = sSt + s * Lay::kStage;
+        const uint32_t bk = st + Lay::ob;  // [b_j; K_j]
+        const uint32_t cv = st + Lay::oc;  // [c_j; V_j]
         wait(&full[s], (j / NS) & 1);
         if (j > 0) wait(consumed, (j - 1) & 1);  // tiles of block j-1 copied out of TMEM
         ptx::tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          ptx::mma_ss(tmem + Lay::cSG, tc::kmajor_desc(sQ, BM, kk), tc::kmajor_desc(kb, 2 * BN, kk), id128, kk > 0);
+          ptx::mma_ss(tmem + Lay::cG, tc::kmajor_desc(sQ, BM, kk), tc::kmajor_desc(bk, 2 * BN, kk), id128, kk > 0);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          ptx::mma_ss(tmem + Lay::cSG + BN, tc::kmajor_desc(sA, BM, kk), tc::kmajor_desc(kb, BN, kk), id64, 1u);
+          ptx::mma_ss(tmem + Lay::cG, tc::kmajor_desc(sA, BM, kk), tc::kmajor_desc(bk + kTile, BN, kk), id64, 1u);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          ptx::mma_ss(tmem + Lay::cPH, tc::kmajor_desc(sdO, BM, kk), tc::kmajor_desc(vc, 2 * BN, kk), id128, kk > 0);
+          ptx::mma_ss(tmem + Lay::cH, tc::kmajor_desc(sdO, BM, kk), tc::kmajor_desc(cv, 2 * BN, kk), id128, kk > 0);
         ptx::mma_commit(s_full);
         if (j > 0) outputs(j - 1);
       }
@@ -251,10 +258,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait(s_full, j & 1);
       ptx::tc_fence_after();
       uint32_t sv[32], gv[32], dv[32], hv[32];
-      ptx::tmem_ld32(tmem + Lay::cSG + c0 + lo, sv);
-      ptx::tmem_ld32(tmem + Lay::cSG + BN + c0 + lo, gv);
-      ptx::tmem_ld32(tmem + Lay::cPH + c0 + lo, dv);
-      ptx::tmem_ld32(tmem + Lay::cPH + BN + c0 + lo, hv);
+      ptx::tmem_ld32(tmem + Lay::cS + c0 + lo, sv);
+      ptx::tmem_ld32(tmem + Lay::cG + c0 + lo, gv);
+      ptx::tmem_ld32(tmem + Lay::cdP + c0 + lo, dv);
+      ptx::tmem_ld32(tmem + Lay::cH + c0 + lo, hv);
       ptx::tmem_wait_ld();
       ptx::tc_fence_before();
       ptx::mbar_arrive(consumed);  // the MMA warp may now overwrite the tile columns
