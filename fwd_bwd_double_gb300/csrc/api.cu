@@ -226,7 +226,8 @@ attn_status_t attn_bwd_projected_dS(const attn_desc_t* desc, const void* Q, cons
 attn_status_t attn_device_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "CUDA: %s", cudaGetErrorString(e));
-  const uint32_t flags = fbd::tc_fwd_take_error() | fbd::tc_bwd_take_error() | fbd::tc_bob_take_error();
+  const uint32_t flags = fbd::tc_fwd_take_error() | fbd::tc_bwd_take_error() | fbd::tc_bwd_wide_take_error() |
+                         fbd::tc_bob_take_error();
   if (flags != 0) return fail(ATTN_ERR_TIMEOUT, "a device-side bounded wait gave up%s");
   return ATTN_OK;
 }

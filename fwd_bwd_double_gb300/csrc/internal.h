@@ -35,6 +35,10 @@ cudaError_t tc_fwd(const Problem& p, const void* Q, const void* K, const void* V
 cudaError_t tc_bwd(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
                    const void* dO, const float* lse, void* dQ, void* dK, void* dV, int gproj, float4* ws,
                    int passes, cudaStream_t st);
+// d = 64 without GProj: the 128-wide backward kernels (tc_bwd_wide.cu).
+cudaError_t tc_bwd_wide(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
+                        const void* dO, const float* lse, void* dQ, void* dK, void* dV, float4* ws, int passes,
+                        cudaStream_t st);
 cudaError_t tc_bob(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
                    const void* dO, const float* lse, const void* a, const void* b, const void* c, void* gQ,
                    void* gK, void* gV, void* gdO, float4* ws, int passes, cudaStream_t st);
@@ -47,6 +51,7 @@ bool tc_supports(int op, int64_t d);  // op: 0 fwd, 1 bwd, 2 bob
 // Device status words (bit FBD_ERR_TIMEOUT), read-and-cleared per translation unit.
 uint32_t tc_fwd_take_error();
 uint32_t tc_bwd_take_error();
+uint32_t tc_bwd_wide_take_error();
 uint32_t tc_bob_take_error();
 
 // Record `msg` as the calling thread's attn_last_error() detail; returns s.

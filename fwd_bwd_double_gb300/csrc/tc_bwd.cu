@@ -567,7 +567,7 @@ cudaError_t tc_bwd(const Problem& p, const void* Q, const void* K, const void* V
                    cudaStream_t st) {
   if (p.d == 64)
     return gproj ? launch<64, 2, 1, true>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st)
-                 : launch<64, 1, 2, false>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st);
+                 : tc_bwd_wide(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st);
   return gproj ? launch<128, 1, 1, true>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st)
                : launch<128, 2, 1, false>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st);
 }

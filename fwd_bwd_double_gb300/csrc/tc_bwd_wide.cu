@@ -1,0 +1,483 @@
+// bf16 causal attention backward, d = 64, no GProj: the row pass (dQ) and the
+// column pass (dK, dV) with 128-wide score tiles.
+//
+// Same mathematics as tc_bwd.cu ("Flash attention for trading models",
+// "Backward pass: recompute instead of store"): P = 2^(S s log2 e - L log2 e),
+// dP = dO V^T, dS = P (dP - D); dQ = s dS K, dK = s dS^T Q, dV = P^T dO, each
+// output block written once.  What differs is the shape of the work: both the
+// held and the streamed blocks are 128 rows, so every score-tile MMA is
+// M = N = 128 (a 64-wide MMA takes about 70 % longer per flop on this GPU), and
+// the tiles live in TMEM single-buffered, released early:
+//   - the compute warps copy their slice of the S and dP tiles into registers and
+//     arrive on `consumed`; the MMA warp may then compute the next block's tiles
+//     into the same columns while the CUDA cores work on this block;
+//   - the bf16 operands (dS, and P in the column pass) have their own TMEM
+//     columns, rewritten only after the previous block's products have read them
+//     (`out_done`).
+// Warps 0-15 compute (warp w: TMEM lanes 32(w%4).., tile columns 32(w/4)..),
+// warp 16 issues TMA loads, warp 17 allocates TMEM and issues the MMAs.
+#include <cuda_bf16.h>
+
+#include <type_traits>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "tc_common.cuh"
+
+namespace fbd {
+namespace {
+
+__device__ unsigned int g_err = 0;
+
+constexpr int D = 64;
+constexpr int BW = 128;        // held and streamed block rows
+constexpr int NS = 4;          // stages of streamed blocks
+constexpr int kCW = 16;        // compute warps
+constexpr int kCompute = kCW * 32;
+constexpr int kThreads = kCompute + 64;
+constexpr int kC = 32;         // tile columns per compute thread (128 / 4 column groups)
+constexpr int DG = D / 4;      // output columns per compute thread
+constexpr int kTile = BW * D * 2;  // 16 KB
+constexpr float kLog2e = 1.4426950408889634f;
+
+using tc::bf16_hi;
+using tc::bf16_lo;
+
+// Shared boilerplate: barriers, TMEM allocation, bounded waits.
+struct Sync {
+  uint64_t* held_full;
+  uint64_t* full;
+  uint64_t* empty;
+  uint64_t* s_full;
+  uint64_t* consumed;
+  uint64_t* ready;
+  uint64_t* out_done;
+  uint64_t* acc_full;
+  uint32_t* tmem_slot;
+  volatile int* abort_flag;
+  __device__ Sync(uint8_t* base) {
+    held_full = reinterpret_cast<uint64_t*>(base);
+    full = held_full + 1;
+    empty = full + NS;
+    s_full = empty + NS;
+    consumed = s_full + 1;
+    ready = consumed + 1;
+    out_done = ready + 1;
+    acc_full = out_done + 1;
+    tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+    abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  }
+  __device__ void init(const uint8_t* sm) {
+    ptx::mbar_init(held_full, 1);
+    for (int s = 0; s < NS; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    ptx::mbar_init(s_full, 1);
+    ptx::mbar_init(consumed, kCompute);
+    ptx::mbar_init(ready, kCompute);
+    ptx::mbar_init(out_done, 1);
+    ptx::mbar_init(acc_full, 1);
+    *abort_flag = (ptx::smem_u32(sm) & 1023u) ? 1 : 0;
+    if (*abort_flag) atomicOr(&g_err, FBD_ERR_TIMEOUT);
+    ptx::fence_mbar_init();
+  }
+};
+
+// ================================================================ row pass
+struct RowLay {
+  static constexpr int oQ = 0, odO = kTile, oK = 2 * kTile, oV = oK + NS * kTile;
+  static constexpr int oRed = oV + NS * kTile;  // float [4][BW]
+  static constexpr int oBar = oRed + 4 * BW * 4;
+  static constexpr int bytes = oBar + 256;
+  static constexpr int cS = 0, cdP = 128, cdS = 256, cdQ = 320;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_row_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
+               const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+               const __nv_bfloat16* __restrict__ O, const __nv_bfloat16* __restrict__ dO,
+               const float* __restrict__ lse, __nv_bfloat16* __restrict__ dQ, float4* __restrict__ ws, int N, int Np,
+               int nrb, int BH, float scale, float c) {
+  using Lay = RowLay;
+  extern __shared__ __align__(1024) uint8_t sm[];
+  Sync sy(sm + Lay::oBar);
+  float* red = reinterpret_cast<float*>(sm + Lay::oRed);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const tc::Order ord = tc::grid_order(BH, nrb);
+  const int bh = ord.bh;
+  const int rb = nrb - 1 - ord.k;  // heaviest first within a group of slices
+  const int nkv = rb + 1;          // 128-key blocks j <= rb
+
+  if (threadIdx.x == 0) sy.init(sm);
+  if (warp == kCW + 1) {
+    ptx::tmem_alloc(sy.tmem_slot, 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *sy.tmem_slot;
+  const ptx::BoundedWait wait{sy.abort_flag, &g_err};
+  const bool ok = *sy.abort_flag == 0;
+
+  if (warp == kCW) {
+    if (lane == 0 && ok) {
+      ptx::prefetch_tmap(&tmK);
+      ptx::prefetch_tmap(&tmV);
+      ptx::mbar_expect_tx(sy.held_full, 2 * kTile);
+      ptx::tma_load_3d(sm + Lay::oQ, &tmQ, sy.held_full, 0, rb * BW, bh);
+      ptx::tma_load_3d(sm + Lay::odO, &tmdO, sy.held_full, 0, rb * BW, bh);
+      for (int j = 0; j < nkv; ++j) {
+        const int s = j % NS;
+        if (j >= NS) wait(&sy.empty[s], ((j / NS) - 1) & 1);
+        ptx::mbar_expect_tx(&sy.full[s], 2 * kTile);
+        ptx::tma_load_3d(sm + Lay::oK + s * kTile, &tmK, &sy.full[s], 0, j * BW, bh);
+        ptx::tma_load_3d(sm + Lay::oV + s * kTile, &tmV, &sy.full[s], 0, j * BW, bh);
+      }
+      for (int j = (nkv > NS ? nkv - NS : 0); j < nkv; ++j) wait(&sy.empty[j % NS], (j / NS) & 1);
+    }
+  } else if (warp == kCW + 1) {
+    if (lane == 0 && ok) {
+      constexpr uint32_t idS = ptx::idesc_bf16(BW, BW, 0, 0);
+      constexpr uint32_t idQ = ptx::idesc_bf16(BW, D, 0, 1);
+      const uint32_t sQ = ptx::smem_u32(sm + Lay::oQ), sdO = ptx::smem_u32(sm + Lay::odO);
+      const uint32_t sK = ptx::smem_u32(sm + Lay::oK), sV = ptx::smem_u32(sm + Lay::oV);
+      auto products = [&](int t) {  // dQ += dS_t K_t, then release the stage and the dS columns
+        const int s = t % NS;
+        wait(sy.ready, t & 1);
+        ptx::tc_fence_after();
+        const uint32_t kt = sK + s * kTile;
+#pragma unroll
+        for (int k = 0; k < BW / 16; ++k)
+          ptx::mma_ts(tmem + Lay::cdQ, tmem + Lay::cdS + k * 8, tc::mnmajor_desc(kt, BW, k), idQ, (t > 0 || k > 0));
+        ptx::mma_commit(&sy.empty[s]);
+        ptx::mma_commit(sy.out_done);
+      };
+      wait(sy.held_full, 0);
+      for (int j = 0; j < nkv; ++j) {
+        const int s = j % NS;
+        wait(&sy.full[s], (j / NS) & 1);
+        if (j > 0) wait(sy.consumed, (j - 1) & 1);  // tiles of block j-1 are in registers
+        ptx::tc_fence_after();
+        const uint32_t kt = sK + s * kTile, vt = sV + s * kTile;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          ptx::mma_ss(tmem + Lay::cS, tc::kmajor_desc(sQ, BW, kk), tc::kmajor_desc(kt, BW, kk), idS, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          ptx::mma_ss(tmem + Lay::cdP, tc::kmajor_desc(sdO, BW, kk), tc::kmajor_desc(vt, BW, kk), idS, kk > 0);
+        ptx::mma_commit(sy.s_full);
+        if (j > 0) products(j - 1);
+      }
+      products(nkv - 1);
+      ptx::mma_commit(sy.acc_full);
+    }
+  } else {
+    const int qd = warp & 3, cg = warp >> 2;
+    const int r = qd * 32 + lane;
+    const uint32_t lo = static_cast<uint32_t>(qd * 32) << 16;
+    const int64_t row = static_cast<int64_t>(rb) * BW + r;
+    const bool live = row < N;
+    const size_t rowoff = (static_cast<size_t>(bh) * N + row) * D;
+    float part = 0.f;
+    if (live) {  // this thread's quarter of D_r = dO_r . O_r
+      const uint4* po = reinterpret_cast<const uint4*>(O + rowoff + cg * DG);
+      const uint4* pg = reinterpret_cast<const uint4*>(dO + rowoff + cg * DG);
+#pragma unroll
+      for (int u = 0; u < DG / 8; ++u) {
+        const uint4 a = po[u], g = pg[u];
+        const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) part += bf16_lo(aw[e]) * bf16_lo(gw[e]) + bf16_hi(aw[e]) * bf16_hi(gw[e]);
+      }
+    }
+    red[cg * BW + r] = part;
+    tc::named_sync(1, kCompute);
+    const float Dr = red[r] + red[BW + r] + red[2 * BW + r] + red[3 * BW + r];
+    const float L2 = live ? lse[static_cast<size_t>(bh) * N + row] * kLog2e : 0.f;
+    const uint64_t c2 = tc::pk2f(c, c), nL2 = tc::pk2f(-L2, -L2), nD2 = tc::pk2f(-Dr, -Dr);
+    const int c0 = cg * kC;
+    for (int j = 0; j < nkv; ++j) {
+      wait(sy.s_full, j & 1);
+      ptx::tc_fence_after();
+      uint32_t sv[kC], pv[kC];
+      ptx::tmem_ld32(tmem + Lay::cS + c0 + lo, sv);
+      ptx::tmem_ld32(tmem + Lay::cdP + c0 + lo, pv);
+      ptx::tmem_wait_ld();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(sy.consumed);
+      uint32_t dsk[kC / 2];
+      auto block = [&](auto masked) {
+#pragma unroll
+        for (int t = 0; t < kC; t += 2) {
+          const float2 arg = tc::unpk2(tc::fma2(tc::pk2(sv[t], sv[t + 1]), c2, nL2));
+          float p0 = ptx::ex2(arg.x), p1 = ptx::ex2(arg.y);
+          if constexpr (decltype(masked)::value) {
+            if (c0 + t > r) p0 = 0.f;  // only the diagonal block is masked: key - row = column - lane row
+            if (c0 + t + 1 > r) p1 = 0.f;
+          }
+          const float2 ds = tc::unpk2(tc::mul2(tc::pk2f(p0, p1), tc::add2(tc::pk2(pv[t], pv[t + 1]), nD2)));
+          dsk[t >> 1] = ptx::pack_bf16(ds.x, ds.y);
+        }
+      };
+      if (j == rb)
+        block(std::true_type{});
+      else
+        block(std::false_type{});
+      if (j > 0) wait(sy.out_done, (j - 1) & 1);  // the previous block's dQ product has read dS
+      ptx::tmem_st16(tmem + Lay::cdS + c0 / 2 + lo, dsk);
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(sy.ready);
+    }
+    wait(sy.acc_full, 0);
+    ptx::tc_fence_after();
+    uint32_t a[DG];
+    ptx::tmem_ld16(tmem + Lay::cdQ + cg * DG + lo, a);
+    ptx::tmem_wait_ld();
+    if (live) {
+      uint32_t o[DG / 2];
+#pragma unroll
+      for (int t = 0; t < DG; t += 2) o[t >> 1] = ptx::pack_bf16(scale * tc::f(a[t]), scale * tc::f(a[t + 1]));
+      uint4* dst = reinterpret_cast<uint4*>(dQ + rowoff + cg * DG);
+      dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+      dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+      if (cg == 0) {  // row statistics, negated, pair-interleaved (format shared with tc_bwd.cu)
+        float* wf = reinterpret_cast<float*>(ws) + static_cast<size_t>(bh) * Np * 4;
+        const int64_t k2 = row & ~static_cast<int64_t>(1);
+        const int odd = static_cast<int>(row & 1);
+        wf[k2 * 4 + odd] = -L2;
+        wf[k2 * 4 + 2 + odd] = -Dr;
+        wf[(k2 + 1) * 4 + odd] = 0.f;
+        wf[(k2 + 1) * 4 + 2 + odd] = 0.f;
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kCW + 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+// ============================================================= column pass
+struct ColLay {
+  static constexpr int kStat = BW * 16;
+  static constexpr int kStage = 2 * kTile + kStat;  // Q_i, dO_i, statistics
+  static constexpr int oK = 0, oV = kTile, oStage = 2 * kTile;
+  static constexpr int oBar = oStage + NS * kStage;
+  static constexpr int bytes = oBar + 256;
+  static constexpr int cS = 0, cdP = 128, cP = 256, cdS = 320, cdV = 384, cdK = 448;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_col_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+               const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
+               const __grid_constant__ CUtensorMap tmSt, __nv_bfloat16* __restrict__ dK,
+               __nv_bfloat16* __restrict__ dV, int N, int nb, int BH, float scale, float c) {
+  using Lay = ColLay;
+  extern __shared__ __align__(1024) uint8_t sm[];
+  Sync sy(sm + Lay::oBar);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const tc::Order ord = tc::grid_order(BH, nb);
+  const int bh = ord.bh;
+  const int kb = ord.k;          // first key blocks have the most query blocks: first
+  const int ntile = nb - kb;     // query blocks i >= kb
+
+  if (threadIdx.x == 0) sy.init(sm);
+  if (warp == kCW + 1) {
+    ptx::tmem_alloc(sy.tmem_slot, 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *sy.tmem_slot;
+  const ptx::BoundedWait wait{sy.abort_flag, &g_err};
+  const bool ok = *sy.abort_flag == 0;
+
+  if (warp == kCW) {
+    if (lane == 0 && ok) {
+      ptx::prefetch_tmap(&tmQ);
+      ptx::prefetch_tmap(&tmdO);
+      ptx::prefetch_tmap(&tmSt);
+      ptx::mbar_expect_tx(sy.held_full, 2 * kTile);
+      ptx::tma_load_3d(sm + Lay::oK, &tmK, sy.held_full, 0, kb * BW, bh);
+      ptx::tma_load_3d(sm + Lay::oV, &tmV, sy.held_full, 0, kb * BW, bh);
+      for (int t = 0; t < ntile; ++t) {
+        const int s = t % NS, i = kb + t;
+        if (t >= NS) wait(&sy.empty[s], ((t / NS) - 1) & 1);
+        uint8_t* st = sm + Lay::oStage + s * Lay::kStage;
+        ptx::mbar_expect_tx(&sy.full[s], 2 * kTile + Lay::kStat);
+        ptx::tma_load_3d(st, &tmQ, &sy.full[s], 0, i * BW, bh);
+        ptx::tma_load_3d(st + kTile, &tmdO, &sy.full[s], 0, i * BW, bh);
+        ptx::tma_load_3d(st + 2 * kTile, &tmSt, &sy.full[s], 0, i * BW, bh);
+      }
+      for (int t = (ntile > NS ? ntile - NS : 0); t < ntile; ++t) wait(&sy.empty[t % NS], (t / NS) & 1);
+    }
+  } else if (warp == kCW + 1) {
+    if (lane == 0 && ok) {
+      constexpr uint32_t idS = ptx::idesc_bf16(BW, BW, 0, 0);
+      constexpr uint32_t idKV = ptx::idesc_bf16(BW, D, 0, 1);
+      const uint32_t sK = ptx::smem_u32(sm + Lay::oK), sV = ptx::smem_u32(sm + Lay::oV);
+      const uint32_t sSt = ptx::smem_u32(sm + Lay::oStage);
+      auto outputs = [&](int t) {  // dV += P^T dO_i, dK += dS^T Q_i
+        const int s = t % NS;
+        const uint32_t qt = sSt + s * Lay::kStage, gt = qt + kTile;
+        wait(sy.ready, t & 1);
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < BW / 16; ++k) {
+          const uint32_t acc = (t > 0 || k > 0) ? 1u : 0u;
+          ptx::mma_ts(tmem + Lay::cdV, tmem + Lay::cP + k * 8, tc::mnmajor_desc(gt, BW, k), idKV, acc);
+          ptx::mma_ts(tmem + Lay::cdK, tmem + Lay::cdS + k * 8, tc::mnmajor_desc(qt, BW, k), idKV, acc);
+        }
+        ptx::mma_commit(&sy.empty[s]);
+        ptx::mma_commit(sy.out_done);
+      };
+      wait(sy.held_full, 0);
+      for (int t = 0; t < ntile; ++t) {
+        const int s = t % NS;
+        const uint32_t qt = sSt + s * Lay::kStage, gt = qt + kTile;
+        wait(&sy.full[s], (t / NS) & 1);
+        if (t > 0) wait(sy.consumed, (t - 1) & 1);
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          ptx::mma_ss(tmem + Lay::cS, tc::kmajor_desc(sK, BW, kk), tc::kmajor_desc(qt, BW, kk), idS, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          ptx::mma_ss(tmem + Lay::cdP, tc::kmajor_desc(sV, BW, kk), tc::kmajor_desc(gt, BW, kk), idS, kk > 0);
+        ptx::mma_commit(sy.s_full);
+        if (t > 0) outputs(t - 1);
+      }
+      outputs(ntile - 1);
+      ptx::mma_commit(sy.acc_full);
+    }
+  } else {
+    const int qd = warp & 3, cg = warp >> 2;
+    const int r = qd * 32 + lane;  // key row of the held block (TMEM lane)
+    const uint32_t lo = static_cast<uint32_t>(qd * 32) << 16;
+    const int key = kb * BW + r;
+    const int c0 = cg * kC;
+    const uint64_t c2 = tc::pk2f(c, c);
+    for (int t = 0; t < ntile; ++t) {
+      const int s = t % NS, i = kb + t;
+      wait(sy.s_full, t & 1);
+      ptx::tc_fence_after();
+      uint32_t sv[kC], pv[kC];
+      ptx::tmem_ld32(tmem + Lay::cS + c0 + lo, sv);
+      ptx::tmem_ld32(tmem + Lay::cdP + c0 + lo, pv);
+      ptx::tmem_wait_ld();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(sy.consumed);
+      // Statistics of the block's queries, pair-interleaved and negated:
+      // float4 2m = (-L2, -L2', -D, -D') of queries 2m, 2m+1.
+      const float4* st = reinterpret_cast<const float4*>(sm + Lay::oStage + s * Lay::kStage + 2 * kTile) + c0;
+      const int qbase = i * BW + c0;
+      uint32_t pk[kC / 2], dk[kC / 2];
+      auto block = [&](auto masked) {
+#pragma unroll
+        for (int u = 0; u < kC; u += 2) {
+          const float4 A = st[u];
+          const float2 arg = tc::unpk2(tc::fma2(tc::pk2(sv[u], sv[u + 1]), c2, tc::pk2f(A.x, A.y)));
+          float p0 = ptx::ex2(arg.x), p1 = ptx::ex2(arg.y);
+          if constexpr (decltype(masked)::value) {
+            const int q0 = qbase + u;
+            if (q0 < key || q0 >= N) p0 = 0.f;
+            if (q0 + 1 < key || q0 + 1 >= N) p1 = 0.f;
+          }
+          const float2 ds =
+              tc::unpk2(tc::mul2(tc::pk2f(p0, p1), tc::add2(tc::pk2(pv[u], pv[u + 1]), tc::pk2f(A.z, A.w))));
+          pk[u >> 1] = ptx::pack_bf16(p0, p1);
+          dk[u >> 1] = ptx::pack_bf16(ds.x, ds.y);
+        }
+      };
+      if (t == 0 || qbase + kC > N)  // the diagonal block, or the block reaching past N
+        block(std::true_type{});
+      else
+        block(std::false_type{});
+      if (t > 0) wait(sy.out_done, (t - 1) & 1);  // the previous block's products have read P, dS
+      ptx::tmem_st16(tmem + Lay::cP + c0 / 2 + lo, pk);
+      ptx::tmem_st16(tmem + Lay::cdS + c0 / 2 + lo, dk);
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(sy.ready);
+    }
+    wait(sy.acc_full, 0);
+    ptx::tc_fence_after();
+    uint32_t a[DG], g[DG];
+    ptx::tmem_ld16(tmem + Lay::cdV + cg * DG + lo, a);
+    ptx::tmem_ld16(tmem + Lay::cdK + cg * DG + lo, g);
+    ptx::tmem_wait_ld();
+    if (key < N) {
+      const size_t rowoff = (static_cast<size_t>(bh) * N + key) * D;
+      uint32_t ov[DG / 2], okk[DG / 2];
+#pragma unroll
+      for (int u = 0; u < DG; u += 2) {
+        ov[u >> 1] = ptx::pack_bf16(tc::f(a[u]), tc::f(a[u + 1]));
+        okk[u >> 1] = ptx::pack_bf16(scale * tc::f(g[u]), scale * tc::f(g[u + 1]));
+      }
+      uint4* dv = reinterpret_cast<uint4*>(dV + rowoff + cg * DG);
+      uint4* dk2 = reinterpret_cast<uint4*>(dK + rowoff + cg * DG);
+      dv[0] = make_uint4(ov[0], ov[1], ov[2], ov[3]);
+      dv[1] = make_uint4(ov[4], ov[5], ov[6], ov[7]);
+      dk2[0] = make_uint4(okk[0], okk[1], okk[2], okk[3]);
+      dk2[1] = make_uint4(okk[4], okk[5], okk[6], okk[7]);
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kCW + 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+cudaError_t tc_bwd_wide(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
+                        const void* dO, const float* lse, void* dQ, void* dK, void* dV, float4* ws, int passes,
+                        cudaStream_t st) {
+  if (p.d != D) return cudaErrorInvalidValue;
+  alignas(64) CUtensorMap q, g, k, v, s;
+  const int64_t N = p.N, BH = p.BH, Np = (p.N + 1) & ~static_cast<int64_t>(1);
+  if (!make_tmap_bf16(&q, Q, N, D, BH, BW) || !make_tmap_bf16(&g, dO, N, D, BH, BW) ||
+      !make_tmap_bf16(&k, K, N, D, BH, BW) || !make_tmap_bf16(&v, V, N, D, BH, BW) ||
+      !make_tmap_stats(&s, ws, Np, BH, BW))
+    return cudaErrorInvalidValue;
+  const float c = p.scale * kLog2e;
+  const int nb = static_cast<int>((N + BW - 1) / BW);
+  cudaError_t e = cudaSuccess;
+  if (passes & 1) {
+    e = cudaFuncSetAttribute(bwd_row_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, RowLay::bytes);
+    if (e != cudaSuccess) return e;
+    bwd_row_wide_kernel<<<static_cast<unsigned>(nb * BH), kThreads, RowLay::bytes, st>>>(
+        q, g, k, v, static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), lse,
+        static_cast<__nv_bfloat16*>(dQ), ws, static_cast<int>(N), static_cast<int>(Np), nb, static_cast<int>(BH),
+        p.scale, c);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (passes & 2) {
+    e = cudaFuncSetAttribute(bwd_col_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ColLay::bytes);
+    if (e != cudaSuccess) return e;
+    bwd_col_wide_kernel<<<static_cast<unsigned>(nb * BH), kThreads, ColLay::bytes, st>>>(
+        k, v, q, g, s, static_cast<__nv_bfloat16*>(dK), static_cast<__nv_bfloat16*>(dV), static_cast<int>(N), nb,
+        static_cast<int>(BH), p.scale, c);
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+uint32_t tc_bwd_wide_take_error() {
+  uint32_t v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, g_err, sizeof(v)) != cudaSuccess) return 0;
+  if (v) cudaMemcpyToSymbol(g_err, &z, sizeof(z));
+  return v;
+}
+
+}  // namespace fbd
