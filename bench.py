@@ -67,7 +67,13 @@ def traffic_for(kernel, w):
 # dram__bytes_read.sum + dram__bytes_write.sum per launch (ncu, one-pass capture of
 # the bench command; see profiles/), keyed by (kernel, workload), with the source
 # hash of the kernel file the counters were taken on.
-MEASURED_TRAFFIC = {}
+MEASURED_TRAFFIC = {
+    ("fwd", "gpt2small_B4H12N8192d64"): {"bytes": 184911360, "source": "tc_fwd.cu", "sha": "59e8f8c90222fc9a"},
+    ("bwd_row", "gpt2small_B4H12N8192d64"): {"bytes": 293702400, "source": "tc_bwd_wide.cu", "sha": "ce7b8d8ec495350b"},
+    ("bwd_col", "gpt2small_B4H12N8192d64"): {"bytes": 277961728, "source": "tc_bwd_wide.cu", "sha": "ce7b8d8ec495350b"},
+    ("bob_row", "gpt2small_B4H12N8192d64"): {"bytes": 505077248, "source": "tc_bob.cu", "sha": "0e4e3713f841cd8d"},
+    ("bob_col", "gpt2small_B4H12N8192d64"): {"bytes": 438809856, "source": "tc_bob.cu", "sha": "0e4e3713f841cd8d"},
+}
 
 
 def peaks():
