@@ -169,57 +169,65 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = (nkv > NS ? nkv - NS : 0); j < nkv; ++j) wait(&empty[j % NS], (j / NS) & 1);
     }
   } else if (warp == 9) {
-    if (lane == 0 && ok) {
+    if (ok) {  // all 32 lanes; one elected lane issues each MMA and commit
       constexpr uint32_t id128 = ptx::idesc_bf16(BM, 2 * BN, 0, 0);
       constexpr uint32_t id64 = ptx::idesc_bf16(BM, BN, 0, 0);
       constexpr uint32_t idO = ptx::idesc_bf16(BM, D, 0, 1);
       constexpr uint32_t idO2 = ptx::idesc_bf16(BM, 2 * D, 0, 1);
-      const uint32_t sQ = ptx::smem_u32(sm + Lay::oQ), sdO = ptx::smem_u32(sm + Lay::odO);
-      const uint32_t sA = ptx::smem_u32(sm + Lay::oA), sSt = ptx::smem_u32(sm + Lay::oStage);
-      const uint32_t sOp = ptx::smem_u32(sm + Lay::oOp);
+      const uint32_t sSt = ptx::smem_u32(sm + Lay::oStage);
+      // Descriptors at K-step 0 of stage 0.  A K-step moves a K-major operand by 32 B
+      // and an MN-major one by 16 rows (2 KB); stage s adds s * kStage.
+      const uint64_t dQ = tc::kmajor_desc(ptx::smem_u32(sm + Lay::oQ), BM, 0);
+      const uint64_t ddO = tc::kmajor_desc(ptx::smem_u32(sm + Lay::odO), BM, 0);
+      const uint64_t dA = tc::kmajor_desc(ptx::smem_u32(sm + Lay::oA), BM, 0);
+      const uint64_t dOp = tc::kmajor_desc(ptx::smem_u32(sm + Lay::oOp), BM, 0);  // P^; + kHeld per operand
+      const uint64_t dBK = tc::kmajor_desc(sSt + Lay::ob, 2 * BN, 0);   // [b_j; K_j], K-major
+      const uint64_t dKk = tc::kmajor_desc(sSt + Lay::oKs, BN, 0);      // K_j, K-major
+      const uint64_t dCV = tc::kmajor_desc(sSt + Lay::oc, 2 * BN, 0);   // [c_j; V_j], K-major
+      const uint64_t dCK = ptx::sdesc_sw128(sSt + Lay::oc, Lay::oKs - Lay::oc, 1024);  // [c_j | K_j], MN-major
+      const uint64_t dVm = tc::mnmajor_desc(sSt + Lay::oV, BN, 0);      // V_j, MN-major
+      const uint64_t dBKm = ptx::sdesc_sw128(sSt + Lay::ob, Lay::oKs - Lay::ob, 1024);  // [b_j | K_j], MN-major
+      const uint64_t dKm = tc::mnmajor_desc(sSt + Lay::oKs, BN, 0);     // K_j, MN-major
+      const uint32_t tG = tmem + Lay::cG, tH = tmem + Lay::cH, tX = tmem + Lay::cX, tY = tmem + Lay::cY;
       auto outputs = [&](int j) {  // X, Y, Z, U += block j's operands x its streamed tiles
         const int s = j % NS;
-        const uint32_t st = sSt + s * Lay::kStage;
-        const uint32_t ct = st + Lay::oc, vt = st + Lay::oV, bt = st + Lay::ob, kt = st + Lay::oKs;
+        const uint32_t so = static_cast<uint32_t>(s * Lay::kStage);
         wait(ready, j & 1);
         ptx::tc_fence_after();
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k) {
           const uint32_t acc = (j > 0 || k > 0) ? 1u : 0u;
-          const uint64_t aP = tc::kmajor_desc(sOp, BM, k), aPG = tc::kmajor_desc(sOp + kHeld, BM, k);
-          const uint64_t adS = tc::kmajor_desc(sOp + 2 * kHeld, BM, k), aW = tc::kmajor_desc(sOp + 3 * kHeld, BM, k);
+          const uint32_t ka = 32 * k, kb = so + 2048 * k;
           // [X | U] += P [c | K],  X += (PG) V,  [Y | Z] += dS [b | K],  Y += W K
-          ptx::mma_ss(tmem + Lay::cX, aP, ptx::sdesc_sw128(ct + k * 16 * 128, Lay::oKs - Lay::oc, 1024), idO2, acc);
-          ptx::mma_ss(tmem + Lay::cX, aPG, tc::mnmajor_desc(vt, BN, k), idO, 1u);
-          ptx::mma_ss(tmem + Lay::cY, adS, ptx::sdesc_sw128(bt + k * 16 * 128, Lay::oKs - Lay::ob, 1024), idO2, acc);
-          ptx::mma_ss(tmem + Lay::cY, aW, tc::mnmajor_desc(kt, BN, k), idO, 1u);
+          ptx::mma_ss_e(tX, tc::desc_add(dOp, ka), tc::desc_add(dCK, kb), idO2, acc);
+          ptx::mma_ss_e(tX, tc::desc_add(dOp, kHeld + ka), tc::desc_add(dVm, kb), idO, 1u);
+          ptx::mma_ss_e(tY, tc::desc_add(dOp, 2 * kHeld + ka), tc::desc_add(dBKm, kb), idO2, acc);
+          ptx::mma_ss_e(tY, tc::desc_add(dOp, 3 * kHeld + ka), tc::desc_add(dKm, kb), idO, 1u);
         }
-        ptx::mma_commit(&empty[s]);
-        ptx::mma_commit(out_done);
+        ptx::mma_commit_e(&empty[s]);
+        ptx::mma_commit_e(out_done);
       };
       wait(q_full, 0);
       for (int j = 0; j < nkv; ++j) {
         const int s = j % NS;
-        const uint32_t st = sSt + s * Lay::kStage;
-        const uint32_t bk = st + Lay::ob;  // [b_j; K_j]
-        const uint32_t cv = st + Lay::oc;  // [c_j; V_j]
+        const uint32_t so = static_cast<uint32_t>(s * Lay::kStage);
         wait(&full[s], (j / NS) & 1);
         if (j > 0) wait(consumed, (j - 1) & 1);  // tiles of block j-1 copied out of TMEM
         ptx::tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          ptx::mma_ss(tmem + Lay::cG, tc::kmajor_desc(sQ, BM, kk), tc::kmajor_desc(bk, 2 * BN, kk), id128, kk > 0);
+          ptx::mma_ss_e(tG, tc::desc_add(dQ, 32 * kk), tc::desc_add(dBK, so + 32 * kk), id128, kk > 0);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          ptx::mma_ss(tmem + Lay::cG, tc::kmajor_desc(sA, BM, kk), tc::kmajor_desc(bk + kTile, BN, kk), id64, 1u);
+          ptx::mma_ss_e(tG, tc::desc_add(dA, 32 * kk), tc::desc_add(dKk, so + 32 * kk), id64, 1u);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          ptx::mma_ss(tmem + Lay::cH, tc::kmajor_desc(sdO, BM, kk), tc::kmajor_desc(cv, 2 * BN, kk), id128, kk > 0);
-        ptx::mma_commit(s_full);
+          ptx::mma_ss_e(tH, tc::desc_add(ddO, 32 * kk), tc::desc_add(dCV, so + 32 * kk), id128, kk > 0);
+        ptx::mma_commit_e(s_full);
         if (j > 0) outputs(j - 1);
       }
       outputs(nkv - 1);
-      ptx::mma_commit(acc_full);
+      ptx::mma_commit_e(acc_full);
     }
   } else {
     const int qd = warp & 3, hf = warp >> 2;
@@ -470,53 +478,64 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = (ntile > NS ? ntile - NS : 0); t < ntile; ++t) wait(&empty[t % NS], (t / NS) & 1);
     }
   } else if (warp == 9) {
-    if (lane == 0 && ok) {
+    if (ok) {  // all 32 lanes; one elected lane issues each MMA and commit
       constexpr uint32_t id128 = ptx::idesc_bf16(BM, 2 * BN, 0, 0);
       constexpr uint32_t id64 = ptx::idesc_bf16(BM, BN, 0, 0);
       constexpr uint32_t idO = ptx::idesc_bf16(BM, D, 0, 1);
-      const uint32_t sK = ptx::smem_u32(sm + Lay::oK), sB = ptx::smem_u32(sm + Lay::oB);
-      const uint32_t sV = ptx::smem_u32(sm + Lay::oV), sC = ptx::smem_u32(sm + Lay::oC);
       const uint32_t sSt = ptx::smem_u32(sm + Lay::oStage);
+      // Descriptors at K-step 0 of stage 0 (see the row pass).
+      const uint64_t dK = tc::kmajor_desc(ptx::smem_u32(sm + Lay::oK), BM, 0);
+      const uint64_t dB = tc::kmajor_desc(ptx::smem_u32(sm + Lay::oB), BM, 0);
+      const uint64_t dV = tc::kmajor_desc(ptx::smem_u32(sm + Lay::oV), BM, 0);
+      const uint64_t dC = tc::kmajor_desc(ptx::smem_u32(sm + Lay::oC), BM, 0);
+      const uint64_t dQA = tc::kmajor_desc(sSt, 2 * BN, 0);            // [Q_i; a_i], K-major
+      const uint64_t dQk = tc::kmajor_desc(sSt, BN, 0);                // Q_i, K-major
+      const uint64_t ddOk = tc::kmajor_desc(sSt + 2 * kTile, BN, 0);   // dO_i, K-major
+      const uint64_t dQm = tc::mnmajor_desc(sSt, BN, 0);               // Q_i, MN-major
+      const uint64_t dAm = tc::mnmajor_desc(sSt + kTile, BN, 0);       // a_i, MN-major
+      const uint64_t ddOm = tc::mnmajor_desc(sSt + 2 * kTile, BN, 0);  // dO_i, MN-major
+      const uint32_t tSG = tmem + Lay::cSG, tPH = tmem + Lay::cPH, tOp = tmem + Lay::cOp;
+      const uint32_t tgV = tmem + Lay::cgV, tgK = tmem + Lay::cgK;
       auto outputs = [&](int t) {
         const int s = t % NS;
-        const uint32_t qa = sSt + s * Lay::kStage, gt = qa + 2 * kTile;
+        const uint32_t so = static_cast<uint32_t>(s * Lay::kStage);
         wait(ready, t & 1);
         ptx::tc_fence_after();
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k) {
           const uint32_t acc = (t > 0 || k > 0) ? 1u : 0u;
-          ptx::mma_ts(tmem + Lay::cgV, tmem + Lay::cOp + k * 8, tc::mnmajor_desc(gt, BN, k), idO, acc);
-          ptx::mma_ts(tmem + Lay::cgK, tmem + Lay::cOp + 32 + k * 8, tc::mnmajor_desc(qa + kTile, BN, k), idO, acc);
-          ptx::mma_ts(tmem + Lay::cgK, tmem + Lay::cOp + 64 + k * 8, tc::mnmajor_desc(qa, BN, k), idO, 1u);
+          const uint32_t kb = so + 2048 * k;
+          ptx::mma_ts_e(tgV, tOp + k * 8, tc::desc_add(ddOm, kb), idO, acc);
+          ptx::mma_ts_e(tgK, tOp + 32 + k * 8, tc::desc_add(dAm, kb), idO, acc);
+          ptx::mma_ts_e(tgK, tOp + 64 + k * 8, tc::desc_add(dQm, kb), idO, 1u);
         }
-        ptx::mma_commit(&empty[s]);
-        ptx::mma_commit(out_done);
+        ptx::mma_commit_e(&empty[s]);
+        ptx::mma_commit_e(out_done);
       };
       wait(k_full, 0);
       for (int t = 0; t < ntile; ++t) {
         const int s = t % NS;
-        const uint32_t qa = sSt + s * Lay::kStage;  // [Q_i; a_i]
-        const uint32_t gt = qa + 2 * kTile;          // dO_i
+        const uint32_t so = static_cast<uint32_t>(s * Lay::kStage);
         wait(&full[s], (t / NS) & 1);
         if (t > 0) wait(consumed, (t - 1) & 1);
         ptx::tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          ptx::mma_ss(tmem + Lay::cSG, tc::kmajor_desc(sK, BM, kk), tc::kmajor_desc(qa, 2 * BN, kk), id128, kk > 0);
+          ptx::mma_ss_e(tSG, tc::desc_add(dK, 32 * kk), tc::desc_add(dQA, so + 32 * kk), id128, kk > 0);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          ptx::mma_ss(tmem + Lay::cSG + BN, tc::kmajor_desc(sB, BM, kk), tc::kmajor_desc(qa, BN, kk), id64, 1u);
+          ptx::mma_ss_e(tSG + BN, tc::desc_add(dB, 32 * kk), tc::desc_add(dQk, so + 32 * kk), id64, 1u);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          ptx::mma_ss(tmem + Lay::cPH, tc::kmajor_desc(sV, BM, kk), tc::kmajor_desc(gt, BN, kk), id64, kk > 0);
+          ptx::mma_ss_e(tPH, tc::desc_add(dV, 32 * kk), tc::desc_add(ddOk, so + 32 * kk), id64, kk > 0);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          ptx::mma_ss(tmem + Lay::cPH + BN, tc::kmajor_desc(sC, BM, kk), tc::kmajor_desc(gt, BN, kk), id64, kk > 0);
-        ptx::mma_commit(s_full);
+          ptx::mma_ss_e(tPH + BN, tc::desc_add(dC, 32 * kk), tc::desc_add(ddOk, so + 32 * kk), id64, kk > 0);
+        ptx::mma_commit_e(s_full);
         if (t > 0) outputs(t - 1);
       }
       outputs(ntile - 1);
-      ptx::mma_commit(acc_full);
+      ptx::mma_commit_e(acc_full);
     }
   } else {
     const int qd = warp & 3, hf = warp >> 2;

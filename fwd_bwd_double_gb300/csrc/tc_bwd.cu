@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
     }
   } else if (warp == 9) {
     // ---------------------------------------------------------------- MMA
-    if (lane == 0 && ok) {
+    if (ok) {  // all 32 lanes; one elected lane issues each MMA and commit
       constexpr uint32_t idS = ptx::idesc_bf16(BM, BN, 0, 0);
       constexpr uint32_t idQ = ptx::idesc_bf16(BM, D, 0, 1);
       const uint32_t sQ = ptx::smem_u32(sm + Lay::oQ), sdO = ptx::smem_u32(sm + Lay::odO);
@@ -162,11 +162,11 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k) {
           const uint64_t bd = tc::mnmajor_desc(kt, BN, k);
-          ptx::mma_ts(tmem + Lay::cdQ, tmem + Lay::cdS + b * (BN / 2) + k * 8, bd, idQ, (t > 0 || k > 0));
+          ptx::mma_ts_e(tmem + Lay::cdQ, tmem + Lay::cdS + b * (BN / 2) + k * 8, bd, idQ, (t > 0 || k > 0));
           if constexpr (GP)
-            ptx::mma_ts(tmem + Lay::cPK, tmem + Lay::cP + b * (BN / 2) + k * 8, bd, idQ, (t > 0 || k > 0));
+            ptx::mma_ts_e(tmem + Lay::cPK, tmem + Lay::cP + b * (BN / 2) + k * 8, bd, idQ, (t > 0 || k > 0));
         }
-        ptx::mma_commit(&empty[s]);
+        ptx::mma_commit_e(&empty[s]);
       };
       wait(q_full, 0);
       for (int j = 0; j < nkv; ++j) {
@@ -177,15 +177,15 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
         const uint32_t kt = sK + s * Lay::kStream, vt = sV + s * Lay::kStream;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          ptx::mma_ss(tmem + Lay::cS + b * BN, tc::kmajor_desc(sQ, BM, kk), tc::kmajor_desc(kt, BN, kk), idS, kk > 0);
+          ptx::mma_ss_e(tmem + Lay::cS + b * BN, tc::kmajor_desc(sQ, BM, kk), tc::kmajor_desc(kt, BN, kk), idS, kk > 0);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          ptx::mma_ss(tmem + Lay::cdP + b * BN, tc::kmajor_desc(sdO, BM, kk), tc::kmajor_desc(vt, BN, kk), idS,
+          ptx::mma_ss_e(tmem + Lay::cdP + b * BN, tc::kmajor_desc(sdO, BM, kk), tc::kmajor_desc(vt, BN, kk), idS,
                       kk > 0);
-        ptx::mma_commit(&s_full[b]);
+        ptx::mma_commit_e(&s_full[b]);
       }
       for (int t = (nkv > NB ? nkv - NB : 0); t < nkv; ++t) products(t);
-      ptx::mma_commit(acc_full);
+      ptx::mma_commit_e(acc_full);
     }
   } else {
     // ------------------------------------------------------------- compute
@@ -395,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = (ntile > NS ? ntile - NS : 0); t < ntile; ++t) wait(&empty[t % NS], (t / NS) & 1);
     }
   } else if (warp == 9) {
-    if (lane == 0 && ok) {
+    if (ok) {  // all 32 lanes; one elected lane issues each MMA and commit
       constexpr uint32_t idS = ptx::idesc_bf16(BM, BN, 0, 0);
       constexpr uint32_t idKV = ptx::idesc_bf16(BM, D, 0, 1);
       const uint32_t sK = ptx::smem_u32(sm + Lay::oK), sV = ptx::smem_u32(sm + Lay::oV);
@@ -407,13 +407,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t qt = sQ + s * Lay::kStream, gt = sdO + s * Lay::kStream;
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k) {
-          ptx::mma_ts(tmem + Lay::cdV, tmem + Lay::cP + b * (BN / 2) + k * 8, tc::mnmajor_desc(gt, BN, k), idKV,
+          ptx::mma_ts_e(tmem + Lay::cdV, tmem + Lay::cP + b * (BN / 2) + k * 8, tc::mnmajor_desc(gt, BN, k), idKV,
                       (t > 0 || k > 0));
           const uint64_t bq = tc::mnmajor_desc(qt, BN, k);
-          ptx::mma_ts(tmem + Lay::cdK, tmem + Lay::cdS + b * (BN / 2) + k * 8, bq, idKV, (t > 0 || k > 0));
-          if constexpr (GP) ptx::mma_ts(tmem + Lay::cdK, tmem + Lay::cG + b * (BN / 2) + k * 8, bq, idKV, 1u);
+          ptx::mma_ts_e(tmem + Lay::cdK, tmem + Lay::cdS + b * (BN / 2) + k * 8, bq, idKV, (t > 0 || k > 0));
+          if constexpr (GP) ptx::mma_ts_e(tmem + Lay::cdK, tmem + Lay::cG + b * (BN / 2) + k * 8, bq, idKV, 1u);
         }
-        ptx::mma_commit(&empty[s]);
+        ptx::mma_commit_e(&empty[s]);
       };
       wait(k_full, 0);
       for (int t = 0; t < ntile; ++t) {
@@ -424,15 +424,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t qt = sQ + s * Lay::kStream, gt = sdO + s * Lay::kStream;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          ptx::mma_ss(tmem + Lay::cS + b * BN, tc::kmajor_desc(sK, BM, kk), tc::kmajor_desc(qt, BN, kk), idS, kk > 0);
+          ptx::mma_ss_e(tmem + Lay::cS + b * BN, tc::kmajor_desc(sK, BM, kk), tc::kmajor_desc(qt, BN, kk), idS, kk > 0);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          ptx::mma_ss(tmem + Lay::cdP + b * BN, tc::kmajor_desc(sV, BM, kk), tc::kmajor_desc(gt, BN, kk), idS,
+          ptx::mma_ss_e(tmem + Lay::cdP + b * BN, tc::kmajor_desc(sV, BM, kk), tc::kmajor_desc(gt, BN, kk), idS,
                       kk > 0);
-        ptx::mma_commit(&s_full[b]);
+        ptx::mma_commit_e(&s_full[b]);
       }
       for (int t = (ntile > NB ? ntile - NB : 0); t < ntile; ++t) products(t);
-      ptx::mma_commit(acc_full);
+      ptx::mma_commit_e(acc_full);
     }
   } else {
     const int qd = warp & 3, hf = warp >> 2;

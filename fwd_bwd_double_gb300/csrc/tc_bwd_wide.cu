@@ -138,21 +138,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = (nkv > NS ? nkv - NS : 0); j < nkv; ++j) wait(&sy.empty[j % NS], (j / NS) & 1);
     }
   } else if (warp == kCW + 1) {
-    if (lane == 0 && ok) {
+    if (ok) {  // all 32 lanes; one elected lane issues each MMA and commit
       constexpr uint32_t idS = ptx::idesc_bf16(BW, BW, 0, 0);
       constexpr uint32_t idQ = ptx::idesc_bf16(BW, D, 0, 1);
-      const uint32_t sQ = ptx::smem_u32(sm + Lay::oQ), sdO = ptx::smem_u32(sm + Lay::odO);
+      // Descriptors at K-step 0 of stage 0, stepped with one add per MMA.
+      const uint64_t dQ = tc::kmajor_desc(ptx::smem_u32(sm + Lay::oQ), BW, 0);
+      const uint64_t ddO = tc::kmajor_desc(ptx::smem_u32(sm + Lay::odO), BW, 0);
       const uint32_t sK = ptx::smem_u32(sm + Lay::oK), sV = ptx::smem_u32(sm + Lay::oV);
+      const uint64_t dKk = tc::kmajor_desc(sK, BW, 0), dVk = tc::kmajor_desc(sV, BW, 0);
+      const uint64_t dKm = tc::mnmajor_desc(sK, BW, 0);
+      const uint32_t tS = tmem + Lay::cS, tdP = tmem + Lay::cdP, tdQ = tmem + Lay::cdQ, tdS = tmem + Lay::cdS;
       auto products = [&](int t) {  // dQ += dS_t K_t, then release the stage and the dS columns
         const int s = t % NS;
         wait(sy.ready, t & 1);
         ptx::tc_fence_after();
-        const uint32_t kt = sK + s * kTile;
+        const uint32_t so = static_cast<uint32_t>(s * kTile);
 #pragma unroll
         for (int k = 0; k < BW / 16; ++k)
-          ptx::mma_ts(tmem + Lay::cdQ, tmem + Lay::cdS + k * 8, tc::mnmajor_desc(kt, BW, k), idQ, (t > 0 || k > 0));
-        ptx::mma_commit(&sy.empty[s]);
-        ptx::mma_commit(sy.out_done);
+          ptx::mma_ts_e(tdQ, tdS + k * 8, tc::desc_add(dKm, so + 2048 * k), idQ, (t > 0 || k > 0));
+        ptx::mma_commit_e(&sy.empty[s]);
+        ptx::mma_commit_e(sy.out_done);
       };
       wait(sy.held_full, 0);
       for (int j = 0; j < nkv; ++j) {
@@ -160,18 +165,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         wait(&sy.full[s], (j / NS) & 1);
         if (j > 0) wait(sy.consumed, (j - 1) & 1);  // tiles of block j-1 are in registers
         ptx::tc_fence_after();
-        const uint32_t kt = sK + s * kTile, vt = sV + s * kTile;
+        const uint32_t so = static_cast<uint32_t>(s * kTile);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          ptx::mma_ss(tmem + Lay::cS, tc::kmajor_desc(sQ, BW, kk), tc::kmajor_desc(kt, BW, kk), idS, kk > 0);
+          ptx::mma_ss_e(tS, tc::desc_add(dQ, tc::kmajor_off(BW, kk)), tc::desc_add(dKk, so + tc::kmajor_off(BW, kk)), idS,
+                      kk > 0);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          ptx::mma_ss(tmem + Lay::cdP, tc::kmajor_desc(sdO, BW, kk), tc::kmajor_desc(vt, BW, kk), idS, kk > 0);
-        ptx::mma_commit(sy.s_full);
+          ptx::mma_ss_e(tdP, tc::desc_add(ddO, tc::kmajor_off(BW, kk)), tc::desc_add(dVk, so + tc::kmajor_off(BW, kk)),
+                      idS, kk > 0);
+        ptx::mma_commit_e(sy.s_full);
         if (j > 0) products(j - 1);
       }
       products(nkv - 1);
-      ptx::mma_commit(sy.acc_full);
+      ptx::mma_commit_e(sy.acc_full);
     }
   } else {
     const int qd = warp & 3, cg = warp >> 2;
@@ -319,43 +326,51 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = (ntile > NS ? ntile - NS : 0); t < ntile; ++t) wait(&sy.empty[t % NS], (t / NS) & 1);
     }
   } else if (warp == kCW + 1) {
-    if (lane == 0 && ok) {
+    if (ok) {  // all 32 lanes; one elected lane issues each MMA and commit
       constexpr uint32_t idS = ptx::idesc_bf16(BW, BW, 0, 0);
       constexpr uint32_t idKV = ptx::idesc_bf16(BW, D, 0, 1);
-      const uint32_t sK = ptx::smem_u32(sm + Lay::oK), sV = ptx::smem_u32(sm + Lay::oV);
+      // Descriptors at K-step 0 of stage 0, stepped with one add per MMA.
+      const uint64_t dK = tc::kmajor_desc(ptx::smem_u32(sm + Lay::oK), BW, 0);
+      const uint64_t dV = tc::kmajor_desc(ptx::smem_u32(sm + Lay::oV), BW, 0);
       const uint32_t sSt = ptx::smem_u32(sm + Lay::oStage);
+      const uint64_t dQk = tc::kmajor_desc(sSt, BW, 0), ddOk = tc::kmajor_desc(sSt + kTile, BW, 0);
+      const uint64_t dQm = tc::mnmajor_desc(sSt, BW, 0), ddOm = tc::mnmajor_desc(sSt + kTile, BW, 0);
+      const uint32_t tS = tmem + Lay::cS, tdP = tmem + Lay::cdP, tP = tmem + Lay::cP, tdS = tmem + Lay::cdS;
+      const uint32_t tdV = tmem + Lay::cdV, tdK = tmem + Lay::cdK;
       auto outputs = [&](int t) {  // dV += P^T dO_i, dK += dS^T Q_i
         const int s = t % NS;
-        const uint32_t qt = sSt + s * Lay::kStage, gt = qt + kTile;
+        const uint32_t so = static_cast<uint32_t>(s * Lay::kStage);
         wait(sy.ready, t & 1);
         ptx::tc_fence_after();
 #pragma unroll
         for (int k = 0; k < BW / 16; ++k) {
           const uint32_t acc = (t > 0 || k > 0) ? 1u : 0u;
-          ptx::mma_ts(tmem + Lay::cdV, tmem + Lay::cP + k * 8, tc::mnmajor_desc(gt, BW, k), idKV, acc);
-          ptx::mma_ts(tmem + Lay::cdK, tmem + Lay::cdS + k * 8, tc::mnmajor_desc(qt, BW, k), idKV, acc);
+          ptx::mma_ts_e(tdV, tP + k * 8, tc::desc_add(ddOm, so + 2048 * k), idKV, acc);
+          ptx::mma_ts_e(tdK, tdS + k * 8, tc::desc_add(dQm, so + 2048 * k), idKV, acc);
         }
-        ptx::mma_commit(&sy.empty[s]);
-        ptx::mma_commit(sy.out_done);
+        ptx::mma_commit_e(&sy.empty[s]);
+        ptx::mma_commit_e(sy.out_done);
       };
       wait(sy.held_full, 0);
       for (int t = 0; t < ntile; ++t) {
         const int s = t % NS;
-        const uint32_t qt = sSt + s * Lay::kStage, gt = qt + kTile;
+        const uint32_t so = static_cast<uint32_t>(s * Lay::kStage);
         wait(&sy.full[s], (t / NS) & 1);
         if (t > 0) wait(sy.consumed, (t - 1) & 1);
         ptx::tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          ptx::mma_ss(tmem + Lay::cS, tc::kmajor_desc(sK, BW, kk), tc::kmajor_desc(qt, BW, kk), idS, kk > 0);
+          ptx::mma_ss_e(tS, tc::desc_add(dK, tc::kmajor_off(BW, kk)), tc::desc_add(dQk, so + tc::kmajor_off(BW, kk)), idS,
+                      kk > 0);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          ptx::mma_ss(tmem + Lay::cdP, tc::kmajor_desc(sV, BW, kk), tc::kmajor_desc(gt, BW, kk), idS, kk > 0);
-        ptx::mma_commit(sy.s_full);
+          ptx::mma_ss_e(tdP, tc::desc_add(dV, tc::kmajor_off(BW, kk)), tc::desc_add(ddOk, so + tc::kmajor_off(BW, kk)),
+                      idS, kk > 0);
+        ptx::mma_commit_e(sy.s_full);
         if (t > 0) outputs(t - 1);
       }
       outputs(ntile - 1);
-      ptx::mma_commit(sy.acc_full);
+      ptx::mma_commit_e(sy.acc_full);
     }
   } else {
     const int qd = warp & 3, cg = warp >> 2;

@@ -16,10 +16,29 @@ namespace tc {
 __device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int rows, int k) {
   return ptx::sdesc_sw128(base + (k >> 2) * rows * 128 + (k & 3) * 32, 16, 1024);
 }
+// Byte offset of K-step k within a K-major operand of `rows` rows (what kmajor_desc adds).
+__host__ __device__ constexpr uint32_t kmajor_off(int rows, int k) {
+  return static_cast<uint32_t>((k >> 2) * rows * 128 + (k & 3) * 32);
+}
 // MN-major operand (rows = K index, columns = M or N), advanced to K-step k (16 rows).
 // Leading byte offset = slab stride (next 64 columns), stride byte offset = 8 rows.
 __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int rows, int k) {
   return ptx::sdesc_sw128(base + k * 16 * 128, rows * 128, 1024);
+}
+
+// A descriptor moved by `bytes` within shared memory: the start address sits in
+// bits 0-13 of the low word in 16-byte units, and every operand of these kernels
+// lies in the first 256 KB, so the move never carries out of the low word.  The
+// MMA warps build their descriptors once and step them with this single add, so
+// the issuing thread spends few instructions per MMA (it shares its scheduler
+// with two compute warps).
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) {
+  uint32_t lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(d));
+  lo += bytes >> 4;
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
 }
 
 // Barrier among the first `n` threads (the compute warps), id 1 (id 0 is __syncthreads).

@@ -134,18 +134,19 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------- MMA issuer
-    if (lane == 0 && ok) {
+    if (ok) {  // all 32 lanes; one elected lane issues each MMA and commit
       constexpr uint32_t idS = ptx::idesc_bf16(BM, BN, 0, 0);
       constexpr uint32_t idO = ptx::idesc_bf16(BM, D, 0, 1);
-      const uint32_t sQ = ptx::smem_u32(sm + Lay::oQ);
-      const uint32_t sK = ptx::smem_u32(sm + Lay::oK);
-      const uint32_t sV = ptx::smem_u32(sm + Lay::oV);
+      // Descriptors at K-step 0 of stage 0, stepped with one add per MMA.
+      const uint64_t dQ = kmajor_desc(ptx::smem_u32(sm + Lay::oQ), BM, 0);
+      const uint64_t dK = kmajor_desc(ptx::smem_u32(sm + Lay::oK), BN, 0);
+      const uint64_t dV = mnmajor_desc(ptx::smem_u32(sm + Lay::oV), BN, 0);
       auto issue_pv = [&](int j) {
-        const uint32_t v = sV + (j % NS) * Lay::kKV;
+        const uint32_t so = static_cast<uint32_t>((j % NS) * Lay::kKV);
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k)
-          ptx::mma_ts(tO, tP + k * 8, mnmajor_desc(v, BN, k), idO, (j > 0 || k > 0) ? 1u : 0u);
-        ptx::mma_commit(&empty[j % NS]);
+          ptx::mma_ts_e(tO, tP + k * 8, tc::desc_add(dV, so + k * 16 * 128), idO, (j > 0 || k > 0) ? 1u : 0u);
+        ptx::mma_commit_e(&empty[j % NS]);
       };
       wait(q_full, 0);
       for (int j = 0; j < nkv; ++j) {
@@ -157,16 +158,17 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
           issue_pv(j - 1);
         }
         ptx::tc_fence_after();
-        const uint32_t k = sK + s * Lay::kKV;
+        const uint32_t so = static_cast<uint32_t>(s * Lay::kKV);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          ptx::mma_ss(tS, kmajor_desc(sQ, BM, kk), kmajor_desc(k, BN, kk), idS, kk > 0 ? 1u : 0u);
-        ptx::mma_commit(s_full);
+          ptx::mma_ss_e(tS, tc::desc_add(dQ, tc::kmajor_off(BM, kk)), tc::desc_add(dK, so + tc::kmajor_off(BN, kk)), idS,
+                      kk > 0 ? 1u : 0u);
+        ptx::mma_commit_e(s_full);
       }
       wait(p_ready, (nkv - 1) & 1);
       ptx::tc_fence_after();
       issue_pv(nkv - 1);
-      ptx::mma_commit(o_full);
+      ptx::mma_commit_e(o_full);
     }
   } else {
     // ---------------------------------------- softmax: thread r owns query row r
