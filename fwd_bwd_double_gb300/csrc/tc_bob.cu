@@ -33,13 +33,16 @@
 // ("FlashAttention bf16 gradient and GProj", "How the zero sum turns into a false
 // gradient").  The stored state F_i = sum_j W_ij - E_i D_i uses the fp32 sums.
 //
-// Row-pass TMEM: [S | G] 128 columns, [dP | H] 128, X, Y, Z, U 64 each = 512; its
-// four bf16 operands go to 128-byte-swizzled shared memory (A operand of the
-// output products).  Column-pass TMEM: tiles 256, operands 96, gV, gK 128.
-// In both passes the compute warps copy a block's tiles into registers and
-// release the tile columns at once, so the next block's tile MMAs overlap this
-// block's CUDA-core work; no TMEM region is read by one MMA while a later MMA
-// with a different accumulator writes it (such MMAs carry no ordering guarantee).
+// Row-pass TMEM: one 128-column tile region holding first [G | S] and then
+// [H | dP] of the same key block, the four bf16 operands (32 columns each, the A
+// operand of the output products), X, U, Y, Z 64 each = 512.  Column-pass TMEM:
+// tiles 256, operands 96, gV, gK 128.  An MMA with both operands in shared memory
+// needs 8 KB per 128 x 128 x 16 step, which is the whole shared-memory bandwidth
+// of the SM (128 B per clock); taking the output products' A operand from TMEM
+// keeps the passes off that limit.  In both passes the compute warps copy tiles
+// into registers and release their columns at once, so the next tile MMAs overlap
+// the CUDA-core work; no TMEM region is read by one MMA while a later MMA with a
+// different accumulator writes it (such MMAs carry no ordering guarantee).
 #include <cuda_bf16.h>
 
 #include <type_traits>
@@ -57,7 +60,7 @@ constexpr int D = 64;
 constexpr int BM = 128;
 constexpr int BN = 64;
 constexpr int kCompute = 256;
-constexpr int kThreads = kCompute + 64;
+constexpr int kThreads = kCompute + 96;  // compute warps, TMA warp, tile-MMA warp, output-MMA warp
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kTile = BN * D * 2;  // 8 KB: one streamed 64-row tile
 constexpr int kHeld = BM * D * 2;  // 16 KB: one held 128-row tile
@@ -67,17 +70,19 @@ using tc::bf16_lo;
 using tc::f;
 
 // ================================================================ row pass
-// Per 64-key block j the MMA warp issues tiles(j) as soon as the compute warps
-// have copied tiles(j-1) out of TMEM (barrier `consumed`), then outputs(j-1) once
-// the bf16 operands of block j-1 are in shared memory (`ready`).  The tensor pipe
-// thus computes tiles(j) while the CUDA cores turn tiles(j-1) into operands.  The
-// operands live in one shared buffer, rewritten only after outputs(j-1) finished
-// reading it (`out_done`).
+// Two MMA warps share the tensor pipe.  Per 64-key block j the tile warp issues
+// [G | S](j) into the tile region once the compute warps have copied [H | dP](j-1)
+// out (barrier `consumed_b`), then [H | dP](j) once they have copied [G | S](j)
+// out (`consumed_a`); the output warp issues outputs(j) once the bf16 operands of
+// block j are in TMEM (`ready`).  With one issuing warp the barrier waits between
+// the phases left the pipe idle; with two, each warp's waits overlap the other's
+// MMAs.  The compute warps turn S and G into P and PG while [H | dP] is computed.
+// The operand columns are rewritten only after outputs(j-1) finished reading them
+// (`out_done`); a stage is refilled once both warps have committed its MMAs.
 struct RowLay {
-  static constexpr int NS = 3;
+  static constexpr int NS = 5;
   static constexpr int oQ = 0, odO = kHeld, oA = 2 * kHeld;
-  static constexpr int oOp = 3 * kHeld;          // P^, (PG)^, dS^, W^: 4 x (128 rows x 64 keys) bf16
-  static constexpr int oStage = oOp + 4 * kHeld;
+  static constexpr int oStage = 3 * kHeld;
   // One stage: c_j, V_j, b_j, K_j (8 KB each).  [c_j; V_j] and [b_j; K_j] are the
   // 128-row B operands of the tile products; K_j sits at a fixed positive offset
   // from c_j and from b_j, so [c_j | K_j] and [b_j | K_j] are 128-wide MN-major B
@@ -87,8 +92,11 @@ struct RowLay {
   static constexpr int oRed = oStage + NS * kStage;
   static constexpr int oBar = oRed + 12 * BM * 4;
   static constexpr int bytes = oBar + 256;
-  // TMEM: [G | S] (Q b^T + a K^T, then Q K^T), [H | dP], [X | U], [Y | Z].
-  static constexpr int cG = 0, cS = 64, cH = 128, cdP = 192, cX = 256, cU = 320, cY = 384, cZ = 448;
+  // TMEM: tile region [G | S] (Q b^T + a K^T, then Q K^T), later [H | dP] of the same
+  // block; bf16 operands P^, (PG)^, dS^, W^; accumulators [X | U], [Y | Z].
+  static constexpr int cG = 0, cS = 64, cH = 0, cdP = 64;
+  static constexpr int cP = 128, cPG = 160, cdS = 192, cW = 224;
+  static constexpr int cX = 256, cU = 320, cY = 384, cZ = 448;
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -105,9 +113,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* q_full = reinterpret_cast<uint64_t*>(sm + Lay::oBar);
   uint64_t* full = q_full + 1;
   uint64_t* empty = full + NS;
-  uint64_t* s_full = empty + NS;
-  uint64_t* consumed = s_full + 1;
-  uint64_t* ready = consumed + 1;
+  uint64_t* sa_full = empty + NS;     // [G | S] of the current block in TMEM
+  uint64_t* sb_full = sa_full + 1;    // [H | dP] of the current block in TMEM
+  uint64_t* consumed_a = sb_full + 1;
+  uint64_t* consumed_b = consumed_a + 1;
+  uint64_t* ready = consumed_b + 1;
   uint64_t* out_done = ready + 1;
   uint64_t* acc_full = out_done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
@@ -124,10 +134,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(q_full, 1);
     for (int s = 0; s < NS; ++s) {
       ptx::mbar_init(&full[s], 1);
-      ptx::mbar_init(&empty[s], 1);
+      ptx::mbar_init(&empty[s], 2);  // released by the tile warp and by the output warp
     }
-    ptx::mbar_init(s_full, 1);
-    ptx::mbar_init(consumed, kCompute);
+    ptx::mbar_init(sa_full, 1);
+    ptx::mbar_init(sb_full, 1);
+    ptx::mbar_init(consumed_a, kCompute);
+    ptx::mbar_init(consumed_b, kCompute);
     ptx::mbar_init(ready, kCompute);
     ptx::mbar_init(out_done, 1);
     ptx::mbar_init(acc_full, 1);
@@ -172,47 +184,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {  // all 32 lanes; one elected lane issues each MMA and commit
       constexpr uint32_t id128 = ptx::idesc_bf16(BM, 2 * BN, 0, 0);
       constexpr uint32_t id64 = ptx::idesc_bf16(BM, BN, 0, 0);
-      constexpr uint32_t idO = ptx::idesc_bf16(BM, D, 0, 1);
-      constexpr uint32_t idO2 = ptx::idesc_bf16(BM, 2 * D, 0, 1);
       const uint32_t sSt = ptx::smem_u32(sm + Lay::oStage);
       // Descriptors at K-step 0 of stage 0.  A K-step moves a K-major operand by 32 B
       // and an MN-major one by 16 rows (2 KB); stage s adds s * kStage.
       const uint64_t dQ = tc::kmajor_desc(ptx::smem_u32(sm + Lay::oQ), BM, 0);
       const uint64_t ddO = tc::kmajor_desc(ptx::smem_u32(sm + Lay::odO), BM, 0);
       const uint64_t dA = tc::kmajor_desc(ptx::smem_u32(sm + Lay::oA), BM, 0);
-      const uint64_t dOp = tc::kmajor_desc(ptx::smem_u32(sm + Lay::oOp), BM, 0);  // P^; + kHeld per operand
       const uint64_t dBK = tc::kmajor_desc(sSt + Lay::ob, 2 * BN, 0);   // [b_j; K_j], K-major
       const uint64_t dKk = tc::kmajor_desc(sSt + Lay::oKs, BN, 0);      // K_j, K-major
       const uint64_t dCV = tc::kmajor_desc(sSt + Lay::oc, 2 * BN, 0);   // [c_j; V_j], K-major
-      const uint64_t dCK = ptx::sdesc_sw128(sSt + Lay::oc, Lay::oKs - Lay::oc, 1024);  // [c_j | K_j], MN-major
-      const uint64_t dVm = tc::mnmajor_desc(sSt + Lay::oV, BN, 0);      // V_j, MN-major
-      const uint64_t dBKm = ptx::sdesc_sw128(sSt + Lay::ob, Lay::oKs - Lay::ob, 1024);  // [b_j | K_j], MN-major
-      const uint64_t dKm = tc::mnmajor_desc(sSt + Lay::oKs, BN, 0);     // K_j, MN-major
-      const uint32_t tG = tmem + Lay::cG, tH = tmem + Lay::cH, tX = tmem + Lay::cX, tY = tmem + Lay::cY;
-      auto outputs = [&](int j) {  // X, Y, Z, U += block j's operands x its streamed tiles
-        const int s = j % NS;
-        const uint32_t so = static_cast<uint32_t>(s * Lay::kStage);
-        wait(ready, j & 1);
-        ptx::tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < BN / 16; ++k) {
-          const uint32_t acc = (j > 0 || k > 0) ? 1u : 0u;
-          const uint32_t ka = 32 * k, kb = so + 2048 * k;
-          // [X | U] += P [c | K],  X += (PG) V,  [Y | Z] += dS [b | K],  Y += W K
-          ptx::mma_ss_e(tX, tc::desc_add(dOp, ka), tc::desc_add(dCK, kb), idO2, acc);
-          ptx::mma_ss_e(tX, tc::desc_add(dOp, kHeld + ka), tc::desc_add(dVm, kb), idO, 1u);
-          ptx::mma_ss_e(tY, tc::desc_add(dOp, 2 * kHeld + ka), tc::desc_add(dBKm, kb), idO2, acc);
-          ptx::mma_ss_e(tY, tc::desc_add(dOp, 3 * kHeld + ka), tc::desc_add(dKm, kb), idO, 1u);
-        }
-        ptx::mma_commit_e(&empty[s]);
-        ptx::mma_commit_e(out_done);
-      };
+      const uint32_t tG = tmem + Lay::cG, tH = tmem + Lay::cH;
       wait(q_full, 0);
       for (int j = 0; j < nkv; ++j) {
         const int s = j % NS;
         const uint32_t so = static_cast<uint32_t>(s * Lay::kStage);
         wait(&full[s], (j / NS) & 1);
-        if (j > 0) wait(consumed, (j - 1) & 1);  // tiles of block j-1 copied out of TMEM
+        if (j > 0) wait(consumed_b, (j - 1) & 1);  // [H | dP] of block j-1 copied out of TMEM
         ptx::tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
@@ -220,13 +207,46 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           ptx::mma_ss_e(tG, tc::desc_add(dA, 32 * kk), tc::desc_add(dKk, so + 32 * kk), id64, 1u);
+        ptx::mma_commit_e(sa_full);
+        wait(consumed_a, j & 1);  // [G | S] of block j copied out of TMEM
+        ptx::tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           ptx::mma_ss_e(tH, tc::desc_add(ddO, 32 * kk), tc::desc_add(dCV, so + 32 * kk), id128, kk > 0);
-        ptx::mma_commit_e(s_full);
-        if (j > 0) outputs(j - 1);
+        ptx::mma_commit_e(sb_full);
+        ptx::mma_commit_e(&empty[s]);
       }
-      outputs(nkv - 1);
+    }
+  } else if (warp == 10) {
+    if (ok) {  // all 32 lanes; one elected lane issues each MMA and commit
+      constexpr uint32_t idO = ptx::idesc_bf16(BM, D, 0, 1);
+      constexpr uint32_t idO2 = ptx::idesc_bf16(BM, 2 * D, 0, 1);
+      const uint32_t sSt = ptx::smem_u32(sm + Lay::oStage);
+      const uint64_t dCK = ptx::sdesc_sw128(sSt + Lay::oc, Lay::oKs - Lay::oc, 1024);  // [c_j | K_j], MN-major
+      const uint64_t dVm = tc::mnmajor_desc(sSt + Lay::oV, BN, 0);      // V_j, MN-major
+      const uint64_t dBKm = ptx::sdesc_sw128(sSt + Lay::ob, Lay::oKs - Lay::ob, 1024);  // [b_j | K_j], MN-major
+      const uint64_t dKm = tc::mnmajor_desc(sSt + Lay::oKs, BN, 0);     // K_j, MN-major
+      const uint32_t tX = tmem + Lay::cX, tY = tmem + Lay::cY;
+      const uint32_t tP = tmem + Lay::cP, tPG = tmem + Lay::cPG, tdS = tmem + Lay::cdS, tW = tmem + Lay::cW;
+      for (int j = 0; j < nkv; ++j) {  // X, Y, Z, U += block j's operands x its streamed tiles
+        const int s = j % NS;
+        const uint32_t so = static_cast<uint32_t>(s * Lay::kStage);
+        wait(ready, j & 1);
+        wait(&full[s], (j / NS) & 1);  // already complete: the stage cannot refill before this warp releases it
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k) {
+          const uint32_t acc = (j > 0 || k > 0) ? 1u : 0u;
+          const uint32_t kb = so + 2048 * k;
+          // [X | U] += P [c | K],  X += (PG) V,  [Y | Z] += dS [b | K],  Y += W K
+          ptx::mma_ts_e(tX, tP + 8 * k, tc::desc_add(dCK, kb), idO2, acc);
+          ptx::mma_ts_e(tX, tPG + 8 * k, tc::desc_add(dVm, kb), idO, 1u);
+          ptx::mma_ts_e(tY, tdS + 8 * k, tc::desc_add(dBKm, kb), idO2, acc);
+          ptx::mma_ts_e(tY, tW + 8 * k, tc::desc_add(dKm, kb), idO, 1u);
+        }
+        ptx::mma_commit_e(&empty[s]);
+        ptx::mma_commit_e(out_done);
+      }
       ptx::mma_commit_e(acc_full);
     }
   } else {
@@ -237,17 +257,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool live = row < N;
     const size_t rowoff = (static_cast<size_t>(bh) * N + row) * D;
     float part = 0.f;
-    uint4 oh[4];  // this thread's half of the O row (32 bf16), reused in the epilogue
-#pragma unroll
-    for (int u = 0; u < 4; ++u) oh[u] = make_uint4(0, 0, 0, 0);
     if (live) {
       const uint4* po = reinterpret_cast<const uint4*>(O + rowoff + hf * 32);
       const uint4* pg = reinterpret_cast<const uint4*>(dO + rowoff + hf * 32);
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        oh[u] = po[u];
-        const uint4 g = pg[u];
-        const uint32_t aw[4] = {oh[u].x, oh[u].y, oh[u].z, oh[u].w}, gw[4] = {g.x, g.y, g.z, g.w};
+        const uint4 o = po[u], g = pg[u];
+        const uint32_t aw[4] = {o.x, o.y, o.z, o.w}, gw[4] = {g.x, g.y, g.z, g.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) part += bf16_lo(aw[e]) * bf16_lo(gw[e]) + bf16_hi(aw[e]) * bf16_hi(gw[e]);
       }
@@ -261,21 +277,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t c2 = tc::pk2f(c, c), s2 = tc::pk2f(scale, scale);
     const uint64_t nL2 = tc::pk2f(-L2, -L2), nD2 = tc::pk2f(-Dr, -Dr);
     const int c0 = hf * 32;
-    uint8_t* op = sm + Lay::oOp;
+    const uint32_t tOp = tmem + static_cast<uint32_t>(hf * 16) + lo;  // this thread's keys in the operand columns
     for (int j = 0; j < nkv; ++j) {
-      wait(s_full, j & 1);
+      wait(sa_full, j & 1);
       ptx::tc_fence_after();
-      uint32_t sv[32], gv[32], dv[32], hv[32];
+      uint32_t sv[32], gv[32];
       ptx::tmem_ld32(tmem + Lay::cS + c0 + lo, sv);
       ptx::tmem_ld32(tmem + Lay::cG + c0 + lo, gv);
-      ptx::tmem_ld32(tmem + Lay::cdP + c0 + lo, dv);
-      ptx::tmem_ld32(tmem + Lay::cH + c0 + lo, hv);
       ptx::tmem_wait_ld();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(consumed);  // the MMA warp may now overwrite the tile columns
+      ptx::mbar_arrive(consumed_a);  // the MMA warp may now write [H | dP] into the tile region
       const int krel = j * BN + c0 - rb * BM;
+      uint64_t P2[16], G2[16];
       uint32_t pP[16], pG[16], pS[16], pW[16];
-      auto block = [&](auto masked) {
+      // P, PG from the [G | S] tiles (while [H | dP] is being computed)
+      auto first = [&](auto masked) {
 #pragma unroll
         for (int t = 0; t < 32; t += 2) {
           const float2 arg = tc::unpk2(tc::fma2(tc::pk2(sv[t], sv[t + 1]), c2, nL2));
@@ -284,42 +300,49 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (krel + t > r) p0 = 0.f;
             if (krel + t + 1 > r) p1 = 0.f;
           }
-          const uint64_t P2 = tc::pk2f(p0, p1);
-          const uint64_t G2 = tc::mul2(tc::pk2(gv[t], gv[t + 1]), s2);
-          const uint64_t ds2 = tc::mul2(P2, tc::add2(tc::pk2(dv[t], dv[t + 1]), nD2));
-          const uint64_t pg2 = tc::mul2(P2, G2);
-          const uint64_t w2 = tc::fma2(G2, ds2, tc::mul2(P2, tc::pk2(hv[t], hv[t + 1])));
-          accF = tc::add2(accF, w2);
-          accE = tc::add2(accE, pg2);
-          const float2 ds = tc::unpk2(ds2), pg = tc::unpk2(pg2), w = tc::unpk2(w2);
           const int idx = t >> 1;
+          P2[idx] = tc::pk2f(p0, p1);
+          G2[idx] = tc::mul2(tc::pk2(gv[t], gv[t + 1]), s2);
+          const uint64_t pg2 = tc::mul2(P2[idx], G2[idx]);
+          accE = tc::add2(accE, pg2);
+          const float2 pg = tc::unpk2(pg2);
           pP[idx] = ptx::pack_bf16(p0, p1);
           pG[idx] = ptx::pack_bf16(pg.x, pg.y);
-          pS[idx] = ptx::pack_bf16(ds.x, ds.y);
-          pW[idx] = ptx::pack_bf16(w.x, w.y);
-          accW = tc::add2(accW, tc::bf2_to_f2(pW[idx]));
-          accdS = tc::add2(accdS, tc::bf2_to_f2(pS[idx]));
           accP = tc::add2(accP, tc::bf2_to_f2(pP[idx]));
         }
       };
       if (krel + 31 > 0)  // a block reaching past the first row of this CTA: causal mask needed
-        block(std::true_type{});
+        first(std::true_type{});
       else
-        block(std::false_type{});
-      if (j > 0) wait(out_done, (j - 1) & 1);  // block j-1's products have read the operands
-      // Keys 32 hf .. 32 hf + 31 of row r = 16-byte chunks 4 hf .. 4 hf + 3, 128-byte swizzled.
+        first(std::false_type{});
+      wait(sb_full, j & 1);
+      ptx::tc_fence_after();
+      uint32_t dv[32], hv[32];
+      ptx::tmem_ld32(tmem + Lay::cdP + c0 + lo, dv);
+      ptx::tmem_ld32(tmem + Lay::cH + c0 + lo, hv);
+      ptx::tmem_wait_ld();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(consumed_b);  // the MMA warp may now write the next block's [G | S]
+      // dS, W from the [H | dP] tiles
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int chunk = (4 * hf + u) ^ (r & 7);
-        uint8_t* dst = op + r * 128 + chunk * 16;
-        *reinterpret_cast<uint4*>(dst) = make_uint4(pP[4 * u], pP[4 * u + 1], pP[4 * u + 2], pP[4 * u + 3]);
-        *reinterpret_cast<uint4*>(dst + kHeld) = make_uint4(pG[4 * u], pG[4 * u + 1], pG[4 * u + 2], pG[4 * u + 3]);
-        *reinterpret_cast<uint4*>(dst + 2 * kHeld) =
-            make_uint4(pS[4 * u], pS[4 * u + 1], pS[4 * u + 2], pS[4 * u + 3]);
-        *reinterpret_cast<uint4*>(dst + 3 * kHeld) =
-            make_uint4(pW[4 * u], pW[4 * u + 1], pW[4 * u + 2], pW[4 * u + 3]);
+      for (int t = 0; t < 32; t += 2) {
+        const int idx = t >> 1;
+        const uint64_t ds2 = tc::mul2(P2[idx], tc::add2(tc::pk2(dv[t], dv[t + 1]), nD2));
+        const uint64_t w2 = tc::fma2(G2[idx], ds2, tc::mul2(P2[idx], tc::pk2(hv[t], hv[t + 1])));
+        accF = tc::add2(accF, w2);
+        const float2 ds = tc::unpk2(ds2), w = tc::unpk2(w2);
+        pS[idx] = ptx::pack_bf16(ds.x, ds.y);
+        pW[idx] = ptx::pack_bf16(w.x, w.y);
+        accW = tc::add2(accW, tc::bf2_to_f2(pW[idx]));
+        accdS = tc::add2(accdS, tc::bf2_to_f2(pS[idx]));
       }
-      ptx::fence_proxy_async_smem();
+      if (j > 0) wait(out_done, (j - 1) & 1);  // block j-1's products have read the operand columns
+      ptx::tmem_st16(tOp + Lay::cP, pP);
+      ptx::tmem_st16(tOp + Lay::cPG, pG);
+      ptx::tmem_st16(tOp + Lay::cdS, pS);
+      ptx::tmem_st16(tOp + Lay::cW, pW);
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
       ptx::mbar_arrive(ready);
     }
     auto hsum = [](uint64_t x) {
@@ -347,8 +370,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tmem_ld32(tmem + Lay::cU + c0 + lo, uv);
     ptx::tmem_wait_ld();
     if (live) {
-      const uint32_t ow[16] = {oh[0].x, oh[0].y, oh[0].z, oh[0].w, oh[1].x, oh[1].y, oh[1].z, oh[1].w,
-                               oh[2].x, oh[2].y, oh[2].z, oh[2].w, oh[3].x, oh[3].y, oh[3].z, oh[3].w};
+      uint32_t ow[16];  // this thread's half of the O row (32 bf16), read again here
+      const uint4* po = reinterpret_cast<const uint4*>(O + rowoff + c0);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint4 o = po[u];
+        ow[4 * u] = o.x;
+        ow[4 * u + 1] = o.y;
+        ow[4 * u + 2] = o.z;
+        ow[4 * u + 3] = o.w;
+      }
       uint32_t go[16], gq[16];
 #pragma unroll
       for (int t = 0; t < 32; t += 2) {
@@ -386,8 +417,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 
 // ============================================================= column pass
-// Same hand-off as the row pass (`consumed` releases the tile columns early,
-// `out_done` guards the operand columns); the three bf16 operands stay in TMEM.
+// Same hand-off as the row pass (two MMA warps; `consumed` releases the tile
+// columns early, `out_done` guards the operand columns); the three bf16 operands
+// stay in TMEM.
 struct ColLay {
   static constexpr int NS = 5;
   static constexpr int oK = 0, oB = kHeld, oV = 2 * kHeld, oC = 3 * kHeld, oStage = 4 * kHeld;
@@ -432,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(k_full, 1);
     for (int s = 0; s < NS; ++s) {
       ptx::mbar_init(&full[s], 1);
-      ptx::mbar_init(&empty[s], 1);
+      ptx::mbar_init(&empty[s], 2);  // released by the tile warp and by the output warp
     }
     ptx::mbar_init(s_full, 1);
     ptx::mbar_init(consumed, kCompute);
@@ -481,7 +513,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {  // all 32 lanes; one elected lane issues each MMA and commit
       constexpr uint32_t id128 = ptx::idesc_bf16(BM, 2 * BN, 0, 0);
       constexpr uint32_t id64 = ptx::idesc_bf16(BM, BN, 0, 0);
-      constexpr uint32_t idO = ptx::idesc_bf16(BM, D, 0, 1);
       const uint32_t sSt = ptx::smem_u32(sm + Lay::oStage);
       // Descriptors at K-step 0 of stage 0 (see the row pass).
       const uint64_t dK = tc::kmajor_desc(ptx::smem_u32(sm + Lay::oK), BM, 0);
@@ -491,27 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dQA = tc::kmajor_desc(sSt, 2 * BN, 0);            // [Q_i; a_i], K-major
       const uint64_t dQk = tc::kmajor_desc(sSt, BN, 0);                // Q_i, K-major
       const uint64_t ddOk = tc::kmajor_desc(sSt + 2 * kTile, BN, 0);   // dO_i, K-major
-      const uint64_t dQm = tc::mnmajor_desc(sSt, BN, 0);               // Q_i, MN-major
-      const uint64_t dAm = tc::mnmajor_desc(sSt + kTile, BN, 0);       // a_i, MN-major
-      const uint64_t ddOm = tc::mnmajor_desc(sSt + 2 * kTile, BN, 0);  // dO_i, MN-major
-      const uint32_t tSG = tmem + Lay::cSG, tPH = tmem + Lay::cPH, tOp = tmem + Lay::cOp;
-      const uint32_t tgV = tmem + Lay::cgV, tgK = tmem + Lay::cgK;
-      auto outputs = [&](int t) {
-        const int s = t % NS;
-        const uint32_t so = static_cast<uint32_t>(s * Lay::kStage);
-        wait(ready, t & 1);
-        ptx::tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < BN / 16; ++k) {
-          const uint32_t acc = (t > 0 || k > 0) ? 1u : 0u;
-          const uint32_t kb = so + 2048 * k;
-          ptx::mma_ts_e(tgV, tOp + k * 8, tc::desc_add(ddOm, kb), idO, acc);
-          ptx::mma_ts_e(tgK, tOp + 32 + k * 8, tc::desc_add(dAm, kb), idO, acc);
-          ptx::mma_ts_e(tgK, tOp + 64 + k * 8, tc::desc_add(dQm, kb), idO, 1u);
-        }
-        ptx::mma_commit_e(&empty[s]);
-        ptx::mma_commit_e(out_done);
-      };
+      const uint32_t tSG = tmem + Lay::cSG, tPH = tmem + Lay::cPH;
       wait(k_full, 0);
       for (int t = 0; t < ntile; ++t) {
         const int s = t % NS;
@@ -532,9 +543,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < D / 16; ++kk)
           ptx::mma_ss_e(tPH + BN, tc::desc_add(dC, 32 * kk), tc::desc_add(ddOk, so + 32 * kk), id64, kk > 0);
         ptx::mma_commit_e(s_full);
-        if (t > 0) outputs(t - 1);
+        ptx::mma_commit_e(&empty[s]);
       }
-      outputs(ntile - 1);
+    }
+  } else if (warp == 10) {
+    if (ok) {  // all 32 lanes; one elected lane issues each MMA and commit
+      constexpr uint32_t idO = ptx::idesc_bf16(BM, D, 0, 1);
+      const uint32_t sSt = ptx::smem_u32(sm + Lay::oStage);
+      const uint64_t dQm = tc::mnmajor_desc(sSt, BN, 0);               // Q_i, MN-major
+      const uint64_t dAm = tc::mnmajor_desc(sSt + kTile, BN, 0);       // a_i, MN-major
+      const uint64_t ddOm = tc::mnmajor_desc(sSt + 2 * kTile, BN, 0);  // dO_i, MN-major
+      const uint32_t tOp = tmem + Lay::cOp, tgV = tmem + Lay::cgV, tgK = tmem + Lay::cgK;
+      for (int t = 0; t < ntile; ++t) {
+        const int s = t % NS;
+        const uint32_t so = static_cast<uint32_t>(s * Lay::kStage);
+        wait(ready, t & 1);
+        wait(&full[s], (t / NS) & 1);  // already complete: the stage cannot refill before this warp releases it
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k) {
+          const uint32_t acc = (t > 0 || k > 0) ? 1u : 0u;
+          const uint32_t kb = so + 2048 * k;
+          ptx::mma_ts_e(tgV, tOp + k * 8, tc::desc_add(ddOm, kb), idO, acc);
+          ptx::mma_ts_e(tgK, tOp + 32 + k * 8, tc::desc_add(dAm, kb), idO, acc);
+          ptx::mma_ts_e(tgK, tOp + 64 + k * 8, tc::desc_add(dQm, kb), idO, 1u);
+        }
+        ptx::mma_commit_e(&empty[s]);
+        ptx::mma_commit_e(out_done);
+      }
       ptx::mma_commit_e(acc_full);
     }
   } else {

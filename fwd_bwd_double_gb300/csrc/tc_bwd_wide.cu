@@ -34,7 +34,7 @@ constexpr int BW = 128;        // held and streamed block rows
 constexpr int NS = 4;          // stages of streamed blocks
 constexpr int kCW = 16;        // compute warps
 constexpr int kCompute = kCW * 32;
-constexpr int kThreads = kCompute + 64;
+constexpr int kThreads = kCompute + 96;  // + TMA warp, tile-MMA warp, output-MMA warp
 constexpr int kC = 32;         // tile columns per compute thread (128 / 4 column groups)
 constexpr int DG = D / 4;      // output columns per compute thread
 constexpr int kTile = BW * D * 2;  // 16 KB
@@ -71,7 +71,7 @@ struct Sync {
     ptx::mbar_init(held_full, 1);
     for (int s = 0; s < NS; ++s) {
       ptx::mbar_init(&full[s], 1);
-      ptx::mbar_init(&empty[s], 1);
+      ptx::mbar_init(&empty[s], 2);  // released by the tile warp and by the output warp
     }
     ptx::mbar_init(s_full, 1);
     ptx::mbar_init(consumed, kCompute);
@@ -140,25 +140,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kCW + 1) {
     if (ok) {  // all 32 lanes; one elected lane issues each MMA and commit
       constexpr uint32_t idS = ptx::idesc_bf16(BW, BW, 0, 0);
-      constexpr uint32_t idQ = ptx::idesc_bf16(BW, D, 0, 1);
       // Descriptors at K-step 0 of stage 0, stepped with one add per MMA.
       const uint64_t dQ = tc::kmajor_desc(ptx::smem_u32(sm + Lay::oQ), BW, 0);
       const uint64_t ddO = tc::kmajor_desc(ptx::smem_u32(sm + Lay::odO), BW, 0);
       const uint32_t sK = ptx::smem_u32(sm + Lay::oK), sV = ptx::smem_u32(sm + Lay::oV);
       const uint64_t dKk = tc::kmajor_desc(sK, BW, 0), dVk = tc::kmajor_desc(sV, BW, 0);
-      const uint64_t dKm = tc::mnmajor_desc(sK, BW, 0);
-      const uint32_t tS = tmem + Lay::cS, tdP = tmem + Lay::cdP, tdQ = tmem + Lay::cdQ, tdS = tmem + Lay::cdS;
-      auto products = [&](int t) {  // dQ += dS_t K_t, then release the stage and the dS columns
-        const int s = t % NS;
-        wait(sy.ready, t & 1);
-        ptx::tc_fence_after();
-        const uint32_t so = static_cast<uint32_t>(s * kTile);
-#pragma unroll
-        for (int k = 0; k < BW / 16; ++k)
-          ptx::mma_ts_e(tdQ, tdS + k * 8, tc::desc_add(dKm, so + 2048 * k), idQ, (t > 0 || k > 0));
-        ptx::mma_commit_e(&sy.empty[s]);
-        ptx::mma_commit_e(sy.out_done);
-      };
+      const uint32_t tS = tmem + Lay::cS, tdP = tmem + Lay::cdP;
       wait(sy.held_full, 0);
       for (int j = 0; j < nkv; ++j) {
         const int s = j % NS;
@@ -175,9 +162,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::mma_ss_e(tdP, tc::desc_add(ddO, tc::kmajor_off(BW, kk)), tc::desc_add(dVk, so + tc::kmajor_off(BW, kk)),
                       idS, kk > 0);
         ptx::mma_commit_e(sy.s_full);
-        if (j > 0) products(j - 1);
+        ptx::mma_commit_e(&sy.empty[s]);
       }
-      products(nkv - 1);
+    }
+  } else if (warp == kCW + 2) {
+    if (ok) {  // all 32 lanes; one elected lane issues each MMA and commit
+      constexpr uint32_t idQ = ptx::idesc_bf16(BW, D, 0, 1);
+      const uint64_t dKm = tc::mnmajor_desc(ptx::smem_u32(sm + Lay::oK), BW, 0);
+      const uint32_t tdQ = tmem + Lay::cdQ, tdS = tmem + Lay::cdS;
+      for (int t = 0; t < nkv; ++t) {  // dQ += dS_t K_t, then release the stage and the dS columns
+        const int s = t % NS;
+        wait(sy.ready, t & 1);
+        wait(&sy.full[s], (t / NS) & 1);  // already complete: the stage cannot refill before this warp releases it
+        ptx::tc_fence_after();
+        const uint32_t so = static_cast<uint32_t>(s * kTile);
+#pragma unroll
+        for (int k = 0; k < BW / 16; ++k)
+          ptx::mma_ts_e(tdQ, tdS + k * 8, tc::desc_add(dKm, so + 2048 * k), idQ, (t > 0 || k > 0));
+        ptx::mma_commit_e(&sy.empty[s]);
+        ptx::mma_commit_e(sy.out_done);
+      }
       ptx::mma_commit_e(sy.acc_full);
     }
   } else {
@@ -328,29 +332,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kCW + 1) {
     if (ok) {  // all 32 lanes; one elected lane issues each MMA and commit
       constexpr uint32_t idS = ptx::idesc_bf16(BW, BW, 0, 0);
-      constexpr uint32_t idKV = ptx::idesc_bf16(BW, D, 0, 1);
       // Descriptors at K-step 0 of stage 0, stepped with one add per MMA.
       const uint64_t dK = tc::kmajor_desc(ptx::smem_u32(sm + Lay::oK), BW, 0);
       const uint64_t dV = tc::kmajor_desc(ptx::smem_u32(sm + Lay::oV), BW, 0);
       const uint32_t sSt = ptx::smem_u32(sm + Lay::oStage);
       const uint64_t dQk = tc::kmajor_desc(sSt, BW, 0), ddOk = tc::kmajor_desc(sSt + kTile, BW, 0);
-      const uint64_t dQm = tc::mnmajor_desc(sSt, BW, 0), ddOm = tc::mnmajor_desc(sSt + kTile, BW, 0);
-      const uint32_t tS = tmem + Lay::cS, tdP = tmem + Lay::cdP, tP = tmem + Lay::cP, tdS = tmem + Lay::cdS;
-      const uint32_t tdV = tmem + Lay::cdV, tdK = tmem + Lay::cdK;
-      auto outputs = [&](int t) {  // dV += P^T dO_i, dK += dS^T Q_i
-        const int s = t % NS;
-        const uint32_t so = static_cast<uint32_t>(s * Lay::kStage);
-        wait(sy.ready, t & 1);
-        ptx::tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < BW / 16; ++k) {
-          const uint32_t acc = (t > 0 || k > 0) ? 1u : 0u;
-          ptx::mma_ts_e(tdV, tP + k * 8, tc::desc_add(ddOm, so + 2048 * k), idKV, acc);
-          ptx::mma_ts_e(tdK, tdS + k * 8, tc::desc_add(dQm, so + 2048 * k), idKV, acc);
-        }
-        ptx::mma_commit_e(&sy.empty[s]);
-        ptx::mma_commit_e(sy.out_done);
-      };
+      const uint32_t tS = tmem + Lay::cS, tdP = tmem + Lay::cdP;
       wait(sy.held_full, 0);
       for (int t = 0; t < ntile; ++t) {
         const int s = t % NS;
@@ -367,9 +354,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::mma_ss_e(tdP, tc::desc_add(dV, tc::kmajor_off(BW, kk)), tc::desc_add(ddOk, so + tc::kmajor_off(BW, kk)),
                       idS, kk > 0);
         ptx::mma_commit_e(sy.s_full);
-        if (t > 0) outputs(t - 1);
+        ptx::mma_commit_e(&sy.empty[s]);
       }
-      outputs(ntile - 1);
+    }
+  } else if (warp == kCW + 2) {
+    if (ok) {  // all 32 lanes; one elected lane issues each MMA and commit
+      constexpr uint32_t idKV = ptx::idesc_bf16(BW, D, 0, 1);
+      const uint32_t sSt = ptx::smem_u32(sm + Lay::oStage);
+      const uint64_t dQm = tc::mnmajor_desc(sSt, BW, 0), ddOm = tc::mnmajor_desc(sSt + kTile, BW, 0);
+      const uint32_t tP = tmem + Lay::cP, tdS = tmem + Lay::cdS, tdV = tmem + Lay::cdV, tdK = tmem + Lay::cdK;
+      for (int t = 0; t < ntile; ++t) {  // dV += P^T dO_i, dK += dS^T Q_i
+        const int s = t % NS;
+        const uint32_t so = static_cast<uint32_t>(s * Lay::kStage);
+        wait(sy.ready, t & 1);
+        wait(&sy.full[s], (t / NS) & 1);  // already complete: the stage cannot refill before this warp releases it
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < BW / 16; ++k) {
+          const uint32_t acc = (t > 0 || k > 0) ? 1u : 0u;
+          ptx::mma_ts_e(tdV, tP + k * 8, tc::desc_add(ddOm, so + 2048 * k), idKV, acc);
+          ptx::mma_ts_e(tdK, tdS + k * 8, tc::desc_add(dQm, so + 2048 * k), idKV, acc);
+        }
+        ptx::mma_commit_e(&sy.empty[s]);
+        ptx::mma_commit_e(sy.out_done);
+      }
       ptx::mma_commit_e(sy.acc_full);
     }
   } else {
