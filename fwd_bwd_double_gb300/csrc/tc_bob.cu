@@ -273,7 +273,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float Dr = red[r] + red[BM + r];
     const float L2 = live ? lse[static_cast<size_t>(bh) * N + row] * kLog2e : 0.f;
     // Per-row sums as fp32 pairs (two keys per f32x2 instruction).
-    uint64_t accE = 0, accF = 0, accW = 0, accdS = 0, accP = 0;
+    uint64_t accE = 0, accF = 0;
+    // Sums of the bf16 operands (even and odd keys apart), for the consistent-rounding state.
+    float accW0 = 0.f, accW1 = 0.f, accdS0 = 0.f, accdS1 = 0.f, accP0 = 0.f, accP1 = 0.f;
     const uint64_t c2 = tc::pk2f(c, c), s2 = tc::pk2f(scale, scale);
     const uint64_t nL2 = tc::pk2f(-L2, -L2), nD2 = tc::pk2f(-Dr, -Dr);
     const int c0 = hf * 32;
@@ -308,7 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float2 pg = tc::unpk2(pg2);
           pP[idx] = ptx::pack_bf16(p0, p1);
           pG[idx] = ptx::pack_bf16(pg.x, pg.y);
-          accP = tc::add2(accP, tc::bf2_to_f2(pP[idx]));
+          accP0 = tc::add_bf16_lo(accP0, pP[idx]);
+          accP1 = tc::add_bf16_hi(accP1, pP[idx]);
         }
       };
       if (krel + 31 > 0)  // a block reaching past the first row of this CTA: causal mask needed
@@ -333,8 +336,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float2 ds = tc::unpk2(ds2), w = tc::unpk2(w2);
         pS[idx] = ptx::pack_bf16(ds.x, ds.y);
         pW[idx] = ptx::pack_bf16(w.x, w.y);
-        accW = tc::add2(accW, tc::bf2_to_f2(pW[idx]));
-        accdS = tc::add2(accdS, tc::bf2_to_f2(pS[idx]));
+        accW0 = tc::add_bf16_lo(accW0, pW[idx]);
+        accW1 = tc::add_bf16_hi(accW1, pW[idx]);
+        accdS0 = tc::add_bf16_lo(accdS0, pS[idx]);
+        accdS1 = tc::add_bf16_hi(accdS1, pS[idx]);
       }
       if (j > 0) wait(out_done, (j - 1) & 1);  // block j-1's products have read the operand columns
       ptx::tmem_st16(tOp + Lay::cP, pP);
@@ -351,9 +356,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     red[2 * BM + hf * BM + r] = hsum(accE);
     red[4 * BM + hf * BM + r] = hsum(accF);
-    red[6 * BM + hf * BM + r] = hsum(accW);
-    red[8 * BM + hf * BM + r] = hsum(accdS);
-    red[10 * BM + hf * BM + r] = hsum(accP);
+    red[6 * BM + hf * BM + r] = accW0 + accW1;
+    red[8 * BM + hf * BM + r] = accdS0 + accdS1;
+    red[10 * BM + hf * BM + r] = accP0 + accP1;
     tc::named_sync(1, kCompute);
     const float E = red[2 * BM + r] + red[3 * BM + r];
     const float Fp = red[4 * BM + r] + red[5 * BM + r];

@@ -104,6 +104,20 @@ __device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
   return r;
 }
+// acc + the bf16 held in the low (high) half of w, in one mixed-precision add: the
+// widening of a bf16 to fp32 is exact, so this rounds exactly as widening and then
+// adding in fp32 would.
+__device__ __forceinline__ float add_bf16_lo(float acc, uint32_t w) {
+  float r;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tadd.rn.f32.bf16 %0, l, %2;\n\t}" : "=f"(r) : "r"(w), "f"(acc));
+  return r;
+}
+__device__ __forceinline__ float add_bf16_hi(float acc, uint32_t w) {
+  float r;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tadd.rn.f32.bf16 %0, h, %2;\n\t}" : "=f"(r) : "r"(w), "f"(acc));
+  return r;
+}
+
 // The bf16x2 word as an fp32 pair (exact widening).
 __device__ __forceinline__ uint64_t bf2_to_f2(uint32_t w) { return pk2(w << 16, w & 0xffff0000u); }
 
