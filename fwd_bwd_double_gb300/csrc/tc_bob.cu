@@ -9,19 +9,20 @@
 //   tiles   [Q b^T | S] = Q [b_j; K_j]^T,  G += a K_j^T,  [H | dP] = dO [c_j; V_j]^T
 //   outputs [X | U] += P [c_j | K_j],  X += (P G) V_j,  [Y | Z] += dS [b_j | K_j],
 //           Y += W K_j   (128-wide products wherever two share an A operand)
-//   end     gdO = X - E O,  gQ = s (Y - E Z - F' U); row states (L log2 e, D, E, F)
+//   end     gdO = X - E O,  gQ = s (Y - E Z - F' U); row states (L log2 e, E, D, F')
 // (the corrections after the finished row are linear in E and F', so they are
 // applied once per row: "partial sums accumulated early, corrected after").
 // Column pass (CTA holds 128 keys; 64-query blocks i >= j stream past, with the
 // row states re-read): transposed tiles, lanes = keys,
 //   tiles   [S^T | K a^T] = K [Q_i; a_i]^T,  G^T += b Q_i^T,  dP^T = V dO_i^T,
 //           H^T = c dO_i^T
-//   dPbar = P (G - E),  Sbar = P (G (dP - D) - E dP + H - F)
+//   dPbar = P (G - E),  Sbar = P (G (dP - D) - E dP + H - F) = P ((G - E)(dP - D) + H - F')
 //   outputs gV += dPbar^T dO_i,  gK += dS^T a_i + Sbar^T Q_i;  end gK *= s.
-// All tile products take A and B from 128-byte-swizzled shared memory (TMA);
-// the output products take the bf16 tiles (P, P G, dS, W from shared memory in
-// the row pass; dPbar, dS, Sbar from TMEM in the column pass) as the A operand
-// and the streamed block, MN-major, as B.
+// The row pass's tile products read both operands from 128-byte-swizzled shared
+// memory (TMA); the column pass's take the held K, b, V, c from TMEM.  The output
+// products take the bf16 tiles (P, P G, dS, W in the row pass; dPbar, dS, Sbar in
+// the column pass) from TMEM as the A operand and the streamed block, MN-major,
+// from shared memory as B.
 //
 // Rounding: the output products see bf16 copies P^, (PG)^, dS^, W^ of the tiles.
 // The corrections use E_i = sum_j (PG)_ij (fp32) and a second state taken from
@@ -31,12 +32,13 @@
 // definitions above (sum dS = 0, sum P = 1); in bf16 they keep the rounding of W
 // from being multiplied by the mean key, the same mechanism GProj removes from dQ
 // ("FlashAttention bf16 gradient and GProj", "How the zero sum turns into a false
-// gradient").  The stored state F_i = sum_j W_ij - E_i D_i uses the fp32 sums.
+// gradient").  The stored state F'_i = sum_j W_ij uses the fp32 sums.
 //
 // Row-pass TMEM: one 128-column tile region holding first [G | S] and then
 // [H | dP] of the same key block, the four bf16 operands (32 columns each, the A
 // operand of the output products), X, U, Y, Z 64 each = 512.  Column-pass TMEM:
-// tiles 256, operands 96, gV, gK 128.  An MMA with both operands in shared memory
+// tile region 128, held K, b, V, c 128, operands 96, gV, gK 128.  An MMA with both
+// operands in shared memory
 // needs 8 KB per 128 x 128 x 16 step, which is the whole shared-memory bandwidth
 // of the SM (128 B per clock); taking the output products' A operand from TMEM
 // keeps the passes off that limit.  In both passes the compute warps copy tiles
@@ -400,15 +402,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         d0[u] = make_uint4(go[4 * u], go[4 * u + 1], go[4 * u + 2], go[4 * u + 3]);
         d1[u] = make_uint4(gq[4 * u], gq[4 * u + 1], gq[4 * u + 2], gq[4 * u + 3]);
       }
-      if (hf == 0) {  // row states, negated, pair-interleaved (see the column pass)
-        float* wf = reinterpret_cast<float*>(ws) + static_cast<size_t>(bh) * Np * 4;
-        const int64_t k2 = row & ~static_cast<int64_t>(1);
-        const int odd = static_cast<int>(row & 1);
-        wf[k2 * 4 + odd] = -L2;
-        wf[k2 * 4 + 2 + odd] = -Dr;
-        wf[(k2 + 1) * 4 + odd] = -E;
-        wf[(k2 + 1) * 4 + 2 + odd] = -(Fp - E * Dr);
-      }
+    }
+    if (hf == 0 && row < Np) {  // row states, negated, pair-interleaved (see the column pass)
+      // F' = F + E D = sum_j W_ij is what the column pass needs (its (G - E)(dP - D) form).
+      // The row past N of an odd-length slice gets zeros, so the column pass never reads
+      // unwritten workspace (its P is masked to 0 there).
+      float* wf = reinterpret_cast<float*>(ws) + static_cast<size_t>(bh) * Np * 4;
+      const int64_t k2 = row & ~static_cast<int64_t>(1);
+      const int odd = static_cast<int>(row & 1);
+      wf[k2 * 4 + odd] = live ? -L2 : 0.f;
+      wf[k2 * 4 + 2 + odd] = live ? -E : 0.f;
+      wf[(k2 + 1) * 4 + odd] = live ? -Dr : 0.f;
+      wf[(k2 + 1) * 4 + 2 + odd] = live ? -Fp : 0.f;
     }
   }
 
@@ -422,35 +427,46 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 
 // ============================================================= column pass
-// Same hand-off as the row pass (two MMA warps; `consumed` releases the tile
-// columns early, `out_done` guards the operand columns); the three bf16 operands
-// stay in TMEM.
+// Same hand-off as the row pass: the tile region holds first [S^T | G^T] and then
+// [dP^T | H^T] of the same 64-query block (barriers `consumed_a`, `consumed_b`), a
+// tile warp and an output warp issue the MMAs, `out_done` guards the operand
+// columns.  The held key-side operands K, b, V, c sit in TMEM as the A operands of
+// the tile products, so those MMAs read only the streamed operand from shared
+// memory; with both operands in shared memory they took the SM's whole
+// shared-memory bandwidth and starved the compute warps' reads of the row states.
+// Per element the compute warps form
+//   P = 2^(S c - L log2 e),  dPbar = P (G - E),  dS = P (dP - D),
+//   Sbar = P ((G - E)(dP - D) + H - F')          (F' = F + E D, stored by the row pass)
 struct ColLay {
-  static constexpr int NS = 5;
-  static constexpr int oK = 0, oB = kHeld, oV = 2 * kHeld, oC = 3 * kHeld, oStage = 4 * kHeld;
+  static constexpr int NS = 8;
   static constexpr int kStat = BN * 16;
-  static constexpr int kStage = 3 * kTile + 2048;  // [Q_i; a_i], dO_i, stats (padded to 1 KB multiple)
+  static constexpr int kStage = 3 * kTile + 2048;  // [Q_i; a_i], dO_i, row states (padded to a 1 KB multiple)
+  static constexpr int oStage = 0;
   static constexpr int oBar = oStage + NS * kStage;
   static constexpr int bytes = oBar + 256;
-  static constexpr int cSG = 0, cPH = 128, cOp = 256, cgV = 352, cgK = 416;
+  // TMEM: tile region, held bf16 A operands K, b, V, c (32 columns each), the bf16
+  // output operands dPbar, dS, Sbar (32 each), accumulators gV, gK.
+  static constexpr int cT = 0, cK = 128, cB = 160, cV = 192, cC = 224, cOp = 256, cgV = 352, cgK = 416;
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
-    bob_col_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmC,
-                   const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmA,
+    bob_col_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmdO, const __grid_constant__ CUtensorMap tmSt,
+                   const __nv_bfloat16* __restrict__ Kp, const __nv_bfloat16* __restrict__ Bp,
+                   const __nv_bfloat16* __restrict__ Vp, const __nv_bfloat16* __restrict__ Cp,
                    __nv_bfloat16* __restrict__ gK, __nv_bfloat16* __restrict__ gV, int N, int BH, float scale,
                    float c) {
   using Lay = ColLay;
   constexpr int NS = Lay::NS;
   extern __shared__ __align__(1024) uint8_t sm[];
-  uint64_t* k_full = reinterpret_cast<uint64_t*>(sm + Lay::oBar);
-  uint64_t* full = k_full + 1;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + Lay::oBar);
   uint64_t* empty = full + NS;
-  uint64_t* s_full = empty + NS;
-  uint64_t* consumed = s_full + 1;
-  uint64_t* ready = consumed + 1;
+  uint64_t* held_ready = empty + NS;  // K, b, V, c of this key block in TMEM
+  uint64_t* sa_full = held_ready + 1;
+  uint64_t* sb_full = sa_full + 1;
+  uint64_t* consumed_a = sb_full + 1;
+  uint64_t* consumed_b = consumed_a + 1;
+  uint64_t* ready = consumed_b + 1;
   uint64_t* out_done = ready + 1;
   uint64_t* acc_full = out_done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
@@ -466,13 +482,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ntile = nq - i0;
 
   if (threadIdx.x == 0) {
-    ptx::mbar_init(k_full, 1);
     for (int s = 0; s < NS; ++s) {
       ptx::mbar_init(&full[s], 1);
       ptx::mbar_init(&empty[s], 2);  // released by the tile warp and by the output warp
     }
-    ptx::mbar_init(s_full, 1);
-    ptx::mbar_init(consumed, kCompute);
+    ptx::mbar_init(held_ready, kCompute);
+    ptx::mbar_init(sa_full, 1);
+    ptx::mbar_init(sb_full, 1);
+    ptx::mbar_init(consumed_a, kCompute);
+    ptx::mbar_init(consumed_b, kCompute);
     ptx::mbar_init(ready, kCompute);
     ptx::mbar_init(out_done, 1);
     ptx::mbar_init(acc_full, 1);
@@ -497,11 +515,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::prefetch_tmap(&tmA);
       ptx::prefetch_tmap(&tmdO);
       ptx::prefetch_tmap(&tmSt);
-      ptx::mbar_expect_tx(k_full, 4 * kHeld);
-      ptx::tma_load_3d(sm + Lay::oK, &tmK, k_full, 0, kb * BM, bh);
-      ptx::tma_load_3d(sm + Lay::oB, &tmB, k_full, 0, kb * BM, bh);
-      ptx::tma_load_3d(sm + Lay::oV, &tmV, k_full, 0, kb * BM, bh);
-      ptx::tma_load_3d(sm + Lay::oC, &tmC, k_full, 0, kb * BM, bh);
       for (int t = 0; t < ntile; ++t) {
         const int s = t % NS, i = i0 + t;
         if (t >= NS) wait(&empty[s], ((t / NS) - 1) & 1);
@@ -519,35 +532,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id128 = ptx::idesc_bf16(BM, 2 * BN, 0, 0);
       constexpr uint32_t id64 = ptx::idesc_bf16(BM, BN, 0, 0);
       const uint32_t sSt = ptx::smem_u32(sm + Lay::oStage);
-      // Descriptors at K-step 0 of stage 0 (see the row pass).
-      const uint64_t dK = tc::kmajor_desc(ptx::smem_u32(sm + Lay::oK), BM, 0);
-      const uint64_t dB = tc::kmajor_desc(ptx::smem_u32(sm + Lay::oB), BM, 0);
-      const uint64_t dV = tc::kmajor_desc(ptx::smem_u32(sm + Lay::oV), BM, 0);
-      const uint64_t dC = tc::kmajor_desc(ptx::smem_u32(sm + Lay::oC), BM, 0);
+      // B descriptors at K-step 0 of stage 0 (a K-step adds 32 B, stage s adds s * kStage).
       const uint64_t dQA = tc::kmajor_desc(sSt, 2 * BN, 0);            // [Q_i; a_i], K-major
       const uint64_t dQk = tc::kmajor_desc(sSt, BN, 0);                // Q_i, K-major
       const uint64_t ddOk = tc::kmajor_desc(sSt + 2 * kTile, BN, 0);   // dO_i, K-major
-      const uint32_t tSG = tmem + Lay::cSG, tPH = tmem + Lay::cPH;
-      wait(k_full, 0);
+      const uint32_t tT = tmem + Lay::cT, tK = tmem + Lay::cK, tB = tmem + Lay::cB;
+      const uint32_t tV = tmem + Lay::cV, tC = tmem + Lay::cC;
+      wait(held_ready, 0);
       for (int t = 0; t < ntile; ++t) {
         const int s = t % NS;
         const uint32_t so = static_cast<uint32_t>(s * Lay::kStage);
         wait(&full[s], (t / NS) & 1);
-        if (t > 0) wait(consumed, (t - 1) & 1);
+        if (t > 0) wait(consumed_b, (t - 1) & 1);  // [dP^T | H^T] of block t-1 copied out of TMEM
         ptx::tc_fence_after();
+        // [S^T | K a^T] = K [Q_i; a_i]^T,  G^T += b Q_i^T
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          ptx::mma_ss_e(tSG, tc::desc_add(dK, 32 * kk), tc::desc_add(dQA, so + 32 * kk), id128, kk > 0);
+          ptx::mma_ts_e(tT, tK + 8 * kk, tc::desc_add(dQA, so + 32 * kk), id128, kk > 0);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          ptx::mma_ss_e(tSG + BN, tc::desc_add(dB, 32 * kk), tc::desc_add(dQk, so + 32 * kk), id64, 1u);
+          ptx::mma_ts_e(tT + BN, tB + 8 * kk, tc::desc_add(dQk, so + 32 * kk), id64, 1u);
+        ptx::mma_commit_e(sa_full);
+        wait(consumed_a, t & 1);  // [S^T | G^T] of block t copied out of TMEM
+        ptx::tc_fence_after();
+        // dP^T = V dO_i^T,  H^T = c dO_i^T
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          ptx::mma_ss_e(tPH, tc::desc_add(dV, 32 * kk), tc::desc_add(ddOk, so + 32 * kk), id64, kk > 0);
+          ptx::mma_ts_e(tT, tV + 8 * kk, tc::desc_add(ddOk, so + 32 * kk), id64, kk > 0);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          ptx::mma_ss_e(tPH + BN, tc::desc_add(dC, 32 * kk), tc::desc_add(ddOk, so + 32 * kk), id64, kk > 0);
-        ptx::mma_commit_e(s_full);
+          ptx::mma_ts_e(tT + BN, tC + 8 * kk, tc::desc_add(ddOk, so + 32 * kk), id64, kk > 0);
+        ptx::mma_commit_e(sb_full);
         ptx::mma_commit_e(&empty[s]);
       }
     }
@@ -568,10 +583,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k) {
           const uint32_t acc = (t > 0 || k > 0) ? 1u : 0u;
-          const uint32_t kb = so + 2048 * k;
-          ptx::mma_ts_e(tgV, tOp + k * 8, tc::desc_add(ddOm, kb), idO, acc);
-          ptx::mma_ts_e(tgK, tOp + 32 + k * 8, tc::desc_add(dAm, kb), idO, acc);
-          ptx::mma_ts_e(tgK, tOp + 64 + k * 8, tc::desc_add(dQm, kb), idO, 1u);
+          const uint32_t kb2 = so + 2048 * k;
+          // gV += dPbar^T dO_i,  gK += dS^T a_i + Sbar^T Q_i
+          ptx::mma_ts_e(tgV, tOp + k * 8, tc::desc_add(ddOm, kb2), idO, acc);
+          ptx::mma_ts_e(tgK, tOp + 32 + k * 8, tc::desc_add(dAm, kb2), idO, acc);
+          ptx::mma_ts_e(tgK, tOp + 64 + k * 8, tc::desc_add(dQm, kb2), idO, 1u);
         }
         ptx::mma_commit_e(&empty[s]);
         ptx::mma_commit_e(out_done);
@@ -584,62 +600,98 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lo = static_cast<uint32_t>(qd * 32) << 16;
     const int key = kb * BM + r;
     const int c0 = hf * 32;
+    {  // K, b, V, c rows of this key, elements 32 hf .. 32 hf + 31, into TMEM (A operands)
+      const __nv_bfloat16* src[4] = {Kp, Bp, Vp, Cp};
+      const uint32_t col[4] = {Lay::cK, Lay::cB, Lay::cV, Lay::cC};
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        uint32_t w[16];
+        if (key < N) {
+          const uint4* g = reinterpret_cast<const uint4*>(src[m] + (static_cast<size_t>(bh) * N + key) * D + c0);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint4 v = g[u];
+            w[4 * u] = v.x;
+            w[4 * u + 1] = v.y;
+            w[4 * u + 2] = v.z;
+            w[4 * u + 3] = v.w;
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < 16; ++u) w[u] = 0u;
+        }
+        ptx::tmem_st16(tmem + col[m] + static_cast<uint32_t>(hf * 16) + lo, w);
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(held_ready);
+    }
+    const uint64_t c2 = tc::pk2f(c, c), s2 = tc::pk2f(scale, scale);
+    const uint32_t tOpT = tmem + Lay::cOp + static_cast<uint32_t>(hf * 16) + lo;
     for (int t = 0; t < ntile; ++t) {
       const int s = t % NS, i = i0 + t;
-      wait(s_full, t & 1);
-      ptx::tc_fence_after();
-      uint32_t sv[32], gv[32], dv[32], hv[32];
-      ptx::tmem_ld32(tmem + Lay::cSG + c0 + lo, sv);
-      ptx::tmem_ld32(tmem + Lay::cSG + BN + c0 + lo, gv);
-      ptx::tmem_ld32(tmem + Lay::cPH + c0 + lo, dv);
-      ptx::tmem_ld32(tmem + Lay::cPH + BN + c0 + lo, hv);
-      ptx::tmem_wait_ld();
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(consumed);
-      // Row states of the 64 queries, pair-interleaved: float4 2m = (-L2, -L2', -D, -D'),
-      // float4 2m+1 = (-E, -E', -F, -F') of queries 2m, 2m+1 of the block.
+      // Row states of the 64 queries, pair-interleaved: float4 2m = (-L2, -L2', -E, -E'),
+      // float4 2m+1 = (-D, -D', -F', -F'') of queries 2m, 2m+1 of the block.
       const float4* stat =
           reinterpret_cast<const float4*>(sm + Lay::oStage + s * Lay::kStage + 3 * kTile) + c0;
       const int qbase = i * BN + c0;
-      const uint64_t c2 = tc::pk2f(c, c), s2 = tc::pk2f(scale, scale);
+      wait(sa_full, t & 1);
+      ptx::tc_fence_after();
+      uint32_t sv[32], gv[32];
+      ptx::tmem_ld32(tmem + Lay::cT + c0 + lo, sv);
+      ptx::tmem_ld32(tmem + Lay::cT + BN + c0 + lo, gv);
+      ptx::tmem_wait_ld();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(consumed_a);  // the tile warp may now write [dP^T | H^T]
+      uint64_t P2[16], GE2[16];
       uint32_t pDP[16], pDS[16], pSB[16];
-      auto block = [&](auto masked) {
+      auto first = [&](auto masked) {  // P and P (G - E) from [S^T | G^T]
 #pragma unroll
         for (int u = 0; u < 32; u += 2) {
-          const float4 A = stat[u], Bs = stat[u + 1];
-          const uint64_t nL = tc::pk2f(A.x, A.y), nD = tc::pk2f(A.z, A.w);
-          const uint64_t nE = tc::pk2f(Bs.x, Bs.y), nF = tc::pk2f(Bs.z, Bs.w);
-          const float2 arg = tc::unpk2(tc::fma2(tc::pk2(sv[u], sv[u + 1]), c2, nL));
+          const float4 A = stat[u];
+          const float2 arg = tc::unpk2(tc::fma2(tc::pk2(sv[u], sv[u + 1]), c2, tc::pk2f(A.x, A.y)));
           float p0 = ptx::ex2(arg.x), p1 = ptx::ex2(arg.y);
           if constexpr (decltype(masked)::value) {
             const int q0 = qbase + u;
             if (q0 < key || q0 >= N) p0 = 0.f;
             if (q0 + 1 < key || q0 + 1 >= N) p1 = 0.f;
           }
-          const uint64_t P2 = tc::pk2f(p0, p1);
-          const uint64_t G2 = tc::mul2(tc::pk2(gv[u], gv[u + 1]), s2);
-          const uint64_t dP2 = tc::pk2(dv[u], dv[u + 1]);
-          const uint64_t dmd = tc::add2(dP2, nD);                          // dP - D
-          const uint64_t ds2 = tc::mul2(P2, dmd);
-          const uint64_t dpb2 = tc::mul2(P2, tc::add2(G2, nE));            // P (G - E)
-          const uint64_t t2 = tc::fma2(G2, dmd, tc::mul2(nE, dP2));        // G (dP - D) - E dP
-          const uint64_t sb2 = tc::mul2(P2, tc::add2(tc::add2(t2, tc::pk2(hv[u], hv[u + 1])), nF));
-          const float2 vdp = tc::unpk2(dpb2), vds = tc::unpk2(ds2), vsb = tc::unpk2(sb2);
-          pDP[u >> 1] = ptx::pack_bf16(vdp.x, vdp.y);
-          pDS[u >> 1] = ptx::pack_bf16(vds.x, vds.y);
-          pSB[u >> 1] = ptx::pack_bf16(vsb.x, vsb.y);
+          const int idx = u >> 1;
+          P2[idx] = tc::pk2f(p0, p1);
+          GE2[idx] = tc::fma2(tc::pk2(gv[u], gv[u + 1]), s2, tc::pk2f(A.z, A.w));  // G - E
+          const float2 vdp = tc::unpk2(tc::mul2(P2[idx], GE2[idx]));
+          pDP[idx] = ptx::pack_bf16(vdp.x, vdp.y);
         }
       };
       // Causal mask only in the first blocks (queries before this CTA's last key) and
       // past N only in the last block.
       if (qbase < kb * BM + BM || qbase + 32 > N)
-        block(std::true_type{});
+        first(std::true_type{});
       else
-        block(std::false_type{});
+        first(std::false_type{});
+      wait(sb_full, t & 1);
+      ptx::tc_fence_after();
+      uint32_t dv[32], hv[32];
+      ptx::tmem_ld32(tmem + Lay::cT + c0 + lo, dv);
+      ptx::tmem_ld32(tmem + Lay::cT + BN + c0 + lo, hv);
+      ptx::tmem_wait_ld();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(consumed_b);  // the tile warp may now write the next block's [S^T | G^T]
+#pragma unroll
+      for (int u = 0; u < 32; u += 2) {  // dS and Sbar from [dP^T | H^T]
+        const float4 Bs = stat[u + 1];
+        const int idx = u >> 1;
+        const uint64_t dmd = tc::add2(tc::pk2(dv[u], dv[u + 1]), tc::pk2f(Bs.x, Bs.y));  // dP - D
+        const float2 vds = tc::unpk2(tc::mul2(P2[idx], dmd));
+        const uint64_t in = tc::add2(tc::fma2(GE2[idx], dmd, tc::pk2(hv[u], hv[u + 1])), tc::pk2f(Bs.z, Bs.w));
+        const float2 vsb = tc::unpk2(tc::mul2(P2[idx], in));
+        pDS[idx] = ptx::pack_bf16(vds.x, vds.y);
+        pSB[idx] = ptx::pack_bf16(vsb.x, vsb.y);
+      }
       if (t > 0) wait(out_done, (t - 1) & 1);  // block t-1's products have read the operand columns
-      ptx::tmem_st16(tmem + Lay::cOp + hf * 16 + lo, pDP);
-      ptx::tmem_st16(tmem + Lay::cOp + 32 + hf * 16 + lo, pDS);
-      ptx::tmem_st16(tmem + Lay::cOp + 64 + hf * 16 + lo, pSB);
+      ptx::tmem_st16(tOpT, pDP);
+      ptx::tmem_st16(tOpT + 32, pDS);
+      ptx::tmem_st16(tOpT + 64, pSB);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(ready);
@@ -658,12 +710,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         ov[u >> 1] = ptx::pack_bf16(f(av[u]), f(av[u + 1]));
         ok2[u >> 1] = ptx::pack_bf16(scale * f(bv[u]), scale * f(bv[u + 1]));
       }
-      uint4* dv = reinterpret_cast<uint4*>(gV + rowoff + c0);
-      uint4* dk = reinterpret_cast<uint4*>(gK + rowoff + c0);
+      uint4* dvp = reinterpret_cast<uint4*>(gV + rowoff + c0);
+      uint4* dkp = reinterpret_cast<uint4*>(gK + rowoff + c0);
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        dv[u] = make_uint4(ov[4 * u], ov[4 * u + 1], ov[4 * u + 2], ov[4 * u + 3]);
-        dk[u] = make_uint4(ok2[4 * u], ok2[4 * u + 1], ok2[4 * u + 2], ok2[4 * u + 3]);
+        dvp[u] = make_uint4(ov[4 * u], ov[4 * u + 1], ov[4 * u + 2], ov[4 * u + 3]);
+        dkp[u] = make_uint4(ok2[4 * u], ok2[4 * u + 1], ok2[4 * u + 2], ok2[4 * u + 3]);
       }
     }
   }
@@ -683,14 +735,12 @@ cudaError_t tc_bob(const Problem& p, const void* Q, const void* K, const void* V
                    void* gdO, float4* ws, int passes, cudaStream_t st) {
   if (p.d != D) return cudaErrorInvalidValue;
   alignas(64) CUtensorMap q128, do128, a128, k64, v64, b64, c64;
-  alignas(64) CUtensorMap k128, b128, v128, c128, q64, a64, do64, s64;
+  alignas(64) CUtensorMap q64, a64, do64, s64;
   const int64_t N = p.N, BH = p.BH, Np = (p.N + 1) & ~static_cast<int64_t>(1);
   if (!make_tmap_bf16(&q128, Q, N, D, BH, BM) || !make_tmap_bf16(&do128, dO, N, D, BH, BM) ||
       !make_tmap_bf16(&a128, a, N, D, BH, BM) || !make_tmap_bf16(&k64, K, N, D, BH, BN) ||
       !make_tmap_bf16(&v64, V, N, D, BH, BN) || !make_tmap_bf16(&b64, b, N, D, BH, BN) ||
-      !make_tmap_bf16(&c64, cc, N, D, BH, BN) || !make_tmap_bf16(&k128, K, N, D, BH, BM) ||
-      !make_tmap_bf16(&b128, b, N, D, BH, BM) || !make_tmap_bf16(&v128, V, N, D, BH, BM) ||
-      !make_tmap_bf16(&c128, cc, N, D, BH, BM) || !make_tmap_bf16(&q64, Q, N, D, BH, BN) ||
+      !make_tmap_bf16(&c64, cc, N, D, BH, BN) || !make_tmap_bf16(&q64, Q, N, D, BH, BN) ||
       !make_tmap_bf16(&a64, a, N, D, BH, BN) || !make_tmap_bf16(&do64, dO, N, D, BH, BN) ||
       !make_tmap_stats(&s64, ws, Np, BH, BN))
     return cudaErrorInvalidValue;
@@ -710,8 +760,9 @@ cudaError_t tc_bob(const Problem& p, const void* Q, const void* K, const void* V
   e = cudaFuncSetAttribute(bob_col_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ColLay::bytes);
   if (e != cudaSuccess) return e;
   bob_col_kernel<<<static_cast<unsigned>(nrb * BH), kThreads, ColLay::bytes, st>>>(
-      k128, b128, v128, c128, q64, a64, do64, s64, static_cast<__nv_bfloat16*>(gK), static_cast<__nv_bfloat16*>(gV),
-      static_cast<int>(N), static_cast<int>(BH), p.scale, c);
+      q64, a64, do64, s64, static_cast<const __nv_bfloat16*>(K), static_cast<const __nv_bfloat16*>(b),
+      static_cast<const __nv_bfloat16*>(V), static_cast<const __nv_bfloat16*>(cc), static_cast<__nv_bfloat16*>(gK),
+      static_cast<__nv_bfloat16*>(gV), static_cast<int>(N), static_cast<int>(BH), p.scale, c);
   return cudaGetLastError();
 }
 

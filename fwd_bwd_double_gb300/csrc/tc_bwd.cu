@@ -284,13 +284,14 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
         for (int u = 0; u < 4; ++u) dst[u] = make_uint4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
       }
     }
-    if (live && hf == 0) {  // row statistics, negated, pair-interleaved (see the column pass)
+    if (hf == 0 && row < Np) {  // row statistics, negated, pair-interleaved (see the column pass)
+      // The row past N of an odd-length slice gets zeros: the column pass reads it (with P = 0).
       float* wf = reinterpret_cast<float*>(ws) + static_cast<size_t>(bh) * Np * 4;
       const int64_t k2 = row & ~static_cast<int64_t>(1);
       const int odd = static_cast<int>(row & 1);
-      wf[k2 * 4 + odd] = -L2;
-      wf[k2 * 4 + 2 + odd] = -Dr;
-      wf[(k2 + 1) * 4 + odd] = -rho;
+      wf[k2 * 4 + odd] = live ? -L2 : 0.f;
+      wf[k2 * 4 + 2 + odd] = live ? -Dr : 0.f;
+      wf[(k2 + 1) * 4 + odd] = live ? -rho : 0.f;
       wf[(k2 + 1) * 4 + 2 + odd] = 0.f;
     }
   }

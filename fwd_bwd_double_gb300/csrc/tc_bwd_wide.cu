@@ -254,15 +254,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint4* dst = reinterpret_cast<uint4*>(dQ + rowoff + cg * DG);
       dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
       dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
-      if (cg == 0) {  // row statistics, negated, pair-interleaved (format shared with tc_bwd.cu)
-        float* wf = reinterpret_cast<float*>(ws) + static_cast<size_t>(bh) * Np * 4;
-        const int64_t k2 = row & ~static_cast<int64_t>(1);
-        const int odd = static_cast<int>(row & 1);
-        wf[k2 * 4 + odd] = -L2;
-        wf[k2 * 4 + 2 + odd] = -Dr;
-        wf[(k2 + 1) * 4 + odd] = 0.f;
-        wf[(k2 + 1) * 4 + 2 + odd] = 0.f;
-      }
+    }
+    if (cg == 0 && row < Np) {  // row statistics, negated, pair-interleaved (format shared with tc_bwd.cu)
+      // The row past N of an odd-length slice gets zeros: the column pass reads it (with P = 0).
+      float* wf = reinterpret_cast<float*>(ws) + static_cast<size_t>(bh) * Np * 4;
+      const int64_t k2 = row & ~static_cast<int64_t>(1);
+      const int odd = static_cast<int>(row & 1);
+      wf[k2 * 4 + odd] = live ? -L2 : 0.f;
+      wf[k2 * 4 + 2 + odd] = live ? -Dr : 0.f;
+      wf[(k2 + 1) * 4 + odd] = 0.f;
+      wf[(k2 + 1) * 4 + 2 + odd] = 0.f;
     }
   }
 
