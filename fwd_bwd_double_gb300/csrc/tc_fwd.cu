@@ -18,9 +18,12 @@
 //
 // Warp roles (192 threads): warps 0-3 own TMEM lanes 0-127, one query row per
 // thread (softmax, rescale, epilogue); warp 4 issues TMA loads (Q once, K/V
-// through a 2-stage ring); warp 5 allocates TMEM and issues the MMAs.  With d = 64
-// two CTAs fit on an SM (80 KB shared, 256 TMEM columns each), so one CTA's
-// softmax overlaps the other's MMAs.
+// through a 3-stage ring); warp 5 allocates TMEM and issues the MMAs.  The softmax
+// warps copy S_j into registers and release it at once (`s_consumed`), so
+// S_{j+1} = Q K_{j+1}^T runs on the tensor pipe while they exponentiate S_j; P_j
+// is written into its TMEM columns, and O rescaled, only after P_{j-1} V_{j-1}
+// has finished (`pv_done`).  With d = 64 two CTAs fit on an SM (256 TMEM columns
+// each), so one CTA's softmax also overlaps the other's MMAs.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -73,9 +76,11 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
   uint64_t* full = bars + 1;            // [NS]
   uint64_t* empty = bars + 1 + NS;      // [NS]
   uint64_t* s_full = bars + 1 + 2 * NS;
-  uint64_t* p_ready = s_full + 1;
+  uint64_t* p_ready = s_full + 1;     // P_j in TMEM and O rescaled
   uint64_t* o_full = s_full + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 3);
+  uint64_t* s_consumed = s_full + 3;  // S_j copied into the softmax registers
+  uint64_t* pv_done = s_full + 4;     // P_j V_j finished: P columns and O free
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -93,6 +98,8 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
     ptx::mbar_init(s_full, 1);
     ptx::mbar_init(p_ready, 128);
     ptx::mbar_init(o_full, 1);
+    ptx::mbar_init(s_consumed, 128);
+    ptx::mbar_init(pv_done, 1);
     // The swizzled operand layout needs 1024-byte aligned tiles.
     *abort_flag = (ptx::smem_u32(sm) & 1023u) ? 1 : 0;
     if (*abort_flag) atomicOr(&g_err, FBD_ERR_TIMEOUT);
@@ -141,22 +148,9 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
       const uint64_t dQ = kmajor_desc(ptx::smem_u32(sm + Lay::oQ), BM, 0);
       const uint64_t dK = kmajor_desc(ptx::smem_u32(sm + Lay::oK), BN, 0);
       const uint64_t dV = mnmajor_desc(ptx::smem_u32(sm + Lay::oV), BN, 0);
-      auto issue_pv = [&](int j) {
-        const uint32_t so = static_cast<uint32_t>((j % NS) * Lay::kKV);
-#pragma unroll
-        for (int k = 0; k < BN / 16; ++k)
-          ptx::mma_ts_e(tO, tP + k * 8, tc::desc_add(dV, so + k * 16 * 128), idO, (j > 0 || k > 0) ? 1u : 0u);
-        ptx::mma_commit_e(&empty[j % NS]);
-      };
-      wait(q_full, 0);
-      for (int j = 0; j < nkv; ++j) {
+      auto issue_s = [&](int j) {  // S_j = Q K_j^T
         const int s = j % NS;
         wait(&full[s], (j / NS) & 1);
-        if (j > 0) {
-          wait(p_ready, (j - 1) & 1);  // P_{j-1} written, S free, O rescaled
-          ptx::tc_fence_after();
-          issue_pv(j - 1);
-        }
         ptx::tc_fence_after();
         const uint32_t so = static_cast<uint32_t>(s * Lay::kKV);
 #pragma unroll
@@ -164,10 +158,23 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
           ptx::mma_ss_e(tS, tc::desc_add(dQ, tc::kmajor_off(BM, kk)), tc::desc_add(dK, so + tc::kmajor_off(BN, kk)), idS,
                       kk > 0 ? 1u : 0u);
         ptx::mma_commit_e(s_full);
+      };
+      wait(q_full, 0);
+      issue_s(0);
+      for (int j = 0; j < nkv; ++j) {
+        if (j + 1 < nkv) {
+          wait(s_consumed, j & 1);  // S_j is in the softmax registers: the S columns are free
+          issue_s(j + 1);
+        }
+        wait(p_ready, j & 1);  // P_j written, O rescaled
+        ptx::tc_fence_after();
+        const uint32_t so = static_cast<uint32_t>((j % NS) * Lay::kKV);
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k)
+          ptx::mma_ts_e(tO, tP + k * 8, tc::desc_add(dV, so + k * 16 * 128), idO, (j > 0 || k > 0) ? 1u : 0u);
+        ptx::mma_commit_e(&empty[j % NS]);
+        ptx::mma_commit_e(pv_done);
       }
-      wait(p_ready, (nkv - 1) & 1);
-      ptx::tc_fence_after();
-      issue_pv(nkv - 1);
       ptx::mma_commit_e(o_full);
     }
   } else {
@@ -185,6 +192,8 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) ptx::tmem_ld32(tS + lane_off + ch * 32, v[ch]);
       ptx::tmem_wait_ld();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(s_consumed);  // the MMA warp may now compute S_{j+1} into these columns
       if (diag) {
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch)
@@ -211,19 +220,22 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
       // Packed f32x2: (s - m) then * s log2 e for two keys per instruction.
       const uint64_t nm2 = tc::pk2f(-m, -m), c2 = tc::pk2f(scale_log2, scale_log2);
       uint64_t rs4[4] = {0, 0, 0, 0};
+      uint32_t pk[4][16];  // P_j as bf16 pairs, written once P_{j-1} V_{j-1} is done
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
-        uint32_t pk[16];
 #pragma unroll
         for (int t = 0; t < 32; t += 2) {
           const float2 arg = tc::unpk2(tc::mul2(tc::add2(tc::pk2(v[ch][t], v[ch][t + 1]), nm2), c2));
           const float p0 = ptx::ex2(arg.x), p1 = ptx::ex2(arg.y);
           const uint64_t P2 = tc::pk2f(p0, p1);
           rs4[(t >> 1) & 3] = tc::add2(rs4[(t >> 1) & 3], P2);
-          pk[t >> 1] = ptx::pack_bf16(p0, p1);
+          pk[ch][t >> 1] = ptx::pack_bf16(p0, p1);
         }
-        ptx::tmem_st16(tP + lane_off + ch * 16, pk);  // keys ch*32 .. ch*32+31
       }
+      if (j > 0) wait(pv_done, (j - 1) & 1);  // P_{j-1} V_{j-1} has read the P columns and updated O
+      ptx::tc_fence_after();
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) ptx::tmem_st16(tP + lane_off + ch * 16, pk[ch]);  // keys ch*32 .. ch*32+31
       const float2 rsa = tc::unpk2(tc::add2(tc::add2(rs4[0], rs4[1]), tc::add2(rs4[2], rs4[3])));
       const float rs = rsa.x + rsa.y;
       if (__any_sync(0xffffffffu, moved)) {  // rescale O for rows whose max moved
