@@ -383,50 +383,71 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     const int qd = warp & 3, cg = warp >> 2;
-    const int r = qd * 32 + lane;  // key row of the held block (TMEM lane)
+    const int r = qd * 32 + lane;  // key row of the held block (TMEM lane) in the epilogue
     const uint32_t lo = static_cast<uint32_t>(qd * 32) << 16;
     const int key = kb * BW + r;
     const int c0 = cg * kC;
+    // Score tiles are read with the 16-lane shapes, so that a thread sees 8 queries
+    // of its 32 (pairs 2(t%4) + 8k, k < 4) for 4 keys (quarter rows t/4 + 8m, m < 4):
+    // the row statistics of 4 query pairs stay in registers for the whole block.
+    const int g4 = lane >> 2, q4 = lane & 3;
     const uint64_t c2 = tc::pk2f(c, c);
     for (int t = 0; t < ntile; ++t) {
       const int s = t % NS, i = kb + t;
       wait(sy.s_full, t & 1);
       ptx::tc_fence_after();
-      uint32_t sv[kC], pv[kC];
-      ptx::tmem_ld32(tmem + Lay::cS + c0 + lo, sv);
-      ptx::tmem_ld32(tmem + Lay::cdP + c0 + lo, pv);
+      uint32_t sv[2][16], pv[2][16];  // [lanes +0 / +16 of the quarter][repetition k, (row, row+8) x (col, col+1)]
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t la = lo + (static_cast<uint32_t>(16 * h) << 16);
+        ptx::tmem_ld16x256_x4(tmem + Lay::cS + c0 + la, sv[h]);
+        ptx::tmem_ld16x256_x4(tmem + Lay::cdP + c0 + la, pv[h]);
+      }
       ptx::tmem_wait_ld();
       ptx::tc_fence_before();
       ptx::mbar_arrive(sy.consumed);
       // Statistics of the block's queries, pair-interleaved and negated:
       // float4 2m = (-L2, -L2', -D, -D') of queries 2m, 2m+1.
       const float4* st = reinterpret_cast<const float4*>(sm + Lay::oStage + s * Lay::kStage + 2 * kTile) + c0;
-      const int qbase = i * BW + c0;
-      uint32_t pk[kC / 2], dk[kC / 2];
+      float4 A[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) A[k] = st[8 * k + 2 * q4];
+      const int qbase = i * BW + c0 + 2 * q4;   // query of column (k = 0, col 0)
+      const int kbase = kb * BW + qd * 32 + g4;  // key of (h = 0, row 0)
+      uint32_t pk[2][8], dk[2][8];  // [h][2k + (row, row+8)]
       auto block = [&](auto masked) {
 #pragma unroll
-        for (int u = 0; u < kC; u += 2) {
-          const float4 A = st[u];
-          const float2 arg = tc::unpk2(tc::fma2(tc::pk2(sv[u], sv[u + 1]), c2, tc::pk2f(A.x, A.y)));
-          float p0 = ptx::ex2(arg.x), p1 = ptx::ex2(arg.y);
-          if constexpr (decltype(masked)::value) {
-            const int q0 = qbase + u;
-            if (q0 < key || q0 >= N) p0 = 0.f;
-            if (q0 + 1 < key || q0 + 1 >= N) p1 = 0.f;
-          }
-          const float2 ds =
-              tc::unpk2(tc::mul2(tc::pk2f(p0, p1), tc::add2(tc::pk2(pv[u], pv[u + 1]), tc::pk2f(A.z, A.w))));
-          pk[u >> 1] = ptx::pack_bf16(p0, p1);
-          dk[u >> 1] = ptx::pack_bf16(ds.x, ds.y);
-        }
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+              const int e = 4 * k + 2 * m;
+              const float2 arg =
+                  tc::unpk2(tc::fma2(tc::pk2(sv[h][e], sv[h][e + 1]), c2, tc::pk2f(A[k].x, A[k].y)));
+              float p0 = ptx::ex2(arg.x), p1 = ptx::ex2(arg.y);
+              if constexpr (decltype(masked)::value) {
+                const int q0 = qbase + 8 * k, kk = kbase + 16 * h + 8 * m;
+                if (q0 < kk || q0 >= N) p0 = 0.f;
+                if (q0 + 1 < kk || q0 + 1 >= N) p1 = 0.f;
+              }
+              const float2 ds = tc::unpk2(
+                  tc::mul2(tc::pk2f(p0, p1), tc::add2(tc::pk2(pv[h][e], pv[h][e + 1]), tc::pk2f(A[k].z, A[k].w))));
+              pk[h][2 * k + m] = ptx::pack_bf16(p0, p1);
+              dk[h][2 * k + m] = ptx::pack_bf16(ds.x, ds.y);
+            }
       };
-      if (t == 0 || qbase + kC > N)  // the diagonal block, or the block reaching past N
+      if (t == 0 || i * BW + c0 + kC > N)  // the diagonal block, or the block reaching past N
         block(std::true_type{});
       else
         block(std::false_type{});
       if (t > 0) wait(sy.out_done, (t - 1) & 1);  // the previous block's products have read P, dS
-      ptx::tmem_st16(tmem + Lay::cP + c0 / 2 + lo, pk);
-      ptx::tmem_st16(tmem + Lay::cdS + c0 / 2 + lo, dk);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t la = lo + (static_cast<uint32_t>(16 * h) << 16);
+        ptx::tmem_st16x128_x4(tmem + Lay::cP + c0 / 2 + la, pk[h]);
+        ptx::tmem_st16x128_x4(tmem + Lay::cdS + c0 / 2 + la, dk[h]);
+      }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(sy.ready);
