@@ -229,23 +229,54 @@ def run_ours(args, w, rank, world):
 
     bwd0, bwd1 = time_bwd(0), time_bwd(1)
 
-    # End to end: pinned host inputs -> device, the step, all outputs -> host, every step.
+    # End to end: every step copies its 7 inputs from pinned host memory to the device,
+    # runs the five launches and copies O, lse and the 7 outputs back to pinned host
+    # memory.  The copies of step i+1's inputs and of step i-1's outputs run on their
+    # own streams (the GPU's copy engines) while step i computes; input and output
+    # device buffers are double-buffered, and events order reuse.
     host_out = {k: torch.empty(shp, dtype=bf).pin_memory() for k in out}
     host_lse = torch.empty(shp[:3], dtype=torch.float32).pin_memory()
-    e2e_steps = max(2, min(args.steps, 5))
+    e2e_steps = max(4, min(args.steps, 8))
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    xin = [{k: torch.empty_like(v) for k, v in x.items()} for _ in range(2)]
+    outs = [{k: torch.empty(shp, dtype=bf, device=dev) for k in out} for _ in range(2)]
+    lses = [torch.empty(shp[:3], dtype=torch.float32, device=dev) for _ in range(2)]
+
+    def e2e_step(xx, oo, ll):
+        fbd.attn_fwd(xx["Q"], xx["K"], xx["V"], O=oo["O"], lse=ll, stream=stream, desc=desc)
+        fbd.attn_bwd(xx["Q"], xx["K"], xx["V"], oo["O"], xx["dO"], ll, gproj=args.gproj, dQ=oo["dQ"], dK=oo["dK"],
+                     dV=oo["dV"], workspace=ws, stream=stream, desc=desc)
+        fbd.attn_bob(xx["Q"], xx["K"], xx["V"], oo["O"], xx["dO"], ll, xx["gdQ"], xx["gdK"], xx["gdV"], gQ=oo["gQ"],
+                     gK=oo["gK"], gV=oo["gV"], gdO=oo["gdO"], workspace=ws2, stream=stream, desc=desc)
+
+    ev = lambda: torch.cuda.Event(enable_timing=False)
+    in_done = [ev() for _ in range(e2e_steps)]
+    comp_done = [ev() for _ in range(e2e_steps)]
+    out_done = [ev() for _ in range(e2e_steps)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    xin = {k: torch.empty_like(v) for k, v in x.items()}
     torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            for k in xin:
-                xin[k].copy_(pinned[k], non_blocking=True)
-            step(xin)
+    e0.record(s_in)
+    for i in range(e2e_steps):
+        b = i % 2
+        if i >= 2:
+            s_in.wait_event(comp_done[i - 2])  # step i-2 has read this input buffer
+        with torch.cuda.stream(s_in):
+            for k in xin[b]:
+                xin[b][k].copy_(pinned[k], non_blocking=True)
+        in_done[i].record(s_in)
+        stream.wait_event(in_done[i])
+        if i >= 2:
+            stream.wait_event(out_done[i - 2])  # step i-2's outputs have left this buffer
+        with torch.cuda.stream(stream):
+            e2e_step(xin[b], outs[b], lses[b])
+        comp_done[i].record(stream)
+        s_out.wait_event(comp_done[i])
+        with torch.cuda.stream(s_out):
             for k in out:
-                host_out[k].copy_(out[k], non_blocking=True)
-            host_lse.copy_(lse, non_blocking=True)
-        e1.record(stream)
+                host_out[k].copy_(outs[b][k], non_blocking=True)
+            host_lse.copy_(lses[b], non_blocking=True)
+        out_done[i].record(s_out)
+    e1.record(s_out)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     h2d = sum(v.numel() * v.element_size() for v in pinned.values())
