@@ -43,6 +43,37 @@ DENSE_CONTRACTIONS = {"fwd": 2, "bwd_row": 3, "bwd_col": 2, "bob_row": 9, "bob_c
 EXECUTED_CONTRACTIONS = {"fwd": 2, "bwd_row": 3, "bwd_col": 4, "bob_row": 11, "bob_col": 8}
 
 
+def dist_init(world, backend="nccl"):
+    """One process per GPU: join the job's process group (rendezvous from the
+    torchrun environment: RANK, WORLD_SIZE, MASTER_ADDR, MASTER_PORT)."""
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend, init_method="env://")
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value, world, device="cpu"):
+    """The largest of the ranks' values (the slowest rank's step time)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_rank_step, world, ms_max):
+    """Whole-job throughput: every rank processes its own copy of the workload
+    (independent replicas), timed by the slowest rank."""
+    return flops_per_rank_step * world / (ms_max * 1e-3) / 1e12
+
+
 def dense_flops(w, op):
     unit = w.B * w.H * w.N * w.N * w.d / 2.0
     return {"fwd": 4, "bwd": 10, "bob": 24}[op] * unit
@@ -181,13 +212,8 @@ def run_ours(args, w, rank, world):
     torch.cuda.synchronize()
     fbd.attn_device_status(stream)
 
-    def barrier():
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
-
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
-    barrier()
+    barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(dev.index) as clk:
         t0 = time.perf_counter()
@@ -196,7 +222,7 @@ def run_ours(args, w, rank, world):
                 step(x, ev=evs[k])
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
-    barrier()
+    barrier(world)
     fbd.attn_device_status(stream)
     per_kernel = {kn: [evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps)]
                   for i, kn in enumerate(KERNELS)}
@@ -205,12 +231,7 @@ def run_ours(args, w, rank, world):
               "bob": [x + y for x, y in zip(per_kernel["bob_row"], per_kernel["bob_col"])]}
     step_ms = [sum(per_op[op][k] for op in per_op) for k in range(args.steps)]
     ms = statistics.mean(step_ms)
-    ms_max = ms
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
+    ms_max = max_over_ranks(ms, world, dev)
     flops_step = sum(dense_flops(w, op) for op in per_op)
 
     # GProj overhead on the backward alone (same inputs), reported beside the step.
@@ -426,14 +447,12 @@ def main():
                                   "d2h_bytes_per_step": 0}}))
         return
 
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
+    dist_init(world)
     import __graft_entry__
     __graft_entry__.build()
     r = run_ours(args, w, rank, world)
     pk = peaks()
-    value = r["flops_step"] * world / (r["ms_max"] * 1e-3) / 1e12
+    value = job_tflops(r["flops_step"], world, r["ms_max"])
     # Dominant kernel: the longest of the five launches of a step.
     dom = max(r["per_kernel"], key=lambda kn: r["per_kernel"][kn])
     ach = kernel_flops(w, dom, DENSE_CONTRACTIONS) / (r["per_kernel"][dom] * 1e-3) / 1e12
