@@ -134,7 +134,10 @@ def test_full_day_ragged_tail():
 def test_large_key_gproj_reduces_dQ_error():
     """GProj page, "How the zero sum turns into a false gradient": large shared key
     mean + near-copy queries.  Reports the median per-row relative dQ error with and
-    without GProj on batches 0-1 (16 slices) against the exact fp64 dQ."""
+    without GProj on batches 0-1 (16 slices) against the exact fp64 dQ, and beside
+    them the cheaper fix the page compares against: subtracting the mean key of each
+    slice before attention (softmax does not change when every key moves by the same
+    vector, so the exact dQ is the same; the caller centres K and rounds it to bf16)."""
     import fwd_bwd_double_gb300 as fbd
     w = W.LARGE_KEY
     x = W.inputs(w)
@@ -142,20 +145,26 @@ def test_large_key_gproj_reduces_dQ_error():
     O, lse = fbd.attn_fwd(xd["Q"], xd["K"], xd["V"], scale=w.scale)
     dQ0, dK0, _ = fbd.attn_bwd(xd["Q"], xd["K"], xd["V"], O, xd["dO"], lse, gproj=0, scale=w.scale)
     dQ1, dK1, dV1 = fbd.attn_bwd(xd["Q"], xd["K"], xd["V"], O, xd["dO"], lse, gproj=1, scale=w.scale)
+    Kc = W.round_to_bf16((x["K"] - x["K"].astype(np.float64).mean(axis=2, keepdims=True)).astype(np.float32))
+    xc = to_device({"K": Kc}, w)
+    Oc, lsec = fbd.attn_fwd(xd["Q"], xc["K"], xd["V"], scale=w.scale)
+    dQc, _, _ = fbd.attn_bwd(xd["Q"], xc["K"], xd["V"], Oc, xd["dO"], lsec, gproj=0, scale=w.scale)
     fbd.attn_device_status()
-    e0, e1, maxp = [], [], []
+    e0, e1, ec, maxp = [], [], [], []
     for b in range(2):
         for h in range(w.H):
             s = {k: x[k][b, h].astype(np.float64) for k in ("Q", "K", "V", "dO")}
             ref = oracle.backward(s["Q"], s["K"], s["V"], s["dO"], scale=w.scale)
             e0.append(row_rel_errors(host(dQ0[b, h]), ref["dQ"]))
             e1.append(row_rel_errors(host(dQ1[b, h]), ref["dQ"]))
+            ec.append(row_rel_errors(host(dQc[b, h]), ref["dQ"]))
             P, _ = oracle.softmax_rows(oracle.scores(s["Q"], s["K"], np.arange(256, 2048, 64), w.scale))
             maxp.append(P.max(axis=1))
-    m0, m1 = float(np.median(np.concatenate(e0))), float(np.median(np.concatenate(e1)))
-    print(f"{w.name}: median row dQ rel err no-GProj {m0:.4e}, GProj {m1:.4e}; "
+    m0, m1, mc = (float(np.median(np.concatenate(e))) for e in (e0, e1, ec))
+    print(f"{w.name}: median row dQ rel err no-GProj {m0:.4e}, GProj {m1:.4e}, mean-key subtraction {mc:.4e}; "
           f"median row max P {float(np.median(np.concatenate(maxp))):.3f}")
     assert m1 < m0
+    assert mc < m0
 
 
 def test_large_key_projected_rows_sum_to_zero():
