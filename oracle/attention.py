@@ -1,16 +1,17 @@
-"""CPU fp64 oracle for causal softmax attention, its backward and its backward-over-backward.
+"""CPU fp64 oracle for softmax attention (causal by default), its backward and its backward-over-backward.
 
 TEST INFRASTRUCTURE ONLY.  Nothing in the library's product path may import this
 module: only the tests, the smoke check and the benchmark's CPU-baseline leg use it.
 It shares no code with the CUDA path.
 
 Everything here is the plain definition written out in float64 with S and P
-materialised, one block of query rows at a time (the rows of a block see keys
-0..max(row)).  Row blocking changes nothing in the arithmetic: every output row
-or column is the same sum of the same terms.
+materialised, one block of query rows at a time (with the causal mask the rows of
+a block see keys 0..max(row); without it, every key).  Row blocking changes nothing
+in the arithmetic: every output row or column is the same sum of the same terms.
 
 Notation (one (batch, head) slice; Q, K, V, dO, a, b, c are [N, d]):
-  s = 1/sqrt(d) unless given;  S = s Q K^T with S_ij = -inf for j > i (causal);
+  s = 1/sqrt(d) unless given;  S = s Q K^T with S_ij = -inf for j > i when causal
+  (the default; causal=False keeps every key);
   L_i = log sum_j exp(S_ij);   P = exp(S - L);   O = P V.
 Sources:
   * forward and stored statistics: "Flash attention for trading models", sections
@@ -63,9 +64,12 @@ def _panel_budget(n_keys: int, mats: int = 8) -> int:
 # Forward (two-pass softmax, materialised)
 # ---------------------------------------------------------------------------
 
-def scores(Q, K, rows, scale):
-    """S[rows, 0..max(rows)] = scale * Q[rows] K^T with the causal mask (-inf for j > i)."""
+def scores(Q, K, rows, scale, causal=True):
+    """S[rows, keys] = scale * Q[rows] K^T: with the causal mask the keys are
+    0..max(rows) and S = -inf for j > i; without it, all keys."""
     rows = np.asarray(rows)
+    if not causal:
+        return scale * (Q[rows] @ K.T)
     kmax = int(rows.max()) + 1
     S = scale * (Q[rows] @ K[:kmax].T)
     S[np.arange(kmax)[None, :] > rows[:, None]] = NEG_INF
@@ -84,8 +88,8 @@ def softmax_rows(S):
     return E / l[:, None], L
 
 
-def forward(Q, K, V, scale=None, block=None):
-    """Causal attention forward for one slice: returns (O [N,d], L [N])."""
+def forward(Q, K, V, scale=None, block=None, causal=True):
+    """Attention forward for one slice: returns (O [N,d], L [N])."""
     Q, K, V = _f64(Q), _f64(K), _f64(V)
     N, d = Q.shape
     scale = default_scale(d) if scale is None else scale
@@ -93,28 +97,28 @@ def forward(Q, K, V, scale=None, block=None):
     L = np.empty(N)
     block = block or _panel_budget(N, 3)
     for r in _blocks(np.arange(N), block):
-        P, Lr = softmax_rows(scores(Q, K, r, scale))
+        P, Lr = softmax_rows(scores(Q, K, r, scale, causal))
         O[r] = P @ V[:P.shape[1]]
         L[r] = Lr
     return O, L
 
 
-def forward_rows(Q, K, V, rows, scale=None):
-    """O[rows], L[rows] only (each row needs keys 0..row): for sampled checks at large N."""
+def forward_rows(Q, K, V, rows, scale=None, causal=True):
+    """O[rows], L[rows] only (a causal row needs keys 0..row): for sampled checks at large N."""
     Q, K, V = _f64(Q), _f64(K), _f64(V)
     scale = default_scale(Q.shape[1]) if scale is None else scale
     rows = np.asarray(rows)
     O = np.empty((len(rows), Q.shape[1]))
     L = np.empty(len(rows))
     order = np.argsort(rows)
-    for blk in _blocks(order, _panel_budget(int(rows.max()) + 1, 3)):
-        P, Lr = softmax_rows(scores(Q, K, rows[blk], scale))
+    for blk in _blocks(order, _panel_budget(int(rows.max()) + 1 if causal else len(K), 3)):
+        P, Lr = softmax_rows(scores(Q, K, rows[blk], scale, causal))
         O[blk] = P @ V[:P.shape[1]]
         L[blk] = Lr
     return O, L
 
 
-def forward_online(Q, K, V, Br, Bc, scale=None):
+def forward_online(Q, K, V, Br, Bc, scale=None, causal=True):
     """The tiled forward with the online softmax recurrence, in the pages' order.
 
     "Flash attention for trading models", sections "The Flash Attention algorithm"
@@ -123,7 +127,7 @@ def forward_online(Q, K, V, Br, Bc, scale=None):
     the output O start at (-inf, 0, 0); every key/value block contributes its local
     max, its exponentials and local sum, and the running state is rescaled so that
     it is as if the new max had been known from the start.  Key blocks entirely in
-    the future of a query block are skipped (section on causal masking).  Exact
+    the future of a query block are skipped when causal (section on causal masking).  Exact
     arithmetic gives the two-pass result; this is used only to pin that fact.
     Returns (O, L) with L = m + log l.
     """
@@ -139,10 +143,11 @@ def forward_online(Q, K, V, Br, Bc, scale=None):
         li = np.zeros(len(qi))
         for k0 in range(0, N, Bc):
             kj = np.arange(k0, min(k0 + Bc, N))
-            if kj[0] > qi[-1]:
+            if causal and kj[0] > qi[-1]:
                 break  # the whole block is in the future of every query: never loaded
             Sij = scale * (Q[qi] @ K[kj].T)
-            Sij[kj[None, :] > qi[:, None]] = NEG_INF
+            if causal:
+                Sij[kj[None, :] > qi[:, None]] = NEG_INF
             mij = Sij.max(axis=1)
             # a row whose keys in this block are all masked contributes nothing
             live = np.isfinite(mij)
@@ -164,13 +169,14 @@ def forward_online(Q, K, V, Br, Bc, scale=None):
 # Row-block quantities shared by the first and second backward
 # ---------------------------------------------------------------------------
 
-def _row_terms(Q, K, V, dO, rows, scale, a=None, b=None, c=None):
+def _row_terms(Q, K, V, dO, rows, scale, a=None, b=None, c=None, causal=True):
     """All per-row-block tiles of the first backward (and of BoB if a, b, c given).
 
-    Keys are 0..max(rows).  Returns a dict of [len(rows), n_keys] matrices and
-    per-row vectors.  Everything is computed from Q, K, V, dO alone (the statistics
-    are recomputed, as the oracle has no stored ones to trust)."""
-    S = scores(Q, K, rows, scale)
+    Keys are 0..max(rows) when causal, else all keys.  Returns a dict of
+    [len(rows), n_keys] matrices and per-row vectors.  Everything is computed from
+    Q, K, V, dO alone (the statistics are recomputed, as the oracle has no stored
+    ones to trust)."""
+    S = scores(Q, K, rows, scale, causal)
     P, L = softmax_rows(S)
     nk = P.shape[1]
     dP = dO[rows] @ V[:nk].T
@@ -180,9 +186,10 @@ def _row_terms(Q, K, V, dO, rows, scale, a=None, b=None, c=None):
     if a is not None:
         G = scale * (a[rows] @ K[:nk].T + Q[rows] @ b[:nk].T)
         Hm = dO[rows] @ c[:nk].T
-        mask = np.arange(nk)[None, :] > rows[:, None]
-        G[mask] = 0.0
-        Hm[mask] = 0.0
+        if causal:
+            mask = np.arange(nk)[None, :] > rows[:, None]
+            G[mask] = 0.0
+            Hm[mask] = 0.0
         E = (P * G).sum(axis=1)
         dPbar = P * (G - E[:, None])
         Pbar = G * (dP - D[:, None]) - E[:, None] * dP + Hm
@@ -196,7 +203,7 @@ def _row_terms(Q, K, V, dO, rows, scale, a=None, b=None, c=None):
 # First backward
 # ---------------------------------------------------------------------------
 
-def backward(Q, K, V, dO, scale=None, block=None):
+def backward(Q, K, V, dO, scale=None, block=None, causal=True):
     """Vector-Jacobian product of O = attn(Q, K, V) against dO, for one slice.
 
     Returns dict(dQ, dK, dV, D, L)."""
@@ -206,7 +213,7 @@ def backward(Q, K, V, dO, scale=None, block=None):
     dQ, dK, dV = np.zeros((N, d)), np.zeros((N, d)), np.zeros((N, d))
     D, L = np.empty(N), np.empty(N)
     for r in _blocks(np.arange(N), block or _panel_budget(N, 4)):
-        t = _row_terms(Q, K, V, dO, r, scale)
+        t = _row_terms(Q, K, V, dO, r, scale, causal=causal)
         nk = t["nk"]
         dQ[r] = scale * (t["dS"] @ K[:nk])
         dK[:nk] += scale * (t["dS"].T @ Q[r])
@@ -215,28 +222,29 @@ def backward(Q, K, V, dO, scale=None, block=None):
     return dict(dQ=dQ, dK=dK, dV=dV, D=D, L=L)
 
 
-def backward_rows(Q, K, V, dO, rows, scale=None):
+def backward_rows(Q, K, V, dO, rows, scale=None, causal=True):
     """dQ[rows] only."""
     Q, K, V, dO = map(_f64, (Q, K, V, dO))
     scale = default_scale(Q.shape[1]) if scale is None else scale
     rows = np.asarray(rows)
     out = np.empty((len(rows), Q.shape[1]))
     order = np.argsort(rows)
-    for blk in _blocks(order, _panel_budget(int(rows.max()) + 1, 4)):
-        t = _row_terms(Q, K, V, dO, rows[blk], scale)
+    for blk in _blocks(order, _panel_budget(int(rows.max()) + 1 if causal else len(K), 4)):
+        t = _row_terms(Q, K, V, dO, rows[blk], scale, causal=causal)
         out[blk] = scale * (t["dS"] @ K[:t["nk"]])
     return out
 
 
-def backward_cols(Q, K, V, dO, cols, scale=None):
-    """dK[cols], dV[cols] only.  Needs every row i >= min(cols): cheap for late columns."""
+def backward_cols(Q, K, V, dO, cols, scale=None, causal=True):
+    """dK[cols], dV[cols] only.  Causal: needs every row i >= min(cols), cheap for late
+    columns; otherwise every row."""
     Q, K, V, dO = map(_f64, (Q, K, V, dO))
     N, d = Q.shape
     scale = default_scale(d) if scale is None else scale
     cols = np.asarray(cols)
     dK, dV = np.zeros((len(cols), d)), np.zeros((len(cols), d))
-    for r in _blocks(np.arange(int(cols.min()), N), _panel_budget(N, 4)):
-        t = _row_terms(Q, K, V, dO, r, scale)
+    for r in _blocks(np.arange(int(cols.min()) if causal else 0, N), _panel_budget(N, 4)):
+        t = _row_terms(Q, K, V, dO, r, scale, causal=causal)
         ok = cols < t["nk"]
         cc = cols[ok]
         dK[ok] += scale * (t["dS"][:, cc].T @ Q[r])
@@ -254,7 +262,7 @@ def bf16_round(x):
     return u.astype(np.uint32).view(np.float32).astype(np.float64)
 
 
-def backward_bf16_dS(Q, K, V, dO, gproj, scale=None, block=None):
+def backward_bf16_dS(Q, K, V, dO, gproj, scale=None, block=None, causal=True):
     """Emulate a backward that rounds dS to bf16 before the dS K and dS^T Q products.
 
     Without GProj: dQ = s bf16(dS) K, dK = s bf16(dS)^T Q.  With GProj (GProj page,
@@ -274,7 +282,7 @@ def backward_bf16_dS(Q, K, V, dO, gproj, scale=None, block=None):
     r_all = np.zeros(N)
     worst = 0.0
     for r in _blocks(np.arange(N), block or _panel_budget(N, 4)):
-        t = _row_terms(Q, K, V, dO, r, scale)
+        t = _row_terms(Q, K, V, dO, r, scale, causal=causal)
         nk = t["nk"]
         dSh = bf16_round(t["dS"])
         if gproj:
@@ -297,7 +305,7 @@ def backward_bf16_dS(Q, K, V, dO, gproj, scale=None, block=None):
 # Backward over backward (FlashBoB)
 # ---------------------------------------------------------------------------
 
-def bob(Q, K, V, dO, a, b, c, scale=None, block=None, keep=False):
+def bob(Q, K, V, dO, a, b, c, scale=None, block=None, keep=False, causal=True):
     """Backward-over-backward for one slice, closed form.
 
     Let Phi(Q, K, V, dO) = (dQ, dK, dV) be the first backward and
@@ -321,7 +329,7 @@ def bob(Q, K, V, dO, a, b, c, scale=None, block=None, keep=False):
     E, F, D, L = (np.empty(N) for _ in range(4))
     kept = None
     for r in _blocks(np.arange(N), block or _panel_budget(N, 12)):
-        t = _row_terms(Q, K, V, dO, r, scale, a, b, c)
+        t = _row_terms(Q, K, V, dO, r, scale, a, b, c, causal=causal)
         nk = t["nk"]
         gQ[r] = scale * (t["dS"] @ b[:nk] + t["Sbar"] @ K[:nk])
         gK[:nk] += scale * (t["dS"].T @ a[r] + t["Sbar"].T @ Q[r])
@@ -335,7 +343,7 @@ def bob(Q, K, V, dO, a, b, c, scale=None, block=None, keep=False):
     return out
 
 
-def bob_rows(Q, K, V, dO, a, b, c, rows, scale=None):
+def bob_rows(Q, K, V, dO, a, b, c, rows, scale=None, causal=True):
     """gQ[rows], gdO[rows] and the row states (E, F) only."""
     Q, K, V, dO, a, b, c = map(_f64, (Q, K, V, dO, a, b, c))
     d = Q.shape[1]
@@ -344,8 +352,8 @@ def bob_rows(Q, K, V, dO, a, b, c, rows, scale=None):
     gQ, gdO = np.empty((len(rows), d)), np.empty((len(rows), d))
     E, F = np.empty(len(rows)), np.empty(len(rows))
     order = np.argsort(rows)
-    for blk in _blocks(order, _panel_budget(int(rows.max()) + 1, 12)):
-        t = _row_terms(Q, K, V, dO, rows[blk], scale, a, b, c)
+    for blk in _blocks(order, _panel_budget(int(rows.max()) + 1 if causal else len(K), 12)):
+        t = _row_terms(Q, K, V, dO, rows[blk], scale, a, b, c, causal=causal)
         nk = t["nk"]
         gQ[blk] = scale * (t["dS"] @ b[:nk] + t["Sbar"] @ K[:nk])
         gdO[blk] = t["P"] @ c[:nk] + t["dPbar"] @ V[:nk]
@@ -353,15 +361,16 @@ def bob_rows(Q, K, V, dO, a, b, c, rows, scale=None):
     return dict(gQ=gQ, gdO=gdO, E=E, F=F)
 
 
-def bob_cols(Q, K, V, dO, a, b, c, cols, scale=None):
-    """gK[cols], gV[cols] only.  Needs every row i >= min(cols): cheap for late columns."""
+def bob_cols(Q, K, V, dO, a, b, c, cols, scale=None, causal=True):
+    """gK[cols], gV[cols] only.  Causal: needs every row i >= min(cols), cheap for late
+    columns; otherwise every row."""
     Q, K, V, dO, a, b, c = map(_f64, (Q, K, V, dO, a, b, c))
     N, d = Q.shape
     scale = default_scale(d) if scale is None else scale
     cols = np.asarray(cols)
     gK, gV = np.zeros((len(cols), d)), np.zeros((len(cols), d))
-    for r in _blocks(np.arange(int(cols.min()), N), _panel_budget(N, 12)):
-        t = _row_terms(Q, K, V, dO, r, scale, a, b, c)
+    for r in _blocks(np.arange(int(cols.min()) if causal else 0, N), _panel_budget(N, 12)):
+        t = _row_terms(Q, K, V, dO, r, scale, a, b, c, causal=causal)
         ok = cols < t["nk"]
         cc = cols[ok]
         gK[ok] += scale * (t["dS"][:, cc].T @ a[r] + t["Sbar"][:, cc].T @ Q[r])
@@ -369,14 +378,14 @@ def bob_cols(Q, K, V, dO, a, b, c, cols, scale=None):
     return gK, gV
 
 
-def bob_row_pass(Q, K, V, dO, a, b, c, O, L, Bc, scale=None):
+def bob_row_pass(Q, K, V, dO, a, b, c, O, L, Bc, scale=None, causal=True):
     """The BoB row pass in its streaming form, for one slice.
 
     FlashBoB page, section "Two scalar states replace quadratic tensors": a block of
     query rows stays on chip while key/value blocks stream past; probabilities are
     recomputed from the stored normaliser L; row sums are accumulated, and the
     corrections that need the finished row are applied once the row is complete.
-    Per row i, over key blocks (keys <= i):
+    Per row i, over key blocks (keys <= i when causal, else all keys):
         P = exp(S - L), dP = dO V^T, dS = P*(dP - D) with D_i = dO_i . O_i,
         G = s(a K^T + Q b^T), H = dO c^T, W = G*dS + P*H,
         E_i += sum P*G,  F'_i += sum W,
@@ -396,10 +405,10 @@ def bob_row_pass(Q, K, V, dO, a, b, c, O, L, Bc, scale=None):
     rows = np.arange(N)
     for k0 in range(0, N, Bc):
         kj = np.arange(k0, min(k0 + Bc, N))
-        live = rows >= k0                       # rows that see at least one key here
+        live = rows >= k0 if causal else rows >= 0  # rows that see at least one key here
         r = rows[live]
         S = scale * (Q[r] @ K[kj].T)
-        mask = kj[None, :] > r[:, None]
+        mask = kj[None, :] > r[:, None] if causal else np.zeros((len(r), len(kj)), bool)
         P = np.exp(np.where(mask, NEG_INF, S) - L[r, None])
         dP = dO[r] @ V[kj].T
         dS = P * (dP - D[r, None])
@@ -417,12 +426,13 @@ def bob_row_pass(Q, K, V, dO, a, b, c, O, L, Bc, scale=None):
     return dict(gQ=gQ, gdO=gdO, E=E, F=Fp - E * D, D=D)
 
 
-def bob_col_pass(Q, K, V, dO, a, b, c, L, D, E, F, Br, scale=None):
+def bob_col_pass(Q, K, V, dO, a, b, c, L, D, E, F, Br, scale=None, causal=True):
     """The BoB column pass in its streaming form, for one slice.
 
     FlashBoB page, same section: a block of keys stays on chip while query rows
     stream past; the probabilities are recomputed and the stored row states (L, D,
-    E, F) of each streamed row are read back.  Per key j, over query rows i >= j:
+    E, F) of each streamed row are read back.  Per key j, over query rows i >= j
+    (all rows when not causal):
         dPbar = P*(G - E),  Sbar = P*(G*(dP - D) - E*dP + H - F),
         gV_j += dPbar^T dO,  gK_j += s (dS^T a + Sbar^T Q).
     Returns (gK, gV)."""
@@ -432,8 +442,8 @@ def bob_col_pass(Q, K, V, dO, a, b, c, L, D, E, F, Br, scale=None):
     gK, gV = np.zeros((N, d)), np.zeros((N, d))
     for q0 in range(0, N, Br):
         qi = np.arange(q0, min(q0 + Br, N))
-        kj = np.arange(0, qi[-1] + 1)
-        mask = kj[None, :] > qi[:, None]
+        kj = np.arange(0, qi[-1] + 1) if causal else np.arange(N)
+        mask = kj[None, :] > qi[:, None] if causal else np.zeros((len(qi), len(kj)), bool)
         S = scale * (Q[qi] @ K[kj].T)
         P = np.exp(np.where(mask, NEG_INF, S) - L[qi, None])
         dP = dO[qi] @ V[kj].T
@@ -465,14 +475,14 @@ def _each_slice(fn, *tensors, **kw):
     return outs
 
 
-def forward_all(Q, K, V, scale=None):
+def forward_all(Q, K, V, scale=None, causal=True):
     return _each_slice(lambda q, k, v, **kw: dict(zip(("O", "L"), forward(q, k, v, **kw))),
-                       Q, K, V, scale=scale)
+                       Q, K, V, scale=scale, causal=causal)
 
 
-def backward_all(Q, K, V, dO, scale=None):
-    return _each_slice(backward, Q, K, V, dO, scale=scale)
+def backward_all(Q, K, V, dO, scale=None, causal=True):
+    return _each_slice(backward, Q, K, V, dO, scale=scale, causal=causal)
 
 
-def bob_all(Q, K, V, dO, a, b, c, scale=None):
-    return _each_slice(bob, Q, K, V, dO, a, b, c, scale=scale)
+def bob_all(Q, K, V, dO, a, b, c, scale=None, causal=True):
+    return _each_slice(bob, Q, K, V, dO, a, b, c, scale=scale, causal=causal)

@@ -14,6 +14,9 @@ Each pin names the page passage (or the mathematical fact) it rests on:
   * symbolic differentiation (sympy) and fp64 autograd on tiny cases, both of
     which know nothing of the hand-derived closed form;
   * closed-form special cases (N = 1; Q = 0 gives uniform causal attention);
+  * the non-causal mode (every key visible) against the same kinds of pins:
+    brute force, online = two-pass, finite differences, the Hessian-vector
+    product, the forward JVP, the streaming passes and fp64 autograd;
   * the streaming row/column-pass form of BoB (FlashBoB page, "Two scalar states
     replace quadratic tensors") equals the closed form.
 A final group plants mistakes in the oracle and checks that these pins catch them.
@@ -44,28 +47,30 @@ def slice_set(N, d, seed=0):
 
 # ---------------------------------------------------------------- forward ----
 
-def brute_forward(Q, K, V, scale):
+def brute_forward(Q, K, V, scale, causal=True):
     """Pure-Python loops over the definition: no NumPy linear algebra."""
     N, d = len(Q), len(Q[0])
     O = [[0.0] * d for _ in range(N)]
     L = [0.0] * N
     for i in range(N):
-        s = [scale * sum(Q[i][t] * K[j][t] for t in range(d)) for j in range(i + 1)]
+        n = i + 1 if causal else N
+        s = [scale * sum(Q[i][t] * K[j][t] for t in range(d)) for j in range(n)]
         m = max(s)
         e = [math.exp(x - m) for x in s]
         tot = sum(e)
         L[i] = m + math.log(tot)
         for t in range(d):
-            O[i][t] = sum(e[j] / tot * V[j][t] for j in range(i + 1))
+            O[i][t] = sum(e[j] / tot * V[j][t] for j in range(n))
     return O, L
 
 
+@pytest.mark.parametrize("causal", [True, False])
 @pytest.mark.parametrize("N,d", [(1, 4), (2, 3), (7, 5), (16, 8)])
-def test_forward_brute_force(N, d):
+def test_forward_brute_force(N, d, causal):
     Q, K, V = rnd(1, N, d), rnd(2, N, d), rnd(3, N, d)
     s = 0.37
-    Ob, Lb = brute_forward(Q.tolist(), K.tolist(), V.tolist(), s)
-    O, L = oracle.forward(Q, K, V, scale=s)
+    Ob, Lb = brute_forward(Q.tolist(), K.tolist(), V.tolist(), s, causal)
+    O, L = oracle.forward(Q, K, V, scale=s, causal=causal)
     assert rel(O, Ob) <= 1e-13
     assert rel(L, Lb) <= 1e-13
 
@@ -394,10 +399,10 @@ def test_planted_mistakes_are_caught(name, monkeypatch):
     """Plant a plausible mistake in the oracle's BoB and check the FD pin fails."""
     orig = A._row_terms
 
-    def mutated(Q, K, V, dO, rows, scale, a=None, b=None, c=None):
+    def mutated(Q, K, V, dO, rows, scale, a=None, b=None, c=None, causal=True):
         if name == "transpose_b" and a is not None:
-            return orig(Q, K, V, dO, rows, scale, b, a, c)
-        t = orig(Q, K, V, dO, rows, scale, a, b, c)
+            return orig(Q, K, V, dO, rows, scale, b, a, c, causal=causal)
+        t = orig(Q, K, V, dO, rows, scale, a, b, c, causal=causal)
         if a is not None:
             MUTATIONS[name](t)
             # re-derive the dependants of the mutated tile as the real code would
@@ -420,3 +425,129 @@ def test_planted_mistakes_are_caught(name, monkeypatch):
     out = A.bob(Q, K, V, dO, a, b, c, scale=s)
     errs = [rel(out[k], w) for k, w in zip(("gQ", "gK", "gV", "gdO"), fd)]
     assert max(errs) > 1e-4, (name, errs)
+
+
+# ------------------------------------------------------------- non-causal ----
+# The same method with every key visible to every query (the "causal=False" mode):
+# pinned the same ways as the causal default.
+
+def loss_nc(Q, K, V, dO, s):
+    O, _ = oracle.forward(Q, K, V, scale=s, causal=False)
+    return float((O * dO).sum())
+
+
+@pytest.mark.parametrize("Br,Bc", [(1, 1), (16, 3), (5, 37), (37, 37)])
+def test_noncausal_online_softmax_equals_two_pass(Br, Bc):
+    N, d = 37, 8
+    Q, K, V = rnd(80, N, d) * 2, rnd(81, N, d) * 2, rnd(82, N, d)
+    O2, L2 = oracle.forward(Q, K, V, causal=False)
+    O1, L1 = oracle.forward_online(Q, K, V, Br, Bc, causal=False)
+    assert rel(O1, O2) <= 1e-13 and rel(L1, L2) <= 1e-13
+
+
+def test_noncausal_uniform_attention_closed_form():
+    """Q = 0: P_ij = 1/N for every pair, O_i = the mean of V, L_i = log N."""
+    N, d = 29, 5
+    K, V = rnd(83, N, d), rnd(84, N, d)
+    O, L = oracle.forward(np.zeros((N, d)), K, V, causal=False)
+    assert rel(O, np.broadcast_to(V.mean(axis=0), (N, d))) <= 1e-14
+    assert np.allclose(L, np.log(N), rtol=0, atol=1e-14)
+
+
+def test_noncausal_probabilities_have_full_support_and_differ_from_causal():
+    N, d = 30, 8
+    Q, K, V = rnd(85, N, d), rnd(86, N, d), rnd(87, N, d)
+    P, _ = oracle.softmax_rows(oracle.scores(Q, K, np.arange(N), 0.3, causal=False))
+    assert P.shape == (N, N) and np.all(P > 0) and np.max(np.abs(P.sum(axis=1) - 1.0)) <= 1e-14
+    Oc, _ = oracle.forward(Q, K, V, causal=True)
+    On, _ = oracle.forward(Q, K, V, causal=False)
+    assert rel(On[-1], Oc[-1]) <= 1e-15       # the last row sees every key either way
+    assert rel(On[:-1], Oc[:-1]) > 1e-3
+
+
+@pytest.mark.parametrize("N,d", [(1, 3), (6, 3), (11, 4)])
+def test_noncausal_backward_matches_finite_differences(N, d):
+    Q, K, V, dO = (x * 0.8 for x in slice_set(N, d, 88)[:4])
+    s = 0.6
+    g = oracle.backward(Q, K, V, dO, scale=s, causal=False)
+    gQ = fd_grad(lambda X: loss_nc(X, K, V, dO, s), Q)
+    gK = fd_grad(lambda X: loss_nc(Q, X, V, dO, s), K)
+    gV = fd_grad(lambda X: loss_nc(Q, K, X, dO, s), V)
+    top = max(np.abs(gQ).max(), np.abs(gK).max(), np.abs(gV).max(), 1e-3)
+    assert np.abs(g["dQ"] - gQ).max() <= 1e-8 * top
+    assert np.abs(g["dK"] - gK).max() <= 1e-8 * top
+    assert np.abs(g["dV"] - gV).max() <= 1e-8 * top
+
+
+def test_noncausal_backward_sampling_agrees():
+    N, d = 45, 6
+    Q, K, V, dO = slice_set(N, d, 89)[:4]
+    ref = oracle.backward(Q, K, V, dO, block=7, causal=False)
+    rows, cols = np.array([0, 44, 13]), np.array([0, 30, 44])
+    assert rel(oracle.backward_rows(Q, K, V, dO, rows, causal=False), ref["dQ"][rows]) <= 1e-13
+    dK, dV = oracle.backward_cols(Q, K, V, dO, cols, causal=False)
+    assert rel(dK, ref["dK"][cols]) <= 1e-13 and rel(dV, ref["dV"][cols]) <= 1e-13
+
+
+def grads_nc(Q, K, V, dO, s):
+    g = oracle.backward(Q, K, V, dO, scale=s, causal=False)
+    return g["dQ"], g["dK"], g["dV"]
+
+
+@pytest.mark.parametrize("N,d", [(1, 3), (5, 3), (12, 4)])
+def test_noncausal_bob_is_hessian_vector_product(N, d):
+    Q, K, V, dO, a, b, c = slice_set(N, d, 90)
+    s, h = 0.55, 1e-5
+    out = oracle.bob(Q, K, V, dO, a, b, c, scale=s, causal=False)
+    gp = grads_nc(Q + h * a, K + h * b, V + h * c, dO, s)
+    gm = grads_nc(Q - h * a, K - h * b, V - h * c, dO, s)
+    fd = [(p - m) / (2 * h) for p, m in zip(gp, gm)]
+    top = max(np.abs(x).max() for x in fd)
+    for name, want in zip(("gQ", "gK", "gV"), fd):
+        assert np.abs(out[name] - want).max() <= 1e-8 * max(top, 1e-3), name
+
+
+def test_noncausal_bob_gdO_is_forward_jvp():
+    Q, K, V, dO, a, b, c = slice_set(9, 4, 91)
+    s, h = 0.4, 1e-5
+    out = oracle.bob(Q, K, V, dO, a, b, c, scale=s, causal=False)
+    Op, _ = oracle.forward(Q + h * a, K + h * b, V + h * c, scale=s, causal=False)
+    Om, _ = oracle.forward(Q - h * a, K - h * b, V - h * c, scale=s, causal=False)
+    fd = (Op - Om) / (2 * h)
+    assert np.abs(out["gdO"] - fd).max() <= 1e-8 * max(np.abs(fd).max(), 1e-3)
+
+
+@pytest.mark.parametrize("Bc,Br", [(1, 1), (4, 7), (16, 16)])
+def test_noncausal_bob_streaming_passes_equal_closed_form(Bc, Br):
+    N, d = 41, 8
+    Q, K, V, dO, a, b, c = slice_set(N, d, 92)
+    ref = oracle.bob(Q, K, V, dO, a, b, c, causal=False)
+    O, L = oracle.forward(Q, K, V, causal=False)
+    rp = oracle.bob_row_pass(Q, K, V, dO, a, b, c, O, L, Bc, causal=False)
+    for k in ("gQ", "gdO", "E", "F"):
+        assert rel(rp[k], ref[k]) <= 1e-12, k
+    gK, gV = oracle.bob_col_pass(Q, K, V, dO, a, b, c, L, rp["D"], rp["E"], rp["F"], Br, causal=False)
+    assert rel(gK, ref["gK"]) <= 1e-12 and rel(gV, ref["gV"]) <= 1e-12
+    rows, cols = np.array([40, 3]), np.array([0, 40])
+    r = oracle.bob_rows(Q, K, V, dO, a, b, c, rows, causal=False)
+    assert rel(r["gQ"], ref["gQ"][rows]) <= 1e-13 and rel(r["gdO"], ref["gdO"][rows]) <= 1e-13
+    gKc, gVc = oracle.bob_cols(Q, K, V, dO, a, b, c, cols, causal=False)
+    assert rel(gKc, ref["gK"][cols]) <= 1e-13 and rel(gVc, ref["gV"][cols]) <= 1e-13
+
+
+def test_noncausal_bob_against_fp64_autograd():
+    torch = pytest.importorskip("torch")
+    N, d = 11, 6
+    arrs = slice_set(N, d, 93)
+    s = 1 / math.sqrt(d)
+    Q, K, V, dO, a, b, c = (torch.tensor(x, dtype=torch.float64, requires_grad=i < 4)
+                            for i, x in enumerate(arrs))
+    O = torch.softmax((Q @ K.T) * s, dim=-1) @ V
+    dQ, dK, dV = torch.autograd.grad((O * dO).sum(), (Q, K, V), create_graph=True)
+    psi = (a * dQ).sum() + (b * dK).sum() + (c * dV).sum()
+    gQ, gK, gV, gdO = torch.autograd.grad(psi, (Q, K, V, dO))
+    ref = oracle.bob(*arrs, causal=False)
+    for k, t in zip(("gQ", "gK", "gV", "gdO"), (gQ, gK, gV, gdO)):
+        assert rel(ref[k], t.numpy()) <= 1e-13, k
+    fb = oracle.backward(*arrs[:4], causal=False)
+    assert rel(fb["dQ"], dQ.detach().numpy()) <= 1e-13
