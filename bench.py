@@ -74,13 +74,18 @@ def job_tflops(flops_per_rank_step, world, ms_max):
     return flops_per_rank_step * world / (ms_max * 1e-3) / 1e12
 
 
+# Causal attention by default; --causal 0 measures the same step with every key
+# visible (its flop counts are not halved).
+CAUSAL = True
+
+
 def dense_flops(w, op):
-    unit = w.B * w.H * w.N * w.N * w.d / 2.0
+    unit = w.B * w.H * w.N * w.N * w.d / (2.0 if CAUSAL else 1.0)
     return {"fwd": 4, "bwd": 10, "bob": 24}[op] * unit
 
 
 def kernel_flops(w, kn, table):
-    return 2 * table[kn] * w.B * w.H * w.N * w.N * w.d / 2.0
+    return 2 * table[kn] * w.B * w.H * w.N * w.N * w.d / (2.0 if CAUSAL else 1.0)
 
 
 def traffic_for(kernel, w):
@@ -178,7 +183,7 @@ def run_ours(args, w, rank, world):
     stream = torch.cuda.Stream(device=dev)
     pinned, x = make_inputs(w, dev)
     torch.cuda.synchronize()
-    desc = fbd.make_desc(x["Q"], w.scale)
+    desc = fbd.make_desc(x["Q"], w.scale, int(CAUSAL))
     bf = torch.bfloat16
     shp = x["Q"].shape
     out = {k: torch.empty(shp, dtype=bf, device=dev) for k in ("O", "dQ", "dK", "dV", "gQ", "gK", "gV", "gdO")}
@@ -317,9 +322,9 @@ def cpu_baseline(w, budget_s=20.0):
     t0 = time.perf_counter()
     reps = 0
     while True:
-        oracle.forward(x["Q"], x["K"], x["V"], scale=w.scale)
-        oracle.backward(x["Q"], x["K"], x["V"], x["dO"], scale=w.scale)
-        oracle.bob(x["Q"], x["K"], x["V"], x["dO"], x["gdQ"], x["gdK"], x["gdV"], scale=w.scale)
+        oracle.forward(x["Q"], x["K"], x["V"], scale=w.scale, causal=CAUSAL)
+        oracle.backward(x["Q"], x["K"], x["V"], x["dO"], scale=w.scale, causal=CAUSAL)
+        oracle.bob(x["Q"], x["K"], x["V"], x["dO"], x["gdQ"], x["gdK"], x["gdV"], scale=w.scale, causal=CAUSAL)
         reps += 1
         if time.perf_counter() - t0 > budget_s or reps >= 50:
             break
@@ -408,6 +413,8 @@ def main():
     ap.add_argument("--batch", type=int, default=4)
     ap.add_argument("--heads", type=int, default=12)
     ap.add_argument("--gproj", type=int, default=0)
+    ap.add_argument("--causal", type=int, default=1, choices=[0, 1],
+                    help="1: causal attention (the headline workload); 0: every key visible")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--max-n", action="store_true", help="report the largest N that fits in HBM instead")
     args = ap.parse_args()
@@ -417,11 +424,13 @@ def main():
         max_n(args)
         return
     args.warmup = max(args.warmup, 3)
-    w = W.Workload(f"gpt2small_B{args.batch}H{args.heads}N{args.n_seq}d64", args.batch, args.heads, args.n_seq,
-                   64, "bf16")
+    global CAUSAL
+    CAUSAL = bool(args.causal)
+    w = W.Workload(f"gpt2small_B{args.batch}H{args.heads}N{args.n_seq}d64" + ("" if CAUSAL else "_noncausal"),
+                   args.batch, args.heads, args.n_seq, 64, "bf16")
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
-    config = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": 64, "causal": True,
+    config = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": 64, "causal": CAUSAL,
               "ops": "fwd + bwd(gproj=%d) + BoB" % args.gproj,
               "l2": "inputs larger than L2 (each input tensor %.0f MB; 7 inputs)" % (w.rows * 64 * 2 / 1e6),
               "parallelism": f"independent replicas x{world}"}
@@ -438,7 +447,9 @@ def main():
             times.append(base["value"])
         v = statistics.mean(times)
         flops = sum(dense_flops(w, op) for op in ("fwd", "bwd", "bob"))
-        print(json.dumps({"impl": "reference", "metric": "fwd+bwd+BoB attention TFLOP/s (dense definition)",
+        print(json.dumps({"impl": "reference",
+                          "metric": "fwd+bwd+BoB attention TFLOP/s (dense definition%s)"
+                          % (", causal-halved" if CAUSAL else ""),
                           "value": v, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
                           "warmup": args.warmup, "ms_per_step": flops / (v * 1e12) * 1e3,
                           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -461,7 +472,7 @@ def main():
         return flops / (ms * 1e-3) / 1e12
 
     line = {
-        "metric": "fwd+bwd+BoB attention TFLOP/s (dense definition, causal-halved)",
+        "metric": "fwd+bwd+BoB attention TFLOP/s (dense definition%s)" % (", causal-halved" if CAUSAL else ""),
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": r["ms_max"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic", "config": config,

@@ -1,4 +1,4 @@
-"""Python binding of libfbd: exact causal attention forward, backward (GProj) and
+"""Python binding of libfbd: exact attention (causal by default) forward, backward (GProj) and
 backward-over-backward on GB300.
 
 Argument marshalling only.  Every computation runs in the CUDA kernels of
@@ -69,10 +69,10 @@ def _check(status: int):
         raise FbdError(status, lib.attn_last_error().decode())
 
 
-def attn_fwd(Q, K, V, O=None, lse=None, scale: float = 0.0, stream=None, desc=None):
+def attn_fwd(Q, K, V, O=None, lse=None, scale: float = 0.0, stream=None, desc=None, causal: bool = True):
     """O, lse = attention forward (allocates O and lse with torch when not given)."""
     torch = _torch()
-    desc = desc or make_desc(Q, scale)
+    desc = desc or make_desc(Q, scale, int(causal))
     if O is None:
         O = torch.empty_like(Q)
     if lse is None:
@@ -97,17 +97,17 @@ def _workspace(nbytes, like, workspace):
 
 
 def attn_bwd(Q, K, V, O, dO, lse, gproj: int = 0, dQ=None, dK=None, dV=None, workspace=None,
-             scale: float = 0.0, stream=None, desc=None):
+             scale: float = 0.0, stream=None, desc=None, causal: bool = True):
     """dQ, dK, dV = recompute backward (GProj when gproj != 0, bf16 only)."""
     return attn_bwd_passes(Q, K, V, O, dO, lse, ATTN_ROW_PASS | ATTN_COL_PASS, gproj, dQ, dK, dV, workspace,
-                           scale, stream, desc)
+                           scale, stream, desc, causal)
 
 
 def attn_bwd_passes(Q, K, V, O, dO, lse, passes, gproj: int = 0, dQ=None, dK=None, dV=None, workspace=None,
-                    scale: float = 0.0, stream=None, desc=None):
+                    scale: float = 0.0, stream=None, desc=None, causal: bool = True):
     """The backward's row pass (dQ) and/or column pass (dK, dV); see attn_bwd_passes in fbd.h."""
     torch = _torch()
-    desc = desc or make_desc(Q, scale)
+    desc = desc or make_desc(Q, scale, int(causal))
     dQ = torch.empty_like(Q) if dQ is None else dQ
     dK = torch.empty_like(K) if dK is None else dK
     dV = torch.empty_like(V) if dV is None else dV
@@ -121,17 +121,17 @@ def attn_bwd_passes(Q, K, V, O, dO, lse, passes, gproj: int = 0, dQ=None, dK=Non
 
 
 def attn_bob(Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ=None, gK=None, gV=None, gdO=None, workspace=None,
-             scale: float = 0.0, stream=None, desc=None):
+             scale: float = 0.0, stream=None, desc=None, causal: bool = True):
     """gQ, gK, gV, gdO = backward over backward against cotangents (gdQ, gdK, gdV)."""
     return attn_bob_passes(Q, K, V, O, dO, lse, gdQ, gdK, gdV, ATTN_ROW_PASS | ATTN_COL_PASS, gQ, gK, gV, gdO,
-                           workspace, scale, stream, desc)
+                           workspace, scale, stream, desc, causal)
 
 
 def attn_bob_passes(Q, K, V, O, dO, lse, gdQ, gdK, gdV, passes, gQ=None, gK=None, gV=None, gdO=None,
-                    workspace=None, scale: float = 0.0, stream=None, desc=None):
+                    workspace=None, scale: float = 0.0, stream=None, desc=None, causal: bool = True):
     """BoB's row pass (gQ, gdO, row states) and/or column pass (gK, gV); see fbd.h."""
     torch = _torch()
-    desc = desc or make_desc(Q, scale)
+    desc = desc or make_desc(Q, scale, int(causal))
     gQ = torch.empty_like(Q) if gQ is None else gQ
     gK = torch.empty_like(K) if gK is None else gK
     gV = torch.empty_like(V) if gV is None else gV
@@ -145,11 +145,11 @@ def attn_bob_passes(Q, K, V, O, dO, lse, gdQ, gdK, gdV, passes, gQ=None, gK=None
 
 
 def attn_bob_static(Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ=None, gK=None, gV=None, gdO=None,
-                    scale: float = 0.0, stream=None, desc=None):
+                    scale: float = 0.0, stream=None, desc=None, causal: bool = True):
     """attn_bob without a workspace argument: the library's static scratch array is used
     (for callers that cannot allocate device memory; B*H*N <= 1,048,576)."""
     torch = _torch()
-    desc = desc or make_desc(Q, scale)
+    desc = desc or make_desc(Q, scale, int(causal))
     gQ = torch.empty_like(Q) if gQ is None else gQ
     gK = torch.empty_like(K) if gK is None else gK
     gV = torch.empty_like(V) if gV is None else gV
@@ -160,10 +160,10 @@ def attn_bob_static(Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ=None, gK=None, gV=Non
     return gQ, gK, gV, gdO
 
 
-def attn_bwd_projected_dS(Q, K, V, O, dO, lse, dS=None, scale: float = 0.0, stream=None, desc=None):
+def attn_bwd_projected_dS(Q, K, V, O, dO, lse, dS=None, scale: float = 0.0, stream=None, desc=None, causal: bool = True):
     """Diagnostic: the GProj-projected dS [B, H, N, N] float32 (small N only)."""
     torch = _torch()
-    desc = desc or make_desc(Q, scale)
+    desc = desc or make_desc(Q, scale, int(causal))
     B, H, N, _ = Q.shape
     dS = torch.empty((B, H, N, N), dtype=torch.float32, device=Q.device) if dS is None else dS
     _check(lib.attn_bwd_projected_dS(ctypes.byref(desc), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO),

@@ -34,7 +34,7 @@ attn_status_t check_desc(const attn_desc_t* desc, fbd::Problem& p) {
   if (desc == nullptr) return fail(ATTN_ERR_INVALID_ARG, "desc is NULL%s");
   if (desc->B < 0 || desc->H < 0 || desc->N < 0 || desc->d <= 0)
     return fail(ATTN_ERR_INVALID_ARG, "negative B/H/N or non-positive d%s");
-  if (desc->causal != 1) return fail(ATTN_ERR_UNSUPPORTED, "only causal attention (causal=1) is supported%s");
+  if (desc->causal != 0 && desc->causal != 1) return fail(ATTN_ERR_UNSUPPORTED, "causal must be 0 or 1%s");
   if (desc->d != 64 && desc->d != 128) return fail(ATTN_ERR_UNSUPPORTED, "head dim must be 64 or 128%s");
   if (desc->dtype != ATTN_F32 && desc->dtype != ATTN_BF16) return fail(ATTN_ERR_UNSUPPORTED, "unknown dtype%s");
   if (!std::isfinite(desc->scale) || desc->scale < 0.f)
@@ -53,6 +53,7 @@ attn_status_t check_desc(const attn_desc_t* desc, fbd::Problem& p) {
   p.BH = desc->B * desc->H;
   p.scale = desc->scale == 0.f ? 1.0f / std::sqrt(static_cast<float>(desc->d)) : desc->scale;
   p.dtype = desc->dtype;
+  p.causal = desc->causal;
   if (p.BH >= lim) return fail(ATTN_ERR_INVALID_ARG, "B*H must be < 2^31%s");
   if (((p.N + 7) / 8) * p.BH >= lim) return fail(ATTN_ERR_INVALID_ARG, "B*H*N too large for one launch%s");
   return ATTN_OK;

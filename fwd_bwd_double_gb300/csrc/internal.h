@@ -14,6 +14,7 @@ struct Problem {
   int64_t BH;     // B * H independent (batch, head) slices
   float scale;    // s, already resolved (1/sqrt(d) when the caller passed 0)
   int dtype;      // attn_dtype_t
+  int causal;     // 1: key j visible to query i iff j <= i; 0: every key visible
 };
 
 // Float32 path: CUDA-core kernels with float32 inputs/outputs (exact fp32 arithmetic).

@@ -107,7 +107,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) fwd_kernel(const T* __restrict__ Q, const T* __restrict__ K,
                                                        const T* __restrict__ Vt, T* __restrict__ O,
                                                        float* __restrict__ lse, int64_t N, int64_t BH,
-                                                       float scale) {
+                                                       float scale, int causal) {
   constexpr int V = D / 32;
   extern __shared__ float sm[];
   float* Ks = sm;
@@ -123,14 +123,14 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(const T* __restrict__ Q, 
   for (int t = 0; t < V; ++t) o[t] = 0.f;
   if (live) load_vec(Q + base + i * D, lane, q);
   float m = -CUDART_INF_F, l = 0.f;  // running max of raw dot products, running sum
-  const int64_t last = min(row0 + kWarps, N) - 1;
+  const int64_t last = causal ? min(row0 + kWarps, N) - 1 : N - 1;  // last key any row of the block sees
   for (int64_t k0 = 0; k0 <= last; k0 += kTile) {
     __syncthreads();
     stage<T, D>(Ks, K + base, k0, N);
     stage<T, D>(Vs, Vt + base, k0, N);
     __syncthreads();
     if (!live) continue;
-    const int jn = static_cast<int>(lmin(kTile, i - k0 + 1));
+    const int jn = static_cast<int>(lmin(kTile, (causal ? i + 1 : N) - k0));
     for (int jj = 0; jj < jn; ++jj) {
       float kv[V], vv[V];
       load_smem(Ks + jj * D, lane, kv);
@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(kThreads) bwd_row_kernel(const T* __restrict__
                                                            const T* __restrict__ Vt, const T* __restrict__ O,
                                                            const T* __restrict__ dO, const float* __restrict__ lse,
                                                            T* __restrict__ dQ, float4* __restrict__ ws, int64_t N,
-                                                           int64_t BH, float scale) {
+                                                           int64_t BH, float scale, int causal) {
   constexpr int V = D / 32;
   extern __shared__ float sm[];
   float* Ks = sm;
@@ -191,14 +191,14 @@ __global__ void __launch_bounds__(kThreads) bwd_row_kernel(const T* __restrict__
     Di = x[0];
     Li = lse[tl.bh * N + i];
   }
-  const int64_t last = min(row0 + kWarps, N) - 1;
+  const int64_t last = causal ? min(row0 + kWarps, N) - 1 : N - 1;  // last key any row of the block sees
   for (int64_t k0 = 0; k0 <= last; k0 += kTile) {
     __syncthreads();
     stage<T, D>(Ks, K + base, k0, N);
     stage<T, D>(Vs, Vt + base, k0, N);
     __syncthreads();
     if (!live) continue;
-    const int jn = static_cast<int>(lmin(kTile, i - k0 + 1));
+    const int jn = static_cast<int>(lmin(kTile, (causal ? i + 1 : N) - k0));
     for (int jj = 0; jj < jn; ++jj) {
       float kv[V], vv[V];
       load_smem(Ks + jj * D, lane, kv);
@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(kThreads) bwd_col_kernel(const T* __restrict__
                                                            const T* __restrict__ Vt, const T* __restrict__ dO,
                                                            const float4* __restrict__ ws, T* __restrict__ dK,
                                                            T* __restrict__ dV, int64_t N, int64_t BH,
-                                                           float scale) {
+                                                           float scale, int causal) {
   constexpr int V = D / 32;
   extern __shared__ float sm[];
   float* Qs = sm;
@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(kThreads) bwd_col_kernel(const T* __restrict__
     load_vec(K + base + j * D, lane, kv);
     load_vec(Vt + base + j * D, lane, vv);
   }
-  for (int64_t i0 = col0; i0 < N; i0 += kTile) {
+  for (int64_t i0 = causal ? col0 : 0; i0 < N; i0 += kTile) {
     __syncthreads();
     stage<T, D>(Qs, Q + base, i0, N);
     stage<T, D>(Gs, dO + base, i0, N);
@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(kThreads) bwd_col_kernel(const T* __restrict__
       Ss[threadIdx.x] = (i0 + threadIdx.x < N) ? ws[tl.bh * N + i0 + threadIdx.x] : make_float4(0, 0, 0, 0);
     __syncthreads();
     if (!live) continue;
-    const int ib = static_cast<int>(lmax(0, j - i0));  // rows i >= j only
+    const int ib = causal ? static_cast<int>(lmax(0, j - i0)) : 0;  // causal: rows i >= j only
     const int ie = static_cast<int>(lmin(kTile, N - i0));
     for (int ii = ib; ii < ie; ++ii) {
       float qv[V], gv[V];
@@ -306,7 +306,7 @@ __global__ void __launch_bounds__(kThreads) bob_row_kernel(
     const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ Vt, const T* __restrict__ O,
     const T* __restrict__ dO, const float* __restrict__ lse, const T* __restrict__ A, const T* __restrict__ Bm,
     const T* __restrict__ C, T* __restrict__ gQ, T* __restrict__ gdO, float4* __restrict__ ws, int64_t N,
-    int64_t BH, float scale) {
+    int64_t BH, float scale, int causal) {
   constexpr int V = D / 32;
   extern __shared__ float sm[];
   float* Ks = sm;
@@ -333,7 +333,7 @@ __global__ void __launch_bounds__(kThreads) bob_row_kernel(
     Di = x[0];
     Li = lse[tl.bh * N + i];
   }
-  const int64_t last = min(row0 + kWarps, N) - 1;
+  const int64_t last = causal ? min(row0 + kWarps, N) - 1 : N - 1;  // last key any row of the block sees
   for (int64_t k0 = 0; k0 <= last; k0 += kTile) {
     __syncthreads();
     stage<T, D>(Ks, K + base, k0, N);
@@ -342,7 +342,7 @@ __global__ void __launch_bounds__(kThreads) bob_row_kernel(
     stage<T, D>(Cs, C + base, k0, N);
     __syncthreads();
     if (!live) continue;
-    const int jn = static_cast<int>(lmin(kTile, i - k0 + 1));
+    const int jn = static_cast<int>(lmin(kTile, (causal ? i + 1 : N) - k0));
     for (int jj = 0; jj < jn; ++jj) {
       float kv[V], vv[V], bv[V], cv[V];
       load_smem(Ks + jj * D, lane, kv);
@@ -386,7 +386,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) bob_col_kernel(
     const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ Vt, const T* __restrict__ dO,
     const T* __restrict__ A, const T* __restrict__ Bm, const T* __restrict__ C, const float4* __restrict__ ws,
-    T* __restrict__ gK, T* __restrict__ gV, int64_t N, int64_t BH, float scale) {
+    T* __restrict__ gK, T* __restrict__ gV, int64_t N, int64_t BH, float scale, int causal) {
   constexpr int V = D / 32;
   extern __shared__ float sm[];
   float* Qs = sm;
@@ -408,7 +408,7 @@ __global__ void __launch_bounds__(kThreads) bob_col_kernel(
     load_vec(Bm + base + j * D, lane, bv);
     load_vec(C + base + j * D, lane, cv);
   }
-  for (int64_t i0 = col0; i0 < N; i0 += kTile) {
+  for (int64_t i0 = causal ? col0 : 0; i0 < N; i0 += kTile) {
     __syncthreads();
     stage<T, D>(Qs, Q + base, i0, N);
     stage<T, D>(Gs, dO + base, i0, N);
@@ -417,7 +417,7 @@ __global__ void __launch_bounds__(kThreads) bob_col_kernel(
       Ss[threadIdx.x] = (i0 + threadIdx.x < N) ? ws[tl.bh * N + i0 + threadIdx.x] : make_float4(0, 0, 0, 0);
     __syncthreads();
     if (!live) continue;
-    const int ib = static_cast<int>(lmax(0, j - i0));
+    const int ib = causal ? static_cast<int>(lmax(0, j - i0)) : 0;
     const int ie = static_cast<int>(lmin(kTile, N - i0));
     for (int ii = ib; ii < ie; ++ii) {
       float qv[V], gv[V], a2[V];
@@ -450,14 +450,15 @@ __global__ void __launch_bounds__(kThreads) bob_col_kernel(
 
 // ------------------------------------------- GProj projected dS (diagnostic)
 // One warp per row: sweep 1 accumulates r = sum bf16(dS) and sum bf16(P);
-// sweep 2 writes dS~ = bf16(dS) - rho bf16(P) for j <= i and 0 beyond.
+// sweep 2 writes dS~ = bf16(dS) - rho bf16(P) for every visible key (0 for j > i
+// under the causal mask).
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) projected_dS_kernel(const T* __restrict__ Q, const T* __restrict__ K,
                                                                 const T* __restrict__ Vt, const T* __restrict__ O,
                                                                 const T* __restrict__ dO,
                                                                 const float* __restrict__ lse,
                                                                 float* __restrict__ out, int64_t N, int64_t BH,
-                                                                float scale) {
+                                                                float scale, int causal) {
   constexpr int V = D / 32;
   const int64_t nblk = (N + kWarps - 1) / kWarps;
   const Tile tl = decode(BH, nblk, true);
@@ -477,7 +478,7 @@ __global__ void __launch_bounds__(kThreads) projected_dS_kernel(const T* __restr
     const float rho = r / sp;
     for (int64_t j = 0; j < N; ++j) {
       float* dst = out + (static_cast<size_t>(tl.bh) * N + i) * N + j;
-      if (j > i) {
+      if (causal && j > i) {
         if (pass == 1 && lane == 0) *dst = 0.f;
         continue;
       }
@@ -516,7 +517,7 @@ cudaError_t fwd_t(const Problem& p, const void* Q, const void* K, const void* V,
   cudaError_t e = allow_smem(k, sm);
   if (e != cudaSuccess) return e;
   k<<<grid_for(p), kThreads, sm, st>>>(static_cast<const T*>(Q), static_cast<const T*>(K),
-                                        static_cast<const T*>(V), static_cast<T*>(O), lse, p.N, p.BH, p.scale);
+                                        static_cast<const T*>(V), static_cast<T*>(O), lse, p.N, p.BH, p.scale, p.causal);
   return cudaGetLastError();
 }
 
@@ -534,14 +535,14 @@ cudaError_t bwd_t(const Problem& p, const void* Q, const void* K, const void* V,
     kr<<<grid_for(p), kThreads, sm_row, st>>>(static_cast<const T*>(Q), static_cast<const T*>(K),
                                                static_cast<const T*>(V), static_cast<const T*>(O),
                                                static_cast<const T*>(dO), lse, static_cast<T*>(dQ), ws, p.N, p.BH,
-                                               p.scale);
+                                               p.scale, p.causal);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   if (!(passes & 2)) return cudaSuccess;
   kc<<<grid_for(p), kThreads, sm_col, st>>>(static_cast<const T*>(Q), static_cast<const T*>(K),
                                              static_cast<const T*>(V), static_cast<const T*>(dO), ws,
-                                             static_cast<T*>(dK), static_cast<T*>(dV), p.N, p.BH, p.scale);
+                                             static_cast<T*>(dK), static_cast<T*>(dV), p.N, p.BH, p.scale, p.causal);
   return cudaGetLastError();
 }
 
@@ -561,7 +562,7 @@ cudaError_t bob_t(const Problem& p, const void* Q, const void* K, const void* V,
     kr<<<grid_for(p), kThreads, sm_row, st>>>(
         static_cast<CT>(Q), static_cast<CT>(K), static_cast<CT>(V), static_cast<CT>(O), static_cast<CT>(dO), lse,
         static_cast<CT>(a), static_cast<CT>(b), static_cast<CT>(c), static_cast<T*>(gQ), static_cast<T*>(gdO), ws,
-        p.N, p.BH, p.scale);
+        p.N, p.BH, p.scale, p.causal);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -569,7 +570,7 @@ cudaError_t bob_t(const Problem& p, const void* Q, const void* K, const void* V,
   kc<<<grid_for(p), kThreads, sm_col, st>>>(static_cast<CT>(Q), static_cast<CT>(K), static_cast<CT>(V),
                                              static_cast<CT>(dO), static_cast<CT>(a), static_cast<CT>(b),
                                              static_cast<CT>(c), ws, static_cast<T*>(gK), static_cast<T*>(gV),
-                                             p.N, p.BH, p.scale);
+                                             p.N, p.BH, p.scale, p.causal);
   return cudaGetLastError();
 }
 
@@ -604,11 +605,11 @@ cudaError_t simt_projected_dS(const Problem& p, const void* Q, const void* K, co
   if (p.d == 64)
     projected_dS_kernel<T, 64><<<grid_for(p), kThreads, 0, st>>>(
         static_cast<const T*>(Q), static_cast<const T*>(K), static_cast<const T*>(V), static_cast<const T*>(O),
-        static_cast<const T*>(dO), lse, dS, p.N, p.BH, p.scale);
+        static_cast<const T*>(dO), lse, dS, p.N, p.BH, p.scale, p.causal);
   else
     projected_dS_kernel<T, 128><<<grid_for(p), kThreads, 0, st>>>(
         static_cast<const T*>(Q), static_cast<const T*>(K), static_cast<const T*>(V), static_cast<const T*>(O),
-        static_cast<const T*>(dO), lse, dS, p.N, p.BH, p.scale);
+        static_cast<const T*>(dO), lse, dS, p.N, p.BH, p.scale, p.causal);
   return cudaGetLastError();
 }
 

@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tmC, const __nv_bfloat16* __restrict__ O,
                    const __nv_bfloat16* __restrict__ dO, const float* __restrict__ lse,
                    __nv_bfloat16* __restrict__ gQ, __nv_bfloat16* __restrict__ gdO, float4* __restrict__ ws, int N,
-                   int Np, int nrb, int BH, float scale, float c) {
+                   int Np, int nrb, int BH, float scale, float c, int causal) {
   using Lay = RowLay;
   constexpr int NS = Lay::NS;
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -130,7 +130,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const tc::Order ord = tc::grid_order(BH, nrb);
   const int bh = ord.bh;
   const int rb = nrb - 1 - ord.k;  // heaviest row blocks first (within a group of slices)
-  const int nkv = ((rb + 1) * BM + BN - 1) / BN;
+  // 64-key blocks this row block sees: up to its last row, or all of them when not causal
+  const int nkv = causal ? ((rb + 1) * BM + BN - 1) / BN : (N + BN - 1) / BN;
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(q_full, 1);
@@ -292,6 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_before();
       ptx::mbar_arrive(consumed_a);  // the MMA warp may now write [H | dP] into the tile region
       const int krel = j * BN + c0 - rb * BM;
+      // last visible key of this row, relative to the thread's first key of the block
+      const int klim = causal ? r - krel : N - 1 - (j * BN + c0);
       uint64_t P2[16], G2[16];
       uint32_t pP[16], pG[16], pS[16], pW[16];
       // P, PG from the [G | S] tiles (while [H | dP] is being computed)
@@ -301,8 +304,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float2 arg = tc::unpk2(tc::fma2(tc::pk2(sv[t], sv[t + 1]), c2, nL2));
           float p0 = ptx::ex2(arg.x), p1 = ptx::ex2(arg.y);
           if constexpr (decltype(masked)::value) {
-            if (krel + t > r) p0 = 0.f;
-            if (krel + t + 1 > r) p1 = 0.f;
+            if (t > klim) p0 = 0.f;
+            if (t + 1 > klim) p1 = 0.f;
           }
           const int idx = t >> 1;
           P2[idx] = tc::pk2f(p0, p1);
@@ -316,7 +319,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           accP1 = tc::add_bf16_hi(accP1, pP[idx]);
         }
       };
-      if (krel + 31 > 0)  // a block reaching past the first row of this CTA: causal mask needed
+      // Causal: a block reaching past the first row of this CTA.  Otherwise: a block reaching past N.
+      if (causal ? krel + 31 > 0 : j * BN + c0 + 32 > N)
         first(std::true_type{});
       else
         first(std::false_type{});
@@ -455,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __nv_bfloat16* __restrict__ Kp, const __nv_bfloat16* __restrict__ Bp,
                    const __nv_bfloat16* __restrict__ Vp, const __nv_bfloat16* __restrict__ Cp,
                    __nv_bfloat16* __restrict__ gK, __nv_bfloat16* __restrict__ gV, int N, int BH, float scale,
-                   float c) {
+                   float c, int causal) {
   using Lay = ColLay;
   constexpr int NS = Lay::NS;
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -478,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int bh = ord.bh;
   const int kb = ord.k;  // first key blocks have the most rows: first
   const int nq = (N + BN - 1) / BN;
-  const int i0 = (kb * BM) / BN;
+  const int i0 = causal ? (kb * BM) / BN : 0;  // first query block that sees this key block
   const int ntile = nq - i0;
 
   if (threadIdx.x == 0) {
@@ -653,8 +657,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           float p0 = ptx::ex2(arg.x), p1 = ptx::ex2(arg.y);
           if constexpr (decltype(masked)::value) {
             const int q0 = qbase + u;
-            if (q0 < key || q0 >= N) p0 = 0.f;
-            if (q0 + 1 < key || q0 + 1 >= N) p1 = 0.f;
+            if ((causal && q0 < key) || q0 >= N) p0 = 0.f;
+            if ((causal && q0 + 1 < key) || q0 + 1 >= N) p1 = 0.f;
           }
           const int idx = u >> 1;
           P2[idx] = tc::pk2f(p0, p1);
@@ -665,7 +669,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       // Causal mask only in the first blocks (queries before this CTA's last key) and
       // past N only in the last block.
-      if (qbase < kb * BM + BM || qbase + 32 > N)
+      if ((causal && qbase < kb * BM + BM) || qbase + 32 > N)
         first(std::true_type{});
       else
         first(std::false_type{});
@@ -753,7 +757,7 @@ cudaError_t tc_bob(const Problem& p, const void* Q, const void* K, const void* V
   bob_row_kernel<<<static_cast<unsigned>(nrb * BH), kThreads, RowLay::bytes, st>>>(
       q128, do128, a128, k64, v64, b64, c64, static_cast<const __nv_bfloat16*>(O),
       static_cast<const __nv_bfloat16*>(dO), lse, static_cast<__nv_bfloat16*>(gQ), static_cast<__nv_bfloat16*>(gdO),
-      ws, static_cast<int>(N), static_cast<int>(Np), nrb, static_cast<int>(BH), p.scale, c);
+      ws, static_cast<int>(N), static_cast<int>(Np), nrb, static_cast<int>(BH), p.scale, c, p.causal);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (!(passes & 2)) return cudaSuccess;
@@ -762,7 +766,7 @@ cudaError_t tc_bob(const Problem& p, const void* Q, const void* K, const void* V
   bob_col_kernel<<<static_cast<unsigned>(nrb * BH), kThreads, ColLay::bytes, st>>>(
       q64, a64, do64, s64, static_cast<const __nv_bfloat16*>(K), static_cast<const __nv_bfloat16*>(b),
       static_cast<const __nv_bfloat16*>(V), static_cast<const __nv_bfloat16*>(cc), static_cast<__nv_bfloat16*>(gK),
-      static_cast<__nv_bfloat16*>(gV), static_cast<int>(N), static_cast<int>(BH), p.scale, c);
+      static_cast<__nv_bfloat16*>(gV), static_cast<int>(N), static_cast<int>(BH), p.scale, c, p.causal);
   return cudaGetLastError();
 }
 

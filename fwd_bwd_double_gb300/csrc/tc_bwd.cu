@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
                    const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const __nv_bfloat16* __restrict__ O, const __nv_bfloat16* __restrict__ dO,
                    const float* __restrict__ lse, __nv_bfloat16* __restrict__ dQ, float4* __restrict__ ws, int N,
-                   int Np, int nrb, int BH, float scale, float c) {
+                   int Np, int nrb, int BH, float scale, float c, int causal) {
   using Lay = RowLay<D, NB, GP>;
   constexpr int NS = Lay::NS;
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -98,7 +98,8 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
   const tc::Order ord = tc::grid_order(BH, nrb);
   const int bh = ord.bh;
   const int rb = nrb - 1 - ord.k;  // heaviest row blocks first (within a group of slices)
-  const int nkv = ((rb + 1) * BM + BN - 1) / BN;                 // key blocks touching rows <= last row
+  // key blocks touching rows <= the last row (all key blocks when not causal)
+  const int nkv = causal ? ((rb + 1) * BM + BN - 1) / BN : (N + BN - 1) / BN;
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(q_full, 1);
@@ -223,6 +224,8 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
       ptx::tmem_ld32(tmem + Lay::cdP + b * BN + c0 + lo, pv);
       ptx::tmem_wait_ld();
       const int krel = j * BN + c0 - rb * BM;  // key of my column 0 minus the block's first row
+      // last visible key of this row, relative to my column 0
+      const int klim = causal ? r - krel : N - 1 - (j * BN + c0);
       uint32_t dsk[16], pk[16];
       auto block = [&](auto masked) {
 #pragma unroll
@@ -230,8 +233,8 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
           const float2 arg = tc::unpk2(tc::fma2(tc::pk2(sv[t], sv[t + 1]), c2, nL2));
           float p0 = ptx::ex2(arg.x), p1 = ptx::ex2(arg.y);
           if constexpr (decltype(masked)::value) {
-            if (krel + t > r) p0 = 0.f;
-            if (krel + t + 1 > r) p1 = 0.f;
+            if (t > klim) p0 = 0.f;
+            if (t + 1 > klim) p1 = 0.f;
           }
           const float2 ds = tc::unpk2(tc::mul2(tc::pk2f(p0, p1), tc::add2(tc::pk2(pv[t], pv[t + 1]), nD2)));
           dsk[t >> 1] = ptx::pack_bf16(ds.x, ds.y);
@@ -242,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
           }
         }
       };
-      if (krel + 31 > 0)  // the causal mask reaches into this thread's columns
+      if (causal ? krel + 31 > 0 : j * BN + c0 + 32 > N)  // the mask reaches into this thread's columns
         block(std::true_type{});
       else
         block(std::false_type{});
@@ -325,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bwd_col_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                    const __grid_constant__ CUtensorMap tmSt, __nv_bfloat16* __restrict__ dK,
-                   __nv_bfloat16* __restrict__ dV, int N, int BH, float scale, float c) {
+                   __nv_bfloat16* __restrict__ dV, int N, int BH, float scale, float c, int causal) {
   using Lay = ColLay<D, NB, GP>;
   constexpr int NS = Lay::NS;
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -344,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int bh = ord.bh;
   const int kb = ord.k;  // first key blocks have the most rows: first
   const int nq = (N + BN - 1) / BN;
-  const int i0 = (kb * BM) / BN;                      // first query block with a query >= first key
+  const int i0 = causal ? (kb * BM) / BN : 0;         // first query block with a query >= first key
   const int ntile = nq - i0;
 
   if (threadIdx.x == 0) {
@@ -463,8 +466,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           float p0 = ptx::ex2(arg.x), p1 = ptx::ex2(arg.y);
           if constexpr (decltype(masked)::value) {
             const int q0 = qbase + u;
-            if (q0 < key || q0 >= N) p0 = 0.f;
-            if (q0 + 1 < key || q0 + 1 >= N) p1 = 0.f;
+            if ((causal && q0 < key) || q0 >= N) p0 = 0.f;
+            if ((causal && q0 + 1 < key) || q0 + 1 >= N) p1 = 0.f;
           }
           const float2 ds =
               tc::unpk2(tc::mul2(tc::pk2f(p0, p1), tc::add2(tc::pk2(pv[u], pv[u + 1]), tc::pk2f(A.z, A.w))));
@@ -477,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       };
-      if (qbase < kb * BM + BM || qbase + 32 > N)  // causal mask (first blocks) or past N (last block)
+      if ((causal && qbase < kb * BM + BM) || qbase + 32 > N)  // causal mask (first blocks) or past N (last block)
         block(std::true_type{});
       else
         block(std::false_type{});
@@ -545,7 +548,7 @@ cudaError_t launch(const Problem& p, const void* Q, const void* K, const void* V
     kern<<<static_cast<unsigned>(nrb * BH), kThreads, Lay::bytes, st>>>(
         q128, do128, k64, v64, static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), lse,
         static_cast<__nv_bfloat16*>(dQ), ws, static_cast<int>(N), static_cast<int>(Np), nrb, static_cast<int>(BH),
-        p.scale, c);
+        p.scale, c, p.causal);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (passes & 2) {
@@ -555,7 +558,7 @@ cudaError_t launch(const Problem& p, const void* Q, const void* K, const void* V
     if (e != cudaSuccess) return e;
     kern<<<static_cast<unsigned>(nrb * BH), kThreads, Lay::bytes, st>>>(
         k128, v128, q64, do64, s64, static_cast<__nv_bfloat16*>(dK), static_cast<__nv_bfloat16*>(dV),
-        static_cast<int>(N), static_cast<int>(BH), p.scale, c);
+        static_cast<int>(N), static_cast<int>(BH), p.scale, c, p.causal);
     return cudaGetLastError();
   }
   return cudaSuccess;

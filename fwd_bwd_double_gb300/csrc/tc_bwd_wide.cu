@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                const __nv_bfloat16* __restrict__ O, const __nv_bfloat16* __restrict__ dO,
                const float* __restrict__ lse, __nv_bfloat16* __restrict__ dQ, float4* __restrict__ ws, int N, int Np,
-               int nrb, int BH, float scale, float c) {
+               int nrb, int BH, float scale, float c, int causal) {
   using Lay = RowLay;
   extern __shared__ __align__(1024) uint8_t sm[];
   Sync sy(sm + Lay::oBar);
@@ -107,7 +107,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const tc::Order ord = tc::grid_order(BH, nrb);
   const int bh = ord.bh;
   const int rb = nrb - 1 - ord.k;  // heaviest first within a group of slices
-  const int nkv = rb + 1;          // 128-key blocks j <= rb
+  const int nkv = causal ? rb + 1 : nrb;  // 128-key blocks j <= rb (all blocks when not causal)
 
   if (threadIdx.x == 0) sy.init(sm);
   if (warp == kCW + 1) {
@@ -219,20 +219,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_before();
       ptx::mbar_arrive(sy.consumed);
       uint32_t dsk[kC / 2];
+      const int klim = causal ? r : N - 1 - j * BW;  // last visible key of this row, relative to the block
       auto block = [&](auto masked) {
 #pragma unroll
         for (int t = 0; t < kC; t += 2) {
           const float2 arg = tc::unpk2(tc::fma2(tc::pk2(sv[t], sv[t + 1]), c2, nL2));
           float p0 = ptx::ex2(arg.x), p1 = ptx::ex2(arg.y);
           if constexpr (decltype(masked)::value) {
-            if (c0 + t > r) p0 = 0.f;  // only the diagonal block is masked: key - row = column - lane row
-            if (c0 + t + 1 > r) p1 = 0.f;
+            // Causal: the diagonal block, key - row = column - lane row.  Otherwise the
+            // last block: keys at or past N.
+            if (c0 + t > klim) p0 = 0.f;
+            if (c0 + t + 1 > klim) p1 = 0.f;
           }
           const float2 ds = tc::unpk2(tc::mul2(tc::pk2f(p0, p1), tc::add2(tc::pk2(pv[t], pv[t + 1]), nD2)));
           dsk[t >> 1] = ptx::pack_bf16(ds.x, ds.y);
         }
       };
-      if (j == rb)
+      if (causal ? j == rb : (j == nkv - 1 && (N % BW) != 0))
         block(std::true_type{});
       else
         block(std::false_type{});
@@ -289,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bwd_col_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                const __grid_constant__ CUtensorMap tmSt, __nv_bfloat16* __restrict__ dK,
-               __nv_bfloat16* __restrict__ dV, int N, int nb, int BH, float scale, float c) {
+               __nv_bfloat16* __restrict__ dV, int N, int nb, int BH, float scale, float c, int causal) {
   using Lay = ColLay;
   extern __shared__ __align__(1024) uint8_t sm[];
   Sync sy(sm + Lay::oBar);
@@ -297,7 +300,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const tc::Order ord = tc::grid_order(BH, nb);
   const int bh = ord.bh;
   const int kb = ord.k;          // first key blocks have the most query blocks: first
-  const int ntile = nb - kb;     // query blocks i >= kb
+  const int i0 = causal ? kb : 0;  // first query block that sees this key block
+  const int ntile = nb - i0;
 
   if (threadIdx.x == 0) sy.init(sm);
   if (warp == kCW + 1) {
@@ -320,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tma_load_3d(sm + Lay::oK, &tmK, sy.held_full, 0, kb * BW, bh);
       ptx::tma_load_3d(sm + Lay::oV, &tmV, sy.held_full, 0, kb * BW, bh);
       for (int t = 0; t < ntile; ++t) {
-        const int s = t % NS, i = kb + t;
+        const int s = t % NS, i = i0 + t;
         if (t >= NS) wait(&sy.empty[s], ((t / NS) - 1) & 1);
         uint8_t* st = sm + Lay::oStage + s * Lay::kStage;
         ptx::mbar_expect_tx(&sy.full[s], 2 * kTile + Lay::kStat);
@@ -393,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int g4 = lane >> 2, q4 = lane & 3;
     const uint64_t c2 = tc::pk2f(c, c);
     for (int t = 0; t < ntile; ++t) {
-      const int s = t % NS, i = kb + t;
+      const int s = t % NS, i = i0 + t;
       wait(sy.s_full, t & 1);
       ptx::tc_fence_after();
       uint32_t sv[2][16], pv[2][16];  // [lanes +0 / +16 of the quarter][repetition k, (row, row+8) x (col, col+1)]
@@ -428,8 +432,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               float p0 = ptx::ex2(arg.x), p1 = ptx::ex2(arg.y);
               if constexpr (decltype(masked)::value) {
                 const int q0 = qbase + 8 * k, kk = kbase + 16 * h + 8 * m;
-                if (q0 < kk || q0 >= N) p0 = 0.f;
-                if (q0 + 1 < kk || q0 + 1 >= N) p1 = 0.f;
+                if ((causal && q0 < kk) || q0 >= N) p0 = 0.f;
+                if ((causal && q0 + 1 < kk) || q0 + 1 >= N) p1 = 0.f;
               }
               const float2 ds = tc::unpk2(
                   tc::mul2(tc::pk2f(p0, p1), tc::add2(tc::pk2(pv[h][e], pv[h][e + 1]), tc::pk2f(A[k].z, A[k].w))));
@@ -437,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               dk[h][2 * k + m] = ptx::pack_bf16(ds.x, ds.y);
             }
       };
-      if (t == 0 || i * BW + c0 + kC > N)  // the diagonal block, or the block reaching past N
+      if ((causal && t == 0) || i * BW + c0 + kC > N)  // the diagonal block, or the block reaching past N
         block(std::true_type{});
       else
         block(std::false_type{});
@@ -504,7 +508,7 @@ cudaError_t tc_bwd_wide(const Problem& p, const void* Q, const void* K, const vo
     bwd_row_wide_kernel<<<static_cast<unsigned>(nb * BH), kThreads, RowLay::bytes, st>>>(
         q, g, k, v, static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), lse,
         static_cast<__nv_bfloat16*>(dQ), ws, static_cast<int>(N), static_cast<int>(Np), nb, static_cast<int>(BH),
-        p.scale, c);
+        p.scale, c, p.causal);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (passes & 2) {
@@ -512,7 +516,7 @@ cudaError_t tc_bwd_wide(const Problem& p, const void* Q, const void* K, const vo
     if (e != cudaSuccess) return e;
     bwd_col_wide_kernel<<<static_cast<unsigned>(nb * BH), kThreads, ColLay::bytes, st>>>(
         k, v, q, g, s, static_cast<__nv_bfloat16*>(dK), static_cast<__nv_bfloat16*>(dV), static_cast<int>(N), nb,
-        static_cast<int>(BH), p.scale, c);
+        static_cast<int>(BH), p.scale, c, p.causal);
     e = cudaGetLastError();
   }
   return e;

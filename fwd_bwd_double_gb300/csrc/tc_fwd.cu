@@ -68,7 +68,7 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O, float* __restrict__ lse,
-               int N, int nrb, int BH, float scale, float scale_log2) {
+               int N, int nrb, int BH, float scale, float scale_log2, int causal) {
   using Lay = Layout<D>;
   extern __shared__ __align__(1024) uint8_t sm[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Lay::oBar);
@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
   const tc::Order ord = tc::grid_order(BH, nrb);
   const int bh = ord.bh;
   const int rb = nrb - 1 - ord.k;  // heaviest row blocks first (within a group of slices)
-  const int nkv = rb + 1;
+  const int nkv = causal ? rb + 1 : nrb;  // key blocks this row block sees
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(q_full, 1);
@@ -186,7 +186,10 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
     for (int j = 0; j < nkv; ++j) {
       wait(s_full, j & 1);
       ptx::tc_fence_after();
-      const bool diag = (j == rb);  // the only block holding keys after some rows
+      // Causal: only the diagonal block holds keys after some rows.  Otherwise only
+      // the last block can hold keys past N (TMA reads them as zeros).
+      const bool diag = causal ? (j == rb) : (j == nkv - 1 && (N % BN) != 0);
+      const int klim = causal ? r : N - 1 - j * BN;  // last visible key of this row, relative to the block
       // The whole 128-column S row in registers: four loads, one wait.
       uint32_t v[4][32];
 #pragma unroll
@@ -199,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
         for (int ch = 0; ch < 4; ++ch)
 #pragma unroll
           for (int t = 0; t < 32; ++t)
-            if (ch * 32 + t > r) v[ch][t] = __float_as_uint(-INFINITY);
+            if (ch * 32 + t > klim) v[ch][t] = __float_as_uint(-INFINITY);
       }
       // Row max over 8 independent partial maxima (short dependency chains).
       float mx8[8];
@@ -299,7 +302,7 @@ cudaError_t launch(const Problem& p, const void* Q, const void* K, const void* V
   const float log2e = 1.4426950408889634f;
   fwd_kernel<D><<<static_cast<unsigned>(nrb * p.BH), kThreads, smem, st>>>(
       mq, mk, mv, static_cast<__nv_bfloat16*>(O), lse, static_cast<int>(p.N), nrb, static_cast<int>(p.BH),
-      p.scale, p.scale * log2e);
+      p.scale, p.scale * log2e, p.causal);
   return cudaGetLastError();
 }
 

@@ -1,6 +1,7 @@
 /*
- * fbd.h -- C ABI of libfbd: exact causal softmax attention on GB300 (sm_103a):
- * forward, recompute backward (optional GProj), and backward-over-backward.
+ * fbd.h -- C ABI of libfbd: exact softmax attention (causal or not) on GB300
+ * (sm_103a): forward, recompute backward (optional GProj), and
+ * backward-over-backward.
  *
  * The N x N score matrix is never written to device memory.  All entry points
  * take plain device pointers owned by the caller; the library allocates and
@@ -29,7 +30,7 @@
  *               (inputs and outputs alike): ATTN_F32 = float, ATTN_BF16 =
  *               bfloat16.  Arithmetic is float32 throughout (bf16 tensor-core
  *               products accumulate in float32).
- *   Supported:  causal == 1; d in {64, 128}; dtype in {ATTN_F32, ATTN_BF16};
+ *   Supported:  causal in {0, 1}; d in {64, 128}; dtype in {ATTN_F32, ATTN_BF16};
  *               for attn_bob with ATTN_BF16, d == 64.  Anything else returns
  *               ATTN_ERR_UNSUPPORTED before any launch; there is no fallback.
  *   Scale:      desc->scale == 0 means 1/sqrt(d); otherwise it must be finite and
@@ -61,7 +62,7 @@ extern "C" {
 typedef enum {
   ATTN_OK = 0,
   ATTN_ERR_INVALID_ARG = 1,  /* NULL/negative/overlapping arguments, non-finite scale */
-  ATTN_ERR_UNSUPPORTED = 2,  /* causal != 1, d not supported, unknown dtype */
+  ATTN_ERR_UNSUPPORTED = 2,  /* causal not 0 or 1, d not supported, unknown dtype */
   ATTN_ERR_ALIGNMENT = 3,    /* a pointer is not 16-byte aligned */
   ATTN_ERR_WORKSPACE = 4,    /* workspace NULL or smaller than the *_workspace_bytes query */
   ATTN_ERR_LAUNCH = 5,       /* CUDA rejected a launch or a tensor-map encode */
@@ -74,7 +75,9 @@ typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1 } attn_dtype_t;
 typedef struct {
   int64_t B, H, N, d;  /* batch, heads, sequence length, head dimension */
   float scale;         /* softmax scale s; 0 means 1/sqrt(d) */
-  int32_t causal;      /* must be 1: key j is visible to query i iff j <= i */
+  int32_t causal;      /* 1: key j is visible to query i iff j <= i ([FA] "Causal
+                          masking is where trading gets a discount"); 0: every key
+                          is visible to every query (a full softmax over the row) */
   int32_t dtype;       /* attn_dtype_t */
 } attn_desc_t;
 
@@ -82,8 +85,8 @@ typedef struct {
  * causal masking; [GP] "Why the error appears late" (max subtracted before the
  * scale is applied, so the row max maps to exactly exp(0) = 1).
  *   In:  Q, K, V [B,H,N,d].
- *   Out: O [B,H,N,d] = softmax(s Q K^T + causal mask) V;
- *        lse [B,H,N] float32, lse_i = log sum_{j<=i} exp(s q_i.k_j) (natural log),
+ *   Out: O [B,H,N,d] = softmax(s Q K^T + mask) V (mask: causal, or none);
+ *        lse [B,H,N] float32, lse_i = log sum_{j visible} exp(s q_i.k_j) (natural log),
  *        the single-number form of the softmax statistics (m, l) kept for the
  *        recompute backward ([FA] "Backward pass: recompute instead of store"). */
 attn_status_t attn_fwd(const attn_desc_t* desc, const void* Q, const void* K, const void* V,
@@ -187,7 +190,8 @@ attn_status_t attn_bob_passes(const attn_desc_t* desc, const void* Q, const void
 
 /* Diagnostic export of the GProj-projected score gradient (bf16 only).
  * Writes dS_out [B,H,N,N] float32 with dS_out[i][j] = dS^_ij - rho_i P^_ij for
- * j <= i (and 0 for j > i), where dS^, P^ and rho_i = r_i / sum_k P^_ik are the
+ * every visible key j (0 for j > i under the causal mask), where dS^, P^ and
+ * rho_i = r_i / sum_k P^_ik are the
  * very values the GProj row pass feeds to its products.  Meant for small N:
  * the output is N x N per slice.  [GP] "How the zero sum turns into a false
  * gradient". */

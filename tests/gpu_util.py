@@ -47,28 +47,29 @@ def inputs(w):
 
 
 @functools.lru_cache(maxsize=8)
-def oracle_full(w, op):
+def oracle_full(w, op, causal=True):
     """Oracle outputs [B, H, ...] for every slice of workload w (op: fwd, bwd, bob)."""
     x = inputs(w)
     if op == "fwd":
-        return oracle.forward_all(x["Q"], x["K"], x["V"], scale=w.scale)
+        return oracle.forward_all(x["Q"], x["K"], x["V"], scale=w.scale, causal=causal)
     if op == "bwd":
-        return oracle.backward_all(x["Q"], x["K"], x["V"], x["dO"], scale=w.scale)
-    return oracle.bob_all(x["Q"], x["K"], x["V"], x["dO"], x["gdQ"], x["gdK"], x["gdV"], scale=w.scale)
+        return oracle.backward_all(x["Q"], x["K"], x["V"], x["dO"], scale=w.scale, causal=causal)
+    return oracle.bob_all(x["Q"], x["K"], x["V"], x["dO"], x["gdQ"], x["gdK"], x["gdV"], scale=w.scale,
+                          causal=causal)
 
 
-def run_ops(w, x_dev, ops=("fwd", "bwd", "bob"), gproj=0):
+def run_ops(w, x_dev, ops=("fwd", "bwd", "bob"), gproj=0, causal=True):
     """Run the requested ops through the binding; return host fp64 arrays."""
     import fwd_bwd_double_gb300 as fbd
     out = {}
-    O, lse = fbd.attn_fwd(x_dev["Q"], x_dev["K"], x_dev["V"], scale=w.scale)
+    O, lse = fbd.attn_fwd(x_dev["Q"], x_dev["K"], x_dev["V"], scale=w.scale, causal=causal)
     out["O"], out["L"] = O, lse
     if "bwd" in ops:
         out["dQ"], out["dK"], out["dV"] = fbd.attn_bwd(x_dev["Q"], x_dev["K"], x_dev["V"], O, x_dev["dO"], lse,
-                                                       gproj=gproj, scale=w.scale)
+                                                       gproj=gproj, scale=w.scale, causal=causal)
     if "bob" in ops:
         out["gQ"], out["gK"], out["gV"], out["gdO"] = fbd.attn_bob(
             x_dev["Q"], x_dev["K"], x_dev["V"], O, x_dev["dO"], lse, x_dev["gdQ"], x_dev["gdK"], x_dev["gdV"],
-            scale=w.scale)
+            scale=w.scale, causal=causal)
     fbd.attn_device_status()
     return out

@@ -58,7 +58,7 @@ def bob(dsc, p=None, ws_bytes=None):
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(causal=0), UNSUP), (dict(d=32), UNSUP), (dict(d=256), UNSUP), (dict(dtype=7), UNSUP),
+    (dict(causal=2), UNSUP), (dict(causal=-1), UNSUP), (dict(d=32), UNSUP), (dict(d=256), UNSUP), (dict(dtype=7), UNSUP),
     (dict(B=-1), INVALID), (dict(N=-5), INVALID), (dict(d=0), INVALID),
     (dict(scale=float("nan")), INVALID), (dict(scale=float("inf")), INVALID), (dict(scale=-1.0), INVALID),
     (dict(N=1 << 31), INVALID),

@@ -26,17 +26,17 @@ def _lib():
     __graft_entry__.build()
 
 
-def check_full(w, got, ops):
+def check_full(w, got, ops, causal=True):
     tol = TOL[w.dtype]
     errs = {}
-    f = oracle_full(w, "fwd")
+    f = oracle_full(w, "fwd", causal)
     errs["O"], errs["L"] = rel_fro(host(got["O"]), f["O"]), rel_fro(host(got["L"]), f["L"])
     if "bwd" in ops:
-        b = oracle_full(w, "bwd")
+        b = oracle_full(w, "bwd", causal)
         for k in ("dQ", "dK", "dV"):
             errs[k] = rel_fro(host(got[k]), b[k])
     if "bob" in ops:
-        b = oracle_full(w, "bob")
+        b = oracle_full(w, "bob", causal)
         for k in ("gQ", "gK", "gV", "gdO"):
             errs[k] = rel_fro(host(got[k]), b[k])
     bad = {k: v for k, v in errs.items() if not v <= tol}
@@ -288,4 +288,66 @@ def test_result_does_not_depend_on_workspace_content(N, dtype):
 
     for a, b in zip(run(0.0), run(float("nan"))):
         assert not torch.isnan(b).any()
+        assert torch.equal(a, b)
+
+
+
+# ---------------------------------------------------------------- non-causal
+# Every key visible to every query: the same kernels with the causal mask off (only
+# keys past N masked), against the oracle's non-causal mode.
+
+def test_noncausal_tiny_f32_all_ops():
+    w = W.Workload("noncausal_tiny_f32_B1H1N256d64", 1, 1, 256, 64, "f32")
+    got = run_ops(w, to_device(inputs(w), w), causal=False)
+    errs = check_full(w, got, ("bwd", "bob"), causal=False)
+    print(w.name, {k: f"{v:.2e}" for k, v in errs.items()})
+
+
+@pytest.mark.parametrize("gproj", [0, 1])
+def test_noncausal_gpt2_layer_bf16(gproj):
+    w = W.Workload("noncausal_gpt2small_B4H12N1024d64", 4, 12, 1024, 64, "bf16")
+    ops = ("bwd", "bob") if gproj == 0 else ("bwd",)
+    got = run_ops(w, to_device(inputs(w), w), ops=ops, gproj=gproj, causal=False)
+    errs = check_full(w, got, ops, causal=False)
+    print(w.name, gproj, {k: f"{v:.2e}" for k, v in errs.items()})
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", [1, 17, 129, 300])
+def test_noncausal_edge_sizes(N, d, dtype):
+    w = W.Workload(f"noncausal_edge_B1H2N{N}d{d}_{dtype}", 1, 2, N, d, dtype)
+    ops = ("bwd", "bob") if (dtype == "f32" or d == 64) else ("bwd",)
+    got = run_ops(w, to_device(inputs(w), w), ops=ops, causal=False)
+    check_full(w, got, ops, causal=False)
+    if dtype == "bf16":
+        got1 = run_ops(w, to_device(inputs(w), w), ops=("bwd",), gproj=1, causal=False)
+        check_full(w, got1, ("bwd",), causal=False)
+
+
+def test_noncausal_differs_from_causal_and_passes_compose():
+    """The mask flag reaches the kernels (the outputs differ), and the separate row and
+    column passes give the fused call's bits without the causal mask too."""
+    import torch
+
+    import fwd_bwd_double_gb300 as fbd
+    w = W.Workload("noncausal_passes_B2H3N300d64_bf16", 2, 3, 300, 64, "bf16")
+    x = to_device(inputs(w), w)
+    O, lse = fbd.attn_fwd(x["Q"], x["K"], x["V"], causal=False)
+    Oc, _ = fbd.attn_fwd(x["Q"], x["K"], x["V"], causal=True)
+    assert not torch.equal(O[:, :, :-1], Oc[:, :, :-1])
+    ref_b = fbd.attn_bwd(x["Q"], x["K"], x["V"], O, x["dO"], lse, causal=False)
+    ref_g = fbd.attn_bob(x["Q"], x["K"], x["V"], O, x["dO"], lse, x["gdQ"], x["gdK"], x["gdV"], causal=False)
+    outs = [torch.empty_like(x["Q"]) for _ in range(3)]
+    ws = torch.full((fbd.attn_bwd_workspace_bytes(fbd.make_desc(x["Q"]), 1) // 4,), float("nan"),
+                    dtype=torch.float32, device="cuda").view(torch.uint8)
+    for ps in (fbd.ATTN_ROW_PASS, fbd.ATTN_COL_PASS):
+        fbd.attn_bwd_passes(x["Q"], x["K"], x["V"], O, x["dO"], lse, ps, dQ=outs[0], dK=outs[1], dV=outs[2],
+                            workspace=ws, causal=False)
+    gouts = [torch.empty_like(x["Q"]) for _ in range(4)]
+    for ps in (fbd.ATTN_ROW_PASS, fbd.ATTN_COL_PASS):
+        fbd.attn_bob_passes(x["Q"], x["K"], x["V"], O, x["dO"], lse, x["gdQ"], x["gdK"], x["gdV"], ps,
+                            gQ=gouts[0], gK=gouts[1], gV=gouts[2], gdO=gouts[3], workspace=ws, causal=False)
+    fbd.attn_device_status()
+    for a, b in zip(outs + gouts, list(ref_b) + list(ref_g)):
         assert torch.equal(a, b)
