@@ -475,14 +475,38 @@ def _each_slice(fn, *tensors, **kw):
     return outs
 
 
-def forward_all(Q, K, V, scale=None, causal=True):
+def _expand_kv(X, groups):
+    """Grouped key/value heads: query head h of a [B, H, ...] problem reads key/value
+    head h // groups of the [B, H / groups, ...] tensors."""
+    return X if groups == 1 else np.repeat(X, groups, axis=1)
+
+
+def _sum_groups(X, groups):
+    """Gradient of a shared key/value head: the sum over the query heads that read it
+    (chain rule through the repetition)."""
+    if groups == 1:
+        return X
+    B, H = X.shape[:2]
+    return X.reshape((B, H // groups, groups) + X.shape[2:]).sum(axis=2)
+
+
+def forward_all(Q, K, V, scale=None, causal=True, groups=1):
+    K, V = _expand_kv(K, groups), _expand_kv(V, groups)
     return _each_slice(lambda q, k, v, **kw: dict(zip(("O", "L"), forward(q, k, v, **kw))),
                        Q, K, V, scale=scale, causal=causal)
 
 
-def backward_all(Q, K, V, dO, scale=None, causal=True):
-    return _each_slice(backward, Q, K, V, dO, scale=scale, causal=causal)
+def backward_all(Q, K, V, dO, scale=None, causal=True, groups=1):
+    out = _each_slice(backward, Q, _expand_kv(K, groups), _expand_kv(V, groups), dO, scale=scale, causal=causal)
+    out["dK"], out["dV"] = _sum_groups(out["dK"], groups), _sum_groups(out["dV"], groups)
+    return out
 
 
-def bob_all(Q, K, V, dO, a, b, c, scale=None, causal=True):
-    return _each_slice(bob, Q, K, V, dO, a, b, c, scale=scale, causal=causal)
+def bob_all(Q, K, V, dO, a, b, c, scale=None, causal=True, groups=1):
+    """With grouped heads the first backward's dK, dV are sums over each group, so their
+    cotangents b, c are per key/value head and enter every query head of the group; the
+    per-head second derivatives of K and V are summed over the group the same way."""
+    e = lambda X: _expand_kv(X, groups)
+    out = _each_slice(bob, Q, e(K), e(V), dO, a, e(b), e(c), scale=scale, causal=causal)
+    out["gK"], out["gV"] = _sum_groups(out["gK"], groups), _sum_groups(out["gV"], groups)
+    return out

@@ -551,3 +551,62 @@ def test_noncausal_bob_against_fp64_autograd():
         assert rel(ref[k], t.numpy()) <= 1e-13, k
     fb = oracle.backward(*arrs[:4], causal=False)
     assert rel(fb["dQ"], dQ.detach().numpy()) <= 1e-13
+
+
+# ----------------------------------------------------- grouped key/value heads ----
+# H query heads share H / g key/value heads: query head h reads key/value head h // g.
+# Pinned by finite differences of the loss summed over the heads (so the gradient of a
+# shared head is whatever the chain rule makes it, not the oracle's group sum).
+
+def _gqa_loss(Q, K, V, dO, s, g, causal):
+    O = oracle.forward_all(Q, K, V, scale=s, causal=causal, groups=g)["O"]
+    return float((O * dO).sum())
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_gqa_backward_matches_finite_differences(causal):
+    r = np.random.default_rng(94)
+    B, H, g, N, d = 1, 4, 2, 5, 3
+    Q, dO = r.standard_normal((B, H, N, d)), r.standard_normal((B, H, N, d))
+    K, V = r.standard_normal((B, H // g, N, d)), r.standard_normal((B, H // g, N, d))
+    s = 0.6
+    out = oracle.backward_all(Q, K, V, dO, scale=s, causal=causal, groups=g)
+    assert out["dK"].shape == K.shape and out["dQ"].shape == Q.shape
+    gK = fd_grad(lambda X: _gqa_loss(Q, X, V, dO, s, g, causal), K)
+    gV = fd_grad(lambda X: _gqa_loss(Q, K, X, dO, s, g, causal), V)
+    gQ = fd_grad(lambda X: _gqa_loss(X, K, V, dO, s, g, causal), Q)
+    top = max(np.abs(gK).max(), np.abs(gV).max(), np.abs(gQ).max())
+    assert np.abs(out["dK"] - gK).max() <= 1e-8 * top
+    assert np.abs(out["dV"] - gV).max() <= 1e-8 * top
+    assert np.abs(out["dQ"] - gQ).max() <= 1e-8 * top
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_gqa_bob_is_hessian_vector_product(causal):
+    """BoB with shared heads: the directional derivative of the grouped first backward
+    (dQ per query head, dK and dV per shared head) along (a, b, c), by central differences."""
+    r = np.random.default_rng(95)
+    B, H, g, N, d = 1, 4, 2, 5, 3
+    Q, dO, a = (r.standard_normal((B, H, N, d)) for _ in range(3))
+    K, V, b, c = (r.standard_normal((B, H // g, N, d)) for _ in range(4))
+    s, h = 0.55, 1e-5
+    out = oracle.bob_all(Q, K, V, dO, a, b, c, scale=s, causal=causal, groups=g)
+    gp = oracle.backward_all(Q + h * a, K + h * b, V + h * c, dO, scale=s, causal=causal, groups=g)
+    gm = oracle.backward_all(Q - h * a, K - h * b, V - h * c, dO, scale=s, causal=causal, groups=g)
+    for name, key in (("gQ", "dQ"), ("gK", "dK"), ("gV", "dV")):
+        fd = (gp[key] - gm[key]) / (2 * h)
+        assert out[name].shape == fd.shape
+        assert np.abs(out[name] - fd).max() <= 1e-8 * max(np.abs(fd).max(), 1e-3), name
+    Op = oracle.forward_all(Q + h * a, K + h * b, V + h * c, scale=s, causal=causal, groups=g)["O"]
+    Om = oracle.forward_all(Q - h * a, K - h * b, V - h * c, scale=s, causal=causal, groups=g)["O"]
+    fd = (Op - Om) / (2 * h)
+    assert np.abs(out["gdO"] - fd).max() <= 1e-8 * max(np.abs(fd).max(), 1e-3)
+
+
+def test_gqa_with_one_group_is_plain_attention():
+    r = np.random.default_rng(96)
+    X = [r.standard_normal((2, 3, 7, 4)) for _ in range(7)]
+    a = oracle.bob_all(*X, groups=1)
+    b = oracle.bob_all(*X)
+    for k in ("gQ", "gK", "gV", "gdO"):
+        assert np.array_equal(a[k], b[k])
