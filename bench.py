@@ -2,7 +2,7 @@
 on one batch of synthetic inputs, through the C ABI of libfbd.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--n-seq S] [--batch B] [--heads H] [--gproj 0|1]
+                  [--n-seq S] [--batch B] [--heads H] [--group G] [--gproj 0|1] [--causal 0|1]
 
 Workload: the GPT-2 Small layer shape at N = 8192 (B=4, H=12, d=64, causal, bf16
 inputs, fp32 accumulation), the shape the throughput targets are stated on.
@@ -183,10 +183,12 @@ def run_ours(args, w, rank, world):
     stream = torch.cuda.Stream(device=dev)
     pinned, x = make_inputs(w, dev)
     torch.cuda.synchronize()
-    desc = fbd.make_desc(x["Q"], w.scale, int(CAUSAL))
+    desc = fbd.make_desc(x["Q"], w.scale, int(CAUSAL), x["K"])
     bf = torch.bfloat16
     shp = x["Q"].shape
-    out = {k: torch.empty(shp, dtype=bf, device=dev) for k in ("O", "dQ", "dK", "dV", "gQ", "gK", "gV", "gdO")}
+    # Outputs with the shape of their input: dK, dV, gK, gV follow K (H / group heads).
+    like = {"O": "Q", "dQ": "Q", "dK": "K", "dV": "V", "gQ": "Q", "gK": "K", "gV": "V", "gdO": "Q"}
+    out = {k: torch.empty(x[src].shape, dtype=bf, device=dev) for k, src in like.items()}
     lse = torch.empty(shp[:3], dtype=torch.float32, device=dev)
     ws = torch.empty(fbd.attn_bwd_workspace_bytes(desc, 1), dtype=torch.uint8, device=dev)
     ws2 = torch.empty(fbd.attn_bob_workspace_bytes(desc), dtype=torch.uint8, device=dev)
@@ -260,12 +262,12 @@ def run_ours(args, w, rank, world):
     # memory.  The copies of step i+1's inputs and of step i-1's outputs run on their
     # own streams (the GPU's copy engines) while step i computes; input and output
     # device buffers are double-buffered, and events order reuse.
-    host_out = {k: torch.empty(shp, dtype=bf).pin_memory() for k in out}
+    host_out = {k: torch.empty(out[k].shape, dtype=bf).pin_memory() for k in out}
     host_lse = torch.empty(shp[:3], dtype=torch.float32).pin_memory()
     e2e_steps = max(4, min(args.steps, 8))
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     xin = [{k: torch.empty_like(v) for k, v in x.items()} for _ in range(2)]
-    outs = [{k: torch.empty(shp, dtype=bf, device=dev) for k in out} for _ in range(2)]
+    outs = [{k: torch.empty_like(out[k]) for k in out} for _ in range(2)]
     lses = [torch.empty(shp[:3], dtype=torch.float32, device=dev) for _ in range(2)]
 
     def e2e_step(xx, oo, ll):
@@ -412,6 +414,8 @@ def main():
     ap.add_argument("--n-seq", type=int, default=8192)
     ap.add_argument("--batch", type=int, default=4)
     ap.add_argument("--heads", type=int, default=12)
+    ap.add_argument("--group", type=int, default=1,
+                    help="query heads per key/value head (grouped-query attention; 1 = multi-head)")
     ap.add_argument("--gproj", type=int, default=0)
     ap.add_argument("--causal", type=int, default=1, choices=[0, 1],
                     help="1: causal attention (the headline workload); 0: every key visible")
@@ -426,13 +430,15 @@ def main():
     args.warmup = max(args.warmup, 3)
     global CAUSAL
     CAUSAL = bool(args.causal)
-    w = W.Workload(f"gpt2small_B{args.batch}H{args.heads}N{args.n_seq}d64" + ("" if CAUSAL else "_noncausal"),
-                   args.batch, args.heads, args.n_seq, 64, "bf16")
+    w = W.Workload(f"gpt2small_B{args.batch}H{args.heads}N{args.n_seq}d64" + ("" if CAUSAL else "_noncausal")
+                   + (f"_g{args.group}" if args.group > 1 else ""),
+                   args.batch, args.heads, args.n_seq, 64, "bf16", group=args.group)
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
-    config = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": 64, "causal": CAUSAL,
+    config = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": 64, "causal": CAUSAL, "group": w.group,
               "ops": "fwd + bwd(gproj=%d) + BoB" % args.gproj,
-              "l2": "inputs larger than L2 (each input tensor %.0f MB; 7 inputs)" % (w.rows * 64 * 2 / 1e6),
+              "l2": "inputs larger than L2 (7 input tensors, %.0f MB in total)"
+                    % (w.rows * 64 * 2 * (3 + 4 / w.group) / 1e6),
               "parallelism": f"independent replicas x{world}"}
 
     if args.impl == "reference":

@@ -38,12 +38,16 @@ def _dtype_code(t) -> int:
     raise FbdError(2, f"unsupported tensor dtype {t.dtype} (float32 or bfloat16)")
 
 
-def make_desc(Q, scale: float = 0.0, causal: int = 1) -> AttnDesc:
-    """Descriptor from a [B, H, N, d] tensor."""
-    if Q.dim() != 4:
+def make_desc(Q, scale: float = 0.0, causal: int = 1, K=None) -> AttnDesc:
+    """Descriptor from a [B, H, N, d] query tensor and, for grouped key/value heads,
+    the [B, H / g, N, d] key tensor (g query heads per key/value head)."""
+    if Q.dim() != 4 or (K is not None and K.dim() != 4):
         raise FbdError(1, "tensors must be [B, H, N, d]")
     B, H, N, d = Q.shape
-    return AttnDesc(B, H, N, d, float(scale), int(causal), _dtype_code(Q))
+    Hkv = H if K is None else K.shape[1]
+    if (Hkv == 0) != (H == 0) or (Hkv and H % Hkv):
+        raise FbdError(1, f"key/value heads ({Hkv}) must divide query heads ({H})")
+    return AttnDesc(B, H, N, d, float(scale), int(causal), _dtype_code(Q), H // Hkv if Hkv else 1)
 
 
 def _ptr(t):
@@ -72,7 +76,7 @@ def _check(status: int):
 def attn_fwd(Q, K, V, O=None, lse=None, scale: float = 0.0, stream=None, desc=None, causal: bool = True):
     """O, lse = attention forward (allocates O and lse with torch when not given)."""
     torch = _torch()
-    desc = desc or make_desc(Q, scale, int(causal))
+    desc = desc or make_desc(Q, scale, int(causal), K)
     if O is None:
         O = torch.empty_like(Q)
     if lse is None:
@@ -107,7 +111,7 @@ def attn_bwd_passes(Q, K, V, O, dO, lse, passes, gproj: int = 0, dQ=None, dK=Non
                     scale: float = 0.0, stream=None, desc=None, causal: bool = True):
     """The backward's row pass (dQ) and/or column pass (dK, dV); see attn_bwd_passes in fbd.h."""
     torch = _torch()
-    desc = desc or make_desc(Q, scale, int(causal))
+    desc = desc or make_desc(Q, scale, int(causal), K)
     dQ = torch.empty_like(Q) if dQ is None else dQ
     dK = torch.empty_like(K) if dK is None else dK
     dV = torch.empty_like(V) if dV is None else dV
@@ -131,7 +135,7 @@ def attn_bob_passes(Q, K, V, O, dO, lse, gdQ, gdK, gdV, passes, gQ=None, gK=None
                     workspace=None, scale: float = 0.0, stream=None, desc=None, causal: bool = True):
     """BoB's row pass (gQ, gdO, row states) and/or column pass (gK, gV); see fbd.h."""
     torch = _torch()
-    desc = desc or make_desc(Q, scale, int(causal))
+    desc = desc or make_desc(Q, scale, int(causal), K)
     gQ = torch.empty_like(Q) if gQ is None else gQ
     gK = torch.empty_like(K) if gK is None else gK
     gV = torch.empty_like(V) if gV is None else gV
@@ -149,7 +153,7 @@ def attn_bob_static(Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ=None, gK=None, gV=Non
     """attn_bob without a workspace argument: the library's static scratch array is used
     (for callers that cannot allocate device memory; B*H*N <= 1,048,576)."""
     torch = _torch()
-    desc = desc or make_desc(Q, scale, int(causal))
+    desc = desc or make_desc(Q, scale, int(causal), K)
     gQ = torch.empty_like(Q) if gQ is None else gQ
     gK = torch.empty_like(K) if gK is None else gK
     gV = torch.empty_like(V) if gV is None else gV
@@ -163,7 +167,7 @@ def attn_bob_static(Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ=None, gK=None, gV=Non
 def attn_bwd_projected_dS(Q, K, V, O, dO, lse, dS=None, scale: float = 0.0, stream=None, desc=None, causal: bool = True):
     """Diagnostic: the GProj-projected dS [B, H, N, N] float32 (small N only)."""
     torch = _torch()
-    desc = desc or make_desc(Q, scale, int(causal))
+    desc = desc or make_desc(Q, scale, int(causal), K)
     B, H, N, _ = Q.shape
     dS = torch.empty((B, H, N, N), dtype=torch.float32, device=Q.device) if dS is None else dS
     _check(lib.attn_bwd_projected_dS(ctypes.byref(desc), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO),

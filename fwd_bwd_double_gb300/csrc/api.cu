@@ -35,6 +35,9 @@ attn_status_t check_desc(const attn_desc_t* desc, fbd::Problem& p) {
   if (desc->B < 0 || desc->H < 0 || desc->N < 0 || desc->d <= 0)
     return fail(ATTN_ERR_INVALID_ARG, "negative B/H/N or non-positive d%s");
   if (desc->causal != 0 && desc->causal != 1) return fail(ATTN_ERR_UNSUPPORTED, "causal must be 0 or 1%s");
+  if (desc->group < 0) return fail(ATTN_ERR_INVALID_ARG, "group must be >= 0%s");
+  const int64_t g = desc->group == 0 ? 1 : desc->group;
+  if (desc->H % g != 0) return fail(ATTN_ERR_INVALID_ARG, "group must divide H%s");
   if (desc->d != 64 && desc->d != 128) return fail(ATTN_ERR_UNSUPPORTED, "head dim must be 64 or 128%s");
   if (desc->dtype != ATTN_F32 && desc->dtype != ATTN_BF16) return fail(ATTN_ERR_UNSUPPORTED, "unknown dtype%s");
   if (!std::isfinite(desc->scale) || desc->scale < 0.f)
@@ -54,12 +57,17 @@ attn_status_t check_desc(const attn_desc_t* desc, fbd::Problem& p) {
   p.scale = desc->scale == 0.f ? 1.0f / std::sqrt(static_cast<float>(desc->d)) : desc->scale;
   p.dtype = desc->dtype;
   p.causal = desc->causal;
+  p.group = static_cast<int>(g);
+  p.BHkv = p.BH / g;
   if (p.BH >= lim) return fail(ATTN_ERR_INVALID_ARG, "B*H must be < 2^31%s");
   if (((p.N + 7) / 8) * p.BH >= lim) return fail(ATTN_ERR_INVALID_ARG, "B*H*N too large for one launch%s");
   return ATTN_OK;
 }
 
 size_t elem_size(const fbd::Problem& p) { return p.dtype == ATTN_F32 ? 4 : 2; }
+
+// Bytes of one [B, H / group, N, d] key/value-side tensor.
+size_t kv_bytes(const fbd::Problem& p) { return static_cast<size_t>(p.BHkv * p.N * p.d) * elem_size(p); }
 
 // Non-NULL, 16-byte aligned, pairwise non-overlapping outputs vs everything.
 attn_status_t check_ptrs(const Span* in, int nin, const Span* out, int nout) {
@@ -115,7 +123,8 @@ attn_status_t attn_fwd(const attn_desc_t* desc, const void* Q, const void* K, co
   if (s != ATTN_OK) return s;
   if (p.BH * p.N == 0) return ATTN_OK;
   const size_t tb = static_cast<size_t>(p.BH * p.N * p.d) * elem_size(p), sb = p.BH * p.N * sizeof(float);
-  const Span in[] = {span("Q", Q, tb), span("K", K, tb), span("V", V, tb)};
+  const size_t kb = kv_bytes(p);
+  const Span in[] = {span("Q", Q, tb), span("K", K, kb), span("V", V, kb)};
   const Span out[] = {span("O", O, tb), span("lse", lse, sb)};
   if ((s = check_ptrs(in, 3, out, 2)) != ATTN_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -151,9 +160,10 @@ attn_status_t attn_bwd_passes(const attn_desc_t* desc, const void* Q, const void
   if (workspace == nullptr || workspace_bytes < need)
     return fail(ATTN_ERR_WORKSPACE, "workspace NULL or smaller than attn_bwd_workspace_bytes()%s");
   const size_t tb = static_cast<size_t>(p.BH * p.N * p.d) * elem_size(p), sb = p.BH * p.N * sizeof(float);
-  const Span in[] = {span("Q", Q, tb), span("K", K, tb), span("V", V, tb),
+  const size_t kb = kv_bytes(p);
+  const Span in[] = {span("Q", Q, tb), span("K", K, kb), span("V", V, kb),
                      span("O", O, tb), span("dO", dO, tb), span("lse", lse, sb)};
-  const Span out[] = {span("dQ", dQ, tb), span("dK", dK, tb), span("dV", dV, tb),
+  const Span out[] = {span("dQ", dQ, tb), span("dK", dK, kb), span("dV", dV, kb),
                       span("workspace", workspace, need)};
   if ((s = check_ptrs(in, 6, out, 4)) != ATTN_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -186,10 +196,11 @@ attn_status_t attn_bob_passes(const attn_desc_t* desc, const void* Q, const void
   if (workspace == nullptr || workspace_bytes < need)
     return fail(ATTN_ERR_WORKSPACE, "workspace NULL or smaller than attn_bob_workspace_bytes()%s");
   const size_t tb = static_cast<size_t>(p.BH * p.N * p.d) * elem_size(p), sb = p.BH * p.N * sizeof(float);
-  const Span in[] = {span("Q", Q, tb),     span("K", K, tb),     span("V", V, tb),
+  const size_t kb = kv_bytes(p);
+  const Span in[] = {span("Q", Q, tb),     span("K", K, kb),     span("V", V, kb),
                      span("O", O, tb),     span("dO", dO, tb),   span("lse", lse, sb),
-                     span("gdQ", gdQ, tb), span("gdK", gdK, tb), span("gdV", gdV, tb)};
-  const Span out[] = {span("gQ", gQ, tb), span("gK", gK, tb), span("gV", gV, tb), span("gdO", gdO, tb),
+                     span("gdQ", gdQ, tb), span("gdK", gdK, kb), span("gdV", gdV, kb)};
+  const Span out[] = {span("gQ", gQ, tb), span("gK", gK, kb), span("gV", gV, kb), span("gdO", gdO, tb),
                       span("workspace", workspace, need)};
   if ((s = check_ptrs(in, 9, out, 5)) != ATTN_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -217,7 +228,8 @@ attn_status_t attn_bwd_projected_dS(const attn_desc_t* desc, const void* Q, cons
   if (p.BH * p.N == 0) return ATTN_OK;
   const size_t tb = static_cast<size_t>(p.BH * p.N * p.d) * 2, sb = p.BH * p.N * sizeof(float);
   const size_t ob = static_cast<size_t>(p.BH) * p.N * p.N * sizeof(float);
-  const Span in[] = {span("Q", Q, tb), span("K", K, tb), span("V", V, tb),
+  const size_t kb = static_cast<size_t>(p.BHkv * p.N * p.d) * 2;
+  const Span in[] = {span("Q", Q, tb), span("K", K, kb), span("V", V, kb),
                      span("O", O, tb), span("dO", dO, tb), span("lse", lse, sb)};
   const Span out[] = {span("dS_out", dS_out, ob)};
   if ((s = check_ptrs(in, 6, out, 1)) != ATTN_OK) return s;

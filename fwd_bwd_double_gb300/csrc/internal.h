@@ -15,6 +15,8 @@ struct Problem {
   float scale;    // s, already resolved (1/sqrt(d) when the caller passed 0)
   int dtype;      // attn_dtype_t
   int causal;     // 1: key j visible to query i iff j <= i; 0: every key visible
+  int group;      // query heads per key/value head (1: multi-head attention)
+  int64_t BHkv;   // B * H / group key/value slices; query slice bh reads slice bh / group
 };
 
 // Float32 path: CUDA-core kernels with float32 inputs/outputs (exact fp32 arithmetic).

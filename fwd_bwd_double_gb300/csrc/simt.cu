@@ -107,7 +107,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) fwd_kernel(const T* __restrict__ Q, const T* __restrict__ K,
                                                        const T* __restrict__ Vt, T* __restrict__ O,
                                                        float* __restrict__ lse, int64_t N, int64_t BH,
-                                                       float scale, int causal) {
+                                                       float scale, int causal, int64_t G) {
   constexpr int V = D / 32;
   extern __shared__ float sm[];
   float* Ks = sm;
@@ -118,6 +118,7 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(const T* __restrict__ Q, 
   const int64_t row0 = tl.blk * kWarps, i = row0 + warp;
   const bool live = i < N;
   const size_t base = static_cast<size_t>(tl.bh) * N * D;
+  const size_t kvbase = static_cast<size_t>(tl.bh / G) * N * D;  // the key/value head this query head reads
   float q[V], o[V];
 #pragma unroll
   for (int t = 0; t < V; ++t) o[t] = 0.f;
@@ -126,8 +127,8 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(const T* __restrict__ Q, 
   const int64_t last = causal ? min(row0 + kWarps, N) - 1 : N - 1;  // last key any row of the block sees
   for (int64_t k0 = 0; k0 <= last; k0 += kTile) {
     __syncthreads();
-    stage<T, D>(Ks, K + base, k0, N);
-    stage<T, D>(Vs, Vt + base, k0, N);
+    stage<T, D>(Ks, K + kvbase, k0, N);
+    stage<T, D>(Vs, Vt + kvbase, k0, N);
     __syncthreads();
     if (!live) continue;
     const int jn = static_cast<int>(lmin(kTile, (causal ? i + 1 : N) - k0));
@@ -166,7 +167,7 @@ __global__ void __launch_bounds__(kThreads) bwd_row_kernel(const T* __restrict__
                                                            const T* __restrict__ Vt, const T* __restrict__ O,
                                                            const T* __restrict__ dO, const float* __restrict__ lse,
                                                            T* __restrict__ dQ, float4* __restrict__ ws, int64_t N,
-                                                           int64_t BH, float scale, int causal) {
+                                                           int64_t BH, float scale, int causal, int64_t G) {
   constexpr int V = D / 32;
   extern __shared__ float sm[];
   float* Ks = sm;
@@ -177,6 +178,7 @@ __global__ void __launch_bounds__(kThreads) bwd_row_kernel(const T* __restrict__
   const int64_t row0 = tl.blk * kWarps, i = row0 + warp;
   const bool live = i < N;
   const size_t base = static_cast<size_t>(tl.bh) * N * D;
+  const size_t kvbase = static_cast<size_t>(tl.bh / G) * N * D;
   float q[V], g[V], acc[V], pk[V];
   float Di = 0.f, Li = 0.f, r = 0.f, sp = 0.f;
 #pragma unroll
@@ -194,8 +196,8 @@ __global__ void __launch_bounds__(kThreads) bwd_row_kernel(const T* __restrict__
   const int64_t last = causal ? min(row0 + kWarps, N) - 1 : N - 1;  // last key any row of the block sees
   for (int64_t k0 = 0; k0 <= last; k0 += kTile) {
     __syncthreads();
-    stage<T, D>(Ks, K + base, k0, N);
-    stage<T, D>(Vs, Vt + base, k0, N);
+    stage<T, D>(Ks, K + kvbase, k0, N);
+    stage<T, D>(Vs, Vt + kvbase, k0, N);
     __syncthreads();
     if (!live) continue;
     const int jn = static_cast<int>(lmin(kTile, (causal ? i + 1 : N) - k0));
@@ -235,15 +237,15 @@ template <typename T, int D, bool GPROJ>
 __global__ void __launch_bounds__(kThreads) bwd_col_kernel(const T* __restrict__ Q, const T* __restrict__ K,
                                                            const T* __restrict__ Vt, const T* __restrict__ dO,
                                                            const float4* __restrict__ ws, T* __restrict__ dK,
-                                                           T* __restrict__ dV, int64_t N, int64_t BH,
-                                                           float scale, int causal) {
+                                                           T* __restrict__ dV, int64_t N, int64_t BHkv,
+                                                           float scale, int causal, int64_t G) {
   constexpr int V = D / 32;
   extern __shared__ float sm[];
   float* Qs = sm;
   float* Gs = sm + kTile * D;
   float4* Ss = reinterpret_cast<float4*>(sm + 2 * kTile * D);
   const int64_t nblk = (N + kWarps - 1) / kWarps;
-  const Tile tl = decode(BH, nblk, false);  // smallest key index = most rows: first
+  const Tile tl = decode(BHkv, nblk, false);  // tl.bh: a key/value head; smallest key index = most rows: first
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int64_t col0 = tl.blk * kWarps, j = col0 + warp;
   const bool live = j < N;
@@ -255,12 +257,15 @@ __global__ void __launch_bounds__(kThreads) bwd_col_kernel(const T* __restrict__
     load_vec(K + base + j * D, lane, kv);
     load_vec(Vt + base + j * D, lane, vv);
   }
+  // dK and dV of a shared head sum over the G query heads that read it.
+  for (int64_t hq = tl.bh * G; hq < (tl.bh + 1) * G; ++hq)
   for (int64_t i0 = causal ? col0 : 0; i0 < N; i0 += kTile) {
+    const size_t qbase = static_cast<size_t>(hq) * N * D;
     __syncthreads();
-    stage<T, D>(Qs, Q + base, i0, N);
-    stage<T, D>(Gs, dO + base, i0, N);
+    stage<T, D>(Qs, Q + qbase, i0, N);
+    stage<T, D>(Gs, dO + qbase, i0, N);
     if (threadIdx.x < kTile)
-      Ss[threadIdx.x] = (i0 + threadIdx.x < N) ? ws[tl.bh * N + i0 + threadIdx.x] : make_float4(0, 0, 0, 0);
+      Ss[threadIdx.x] = (i0 + threadIdx.x < N) ? ws[hq * N + i0 + threadIdx.x] : make_float4(0, 0, 0, 0);
     __syncthreads();
     if (!live) continue;
     const int ib = causal ? static_cast<int>(lmax(0, j - i0)) : 0;  // causal: rows i >= j only
@@ -306,7 +311,7 @@ __global__ void __launch_bounds__(kThreads) bob_row_kernel(
     const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ Vt, const T* __restrict__ O,
     const T* __restrict__ dO, const float* __restrict__ lse, const T* __restrict__ A, const T* __restrict__ Bm,
     const T* __restrict__ C, T* __restrict__ gQ, T* __restrict__ gdO, float4* __restrict__ ws, int64_t N,
-    int64_t BH, float scale, int causal) {
+    int64_t BH, float scale, int causal, int64_t G) {
   constexpr int V = D / 32;
   extern __shared__ float sm[];
   float* Ks = sm;
@@ -319,6 +324,7 @@ __global__ void __launch_bounds__(kThreads) bob_row_kernel(
   const int64_t row0 = tl.blk * kWarps, i = row0 + warp;
   const bool live = i < N;
   const size_t base = static_cast<size_t>(tl.bh) * N * D;
+  const size_t kvbase = static_cast<size_t>(tl.bh / G) * N * D;  // K, V, b, c of the shared head
   float q[V], g[V], av[V], o[V], X[V], Y[V], Z[V], U[V];
   float Di = 0.f, Li = 0.f, E = 0.f, Fp = 0.f;
 #pragma unroll
@@ -336,10 +342,10 @@ __global__ void __launch_bounds__(kThreads) bob_row_kernel(
   const int64_t last = causal ? min(row0 + kWarps, N) - 1 : N - 1;  // last key any row of the block sees
   for (int64_t k0 = 0; k0 <= last; k0 += kTile) {
     __syncthreads();
-    stage<T, D>(Ks, K + base, k0, N);
-    stage<T, D>(Vs, Vt + base, k0, N);
-    stage<T, D>(Bs, Bm + base, k0, N);
-    stage<T, D>(Cs, C + base, k0, N);
+    stage<T, D>(Ks, K + kvbase, k0, N);
+    stage<T, D>(Vs, Vt + kvbase, k0, N);
+    stage<T, D>(Bs, Bm + kvbase, k0, N);
+    stage<T, D>(Cs, C + kvbase, k0, N);
     __syncthreads();
     if (!live) continue;
     const int jn = static_cast<int>(lmin(kTile, (causal ? i + 1 : N) - k0));
@@ -386,7 +392,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) bob_col_kernel(
     const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ Vt, const T* __restrict__ dO,
     const T* __restrict__ A, const T* __restrict__ Bm, const T* __restrict__ C, const float4* __restrict__ ws,
-    T* __restrict__ gK, T* __restrict__ gV, int64_t N, int64_t BH, float scale, int causal) {
+    T* __restrict__ gK, T* __restrict__ gV, int64_t N, int64_t BHkv, float scale, int causal, int64_t G) {
   constexpr int V = D / 32;
   extern __shared__ float sm[];
   float* Qs = sm;
@@ -394,7 +400,7 @@ __global__ void __launch_bounds__(kThreads) bob_col_kernel(
   float* As = sm + 2 * kTile * D;
   float4* Ss = reinterpret_cast<float4*>(sm + 3 * kTile * D);
   const int64_t nblk = (N + kWarps - 1) / kWarps;
-  const Tile tl = decode(BH, nblk, false);
+  const Tile tl = decode(BHkv, nblk, false);  // tl.bh: a key/value head
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int64_t col0 = tl.blk * kWarps, j = col0 + warp;
   const bool live = j < N;
@@ -408,13 +414,16 @@ __global__ void __launch_bounds__(kThreads) bob_col_kernel(
     load_vec(Bm + base + j * D, lane, bv);
     load_vec(C + base + j * D, lane, cv);
   }
+  // gK and gV of a shared head sum over the G query heads that read it.
+  for (int64_t hq = tl.bh * G; hq < (tl.bh + 1) * G; ++hq)
   for (int64_t i0 = causal ? col0 : 0; i0 < N; i0 += kTile) {
+    const size_t qbase = static_cast<size_t>(hq) * N * D;
     __syncthreads();
-    stage<T, D>(Qs, Q + base, i0, N);
-    stage<T, D>(Gs, dO + base, i0, N);
-    stage<T, D>(As, A + base, i0, N);
+    stage<T, D>(Qs, Q + qbase, i0, N);
+    stage<T, D>(Gs, dO + qbase, i0, N);
+    stage<T, D>(As, A + qbase, i0, N);
     if (threadIdx.x < kTile)
-      Ss[threadIdx.x] = (i0 + threadIdx.x < N) ? ws[tl.bh * N + i0 + threadIdx.x] : make_float4(0, 0, 0, 0);
+      Ss[threadIdx.x] = (i0 + threadIdx.x < N) ? ws[hq * N + i0 + threadIdx.x] : make_float4(0, 0, 0, 0);
     __syncthreads();
     if (!live) continue;
     const int ib = causal ? static_cast<int>(lmax(0, j - i0)) : 0;
@@ -458,7 +467,7 @@ __global__ void __launch_bounds__(kThreads) projected_dS_kernel(const T* __restr
                                                                 const T* __restrict__ dO,
                                                                 const float* __restrict__ lse,
                                                                 float* __restrict__ out, int64_t N, int64_t BH,
-                                                                float scale, int causal) {
+                                                                float scale, int causal, int64_t G) {
   constexpr int V = D / 32;
   const int64_t nblk = (N + kWarps - 1) / kWarps;
   const Tile tl = decode(BH, nblk, true);
@@ -466,6 +475,7 @@ __global__ void __launch_bounds__(kThreads) projected_dS_kernel(const T* __restr
   const int64_t i = tl.blk * kWarps + warp;
   if (i >= N) return;
   const size_t base = static_cast<size_t>(tl.bh) * N * D;
+  const size_t kvbase = static_cast<size_t>(tl.bh / G) * N * D;
   float q[V], g[V], o[V];
   load_vec(Q + base + i * D, lane, q);
   load_vec(dO + base + i * D, lane, g);
@@ -483,8 +493,8 @@ __global__ void __launch_bounds__(kThreads) projected_dS_kernel(const T* __restr
         continue;
       }
       float kv[V], vv[V];
-      load_vec(K + base + j * D, lane, kv);
-      load_vec(Vt + base + j * D, lane, vv);
+      load_vec(K + kvbase + j * D, lane, kv);
+      load_vec(Vt + kvbase + j * D, lane, vv);
       float x[2] = {dot(q, kv), dot(g, vv)};
       warp_sum(x);
       const float p = expf(x[0] * scale - Li);
@@ -508,6 +518,10 @@ cudaError_t allow_smem(Kern k, size_t bytes) {
 inline unsigned grid_for(const Problem& p) {
   return static_cast<unsigned>(((p.N + kWarps - 1) / kWarps) * p.BH);
 }
+// Column passes: one CTA per block of keys of one key/value head.
+inline unsigned grid_for_cols(const Problem& p) {
+  return static_cast<unsigned>(((p.N + kWarps - 1) / kWarps) * p.BHkv);
+}
 
 template <typename T, int D>
 cudaError_t fwd_t(const Problem& p, const void* Q, const void* K, const void* V, void* O, float* lse,
@@ -517,7 +531,7 @@ cudaError_t fwd_t(const Problem& p, const void* Q, const void* K, const void* V,
   cudaError_t e = allow_smem(k, sm);
   if (e != cudaSuccess) return e;
   k<<<grid_for(p), kThreads, sm, st>>>(static_cast<const T*>(Q), static_cast<const T*>(K),
-                                        static_cast<const T*>(V), static_cast<T*>(O), lse, p.N, p.BH, p.scale, p.causal);
+                                        static_cast<const T*>(V), static_cast<T*>(O), lse, p.N, p.BH, p.scale, p.causal, p.group);
   return cudaGetLastError();
 }
 
@@ -535,14 +549,15 @@ cudaError_t bwd_t(const Problem& p, const void* Q, const void* K, const void* V,
     kr<<<grid_for(p), kThreads, sm_row, st>>>(static_cast<const T*>(Q), static_cast<const T*>(K),
                                                static_cast<const T*>(V), static_cast<const T*>(O),
                                                static_cast<const T*>(dO), lse, static_cast<T*>(dQ), ws, p.N, p.BH,
-                                               p.scale, p.causal);
+                                               p.scale, p.causal, p.group);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   if (!(passes & 2)) return cudaSuccess;
-  kc<<<grid_for(p), kThreads, sm_col, st>>>(static_cast<const T*>(Q), static_cast<const T*>(K),
-                                             static_cast<const T*>(V), static_cast<const T*>(dO), ws,
-                                             static_cast<T*>(dK), static_cast<T*>(dV), p.N, p.BH, p.scale, p.causal);
+  kc<<<grid_for_cols(p), kThreads, sm_col, st>>>(static_cast<const T*>(Q), static_cast<const T*>(K),
+                                                  static_cast<const T*>(V), static_cast<const T*>(dO), ws,
+                                                  static_cast<T*>(dK), static_cast<T*>(dV), p.N, p.BHkv, p.scale,
+                                                  p.causal, p.group);
   return cudaGetLastError();
 }
 
@@ -562,15 +577,15 @@ cudaError_t bob_t(const Problem& p, const void* Q, const void* K, const void* V,
     kr<<<grid_for(p), kThreads, sm_row, st>>>(
         static_cast<CT>(Q), static_cast<CT>(K), static_cast<CT>(V), static_cast<CT>(O), static_cast<CT>(dO), lse,
         static_cast<CT>(a), static_cast<CT>(b), static_cast<CT>(c), static_cast<T*>(gQ), static_cast<T*>(gdO), ws,
-        p.N, p.BH, p.scale, p.causal);
+        p.N, p.BH, p.scale, p.causal, p.group);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   if (!(passes & 2)) return cudaSuccess;
-  kc<<<grid_for(p), kThreads, sm_col, st>>>(static_cast<CT>(Q), static_cast<CT>(K), static_cast<CT>(V),
-                                             static_cast<CT>(dO), static_cast<CT>(a), static_cast<CT>(b),
-                                             static_cast<CT>(c), ws, static_cast<T*>(gK), static_cast<T*>(gV),
-                                             p.N, p.BH, p.scale, p.causal);
+  kc<<<grid_for_cols(p), kThreads, sm_col, st>>>(static_cast<CT>(Q), static_cast<CT>(K), static_cast<CT>(V),
+                                                  static_cast<CT>(dO), static_cast<CT>(a), static_cast<CT>(b),
+                                                  static_cast<CT>(c), ws, static_cast<T*>(gK), static_cast<T*>(gV),
+                                                  p.N, p.BHkv, p.scale, p.causal, p.group);
   return cudaGetLastError();
 }
 
@@ -605,11 +620,11 @@ cudaError_t simt_projected_dS(const Problem& p, const void* Q, const void* K, co
   if (p.d == 64)
     projected_dS_kernel<T, 64><<<grid_for(p), kThreads, 0, st>>>(
         static_cast<const T*>(Q), static_cast<const T*>(K), static_cast<const T*>(V), static_cast<const T*>(O),
-        static_cast<const T*>(dO), lse, dS, p.N, p.BH, p.scale, p.causal);
+        static_cast<const T*>(dO), lse, dS, p.N, p.BH, p.scale, p.causal, p.group);
   else
     projected_dS_kernel<T, 128><<<grid_for(p), kThreads, 0, st>>>(
         static_cast<const T*>(Q), static_cast<const T*>(K), static_cast<const T*>(V), static_cast<const T*>(O),
-        static_cast<const T*>(dO), lse, dS, p.N, p.BH, p.scale, p.causal);
+        static_cast<const T*>(dO), lse, dS, p.N, p.BH, p.scale, p.causal, p.group);
   return cudaGetLastError();
 }
 

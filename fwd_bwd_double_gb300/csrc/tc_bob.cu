@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tmC, const __nv_bfloat16* __restrict__ O,
                    const __nv_bfloat16* __restrict__ dO, const float* __restrict__ lse,
                    __nv_bfloat16* __restrict__ gQ, __nv_bfloat16* __restrict__ gdO, float4* __restrict__ ws, int N,
-                   int Np, int nrb, int BH, float scale, float c, int causal) {
+                   int Np, int nrb, int BH, float scale, float c, int causal, int G) {
   using Lay = RowLay;
   constexpr int NS = Lay::NS;
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -129,6 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const tc::Order ord = tc::grid_order(BH, nrb);
   const int bh = ord.bh;
+  const int kvh = bh / G;          // the slice of K, V, b, c this query slice reads
   const int rb = nrb - 1 - ord.k;  // heaviest row blocks first (within a group of slices)
   // 64-key blocks this row block sees: up to its last row, or all of them when not causal
   const int nkv = causal ? ((rb + 1) * BM + BN - 1) / BN : (N + BN - 1) / BN;
@@ -176,10 +177,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j >= NS) wait(&empty[s], ((j / NS) - 1) & 1);
         uint8_t* st = sm + Lay::oStage + s * Lay::kStage;
         ptx::mbar_expect_tx(&full[s], 4 * kTile);
-        ptx::tma_load_3d(st + Lay::oc, &tmC, &full[s], 0, j * BN, bh);
-        ptx::tma_load_3d(st + Lay::oV, &tmV, &full[s], 0, j * BN, bh);
-        ptx::tma_load_3d(st + Lay::ob, &tmB, &full[s], 0, j * BN, bh);
-        ptx::tma_load_3d(st + Lay::oKs, &tmK, &full[s], 0, j * BN, bh);
+        ptx::tma_load_3d(st + Lay::oc, &tmC, &full[s], 0, j * BN, kvh);
+        ptx::tma_load_3d(st + Lay::oV, &tmV, &full[s], 0, j * BN, kvh);
+        ptx::tma_load_3d(st + Lay::ob, &tmB, &full[s], 0, j * BN, kvh);
+        ptx::tma_load_3d(st + Lay::oKs, &tmK, &full[s], 0, j * BN, kvh);
       }
       for (int j = (nkv > NS ? nkv - NS : 0); j < nkv; ++j) wait(&empty[j % NS], (j / NS) & 1);
     }
@@ -453,13 +454,15 @@ struct ColLay {
   static constexpr int cT = 0, cK = 128, cB = 160, cV = 192, cC = 224, cOp = 256, cgV = 352, cgK = 416;
 };
 
+// GR: grouped key/value heads (G > 1).  The G == 1 instance keeps the plain tile loop.
+template <bool GR>
 __global__ void __launch_bounds__(kThreads, 1)
     bob_col_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmdO, const __grid_constant__ CUtensorMap tmSt,
                    const __nv_bfloat16* __restrict__ Kp, const __nv_bfloat16* __restrict__ Bp,
                    const __nv_bfloat16* __restrict__ Vp, const __nv_bfloat16* __restrict__ Cp,
-                   __nv_bfloat16* __restrict__ gK, __nv_bfloat16* __restrict__ gV, int N, int BH, float scale,
-                   float c, int causal) {
+                   __nv_bfloat16* __restrict__ gK, __nv_bfloat16* __restrict__ gV, int N, int BHkv, float scale,
+                   float c, int causal, int G) {
   using Lay = ColLay;
   constexpr int NS = Lay::NS;
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -478,12 +481,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkb = (N + BM - 1) / BM;
-  const tc::Order ord = tc::grid_order(BH, nkb);
-  const int bh = ord.bh;
+  const tc::Order ord = tc::grid_order(BHkv, nkb);
+  const int kvh = ord.bh;  // key/value slice; its G query slices are kvh * G + h, h < G
   const int kb = ord.k;  // first key blocks have the most rows: first
   const int nq = (N + BN - 1) / BN;
   const int i0 = causal ? (kb * BM) / BN : 0;  // first query block that sees this key block
-  const int ntile = nq - i0;
+  const int ntile = nq - i0;                   // query blocks per query slice
+  const int nt = GR ? G * ntile : ntile;       // tiles t = h * ntile + (i - i0), one gK, gV
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -519,8 +523,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::prefetch_tmap(&tmA);
       ptx::prefetch_tmap(&tmdO);
       ptx::prefetch_tmap(&tmSt);
-      for (int t = 0; t < ntile; ++t) {
-        const int s = t % NS, i = i0 + t;
+      for (int t = 0; t < nt; ++t) {
+        const int h = GR ? t / ntile : 0, s = t % NS, i = i0 + t - h * ntile, bh = GR ? kvh * G + h : kvh;
         if (t >= NS) wait(&empty[s], ((t / NS) - 1) & 1);
         uint8_t* st = sm + Lay::oStage + s * Lay::kStage;
         ptx::mbar_expect_tx(&full[s], 3 * kTile + Lay::kStat);
@@ -529,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tma_load_3d(st + 2 * kTile, &tmdO, &full[s], 0, i * BN, bh);
         ptx::tma_load_3d(st + 3 * kTile, &tmSt, &full[s], 0, i * BN, bh);
       }
-      for (int t = (ntile > NS ? ntile - NS : 0); t < ntile; ++t) wait(&empty[t % NS], (t / NS) & 1);
+      for (int t = (nt > NS ? nt - NS : 0); t < nt; ++t) wait(&empty[t % NS], (t / NS) & 1);
     }
   } else if (warp == 9) {
     if (ok) {  // all 32 lanes; one elected lane issues each MMA and commit
@@ -543,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tT = tmem + Lay::cT, tK = tmem + Lay::cK, tB = tmem + Lay::cB;
       const uint32_t tV = tmem + Lay::cV, tC = tmem + Lay::cC;
       wait(held_ready, 0);
-      for (int t = 0; t < ntile; ++t) {
+      for (int t = 0; t < nt; ++t) {
         const int s = t % NS;
         const uint32_t so = static_cast<uint32_t>(s * Lay::kStage);
         wait(&full[s], (t / NS) & 1);
@@ -578,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dAm = tc::mnmajor_desc(sSt + kTile, BN, 0);       // a_i, MN-major
       const uint64_t ddOm = tc::mnmajor_desc(sSt + 2 * kTile, BN, 0);  // dO_i, MN-major
       const uint32_t tOp = tmem + Lay::cOp, tgV = tmem + Lay::cgV, tgK = tmem + Lay::cgK;
-      for (int t = 0; t < ntile; ++t) {
+      for (int t = 0; t < nt; ++t) {
         const int s = t % NS;
         const uint32_t so = static_cast<uint32_t>(s * Lay::kStage);
         wait(ready, t & 1);
@@ -611,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int m = 0; m < 4; ++m) {
         uint32_t w[16];
         if (key < N) {
-          const uint4* g = reinterpret_cast<const uint4*>(src[m] + (static_cast<size_t>(bh) * N + key) * D + c0);
+          const uint4* g = reinterpret_cast<const uint4*>(src[m] + (static_cast<size_t>(kvh) * N + key) * D + c0);
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const uint4 v = g[u];
@@ -632,8 +636,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const uint64_t c2 = tc::pk2f(c, c), s2 = tc::pk2f(scale, scale);
     const uint32_t tOpT = tmem + Lay::cOp + static_cast<uint32_t>(hf * 16) + lo;
-    for (int t = 0; t < ntile; ++t) {
-      const int s = t % NS, i = i0 + t;
+    for (int t = 0; t < nt; ++t) {
+      const int s = t % NS, i = GR ? i0 + t % ntile : i0 + t;
       // Row states of the 64 queries, pair-interleaved: float4 2m = (-L2, -L2', -E, -E'),
       // float4 2m+1 = (-D, -D', -F', -F'') of queries 2m, 2m+1 of the block.
       const float4* stat =
@@ -707,7 +711,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tmem_ld32(tmem + Lay::cgK + c0 + lo, bv);
     ptx::tmem_wait_ld();
     if (key < N) {
-      const size_t rowoff = (static_cast<size_t>(bh) * N + key) * D;
+      const size_t rowoff = (static_cast<size_t>(kvh) * N + key) * D;
       uint32_t ov[16], ok2[16];
 #pragma unroll
       for (int u = 0; u < 32; u += 2) {
@@ -742,9 +746,9 @@ cudaError_t tc_bob(const Problem& p, const void* Q, const void* K, const void* V
   alignas(64) CUtensorMap q64, a64, do64, s64;
   const int64_t N = p.N, BH = p.BH, Np = (p.N + 1) & ~static_cast<int64_t>(1);
   if (!make_tmap_bf16(&q128, Q, N, D, BH, BM) || !make_tmap_bf16(&do128, dO, N, D, BH, BM) ||
-      !make_tmap_bf16(&a128, a, N, D, BH, BM) || !make_tmap_bf16(&k64, K, N, D, BH, BN) ||
-      !make_tmap_bf16(&v64, V, N, D, BH, BN) || !make_tmap_bf16(&b64, b, N, D, BH, BN) ||
-      !make_tmap_bf16(&c64, cc, N, D, BH, BN) || !make_tmap_bf16(&q64, Q, N, D, BH, BN) ||
+      !make_tmap_bf16(&a128, a, N, D, BH, BM) || !make_tmap_bf16(&k64, K, N, D, p.BHkv, BN) ||
+      !make_tmap_bf16(&v64, V, N, D, p.BHkv, BN) || !make_tmap_bf16(&b64, b, N, D, p.BHkv, BN) ||
+      !make_tmap_bf16(&c64, cc, N, D, p.BHkv, BN) || !make_tmap_bf16(&q64, Q, N, D, BH, BN) ||
       !make_tmap_bf16(&a64, a, N, D, BH, BN) || !make_tmap_bf16(&do64, dO, N, D, BH, BN) ||
       !make_tmap_stats(&s64, ws, Np, BH, BN))
     return cudaErrorInvalidValue;
@@ -757,16 +761,19 @@ cudaError_t tc_bob(const Problem& p, const void* Q, const void* K, const void* V
   bob_row_kernel<<<static_cast<unsigned>(nrb * BH), kThreads, RowLay::bytes, st>>>(
       q128, do128, a128, k64, v64, b64, c64, static_cast<const __nv_bfloat16*>(O),
       static_cast<const __nv_bfloat16*>(dO), lse, static_cast<__nv_bfloat16*>(gQ), static_cast<__nv_bfloat16*>(gdO),
-      ws, static_cast<int>(N), static_cast<int>(Np), nrb, static_cast<int>(BH), p.scale, c, p.causal);
+      ws, static_cast<int>(N), static_cast<int>(Np), nrb, static_cast<int>(BH), p.scale, c, p.causal,
+      p.group);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (!(passes & 2)) return cudaSuccess;
-  e = cudaFuncSetAttribute(bob_col_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ColLay::bytes);
+  auto col = p.group > 1 ? bob_col_kernel<true> : bob_col_kernel<false>;
+  e = cudaFuncSetAttribute(col, cudaFuncAttributeMaxDynamicSharedMemorySize, ColLay::bytes);
   if (e != cudaSuccess) return e;
-  bob_col_kernel<<<static_cast<unsigned>(nrb * BH), kThreads, ColLay::bytes, st>>>(
+  col<<<static_cast<unsigned>(nrb * p.BHkv), kThreads, ColLay::bytes, st>>>(
       q64, a64, do64, s64, static_cast<const __nv_bfloat16*>(K), static_cast<const __nv_bfloat16*>(b),
       static_cast<const __nv_bfloat16*>(V), static_cast<const __nv_bfloat16*>(cc), static_cast<__nv_bfloat16*>(gK),
-      static_cast<__nv_bfloat16*>(gV), static_cast<int>(N), static_cast<int>(BH), p.scale, c, p.causal);
+      static_cast<__nv_bfloat16*>(gV), static_cast<int>(N), static_cast<int>(p.BHkv), p.scale, c, p.causal,
+      p.group);
   return cudaGetLastError();
 }
 

@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
                    const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const __nv_bfloat16* __restrict__ O, const __nv_bfloat16* __restrict__ dO,
                    const float* __restrict__ lse, __nv_bfloat16* __restrict__ dQ, float4* __restrict__ ws, int N,
-                   int Np, int nrb, int BH, float scale, float c, int causal) {
+                   int Np, int nrb, int BH, float scale, float c, int causal, int G) {
   using Lay = RowLay<D, NB, GP>;
   constexpr int NS = Lay::NS;
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -142,8 +142,8 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
         if (j >= NS) wait(&empty[s], ((j / NS) - 1) & 1);
         ptx::mbar_expect_tx(&full[s], 2 * Lay::kStream);
         for (int cc = 0; cc < D / 64; ++cc) {
-          ptx::tma_load_3d(sm + Lay::oK + s * Lay::kStream + cc * BN * 128, &tmK, &full[s], cc * 64, j * BN, bh);
-          ptx::tma_load_3d(sm + Lay::oV + s * Lay::kStream + cc * BN * 128, &tmV, &full[s], cc * 64, j * BN, bh);
+          ptx::tma_load_3d(sm + Lay::oK + s * Lay::kStream + cc * BN * 128, &tmK, &full[s], cc * 64, j * BN, bh / G);
+          ptx::tma_load_3d(sm + Lay::oV + s * Lay::kStream + cc * BN * 128, &tmV, &full[s], cc * 64, j * BN, bh / G);
         }
       }
       for (int j = (nkv > NS ? nkv - NS : 0); j < nkv; ++j) wait(&empty[j % NS], (j / NS) & 1);
@@ -323,12 +323,13 @@ struct ColLay {
   static_assert(cols <= 512, "TMEM budget");
 };
 
-template <int D, int NB, bool GP>
+// GR: grouped key/value heads (G > 1).  The G == 1 instance keeps the plain tile loop.
+template <int D, int NB, bool GP, bool GR>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_col_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                    const __grid_constant__ CUtensorMap tmSt, __nv_bfloat16* __restrict__ dK,
-                   __nv_bfloat16* __restrict__ dV, int N, int BH, float scale, float c, int causal) {
+                   __nv_bfloat16* __restrict__ dV, int N, int BHkv, float scale, float c, int causal, int G) {
   using Lay = ColLay<D, NB, GP>;
   constexpr int NS = Lay::NS;
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -343,12 +344,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkb = (N + BM - 1) / BM;
-  const tc::Order ord = tc::grid_order(BH, nkb);
-  const int bh = ord.bh;
+  const tc::Order ord = tc::grid_order(BHkv, nkb);
+  const int kvh = ord.bh;  // key/value slice; its G query slices are kvh * G + h, h < G
   const int kb = ord.k;  // first key blocks have the most rows: first
   const int nq = (N + BN - 1) / BN;
   const int i0 = causal ? (kb * BM) / BN : 0;         // first query block with a query >= first key
-  const int ntile = nq - i0;
+  const int ntile = nq - i0;                          // query blocks per query slice
+  const int nt = GR ? G * ntile : ntile;              // tiles t = h * ntile + (i - i0), one dK, dV
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(k_full, 1);
@@ -383,11 +385,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::prefetch_tmap(&tmSt);
       ptx::mbar_expect_tx(k_full, 2 * Lay::kHeld);
       for (int cc = 0; cc < D / 64; ++cc) {
-        ptx::tma_load_3d(sm + Lay::oK + cc * BM * 128, &tmK, k_full, cc * 64, kb * BM, bh);
-        ptx::tma_load_3d(sm + Lay::oV + cc * BM * 128, &tmV, k_full, cc * 64, kb * BM, bh);
+        ptx::tma_load_3d(sm + Lay::oK + cc * BM * 128, &tmK, k_full, cc * 64, kb * BM, kvh);
+        ptx::tma_load_3d(sm + Lay::oV + cc * BM * 128, &tmV, k_full, cc * 64, kb * BM, kvh);
       }
-      for (int t = 0; t < ntile; ++t) {
-        const int s = t % NS, i = i0 + t;
+      for (int t = 0; t < nt; ++t) {
+        const int h = GR ? t / ntile : 0, s = t % NS, i = i0 + t - h * ntile, bh = GR ? kvh * G + h : kvh;
         if (t >= NS) wait(&empty[s], ((t / NS) - 1) & 1);
         ptx::mbar_expect_tx(&full[s], 2 * Lay::kStream + Lay::kStat);
         for (int cc = 0; cc < D / 64; ++cc) {
@@ -396,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::tma_load_3d(sm + Lay::oSt + s * Lay::kStat, &tmSt, &full[s], 0, i * BN, bh);
       }
-      for (int t = (ntile > NS ? ntile - NS : 0); t < ntile; ++t) wait(&empty[t % NS], (t / NS) & 1);
+      for (int t = (nt > NS ? nt - NS : 0); t < nt; ++t) wait(&empty[t % NS], (t / NS) & 1);
     }
   } else if (warp == 9) {
     if (ok) {  // all 32 lanes; one elected lane issues each MMA and commit
@@ -420,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mma_commit_e(&empty[s]);
       };
       wait(k_full, 0);
-      for (int t = 0; t < ntile; ++t) {
+      for (int t = 0; t < nt; ++t) {
         const int s = t % NS, b = t % NB;
         wait(&full[s], (t / NS) & 1);
         if (t >= NB) products(t - NB);
@@ -435,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       kk > 0);
         ptx::mma_commit_e(&s_full[b]);
       }
-      for (int t = (ntile > NB ? ntile - NB : 0); t < ntile; ++t) products(t);
+      for (int t = (nt > NB ? nt - NB : 0); t < nt; ++t) products(t);
       ptx::mma_commit_e(acc_full);
     }
   } else {
@@ -445,8 +447,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int key = kb * BM + r;
     const int c0 = hf * (BN / 2);
     const uint64_t c2 = tc::pk2f(c, c);
-    for (int t = 0; t < ntile; ++t) {
-      const int s = t % NS, b = t % NB, i = i0 + t;
+    for (int t = 0; t < nt; ++t) {
+      const int s = t % NS, b = t % NB, i = GR ? i0 + t % ntile : i0 + t;
       wait(&s_full[b], (t / NB) & 1);
       ptx::tc_fence_after();
       uint32_t sv[32], pv[32];
@@ -494,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     wait(acc_full, 0);
     ptx::tc_fence_after();
     const bool live = key < N;
-    const size_t rowoff = (static_cast<size_t>(bh) * N + key) * D;
+    const size_t rowoff = (static_cast<size_t>(kvh) * N + key) * D;
 #pragma unroll
     for (int cc = 0; cc < D / 2; cc += 32) {
       uint32_t a[32], g[32];
@@ -533,8 +535,8 @@ cudaError_t launch(const Problem& p, const void* Q, const void* K, const void* V
   alignas(64) CUtensorMap q128, do128, k64, v64, k128, v128, q64, do64, s64;
   const int64_t N = p.N, BH = p.BH, Np = (p.N + 1) & ~static_cast<int64_t>(1);
   if (!make_tmap_bf16(&q128, Q, N, D, BH, BM) || !make_tmap_bf16(&do128, dO, N, D, BH, BM) ||
-      !make_tmap_bf16(&k64, K, N, D, BH, BN) || !make_tmap_bf16(&v64, V, N, D, BH, BN) ||
-      !make_tmap_bf16(&k128, K, N, D, BH, BM) || !make_tmap_bf16(&v128, V, N, D, BH, BM) ||
+      !make_tmap_bf16(&k64, K, N, D, p.BHkv, BN) || !make_tmap_bf16(&v64, V, N, D, p.BHkv, BN) ||
+      !make_tmap_bf16(&k128, K, N, D, p.BHkv, BM) || !make_tmap_bf16(&v128, V, N, D, p.BHkv, BM) ||
       !make_tmap_bf16(&q64, Q, N, D, BH, BN) || !make_tmap_bf16(&do64, dO, N, D, BH, BN) ||
       !make_tmap_stats(&s64, ws, Np, BH, BN))
     return cudaErrorInvalidValue;
@@ -548,17 +550,17 @@ cudaError_t launch(const Problem& p, const void* Q, const void* K, const void* V
     kern<<<static_cast<unsigned>(nrb * BH), kThreads, Lay::bytes, st>>>(
         q128, do128, k64, v64, static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), lse,
         static_cast<__nv_bfloat16*>(dQ), ws, static_cast<int>(N), static_cast<int>(Np), nrb, static_cast<int>(BH),
-        p.scale, c, p.causal);
+        p.scale, c, p.causal, p.group);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (passes & 2) {
     using Lay = ColLay<D, NBC, GP>;
-    auto kern = bwd_col_kernel<D, NBC, GP>;
+    auto kern = p.group > 1 ? bwd_col_kernel<D, NBC, GP, true> : bwd_col_kernel<D, NBC, GP, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::bytes);
     if (e != cudaSuccess) return e;
-    kern<<<static_cast<unsigned>(nrb * BH), kThreads, Lay::bytes, st>>>(
+    kern<<<static_cast<unsigned>(nrb * p.BHkv), kThreads, Lay::bytes, st>>>(
         k128, v128, q64, do64, s64, static_cast<__nv_bfloat16*>(dK), static_cast<__nv_bfloat16*>(dV),
-        static_cast<int>(N), static_cast<int>(BH), p.scale, c, p.causal);
+        static_cast<int>(N), static_cast<int>(p.BHkv), p.scale, c, p.causal, p.group);
     return cudaGetLastError();
   }
   return cudaSuccess;

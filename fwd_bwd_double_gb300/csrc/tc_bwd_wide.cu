@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                const __nv_bfloat16* __restrict__ O, const __nv_bfloat16* __restrict__ dO,
                const float* __restrict__ lse, __nv_bfloat16* __restrict__ dQ, float4* __restrict__ ws, int N, int Np,
-               int nrb, int BH, float scale, float c, int causal) {
+               int nrb, int BH, float scale, float c, int causal, int G) {
   using Lay = RowLay;
   extern __shared__ __align__(1024) uint8_t sm[];
   Sync sy(sm + Lay::oBar);
@@ -132,8 +132,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = j % NS;
         if (j >= NS) wait(&sy.empty[s], ((j / NS) - 1) & 1);
         ptx::mbar_expect_tx(&sy.full[s], 2 * kTile);
-        ptx::tma_load_3d(sm + Lay::oK + s * kTile, &tmK, &sy.full[s], 0, j * BW, bh);
-        ptx::tma_load_3d(sm + Lay::oV + s * kTile, &tmV, &sy.full[s], 0, j * BW, bh);
+        ptx::tma_load_3d(sm + Lay::oK + s * kTile, &tmK, &sy.full[s], 0, j * BW, bh / G);
+        ptx::tma_load_3d(sm + Lay::oV + s * kTile, &tmV, &sy.full[s], 0, j * BW, bh / G);
       }
       for (int j = (nkv > NS ? nkv - NS : 0); j < nkv; ++j) wait(&sy.empty[j % NS], (j / NS) & 1);
     }
@@ -288,20 +288,23 @@ struct ColLay {
   static constexpr int cS = 0, cdP = 128, cP = 256, cdS = 320, cdV = 384, cdK = 448;
 };
 
+// GR: grouped key/value heads (G > 1).  The G == 1 instance keeps the plain tile loop.
+template <bool GR>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_col_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                const __grid_constant__ CUtensorMap tmSt, __nv_bfloat16* __restrict__ dK,
-               __nv_bfloat16* __restrict__ dV, int N, int nb, int BH, float scale, float c, int causal) {
+               __nv_bfloat16* __restrict__ dV, int N, int nb, int BHkv, float scale, float c, int causal, int G) {
   using Lay = ColLay;
   extern __shared__ __align__(1024) uint8_t sm[];
   Sync sy(sm + Lay::oBar);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const tc::Order ord = tc::grid_order(BH, nb);
-  const int bh = ord.bh;
+  const tc::Order ord = tc::grid_order(BHkv, nb);
+  const int kvh = ord.bh;        // key/value slice; its G query slices are kvh * G + h, h < G
   const int kb = ord.k;          // first key blocks have the most query blocks: first
   const int i0 = causal ? kb : 0;  // first query block that sees this key block
-  const int ntile = nb - i0;
+  const int ntile = nb - i0;     // query blocks per query slice
+  const int nt = GR ? G * ntile : ntile;  // tiles t = h * ntile + (i - i0), summed into one dK, dV
 
   if (threadIdx.x == 0) sy.init(sm);
   if (warp == kCW + 1) {
@@ -321,10 +324,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::prefetch_tmap(&tmdO);
       ptx::prefetch_tmap(&tmSt);
       ptx::mbar_expect_tx(sy.held_full, 2 * kTile);
-      ptx::tma_load_3d(sm + Lay::oK, &tmK, sy.held_full, 0, kb * BW, bh);
-      ptx::tma_load_3d(sm + Lay::oV, &tmV, sy.held_full, 0, kb * BW, bh);
-      for (int t = 0; t < ntile; ++t) {
-        const int s = t % NS, i = i0 + t;
+      ptx::tma_load_3d(sm + Lay::oK, &tmK, sy.held_full, 0, kb * BW, kvh);
+      ptx::tma_load_3d(sm + Lay::oV, &tmV, sy.held_full, 0, kb * BW, kvh);
+      for (int t = 0; t < nt; ++t) {
+        const int h = GR ? t / ntile : 0, s = t % NS, i = i0 + t - h * ntile, bh = GR ? kvh * G + h : kvh;
         if (t >= NS) wait(&sy.empty[s], ((t / NS) - 1) & 1);
         uint8_t* st = sm + Lay::oStage + s * Lay::kStage;
         ptx::mbar_expect_tx(&sy.full[s], 2 * kTile + Lay::kStat);
@@ -332,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tma_load_3d(st + kTile, &tmdO, &sy.full[s], 0, i * BW, bh);
         ptx::tma_load_3d(st + 2 * kTile, &tmSt, &sy.full[s], 0, i * BW, bh);
       }
-      for (int t = (ntile > NS ? ntile - NS : 0); t < ntile; ++t) wait(&sy.empty[t % NS], (t / NS) & 1);
+      for (int t = (nt > NS ? nt - NS : 0); t < nt; ++t) wait(&sy.empty[t % NS], (t / NS) & 1);
     }
   } else if (warp == kCW + 1) {
     if (ok) {  // all 32 lanes; one elected lane issues each MMA and commit
@@ -344,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dQk = tc::kmajor_desc(sSt, BW, 0), ddOk = tc::kmajor_desc(sSt + kTile, BW, 0);
       const uint32_t tS = tmem + Lay::cS, tdP = tmem + Lay::cdP;
       wait(sy.held_full, 0);
-      for (int t = 0; t < ntile; ++t) {
+      for (int t = 0; t < nt; ++t) {
         const int s = t % NS;
         const uint32_t so = static_cast<uint32_t>(s * Lay::kStage);
         wait(&sy.full[s], (t / NS) & 1);
@@ -368,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sSt = ptx::smem_u32(sm + Lay::oStage);
       const uint64_t dQm = tc::mnmajor_desc(sSt, BW, 0), ddOm = tc::mnmajor_desc(sSt + kTile, BW, 0);
       const uint32_t tP = tmem + Lay::cP, tdS = tmem + Lay::cdS, tdV = tmem + Lay::cdV, tdK = tmem + Lay::cdK;
-      for (int t = 0; t < ntile; ++t) {  // dV += P^T dO_i, dK += dS^T Q_i
+      for (int t = 0; t < nt; ++t) {  // dV += P^T dO_i, dK += dS^T Q_i
         const int s = t % NS;
         const uint32_t so = static_cast<uint32_t>(s * Lay::kStage);
         wait(sy.ready, t & 1);
@@ -396,8 +399,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the row statistics of 4 query pairs stay in registers for the whole block.
     const int g4 = lane >> 2, q4 = lane & 3;
     const uint64_t c2 = tc::pk2f(c, c);
-    for (int t = 0; t < ntile; ++t) {
-      const int s = t % NS, i = i0 + t;
+    for (int t = 0; t < nt; ++t) {
+      const int s = t % NS, i = GR ? i0 + t % ntile : i0 + t;
       wait(sy.s_full, t & 1);
       ptx::tc_fence_after();
       uint32_t sv[2][16], pv[2][16];  // [lanes +0 / +16 of the quarter][repetition k, (row, row+8) x (col, col+1)]
@@ -441,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               dk[h][2 * k + m] = ptx::pack_bf16(ds.x, ds.y);
             }
       };
-      if ((causal && t == 0) || i * BW + c0 + kC > N)  // the diagonal block, or the block reaching past N
+      if ((causal && (GR ? i == kb : t == 0)) || i * BW + c0 + kC > N)  // the diagonal block, or past N
         block(std::true_type{});
       else
         block(std::false_type{});
@@ -463,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tmem_ld16(tmem + Lay::cdK + cg * DG + lo, g);
     ptx::tmem_wait_ld();
     if (key < N) {
-      const size_t rowoff = (static_cast<size_t>(bh) * N + key) * D;
+      const size_t rowoff = (static_cast<size_t>(kvh) * N + key) * D;
       uint32_t ov[DG / 2], okk[DG / 2];
 #pragma unroll
       for (int u = 0; u < DG; u += 2) {
@@ -496,7 +499,7 @@ cudaError_t tc_bwd_wide(const Problem& p, const void* Q, const void* K, const vo
   alignas(64) CUtensorMap q, g, k, v, s;
   const int64_t N = p.N, BH = p.BH, Np = (p.N + 1) & ~static_cast<int64_t>(1);
   if (!make_tmap_bf16(&q, Q, N, D, BH, BW) || !make_tmap_bf16(&g, dO, N, D, BH, BW) ||
-      !make_tmap_bf16(&k, K, N, D, BH, BW) || !make_tmap_bf16(&v, V, N, D, BH, BW) ||
+      !make_tmap_bf16(&k, K, N, D, p.BHkv, BW) || !make_tmap_bf16(&v, V, N, D, p.BHkv, BW) ||
       !make_tmap_stats(&s, ws, Np, BH, BW))
     return cudaErrorInvalidValue;
   const float c = p.scale * kLog2e;
@@ -508,15 +511,16 @@ cudaError_t tc_bwd_wide(const Problem& p, const void* Q, const void* K, const vo
     bwd_row_wide_kernel<<<static_cast<unsigned>(nb * BH), kThreads, RowLay::bytes, st>>>(
         q, g, k, v, static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), lse,
         static_cast<__nv_bfloat16*>(dQ), ws, static_cast<int>(N), static_cast<int>(Np), nb, static_cast<int>(BH),
-        p.scale, c, p.causal);
+        p.scale, c, p.causal, p.group);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (passes & 2) {
-    e = cudaFuncSetAttribute(bwd_col_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ColLay::bytes);
+    auto kern = p.group > 1 ? bwd_col_wide_kernel<true> : bwd_col_wide_kernel<false>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ColLay::bytes);
     if (e != cudaSuccess) return e;
-    bwd_col_wide_kernel<<<static_cast<unsigned>(nb * BH), kThreads, ColLay::bytes, st>>>(
+    kern<<<static_cast<unsigned>(nb * p.BHkv), kThreads, ColLay::bytes, st>>>(
         k, v, q, g, s, static_cast<__nv_bfloat16*>(dK), static_cast<__nv_bfloat16*>(dV), static_cast<int>(N), nb,
-        static_cast<int>(BH), p.scale, c, p.causal);
+        static_cast<int>(p.BHkv), p.scale, c, p.causal, p.group);
     e = cudaGetLastError();
   }
   return e;

@@ -68,7 +68,7 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O, float* __restrict__ lse,
-               int N, int nrb, int BH, float scale, float scale_log2, int causal) {
+               int N, int nrb, int BH, float scale, float scale_log2, int causal, int G) {
   using Lay = Layout<D>;
   extern __shared__ __align__(1024) uint8_t sm[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Lay::oBar);
@@ -86,6 +86,7 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const tc::Order ord = tc::grid_order(BH, nrb);
   const int bh = ord.bh;
+  const int kvh = bh / G;          // the key/value slice this query slice reads
   const int rb = nrb - 1 - ord.k;  // heaviest row blocks first (within a group of slices)
   const int nkv = causal ? rb + 1 : nrb;  // key blocks this row block sees
 
@@ -132,8 +133,8 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
         if (j >= NS) wait(&empty[s], ((j / NS) - 1) & 1);
         ptx::mbar_expect_tx(&full[s], 2 * Lay::kKV);
         for (int c = 0; c < D / 64; ++c) {
-          ptx::tma_load_3d(sm + Lay::oK + s * Lay::kKV + c * BN * 128, &tmK, &full[s], c * 64, j * BN, bh);
-          ptx::tma_load_3d(sm + Lay::oV + s * Lay::kKV + c * BN * 128, &tmV, &full[s], c * 64, j * BN, bh);
+          ptx::tma_load_3d(sm + Lay::oK + s * Lay::kKV + c * BN * 128, &tmK, &full[s], c * 64, j * BN, kvh);
+          ptx::tma_load_3d(sm + Lay::oV + s * Lay::kKV + c * BN * 128, &tmV, &full[s], c * 64, j * BN, kvh);
         }
       }
       // Drain: the last NS stages must have been consumed before the CTA exits.
@@ -291,8 +292,8 @@ template <int D>
 cudaError_t launch(const Problem& p, const void* Q, const void* K, const void* V, void* O, float* lse,
                    cudaStream_t st) {
   alignas(64) CUtensorMap mq, mk, mv;
-  if (!make_tmap_bf16(&mq, Q, p.N, D, p.BH, BM) || !make_tmap_bf16(&mk, K, p.N, D, p.BH, BN) ||
-      !make_tmap_bf16(&mv, V, p.N, D, p.BH, BN))
+  if (!make_tmap_bf16(&mq, Q, p.N, D, p.BH, BM) || !make_tmap_bf16(&mk, K, p.N, D, p.BHkv, BN) ||
+      !make_tmap_bf16(&mv, V, p.N, D, p.BHkv, BN))
     return cudaErrorInvalidValue;
   const int nrb = static_cast<int>((p.N + BM - 1) / BM);
   const size_t smem = Layout<D>::bytes;
@@ -302,7 +303,7 @@ cudaError_t launch(const Problem& p, const void* Q, const void* K, const void* V
   const float log2e = 1.4426950408889634f;
   fwd_kernel<D><<<static_cast<unsigned>(nrb * p.BH), kThreads, smem, st>>>(
       mq, mk, mv, static_cast<__nv_bfloat16*>(O), lse, static_cast<int>(p.N), nrb, static_cast<int>(p.BH),
-      p.scale, p.scale * log2e, p.causal);
+      p.scale, p.scale * log2e, p.causal, p.group);
   return cudaGetLastError();
 }
 

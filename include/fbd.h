@@ -30,7 +30,7 @@
  *               (inputs and outputs alike): ATTN_F32 = float, ATTN_BF16 =
  *               bfloat16.  Arithmetic is float32 throughout (bf16 tensor-core
  *               products accumulate in float32).
- *   Supported:  causal in {0, 1}; d in {64, 128}; dtype in {ATTN_F32, ATTN_BF16};
+ *   Supported:  causal in {0, 1}; any group dividing H; d in {64, 128}; dtype in {ATTN_F32, ATTN_BF16};
  *               for attn_bob with ATTN_BF16, d == 64.  Anything else returns
  *               ATTN_ERR_UNSUPPORTED before any launch; there is no fallback.
  *   Scale:      desc->scale == 0 means 1/sqrt(d); otherwise it must be finite and
@@ -48,6 +48,15 @@
  *               synchronised.  Each output element is written exactly once.
  *   Ragged N:   any N >= 1 is accepted; tiles past N are zero-filled on load and
  *               never stored.
+ *   Grouped key/value heads ([BoB] "When FlashBoB changes the engineering plan"
+ *               lists shared keys and values among the next extensions; the reading
+ *               here is the usual grouped-query one): with g = desc->group > 1 the tensors on the key
+ *               side -- K, V and, for the backward and BoB, dK, dV, gdK, gdV, gK,
+ *               gV -- are [B, H/g, N, d]; every other tensor keeps H heads.  The
+ *               result equals plain attention with each key/value head repeated
+ *               for its g query heads, and the gradients of a shared head (dK, dV,
+ *               gK, gV) are sums over its g query heads; gdK and gdV, cotangents of
+ *               those sums, enter each of the g heads unchanged.
  */
 #ifndef FBD_H
 #define FBD_H
@@ -61,7 +70,8 @@ extern "C" {
 
 typedef enum {
   ATTN_OK = 0,
-  ATTN_ERR_INVALID_ARG = 1,  /* NULL/negative/overlapping arguments, non-finite scale */
+  ATTN_ERR_INVALID_ARG = 1,  /* NULL/negative/overlapping arguments, non-finite scale,
+                                group < 0 or not dividing H */
   ATTN_ERR_UNSUPPORTED = 2,  /* causal not 0 or 1, d not supported, unknown dtype */
   ATTN_ERR_ALIGNMENT = 3,    /* a pointer is not 16-byte aligned */
   ATTN_ERR_WORKSPACE = 4,    /* workspace NULL or smaller than the *_workspace_bytes query */
@@ -79,6 +89,10 @@ typedef struct {
                           masking is where trading gets a discount"); 0: every key
                           is visible to every query (a full softmax over the row) */
   int32_t dtype;       /* attn_dtype_t */
+  int32_t group;       /* query heads per key/value head, g (0 and 1 both mean plain
+                          multi-head attention; g must divide H; g == H is multi-query).
+                          Query head h reads key/value head h / g (integer division);
+                          see "Grouped key/value heads" above. */
 } attn_desc_t;
 
 /* Forward.  [FA] "The Flash Attention algorithm", "Online softmax recurrence",

@@ -50,12 +50,13 @@ def inputs(w):
 def oracle_full(w, op, causal=True):
     """Oracle outputs [B, H, ...] for every slice of workload w (op: fwd, bwd, bob)."""
     x = inputs(w)
+    g = w.group
     if op == "fwd":
-        return oracle.forward_all(x["Q"], x["K"], x["V"], scale=w.scale, causal=causal)
+        return oracle.forward_all(x["Q"], x["K"], x["V"], scale=w.scale, causal=causal, groups=g)
     if op == "bwd":
-        return oracle.backward_all(x["Q"], x["K"], x["V"], x["dO"], scale=w.scale, causal=causal)
+        return oracle.backward_all(x["Q"], x["K"], x["V"], x["dO"], scale=w.scale, causal=causal, groups=g)
     return oracle.bob_all(x["Q"], x["K"], x["V"], x["dO"], x["gdQ"], x["gdK"], x["gdV"], scale=w.scale,
-                          causal=causal)
+                          causal=causal, groups=g)
 
 
 def run_ops(w, x_dev, ops=("fwd", "bwd", "bob"), gproj=0, causal=True):

@@ -32,8 +32,8 @@ def test_library_exports_every_declared_function():
         assert n in fbd._lib.PROTOTYPES, f"binding lacks a prototype for {n}"
 
 
-def desc(B=1, H=2, N=64, d=64, scale=0.0, causal=1, dtype=1):
-    return AttnDesc(B, H, N, d, scale, causal, dtype)
+def desc(B=1, H=2, N=64, d=64, scale=0.0, causal=1, dtype=1, group=0):
+    return AttnDesc(B, H, N, d, scale, causal, dtype, group)
 
 
 def ptrs(n, base=FAKE, stride=1 << 30):
@@ -62,6 +62,7 @@ def bob(dsc, p=None, ws_bytes=None):
     (dict(B=-1), INVALID), (dict(N=-5), INVALID), (dict(d=0), INVALID),
     (dict(scale=float("nan")), INVALID), (dict(scale=float("inf")), INVALID), (dict(scale=-1.0), INVALID),
     (dict(N=1 << 31), INVALID),
+    (dict(group=-1), INVALID), (dict(H=2, group=3), INVALID), (dict(H=6, group=4), INVALID),
 ])
 def test_rejects_bad_descriptors(kw, code):
     d = desc(**kw)
@@ -142,3 +143,24 @@ def test_pass_masks_are_validated():
     for bad in (0, 7):
         assert lib.attn_bob_passes(ctypes.byref(d), *q[:13], q[13], wsb, bad, None) == INVALID
     assert fbd.ATTN_ROW_PASS == 1 and fbd.ATTN_COL_PASS == 2
+
+
+def test_grouped_heads_size_the_key_side_tensors():
+    """With g query heads per key/value head, K and V span B * H/g * N * d elements: an
+    output starting one byte before the end of that span overlaps K, and the span of an
+    ungrouped K (four times longer here) covers the same address."""
+    nb = 1 * 1 * 64 * 64 * 2  # bytes of K for B=1, H=4, g=4, N=64, d=64, bf16
+    for group, off in ((4, nb - 16), (1, nb), (1, 3 * nb)):
+        p = ptrs(5)
+        p[3] = ctypes.c_void_p(p[1].value + off)  # O placed inside K
+        assert fwd(desc(H=4, group=group), p) == INVALID, (group, off)
+
+
+def test_binding_derives_the_group_from_the_key_heads():
+    torch = pytest.importorskip("torch")
+    q, k = torch.zeros(2, 6, 8, 64), torch.zeros(2, 3, 8, 64)
+    dsc = fbd.make_desc(q, K=k)
+    assert (dsc.H, dsc.group) == (6, 2)
+    assert fbd.make_desc(q).group == 1
+    with pytest.raises(fbd.FbdError):
+        fbd.make_desc(q, K=torch.zeros(2, 4, 8, 64))  # 4 key/value heads do not divide 6

@@ -351,3 +351,69 @@ def test_noncausal_differs_from_causal_and_passes_compose():
     fbd.attn_device_status()
     for a, b in zip(outs + gouts, list(ref_b) + list(ref_g)):
         assert torch.equal(a, b)
+
+
+# ------------------------------------------------------ grouped key/value heads
+# g query heads share one key/value head: K, V, gdK, gdV (and dK, dV, gK, gV) have
+# H / g heads.  Checked against the oracle's grouped mode, and bit for bit against
+# plain multi-head attention on repeated K, V where the arithmetic is the same.
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_gqa_tiny_f32_all_ops(causal):
+    w = W.Workload("gqa_tiny_f32_B1H4g2N256d64", 1, 4, 256, 64, "f32", group=2)
+    got = run_ops(w, to_device(inputs(w), w), causal=causal)
+    errs = check_full(w, got, ("bwd", "bob"), causal=causal)
+    print(w.name, causal, {k: f"{v:.2e}" for k, v in errs.items()})
+
+
+@pytest.mark.parametrize("group,gproj", [(3, 0), (3, 1), (12, 0)])
+def test_gqa_gpt2_layer_bf16(group, gproj):
+    """GPT-2 small layer shape with 4 key/value heads (g = 3) and multi-query (g = 12)."""
+    w = W.Workload(f"gqa_gpt2small_B2H12g{group}N1024d64", 2, 12, 1024, 64, "bf16", group=group)
+    ops = ("bwd", "bob") if gproj == 0 else ("bwd",)
+    got = run_ops(w, to_device(inputs(w), w), ops=ops, gproj=gproj)
+    errs = check_full(w, got, ops)
+    print(w.name, gproj, {k: f"{v:.2e}" for k, v in errs.items()})
+
+
+@pytest.mark.parametrize("N", [1, 17, 129, 300])
+@pytest.mark.parametrize("d,dtype", [(64, "bf16"), (128, "bf16"), (64, "f32")])
+@pytest.mark.parametrize("causal", [True, False])
+def test_gqa_edge_sizes(N, d, dtype, causal):
+    w = W.Workload(f"gqa_edge_B2H4g2N{N}d{d}_{dtype}", 2, 4, N, d, dtype, group=2)
+    ops = ("bwd", "bob") if (dtype == "f32" or d == 64) else ("bwd",)
+    got = run_ops(w, to_device(inputs(w), w), ops=ops, causal=causal)
+    check_full(w, got, ops, causal=causal)
+    if dtype == "bf16":
+        got1 = run_ops(w, to_device(inputs(w), w), ops=("bwd",), gproj=1, causal=causal)
+        check_full(w, got1, ("bwd",), causal=causal)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_gqa_row_outputs_equal_repeated_heads_bitwise(dtype):
+    """O, lse, dQ, gQ and gdO of a query head depend on its own key/value head only, and
+    the kernels do the same arithmetic whether that head is shared or repeated: the bits
+    must match.  dK, dV, gK, gV are sums over the group (checked against the oracle)."""
+    import torch
+    import fwd_bwd_double_gb300 as fbd
+    w = W.Workload(f"gqa_bits_B2H6g3N300d64_{dtype}", 2, 6, 300, 64, dtype, group=3)
+    x = to_device(inputs(w), w)
+    rep = {k: (v.repeat_interleave(3, dim=1).contiguous() if k in W.KV_TENSORS else v) for k, v in x.items()}
+    for causal in (True, False):
+        O, lse = fbd.attn_fwd(x["Q"], x["K"], x["V"], causal=causal)
+        Or, lser = fbd.attn_fwd(rep["Q"], rep["K"], rep["V"], causal=causal)
+        assert torch.equal(O, Or) and torch.equal(lse, lser)
+        dQ, dK, dV = fbd.attn_bwd(x["Q"], x["K"], x["V"], O, x["dO"], lse, causal=causal)
+        dQr, dKr, dVr = fbd.attn_bwd(rep["Q"], rep["K"], rep["V"], O, x["dO"], lse, causal=causal)
+        assert torch.equal(dQ, dQr)
+        assert dK.shape == x["K"].shape
+        g = fbd.attn_bob(x["Q"], x["K"], x["V"], O, x["dO"], lse, x["gdQ"], x["gdK"], x["gdV"], causal=causal)
+        gr = fbd.attn_bob(rep["Q"], rep["K"], rep["V"], O, x["dO"], lse, x["gdQ"], rep["gdK"], rep["gdV"],
+                          causal=causal)
+        assert torch.equal(g[0], gr[0]) and torch.equal(g[3], gr[3])
+        # The group sum of the repeated heads' key-side gradients is the same quantity.
+        tol = TOL[dtype] if dtype == "bf16" else 1e-5
+        for a, b in ((dK, dKr), (dV, dVr), (g[1], gr[1]), (g[2], gr[2])):
+            s = host(b).reshape(2, 2, 3, 300, 64).sum(axis=2)
+            assert rel_fro(host(a), s) <= tol
+    fbd.attn_device_status()

@@ -56,3 +56,17 @@ def test_workload_table():
     assert [w.N for w in W.LONG_SWEEP] == [4096, 16384, 65536, 262144]
     assert W.FULL_DAY.N % 128 == 104
     assert W.LARGE_KEY.d == 128 and abs(W.LARGE_KEY.scale - 128 ** -0.5) < 1e-15
+
+
+def test_grouped_heads_draw_key_side_tensors_per_key_value_head():
+    w = W.Workload("gqa", 2, 6, 9, 8, "bf16", group=3)
+    x = W.inputs(w)
+    for n in W.TENSORS:
+        assert x[n].shape == (2, 2 if n in W.KV_TENSORS else 6, 9, 8), n
+    plain = W.inputs(W.Workload("gqa", 2, 6, 9, 8, "bf16"))
+    for n in W.TENSORS:  # the same per-slice streams as the ungrouped workload
+        k = x[n].shape[1]
+        assert np.array_equal(x[n], plain[n][:, :k])
+    import pytest
+    with pytest.raises(ValueError):
+        W.inputs(w, heads=[0])

@@ -26,6 +26,8 @@ import numpy as np
 
 # Tensor ids for the per-slice streams (order matters only for stream keys).
 TENSORS = ("Q", "K", "V", "dO", "gdQ", "gdK", "gdV")
+# Key-side tensors: with grouped key/value heads these have H / group heads.
+KV_TENSORS = ("K", "V", "gdK", "gdV")
 _TID = {name: i for i, name in enumerate(TENSORS)}
 _TID_SHARED_MEAN = 100  # per-head shared key mean of the large-key workload
 _TID_PERM = 101         # per-slice earlier-position draw of the large-key workload
@@ -43,6 +45,11 @@ class Workload:
     kind: str = "iid"   # "iid" or "large_key"
     dO_std: float = 1.0
     seed: int = 0
+    group: int = 1      # query heads per key/value head: K, V, gdK, gdV have H / group heads
+
+    @property
+    def Hkv(self) -> int:
+        return self.H // self.group
 
     @property
     def scale(self) -> float:
@@ -119,13 +126,21 @@ def slice_inputs(w: Workload, b: int, h: int, names=TENSORS) -> dict:
 
 
 def inputs(w: Workload, names=TENSORS, heads=None, batches=None) -> dict:
-    """Full inputs [B', H', N, d] float32 for the selected batches/heads (default: all)."""
+    """Full inputs [B', H', N, d] float32 for the selected batches/heads (default: all).
+
+    With w.group > 1 the key-side tensors (KV_TENSORS) hold heads 0 .. H/group - 1 and
+    are drawn from the same per-slice streams; only full inputs are offered then."""
+    if w.group != 1 and (heads is not None or w.kind != "iid" or w.H % w.group):
+        raise ValueError("grouped key/value heads: full iid inputs only, group dividing H")
     batches = range(w.B) if batches is None else list(batches)
     heads = range(w.H) if heads is None else list(heads)
-    out = {n: np.empty((len(batches), len(heads), w.N, w.d), dtype=np.float32) for n in names}
+    def nheads(n):
+        return w.Hkv if (w.group != 1 and n in KV_TENSORS) else len(heads)
+    out = {n: np.empty((len(batches), nheads(n), w.N, w.d), dtype=np.float32) for n in names}
     for bi, b in enumerate(batches):
         for hi, h in enumerate(heads):
-            s = slice_inputs(w, b, h, names)
-            for n in names:
+            here = [n for n in names if hi < nheads(n)]
+            s = slice_inputs(w, b, h, here)
+            for n in here:
                 out[n][bi, hi] = s[n]
     return out
