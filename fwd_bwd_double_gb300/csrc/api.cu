@@ -38,7 +38,8 @@ attn_status_t check_desc(const attn_desc_t* desc, fbd::Problem& p) {
   if (desc->group < 0) return fail(ATTN_ERR_INVALID_ARG, "group must be >= 0%s");
   const int64_t g = desc->group == 0 ? 1 : desc->group;
   if (desc->H % g != 0) return fail(ATTN_ERR_INVALID_ARG, "group must divide H%s");
-  if (desc->d != 64 && desc->d != 128) return fail(ATTN_ERR_UNSUPPORTED, "head dim must be 64 or 128%s");
+  if (desc->d != 32 && desc->d != 64 && desc->d != 96 && desc->d != 128 && desc->d != 256)
+    return fail(ATTN_ERR_UNSUPPORTED, "head dim must be 32, 64, 96, 128 or 256%s");
   if (desc->dtype != ATTN_F32 && desc->dtype != ATTN_BF16) return fail(ATTN_ERR_UNSUPPORTED, "unknown dtype%s");
   if (!std::isfinite(desc->scale) || desc->scale < 0.f)
     return fail(ATTN_ERR_INVALID_ARG, "scale must be finite and >= 0 (0 selects 1/sqrt(d))%s");
@@ -101,9 +102,10 @@ bool tc_path(const fbd::Problem& p, int op) { return p.dtype == ATTN_BF16 && fbd
 }  // namespace
 
 namespace fbd {
-// bf16 kernels by operation: forward and backward for d in {64, 128};
+// bf16 tensor-core kernels by operation: forward and backward for d in {64, 128};
 // backward-over-backward for d = 64 (its row pass keeps four d-wide accumulators
-// and four score-sized tiles in the 512 TMEM columns).
+// and four score-sized tiles in the 512 TMEM columns).  Other supported head dims
+// run on the CUDA-core kernels (simt.cu).
 bool tc_supports(int op, int64_t d) {
   if (op == 2) return d == 64;
   return d == 64 || d == 128;
@@ -128,8 +130,7 @@ attn_status_t attn_fwd(const attn_desc_t* desc, const void* Q, const void* K, co
   const Span out[] = {span("O", O, tb), span("lse", lse, sb)};
   if ((s = check_ptrs(in, 3, out, 2)) != ATTN_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (p.dtype == ATTN_F32) return launch_status(fbd::simt_fwd(p, Q, K, V, O, lse, st));
-  if (!tc_path(p, 0)) return fail(ATTN_ERR_UNSUPPORTED, "no bf16 forward kernel for this head dim%s");
+  if (!tc_path(p, 0)) return launch_status(fbd::simt_fwd(p, Q, K, V, O, lse, st));
   return launch_status(fbd::tc_fwd(p, Q, K, V, O, lse, st));
 }
 
@@ -168,9 +169,8 @@ attn_status_t attn_bwd_passes(const attn_desc_t* desc, const void* Q, const void
   if ((s = check_ptrs(in, 6, out, 4)) != ATTN_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   float4* ws = static_cast<float4*>(workspace);
-  if (p.dtype == ATTN_F32)
-    return launch_status(fbd::simt_bwd(p, Q, K, V, O, dO, lse, dQ, dK, dV, 0, ws, passes, st));
-  if (!tc_path(p, 1)) return fail(ATTN_ERR_UNSUPPORTED, "no bf16 backward kernel for this head dim%s");
+  if (!tc_path(p, 1))
+    return launch_status(fbd::simt_bwd(p, Q, K, V, O, dO, lse, dQ, dK, dV, gproj, ws, passes, st));
   return launch_status(fbd::tc_bwd(p, Q, K, V, O, dO, lse, dQ, dK, dV, gproj != 0, ws, passes, st));
 }
 
@@ -188,8 +188,6 @@ attn_status_t attn_bob_passes(const attn_desc_t* desc, const void* Q, const void
   fbd::Problem p;
   attn_status_t s = check_desc(desc, p);
   if (s != ATTN_OK) return s;
-  if (p.dtype == ATTN_BF16 && !fbd::tc_supports(2, p.d))
-    return fail(ATTN_ERR_UNSUPPORTED, "bf16 backward-over-backward supports d = 64 only%s");
   if (passes < 1 || passes > 3) return fail(ATTN_ERR_INVALID_ARG, "passes must be ATTN_ROW_PASS, ATTN_COL_PASS or both%s");
   if (p.BH * p.N == 0) return ATTN_OK;
   const size_t need = attn_bob_workspace_bytes(desc);
@@ -205,7 +203,7 @@ attn_status_t attn_bob_passes(const attn_desc_t* desc, const void* Q, const void
   if ((s = check_ptrs(in, 9, out, 5)) != ATTN_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   float4* ws = static_cast<float4*>(workspace);
-  if (p.dtype == ATTN_F32)
+  if (!tc_path(p, 2))
     return launch_status(fbd::simt_bob(p, Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ, gK, gV, gdO, ws, passes, st));
   return launch_status(fbd::tc_bob(p, Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ, gK, gV, gdO, ws, passes, st));
 }

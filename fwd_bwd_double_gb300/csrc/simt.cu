@@ -1,5 +1,8 @@
-// Float32 path: forward, backward and BoB on CUDA cores in exact fp32 arithmetic,
-// plus the GProj projected-dS diagnostic export (bf16 inputs).
+// CUDA-core path: forward, backward and BoB in fp32 arithmetic, for float32
+// inputs at every supported head dim and for bf16 inputs at the head dims that
+// have no tensor-core kernel (bf16 is widened on load and rounded once on store;
+// with GProj the bf16 rounding of dS and P is emulated); plus the GProj
+// projected-dS diagnostic export (bf16 inputs).
 //
 // Work split: one warp per query row (row passes) or per key (column passes);
 // a warp's 32 lanes each hold d/32 consecutive elements of the row's vectors, so
@@ -591,41 +594,75 @@ cudaError_t bob_t(const Problem& p, const void* Q, const void* K, const void* V,
 
 }  // namespace
 
+// Head dimensions the CUDA-core kernels are built for (a warp's lanes hold d/32
+// elements each).  Returns false for any other d.
+template <typename F>
+bool with_head_dim(int64_t d, F&& f) {
+  switch (d) {
+    case 32: f(std::integral_constant<int, 32>{}); return true;
+    case 64: f(std::integral_constant<int, 64>{}); return true;
+    case 96: f(std::integral_constant<int, 96>{}); return true;
+    case 128: f(std::integral_constant<int, 128>{}); return true;
+    case 256: f(std::integral_constant<int, 256>{}); return true;
+  }
+  return false;
+}
+
+// Element type of the [B,H,N,d] tensors: float (ATTN_F32) or bf16 (ATTN_BF16).
+template <typename F>
+void with_type(int dtype, F&& f) {
+  if (dtype == ATTN_F32) f(float{});
+  else f(__nv_bfloat16{});
+}
+
 cudaError_t simt_fwd(const Problem& p, const void* Q, const void* K, const void* V, void* O, float* lse,
                      cudaStream_t st) {
-  if (p.dtype == ATTN_F32) return p.d == 64 ? fwd_t<float, 64>(p, Q, K, V, O, lse, st)
-                                            : fwd_t<float, 128>(p, Q, K, V, O, lse, st);
-  return p.d == 64 ? fwd_t<__nv_bfloat16, 64>(p, Q, K, V, O, lse, st)
-                   : fwd_t<__nv_bfloat16, 128>(p, Q, K, V, O, lse, st);
+  cudaError_t e = cudaErrorInvalidValue;
+  with_type(p.dtype, [&](auto t) {
+    with_head_dim(p.d, [&](auto dd) { e = fwd_t<decltype(t), dd()>(p, Q, K, V, O, lse, st); });
+  });
+  return e;
 }
 
 cudaError_t simt_bwd(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
                      const void* dO, const float* lse, void* dQ, void* dK, void* dV, int gproj, float4* ws,
                      int passes, cudaStream_t st) {
-  (void)gproj;  // fp32 dS is never rounded, so there is nothing to project
-  return p.d == 64 ? bwd_t<float, 64, false>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st)
-                   : bwd_t<float, 128, false>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st);
+  // float32 dS is never rounded, so GProj applies to bf16 only (its rounding is emulated).
+  const bool gp = gproj != 0 && p.dtype == ATTN_BF16;
+  cudaError_t e = cudaErrorInvalidValue;
+  with_type(p.dtype, [&](auto t) {
+    using T = decltype(t);
+    with_head_dim(p.d, [&](auto dd) {
+      e = gp ? bwd_t<T, dd(), true>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st)
+             : bwd_t<T, dd(), false>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st);
+    });
+  });
+  return e;
 }
 
 cudaError_t simt_bob(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
                      const void* dO, const float* lse, const void* a, const void* b, const void* c, void* gQ,
                      void* gK, void* gV, void* gdO, float4* ws, int passes, cudaStream_t st) {
-  return p.d == 64 ? bob_t<float, 64>(p, Q, K, V, O, dO, lse, a, b, c, gQ, gK, gV, gdO, ws, passes, st)
-                   : bob_t<float, 128>(p, Q, K, V, O, dO, lse, a, b, c, gQ, gK, gV, gdO, ws, passes, st);
+  cudaError_t e = cudaErrorInvalidValue;
+  with_type(p.dtype, [&](auto t) {
+    with_head_dim(p.d, [&](auto dd) {
+      e = bob_t<decltype(t), dd()>(p, Q, K, V, O, dO, lse, a, b, c, gQ, gK, gV, gdO, ws, passes, st);
+    });
+  });
+  return e;
 }
 
 cudaError_t simt_projected_dS(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
                               const void* dO, const float* lse, float* dS, cudaStream_t st) {
   using T = __nv_bfloat16;
-  if (p.d == 64)
-    projected_dS_kernel<T, 64><<<grid_for(p), kThreads, 0, st>>>(
+  cudaError_t e = cudaErrorInvalidValue;
+  with_head_dim(p.d, [&](auto dd) {
+    projected_dS_kernel<T, dd()><<<grid_for(p), kThreads, 0, st>>>(
         static_cast<const T*>(Q), static_cast<const T*>(K), static_cast<const T*>(V), static_cast<const T*>(O),
         static_cast<const T*>(dO), lse, dS, p.N, p.BH, p.scale, p.causal, p.group);
-  else
-    projected_dS_kernel<T, 128><<<grid_for(p), kThreads, 0, st>>>(
-        static_cast<const T*>(Q), static_cast<const T*>(K), static_cast<const T*>(V), static_cast<const T*>(O),
-        static_cast<const T*>(dO), lse, dS, p.N, p.BH, p.scale, p.causal, p.group);
-  return cudaGetLastError();
+    e = cudaGetLastError();
+  });
+  return e;
 }
 
 }  // namespace fbd

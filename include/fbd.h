@@ -30,9 +30,15 @@
  *               (inputs and outputs alike): ATTN_F32 = float, ATTN_BF16 =
  *               bfloat16.  Arithmetic is float32 throughout (bf16 tensor-core
  *               products accumulate in float32).
- *   Supported:  causal in {0, 1}; any group dividing H; d in {64, 128}; dtype in {ATTN_F32, ATTN_BF16};
- *               for attn_bob with ATTN_BF16, d == 64.  Anything else returns
- *               ATTN_ERR_UNSUPPORTED before any launch; there is no fallback.
+ *   Supported:  causal in {0, 1}; any group dividing H; d in {32, 64, 96, 128,
+ *               256}; dtype in {ATTN_F32, ATTN_BF16}.  Anything else returns
+ *               ATTN_ERR_UNSUPPORTED before any launch.
+ *   Kernels:    the shape decides, never a failure: bf16 attn_fwd / attn_bwd at
+ *               d in {64, 128} and bf16 attn_bob at d = 64 run on the tcgen05/TMA
+ *               tensor-core kernels; every other (dtype, d) runs on the CUDA-core
+ *               kernels (fp32 arithmetic; bf16 inputs widened on load, outputs
+ *               rounded once on store), which are exact to fp32 rounding but one to
+ *               two orders of magnitude slower.
  *   Scale:      desc->scale == 0 means 1/sqrt(d); otherwise it must be finite and
  *               positive (the row max is subtracted before scaling).
  *   Pointers:   device pointers, 16-byte aligned (ATTN_ERR_ALIGNMENT otherwise),

@@ -58,7 +58,7 @@ def bob(dsc, p=None, ws_bytes=None):
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(causal=2), UNSUP), (dict(causal=-1), UNSUP), (dict(d=32), UNSUP), (dict(d=256), UNSUP), (dict(dtype=7), UNSUP),
+    (dict(causal=2), UNSUP), (dict(causal=-1), UNSUP), (dict(d=16), UNSUP), (dict(d=48), UNSUP), (dict(d=512), UNSUP), (dict(dtype=7), UNSUP),
     (dict(B=-1), INVALID), (dict(N=-5), INVALID), (dict(d=0), INVALID),
     (dict(scale=float("nan")), INVALID), (dict(scale=float("inf")), INVALID), (dict(scale=-1.0), INVALID),
     (dict(N=1 << 31), INVALID),
@@ -72,12 +72,16 @@ def test_rejects_bad_descriptors(kw, code):
     assert lib.attn_last_error()  # a detail message is recorded
 
 
-def test_bob_bf16_head_dim_128_is_unsupported_but_f32_is_checked_further():
-    assert bob(desc(d=128, dtype=1)) == UNSUP
-    # fp32 d=128 passes the descriptor check and fails on the NULL workspace instead
+@pytest.mark.parametrize("d", [32, 64, 96, 128, 256])
+@pytest.mark.parametrize("dtype", [0, 1])
+def test_every_supported_head_dim_passes_the_descriptor_check(d, dtype):
+    # each (d, dtype) passes the descriptor check and fails on the NULL workspace instead
     p = ptrs(14)
     p[13] = ctypes.c_void_p(0)
-    assert bob(desc(d=128, dtype=0), p) == WS
+    assert bob(desc(d=d, dtype=dtype), p) == WS
+    p = ptrs(10)
+    p[9] = ctypes.c_void_p(0)
+    assert bwd(desc(d=d, dtype=dtype), p) == WS
 
 
 def test_null_misaligned_and_overlapping_pointers():
@@ -126,7 +130,7 @@ def test_status_strings_and_version():
 
 def test_python_binding_raises_on_error():
     torch = pytest.importorskip("torch")
-    q = torch.zeros(1, 1, 4, 32)  # d = 32 is unsupported: rejected before any device use
+    q = torch.zeros(1, 1, 4, 48)  # d = 48 is unsupported: rejected before any device use
     with pytest.raises(fbd.FbdError) as e:
         fbd.attn_fwd(q, q, q, O=torch.zeros_like(q), lse=torch.zeros(1, 1, 4))
     assert e.value.status == UNSUP

@@ -192,9 +192,30 @@ EDGE_N = [1, 2, 15, 17, 127, 128, 129, 255, 300]
 @pytest.mark.parametrize("N", EDGE_N)
 def test_edge_sizes(N, d, dtype):
     w = W.Workload(f"edge_B1H2N{N}d{d}_{dtype}", 1, 2, N, d, dtype)
-    ops = ("bwd", "bob") if (dtype == "f32" or d == 64) else ("bwd",)
-    got = run_ops(w, to_device(inputs(w), w), ops=ops)
-    check_full(w, got, ops)
+    got = run_ops(w, to_device(inputs(w), w), ops=("bwd", "bob"))
+    check_full(w, got, ("bwd", "bob"))
+
+
+# Head dims 32, 96 and 256 (every op, both dtypes, causal or not, grouped heads, a
+# ragged N spanning several tiles) and bf16 BoB at d = 128.
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("d", [32, 96, 256])
+@pytest.mark.parametrize("N", [1, 17, 300])
+def test_other_head_dims(N, d, dtype, causal):
+    w = W.Workload(f"headdim_B1H2N{N}d{d}_{dtype}", 1, 2, N, d, dtype)
+    got = run_ops(w, to_device(inputs(w), w), ops=("bwd", "bob"), causal=causal)
+    check_full(w, got, ("bwd", "bob"), causal=causal)
+    if dtype == "bf16":
+        got1 = run_ops(w, to_device(inputs(w), w), ops=("bwd",), gproj=1, causal=causal)
+        check_full(w, got1, ("bwd",), causal=causal)
+
+
+@pytest.mark.parametrize("d", [32, 96, 128, 256])
+def test_other_head_dims_grouped_bf16(d):
+    w = W.Workload(f"headdim_gqa_B2H4g2N200d{d}_bf16", 2, 4, 200, d, "bf16", group=2)
+    got = run_ops(w, to_device(inputs(w), w), ops=("bwd", "bob"))
+    check_full(w, got, ("bwd", "bob"))
 
 
 def test_outputs_written_once_and_nothing_outside():
@@ -317,7 +338,7 @@ def test_noncausal_gpt2_layer_bf16(gproj):
 @pytest.mark.parametrize("N", [1, 17, 129, 300])
 def test_noncausal_edge_sizes(N, d, dtype):
     w = W.Workload(f"noncausal_edge_B1H2N{N}d{d}_{dtype}", 1, 2, N, d, dtype)
-    ops = ("bwd", "bob") if (dtype == "f32" or d == 64) else ("bwd",)
+    ops = ("bwd", "bob")
     got = run_ops(w, to_device(inputs(w), w), ops=ops, causal=False)
     check_full(w, got, ops, causal=False)
     if dtype == "bf16":
@@ -381,7 +402,7 @@ def test_gqa_gpt2_layer_bf16(group, gproj):
 @pytest.mark.parametrize("causal", [True, False])
 def test_gqa_edge_sizes(N, d, dtype, causal):
     w = W.Workload(f"gqa_edge_B2H4g2N{N}d{d}_{dtype}", 2, 4, N, d, dtype, group=2)
-    ops = ("bwd", "bob") if (dtype == "f32" or d == 64) else ("bwd",)
+    ops = ("bwd", "bob")
     got = run_ops(w, to_device(inputs(w), w), ops=ops, causal=causal)
     check_full(w, got, ops, causal=causal)
     if dtype == "bf16":
