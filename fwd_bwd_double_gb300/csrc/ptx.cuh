@@ -41,6 +41,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is not complete is
+// suspended (it issues nothing) until the phase completes or about `hint_ns`
+// have passed, whichever comes first.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -51,8 +66,10 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // the TU's take-error function).  Bit 0: a bounded wait gave up.
 #define FBD_ERR_TIMEOUT 1u
 
-// A bounded mbarrier wait.  Spins on try_wait; every 1024 failed tries it checks
-// the elapsed globaltimer and the shared abort flag.  After `limit_ns` (or once
+// A bounded mbarrier wait.  Loops on try_wait with a suspend-time hint (a waiting
+// warp sleeps in hardware instead of taking issue slots from the warps that share
+// its scheduler); every 16 failed tries it checks the elapsed globaltimer and the
+// shared abort flag.  After `limit_ns` (or once
 // any thread of the CTA has aborted, or another CTA has raised the global flag)
 // it sets the abort flag and returns false; callers keep going without waiting,
 // so the kernel always reaches its teardown.
@@ -60,14 +77,15 @@ struct BoundedWait {
   volatile int* abort_flag;      // shared memory, one per CTA
   unsigned int* global_flag;     // device memory status word of this TU
   static constexpr uint64_t kLimitNs = 2000000000ull;  // 2 s
+  static constexpr uint32_t kSuspendNs = 100000u;       // longest suspension per try (100 us)
 
   __device__ __forceinline__ bool operator()(uint64_t* bar, uint32_t parity) const {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
     uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
-      if (mbar_try_wait(bar, parity)) return true;
-      if ((it & 1023u) == 0) {
+      if (mbar_try_wait_hint(bar, parity, kSuspendNs)) return true;
+      if ((it & 15u) == 0) {
         if (*abort_flag) return false;
         if (*(volatile unsigned int*)global_flag != 0u ||
             globaltimer_ns() - t0 > kLimitNs || it > (1u << 30)) {
