@@ -405,6 +405,72 @@ def max_n(args):
     print(json.dumps(out))
 
 
+def sweep(args):
+    """Per-config timing of the ops on the checked workloads, one JSON line each:
+    the long sweep (B1 H12 d64 at N = 4096 ... 262144: bwd and BoB, with the forward
+    that produces O and L), the target shape at B = 1 and B = 4 (fwd, bwd, BoB), the
+    full trading day (B2 H12 N23400: fwd, bwd) and the large-key shape (B8 H8 N2048
+    d128: bwd with and without GProj).  Median of `--steps` runs after `--warmup`,
+    CUDA events on the launching stream, min and max beside; peak device memory
+    of the op's buffers (nothing else is allocated: the library allocates nothing).
+    Inputs are device-drawn N(0,1) values rounded to bf16 (a timing run, not parity)."""
+    import torch
+
+    import fwd_bwd_double_gb300 as fbd
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    configs = [(f"long_B1H12N{n}d64", 1, 12, n, 64, ("bwd", "bob")) for n in (4096, 16384, 65536, 262144)]
+    configs += [("gpt2small_B1H12N8192d64", 1, 12, 8192, 64, ("fwd", "bwd", "bob")),
+                ("gpt2small_B4H12N8192d64", 4, 12, 8192, 64, ("fwd", "bwd", "bob")),
+                ("fullday_B2H12N23400d64", 2, 12, 23400, 64, ("fwd", "bwd")),
+                ("largekey_B8H8N2048d128", 8, 8, 2048, 128, ("bwd", "bwd_gproj"))]
+    reps, warm = max(args.steps, 1), max(args.warmup, 1)
+    for name, B, H, N, d, ops in configs:
+        torch.cuda.empty_cache()
+        torch.cuda.reset_peak_memory_stats(dev)
+        g = torch.Generator(device=dev)
+        g.manual_seed(0)
+        names = ("Q", "K", "V", "dO") + (("gdQ", "gdK", "gdV") if "bob" in ops else ())
+        x = {k: torch.randn((B, H, N, d), generator=g, device=dev).to(torch.bfloat16) for k in names}
+        O, lse = fbd.attn_fwd(x["Q"], x["K"], x["V"])
+        desc = fbd.make_desc(x["Q"])
+        outs = [torch.empty_like(x["Q"]) for _ in range(4)]
+        ws = torch.empty(fbd.attn_bob_workspace_bytes(desc), dtype=torch.uint8, device=dev)
+        run = {
+            "fwd": lambda: fbd.attn_fwd(x["Q"], x["K"], x["V"], O=outs[0], lse=lse, desc=desc),
+            "bwd": lambda: fbd.attn_bwd(x["Q"], x["K"], x["V"], O, x["dO"], lse, 0, *outs[:3], workspace=ws,
+                                        desc=desc),
+            "bwd_gproj": lambda: fbd.attn_bwd(x["Q"], x["K"], x["V"], O, x["dO"], lse, 1, *outs[:3], workspace=ws,
+                                              desc=desc),
+            "bob": lambda: fbd.attn_bob(x["Q"], x["K"], x["V"], O, x["dO"], lse, x["gdQ"], x["gdK"], x["gdV"],
+                                        *outs, workspace=ws, desc=desc),
+        }
+        line = {"sweep": name, "B": B, "H": H, "N": N, "d": d, "dtype": "bf16", "causal": True}
+        w = W.Workload(name, B, H, N, d, "bf16")
+        for op in ops:
+            for _ in range(warm):
+                run[op]()
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+            torch.cuda.synchronize()
+            ev[0].record(stream)
+            for i in range(reps):
+                run[op]()
+                ev[i + 1].record(stream)
+            torch.cuda.synchronize()
+            fbd.attn_device_status()
+            ms = sorted(ev[i].elapsed_time(ev[i + 1]) for i in range(reps))
+            med = statistics.median(ms)
+            fl = dense_flops(w, "bwd" if op == "bwd_gproj" else op)
+            line[op] = {"ms_median": med, "ms_min": ms[0], "ms_max": ms[-1],
+                        "tflops_dense": fl / (med * 1e-3) / 1e12}
+        line["peak_hbm_bytes"] = torch.cuda.max_memory_allocated(dev)
+        if "bwd_gproj" in line:
+            line["gproj_overhead_pct"] = 100.0 * (line["bwd_gproj"]["ms_median"] / line["bwd"]["ms_median"] - 1.0)
+        print(json.dumps(line), flush=True)
+        del x, O, lse, outs, ws
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -421,11 +487,14 @@ def main():
                     help="1: causal attention (the headline workload); 0: every key visible")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--max-n", action="store_true", help="report the largest N that fits in HBM instead")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time the ops on the long sweep, the target shape at B = 1 and 4, the full day and "
+                         "the large-key shape instead (one JSON line per config)")
     args = ap.parse_args()
-    if args.max_n:
+    if args.max_n or args.sweep:
         import __graft_entry__
         __graft_entry__.build()
-        max_n(args)
+        (max_n if args.max_n else sweep)(args)
         return
     args.warmup = max(args.warmup, 3)
     global CAUSAL
