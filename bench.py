@@ -409,8 +409,9 @@ def sweep(args):
     """Per-config timing of the ops on the checked workloads, one JSON line each:
     the long sweep (B1 H12 d64 at N = 4096 ... 262144: bwd and BoB, with the forward
     that produces O and L), the target shape at B = 1 and B = 4 (fwd, bwd, BoB), the
-    full trading day (B2 H12 N23400: fwd, bwd) and the large-key shape (B8 H8 N2048
-    d128: bwd with and without GProj).  Median of `--steps` runs after `--warmup`,
+    full trading day (B2 H12 N23400: fwd, bwd), the large-key shape (B8 H8 N2048
+    d128: bwd with and without GProj) and the target shape at d = 128 (fwd, bwd with
+    and without GProj).  Median of `--steps` runs after `--warmup`,
     CUDA events on the launching stream, min and max beside; peak device memory
     of the op's buffers (nothing else is allocated: the library allocates nothing).
     Inputs are device-drawn N(0,1) values rounded to bf16 (a timing run, not parity)."""
@@ -424,7 +425,8 @@ def sweep(args):
     configs += [("gpt2small_B1H12N8192d64", 1, 12, 8192, 64, ("fwd", "bwd", "bob")),
                 ("gpt2small_B4H12N8192d64", 4, 12, 8192, 64, ("fwd", "bwd", "bob")),
                 ("fullday_B2H12N23400d64", 2, 12, 23400, 64, ("fwd", "bwd")),
-                ("largekey_B8H8N2048d128", 8, 8, 2048, 128, ("bwd", "bwd_gproj"))]
+                ("largekey_B8H8N2048d128", 8, 8, 2048, 128, ("bwd", "bwd_gproj")),
+                ("headdim128_B4H12N8192d128", 4, 12, 8192, 128, ("fwd", "bwd", "bwd_gproj"))]
     reps, warm = max(args.steps, 1), max(args.warmup, 1)
     for name, B, H, N, d, ops in configs:
         torch.cuda.empty_cache()
@@ -446,6 +448,14 @@ def sweep(args):
             "bob": lambda: fbd.attn_bob(x["Q"], x["K"], x["V"], O, x["dO"], lse, x["gdQ"], x["gdK"], x["gdV"],
                                         *outs, workspace=ws, desc=desc),
         }
+        for nm, ps in (("row", fbd.ATTN_ROW_PASS), ("col", fbd.ATTN_COL_PASS)):  # the two launches apart
+            run["bwd_" + nm] = (lambda ps=ps: fbd.attn_bwd_passes(x["Q"], x["K"], x["V"], O, x["dO"], lse, ps, 0,
+                                                                 *outs[:3], workspace=ws, desc=desc))
+            if "bob" in ops:
+                run["bob_" + nm] = (lambda ps=ps: fbd.attn_bob_passes(
+                    x["Q"], x["K"], x["V"], O, x["dO"], lse, x["gdQ"], x["gdK"], x["gdV"], ps, *outs,
+                    workspace=ws, desc=desc))
+        ops = ops + tuple(f"{op}_{nm}" for op in ("bwd", "bob") if op in ops for nm in ("row", "col"))
         line = {"sweep": name, "B": B, "H": H, "N": N, "d": d, "dtype": "bf16", "causal": True}
         w = W.Workload(name, B, H, N, d, "bf16")
         for op in ops:
@@ -461,9 +471,10 @@ def sweep(args):
             fbd.attn_device_status()
             ms = sorted(ev[i].elapsed_time(ev[i + 1]) for i in range(reps))
             med = statistics.median(ms)
-            fl = dense_flops(w, "bwd" if op == "bwd_gproj" else op)
-            line[op] = {"ms_median": med, "ms_min": ms[0], "ms_max": ms[-1],
-                        "tflops_dense": fl / (med * 1e-3) / 1e12}
+            line[op] = {"ms_median": med, "ms_min": ms[0], "ms_max": ms[-1]}
+            if op in ("fwd", "bwd", "bob", "bwd_gproj"):
+                fl = dense_flops(w, "bwd" if op == "bwd_gproj" else op)
+                line[op]["tflops_dense"] = fl / (med * 1e-3) / 1e12
         line["peak_hbm_bytes"] = torch.cuda.max_memory_allocated(dev)
         if "bwd_gproj" in line:
             line["gproj_overhead_pct"] = 100.0 * (line["bwd_gproj"]["ms_median"] / line["bwd"]["ms_median"] - 1.0)
