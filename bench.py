@@ -411,7 +411,7 @@ def sweep(args):
     that produces O and L), the target shape at B = 1 and B = 4 (fwd, bwd, BoB), the
     full trading day (B2 H12 N23400: fwd, bwd), the large-key shape (B8 H8 N2048
     d128: bwd with and without GProj) and the target shape at d = 128 (fwd, bwd with
-    and without GProj).  Median of `--steps` runs after `--warmup`,
+    and without GProj, BoB).  Median of `--steps` runs after `--warmup`,
     CUDA events on the launching stream, min and max beside; peak device memory
     of the op's buffers (nothing else is allocated: the library allocates nothing).
     Inputs are device-drawn N(0,1) values rounded to bf16 (a timing run, not parity)."""
@@ -426,7 +426,7 @@ def sweep(args):
                 ("gpt2small_B4H12N8192d64", 4, 12, 8192, 64, ("fwd", "bwd", "bob")),
                 ("fullday_B2H12N23400d64", 2, 12, 23400, 64, ("fwd", "bwd")),
                 ("largekey_B8H8N2048d128", 8, 8, 2048, 128, ("bwd", "bwd_gproj")),
-                ("headdim128_B4H12N8192d128", 4, 12, 8192, 128, ("fwd", "bwd", "bwd_gproj"))]
+                ("headdim128_B4H12N8192d128", 4, 12, 8192, 128, ("fwd", "bwd", "bwd_gproj", "bob"))]
     reps, warm = max(args.steps, 1), max(args.warmup, 1)
     for name, B, H, N, d, ops in configs:
         torch.cuda.empty_cache()

@@ -102,12 +102,12 @@ bool tc_path(const fbd::Problem& p, int op) { return p.dtype == ATTN_BF16 && fbd
 }  // namespace
 
 namespace fbd {
-// bf16 tensor-core kernels by operation: forward and backward for d in {64, 128};
-// backward-over-backward for d = 64 (its row pass keeps four d-wide accumulators
-// and four score-sized tiles in the 512 TMEM columns).  Other supported head dims
-// run on the CUDA-core kernels (simt.cu).
+// bf16 tensor-core kernels by operation: forward, backward and backward-over-backward
+// for d in {64, 128} (BoB at d = 128 splits each block over two CTAs by output half:
+// its row pass's four d-wide accumulators would otherwise fill the 512 TMEM columns).
+// Other supported head dims run on the CUDA-core kernels (simt.cu).
 bool tc_supports(int op, int64_t d) {
-  if (op == 2) return d == 64;
+  (void)op;
   return d == 64 || d == 128;
 }
 }  // namespace fbd
@@ -205,6 +205,8 @@ attn_status_t attn_bob_passes(const attn_desc_t* desc, const void* Q, const void
   float4* ws = static_cast<float4*>(workspace);
   if (!tc_path(p, 2))
     return launch_status(fbd::simt_bob(p, Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ, gK, gV, gdO, ws, passes, st));
+  if (p.d == 128)
+    return launch_status(fbd::tc_bob128(p, Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ, gK, gV, gdO, ws, passes, st));
   return launch_status(fbd::tc_bob(p, Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ, gK, gV, gdO, ws, passes, st));
 }
 
@@ -238,7 +240,7 @@ attn_status_t attn_device_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "CUDA: %s", cudaGetErrorString(e));
   const uint32_t flags = fbd::tc_fwd_take_error() | fbd::tc_bwd_take_error() | fbd::tc_bwd_wide_take_error() |
-                         fbd::tc_bob_take_error();
+                         fbd::tc_bob_take_error() | fbd::tc_bob128_take_error();
   if (flags != 0) return fail(ATTN_ERR_TIMEOUT, "a device-side bounded wait gave up%s");
   return ATTN_OK;
 }

@@ -45,6 +45,11 @@ cudaError_t tc_bwd_wide(const Problem& p, const void* Q, const void* K, const vo
 cudaError_t tc_bob(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
                    const void* dO, const float* lse, const void* a, const void* b, const void* c, void* gQ,
                    void* gK, void* gV, void* gdO, float4* ws, int passes, cudaStream_t st);
+// d = 128: the same passes with each block of rows (keys) split over two CTAs by
+// output half (tc_bob128.cu).
+cudaError_t tc_bob128(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
+                      const void* dO, const float* lse, const void* a, const void* b, const void* c, void* gQ,
+                      void* gK, void* gV, void* gdO, float4* ws, int passes, cudaStream_t st);
 
 // passes: bit 0 = the row pass, bit 1 = the column pass (ATTN_ROW_PASS / ATTN_COL_PASS).
 
@@ -56,6 +61,7 @@ uint32_t tc_fwd_take_error();
 uint32_t tc_bwd_take_error();
 uint32_t tc_bwd_wide_take_error();
 uint32_t tc_bob_take_error();
+uint32_t tc_bob128_take_error();
 
 // Record `msg` as the calling thread's attn_last_error() detail; returns s.
 attn_status_t set_last_error(attn_status_t s, const char* msg);

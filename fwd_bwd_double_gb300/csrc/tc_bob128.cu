@@ -1,0 +1,768 @@
+// bf16 backward-over-backward (FlashBoB) on sm_103a at head dim d = 128: the same
+// row pass and column pass as the d = 64 kernels (tc_bob.cu), split over the two
+// halves of d.
+//
+// "FlashBoB: second-order attention", "Two scalar states replace quadratic
+// tensors".  The quantities, the two scalar states E and F', the consistent-rounding
+// state of the row pass and every hand-off between the warps are those of the d = 64
+// kernels (see the header of tc_bob.cu); only the division of the work differs.
+//
+// Why split.  At d = 128 the row pass's four d-wide fp32 accumulators X, U, Y, Z
+// alone would fill the 512 TMEM columns, and the column pass's held K, b, V, c and
+// its accumulators gV, gK would need 608.  So each block of rows (keys) is run by two
+// CTAs, h = 0 and h = 1, adjacent in the grid: both compute every score-sized tile
+// over the full d (the tile products' contraction is over d), and CTA h accumulates
+// and writes only the output columns [64h, 64h + 64).  Each CTA then needs the TMEM
+// of the d = 64 kernels.  The tile products are computed twice; that is the price of
+// keeping every output block written once with no cross-CTA reduction.
+//
+// Shared memory holds every operand of a tile product at the full d as two 64-column
+// slabs (the layout a TMA box of 64 columns writes).  A streamed stage is stored
+// slab-major, [c V b K] of columns 0-63 and then of columns 64-127 (row pass) or
+// [Q a dO] likewise (column pass), so that the stacked operands [c; V], [b; K],
+// [Q; a] of one slab are contiguous 128-row blocks and a CTA's output half is one
+// 64-column slab of each tensor.  The column pass keeps K and b in TMEM (A operands
+// of its tile products, as at d = 64) but V and c in shared memory.
+#include <cuda_bf16.h>
+
+#include <type_traits>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "tc_common.cuh"
+
+namespace fbd {
+namespace {
+
+__device__ unsigned int g_err = 0;
+
+constexpr int D = 128;
+constexpr int DH = 64;  // the output columns one CTA owns
+constexpr int BM = 128;
+constexpr int BN = 64;
+constexpr int kCompute = 256;
+constexpr int kThreads = kCompute + 96;  // compute warps, TMA warp, tile-MMA warp, output-MMA warp
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kSlab = BN * 128;       // 8 KB: 64 rows x 64 bf16 columns
+constexpr int kHeldSlab = BM * 128;   // 16 KB: 128 rows x 64 bf16 columns
+
+using tc::bf16_hi;
+using tc::bf16_lo;
+using tc::f;
+
+// Byte offset of K-step kk (16 columns of d) in a slab-major stage whose two halves
+// are `half` bytes apart.
+__device__ __forceinline__ uint32_t slab_off(int kk, int half) {
+  return static_cast<uint32_t>((kk >> 2) * half + (kk & 3) * 32);
+}
+
+// ================================================================ row pass
+struct RowLay {
+  static constexpr int NS = 2;
+  static constexpr int oQ = 0, odO = 2 * kHeldSlab, oA = 4 * kHeldSlab;  // two slabs each
+  static constexpr int oStage = 6 * kHeldSlab;
+  static constexpr int kHalf = 4 * kSlab;  // c, V, b, K of one 64-column half
+  static constexpr int kStage = 2 * kHalf;
+  static constexpr int oc = 0, oV = kSlab, ob = 2 * kSlab, oKs = 3 * kSlab;
+  static constexpr int oRed = oStage + NS * kStage;  // D_i halves; the end-of-row sums reuse Q's slabs
+  static constexpr int oBar = oRed + 2 * BM * 4;
+  static constexpr int bytes = oBar + 256;
+  // TMEM as at d = 64: tile region [G | S] then [H | dP]; operands P^, (PG)^, dS^, W^;
+  // accumulators [X | U], [Y | Z] of this CTA's 64 output columns.
+  static constexpr int cG = 0, cS = 64, cH = 0, cdP = 64;
+  static constexpr int cP = 128, cPG = 160, cdS = 192, cW = 224;
+  static constexpr int cX = 256, cU = 320, cY = 384, cZ = 448;
+};
+static_assert(RowLay::bytes <= 232448, "row pass shared memory");
+
+__global__ void __launch_bounds__(kThreads, 1)
+    bob128_row_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
+                      const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmB,
+                      const __grid_constant__ CUtensorMap tmC, const __nv_bfloat16* __restrict__ O,
+                      const __nv_bfloat16* __restrict__ dO, const float* __restrict__ lse,
+                      __nv_bfloat16* __restrict__ gQ, __nv_bfloat16* __restrict__ gdO, float4* __restrict__ ws,
+                      int N, int Np, int nrb, int BH, float scale, float c, int causal, int G) {
+  using Lay = RowLay;
+  constexpr int NS = Lay::NS;
+  extern __shared__ __align__(1024) uint8_t sm[];
+  uint64_t* q_full = reinterpret_cast<uint64_t*>(sm + Lay::oBar);
+  uint64_t* full = q_full + 1;
+  uint64_t* empty = full + NS;
+  uint64_t* sa_full = empty + NS;
+  uint64_t* sb_full = sa_full + 1;
+  uint64_t* consumed_a = sb_full + 1;
+  uint64_t* consumed_b = consumed_a + 1;
+  uint64_t* ready = consumed_b + 1;
+  uint64_t* out_done = ready + 1;
+  uint64_t* acc_full = out_done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* red = reinterpret_cast<float*>(sm + Lay::oRed);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int half = static_cast<int>(blockIdx.x & 1u);  // output columns [64 half, 64 half + 64)
+  const tc::Order ord = tc::grid_order_at(static_cast<int>(blockIdx.x >> 1), BH, nrb);
+  const int bh = ord.bh;
+  const int kvh = bh / G;
+  const int rb = nrb - 1 - ord.k;
+  const int nkv = causal ? ((rb + 1) * BM + BN - 1) / BN : (N + BN - 1) / BN;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(q_full, 1);
+    for (int s = 0; s < NS; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 2);  // released by the tile warp and by the output warp
+    }
+    ptx::mbar_init(sa_full, 1);
+    ptx::mbar_init(sb_full, 1);
+    ptx::mbar_init(consumed_a, kCompute);
+    ptx::mbar_init(consumed_b, kCompute);
+    ptx::mbar_init(ready, kCompute);
+    ptx::mbar_init(out_done, 1);
+    ptx::mbar_init(acc_full, 1);
+    *abort_flag = (ptx::smem_u32(sm) & 1023u) ? 1 : 0;
+    if (*abort_flag) atomicOr(&g_err, FBD_ERR_TIMEOUT);
+    ptx::fence_mbar_init();
+  }
+  if (warp == 9) {
+    ptx::tmem_alloc(tmem_slot, 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const ptx::BoundedWait wait{abort_flag, &g_err};
+  const bool ok = *abort_flag == 0;
+
+  if (warp == 8) {
+    if (lane == 0 && ok) {
+      ptx::prefetch_tmap(&tmK);
+      ptx::prefetch_tmap(&tmV);
+      ptx::prefetch_tmap(&tmB);
+      ptx::prefetch_tmap(&tmC);
+      ptx::mbar_expect_tx(q_full, 6 * kHeldSlab);
+      for (int cc = 0; cc < 2; ++cc) {
+        ptx::tma_load_3d(sm + Lay::oQ + cc * kHeldSlab, &tmQ, q_full, cc * 64, rb * BM, bh);
+        ptx::tma_load_3d(sm + Lay::odO + cc * kHeldSlab, &tmdO, q_full, cc * 64, rb * BM, bh);
+        ptx::tma_load_3d(sm + Lay::oA + cc * kHeldSlab, &tmA, q_full, cc * 64, rb * BM, bh);
+      }
+      for (int j = 0; j < nkv; ++j) {
+        const int s = j % NS;
+        if (j >= NS) wait(&empty[s], ((j / NS) - 1) & 1);
+        uint8_t* st = sm + Lay::oStage + s * Lay::kStage;
+        ptx::mbar_expect_tx(&full[s], 8 * kSlab);
+        for (int cc = 0; cc < 2; ++cc) {
+          uint8_t* hs = st + cc * Lay::kHalf;
+          ptx::tma_load_3d(hs + Lay::oc, &tmC, &full[s], cc * 64, j * BN, kvh);
+          ptx::tma_load_3d(hs + Lay::oV, &tmV, &full[s], cc * 64, j * BN, kvh);
+          ptx::tma_load_3d(hs + Lay::ob, &tmB, &full[s], cc * 64, j * BN, kvh);
+          ptx::tma_load_3d(hs + Lay::oKs, &tmK, &full[s], cc * 64, j * BN, kvh);
+        }
+      }
+      for (int j = (nkv > NS ? nkv - NS : 0); j < nkv; ++j) wait(&empty[j % NS], (j / NS) & 1);
+    }
+  } else if (warp == 9) {
+    if (ok) {  // all 32 lanes; one elected lane issues each MMA and commit
+      constexpr uint32_t id128 = ptx::idesc_bf16(BM, 2 * BN, 0, 0);
+      constexpr uint32_t id64 = ptx::idesc_bf16(BM, BN, 0, 0);
+      const uint32_t sSt = ptx::smem_u32(sm + Lay::oStage);
+      // Held operands: slabs contiguous (kmajor_off); streamed ones: slab-major stage halves.
+      const uint64_t dQ = tc::kmajor_desc(ptx::smem_u32(sm + Lay::oQ), BM, 0);
+      const uint64_t ddO = tc::kmajor_desc(ptx::smem_u32(sm + Lay::odO), BM, 0);
+      const uint64_t dA = tc::kmajor_desc(ptx::smem_u32(sm + Lay::oA), BM, 0);
+      const uint64_t dBK = tc::kmajor_desc(sSt + Lay::ob, 2 * BN, 0);   // [b_j; K_j]
+      const uint64_t dKk = tc::kmajor_desc(sSt + Lay::oKs, BN, 0);      // K_j
+      const uint64_t dCV = tc::kmajor_desc(sSt + Lay::oc, 2 * BN, 0);   // [c_j; V_j]
+      const uint32_t tG = tmem + Lay::cG, tH = tmem + Lay::cH;
+      wait(q_full, 0);
+      for (int j = 0; j < nkv; ++j) {
+        const int s = j % NS;
+        const uint32_t so = static_cast<uint32_t>(s * Lay::kStage);
+        wait(&full[s], (j / NS) & 1);
+        if (j > 0) wait(consumed_b, (j - 1) & 1);
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          ptx::mma_ss_e(tG, tc::desc_add(dQ, tc::kmajor_off(BM, kk)),
+                        tc::desc_add(dBK, so + slab_off(kk, Lay::kHalf)), id128, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          ptx::mma_ss_e(tG, tc::desc_add(dA, tc::kmajor_off(BM, kk)),
+                        tc::desc_add(dKk, so + slab_off(kk, Lay::kHalf)), id64, 1u);
+        ptx::mma_commit_e(sa_full);
+        wait(consumed_a, j & 1);
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          ptx::mma_ss_e(tH, tc::desc_add(ddO, tc::kmajor_off(BM, kk)),
+                        tc::desc_add(dCV, so + slab_off(kk, Lay::kHalf)), id128, kk > 0);
+        ptx::mma_commit_e(sb_full);
+        ptx::mma_commit_e(&empty[s]);
+      }
+    }
+  } else if (warp == 10) {
+    if (ok) {  // all 32 lanes; one elected lane issues each MMA and commit
+      constexpr uint32_t idO = ptx::idesc_bf16(BM, DH, 0, 1);
+      constexpr uint32_t idO2 = ptx::idesc_bf16(BM, 2 * DH, 0, 1);
+      // This CTA's half of c, V, b, K: slabs at half * kHalf in every stage.
+      const uint32_t sH = ptx::smem_u32(sm + Lay::oStage) + static_cast<uint32_t>(half * Lay::kHalf);
+      const uint64_t dCK = ptx::sdesc_sw128(sH + Lay::oc, Lay::oKs - Lay::oc, 1024);   // [c_j | K_j], MN-major
+      const uint64_t dVm = tc::mnmajor_desc(sH + Lay::oV, BN, 0);
+      const uint64_t dBKm = ptx::sdesc_sw128(sH + Lay::ob, Lay::oKs - Lay::ob, 1024);  // [b_j | K_j], MN-major
+      const uint64_t dKm = tc::mnmajor_desc(sH + Lay::oKs, BN, 0);
+      const uint32_t tX = tmem + Lay::cX, tY = tmem + Lay::cY;
+      const uint32_t tP = tmem + Lay::cP, tPG = tmem + Lay::cPG, tdS = tmem + Lay::cdS, tW = tmem + Lay::cW;
+      for (int j = 0; j < nkv; ++j) {
+        const int s = j % NS;
+        const uint32_t so = static_cast<uint32_t>(s * Lay::kStage);
+        wait(ready, j & 1);
+        wait(&full[s], (j / NS) & 1);  // already complete: the stage cannot refill before this warp releases it
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k) {
+          const uint32_t acc = (j > 0 || k > 0) ? 1u : 0u;
+          const uint32_t kb = so + 2048 * k;
+          ptx::mma_ts_e(tX, tP + 8 * k, tc::desc_add(dCK, kb), idO2, acc);
+          ptx::mma_ts_e(tX, tPG + 8 * k, tc::desc_add(dVm, kb), idO, 1u);
+          ptx::mma_ts_e(tY, tdS + 8 * k, tc::desc_add(dBKm, kb), idO2, acc);
+          ptx::mma_ts_e(tY, tW + 8 * k, tc::desc_add(dKm, kb), idO, 1u);
+        }
+        ptx::mma_commit_e(&empty[s]);
+        ptx::mma_commit_e(out_done);
+      }
+      ptx::mma_commit_e(acc_full);
+    }
+  } else {
+    const int qd = warp & 3, hf = warp >> 2;
+    const int r = qd * 32 + lane;
+    const uint32_t lo = static_cast<uint32_t>(qd * 32) << 16;
+    const int64_t row = static_cast<int64_t>(rb) * BM + r;
+    const bool live = row < N;
+    const size_t rowoff = (static_cast<size_t>(bh) * N + row) * D;
+    float part = 0.f;  // D_i over columns [64 hf, 64 hf + 64)
+    if (live) {
+      const uint4* po = reinterpret_cast<const uint4*>(O + rowoff + hf * 64);
+      const uint4* pg = reinterpret_cast<const uint4*>(dO + rowoff + hf * 64);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint4 o = po[u], g = pg[u];
+        const uint32_t aw[4] = {o.x, o.y, o.z, o.w}, gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) part += bf16_lo(aw[e]) * bf16_lo(gw[e]) + bf16_hi(aw[e]) * bf16_hi(gw[e]);
+      }
+    }
+    red[hf * BM + r] = part;
+    tc::named_sync(1, kCompute);
+    const float Dr = red[r] + red[BM + r];
+    const float L2 = live ? lse[static_cast<size_t>(bh) * N + row] * kLog2e : 0.f;
+    uint64_t accE = 0, accF = 0;
+    float accW0 = 0.f, accW1 = 0.f, accdS0 = 0.f, accdS1 = 0.f, accP0 = 0.f, accP1 = 0.f;
+    const uint64_t c2 = tc::pk2f(c, c), s2 = tc::pk2f(scale, scale);
+    const uint64_t nL2 = tc::pk2f(-L2, -L2), nD2 = tc::pk2f(-Dr, -Dr);
+    const int c0 = hf * 32;
+    const uint32_t tOp = tmem + static_cast<uint32_t>(hf * 16) + lo;
+    for (int j = 0; j < nkv; ++j) {
+      wait(sa_full, j & 1);
+      ptx::tc_fence_after();
+      uint32_t sv[32], gv[32];
+      ptx::tmem_ld32(tmem + Lay::cS + c0 + lo, sv);
+      ptx::tmem_ld32(tmem + Lay::cG + c0 + lo, gv);
+      ptx::tmem_wait_ld();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(consumed_a);
+      const int krel = j * BN + c0 - rb * BM;
+      const int klim = causal ? r - krel : N - 1 - (j * BN + c0);
+      uint64_t P2[16], G2[16];
+      uint32_t pP[16], pG[16], pS[16], pW[16];
+      auto first = [&](auto masked) {
+#pragma unroll
+        for (int t = 0; t < 32; t += 2) {
+          const float2 arg = tc::unpk2(tc::fma2(tc::pk2(sv[t], sv[t + 1]), c2, nL2));
+          float p0 = ptx::ex2(arg.x), p1 = ptx::ex2(arg.y);
+          if constexpr (decltype(masked)::value) {
+            if (t > klim) p0 = 0.f;
+            if (t + 1 > klim) p1 = 0.f;
+          }
+          const int idx = t >> 1;
+          P2[idx] = tc::pk2f(p0, p1);
+          G2[idx] = tc::mul2(tc::pk2(gv[t], gv[t + 1]), s2);
+          const uint64_t pg2 = tc::mul2(P2[idx], G2[idx]);
+          accE = tc::add2(accE, pg2);
+          const float2 pg = tc::unpk2(pg2);
+          pP[idx] = ptx::pack_bf16(p0, p1);
+          pG[idx] = ptx::pack_bf16(pg.x, pg.y);
+          accP0 = tc::add_bf16_lo(accP0, pP[idx]);
+          accP1 = tc::add_bf16_hi(accP1, pP[idx]);
+        }
+      };
+      if (causal ? krel + 31 > 0 : j * BN + c0 + 32 > N)
+        first(std::true_type{});
+      else
+        first(std::false_type{});
+      wait(sb_full, j & 1);
+      ptx::tc_fence_after();
+      uint32_t dv[32], hv[32];
+      ptx::tmem_ld32(tmem + Lay::cdP + c0 + lo, dv);
+      ptx::tmem_ld32(tmem + Lay::cH + c0 + lo, hv);
+      ptx::tmem_wait_ld();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(consumed_b);
+#pragma unroll
+      for (int t = 0; t < 32; t += 2) {
+        const int idx = t >> 1;
+        const uint64_t ds2 = tc::mul2(P2[idx], tc::add2(tc::pk2(dv[t], dv[t + 1]), nD2));
+        const uint64_t w2 = tc::fma2(G2[idx], ds2, tc::mul2(P2[idx], tc::pk2(hv[t], hv[t + 1])));
+        accF = tc::add2(accF, w2);
+        const float2 ds = tc::unpk2(ds2), w = tc::unpk2(w2);
+        pS[idx] = ptx::pack_bf16(ds.x, ds.y);
+        pW[idx] = ptx::pack_bf16(w.x, w.y);
+        accW0 = tc::add_bf16_lo(accW0, pW[idx]);
+        accW1 = tc::add_bf16_hi(accW1, pW[idx]);
+        accdS0 = tc::add_bf16_lo(accdS0, pS[idx]);
+        accdS1 = tc::add_bf16_hi(accdS1, pS[idx]);
+      }
+      if (j > 0) wait(out_done, (j - 1) & 1);
+      ptx::tmem_st16(tOp + Lay::cP, pP);
+      ptx::tmem_st16(tOp + Lay::cPG, pG);
+      ptx::tmem_st16(tOp + Lay::cdS, pS);
+      ptx::tmem_st16(tOp + Lay::cW, pW);
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(ready);
+    }
+    auto hsum = [](uint64_t x) {
+      const float2 v = tc::unpk2(x);
+      return v.x + v.y;
+    };
+    // The last tile product that reads Q completed before this warp saw the last
+    // sa_full, so Q's slabs are free for the end-of-row sums.
+    float* red2 = reinterpret_cast<float*>(sm + Lay::oQ);
+    red2[0 * BM + hf * BM + r] = hsum(accE);
+    red2[2 * BM + hf * BM + r] = hsum(accF);
+    red2[4 * BM + hf * BM + r] = accW0 + accW1;
+    red2[6 * BM + hf * BM + r] = accdS0 + accdS1;
+    red2[8 * BM + hf * BM + r] = accP0 + accP1;
+    tc::named_sync(1, kCompute);
+    const float E = red2[0 * BM + r] + red2[1 * BM + r];
+    const float Fp = red2[2 * BM + r] + red2[3 * BM + r];
+    const float sW = red2[4 * BM + r] + red2[5 * BM + r];
+    const float sdS = red2[6 * BM + r] + red2[7 * BM + r];
+    const float sP = red2[8 * BM + r] + red2[9 * BM + r];
+    const float Fq = (sW - E * sdS) / sP;
+    wait(acc_full, 0);
+    ptx::tc_fence_after();
+    uint32_t xv[32], yv[32], zv[32], uv[32];
+    ptx::tmem_ld32(tmem + Lay::cX + c0 + lo, xv);
+    ptx::tmem_ld32(tmem + Lay::cY + c0 + lo, yv);
+    ptx::tmem_ld32(tmem + Lay::cZ + c0 + lo, zv);
+    ptx::tmem_ld32(tmem + Lay::cU + c0 + lo, uv);
+    ptx::tmem_wait_ld();
+    const int gc0 = half * DH + c0;  // first global column of this thread's 32
+    if (live) {
+      uint32_t ow[16];
+      const uint4* po = reinterpret_cast<const uint4*>(O + rowoff + gc0);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint4 o = po[u];
+        ow[4 * u] = o.x;
+        ow[4 * u + 1] = o.y;
+        ow[4 * u + 2] = o.z;
+        ow[4 * u + 3] = o.w;
+      }
+      uint32_t go[16], gq[16];
+#pragma unroll
+      for (int t = 0; t < 32; t += 2) {
+        const float o0 = bf16_lo(ow[t >> 1]), o1 = bf16_hi(ow[t >> 1]);
+        go[t >> 1] = ptx::pack_bf16(f(xv[t]) - E * o0, f(xv[t + 1]) - E * o1);
+        gq[t >> 1] = ptx::pack_bf16(scale * (f(yv[t]) - E * f(zv[t]) - Fq * f(uv[t])),
+                                    scale * (f(yv[t + 1]) - E * f(zv[t + 1]) - Fq * f(uv[t + 1])));
+      }
+      uint4* d0 = reinterpret_cast<uint4*>(gdO + rowoff + gc0);
+      uint4* d1 = reinterpret_cast<uint4*>(gQ + rowoff + gc0);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        d0[u] = make_uint4(go[4 * u], go[4 * u + 1], go[4 * u + 2], go[4 * u + 3]);
+        d1[u] = make_uint4(gq[4 * u], gq[4 * u + 1], gq[4 * u + 2], gq[4 * u + 3]);
+      }
+    }
+    if (half == 0 && hf == 0 && row < Np) {  // row states, negated and pair-interleaved, once per row
+      float* wf = reinterpret_cast<float*>(ws) + static_cast<size_t>(bh) * Np * 4;
+      const int64_t k2 = row & ~static_cast<int64_t>(1);
+      const int odd = static_cast<int>(row & 1);
+      wf[k2 * 4 + odd] = live ? -L2 : 0.f;
+      wf[k2 * 4 + 2 + odd] = live ? -E : 0.f;
+      wf[(k2 + 1) * 4 + odd] = live ? -Dr : 0.f;
+      wf[(k2 + 1) * 4 + 2 + odd] = live ? -Fp : 0.f;
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+// ============================================================= column pass
+struct ColLay {
+  static constexpr int NS = 3;
+  static constexpr int oV = 0, oC = 2 * kHeldSlab;  // held V, c: two slabs each
+  static constexpr int oStage = 4 * kHeldSlab;
+  static constexpr int kHalf = 3 * kSlab;  // Q, a, dO of one 64-column half
+  static constexpr int kStat = BN * 16;
+  static constexpr int kStage = 2 * kHalf + kStat;  // a multiple of 1 KB
+  static constexpr int oBar = oStage + NS * kStage;
+  static constexpr int bytes = oBar + 256;
+  // TMEM: tile region, held K and b (A operands, 64 columns each at d = 128), the bf16
+  // output operands dPbar, dS, Sbar (32 each), accumulators gV, gK of the 64 columns.
+  static constexpr int cT = 0, cK = 128, cB = 192, cOp = 256, cgV = 352, cgK = 416;
+};
+static_assert(ColLay::bytes <= 232448, "column pass shared memory");
+static_assert(ColLay::kStage % 1024 == 0, "stages stay 1024-byte aligned");
+
+template <bool GR>
+__global__ void __launch_bounds__(kThreads, 1)
+    bob128_col_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmA,
+                      const __grid_constant__ CUtensorMap tmdO, const __grid_constant__ CUtensorMap tmSt,
+                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmC,
+                      const __nv_bfloat16* __restrict__ Kp, const __nv_bfloat16* __restrict__ Bp,
+                      __nv_bfloat16* __restrict__ gK, __nv_bfloat16* __restrict__ gV, int N, int BHkv,
+                      float scale, float c, int causal, int G) {
+  using Lay = ColLay;
+  constexpr int NS = Lay::NS;
+  extern __shared__ __align__(1024) uint8_t sm[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + Lay::oBar);
+  uint64_t* empty = full + NS;
+  uint64_t* held_ready = empty + NS;  // K, b of this key block in TMEM
+  uint64_t* held_full = held_ready + 1;  // V, c of this key block in shared memory
+  uint64_t* sa_full = held_full + 1;
+  uint64_t* sb_full = sa_full + 1;
+  uint64_t* consumed_a = sb_full + 1;
+  uint64_t* consumed_b = consumed_a + 1;
+  uint64_t* ready = consumed_b + 1;
+  uint64_t* out_done = ready + 1;
+  uint64_t* acc_full = out_done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int half = static_cast<int>(blockIdx.x & 1u);
+  const int nkb = (N + BM - 1) / BM;
+  const tc::Order ord = tc::grid_order_at(static_cast<int>(blockIdx.x >> 1), BHkv, nkb);
+  const int kvh = ord.bh;
+  const int kb = ord.k;
+  const int nq = (N + BN - 1) / BN;
+  const int i0 = causal ? (kb * BM) / BN : 0;
+  const int ntile = nq - i0;
+  const int nt = GR ? G * ntile : ntile;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 2);  // released by the tile warp and by the output warp
+    }
+    ptx::mbar_init(held_ready, kCompute);
+    ptx::mbar_init(held_full, 1);
+    ptx::mbar_init(sa_full, 1);
+    ptx::mbar_init(sb_full, 1);
+    ptx::mbar_init(consumed_a, kCompute);
+    ptx::mbar_init(consumed_b, kCompute);
+    ptx::mbar_init(ready, kCompute);
+    ptx::mbar_init(out_done, 1);
+    ptx::mbar_init(acc_full, 1);
+    *abort_flag = (ptx::smem_u32(sm) & 1023u) ? 1 : 0;
+    if (*abort_flag) atomicOr(&g_err, FBD_ERR_TIMEOUT);
+    ptx::fence_mbar_init();
+  }
+  if (warp == 9) {
+    ptx::tmem_alloc(tmem_slot, 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const ptx::BoundedWait wait{abort_flag, &g_err};
+  const bool ok = *abort_flag == 0;
+
+  if (warp == 8) {
+    if (lane == 0 && ok) {
+      ptx::prefetch_tmap(&tmQ);
+      ptx::prefetch_tmap(&tmA);
+      ptx::prefetch_tmap(&tmdO);
+      ptx::prefetch_tmap(&tmSt);
+      ptx::mbar_expect_tx(held_full, 4 * kHeldSlab);
+      for (int cc = 0; cc < 2; ++cc) {
+        ptx::tma_load_3d(sm + Lay::oV + cc * kHeldSlab, &tmV, held_full, cc * 64, kb * BM, kvh);
+        ptx::tma_load_3d(sm + Lay::oC + cc * kHeldSlab, &tmC, held_full, cc * 64, kb * BM, kvh);
+      }
+      for (int t = 0; t < nt; ++t) {
+        const int h = GR ? t / ntile : 0, s = t % NS, i = i0 + t - h * ntile, bh = GR ? kvh * G + h : kvh;
+        if (t >= NS) wait(&empty[s], ((t / NS) - 1) & 1);
+        uint8_t* st = sm + Lay::oStage + s * Lay::kStage;
+        ptx::mbar_expect_tx(&full[s], 6 * kSlab + Lay::kStat);
+        for (int cc = 0; cc < 2; ++cc) {
+          uint8_t* hs = st + cc * Lay::kHalf;
+          ptx::tma_load_3d(hs, &tmQ, &full[s], cc * 64, i * BN, bh);
+          ptx::tma_load_3d(hs + kSlab, &tmA, &full[s], cc * 64, i * BN, bh);
+          ptx::tma_load_3d(hs + 2 * kSlab, &tmdO, &full[s], cc * 64, i * BN, bh);
+        }
+        ptx::tma_load_3d(st + 2 * Lay::kHalf, &tmSt, &full[s], 0, i * BN, bh);
+      }
+      for (int t = (nt > NS ? nt - NS : 0); t < nt; ++t) wait(&empty[t % NS], (t / NS) & 1);
+    }
+  } else if (warp == 9) {
+    if (ok) {  // all 32 lanes; one elected lane issues each MMA and commit
+      constexpr uint32_t id128 = ptx::idesc_bf16(BM, 2 * BN, 0, 0);
+      constexpr uint32_t id64 = ptx::idesc_bf16(BM, BN, 0, 0);
+      const uint32_t sSt = ptx::smem_u32(sm + Lay::oStage);
+      const uint64_t dQA = tc::kmajor_desc(sSt, 2 * BN, 0);                 // [Q_i; a_i]
+      const uint64_t dQk = tc::kmajor_desc(sSt, BN, 0);                     // Q_i
+      const uint64_t ddOk = tc::kmajor_desc(sSt + 2 * kSlab, BN, 0);        // dO_i
+      const uint64_t dVk = tc::kmajor_desc(ptx::smem_u32(sm + Lay::oV), BM, 0);  // held V
+      const uint64_t dCk = tc::kmajor_desc(ptx::smem_u32(sm + Lay::oC), BM, 0);  // held c
+      const uint32_t tT = tmem + Lay::cT, tK = tmem + Lay::cK, tB = tmem + Lay::cB;
+      wait(held_ready, 0);
+      wait(held_full, 0);
+      for (int t = 0; t < nt; ++t) {
+        const int s = t % NS;
+        const uint32_t so = static_cast<uint32_t>(s * Lay::kStage);
+        wait(&full[s], (t / NS) & 1);
+        if (t > 0) wait(consumed_b, (t - 1) & 1);
+        ptx::tc_fence_after();
+        // [S^T | K a^T] = K [Q_i; a_i]^T,  G^T += b Q_i^T   (K, b from TMEM)
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          ptx::mma_ts_e(tT, tK + 8 * kk, tc::desc_add(dQA, so + slab_off(kk, Lay::kHalf)), id128, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          ptx::mma_ts_e(tT + BN, tB + 8 * kk, tc::desc_add(dQk, so + slab_off(kk, Lay::kHalf)), id64, 1u);
+        ptx::mma_commit_e(sa_full);
+        wait(consumed_a, t & 1);
+        ptx::tc_fence_after();
+        // dP^T = V dO_i^T,  H^T = c dO_i^T   (V, c from shared memory)
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          ptx::mma_ss_e(tT, tc::desc_add(dVk, tc::kmajor_off(BM, kk)),
+                        tc::desc_add(ddOk, so + slab_off(kk, Lay::kHalf)), id64, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          ptx::mma_ss_e(tT + BN, tc::desc_add(dCk, tc::kmajor_off(BM, kk)),
+                        tc::desc_add(ddOk, so + slab_off(kk, Lay::kHalf)), id64, kk > 0);
+        ptx::mma_commit_e(sb_full);
+        ptx::mma_commit_e(&empty[s]);
+      }
+    }
+  } else if (warp == 10) {
+    if (ok) {  // all 32 lanes; one elected lane issues each MMA and commit
+      constexpr uint32_t idO = ptx::idesc_bf16(BM, DH, 0, 1);
+      const uint32_t sH = ptx::smem_u32(sm + Lay::oStage) + static_cast<uint32_t>(half * Lay::kHalf);
+      const uint64_t dQm = tc::mnmajor_desc(sH, BN, 0);                 // this CTA's half of Q_i
+      const uint64_t dAm = tc::mnmajor_desc(sH + kSlab, BN, 0);         // ... of a_i
+      const uint64_t ddOm = tc::mnmajor_desc(sH + 2 * kSlab, BN, 0);    // ... of dO_i
+      const uint32_t tOp = tmem + Lay::cOp, tgV = tmem + Lay::cgV, tgK = tmem + Lay::cgK;
+      for (int t = 0; t < nt; ++t) {
+        const int s = t % NS;
+        const uint32_t so = static_cast<uint32_t>(s * Lay::kStage);
+        wait(ready, t & 1);
+        wait(&full[s], (t / NS) & 1);
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k) {
+          const uint32_t acc = (t > 0 || k > 0) ? 1u : 0u;
+          const uint32_t kb2 = so + 2048 * k;
+          ptx::mma_ts_e(tgV, tOp + k * 8, tc::desc_add(ddOm, kb2), idO, acc);
+          ptx::mma_ts_e(tgK, tOp + 32 + k * 8, tc::desc_add(dAm, kb2), idO, acc);
+          ptx::mma_ts_e(tgK, tOp + 64 + k * 8, tc::desc_add(dQm, kb2), idO, 1u);
+        }
+        ptx::mma_commit_e(&empty[s]);
+        ptx::mma_commit_e(out_done);
+      }
+      ptx::mma_commit_e(acc_full);
+    }
+  } else {
+    const int qd = warp & 3, hf = warp >> 2;
+    const int r = qd * 32 + lane;
+    const uint32_t lo = static_cast<uint32_t>(qd * 32) << 16;
+    const int key = kb * BM + r;
+    const int c0 = hf * 32;
+    {  // K and b rows of this key, elements 64 hf .. 64 hf + 63, into TMEM (A operands)
+      const __nv_bfloat16* src[2] = {Kp, Bp};
+      const uint32_t col[2] = {Lay::cK, Lay::cB};
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {  // two runs of 32 elements
+          uint32_t w[16];
+          if (key < N) {
+            const uint4* g = reinterpret_cast<const uint4*>(src[m] + (static_cast<size_t>(kvh) * N + key) * D +
+                                                            hf * 64 + q * 32);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const uint4 v = g[u];
+              w[4 * u] = v.x;
+              w[4 * u + 1] = v.y;
+              w[4 * u + 2] = v.z;
+              w[4 * u + 3] = v.w;
+            }
+          } else {
+#pragma unroll
+            for (int u = 0; u < 16; ++u) w[u] = 0u;
+          }
+          ptx::tmem_st16(tmem + col[m] + static_cast<uint32_t>(hf * 32 + q * 16) + lo, w);
+        }
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(held_ready);
+    }
+    const uint64_t c2 = tc::pk2f(c, c), s2 = tc::pk2f(scale, scale);
+    const uint32_t tOpT = tmem + Lay::cOp + static_cast<uint32_t>(hf * 16) + lo;
+    for (int t = 0; t < nt; ++t) {
+      const int s = t % NS, i = GR ? i0 + t % ntile : i0 + t;
+      const float4* stat =
+          reinterpret_cast<const float4*>(sm + Lay::oStage + s * Lay::kStage + 2 * Lay::kHalf) + c0;
+      const int qbase = i * BN + c0;
+      wait(sa_full, t & 1);
+      ptx::tc_fence_after();
+      uint32_t sv[32], gv[32];
+      ptx::tmem_ld32(tmem + Lay::cT + c0 + lo, sv);
+      ptx::tmem_ld32(tmem + Lay::cT + BN + c0 + lo, gv);
+      ptx::tmem_wait_ld();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(consumed_a);
+      uint64_t P2[16], GE2[16];
+      uint32_t pDP[16], pDS[16], pSB[16];
+      auto first = [&](auto masked) {
+#pragma unroll
+        for (int u = 0; u < 32; u += 2) {
+          const float4 A = stat[u];
+          const float2 arg = tc::unpk2(tc::fma2(tc::pk2(sv[u], sv[u + 1]), c2, tc::pk2f(A.x, A.y)));
+          float p0 = ptx::ex2(arg.x), p1 = ptx::ex2(arg.y);
+          if constexpr (decltype(masked)::value) {
+            const int q0 = qbase + u;
+            if ((causal && q0 < key) || q0 >= N) p0 = 0.f;
+            if ((causal && q0 + 1 < key) || q0 + 1 >= N) p1 = 0.f;
+          }
+          const int idx = u >> 1;
+          P2[idx] = tc::pk2f(p0, p1);
+          GE2[idx] = tc::fma2(tc::pk2(gv[u], gv[u + 1]), s2, tc::pk2f(A.z, A.w));
+          const float2 vdp = tc::unpk2(tc::mul2(P2[idx], GE2[idx]));
+          pDP[idx] = ptx::pack_bf16(vdp.x, vdp.y);
+        }
+      };
+      if ((causal && qbase < kb * BM + BM) || qbase + 32 > N)
+        first(std::true_type{});
+      else
+        first(std::false_type{});
+      wait(sb_full, t & 1);
+      ptx::tc_fence_after();
+      uint32_t dv[32], hv[32];
+      ptx::tmem_ld32(tmem + Lay::cT + c0 + lo, dv);
+      ptx::tmem_ld32(tmem + Lay::cT + BN + c0 + lo, hv);
+      ptx::tmem_wait_ld();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(consumed_b);
+#pragma unroll
+      for (int u = 0; u < 32; u += 2) {
+        const float4 Bs = stat[u + 1];
+        const int idx = u >> 1;
+        const uint64_t dmd = tc::add2(tc::pk2(dv[u], dv[u + 1]), tc::pk2f(Bs.x, Bs.y));
+        const float2 vds = tc::unpk2(tc::mul2(P2[idx], dmd));
+        const uint64_t in = tc::add2(tc::fma2(GE2[idx], dmd, tc::pk2(hv[u], hv[u + 1])), tc::pk2f(Bs.z, Bs.w));
+        const float2 vsb = tc::unpk2(tc::mul2(P2[idx], in));
+        pDS[idx] = ptx::pack_bf16(vds.x, vds.y);
+        pSB[idx] = ptx::pack_bf16(vsb.x, vsb.y);
+      }
+      if (t > 0) wait(out_done, (t - 1) & 1);
+      ptx::tmem_st16(tOpT, pDP);
+      ptx::tmem_st16(tOpT + 32, pDS);
+      ptx::tmem_st16(tOpT + 64, pSB);
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(ready);
+    }
+    wait(acc_full, 0);
+    ptx::tc_fence_after();
+    uint32_t av[32], bv[32];
+    ptx::tmem_ld32(tmem + Lay::cgV + c0 + lo, av);
+    ptx::tmem_ld32(tmem + Lay::cgK + c0 + lo, bv);
+    ptx::tmem_wait_ld();
+    if (key < N) {
+      const size_t rowoff = (static_cast<size_t>(kvh) * N + key) * D + half * DH + c0;
+      uint32_t ov[16], ok2[16];
+#pragma unroll
+      for (int u = 0; u < 32; u += 2) {
+        ov[u >> 1] = ptx::pack_bf16(f(av[u]), f(av[u + 1]));
+        ok2[u >> 1] = ptx::pack_bf16(scale * f(bv[u]), scale * f(bv[u + 1]));
+      }
+      uint4* dvp = reinterpret_cast<uint4*>(gV + rowoff);
+      uint4* dkp = reinterpret_cast<uint4*>(gK + rowoff);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        dvp[u] = make_uint4(ov[4 * u], ov[4 * u + 1], ov[4 * u + 2], ov[4 * u + 3]);
+        dkp[u] = make_uint4(ok2[4 * u], ok2[4 * u + 1], ok2[4 * u + 2], ok2[4 * u + 3]);
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+cudaError_t tc_bob128(const Problem& p, const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                      const float* lse, const void* a, const void* b, const void* cc, void* gQ, void* gK, void* gV,
+                      void* gdO, float4* ws, int passes, cudaStream_t st) {
+  if (p.d != D) return cudaErrorInvalidValue;
+  alignas(64) CUtensorMap q128, do128, a128, k64, v64, b64, c64;
+  alignas(64) CUtensorMap q64, a64, do64, s64, v128, c128;
+  const int64_t N = p.N, BH = p.BH, Np = (p.N + 1) & ~static_cast<int64_t>(1);
+  if (!make_tmap_bf16(&q128, Q, N, D, BH, BM) || !make_tmap_bf16(&do128, dO, N, D, BH, BM) ||
+      !make_tmap_bf16(&a128, a, N, D, BH, BM) || !make_tmap_bf16(&k64, K, N, D, p.BHkv, BN) ||
+      !make_tmap_bf16(&v64, V, N, D, p.BHkv, BN) || !make_tmap_bf16(&b64, b, N, D, p.BHkv, BN) ||
+      !make_tmap_bf16(&c64, cc, N, D, p.BHkv, BN) || !make_tmap_bf16(&q64, Q, N, D, BH, BN) ||
+      !make_tmap_bf16(&a64, a, N, D, BH, BN) || !make_tmap_bf16(&do64, dO, N, D, BH, BN) ||
+      !make_tmap_stats(&s64, ws, Np, BH, BN) || !make_tmap_bf16(&v128, V, N, D, p.BHkv, BM) ||
+      !make_tmap_bf16(&c128, cc, N, D, p.BHkv, BM))
+    return cudaErrorInvalidValue;
+  const float c = p.scale * kLog2e;
+  const int nrb = static_cast<int>((N + BM - 1) / BM);
+  cudaError_t e = cudaSuccess;
+  if (passes & 1) {
+    e = cudaFuncSetAttribute(bob128_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, RowLay::bytes);
+    if (e != cudaSuccess) return e;
+    bob128_row_kernel<<<static_cast<unsigned>(2 * nrb * BH), kThreads, RowLay::bytes, st>>>(
+        q128, do128, a128, k64, v64, b64, c64, static_cast<const __nv_bfloat16*>(O),
+        static_cast<const __nv_bfloat16*>(dO), lse, static_cast<__nv_bfloat16*>(gQ),
+        static_cast<__nv_bfloat16*>(gdO), ws, static_cast<int>(N), static_cast<int>(Np), nrb,
+        static_cast<int>(BH), p.scale, c, p.causal, p.group);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (!(passes & 2)) return cudaSuccess;
+  auto col = p.group > 1 ? bob128_col_kernel<true> : bob128_col_kernel<false>;
+  e = cudaFuncSetAttribute(col, cudaFuncAttributeMaxDynamicSharedMemorySize, ColLay::bytes);
+  if (e != cudaSuccess) return e;
+  col<<<static_cast<unsigned>(2 * nrb * p.BHkv), kThreads, ColLay::bytes, st>>>(
+      q64, a64, do64, s64, v128, c128, static_cast<const __nv_bfloat16*>(K), static_cast<const __nv_bfloat16*>(b),
+      static_cast<__nv_bfloat16*>(gK), static_cast<__nv_bfloat16*>(gV), static_cast<int>(N),
+      static_cast<int>(p.BHkv), p.scale, c, p.causal, p.group);
+  return cudaGetLastError();
+}
+
+uint32_t tc_bob128_take_error() {
+  uint32_t v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, g_err, sizeof(v)) != cudaSuccess) return 0;
+  if (v) cudaMemcpyToSymbol(g_err, &z, sizeof(z));
+  return v;
+}
+
+}  // namespace fbd

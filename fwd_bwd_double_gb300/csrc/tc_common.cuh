@@ -53,9 +53,8 @@ __device__ __forceinline__ void named_sync(int id, int n) {
 struct Order {
   int bh, k;
 };
-__device__ __forceinline__ Order grid_order(int BH, int nblk) {
+__device__ __forceinline__ Order grid_order_at(int x, int BH, int nblk) {
   constexpr int G = 8;
-  const int x = static_cast<int>(blockIdx.x);
   const int group = x / (G * nblk);
   const int base = group * G;
   const int gsize = min(G, BH - base);
@@ -64,6 +63,9 @@ __device__ __forceinline__ Order grid_order(int BH, int nblk) {
   o.k = within / gsize;
   o.bh = base + within % gsize;
   return o;
+}
+__device__ __forceinline__ Order grid_order(int BH, int nblk) {
+  return grid_order_at(static_cast<int>(blockIdx.x), BH, nblk);
 }
 
 // The two floats held by a packed bf16x2 word (low half = even element).

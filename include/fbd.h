@@ -33,9 +33,9 @@
  *   Supported:  causal in {0, 1}; any group dividing H; d in {32, 64, 96, 128,
  *               256}; dtype in {ATTN_F32, ATTN_BF16}.  Anything else returns
  *               ATTN_ERR_UNSUPPORTED before any launch.
- *   Kernels:    the shape decides, never a failure: bf16 attn_fwd / attn_bwd at
- *               d in {64, 128} and bf16 attn_bob at d = 64 run on the tcgen05/TMA
- *               tensor-core kernels; every other (dtype, d) runs on the CUDA-core
+ *   Kernels:    the shape decides, never a failure: bf16 attn_fwd, attn_bwd and
+ *               attn_bob at d in {64, 128} run on the tcgen05/TMA tensor-core
+ *               kernels; every other (dtype, d) runs on the CUDA-core
  *               kernels (fp32 arithmetic; bf16 inputs widened on load, outputs
  *               rounded once on store), which are exact to fp32 rounding but one to
  *               two orders of magnitude slower.

@@ -438,3 +438,32 @@ def test_gqa_row_outputs_equal_repeated_heads_bitwise(dtype):
             s = host(b).reshape(2, 2, 3, 300, 64).sum(axis=2)
             assert rel_fro(host(a), s) <= tol
     fbd.attn_device_status()
+
+
+# ------------------------------------------------------- BoB at head dim 128
+# The tensor-core BoB at d = 128 runs each block of rows (keys) as two CTAs, one per
+# output half; both halves and the row states written by half 0 are checked here.
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_bob_head_dim_128_bf16(causal):
+    w = W.Workload("bob_d128_B2H4N1000d128_bf16", 2, 4, 1000, 128, "bf16")
+    got = run_ops(w, to_device(inputs(w), w), ops=("bob",), causal=causal)
+    errs = check_full(w, got, ("bob",), causal=causal)
+    print(w.name, causal, {k: f"{v:.2e}" for k, v in errs.items()})
+
+
+def test_bob_head_dim_128_passes_compose_on_nan_workspace():
+    import torch
+    import fwd_bwd_double_gb300 as fbd
+    w = W.Workload("bob_d128_passes_B1H3N300d128_bf16", 1, 3, 300, 128, "bf16")
+    x = to_device(inputs(w), w)
+    O, lse = fbd.attn_fwd(x["Q"], x["K"], x["V"])
+    ref = fbd.attn_bob(x["Q"], x["K"], x["V"], O, x["dO"], lse, x["gdQ"], x["gdK"], x["gdV"])
+    ws = torch.full((fbd.attn_bob_workspace_bytes(fbd.make_desc(x["Q"])) // 4,), float("nan"), device="cuda")
+    outs = [torch.full_like(x["Q"], float("nan")) for _ in range(4)]
+    for ps in (fbd.ATTN_ROW_PASS, fbd.ATTN_COL_PASS):
+        fbd.attn_bob_passes(x["Q"], x["K"], x["V"], O, x["dO"], lse, x["gdQ"], x["gdK"], x["gdV"], ps,
+                            gQ=outs[0], gK=outs[1], gV=outs[2], gdO=outs[3], workspace=ws)
+    fbd.attn_device_status()
+    for a, b in zip(outs, ref):
+        assert torch.equal(a, b)
