@@ -103,12 +103,15 @@ bool tc_path(const fbd::Problem& p, int op) { return p.dtype == ATTN_BF16 && fbd
 
 namespace fbd {
 // bf16 tensor-core kernels by operation: forward, backward and backward-over-backward
-// for d in {64, 128} (BoB at d = 128 splits each block over two CTAs by output half:
-// its row pass's four d-wide accumulators would otherwise fill the 512 TMEM columns).
-// Other supported head dims run on the CUDA-core kernels (simt.cu).
+// for d in {64, 128}, and for d = 32 and 96 on those kernels with the head dim
+// zero-padded to 64 and 128 in shared memory (TMA fills the columns past d with
+// zeros, which add nothing to any product; nothing past d is stored).  BoB at
+// d > 64 splits each block over two CTAs by output half: its row pass's four d-wide
+// accumulators would otherwise fill the 512 TMEM columns.  d = 256 runs on the
+// CUDA-core kernels (simt.cu).
 bool tc_supports(int op, int64_t d) {
   (void)op;
-  return d == 64 || d == 128;
+  return d == 32 || d == 64 || d == 96 || d == 128;
 }
 }  // namespace fbd
 
@@ -205,7 +208,7 @@ attn_status_t attn_bob_passes(const attn_desc_t* desc, const void* Q, const void
   float4* ws = static_cast<float4*>(workspace);
   if (!tc_path(p, 2))
     return launch_status(fbd::simt_bob(p, Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ, gK, gV, gdO, ws, passes, st));
-  if (p.d == 128)
+  if (p.d > 64)
     return launch_status(fbd::tc_bob128(p, Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ, gK, gV, gdO, ws, passes, st));
   return launch_status(fbd::tc_bob(p, Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ, gK, gV, gdO, ws, passes, st));
 }

@@ -101,6 +101,9 @@ struct RowLay {
   static constexpr int cX = 256, cU = 320, cY = 384, cZ = 448;
 };
 
+// PAD: head dim hd < D (zero-padded in shared memory).  The unpadded instance sees
+// the constant D, so its code is that of a kernel without the option.
+template <bool PAD>
 __global__ void __launch_bounds__(kThreads, 1)
     bob_row_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                    const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmK,
@@ -108,7 +111,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tmC, const __nv_bfloat16* __restrict__ O,
                    const __nv_bfloat16* __restrict__ dO, const float* __restrict__ lse,
                    __nv_bfloat16* __restrict__ gQ, __nv_bfloat16* __restrict__ gdO, float4* __restrict__ ws, int N,
-                   int Np, int nrb, int BH, float scale, float c, int causal, int G) {
+                   int Np, int nrb, int BH, float scale, float c, int causal, int G, int hd_arg) {
+  const int hd = PAD ? hd_arg : D;
   using Lay = RowLay;
   constexpr int NS = Lay::NS;
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -259,9 +263,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lo = static_cast<uint32_t>(qd * 32) << 16;
     const int64_t row = static_cast<int64_t>(rb) * BM + r;
     const bool live = row < N;
-    const size_t rowoff = (static_cast<size_t>(bh) * N + row) * D;
+    const size_t rowoff = (static_cast<size_t>(bh) * N + row) * hd;  // rows of hd <= D columns
     float part = 0.f;
-    if (live) {
+    if (live && hf * 32 < hd) {  // columns past hd are padding
       const uint4* po = reinterpret_cast<const uint4*>(O + rowoff + hf * 32);
       const uint4* pg = reinterpret_cast<const uint4*>(dO + rowoff + hf * 32);
 #pragma unroll
@@ -381,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tmem_ld32(tmem + Lay::cZ + c0 + lo, zv);
     ptx::tmem_ld32(tmem + Lay::cU + c0 + lo, uv);
     ptx::tmem_wait_ld();
-    if (live) {
+    if (live && c0 < hd) {
       uint32_t ow[16];  // this thread's half of the O row (32 bf16), read again here
       const uint4* po = reinterpret_cast<const uint4*>(O + rowoff + c0);
 #pragma unroll
@@ -455,14 +459,16 @@ struct ColLay {
 };
 
 // GR: grouped key/value heads (G > 1).  The G == 1 instance keeps the plain tile loop.
-template <bool GR>
+// PAD as in the row pass.
+template <bool GR, bool PAD>
 __global__ void __launch_bounds__(kThreads, 1)
     bob_col_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmdO, const __grid_constant__ CUtensorMap tmSt,
                    const __nv_bfloat16* __restrict__ Kp, const __nv_bfloat16* __restrict__ Bp,
                    const __nv_bfloat16* __restrict__ Vp, const __nv_bfloat16* __restrict__ Cp,
                    __nv_bfloat16* __restrict__ gK, __nv_bfloat16* __restrict__ gV, int N, int BHkv, float scale,
-                   float c, int causal, int G) {
+                   float c, int causal, int G, int hd_arg) {
+  const int hd = PAD ? hd_arg : D;
   using Lay = ColLay;
   constexpr int NS = Lay::NS;
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -614,8 +620,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
         uint32_t w[16];
-        if (key < N) {
-          const uint4* g = reinterpret_cast<const uint4*>(src[m] + (static_cast<size_t>(kvh) * N + key) * D + c0);
+        if (key < N && c0 < hd) {
+          const uint4* g = reinterpret_cast<const uint4*>(src[m] + (static_cast<size_t>(kvh) * N + key) * hd + c0);
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const uint4 v = g[u];
@@ -710,8 +716,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tmem_ld32(tmem + Lay::cgV + c0 + lo, av);
     ptx::tmem_ld32(tmem + Lay::cgK + c0 + lo, bv);
     ptx::tmem_wait_ld();
-    if (key < N) {
-      const size_t rowoff = (static_cast<size_t>(kvh) * N + key) * D;
+    if (key < N && c0 < hd) {
+      const size_t rowoff = (static_cast<size_t>(kvh) * N + key) * hd;
       uint32_t ov[16], ok2[16];
 #pragma unroll
       for (int u = 0; u < 32; u += 2) {
@@ -741,39 +747,42 @@ __global__ void __launch_bounds__(kThreads, 1)
 cudaError_t tc_bob(const Problem& p, const void* Q, const void* K, const void* V, const void* O, const void* dO,
                    const float* lse, const void* a, const void* b, const void* cc, void* gQ, void* gK, void* gV,
                    void* gdO, float4* ws, int passes, cudaStream_t st) {
-  if (p.d != D) return cudaErrorInvalidValue;
+  if (p.d > D) return cudaErrorInvalidValue;
   alignas(64) CUtensorMap q128, do128, a128, k64, v64, b64, c64;
   alignas(64) CUtensorMap q64, a64, do64, s64;
-  const int64_t N = p.N, BH = p.BH, Np = (p.N + 1) & ~static_cast<int64_t>(1);
-  if (!make_tmap_bf16(&q128, Q, N, D, BH, BM) || !make_tmap_bf16(&do128, dO, N, D, BH, BM) ||
-      !make_tmap_bf16(&a128, a, N, D, BH, BM) || !make_tmap_bf16(&k64, K, N, D, p.BHkv, BN) ||
-      !make_tmap_bf16(&v64, V, N, D, p.BHkv, BN) || !make_tmap_bf16(&b64, b, N, D, p.BHkv, BN) ||
-      !make_tmap_bf16(&c64, cc, N, D, p.BHkv, BN) || !make_tmap_bf16(&q64, Q, N, D, BH, BN) ||
-      !make_tmap_bf16(&a64, a, N, D, BH, BN) || !make_tmap_bf16(&do64, dO, N, D, BH, BN) ||
+  const int64_t N = p.N, BH = p.BH, Np = (p.N + 1) & ~static_cast<int64_t>(1), d = p.d;
+  // Tensor maps over the true head dim d <= D: TMA zero-fills the padding columns.
+  if (!make_tmap_bf16(&q128, Q, N, d, BH, BM) || !make_tmap_bf16(&do128, dO, N, d, BH, BM) ||
+      !make_tmap_bf16(&a128, a, N, d, BH, BM) || !make_tmap_bf16(&k64, K, N, d, p.BHkv, BN) ||
+      !make_tmap_bf16(&v64, V, N, d, p.BHkv, BN) || !make_tmap_bf16(&b64, b, N, d, p.BHkv, BN) ||
+      !make_tmap_bf16(&c64, cc, N, d, p.BHkv, BN) || !make_tmap_bf16(&q64, Q, N, d, BH, BN) ||
+      !make_tmap_bf16(&a64, a, N, d, BH, BN) || !make_tmap_bf16(&do64, dO, N, d, BH, BN) ||
       !make_tmap_stats(&s64, ws, Np, BH, BN))
     return cudaErrorInvalidValue;
   const float c = p.scale * kLog2e;
   const int nrb = static_cast<int>((N + BM - 1) / BM);
   cudaError_t e = cudaSuccess;
   if (passes & 1) {
-  e = cudaFuncSetAttribute(bob_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, RowLay::bytes);
+  auto row = d < D ? bob_row_kernel<true> : bob_row_kernel<false>;
+  e = cudaFuncSetAttribute(row, cudaFuncAttributeMaxDynamicSharedMemorySize, RowLay::bytes);
   if (e != cudaSuccess) return e;
-  bob_row_kernel<<<static_cast<unsigned>(nrb * BH), kThreads, RowLay::bytes, st>>>(
+  row<<<static_cast<unsigned>(nrb * BH), kThreads, RowLay::bytes, st>>>(
       q128, do128, a128, k64, v64, b64, c64, static_cast<const __nv_bfloat16*>(O),
       static_cast<const __nv_bfloat16*>(dO), lse, static_cast<__nv_bfloat16*>(gQ), static_cast<__nv_bfloat16*>(gdO),
       ws, static_cast<int>(N), static_cast<int>(Np), nrb, static_cast<int>(BH), p.scale, c, p.causal,
-      p.group);
+      p.group, static_cast<int>(d));
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (!(passes & 2)) return cudaSuccess;
-  auto col = p.group > 1 ? bob_col_kernel<true> : bob_col_kernel<false>;
+  auto col = p.group > 1 ? (d < D ? bob_col_kernel<true, true> : bob_col_kernel<true, false>)
+                          : (d < D ? bob_col_kernel<false, true> : bob_col_kernel<false, false>);
   e = cudaFuncSetAttribute(col, cudaFuncAttributeMaxDynamicSharedMemorySize, ColLay::bytes);
   if (e != cudaSuccess) return e;
   col<<<static_cast<unsigned>(nrb * p.BHkv), kThreads, ColLay::bytes, st>>>(
       q64, a64, do64, s64, static_cast<const __nv_bfloat16*>(K), static_cast<const __nv_bfloat16*>(b),
       static_cast<const __nv_bfloat16*>(V), static_cast<const __nv_bfloat16*>(cc), static_cast<__nv_bfloat16*>(gK),
       static_cast<__nv_bfloat16*>(gV), static_cast<int>(N), static_cast<int>(p.BHkv), p.scale, c, p.causal,
-      p.group);
+      p.group, static_cast<int>(d));
   return cudaGetLastError();
 }
 

@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tmC, const __nv_bfloat16* __restrict__ O,
                       const __nv_bfloat16* __restrict__ dO, const float* __restrict__ lse,
                       __nv_bfloat16* __restrict__ gQ, __nv_bfloat16* __restrict__ gdO, float4* __restrict__ ws,
-                      int N, int Np, int nrb, int BH, float scale, float c, int causal, int G) {
+                      int N, int Np, int nrb, int BH, float scale, float c, int causal, int G, int hd) {
   using Lay = RowLay;
   constexpr int NS = Lay::NS;
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -240,13 +240,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lo = static_cast<uint32_t>(qd * 32) << 16;
     const int64_t row = static_cast<int64_t>(rb) * BM + r;
     const bool live = row < N;
-    const size_t rowoff = (static_cast<size_t>(bh) * N + row) * D;
+    const size_t rowoff = (static_cast<size_t>(bh) * N + row) * hd;  // rows of hd <= D columns
     float part = 0.f;  // D_i over columns [64 hf, 64 hf + 64)
     if (live) {
       const uint4* po = reinterpret_cast<const uint4*>(O + rowoff + hf * 64);
       const uint4* pg = reinterpret_cast<const uint4*>(dO + rowoff + hf * 64);
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
+        if (hf * 64 + 8 * u >= hd) break;  // padding columns
         const uint4 o = po[u], g = pg[u];
         const uint32_t aw[4] = {o.x, o.y, o.z, o.w}, gw[4] = {g.x, g.y, g.z, g.w};
 #pragma unroll
@@ -360,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tmem_ld32(tmem + Lay::cU + c0 + lo, uv);
     ptx::tmem_wait_ld();
     const int gc0 = half * DH + c0;  // first global column of this thread's 32
-    if (live) {
+    if (live && gc0 < hd) {
       uint32_t ow[16];
       const uint4* po = reinterpret_cast<const uint4*>(O + rowoff + gc0);
 #pragma unroll
@@ -430,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmC,
                       const __nv_bfloat16* __restrict__ Kp, const __nv_bfloat16* __restrict__ Bp,
                       __nv_bfloat16* __restrict__ gK, __nv_bfloat16* __restrict__ gV, int N, int BHkv,
-                      float scale, float c, int causal, int G) {
+                      float scale, float c, int causal, int G, int hd) {
   using Lay = ColLay;
   constexpr int NS = Lay::NS;
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -597,8 +598,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int q = 0; q < 2; ++q) {  // two runs of 32 elements
           uint32_t w[16];
-          if (key < N) {
-            const uint4* g = reinterpret_cast<const uint4*>(src[m] + (static_cast<size_t>(kvh) * N + key) * D +
+          if (key < N && hf * 64 + q * 32 < hd) {
+            const uint4* g = reinterpret_cast<const uint4*>(src[m] + (static_cast<size_t>(kvh) * N + key) * hd +
                                                             hf * 64 + q * 32);
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
@@ -691,8 +692,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tmem_ld32(tmem + Lay::cgV + c0 + lo, av);
     ptx::tmem_ld32(tmem + Lay::cgK + c0 + lo, bv);
     ptx::tmem_wait_ld();
-    if (key < N) {
-      const size_t rowoff = (static_cast<size_t>(kvh) * N + key) * D + half * DH + c0;
+    if (key < N && half * DH + c0 < hd) {
+      const size_t rowoff = (static_cast<size_t>(kvh) * N + key) * hd + half * DH + c0;
       uint32_t ov[16], ok2[16];
 #pragma unroll
       for (int u = 0; u < 32; u += 2) {
@@ -722,17 +723,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 cudaError_t tc_bob128(const Problem& p, const void* Q, const void* K, const void* V, const void* O, const void* dO,
                       const float* lse, const void* a, const void* b, const void* cc, void* gQ, void* gK, void* gV,
                       void* gdO, float4* ws, int passes, cudaStream_t st) {
-  if (p.d != D) return cudaErrorInvalidValue;
+  if (p.d > D || p.d <= DH) return cudaErrorInvalidValue;
   alignas(64) CUtensorMap q128, do128, a128, k64, v64, b64, c64;
   alignas(64) CUtensorMap q64, a64, do64, s64, v128, c128;
-  const int64_t N = p.N, BH = p.BH, Np = (p.N + 1) & ~static_cast<int64_t>(1);
-  if (!make_tmap_bf16(&q128, Q, N, D, BH, BM) || !make_tmap_bf16(&do128, dO, N, D, BH, BM) ||
-      !make_tmap_bf16(&a128, a, N, D, BH, BM) || !make_tmap_bf16(&k64, K, N, D, p.BHkv, BN) ||
-      !make_tmap_bf16(&v64, V, N, D, p.BHkv, BN) || !make_tmap_bf16(&b64, b, N, D, p.BHkv, BN) ||
-      !make_tmap_bf16(&c64, cc, N, D, p.BHkv, BN) || !make_tmap_bf16(&q64, Q, N, D, BH, BN) ||
-      !make_tmap_bf16(&a64, a, N, D, BH, BN) || !make_tmap_bf16(&do64, dO, N, D, BH, BN) ||
-      !make_tmap_stats(&s64, ws, Np, BH, BN) || !make_tmap_bf16(&v128, V, N, D, p.BHkv, BM) ||
-      !make_tmap_bf16(&c128, cc, N, D, p.BHkv, BM))
+  const int64_t N = p.N, BH = p.BH, Np = (p.N + 1) & ~static_cast<int64_t>(1), d = p.d;
+  // Tensor maps over the true head dim d (64 < d <= 128): TMA zero-fills the padding columns.
+  if (!make_tmap_bf16(&q128, Q, N, d, BH, BM) || !make_tmap_bf16(&do128, dO, N, d, BH, BM) ||
+      !make_tmap_bf16(&a128, a, N, d, BH, BM) || !make_tmap_bf16(&k64, K, N, d, p.BHkv, BN) ||
+      !make_tmap_bf16(&v64, V, N, d, p.BHkv, BN) || !make_tmap_bf16(&b64, b, N, d, p.BHkv, BN) ||
+      !make_tmap_bf16(&c64, cc, N, d, p.BHkv, BN) || !make_tmap_bf16(&q64, Q, N, d, BH, BN) ||
+      !make_tmap_bf16(&a64, a, N, d, BH, BN) || !make_tmap_bf16(&do64, dO, N, d, BH, BN) ||
+      !make_tmap_stats(&s64, ws, Np, BH, BN) || !make_tmap_bf16(&v128, V, N, d, p.BHkv, BM) ||
+      !make_tmap_bf16(&c128, cc, N, d, p.BHkv, BM))
     return cudaErrorInvalidValue;
   const float c = p.scale * kLog2e;
   const int nrb = static_cast<int>((N + BM - 1) / BM);
@@ -744,7 +746,7 @@ cudaError_t tc_bob128(const Problem& p, const void* Q, const void* K, const void
         q128, do128, a128, k64, v64, b64, c64, static_cast<const __nv_bfloat16*>(O),
         static_cast<const __nv_bfloat16*>(dO), lse, static_cast<__nv_bfloat16*>(gQ),
         static_cast<__nv_bfloat16*>(gdO), ws, static_cast<int>(N), static_cast<int>(Np), nrb,
-        static_cast<int>(BH), p.scale, c, p.causal, p.group);
+        static_cast<int>(BH), p.scale, c, p.causal, p.group, static_cast<int>(d));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (!(passes & 2)) return cudaSuccess;
@@ -754,7 +756,7 @@ cudaError_t tc_bob128(const Problem& p, const void* Q, const void* K, const void
   col<<<static_cast<unsigned>(2 * nrb * p.BHkv), kThreads, ColLay::bytes, st>>>(
       q64, a64, do64, s64, v128, c128, static_cast<const __nv_bfloat16*>(K), static_cast<const __nv_bfloat16*>(b),
       static_cast<__nv_bfloat16*>(gK), static_cast<__nv_bfloat16*>(gV), static_cast<int>(N),
-      static_cast<int>(p.BHkv), p.scale, c, p.causal, p.group);
+      static_cast<int>(p.BHkv), p.scale, c, p.causal, p.group, static_cast<int>(d));
   return cudaGetLastError();
 }
 

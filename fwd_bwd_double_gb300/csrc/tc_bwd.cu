@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
                    const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const __nv_bfloat16* __restrict__ O, const __nv_bfloat16* __restrict__ dO,
                    const float* __restrict__ lse, __nv_bfloat16* __restrict__ dQ, float4* __restrict__ ws, int N,
-                   int Np, int nrb, int BH, float scale, float c, int causal, int G) {
+                   int Np, int nrb, int BH, float scale, float c, int causal, int G, int dv) {
   using Lay = RowLay<D, NB, GP>;
   constexpr int NS = Lay::NS;
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -195,13 +195,14 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
     const uint32_t lo = static_cast<uint32_t>(qd * 32) << 16;
     const int64_t row = static_cast<int64_t>(rb) * BM + r;
     const bool live = row < N;
-    const size_t rowoff = (static_cast<size_t>(bh) * N + row) * D;
+    const size_t rowoff = (static_cast<size_t>(bh) * N + row) * dv;  // rows of dv <= D columns
     float part = 0.f;
     if (live) {  // this thread's half of D_r = dO_r . O_r
       const uint4* po = reinterpret_cast<const uint4*>(O + rowoff + hf * (D / 2));
       const uint4* pg = reinterpret_cast<const uint4*>(dO + rowoff + hf * (D / 2));
 #pragma unroll
       for (int u = 0; u < D / 16; ++u) {
+        if (hf * (D / 2) + 8 * u >= dv) break;  // padding columns
         const uint4 a = po[u], g = pg[u];
         const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, gw[4] = {g.x, g.y, g.z, g.w};
 #pragma unroll
@@ -271,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
       ptx::tmem_ld32(tmem + Lay::cdQ + hf * (D / 2) + cc + lo, a);
       if constexpr (GP) ptx::tmem_ld32(tmem + Lay::cPK + hf * (D / 2) + cc + lo, pkv);
       ptx::tmem_wait_ld();
-      if (live) {
+      if (live && hf * (D / 2) + cc < dv) {
         uint32_t o[16];
 #pragma unroll
         for (int t = 0; t < 32; t += 2) {
@@ -329,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bwd_col_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                    const __grid_constant__ CUtensorMap tmSt, __nv_bfloat16* __restrict__ dK,
-                   __nv_bfloat16* __restrict__ dV, int N, int BHkv, float scale, float c, int causal, int G) {
+                   __nv_bfloat16* __restrict__ dV, int N, int BHkv, float scale, float c, int causal, int G, int dv) {
   using Lay = ColLay<D, NB, GP>;
   constexpr int NS = Lay::NS;
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -496,25 +497,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     wait(acc_full, 0);
     ptx::tc_fence_after();
     const bool live = key < N;
-    const size_t rowoff = (static_cast<size_t>(kvh) * N + key) * D;
+    const size_t rowoff = (static_cast<size_t>(kvh) * N + key) * dv;
 #pragma unroll
     for (int cc = 0; cc < D / 2; cc += 32) {
       uint32_t a[32], g[32];
       ptx::tmem_ld32(tmem + Lay::cdV + hf * (D / 2) + cc + lo, a);
       ptx::tmem_ld32(tmem + Lay::cdK + hf * (D / 2) + cc + lo, g);
       ptx::tmem_wait_ld();
-      if (live) {
+      if (live && hf * (D / 2) + cc < dv) {
         uint32_t ov[16], ok2[16];
 #pragma unroll
         for (int u = 0; u < 32; u += 2) {
           ov[u >> 1] = ptx::pack_bf16(f(a[u]), f(a[u + 1]));
           ok2[u >> 1] = ptx::pack_bf16(scale * f(g[u]), scale * f(g[u + 1]));
         }
-        uint4* dv = reinterpret_cast<uint4*>(dV + rowoff + hf * (D / 2) + cc);
+        uint4* dvp = reinterpret_cast<uint4*>(dV + rowoff + hf * (D / 2) + cc);
         uint4* dk2 = reinterpret_cast<uint4*>(dK + rowoff + hf * (D / 2) + cc);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          dv[u] = make_uint4(ov[4 * u], ov[4 * u + 1], ov[4 * u + 2], ov[4 * u + 3]);
+          dvp[u] = make_uint4(ov[4 * u], ov[4 * u + 1], ov[4 * u + 2], ov[4 * u + 3]);
           dk2[u] = make_uint4(ok2[4 * u], ok2[4 * u + 1], ok2[4 * u + 2], ok2[4 * u + 3]);
         }
       }
@@ -534,10 +535,11 @@ cudaError_t launch(const Problem& p, const void* Q, const void* K, const void* V
                    const float* lse, void* dQ, void* dK, void* dV, float4* ws, int passes, cudaStream_t st) {
   alignas(64) CUtensorMap q128, do128, k64, v64, k128, v128, q64, do64, s64;
   const int64_t N = p.N, BH = p.BH, Np = (p.N + 1) & ~static_cast<int64_t>(1);
-  if (!make_tmap_bf16(&q128, Q, N, D, BH, BM) || !make_tmap_bf16(&do128, dO, N, D, BH, BM) ||
-      !make_tmap_bf16(&k64, K, N, D, p.BHkv, BN) || !make_tmap_bf16(&v64, V, N, D, p.BHkv, BN) ||
-      !make_tmap_bf16(&k128, K, N, D, p.BHkv, BM) || !make_tmap_bf16(&v128, V, N, D, p.BHkv, BM) ||
-      !make_tmap_bf16(&q64, Q, N, D, BH, BN) || !make_tmap_bf16(&do64, dO, N, D, BH, BN) ||
+  const int64_t d = p.d;  // <= D; TMA zero-fills the padding columns d .. D-1
+  if (!make_tmap_bf16(&q128, Q, N, d, BH, BM) || !make_tmap_bf16(&do128, dO, N, d, BH, BM) ||
+      !make_tmap_bf16(&k64, K, N, d, p.BHkv, BN) || !make_tmap_bf16(&v64, V, N, d, p.BHkv, BN) ||
+      !make_tmap_bf16(&k128, K, N, d, p.BHkv, BM) || !make_tmap_bf16(&v128, V, N, d, p.BHkv, BM) ||
+      !make_tmap_bf16(&q64, Q, N, d, BH, BN) || !make_tmap_bf16(&do64, dO, N, d, BH, BN) ||
       !make_tmap_stats(&s64, ws, Np, BH, BN))
     return cudaErrorInvalidValue;
   const float c = p.scale * kLog2e;
@@ -550,7 +552,7 @@ cudaError_t launch(const Problem& p, const void* Q, const void* K, const void* V
     kern<<<static_cast<unsigned>(nrb * BH), kThreads, Lay::bytes, st>>>(
         q128, do128, k64, v64, static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), lse,
         static_cast<__nv_bfloat16*>(dQ), ws, static_cast<int>(N), static_cast<int>(Np), nrb, static_cast<int>(BH),
-        p.scale, c, p.causal, p.group);
+        p.scale, c, p.causal, p.group, static_cast<int>(d));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (passes & 2) {
@@ -560,7 +562,7 @@ cudaError_t launch(const Problem& p, const void* Q, const void* K, const void* V
     if (e != cudaSuccess) return e;
     kern<<<static_cast<unsigned>(nrb * p.BHkv), kThreads, Lay::bytes, st>>>(
         k128, v128, q64, do64, s64, static_cast<__nv_bfloat16*>(dK), static_cast<__nv_bfloat16*>(dV),
-        static_cast<int>(N), static_cast<int>(p.BHkv), p.scale, c, p.causal, p.group);
+        static_cast<int>(N), static_cast<int>(p.BHkv), p.scale, c, p.causal, p.group, static_cast<int>(d));
     return cudaGetLastError();
   }
   return cudaSuccess;
@@ -571,7 +573,8 @@ cudaError_t launch(const Problem& p, const void* Q, const void* K, const void* V
 cudaError_t tc_bwd(const Problem& p, const void* Q, const void* K, const void* V, const void* O, const void* dO,
                    const float* lse, void* dQ, void* dK, void* dV, int gproj, float4* ws, int passes,
                    cudaStream_t st) {
-  if (p.d == 64)
+  // d = 32 runs the d = 64 kernels and d = 96 the d = 128 ones, zero-padded in shared memory.
+  if (p.d <= 64)
     return gproj ? launch<64, 2, 1, true>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st)
                  : tc_bwd_wide(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st);
   return gproj ? launch<128, 1, 1, true>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st)

@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                const __nv_bfloat16* __restrict__ O, const __nv_bfloat16* __restrict__ dO,
                const float* __restrict__ lse, __nv_bfloat16* __restrict__ dQ, float4* __restrict__ ws, int N, int Np,
-               int nrb, int BH, float scale, float c, int causal, int G) {
+               int nrb, int BH, float scale, float c, int causal, int G, int dv) {
   using Lay = RowLay;
   extern __shared__ __align__(1024) uint8_t sm[];
   Sync sy(sm + Lay::oBar);
@@ -190,9 +190,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lo = static_cast<uint32_t>(qd * 32) << 16;
     const int64_t row = static_cast<int64_t>(rb) * BW + r;
     const bool live = row < N;
-    const size_t rowoff = (static_cast<size_t>(bh) * N + row) * D;
+    const size_t rowoff = (static_cast<size_t>(bh) * N + row) * dv;  // rows of dv <= D columns
     float part = 0.f;
-    if (live) {  // this thread's quarter of D_r = dO_r . O_r
+    if (live && cg * DG < dv) {  // this thread's quarter of D_r = dO_r . O_r (none in the padding)
       const uint4* po = reinterpret_cast<const uint4*>(O + rowoff + cg * DG);
       const uint4* pg = reinterpret_cast<const uint4*>(dO + rowoff + cg * DG);
 #pragma unroll
@@ -250,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t a[DG];
     ptx::tmem_ld16(tmem + Lay::cdQ + cg * DG + lo, a);
     ptx::tmem_wait_ld();
-    if (live) {
+    if (live && cg * DG < dv) {
       uint32_t o[DG / 2];
 #pragma unroll
       for (int t = 0; t < DG; t += 2) o[t >> 1] = ptx::pack_bf16(scale * tc::f(a[t]), scale * tc::f(a[t + 1]));
@@ -294,7 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bwd_col_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                const __grid_constant__ CUtensorMap tmSt, __nv_bfloat16* __restrict__ dK,
-               __nv_bfloat16* __restrict__ dV, int N, int nb, int BHkv, float scale, float c, int causal, int G) {
+               __nv_bfloat16* __restrict__ dV, int N, int nb, int BHkv, float scale, float c, int causal, int G,
+               int dv) {
   using Lay = ColLay;
   extern __shared__ __align__(1024) uint8_t sm[];
   Sync sy(sm + Lay::oBar);
@@ -465,18 +466,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tmem_ld16(tmem + Lay::cdV + cg * DG + lo, a);
     ptx::tmem_ld16(tmem + Lay::cdK + cg * DG + lo, g);
     ptx::tmem_wait_ld();
-    if (key < N) {
-      const size_t rowoff = (static_cast<size_t>(kvh) * N + key) * D;
+    if (key < N && cg * DG < dv) {
+      const size_t rowoff = (static_cast<size_t>(kvh) * N + key) * dv;
       uint32_t ov[DG / 2], okk[DG / 2];
 #pragma unroll
       for (int u = 0; u < DG; u += 2) {
         ov[u >> 1] = ptx::pack_bf16(tc::f(a[u]), tc::f(a[u + 1]));
         okk[u >> 1] = ptx::pack_bf16(scale * tc::f(g[u]), scale * tc::f(g[u + 1]));
       }
-      uint4* dv = reinterpret_cast<uint4*>(dV + rowoff + cg * DG);
+      uint4* dvp = reinterpret_cast<uint4*>(dV + rowoff + cg * DG);
       uint4* dk2 = reinterpret_cast<uint4*>(dK + rowoff + cg * DG);
-      dv[0] = make_uint4(ov[0], ov[1], ov[2], ov[3]);
-      dv[1] = make_uint4(ov[4], ov[5], ov[6], ov[7]);
+      dvp[0] = make_uint4(ov[0], ov[1], ov[2], ov[3]);
+      dvp[1] = make_uint4(ov[4], ov[5], ov[6], ov[7]);
       dk2[0] = make_uint4(okk[0], okk[1], okk[2], okk[3]);
       dk2[1] = make_uint4(okk[4], okk[5], okk[6], okk[7]);
     }
@@ -495,11 +496,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 cudaError_t tc_bwd_wide(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
                         const void* dO, const float* lse, void* dQ, void* dK, void* dV, float4* ws, int passes,
                         cudaStream_t st) {
-  if (p.d != D) return cudaErrorInvalidValue;
+  if (p.d > D) return cudaErrorInvalidValue;
   alignas(64) CUtensorMap q, g, k, v, s;
-  const int64_t N = p.N, BH = p.BH, Np = (p.N + 1) & ~static_cast<int64_t>(1);
-  if (!make_tmap_bf16(&q, Q, N, D, BH, BW) || !make_tmap_bf16(&g, dO, N, D, BH, BW) ||
-      !make_tmap_bf16(&k, K, N, D, p.BHkv, BW) || !make_tmap_bf16(&v, V, N, D, p.BHkv, BW) ||
+  const int64_t N = p.N, BH = p.BH, Np = (p.N + 1) & ~static_cast<int64_t>(1), d = p.d;
+  // Tensor maps over the true head dim d <= D: TMA zero-fills the padding columns.
+  if (!make_tmap_bf16(&q, Q, N, d, BH, BW) || !make_tmap_bf16(&g, dO, N, d, BH, BW) ||
+      !make_tmap_bf16(&k, K, N, d, p.BHkv, BW) || !make_tmap_bf16(&v, V, N, d, p.BHkv, BW) ||
       !make_tmap_stats(&s, ws, Np, BH, BW))
     return cudaErrorInvalidValue;
   const float c = p.scale * kLog2e;
@@ -511,7 +513,7 @@ cudaError_t tc_bwd_wide(const Problem& p, const void* Q, const void* K, const vo
     bwd_row_wide_kernel<<<static_cast<unsigned>(nb * BH), kThreads, RowLay::bytes, st>>>(
         q, g, k, v, static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), lse,
         static_cast<__nv_bfloat16*>(dQ), ws, static_cast<int>(N), static_cast<int>(Np), nb, static_cast<int>(BH),
-        p.scale, c, p.causal, p.group);
+        p.scale, c, p.causal, p.group, static_cast<int>(d));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (passes & 2) {
@@ -520,7 +522,7 @@ cudaError_t tc_bwd_wide(const Problem& p, const void* Q, const void* K, const vo
     if (e != cudaSuccess) return e;
     kern<<<static_cast<unsigned>(nb * p.BHkv), kThreads, ColLay::bytes, st>>>(
         k, v, q, g, s, static_cast<__nv_bfloat16*>(dK), static_cast<__nv_bfloat16*>(dV), static_cast<int>(N), nb,
-        static_cast<int>(p.BHkv), p.scale, c, p.causal, p.group);
+        static_cast<int>(p.BHkv), p.scale, c, p.causal, p.group, static_cast<int>(d));
     e = cudaGetLastError();
   }
   return e;

@@ -68,7 +68,7 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O, float* __restrict__ lse,
-               int N, int nrb, int BH, float scale, float scale_log2, int causal, int G) {
+               int N, int nrb, int BH, float scale, float scale_log2, int causal, int G, int dv) {
   using Lay = Layout<D>;
   extern __shared__ __align__(1024) uint8_t sm[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Lay::oBar);
@@ -267,12 +267,12 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
       uint32_t v[32];
       ptx::tmem_ld32(tO + lane_off + ch * 32, v);
       ptx::tmem_wait_ld();
-      if (row < N) {
+      if (row < N && ch * 32 < dv) {  // columns past the head dim dv are padding
         uint32_t pk[16];
 #pragma unroll
         for (int t = 0; t < 32; t += 2)
           pk[t >> 1] = ptx::pack_bf16(__uint_as_float(v[t]) * inv, __uint_as_float(v[t + 1]) * inv);
-        uint4* dst = reinterpret_cast<uint4*>(O + (static_cast<int64_t>(bh) * N + row) * D + ch * 32);
+        uint4* dst = reinterpret_cast<uint4*>(O + (static_cast<int64_t>(bh) * N + row) * dv + ch * 32);
 #pragma unroll
         for (int u = 0; u < 4; ++u) dst[u] = make_uint4(pk[u * 4], pk[u * 4 + 1], pk[u * 4 + 2], pk[u * 4 + 3]);
       }
@@ -292,8 +292,10 @@ template <int D>
 cudaError_t launch(const Problem& p, const void* Q, const void* K, const void* V, void* O, float* lse,
                    cudaStream_t st) {
   alignas(64) CUtensorMap mq, mk, mv;
-  if (!make_tmap_bf16(&mq, Q, p.N, D, p.BH, BM) || !make_tmap_bf16(&mk, K, p.N, D, p.BHkv, BN) ||
-      !make_tmap_bf16(&mv, V, p.N, D, p.BHkv, BN))
+  // Tensor maps over the true head dim p.d (<= D): TMA zero-fills columns p.d .. D-1,
+  // which add nothing to any product.
+  if (!make_tmap_bf16(&mq, Q, p.N, p.d, p.BH, BM) || !make_tmap_bf16(&mk, K, p.N, p.d, p.BHkv, BN) ||
+      !make_tmap_bf16(&mv, V, p.N, p.d, p.BHkv, BN))
     return cudaErrorInvalidValue;
   const int nrb = static_cast<int>((p.N + BM - 1) / BM);
   const size_t smem = Layout<D>::bytes;
@@ -303,7 +305,7 @@ cudaError_t launch(const Problem& p, const void* Q, const void* K, const void* V
   const float log2e = 1.4426950408889634f;
   fwd_kernel<D><<<static_cast<unsigned>(nrb * p.BH), kThreads, smem, st>>>(
       mq, mk, mv, static_cast<__nv_bfloat16*>(O), lse, static_cast<int>(p.N), nrb, static_cast<int>(p.BH),
-      p.scale, p.scale * log2e, p.causal, p.group);
+      p.scale, p.scale * log2e, p.causal, p.group, static_cast<int>(p.d));
   return cudaGetLastError();
 }
 
@@ -311,7 +313,8 @@ cudaError_t launch(const Problem& p, const void* Q, const void* K, const void* V
 
 cudaError_t tc_fwd(const Problem& p, const void* Q, const void* K, const void* V, void* O, float* lse,
                    cudaStream_t st) {
-  return p.d == 64 ? launch<64>(p, Q, K, V, O, lse, st) : launch<128>(p, Q, K, V, O, lse, st);
+  // d = 32 runs the d = 64 kernel and d = 96 the d = 128 one, zero-padded in shared memory.
+  return p.d <= 64 ? launch<64>(p, Q, K, V, O, lse, st) : launch<128>(p, Q, K, V, O, lse, st);
 }
 
 uint32_t tc_fwd_take_error() {

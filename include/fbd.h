@@ -34,11 +34,13 @@
  *               256}; dtype in {ATTN_F32, ATTN_BF16}.  Anything else returns
  *               ATTN_ERR_UNSUPPORTED before any launch.
  *   Kernels:    the shape decides, never a failure: bf16 attn_fwd, attn_bwd and
- *               attn_bob at d in {64, 128} run on the tcgen05/TMA tensor-core
- *               kernels; every other (dtype, d) runs on the CUDA-core
- *               kernels (fp32 arithmetic; bf16 inputs widened on load, outputs
- *               rounded once on store), which are exact to fp32 rounding but one to
- *               two orders of magnitude slower.
+ *               attn_bob at d in {32, 64, 96, 128} run on the tcgen05/TMA
+ *               tensor-core kernels (d = 32 and 96 on those of d = 64 and 128, the
+ *               head dim zero-padded in shared memory); float32 inputs at every d
+ *               and bf16 at d = 256 run on the CUDA-core kernels (fp32 arithmetic;
+ *               bf16 inputs widened on load, outputs rounded once on store), which
+ *               are exact to fp32 rounding but one to two orders of magnitude
+ *               slower.
  *   Scale:      desc->scale == 0 means 1/sqrt(d); otherwise it must be finite and
  *               positive (the row max is subtracted before scaling).
  *   Pointers:   device pointers, 16-byte aligned (ATTN_ERR_ALIGNMENT otherwise),

@@ -467,3 +467,16 @@ def test_bob_head_dim_128_passes_compose_on_nan_workspace():
     fbd.attn_device_status()
     for a, b in zip(outs, ref):
         assert torch.equal(a, b)
+
+
+# Head dims 32 and 96 on the tensor-core kernels of d = 64 and 128, the head dim
+# zero-padded in shared memory: several row and key blocks and a ragged tail.
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("d", [32, 96])
+def test_padded_head_dims_bf16(d, causal):
+    w = W.Workload(f"padded_B2H4N1000d{d}_bf16", 2, 4, 1000, d, "bf16")
+    got = run_ops(w, to_device(inputs(w), w), ops=("bwd", "bob"), causal=causal)
+    errs = check_full(w, got, ("bwd", "bob"), causal=causal)
+    got1 = run_ops(w, to_device(inputs(w), w), ops=("bwd",), gproj=1, causal=causal)
+    errs1 = check_full(w, got1, ("bwd",), causal=causal)
+    print(w.name, causal, {k: f"{v:.2e}" for k, v in errs.items()}, "gproj dQ", f"{errs1['dQ']:.2e}")
