@@ -2,7 +2,7 @@
 on one batch of synthetic inputs, through the C ABI of libfbd.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--n-seq S] [--batch B] [--heads H] [--group G] [--gproj 0|1] [--causal 0|1]
+                  [--n-seq S] [--batch B] [--heads H] [--head-dim D] [--group G] [--gproj 0|1] [--causal 0|1]
 
 Workload: the GPT-2 Small layer shape at N = 8192 (B=4, H=12, d=64, causal, bf16
 inputs, fp32 accumulation), the shape the throughput targets are stated on.
@@ -41,6 +41,19 @@ KERNELS = ("fwd", "bwd_row", "bwd_col", "bob_row", "bob_col")
 # counted) and what the kernel executes.  Flops = 2 x count x B H N^2 d / 2.
 DENSE_CONTRACTIONS = {"fwd": 2, "bwd_row": 3, "bwd_col": 2, "bob_row": 9, "bob_col": 3}
 EXECUTED_CONTRACTIONS = {"fwd": 2, "bwd_row": 3, "bwd_col": 4, "bob_row": 11, "bob_col": 8}
+# At 64 < d <= 128 the BoB passes run two CTAs per block (one per output half), both
+# computing the five tile products: 2 x 5 + 6 and 2 x 5 + 3 full-width contractions.
+EXECUTED_CONTRACTIONS_D128 = dict(EXECUTED_CONTRACTIONS, bob_row=16, bob_col=13)
+
+
+def executed_flops(w, kn):
+    """Flops the tensor-core kernel executes: head dims 32 and 96 run zero-padded to
+    64 and 128; None for d = 256 (CUDA-core kernels)."""
+    if w.d > 128:
+        return None
+    pad = 64 if w.d <= 64 else 128
+    table = EXECUTED_CONTRACTIONS if pad == 64 else EXECUTED_CONTRACTIONS_D128
+    return 2 * table[kn] * w.B * w.H * w.N * w.N * pad / (2.0 if CAUSAL else 1.0)
 
 
 def dist_init(world, backend="nccl"):
@@ -491,6 +504,7 @@ def main():
     ap.add_argument("--n-seq", type=int, default=8192)
     ap.add_argument("--batch", type=int, default=4)
     ap.add_argument("--heads", type=int, default=12)
+    ap.add_argument("--head-dim", type=int, default=64, choices=[32, 64, 96, 128, 256])
     ap.add_argument("--group", type=int, default=1,
                     help="query heads per key/value head (grouped-query attention; 1 = multi-head)")
     ap.add_argument("--gproj", type=int, default=0)
@@ -510,15 +524,15 @@ def main():
     args.warmup = max(args.warmup, 3)
     global CAUSAL
     CAUSAL = bool(args.causal)
-    w = W.Workload(f"gpt2small_B{args.batch}H{args.heads}N{args.n_seq}d64" + ("" if CAUSAL else "_noncausal")
-                   + (f"_g{args.group}" if args.group > 1 else ""),
-                   args.batch, args.heads, args.n_seq, 64, "bf16", group=args.group)
+    w = W.Workload(f"gpt2small_B{args.batch}H{args.heads}N{args.n_seq}d{args.head_dim}"
+                   + ("" if CAUSAL else "_noncausal") + (f"_g{args.group}" if args.group > 1 else ""),
+                   args.batch, args.heads, args.n_seq, args.head_dim, "bf16", group=args.group)
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
-    config = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": 64, "causal": CAUSAL, "group": w.group,
+    config = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": CAUSAL, "group": w.group,
               "ops": "fwd + bwd(gproj=%d) + BoB" % args.gproj,
               "l2": "inputs larger than L2 (7 input tensors, %.0f MB in total)"
-                    % (w.rows * 64 * 2 * (3 + 4 / w.group) / 1e6),
+                    % (w.rows * w.d * 2 * (3 + 4 / w.group) / 1e6),
               "parallelism": f"independent replicas x{world}"}
 
     if args.impl == "reference":
@@ -567,7 +581,8 @@ def main():
                 for op in r["per_op"]},
         "kernels": {kn: {"ms": r["per_kernel"][kn],
                          "tflops_dense_share": tf(kernel_flops(w, kn, DENSE_CONTRACTIONS), r["per_kernel"][kn]),
-                         "tflops_executed": tf(kernel_flops(w, kn, EXECUTED_CONTRACTIONS), r["per_kernel"][kn])}
+                         "tflops_executed": (tf(executed_flops(w, kn), r["per_kernel"][kn])
+                                             if executed_flops(w, kn) else None)}
                     for kn in KERNELS},
         "gproj_bwd_ms": {"off": r["bwd_gproj_ms"][0], "on": r["bwd_gproj_ms"][1],
                          "overhead_pct": 100.0 * (r["bwd_gproj_ms"][1] / r["bwd_gproj_ms"][0] - 1.0)},
@@ -575,8 +590,8 @@ def main():
                      "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops"], "traffic": traffic_for(dom, w),
                      "peak_source": pk["source"] + " burst bf16",
                      "achieved_basis": "dense-definition contractions of this kernel / its CUDA-event time",
-                     "executed_frac": tf(kernel_flops(w, dom, EXECUTED_CONTRACTIONS), r["per_kernel"][dom])
-                     / pk["bf16_tflops"]},
+                     "executed_frac": (tf(executed_flops(w, dom), r["per_kernel"][dom]) / pk["bf16_tflops"]
+                                       if executed_flops(w, dom) else None)},
         "e2e": {"value": r["flops_step"] / (r["e2e_ms"] * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["e2e_ms"]},
         "gpu_launches": sum(LAUNCHES_PER_STEP.values()) * args.steps,
