@@ -17,7 +17,7 @@ from ._lib import (ATTN_BF16, ATTN_COL_PASS, ATTN_F32, ATTN_ROW_PASS, AttnDesc, 
 
 __all__ = [
     "attn_fwd", "attn_bwd", "attn_bob", "attn_bwd_passes", "attn_bob_passes", "ATTN_ROW_PASS", "ATTN_COL_PASS", "attn_bwd_workspace_bytes", "attn_bob_workspace_bytes",
-    "attn_bob_static", "attn_bwd_projected_dS", "attn_device_status", "attn_status_string", "attn_version", "make_desc",
+    "attn_bob_static", "attn_bwd_projected_dS", "attn_device_status", "attn_check_wait_timeout", "attn_status_string", "attn_version", "make_desc",
     "FbdError", "AttnDesc", "ATTN_F32", "ATTN_BF16", "lib",
 ]
 
@@ -179,6 +179,12 @@ def attn_device_status(stream=None) -> int:
     """Synchronise the stream; raise FbdError if a device-side wait timed out."""
     _check(lib.attn_device_status(_stream(stream)))
     return 0
+
+
+def attn_check_wait_timeout(stream=None) -> int:
+    """Run the library's failure-detection check (a bounded device wait that is made to
+    give up); returns the status code, ATTN_ERR_TIMEOUT (6) when the path works."""
+    return int(lib.attn_check_wait_timeout(_stream(stream)))
 
 
 def attn_status_string(status: int) -> str:

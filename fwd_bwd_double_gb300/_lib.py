@@ -47,6 +47,7 @@ PROTOTYPES = {
     "attn_bob_static": (ctypes.c_int, [_D] + [_P] * 13 + [_P]),
     "attn_bwd_projected_dS": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, _P]),
     "attn_device_status": (ctypes.c_int, [_P]),
+    "attn_check_wait_timeout": (ctypes.c_int, [_P]),
     "attn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "attn_last_error": (ctypes.c_char_p, []),
     "attn_version": (ctypes.c_char_p, []),

@@ -243,9 +243,16 @@ attn_status_t attn_device_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "CUDA: %s", cudaGetErrorString(e));
   const uint32_t flags = fbd::tc_fwd_take_error() | fbd::tc_bwd_take_error() | fbd::tc_bwd_wide_take_error() |
-                         fbd::tc_bob_take_error() | fbd::tc_bob128_take_error();
+                         fbd::tc_bob_take_error() | fbd::tc_bob128_take_error() | fbd::selftest_take_error();
   if (flags != 0) return fail(ATTN_ERR_TIMEOUT, "a device-side bounded wait gave up%s");
   return ATTN_OK;
+}
+
+attn_status_t attn_check_wait_timeout(void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = fbd::selftest_wait_timeout(st);
+  if (e != cudaSuccess) return launch_status(e);
+  return attn_device_status(stream);
 }
 
 const char* attn_status_string(attn_status_t status) {

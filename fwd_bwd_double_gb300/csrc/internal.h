@@ -62,6 +62,11 @@ uint32_t tc_bwd_take_error();
 uint32_t tc_bwd_wide_take_error();
 uint32_t tc_bob_take_error();
 uint32_t tc_bob128_take_error();
+uint32_t selftest_take_error();
+
+// One CTA whose bounded wait on an mbarrier that nothing completes gives up after
+// 20 ms (selftest.cu): the failure-detection path, exercised without a fault.
+cudaError_t selftest_wait_timeout(cudaStream_t st);
 
 // Record `msg` as the calling thread's attn_last_error() detail; returns s.
 attn_status_t set_last_error(attn_status_t s, const char* msg);

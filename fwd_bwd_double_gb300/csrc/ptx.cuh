@@ -73,10 +73,11 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // any thread of the CTA has aborted, or another CTA has raised the global flag)
 // it sets the abort flag and returns false; callers keep going without waiting,
 // so the kernel always reaches its teardown.
-struct BoundedWait {
+template <uint64_t LimitNs>
+struct BoundedWaitT {
   volatile int* abort_flag;      // shared memory, one per CTA
   unsigned int* global_flag;     // device memory status word of this TU
-  static constexpr uint64_t kLimitNs = 2000000000ull;  // 2 s
+  static constexpr uint64_t kLimitNs = LimitNs;
   static constexpr uint32_t kSuspendNs = 100000u;       // longest suspension per try (100 us)
 
   __device__ __forceinline__ bool operator()(uint64_t* bar, uint32_t parity) const {
@@ -97,6 +98,8 @@ struct BoundedWait {
     }
   }
 };
+// The waits of the attention kernels give up after 2 s.
+using BoundedWait = BoundedWaitT<2000000000ull>;
 
 // ----------------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {

@@ -226,6 +226,14 @@ attn_status_t attn_bwd_projected_dS(const attn_desc_t* desc, const void* Q, cons
  * ATTN_ERR_LAUNCH if the stream holds a CUDA error, else ATTN_OK. */
 attn_status_t attn_device_status(void* stream);
 
+/* Check of the failure-detection path, for tests and health checks.  Launches one
+ * CTA on `stream` whose bounded wait (the kind every tensor-core kernel uses) waits
+ * on a barrier that nothing completes; after 20 ms it gives up, records the timeout
+ * in the library's device status word and returns, without any fault.  Returns
+ * attn_device_status(stream): ATTN_ERR_TIMEOUT when the path works (the status is
+ * then cleared, and the context stays usable), ATTN_ERR_LAUNCH if the launch failed. */
+attn_status_t attn_check_wait_timeout(void* stream);
+
 /* Static description of a status code (never NULL). */
 const char* attn_status_string(attn_status_t status);
 

@@ -74,3 +74,9 @@ def run_ops(w, x_dev, ops=("fwd", "bwd", "bob"), gproj=0, causal=True):
             scale=w.scale, causal=causal)
     fbd.attn_device_status()
     return out
+
+
+def check_tol_fwd(w, O, L, causal=True, tol=2e-2):
+    """Forward outputs against the oracle within the bf16 tolerance."""
+    f = oracle_full(w, "fwd", causal)
+    assert rel_fro(O, f["O"]) <= tol and rel_fro(L, f["L"]) <= tol
