@@ -294,6 +294,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t sv[32], gv[32];
       ptx::tmem_ld32(tmem + Lay::cS + c0 + lo, sv);
       ptx::tmem_ld32(tmem + Lay::cG + c0 + lo, gv);
+      if (j > 0) {  // block j-1's operand stores complete while this block's tiles load
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(ready);
+      }
       ptx::tmem_wait_ld();
       ptx::tc_fence_before();
       ptx::mbar_arrive(consumed_a);  // the MMA warp may now write [H | dP] into the tile region
@@ -356,11 +361,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tmem_st16(tOp + Lay::cP, pP);
       ptx::tmem_st16(tOp + Lay::cPG, pG);
       ptx::tmem_st16(tOp + Lay::cdS, pS);
-      ptx::tmem_st16(tOp + Lay::cW, pW);
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(ready);
+      ptx::tmem_st16(tOp + Lay::cW, pW);  // completed (and `ready` arrived) at the next block's loads
     }
+    ptx::tmem_wait_st();
+    ptx::tc_fence_before();
+    ptx::mbar_arrive(ready);  // the last block's operands
     auto hsum = [](uint64_t x) {
       const float2 v = tc::unpk2(x);
       return v.x + v.y;
@@ -654,6 +659,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t sv[32], gv[32];
       ptx::tmem_ld32(tmem + Lay::cT + c0 + lo, sv);
       ptx::tmem_ld32(tmem + Lay::cT + BN + c0 + lo, gv);
+      if (t > 0) {  // block t-1's operand stores complete while this block's tiles load
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(ready);
+      }
       ptx::tmem_wait_ld();
       ptx::tc_fence_before();
       ptx::mbar_arrive(consumed_a);  // the tile warp may now write [dP^T | H^T]
@@ -705,11 +715,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (t > 0) wait(out_done, (t - 1) & 1);  // block t-1's products have read the operand columns
       ptx::tmem_st16(tOpT, pDP);
       ptx::tmem_st16(tOpT + 32, pDS);
-      ptx::tmem_st16(tOpT + 64, pSB);
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(ready);
+      ptx::tmem_st16(tOpT + 64, pSB);  // completed (and `ready` arrived) at the next block's loads
     }
+    ptx::tmem_wait_st();
+    ptx::tc_fence_before();
+    ptx::mbar_arrive(ready);  // the last block's operands
     wait(acc_full, 0);
     ptx::tc_fence_after();
     uint32_t av[32], bv[32];
