@@ -66,31 +66,33 @@ def test_long_sweep_n4096_all_heads():
     print(w.name, {k: f"{v:.2e}" for k, v in errs.items()})
 
 
-def sampled_check(w, got, ops, heads, rows, cols):
-    """Oracle on sampled rows (row outputs) and columns (column outputs) of given heads."""
+def sampled_check(w, got, ops, heads, rows, cols, batch=0):
+    """Oracle on sampled rows (row outputs) and columns (column outputs) of given heads
+    of one batch entry."""
     tol = TOL[w.dtype]
     errs = {}
-    x = W.inputs(w, heads=heads, batches=[0])
+    x = W.inputs(w, heads=heads, batches=[batch])
     acc = {k: ([], []) for k in ("O", "L", "dQ", "dK", "dV", "gQ", "gK", "gV", "gdO")}
+    b = batch
     for hi, h in enumerate(heads):
         s = {k: v[0, hi].astype(np.float64) for k, v in x.items()}
         O, L = oracle.forward_rows(s["Q"], s["K"], s["V"], rows, scale=w.scale)
-        acc["O"][0].append(host(got["O"][0, h])[rows]); acc["O"][1].append(O)
-        acc["L"][0].append(host(got["L"][0, h])[rows]); acc["L"][1].append(L)
+        acc["O"][0].append(host(got["O"][b, h])[rows]); acc["O"][1].append(O)
+        acc["L"][0].append(host(got["L"][b, h])[rows]); acc["L"][1].append(L)
         if "bwd" in ops:
-            acc["dQ"][0].append(host(got["dQ"][0, h])[rows])
+            acc["dQ"][0].append(host(got["dQ"][b, h])[rows])
             acc["dQ"][1].append(oracle.backward_rows(s["Q"], s["K"], s["V"], s["dO"], rows, scale=w.scale))
             dK, dV = oracle.backward_cols(s["Q"], s["K"], s["V"], s["dO"], cols, scale=w.scale)
-            acc["dK"][0].append(host(got["dK"][0, h])[cols]); acc["dK"][1].append(dK)
-            acc["dV"][0].append(host(got["dV"][0, h])[cols]); acc["dV"][1].append(dV)
+            acc["dK"][0].append(host(got["dK"][b, h])[cols]); acc["dK"][1].append(dK)
+            acc["dV"][0].append(host(got["dV"][b, h])[cols]); acc["dV"][1].append(dV)
         if "bob" in ops:
             r = oracle.bob_rows(s["Q"], s["K"], s["V"], s["dO"], s["gdQ"], s["gdK"], s["gdV"], rows, scale=w.scale)
-            acc["gQ"][0].append(host(got["gQ"][0, h])[rows]); acc["gQ"][1].append(r["gQ"])
-            acc["gdO"][0].append(host(got["gdO"][0, h])[rows]); acc["gdO"][1].append(r["gdO"])
+            acc["gQ"][0].append(host(got["gQ"][b, h])[rows]); acc["gQ"][1].append(r["gQ"])
+            acc["gdO"][0].append(host(got["gdO"][b, h])[rows]); acc["gdO"][1].append(r["gdO"])
             gK, gV = oracle.bob_cols(s["Q"], s["K"], s["V"], s["dO"], s["gdQ"], s["gdK"], s["gdV"], cols,
                                      scale=w.scale)
-            acc["gK"][0].append(host(got["gK"][0, h])[cols]); acc["gK"][1].append(gK)
-            acc["gV"][0].append(host(got["gV"][0, h])[cols]); acc["gV"][1].append(gV)
+            acc["gK"][0].append(host(got["gK"][b, h])[cols]); acc["gK"][1].append(gK)
+            acc["gV"][0].append(host(got["gV"][b, h])[cols]); acc["gV"][1].append(gV)
     for k, (g, r) in acc.items():
         if g:
             errs[k] = rel_fro(np.concatenate(g), np.concatenate(r))
@@ -115,6 +117,20 @@ def test_long_sweep_sampled(N):
     rows, cols = sample_rows_cols(N, np.random.default_rng(N))
     errs = sampled_check(w, got, ("bwd", "bob"), heads=[0, 11], rows=rows, cols=cols)
     print(w.name, {k: f"{v:.2e}" for k, v in errs.items()})
+
+
+@pytest.mark.parametrize("gproj", [0, 1])
+def test_bench_workload_sampled(gproj):
+    """The throughput workload itself (B4 H12 N8192 d64 bf16, the kernels and grids the
+    bench times), sampled rows and late columns of the first and the last batch entry."""
+    w = W.GPT2_N8192
+    x = to_device(W.inputs(w), w)
+    ops = ("bwd", "bob") if gproj == 0 else ("bwd",)
+    got = run_ops(w, x, ops=ops, gproj=gproj)
+    rows, cols = sample_rows_cols(w.N, np.random.default_rng(8192))
+    for b in (0, w.B - 1):
+        errs = sampled_check(w, got, ops, heads=[0, 11], rows=rows, cols=cols, batch=b)
+        print(w.name, gproj, b, {k: f"{v:.2e}" for k, v in errs.items()})
 
 
 def test_full_day_ragged_tail():
