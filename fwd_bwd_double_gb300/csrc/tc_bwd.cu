@@ -577,8 +577,15 @@ cudaError_t tc_bwd(const Problem& p, const void* Q, const void* K, const void* V
   if (p.d <= 64)
     return gproj ? launch<64, 2, 1, true>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st)
                  : tc_bwd_wide(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st);
-  return gproj ? launch<128, 1, 1, true>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st)
-               : launch<128, 2, 1, false>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st);
+  if (gproj) return launch<128, 1, 1, true>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st);
+  // d = 96, 128 without GProj: the 128-wide row pass, then this file's column pass
+  // (both use the same pair-interleaved row statistics).
+  if (passes & 1) {
+    const cudaError_t e = tc_bwd_wide(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, 1, st);
+    if (e != cudaSuccess) return e;
+  }
+  if (!(passes & 2)) return cudaSuccess;
+  return launch<128, 2, 1, false>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, 2, st);
 }
 
 uint32_t tc_bwd_take_error() {

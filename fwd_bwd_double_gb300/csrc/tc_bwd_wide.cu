@@ -1,5 +1,8 @@
-// bf16 causal attention backward, d = 64, no GProj: the row pass (dQ) and the
-// column pass (dK, dV) with 128-wide score tiles.
+// bf16 causal attention backward without GProj, with 128-wide score tiles: the row
+// pass (dQ) at d = 64 and d = 128 (96 zero-padded), the column pass (dK, dV) at
+// d = 64 (at d = 128 its tiles and accumulators would need 640 TMEM columns; the
+// 64-wide column pass of tc_bwd.cu, which reads the same row statistics, runs
+// there).
 //
 // Same mathematics as tc_bwd.cu ("Flash attention for trading models",
 // "Backward pass: recompute instead of store"): P = 2^(S s log2 e - L log2 e),
@@ -43,8 +46,10 @@ constexpr float kLog2e = 1.4426950408889634f;
 using tc::bf16_hi;
 using tc::bf16_lo;
 
-// Shared boilerplate: barriers, TMEM allocation, bounded waits.
-struct Sync {
+// Shared boilerplate: barriers, TMEM allocation, bounded waits (NSX stages).
+template <int NSX>
+struct SyncT {
+  static constexpr int NS = NSX;
   uint64_t* held_full;
   uint64_t* full;
   uint64_t* empty;
@@ -55,7 +60,7 @@ struct Sync {
   uint64_t* acc_full;
   uint32_t* tmem_slot;
   volatile int* abort_flag;
-  __device__ Sync(uint8_t* base) {
+  __device__ SyncT(uint8_t* base) {
     held_full = reinterpret_cast<uint64_t*>(base);
     full = held_full + 1;
     empty = full + NS;
@@ -83,25 +88,35 @@ struct Sync {
     ptx::fence_mbar_init();
   }
 };
+using Sync = SyncT<NS>;
 
 // ================================================================ row pass
+// DR = 64, or 128 (d = 96, 128: the held Q, dO and two 64-column slabs per tile, two
+// stages; TMEM S 128 + dP 128 + dS 64 + dQ 128 = 448 columns).
+template <int DR>
 struct RowLay {
-  static constexpr int oQ = 0, odO = kTile, oK = 2 * kTile, oV = oK + NS * kTile;
-  static constexpr int oRed = oV + NS * kTile;  // float [4][BW]
+  static constexpr int NSR = DR == 64 ? NS : 2;
+  static constexpr int kTileR = BW * DR * 2;
+  static constexpr int DGR = DR / 4;  // dQ columns per compute thread
+  static constexpr int oQ = 0, odO = kTileR, oK = 2 * kTileR, oV = oK + NSR * kTileR;
+  static constexpr int oRed = oV + NSR * kTileR;  // float [4][BW]
   static constexpr int oBar = oRed + 4 * BW * 4;
   static constexpr int bytes = oBar + 256;
   static constexpr int cS = 0, cdP = 128, cdS = 256, cdQ = 320;
 };
+static_assert(RowLay<128>::bytes <= 232448, "row pass shared memory at d = 128");
 
+template <int DR>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_row_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                const __nv_bfloat16* __restrict__ O, const __nv_bfloat16* __restrict__ dO,
                const float* __restrict__ lse, __nv_bfloat16* __restrict__ dQ, float4* __restrict__ ws, int N, int Np,
                int nrb, int BH, float scale, float c, int causal, int G, int dv) {
-  using Lay = RowLay;
+  using Lay = RowLay<DR>;
+  constexpr int NS = Lay::NSR, kTile = Lay::kTileR, DG = Lay::DGR, D = DR;
   extern __shared__ __align__(1024) uint8_t sm[];
-  Sync sy(sm + Lay::oBar);
+  SyncT<NS> sy(sm + Lay::oBar);
   float* red = reinterpret_cast<float*>(sm + Lay::oRed);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const tc::Order ord = tc::grid_order(BH, nrb);
@@ -126,14 +141,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::prefetch_tmap(&tmK);
       ptx::prefetch_tmap(&tmV);
       ptx::mbar_expect_tx(sy.held_full, 2 * kTile);
-      ptx::tma_load_3d(sm + Lay::oQ, &tmQ, sy.held_full, 0, rb * BW, bh);
-      ptx::tma_load_3d(sm + Lay::odO, &tmdO, sy.held_full, 0, rb * BW, bh);
+      for (int cc = 0; cc < D / 64; ++cc) {  // 64-column slabs, BW rows each
+        ptx::tma_load_3d(sm + Lay::oQ + cc * BW * 128, &tmQ, sy.held_full, cc * 64, rb * BW, bh);
+        ptx::tma_load_3d(sm + Lay::odO + cc * BW * 128, &tmdO, sy.held_full, cc * 64, rb * BW, bh);
+      }
       for (int j = 0; j < nkv; ++j) {
         const int s = j % NS;
         if (j >= NS) wait(&sy.empty[s], ((j / NS) - 1) & 1);
         ptx::mbar_expect_tx(&sy.full[s], 2 * kTile);
-        ptx::tma_load_3d(sm + Lay::oK + s * kTile, &tmK, &sy.full[s], 0, j * BW, bh / G);
-        ptx::tma_load_3d(sm + Lay::oV + s * kTile, &tmV, &sy.full[s], 0, j * BW, bh / G);
+        for (int cc = 0; cc < D / 64; ++cc) {
+          ptx::tma_load_3d(sm + Lay::oK + s * kTile + cc * BW * 128, &tmK, &sy.full[s], cc * 64, j * BW, bh / G);
+          ptx::tma_load_3d(sm + Lay::oV + s * kTile + cc * BW * 128, &tmV, &sy.full[s], cc * 64, j * BW, bh / G);
+        }
       }
       for (int j = (nkv > NS ? nkv - NS : 0); j < nkv; ++j) wait(&sy.empty[j % NS], (j / NS) & 1);
     }
@@ -192,11 +211,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool live = row < N;
     const size_t rowoff = (static_cast<size_t>(bh) * N + row) * dv;  // rows of dv <= D columns
     float part = 0.f;
-    if (live && cg * DG < dv) {  // this thread's quarter of D_r = dO_r . O_r (none in the padding)
+    if (live) {  // this thread's quarter of D_r = dO_r . O_r (none in the padding)
       const uint4* po = reinterpret_cast<const uint4*>(O + rowoff + cg * DG);
       const uint4* pg = reinterpret_cast<const uint4*>(dO + rowoff + cg * DG);
 #pragma unroll
       for (int u = 0; u < DG / 8; ++u) {
+        if (cg * DG + 8 * u >= dv) break;
         const uint4 a = po[u], g = pg[u];
         const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, gw[4] = {g.x, g.y, g.z, g.w};
 #pragma unroll
@@ -248,15 +268,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     wait(sy.acc_full, 0);
     ptx::tc_fence_after();
     uint32_t a[DG];
-    ptx::tmem_ld16(tmem + Lay::cdQ + cg * DG + lo, a);
+    if constexpr (DG == 16)
+      ptx::tmem_ld16(tmem + Lay::cdQ + cg * DG + lo, a);
+    else
+      ptx::tmem_ld32(tmem + Lay::cdQ + cg * DG + lo, a);
     ptx::tmem_wait_ld();
-    if (live && cg * DG < dv) {
-      uint32_t o[DG / 2];
 #pragma unroll
-      for (int t = 0; t < DG; t += 2) o[t >> 1] = ptx::pack_bf16(scale * tc::f(a[t]), scale * tc::f(a[t + 1]));
-      uint4* dst = reinterpret_cast<uint4*>(dQ + rowoff + cg * DG);
-      dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-      dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    for (int q = 0; q < DG / 16; ++q) {  // runs of 16 columns; none of them in the padding past dv
+      if (live && cg * DG + q * 16 < dv) {
+        uint32_t o[8];
+#pragma unroll
+        for (int t = 0; t < 16; t += 2)
+          o[t >> 1] = ptx::pack_bf16(scale * tc::f(a[q * 16 + t]), scale * tc::f(a[q * 16 + t + 1]));
+        uint4* dst = reinterpret_cast<uint4*>(dQ + rowoff + cg * DG + q * 16);
+        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+      }
     }
     if (cg == 0 && row < Np) {  // row statistics, negated, pair-interleaved (format shared with tc_bwd.cu)
       // The row past N of an odd-length slice gets zeros: the column pass reads it (with P = 0).
@@ -496,7 +523,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 cudaError_t tc_bwd_wide(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
                         const void* dO, const float* lse, void* dQ, void* dK, void* dV, float4* ws, int passes,
                         cudaStream_t st) {
-  if (p.d > D) return cudaErrorInvalidValue;
+  if (p.d > 64) {  // d = 96, 128: the row pass only (the column pass would need 640 TMEM columns)
+    if (p.d > 128 || (passes & 2)) return cudaErrorInvalidValue;
+    alignas(64) CUtensorMap q, g, k, v;
+    const int64_t N = p.N, BH = p.BH, Np = (p.N + 1) & ~static_cast<int64_t>(1), d = p.d;
+    if (!make_tmap_bf16(&q, Q, N, d, BH, BW) || !make_tmap_bf16(&g, dO, N, d, BH, BW) ||
+        !make_tmap_bf16(&k, K, N, d, p.BHkv, BW) || !make_tmap_bf16(&v, V, N, d, p.BHkv, BW))
+      return cudaErrorInvalidValue;
+    const int nb = static_cast<int>((N + BW - 1) / BW);
+    cudaError_t e = cudaFuncSetAttribute(bwd_row_wide_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         RowLay<128>::bytes);
+    if (e != cudaSuccess) return e;
+    bwd_row_wide_kernel<128><<<static_cast<unsigned>(nb * BH), kThreads, RowLay<128>::bytes, st>>>(
+        q, g, k, v, static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), lse,
+        static_cast<__nv_bfloat16*>(dQ), ws, static_cast<int>(N), static_cast<int>(Np), nb, static_cast<int>(BH),
+        p.scale, p.scale * kLog2e, p.causal, p.group, static_cast<int>(d));
+    return cudaGetLastError();
+  }
   alignas(64) CUtensorMap q, g, k, v, s;
   const int64_t N = p.N, BH = p.BH, Np = (p.N + 1) & ~static_cast<int64_t>(1), d = p.d;
   // Tensor maps over the true head dim d <= D: TMA zero-fills the padding columns.
@@ -508,9 +551,10 @@ cudaError_t tc_bwd_wide(const Problem& p, const void* Q, const void* K, const vo
   const int nb = static_cast<int>((N + BW - 1) / BW);
   cudaError_t e = cudaSuccess;
   if (passes & 1) {
-    e = cudaFuncSetAttribute(bwd_row_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, RowLay::bytes);
+    e = cudaFuncSetAttribute(bwd_row_wide_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             RowLay<64>::bytes);
     if (e != cudaSuccess) return e;
-    bwd_row_wide_kernel<<<static_cast<unsigned>(nb * BH), kThreads, RowLay::bytes, st>>>(
+    bwd_row_wide_kernel<64><<<static_cast<unsigned>(nb * BH), kThreads, RowLay<64>::bytes, st>>>(
         q, g, k, v, static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), lse,
         static_cast<__nv_bfloat16*>(dQ), ws, static_cast<int>(N), static_cast<int>(Np), nb, static_cast<int>(BH),
         p.scale, c, p.causal, p.group, static_cast<int>(d));
