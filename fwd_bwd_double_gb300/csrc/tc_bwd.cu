@@ -332,14 +332,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tmSt, __nv_bfloat16* __restrict__ dK,
                    __nv_bfloat16* __restrict__ dV, int N, int BHkv, float scale, float c, int causal, int G, int dv) {
   using Lay = ColLay<D, NB, GP>;
+  static_assert(NB == 1, "one score-tile buffer, released early");
   constexpr int NS = Lay::NS;
   extern __shared__ __align__(1024) uint8_t sm[];
   uint64_t* k_full = reinterpret_cast<uint64_t*>(sm + Lay::oBar);
   uint64_t* full = k_full + 1;
   uint64_t* empty = full + NS;
   uint64_t* s_full = empty + NS;
-  uint64_t* ds_ready = s_full + NB;
-  uint64_t* acc_full = ds_ready + NB;
+  uint64_t* ds_ready = s_full + NB;     // P, dS (and the GProj operand) of the block in TMEM
+  uint64_t* consumed = ds_ready + NB;   // the block's S^T, dP^T copied out: the tile columns are free
+  uint64_t* out_done = consumed + 1;    // the block's dV, dK products have read the operand columns
+  uint64_t* acc_full = out_done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -363,6 +366,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&s_full[b], 1);
       ptx::mbar_init(&ds_ready[b], kCompute);
     }
+    ptx::mbar_init(consumed, kCompute);
+    ptx::mbar_init(out_done, 1);
     ptx::mbar_init(acc_full, 1);
     *abort_flag = (ptx::smem_u32(sm) & 1023u) ? 1 : 0;
     if (*abort_flag) atomicOr(&g_err, FBD_ERR_TIMEOUT);
@@ -421,12 +426,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (GP) ptx::mma_ts_e(tmem + Lay::cdK, tmem + Lay::cG + b * (BN / 2) + k * 8, bq, idKV, 1u);
         }
         ptx::mma_commit_e(&empty[s]);
+        ptx::mma_commit_e(out_done);
       };
+      // Block t's tiles go into the columns block t-1's tiles left as soon as the
+      // compute warps have copied those out (`consumed`), ahead of block t-1's products.
       wait(k_full, 0);
       for (int t = 0; t < nt; ++t) {
         const int s = t % NS, b = t % NB;
         wait(&full[s], (t / NS) & 1);
-        if (t >= NB) products(t - NB);
+        if (t > 0) wait(consumed, (t - 1) & 1);
         ptx::tc_fence_after();
         const uint32_t qt = sQ + s * Lay::kStream, gt = sdO + s * Lay::kStream;
 #pragma unroll
@@ -437,8 +445,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::mma_ss_e(tmem + Lay::cdP + b * BN, tc::kmajor_desc(sV, BM, kk), tc::kmajor_desc(gt, BN, kk), idS,
                       kk > 0);
         ptx::mma_commit_e(&s_full[b]);
+        if (t > 0) products(t - 1);
       }
-      for (int t = (nt > NB ? nt - NB : 0); t < nt; ++t) products(t);
+      if (nt > 0) products(nt - 1);
       ptx::mma_commit_e(acc_full);
     }
   } else {
@@ -456,6 +465,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tmem_ld32(tmem + Lay::cS + b * BN + c0 + lo, sv);
       ptx::tmem_ld32(tmem + Lay::cdP + b * BN + c0 + lo, pv);
       ptx::tmem_wait_ld();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(consumed);  // the MMA warp may now compute the next block's tiles here
       // Row statistics of the 64 queries, pair-interleaved: float4 2m = (-L2, -L2', -D, -D'),
       // float4 2m+1 = (-rho, -rho', 0, 0) of queries 2m, 2m+1 of the block.
       const float4* st = reinterpret_cast<const float4*>(sm + Lay::oSt + s * Lay::kStat) + c0;
@@ -487,6 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         block(std::true_type{});
       else
         block(std::false_type{});
+      if (t > 0) wait(out_done, (t - 1) & 1);  // block t-1's products have read P, dS
       ptx::tmem_st16(tmem + Lay::cP + b * (BN / 2) + c0 / 2 + lo, pk);
       ptx::tmem_st16(tmem + Lay::cdS + b * (BN / 2) + c0 / 2 + lo, dk);
       if constexpr (GP) ptx::tmem_st16(tmem + Lay::cG + b * (BN / 2) + c0 / 2 + lo, gk);
