@@ -38,10 +38,11 @@ cudaError_t tc_fwd(const Problem& p, const void* Q, const void* K, const void* V
 cudaError_t tc_bwd(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
                    const void* dO, const float* lse, void* dQ, void* dK, void* dV, int gproj, float4* ws,
                    int passes, cudaStream_t st);
-// d = 64 without GProj: the 128-wide backward kernels (tc_bwd_wide.cu).
+// The 128-wide backward kernels (tc_bwd_wide.cu): both passes at d <= 64 without
+// GProj; the row pass alone at d <= 64 with GProj and at 64 < d <= 128 without.
 cudaError_t tc_bwd_wide(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
                         const void* dO, const float* lse, void* dQ, void* dK, void* dV, float4* ws, int passes,
-                        cudaStream_t st);
+                        cudaStream_t st, bool gproj = false);
 cudaError_t tc_bob(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
                    const void* dO, const float* lse, const void* a, const void* b, const void* c, void* gQ,
                    void* gK, void* gV, void* gdO, float4* ws, int passes, cudaStream_t st);

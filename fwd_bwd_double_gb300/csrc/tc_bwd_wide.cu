@@ -93,27 +93,33 @@ using Sync = SyncT<NS>;
 // ================================================================ row pass
 // DR = 64, or 128 (d = 96, 128: the held Q, dO and two 64-column slabs per tile, two
 // stages; TMEM S 128 + dP 128 + dS 64 + dQ 128 = 448 columns).
-template <int DR>
+// GP (d = 64 only): GProj.  The bf16 P^ fed to a second output product P^ K (TMEM
+// P^ 64 + PK 64 columns: 512 in all) and the row sums of dS^ and P^ give
+// rho = sum dS^ / sum P^ and dQ = s (dS^ K - rho P^ K), the product of the projected
+// row ("FlashAttention bf16 gradient and GProj", "How the zero sum turns into a
+// false gradient"); -rho goes to the row statistics for the column pass.
+template <int DR, bool GP = false>
 struct RowLay {
+  static_assert(!GP || DR == 64, "GProj rows at d = 64 only (TMEM)");
   static constexpr int NSR = DR == 64 ? NS : 2;
   static constexpr int kTileR = BW * DR * 2;
   static constexpr int DGR = DR / 4;  // dQ columns per compute thread
   static constexpr int oQ = 0, odO = kTileR, oK = 2 * kTileR, oV = oK + NSR * kTileR;
-  static constexpr int oRed = oV + NSR * kTileR;  // float [4][BW]
-  static constexpr int oBar = oRed + 4 * BW * 4;
+  static constexpr int oRed = oV + NSR * kTileR;  // float [4][BW]: D; with GProj [12][BW]: and the sums of dS^, P^
+  static constexpr int oBar = oRed + (GP ? 12 : 4) * BW * 4;
   static constexpr int bytes = oBar + 256;
-  static constexpr int cS = 0, cdP = 128, cdS = 256, cdQ = 320;
+  static constexpr int cS = 0, cdP = 128, cdS = 256, cP = 320, cdQ = GP ? 384 : 320, cPK = cdQ + DR;
 };
 static_assert(RowLay<128>::bytes <= 232448, "row pass shared memory at d = 128");
 
-template <int DR>
+template <int DR, bool GP>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_row_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                const __nv_bfloat16* __restrict__ O, const __nv_bfloat16* __restrict__ dO,
                const float* __restrict__ lse, __nv_bfloat16* __restrict__ dQ, float4* __restrict__ ws, int N, int Np,
                int nrb, int BH, float scale, float c, int causal, int G, int dv) {
-  using Lay = RowLay<DR>;
+  using Lay = RowLay<DR, GP>;
   constexpr int NS = Lay::NSR, kTile = Lay::kTileR, DG = Lay::DGR, D = DR;
   extern __shared__ __align__(1024) uint8_t sm[];
   SyncT<NS> sy(sm + Lay::oBar);
@@ -188,16 +194,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {  // all 32 lanes; one elected lane issues each MMA and commit
       constexpr uint32_t idQ = ptx::idesc_bf16(BW, D, 0, 1);
       const uint64_t dKm = tc::mnmajor_desc(ptx::smem_u32(sm + Lay::oK), BW, 0);
-      const uint32_t tdQ = tmem + Lay::cdQ, tdS = tmem + Lay::cdS;
-      for (int t = 0; t < nkv; ++t) {  // dQ += dS_t K_t, then release the stage and the dS columns
+      const uint32_t tdQ = tmem + Lay::cdQ, tdS = tmem + Lay::cdS, tP = tmem + Lay::cP, tPK = tmem + Lay::cPK;
+      for (int t = 0; t < nkv; ++t) {  // dQ += dS_t K_t (PK += P_t K_t), then release the stage and the operands
         const int s = t % NS;
         wait(sy.ready, t & 1);
         wait(&sy.full[s], (t / NS) & 1);  // already complete: the stage cannot refill before this warp releases it
         ptx::tc_fence_after();
         const uint32_t so = static_cast<uint32_t>(s * kTile);
 #pragma unroll
-        for (int k = 0; k < BW / 16; ++k)
+        for (int k = 0; k < BW / 16; ++k) {
           ptx::mma_ts_e(tdQ, tdS + k * 8, tc::desc_add(dKm, so + 2048 * k), idQ, (t > 0 || k > 0));
+          if constexpr (GP) ptx::mma_ts_e(tPK, tP + k * 8, tc::desc_add(dKm, so + 2048 * k), idQ, (t > 0 || k > 0));
+        }
         ptx::mma_commit_e(&sy.empty[s]);
         ptx::mma_commit_e(sy.out_done);
       }
@@ -229,6 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float L2 = live ? lse[static_cast<size_t>(bh) * N + row] * kLog2e : 0.f;
     const uint64_t c2 = tc::pk2f(c, c), nL2 = tc::pk2f(-L2, -L2), nD2 = tc::pk2f(-Dr, -Dr);
     const int c0 = cg * kC;
+    uint64_t accR = 0, accP = 0;  // GProj: sums of the bf16 dS and P fed to the products
     for (int j = 0; j < nkv; ++j) {
       wait(sy.s_full, j & 1);
       ptx::tc_fence_after();
@@ -238,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tmem_wait_ld();
       ptx::tc_fence_before();
       ptx::mbar_arrive(sy.consumed);
-      uint32_t dsk[kC / 2];
+      uint32_t dsk[kC / 2], pkk[GP ? kC / 2 : 1];
       const int klim = causal ? r : N - 1 - j * BW;  // last visible key of this row, relative to the block
       auto block = [&](auto masked) {
 #pragma unroll
@@ -253,6 +262,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const float2 ds = tc::unpk2(tc::mul2(tc::pk2f(p0, p1), tc::add2(tc::pk2(pv[t], pv[t + 1]), nD2)));
           dsk[t >> 1] = ptx::pack_bf16(ds.x, ds.y);
+          if constexpr (GP) {
+            pkk[t >> 1] = ptx::pack_bf16(p0, p1);
+            accR = tc::add2(accR, tc::bf2_to_f2(dsk[t >> 1]));
+            accP = tc::add2(accP, tc::bf2_to_f2(pkk[t >> 1]));
+          }
         }
       };
       if (causal ? j == rb : (j == nkv - 1 && (N % BW) != 0))
@@ -261,18 +275,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         block(std::false_type{});
       if (j > 0) wait(sy.out_done, (j - 1) & 1);  // the previous block's dQ product has read dS
       ptx::tmem_st16(tmem + Lay::cdS + c0 / 2 + lo, dsk);
+      if constexpr (GP) ptx::tmem_st16(tmem + Lay::cP + c0 / 2 + lo, pkk);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(sy.ready);
     }
+    float rho = 0.f;
+    if constexpr (GP) {  // rho_r = sum dS^ / sum P^ over the whole row (four column groups)
+      const float2 vr = tc::unpk2(accR), vp = tc::unpk2(accP);
+      red[4 * BW + cg * BW + r] = vr.x + vr.y;
+      red[8 * BW + cg * BW + r] = vp.x + vp.y;
+      tc::named_sync(1, kCompute);
+      rho = (red[4 * BW + r] + red[5 * BW + r] + red[6 * BW + r] + red[7 * BW + r]) /
+            (red[8 * BW + r] + red[9 * BW + r] + red[10 * BW + r] + red[11 * BW + r]);
+    }
     wait(sy.acc_full, 0);
     ptx::tc_fence_after();
-    uint32_t a[DG];
-    if constexpr (DG == 16)
+    uint32_t a[DG], pkv[GP ? DG : 1];
+    if constexpr (DG == 16) {
       ptx::tmem_ld16(tmem + Lay::cdQ + cg * DG + lo, a);
-    else
+      if constexpr (GP) ptx::tmem_ld16(tmem + Lay::cPK + cg * DG + lo, pkv);
+    } else {
       ptx::tmem_ld32(tmem + Lay::cdQ + cg * DG + lo, a);
+    }
     ptx::tmem_wait_ld();
+    if constexpr (GP) {
+#pragma unroll
+      for (int t = 0; t < DG; ++t) a[t] = __float_as_uint(tc::f(a[t]) - rho * tc::f(pkv[t]));
+    }
 #pragma unroll
     for (int q = 0; q < DG / 16; ++q) {  // runs of 16 columns; none of them in the padding past dv
       if (live && cg * DG + q * 16 < dv) {
@@ -292,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int odd = static_cast<int>(row & 1);
       wf[k2 * 4 + odd] = live ? -L2 : 0.f;
       wf[k2 * 4 + 2 + odd] = live ? -Dr : 0.f;
-      wf[(k2 + 1) * 4 + odd] = 0.f;
+      wf[(k2 + 1) * 4 + odd] = live ? -rho : 0.f;
       wf[(k2 + 1) * 4 + 2 + odd] = 0.f;
     }
   }
@@ -522,7 +552,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 cudaError_t tc_bwd_wide(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
                         const void* dO, const float* lse, void* dQ, void* dK, void* dV, float4* ws, int passes,
-                        cudaStream_t st) {
+                        cudaStream_t st, bool gproj) {
+  // GProj: the row pass only (d <= 64; the GProj column pass is tc_bwd.cu's).
+  if (gproj && (p.d > 64 || (passes & 2))) return cudaErrorInvalidValue;
   if (p.d > 64) {  // d = 96, 128: the row pass only (the column pass would need 640 TMEM columns)
     if (p.d > 128 || (passes & 2)) return cudaErrorInvalidValue;
     alignas(64) CUtensorMap q, g, k, v;
@@ -531,10 +563,10 @@ cudaError_t tc_bwd_wide(const Problem& p, const void* Q, const void* K, const vo
         !make_tmap_bf16(&k, K, N, d, p.BHkv, BW) || !make_tmap_bf16(&v, V, N, d, p.BHkv, BW))
       return cudaErrorInvalidValue;
     const int nb = static_cast<int>((N + BW - 1) / BW);
-    cudaError_t e = cudaFuncSetAttribute(bwd_row_wide_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         RowLay<128>::bytes);
+    cudaError_t e = cudaFuncSetAttribute(bwd_row_wide_kernel<128, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, RowLay<128>::bytes);
     if (e != cudaSuccess) return e;
-    bwd_row_wide_kernel<128><<<static_cast<unsigned>(nb * BH), kThreads, RowLay<128>::bytes, st>>>(
+    bwd_row_wide_kernel<128, false><<<static_cast<unsigned>(nb * BH), kThreads, RowLay<128>::bytes, st>>>(
         q, g, k, v, static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), lse,
         static_cast<__nv_bfloat16*>(dQ), ws, static_cast<int>(N), static_cast<int>(Np), nb, static_cast<int>(BH),
         p.scale, p.scale * kLog2e, p.causal, p.group, static_cast<int>(d));
@@ -551,10 +583,11 @@ cudaError_t tc_bwd_wide(const Problem& p, const void* Q, const void* K, const vo
   const int nb = static_cast<int>((N + BW - 1) / BW);
   cudaError_t e = cudaSuccess;
   if (passes & 1) {
-    e = cudaFuncSetAttribute(bwd_row_wide_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             RowLay<64>::bytes);
+    auto row = gproj ? bwd_row_wide_kernel<64, true> : bwd_row_wide_kernel<64, false>;
+    const int bytes = gproj ? RowLay<64, true>::bytes : RowLay<64, false>::bytes;
+    e = cudaFuncSetAttribute(row, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
-    bwd_row_wide_kernel<64><<<static_cast<unsigned>(nb * BH), kThreads, RowLay<64>::bytes, st>>>(
+    row<<<static_cast<unsigned>(nb * BH), kThreads, bytes, st>>>(
         q, g, k, v, static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), lse,
         static_cast<__nv_bfloat16*>(dQ), ws, static_cast<int>(N), static_cast<int>(Np), nb, static_cast<int>(BH),
         p.scale, c, p.causal, p.group, static_cast<int>(d));
