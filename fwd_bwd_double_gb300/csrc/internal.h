@@ -38,8 +38,8 @@ cudaError_t tc_fwd(const Problem& p, const void* Q, const void* K, const void* V
 cudaError_t tc_bwd(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
                    const void* dO, const float* lse, void* dQ, void* dK, void* dV, int gproj, float4* ws,
                    int passes, cudaStream_t st);
-// The 128-wide backward kernels (tc_bwd_wide.cu): both passes at d <= 64 without
-// GProj; the row pass alone at d <= 64 with GProj and at 64 < d <= 128 without.
+// The 128-wide backward kernels (tc_bwd_wide.cu): both passes at d <= 64, with or
+// without GProj; the row pass alone at 64 < d <= 128 without GProj.
 cudaError_t tc_bwd_wide(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
                         const void* dO, const float* lse, void* dQ, void* dK, void* dV, float4* ws, int passes,
                         cudaStream_t st, bool gproj = false);

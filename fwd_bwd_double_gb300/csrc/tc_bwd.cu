@@ -586,16 +586,8 @@ cudaError_t tc_bwd(const Problem& p, const void* Q, const void* K, const void* V
                    const float* lse, void* dQ, void* dK, void* dV, int gproj, float4* ws, int passes,
                    cudaStream_t st) {
   // d = 32 runs the d = 64 kernels and d = 96 the d = 128 ones, zero-padded in shared memory.
-  if (p.d <= 64) {
-    if (!gproj) return tc_bwd_wide(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st);
-    // GProj: the 128-wide row pass with the P^ K product, this file's GProj column pass.
-    if (passes & 1) {
-      const cudaError_t e = tc_bwd_wide(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, 1, st, true);
-      if (e != cudaSuccess) return e;
-    }
-    if (!(passes & 2)) return cudaSuccess;
-    return launch<64, 2, 1, true>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, 2, st);
-  }
+  // d <= 64, with or without GProj: the 128-wide kernels.
+  if (p.d <= 64) return tc_bwd_wide(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st, gproj != 0);
   if (gproj) return launch<128, 1, 1, true>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st);
   // d = 96, 128 without GProj: the 128-wide row pass, then this file's column pass
   // (both use the same pair-interleaved row statistics).

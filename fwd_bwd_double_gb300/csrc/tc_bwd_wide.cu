@@ -336,24 +336,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ============================================================= column pass
-struct ColLay {
+// GP: GProj.  The key correction -sum_i rho_i P^_ij Q_i is a third output product
+// that reuses the P^T operand: dK += P^T (-rho Q_i), with -rho_i Q_i (bf16) written by
+// the compute warps into one more shared-memory tile in Q's layout, so the TMEM map
+// stays that of the plain pass (a separate -rho P^ operand would need 576 columns).
+template <bool GP = false>
+struct ColLayT {
   static constexpr int kStat = BW * 16;
   static constexpr int kStage = 2 * kTile + kStat;  // Q_i, dO_i, statistics
   static constexpr int oK = 0, oV = kTile, oStage = 2 * kTile;
-  static constexpr int oBar = oStage + NS * kStage;
+  static constexpr int oRQ = oStage + NS * kStage;  // GProj: -rho Q_i of the current block
+  static constexpr int oBar = oRQ + (GP ? kTile : 0);
   static constexpr int bytes = oBar + 256;
   static constexpr int cS = 0, cdP = 128, cP = 256, cdS = 320, cdV = 384, cdK = 448;
 };
+using ColLay = ColLayT<false>;
+static_assert(ColLayT<true>::bytes <= 232448 && ColLayT<true>::oRQ % 1024 == 0, "GProj column layout");
 
 // GR: grouped key/value heads (G > 1).  The G == 1 instance keeps the plain tile loop.
-template <bool GR>
+template <bool GR, bool GP>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_col_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                const __grid_constant__ CUtensorMap tmSt, __nv_bfloat16* __restrict__ dK,
                __nv_bfloat16* __restrict__ dV, int N, int nb, int BHkv, float scale, float c, int causal, int G,
                int dv) {
-  using Lay = ColLay;
+  using Lay = ColLayT<GP>;
   extern __shared__ __align__(1024) uint8_t sm[];
   Sync sy(sm + Lay::oBar);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -429,7 +437,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sSt = ptx::smem_u32(sm + Lay::oStage);
       const uint64_t dQm = tc::mnmajor_desc(sSt, BW, 0), ddOm = tc::mnmajor_desc(sSt + kTile, BW, 0);
       const uint32_t tP = tmem + Lay::cP, tdS = tmem + Lay::cdS, tdV = tmem + Lay::cdV, tdK = tmem + Lay::cdK;
-      for (int t = 0; t < nt; ++t) {  // dV += P^T dO_i, dK += dS^T Q_i
+      const uint64_t dRQm = tc::mnmajor_desc(ptx::smem_u32(sm + Lay::oRQ), BW, 0);  // GProj: -rho Q_i
+      for (int t = 0; t < nt; ++t) {  // dV += P^T dO_i, dK += dS^T Q_i (+ P^T (-rho Q_i))
         const int s = t % NS;
         const uint32_t so = static_cast<uint32_t>(s * Lay::kStage);
         wait(sy.ready, t & 1);
@@ -440,6 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t acc = (t > 0 || k > 0) ? 1u : 0u;
           ptx::mma_ts_e(tdV, tP + k * 8, tc::desc_add(ddOm, so + 2048 * k), idKV, acc);
           ptx::mma_ts_e(tdK, tdS + k * 8, tc::desc_add(dQm, so + 2048 * k), idKV, acc);
+          if constexpr (GP) ptx::mma_ts_e(tdK, tP + k * 8, tc::desc_add(dRQm, 2048 * k), idKV, 1u);
         }
         ptx::mma_commit_e(&sy.empty[s]);
         ptx::mma_commit_e(sy.out_done);
@@ -506,7 +516,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         block(std::true_type{});
       else
         block(std::false_type{});
-      if (t > 0) wait(sy.out_done, (t - 1) & 1);  // the previous block's products have read P, dS
+      if (t > 0) wait(sy.out_done, (t - 1) & 1);  // the previous block's products have read P, dS (and -rho Q)
+      if constexpr (GP) {
+        // -rho_q Q_q of the block's 128 queries, 16 bytes (8 columns) per chunk, written at
+        // the chunk's own offset (the 128-byte swizzle keeps a chunk within its row q).
+        const uint8_t* qt = sm + Lay::oStage + s * Lay::kStage;
+        const float* stf = reinterpret_cast<const float*>(qt + 2 * kTile);
+#pragma unroll
+        for (int m = 0; m < kTile / 16 / kCompute; ++m) {
+          const int ch = static_cast<int>(threadIdx.x) + m * kCompute;
+          const int q = ch >> 3;
+          const float nrho = stf[((q >> 1) * 2 + 1) * 4 + (q & 1)];  // -rho of query q
+          const uint4 v = reinterpret_cast<const uint4*>(qt)[ch];
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+          uint32_t o[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o[e] = ptx::pack_bf16(nrho * bf16_lo(w[e]), nrho * bf16_hi(w[e]));
+          reinterpret_cast<uint4*>(sm + Lay::oRQ)[ch] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        ptx::fence_proxy_async_smem();  // visible to the tensor core before `ready`
+      }
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const uint32_t la = lo + (static_cast<uint32_t>(16 * h) << 16);
@@ -553,8 +582,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 cudaError_t tc_bwd_wide(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
                         const void* dO, const float* lse, void* dQ, void* dK, void* dV, float4* ws, int passes,
                         cudaStream_t st, bool gproj) {
-  // GProj: the row pass only (d <= 64; the GProj column pass is tc_bwd.cu's).
-  if (gproj && (p.d > 64 || (passes & 2))) return cudaErrorInvalidValue;
+  // GProj: d <= 64 only (TMEM).
+  if (gproj && p.d > 64) return cudaErrorInvalidValue;
   if (p.d > 64) {  // d = 96, 128: the row pass only (the column pass would need 640 TMEM columns)
     if (p.d > 128 || (passes & 2)) return cudaErrorInvalidValue;
     alignas(64) CUtensorMap q, g, k, v;
@@ -594,10 +623,12 @@ cudaError_t tc_bwd_wide(const Problem& p, const void* Q, const void* K, const vo
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (passes & 2) {
-    auto kern = p.group > 1 ? bwd_col_wide_kernel<true> : bwd_col_wide_kernel<false>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ColLay::bytes);
+    auto kern = gproj ? (p.group > 1 ? bwd_col_wide_kernel<true, true> : bwd_col_wide_kernel<false, true>)
+                      : (p.group > 1 ? bwd_col_wide_kernel<true, false> : bwd_col_wide_kernel<false, false>);
+    const int bytes = gproj ? ColLayT<true>::bytes : ColLayT<false>::bytes;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
-    kern<<<static_cast<unsigned>(nb * p.BHkv), kThreads, ColLay::bytes, st>>>(
+    kern<<<static_cast<unsigned>(nb * p.BHkv), kThreads, bytes, st>>>(
         k, v, q, g, s, static_cast<__nv_bfloat16*>(dK), static_cast<__nv_bfloat16*>(dV), static_cast<int>(N), nb,
         static_cast<int>(p.BHkv), p.scale, c, p.causal, p.group, static_cast<int>(d));
     e = cudaGetLastError();
