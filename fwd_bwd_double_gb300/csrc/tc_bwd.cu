@@ -82,14 +82,17 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
                    const float* __restrict__ lse, __nv_bfloat16* __restrict__ dQ, float4* __restrict__ ws, int N,
                    int Np, int nrb, int BH, float scale, float c, int causal, int G, int dv) {
   using Lay = RowLay<D, NB, GP>;
+  static_assert(NB == 1, "one score-tile buffer, released early");
   constexpr int NS = Lay::NS;
   extern __shared__ __align__(1024) uint8_t sm[];
   uint64_t* q_full = reinterpret_cast<uint64_t*>(sm + Lay::oBar);
   uint64_t* full = q_full + 1;
   uint64_t* empty = full + NS;
   uint64_t* s_full = empty + NS;
-  uint64_t* ds_ready = s_full + NB;
-  uint64_t* acc_full = ds_ready + NB;
+  uint64_t* ds_ready = s_full + NB;     // dS (and P^) of the block in TMEM
+  uint64_t* consumed = ds_ready + NB;   // the block's S, dP copied out: the tile columns are free
+  uint64_t* out_done = consumed + 1;    // the block's dQ (and P^ K) products have read the operands
+  uint64_t* acc_full = out_done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* red = reinterpret_cast<float*>(sm + Lay::oRed);
@@ -111,6 +114,8 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
       ptx::mbar_init(&s_full[b], 1);
       ptx::mbar_init(&ds_ready[b], kCompute);
     }
+    ptx::mbar_init(consumed, kCompute);
+    ptx::mbar_init(out_done, 1);
     ptx::mbar_init(acc_full, 1);
     *abort_flag = (ptx::smem_u32(sm) & 1023u) ? 1 : 0;
     if (*abort_flag) atomicOr(&g_err, FBD_ERR_TIMEOUT);
@@ -168,12 +173,15 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
             ptx::mma_ts_e(tmem + Lay::cPK, tmem + Lay::cP + b * (BN / 2) + k * 8, bd, idQ, (t > 0 || k > 0));
         }
         ptx::mma_commit_e(&empty[s]);
+        ptx::mma_commit_e(out_done);
       };
+      // Block j's tiles go into the columns block j-1's tiles left as soon as the
+      // compute warps have copied those out (`consumed`), ahead of block j-1's products.
       wait(q_full, 0);
       for (int j = 0; j < nkv; ++j) {
         const int s = j % NS, b = j % NB;
         wait(&full[s], (j / NS) & 1);
-        if (j >= NB) products(j - NB);  // frees score buffer b
+        if (j > 0) wait(consumed, (j - 1) & 1);
         ptx::tc_fence_after();
         const uint32_t kt = sK + s * Lay::kStream, vt = sV + s * Lay::kStream;
 #pragma unroll
@@ -184,8 +192,9 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
           ptx::mma_ss_e(tmem + Lay::cdP + b * BN, tc::kmajor_desc(sdO, BM, kk), tc::kmajor_desc(vt, BN, kk), idS,
                       kk > 0);
         ptx::mma_commit_e(&s_full[b]);
+        if (j > 0) products(j - 1);
       }
-      for (int t = (nkv > NB ? nkv - NB : 0); t < nkv; ++t) products(t);
+      if (nkv > 0) products(nkv - 1);
       ptx::mma_commit_e(acc_full);
     }
   } else {
@@ -224,6 +233,8 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
       ptx::tmem_ld32(tmem + Lay::cS + b * BN + c0 + lo, sv);
       ptx::tmem_ld32(tmem + Lay::cdP + b * BN + c0 + lo, pv);
       ptx::tmem_wait_ld();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(consumed);  // the MMA warp may now compute the next block's tiles here
       const int krel = j * BN + c0 - rb * BM;  // key of my column 0 minus the block's first row
       // last visible key of this row, relative to my column 0
       const int klim = causal ? r - krel : N - 1 - (j * BN + c0);
@@ -250,6 +261,7 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
         block(std::true_type{});
       else
         block(std::false_type{});
+      if (j > 0) wait(out_done, (j - 1) & 1);  // block j-1's products have read dS (and P^)
       ptx::tmem_st16(tmem + Lay::cdS + b * (BN / 2) + c0 / 2 + lo, dsk);
       if constexpr (GP) ptx::tmem_st16(tmem + Lay::cP + b * (BN / 2) + c0 / 2 + lo, pk);
       ptx::tmem_wait_st();
@@ -596,7 +608,7 @@ cudaError_t tc_bwd(const Problem& p, const void* Q, const void* K, const void* V
     if (e != cudaSuccess) return e;
   }
   if (!(passes & 2)) return cudaSuccess;
-  return launch<128, 2, 1, false>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, 2, st);
+  return launch<128, 1, 1, false>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, 2, st);
 }
 
 uint32_t tc_bwd_take_error() {
