@@ -117,11 +117,11 @@ def traffic_for(kernel, w):
 # the bench command; see profiles/), keyed by (kernel, workload), with the source
 # hash of the kernel file the counters were taken on.
 MEASURED_TRAFFIC = {
-    ("fwd", "gpt2small_B4H12N8192d64"): {"bytes": 184933632, "source": "tc_fwd.cu", "sha": "316a1b3f69c940c5"},
-    ("bwd_row", "gpt2small_B4H12N8192d64"): {"bytes": 293710848, "source": "tc_bwd_wide.cu", "sha": "970aae371eb6585a"},
-    ("bwd_col", "gpt2small_B4H12N8192d64"): {"bytes": 276495104, "source": "tc_bwd_wide.cu", "sha": "970aae371eb6585a"},
-    ("bob_row", "gpt2small_B4H12N8192d64"): {"bytes": 502975488, "source": "tc_bob.cu", "sha": "588d8906743f3253"},
-    ("bob_col", "gpt2small_B4H12N8192d64"): {"bytes": 438091008, "source": "tc_bob.cu", "sha": "588d8906743f3253"},
+    ("fwd", "gpt2small_B4H12N8192d64"): {"bytes": 185316608, "source": "tc_fwd.cu", "sha": "316a1b3f69c940c5"},
+    ("bwd_row", "gpt2small_B4H12N8192d64"): {"bytes": 293595136, "source": "tc_bwd_wide.cu", "sha": "bad96f59c9420ca6"},
+    ("bwd_col", "gpt2small_B4H12N8192d64"): {"bytes": 276578816, "source": "tc_bwd_wide.cu", "sha": "bad96f59c9420ca6"},
+    ("bob_row", "gpt2small_B4H12N8192d64"): {"bytes": 502659840, "source": "tc_bob.cu", "sha": "588d8906743f3253"},
+    ("bob_col", "gpt2small_B4H12N8192d64"): {"bytes": 438088448, "source": "tc_bob.cu", "sha": "588d8906743f3253"},
 }
 
 
