@@ -27,6 +27,8 @@ Sources:
     turns into a false gradient" (exact dS rows sum to zero; bf16 rounding of dS
     leaves a residual that multiplies the mean key; GProj measures the remaining row
     mass of the rounded dS and subtracts the matching share of the probabilities);
+    the same projection applied to the dS that BoB's dS b and dS^T a products see
+    is emulated by ``bob_bf16_dS``;
   * backward-over-backward (BoB): "FlashBoB: second-order attention" page, section
     "Why go backward through an already computed gradient": the gradient of the first
     backward's outputs (dQ, dK, dV) with respect to Q, K, V and the incoming dO,
@@ -343,6 +345,54 @@ def bob(Q, K, V, dO, a, b, c, scale=None, block=None, keep=False, causal=True):
     return out
 
 
+def bob_bf16_dS(Q, K, V, dO, a, b, c, gproj, scale=None, block=None, causal=True, rnd=None):
+    """Emulate a BoB whose dS b and dS^T a products see bf16(dS), with or without GProj.
+
+    The products of the closed form (``bob``) that contract dS, gQ's dS b and gK's
+    dS^T a, get the rounded row dS^ = rnd(dS) (rnd defaults to ``bf16_round``).
+    Without GProj that is all.  With GProj the rounded row is projected back to zero
+    sum as the GProj page describes for the first backward ("FlashAttention bf16
+    gradient and GProj", "How the zero sum turns into a false gradient": measure the
+    remaining row mass r_i = sum_j dS^_ij and subtract the matching share of the
+    probabilities actually fed to the products, P^ = rnd(P)):
+        dS~ = dS^ - (r_i / sum_k P^_ik) P^,
+        gQ = s (dS~ b + Sbar K),   gK = s (dS~^T a + Sbar^T Q);
+    gV, gdO and everything else are the exact fp64 values.  Used only to show what
+    the rounding and the projection do; the reference for errors is always ``bob``.
+    Returns dict(gQ, gK, gV, gdO, r, rho, dS_rowsum_rel) where the last item is
+    max_i |sum_j dS~_ij| / sum_j |dS~_ij| over rows with nonzero L1.
+    """
+    rnd = bf16_round if rnd is None else rnd
+    Q, K, V, dO, a, b, c = map(_f64, (Q, K, V, dO, a, b, c))
+    N, d = Q.shape
+    scale = default_scale(d) if scale is None else scale
+    gQ, gK, gV, gdO = (np.zeros((N, d)) for _ in range(4))
+    r_all, rho_all = np.zeros(N), np.zeros(N)
+    worst = 0.0
+    for r in _blocks(np.arange(N), block or _panel_budget(N, 12)):
+        t = _row_terms(Q, K, V, dO, r, scale, a, b, c, causal=causal)
+        nk = t["nk"]
+        dSh = rnd(t["dS"])
+        if gproj:
+            res = dSh.sum(axis=1)
+            Ph = rnd(t["P"])
+            rho = res / Ph.sum(axis=1)
+            dSt = dSh - rho[:, None] * Ph
+            r_all[r], rho_all[r] = res, rho
+        else:
+            dSt = dSh
+            r_all[r] = dSh.sum(axis=1)
+        l1 = np.abs(dSt).sum(axis=1)
+        nz = l1 > 0
+        if nz.any():
+            worst = max(worst, float(np.max(np.abs(dSt.sum(axis=1))[nz] / l1[nz])))
+        gQ[r] = scale * (dSt @ b[:nk] + t["Sbar"] @ K[:nk])
+        gK[:nk] += scale * (dSt.T @ a[r] + t["Sbar"].T @ Q[r])
+        gV[:nk] += t["dPbar"].T @ dO[r]
+        gdO[r] = t["P"] @ c[:nk] + t["dPbar"] @ V[:nk]
+    return dict(gQ=gQ, gK=gK, gV=gV, gdO=gdO, r=r_all, rho=rho_all, dS_rowsum_rel=worst)
+
+
 def bob_rows(Q, K, V, dO, a, b, c, rows, scale=None, causal=True):
     """gQ[rows], gdO[rows] and the row states (E, F) only."""
     Q, K, V, dO, a, b, c = map(_f64, (Q, K, V, dO, a, b, c))
@@ -508,5 +558,14 @@ def bob_all(Q, K, V, dO, a, b, c, scale=None, causal=True, groups=1):
     per-head second derivatives of K and V are summed over the group the same way."""
     e = lambda X: _expand_kv(X, groups)
     out = _each_slice(bob, Q, e(K), e(V), dO, a, e(b), e(c), scale=scale, causal=causal)
+    out["gK"], out["gV"] = _sum_groups(out["gK"], groups), _sum_groups(out["gV"], groups)
+    return out
+
+
+def bob_bf16_dS_all(Q, K, V, dO, a, b, c, gproj, scale=None, causal=True, groups=1):
+    """``bob_bf16_dS`` over every (batch, head) slice, grouped heads as in ``bob_all``."""
+    e = lambda X: _expand_kv(X, groups)
+    out = _each_slice(lambda *x, **kw: bob_bf16_dS(*x, gproj, **kw), Q, e(K), e(V), dO, a, e(b), e(c),
+                      scale=scale, causal=causal)
     out["gK"], out["gV"] = _sum_groups(out["gK"], groups), _sum_groups(out["gV"], groups)
     return out

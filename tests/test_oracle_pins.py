@@ -7,7 +7,10 @@ Each pin names the page passage (or the mathematical fact) it rests on:
     recurrence");
   * probability rows sum to one; a per-row constant in S changes nothing;
   * exact dS rows sum to zero and dQ ignores a common shift of all keys (GProj page,
-    "How the zero sum turns into a false gradient");
+    "How the zero sum turns into a false gradient"); every BoB output ignores a
+    common shift of the keys and of the cotangent b; the GProj projection of BoB's
+    rounded dS sums to zero and makes gQ ignore a shift of b, which the unprojected
+    residual turns into exactly s r_i v;
   * central finite differences of the forward (first backward) and of the first
     backward (second backward, a Hessian-vector product), and of O along the
     cotangent direction (gdO is that directional derivative);
@@ -295,6 +298,48 @@ def test_bob_invariant_to_common_key_shift():
     o1 = oracle.bob(Q, K + v[None, :], V, dO, a, b, c)
     for k in ("gQ", "gK", "gV", "gdO"):
         assert rel(o1[k], o0[k]) <= 1e-11, k
+
+
+def test_bob_invariant_to_common_shift_of_b():
+    # b = gdK enters only through G = s(a K^T + Q b^T) and the product dS b.  One vector
+    # v added to every row of b adds the per-row constant s q_i.v to G, which
+    # dPbar = P(G - E) and Sbar = P(Pbar - F) do not see (E and F move with it), and
+    # adds s (sum_j dS_ij) v = 0 to dS b (exact dS rows sum to zero).
+    Q, K, V, dO, a, b, c = slice_set(30, 8, 58)
+    v = rnd(59, 8) * 6
+    o0 = oracle.bob(Q, K, V, dO, a, b, c)
+    o1 = oracle.bob(Q, K, V, dO, a, b + v[None, :], c)
+    for k in ("gQ", "gK", "gV", "gdO"):
+        assert rel(o1[k], o0[k]) <= 1e-11, k
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_bob_bf16_dS_projection(causal):
+    # GProj page, "How the zero sum turns into a false gradient", applied to the dS
+    # of BoB's dS b and dS^T a products.
+    N, d = 96, 16
+    Q, K, V, dO, a, b, c = slice_set(N, d, 60)
+    b = b + 10.0  # a large common b: the rounding residual then shows up in gQ
+    s = 1.0 / math.sqrt(d)
+    exact = oracle.bob(Q, K, V, dO, a, b, c, causal=causal)
+    # No rounding: nothing to project (exact rows sum to zero), every output exact.
+    ident = oracle.bob_bf16_dS(Q, K, V, dO, a, b, c, True, causal=causal, rnd=lambda x: x)
+    for k in ("gQ", "gK", "gV", "gdO"):
+        assert rel(ident[k], exact[k]) <= 1e-12, k
+    plain = oracle.bob_bf16_dS(Q, K, V, dO, a, b, c, False, causal=causal)
+    proj = oracle.bob_bf16_dS(Q, K, V, dO, a, b, c, True, causal=causal)
+    assert proj["dS_rowsum_rel"] <= 1e-13
+    assert plain["dS_rowsum_rel"] > 1e-5  # bf16 rounding leaves a row mass
+    for k in ("gV", "gdO"):  # they never see dS
+        assert rel(plain[k], exact[k]) <= 1e-13 and rel(proj[k], exact[k]) <= 1e-13, k
+    # A common shift v of b: unprojected, gQ moves by exactly s r_i v (the residual
+    # times the shift); projected, it does not move at all.
+    v = rnd(61, d) * 3
+    plain_v = oracle.bob_bf16_dS(Q, K, V, dO, a, b + v[None, :], c, False, causal=causal)
+    proj_v = oracle.bob_bf16_dS(Q, K, V, dO, a, b + v[None, :], c, True, causal=causal)
+    assert rel(plain_v["gQ"] - plain["gQ"], s * np.outer(plain["r"], v)) <= 1e-8
+    assert rel(proj_v["gQ"], proj["gQ"]) <= 1e-11
+    assert rel(proj["gQ"], exact["gQ"]) < rel(plain["gQ"], exact["gQ"])
 
 
 def test_bob_single_token_closed_form():
