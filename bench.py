@@ -34,7 +34,7 @@ sys.path.insert(0, ROOT)
 import workloads as W  # noqa: E402
 
 L2_BYTES = 129 * 2 ** 20
-LAUNCHES_PER_STEP = {"fwd": 1, "bwd": 2, "bob": 2}
+LAUNCHES_PER_STEP = {"fwd": 1, "bwd": 2, "bob": 2}  # BoB with GProj: + 1 (the P^ b launch)
 KERNELS = ("fwd", "bwd_row", "bwd_col", "bob_row", "bob_col")
 # Contractions (N^2 d products) per kernel: the dense definition's share (each of
 # the pages' contractions counted once; tiles recomputed by a column pass are not
@@ -204,7 +204,7 @@ def run_ours(args, w, rank, world):
     out = {k: torch.empty(x[src].shape, dtype=bf, device=dev) for k, src in like.items()}
     lse = torch.empty(shp[:3], dtype=torch.float32, device=dev)
     ws = torch.empty(fbd.attn_bwd_workspace_bytes(desc, 1), dtype=torch.uint8, device=dev)
-    ws2 = torch.empty(fbd.attn_bob_workspace_bytes(desc), dtype=torch.uint8, device=dev)
+    ws2 = torch.empty(fbd.attn_bob_workspace_bytes(desc, 1), dtype=torch.uint8, device=dev)  # fits both forms
 
     R, C = fbd.ATTN_ROW_PASS, fbd.ATTN_COL_PASS
 
@@ -223,7 +223,7 @@ def run_ours(args, w, rank, world):
         for i, ps in enumerate((R, C)):
             fbd.attn_bob_passes(xx["Q"], xx["K"], xx["V"], out["O"], xx["dO"], lse, xx["gdQ"], xx["gdK"], xx["gdV"],
                                 ps, gQ=out["gQ"], gK=out["gK"], gV=out["gV"], gdO=out["gdO"], workspace=ws2,
-                                stream=stream, desc=desc)
+                                stream=stream, desc=desc, gproj=gproj)
             mark(4 + i)
 
     with torch.cuda.stream(stream):
@@ -270,6 +270,24 @@ def run_ours(args, w, rank, world):
 
     bwd0, bwd1 = time_bwd(0), time_bwd(1)
 
+    def time_bob(gp, reps=max(3, args.steps)):  # the same for the BoB (GProj: + the P^ b launch)
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+
+        def once():
+            fbd.attn_bob(x["Q"], x["K"], x["V"], out["O"], x["dO"], lse, x["gdQ"], x["gdK"], x["gdV"],
+                         gQ=out["gQ"], gK=out["gK"], gV=out["gV"], gdO=out["gdO"], workspace=ws2, stream=stream,
+                         desc=desc, gproj=gp)
+        with torch.cuda.stream(stream):
+            once()
+            e[0].record(stream)
+            for _ in range(reps):
+                once()
+            e[1].record(stream)
+        torch.cuda.synchronize()
+        return e[0].elapsed_time(e[1]) / reps
+
+    bob0, bob1 = time_bob(0), time_bob(1)
+
     # End to end: every step copies its 7 inputs from pinned host memory to the device,
     # runs the five launches and copies O, lse and the 7 outputs back to pinned host
     # memory.  The copies of step i+1's inputs and of step i-1's outputs run on their
@@ -288,7 +306,8 @@ def run_ours(args, w, rank, world):
         fbd.attn_bwd(xx["Q"], xx["K"], xx["V"], oo["O"], xx["dO"], ll, gproj=args.gproj, dQ=oo["dQ"], dK=oo["dK"],
                      dV=oo["dV"], workspace=ws, stream=stream, desc=desc)
         fbd.attn_bob(xx["Q"], xx["K"], xx["V"], oo["O"], xx["dO"], ll, xx["gdQ"], xx["gdK"], xx["gdV"], gQ=oo["gQ"],
-                     gK=oo["gK"], gV=oo["gV"], gdO=oo["gdO"], workspace=ws2, stream=stream, desc=desc)
+                     gK=oo["gK"], gV=oo["gV"], gdO=oo["gdO"], workspace=ws2, stream=stream, desc=desc,
+                     gproj=args.gproj)
 
     ev = lambda: torch.cuda.Event(enable_timing=False)
     in_done = [ev() for _ in range(e2e_steps)]
@@ -325,6 +344,7 @@ def run_ours(args, w, rank, world):
     return dict(ms=ms, ms_max=ms_max, per_op={op: statistics.mean(v) for op, v in per_op.items()},
                 per_kernel={kn: statistics.mean(v) for kn, v in per_kernel.items()},
                 flops_step=flops_step, wall=wall, clocks=clk.summary(), bwd_gproj_ms=(bwd0, bwd1),
+                bob_gproj_ms=(bob0, bob1),
                 e2e_ms=e2e_ms, h2d=h2d, d2h=d2h)
 
 
@@ -436,10 +456,10 @@ def sweep(args):
     stream = torch.cuda.current_stream(dev)
     configs = [(f"long_B1H12N{n}d64", 1, 12, n, 64, ("bwd", "bob")) for n in (4096, 16384, 65536, 262144)]
     configs += [("gpt2small_B1H12N8192d64", 1, 12, 8192, 64, ("fwd", "bwd", "bob")),
-                ("gpt2small_B4H12N8192d64", 4, 12, 8192, 64, ("fwd", "bwd", "bob")),
+                ("gpt2small_B4H12N8192d64", 4, 12, 8192, 64, ("fwd", "bwd", "bwd_gproj", "bob", "bob_gproj")),
                 ("fullday_B2H12N23400d64", 2, 12, 23400, 64, ("fwd", "bwd")),
                 ("largekey_B8H8N2048d128", 8, 8, 2048, 128, ("bwd", "bwd_gproj")),
-                ("headdim128_B4H12N8192d128", 4, 12, 8192, 128, ("fwd", "bwd", "bwd_gproj", "bob"))]
+                ("headdim128_B4H12N8192d128", 4, 12, 8192, 128, ("fwd", "bwd", "bwd_gproj", "bob", "bob_gproj"))]
     reps, warm = max(args.steps, 1), max(args.warmup, 1)
     for name, B, H, N, d, ops in configs:
         torch.cuda.empty_cache()
@@ -451,7 +471,7 @@ def sweep(args):
         O, lse = fbd.attn_fwd(x["Q"], x["K"], x["V"])
         desc = fbd.make_desc(x["Q"])
         outs = [torch.empty_like(x["Q"]) for _ in range(4)]
-        ws = torch.empty(fbd.attn_bob_workspace_bytes(desc), dtype=torch.uint8, device=dev)
+        ws = torch.empty(fbd.attn_bob_workspace_bytes(desc, 1), dtype=torch.uint8, device=dev)  # fits every op
         run = {
             "fwd": lambda: fbd.attn_fwd(x["Q"], x["K"], x["V"], O=outs[0], lse=lse, desc=desc),
             "bwd": lambda: fbd.attn_bwd(x["Q"], x["K"], x["V"], O, x["dO"], lse, 0, *outs[:3], workspace=ws,
@@ -460,6 +480,8 @@ def sweep(args):
                                               desc=desc),
             "bob": lambda: fbd.attn_bob(x["Q"], x["K"], x["V"], O, x["dO"], lse, x["gdQ"], x["gdK"], x["gdV"],
                                         *outs, workspace=ws, desc=desc),
+            "bob_gproj": lambda: fbd.attn_bob(x["Q"], x["K"], x["V"], O, x["dO"], lse, x["gdQ"], x["gdK"],
+                                              x["gdV"], *outs, workspace=ws, desc=desc, gproj=1),
         }
         for nm, ps in (("row", fbd.ATTN_ROW_PASS), ("col", fbd.ATTN_COL_PASS)):  # the two launches apart
             run["bwd_" + nm] = (lambda ps=ps: fbd.attn_bwd_passes(x["Q"], x["K"], x["V"], O, x["dO"], lse, ps, 0,
@@ -485,12 +507,14 @@ def sweep(args):
             ms = sorted(ev[i].elapsed_time(ev[i + 1]) for i in range(reps))
             med = statistics.median(ms)
             line[op] = {"ms_median": med, "ms_min": ms[0], "ms_max": ms[-1]}
-            if op in ("fwd", "bwd", "bob", "bwd_gproj"):
-                fl = dense_flops(w, "bwd" if op == "bwd_gproj" else op)
+            if op in ("fwd", "bwd", "bob", "bwd_gproj", "bob_gproj"):
+                fl = dense_flops(w, op.replace("_gproj", ""))
                 line[op]["tflops_dense"] = fl / (med * 1e-3) / 1e12
         line["peak_hbm_bytes"] = torch.cuda.max_memory_allocated(dev)
         if "bwd_gproj" in line:
             line["gproj_overhead_pct"] = 100.0 * (line["bwd_gproj"]["ms_median"] / line["bwd"]["ms_median"] - 1.0)
+        if "bob_gproj" in line:
+            line["bob_gproj_overhead_pct"] = 100.0 * (line["bob_gproj"]["ms_median"] / line["bob"]["ms_median"] - 1.0)
         print(json.dumps(line), flush=True)
         del x, O, lse, outs, ws
 
@@ -530,7 +554,7 @@ def main():
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     config = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": CAUSAL, "group": w.group,
-              "ops": "fwd + bwd(gproj=%d) + BoB" % args.gproj,
+              "ops": "fwd + bwd(gproj=%d) + BoB(gproj=%d)" % (args.gproj, args.gproj),
               "l2": "inputs larger than L2 (7 input tensors, %.0f MB in total)"
                     % (w.rows * w.d * 2 * (3 + 4 / w.group) / 1e6),
               "parallelism": f"independent replicas x{world}"}
@@ -586,6 +610,8 @@ def main():
                     for kn in KERNELS},
         "gproj_bwd_ms": {"off": r["bwd_gproj_ms"][0], "on": r["bwd_gproj_ms"][1],
                          "overhead_pct": 100.0 * (r["bwd_gproj_ms"][1] / r["bwd_gproj_ms"][0] - 1.0)},
+        "gproj_bob_ms": {"off": r["bob_gproj_ms"][0], "on": r["bob_gproj_ms"][1],
+                         "overhead_pct": 100.0 * (r["bob_gproj_ms"][1] / r["bob_gproj_ms"][0] - 1.0)},
         "roofline": {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": pk["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops"], "traffic": traffic_for(dom, w),
                      "peak_source": pk["source"] + " burst bf16",
@@ -594,7 +620,7 @@ def main():
                                        if executed_flops(w, dom) else None)},
         "e2e": {"value": r["flops_step"] / (r["e2e_ms"] * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["e2e_ms"]},
-        "gpu_launches": sum(LAUNCHES_PER_STEP.values()) * args.steps,
+        "gpu_launches": (sum(LAUNCHES_PER_STEP.values()) + (1 if args.gproj else 0)) * args.steps,
         "clocks": r["clocks"],
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -89,8 +89,8 @@ def attn_bwd_workspace_bytes(desc: AttnDesc, gproj: int = 0) -> int:
     return int(lib.attn_bwd_workspace_bytes(ctypes.byref(desc), int(gproj)))
 
 
-def attn_bob_workspace_bytes(desc: AttnDesc) -> int:
-    return int(lib.attn_bob_workspace_bytes(ctypes.byref(desc)))
+def attn_bob_workspace_bytes(desc: AttnDesc, gproj: int = 0) -> int:
+    return int(lib.attn_bob_workspace_bytes(ctypes.byref(desc), int(gproj)))
 
 
 def _workspace(nbytes, like, workspace):
@@ -125,14 +125,16 @@ def attn_bwd_passes(Q, K, V, O, dO, lse, passes, gproj: int = 0, dQ=None, dK=Non
 
 
 def attn_bob(Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ=None, gK=None, gV=None, gdO=None, workspace=None,
-             scale: float = 0.0, stream=None, desc=None, causal: bool = True):
-    """gQ, gK, gV, gdO = backward over backward against cotangents (gdQ, gdK, gdV)."""
+             scale: float = 0.0, stream=None, desc=None, causal: bool = True, gproj: int = 0):
+    """gQ, gK, gV, gdO = backward over backward against cotangents (gdQ, gdK, gdV)
+    (GProj on the rounded dS of its dS b and dS^T a products when gproj != 0, bf16 only)."""
     return attn_bob_passes(Q, K, V, O, dO, lse, gdQ, gdK, gdV, ATTN_ROW_PASS | ATTN_COL_PASS, gQ, gK, gV, gdO,
-                           workspace, scale, stream, desc, causal)
+                           workspace, scale, stream, desc, causal, gproj)
 
 
 def attn_bob_passes(Q, K, V, O, dO, lse, gdQ, gdK, gdV, passes, gQ=None, gK=None, gV=None, gdO=None,
-                    workspace=None, scale: float = 0.0, stream=None, desc=None, causal: bool = True):
+                    workspace=None, scale: float = 0.0, stream=None, desc=None, causal: bool = True,
+                    gproj: int = 0):
     """BoB's row pass (gQ, gdO, row states) and/or column pass (gK, gV); see fbd.h."""
     torch = _torch()
     desc = desc or make_desc(Q, scale, int(causal), K)
@@ -140,9 +142,9 @@ def attn_bob_passes(Q, K, V, O, dO, lse, gdQ, gdK, gdV, passes, gQ=None, gK=None
     gK = torch.empty_like(K) if gK is None else gK
     gV = torch.empty_like(V) if gV is None else gV
     gdO = torch.empty_like(dO) if gdO is None else gdO
-    workspace = _workspace(attn_bob_workspace_bytes(desc), Q, workspace)
+    workspace = _workspace(attn_bob_workspace_bytes(desc, gproj), Q, workspace)
     _check(lib.attn_bob_passes(ctypes.byref(desc), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(lse),
-                               _ptr(gdQ), _ptr(gdK), _ptr(gdV), _ptr(gQ), _ptr(gK), _ptr(gV), _ptr(gdO),
+                               _ptr(gdQ), _ptr(gdK), _ptr(gdV), _ptr(gQ), _ptr(gK), _ptr(gV), _ptr(gdO), int(gproj),
                                _ptr(workspace), ctypes.c_size_t(workspace.numel() * workspace.element_size()),
                                int(passes), _stream(stream)))
     return gQ, gK, gV, gdO

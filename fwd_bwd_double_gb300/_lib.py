@@ -39,11 +39,11 @@ PROTOTYPES = {
     "attn_fwd": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P]),
     "attn_bwd_workspace_bytes": (ctypes.c_size_t, [_D, ctypes.c_int]),
     "attn_bwd": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int, _P, ctypes.c_size_t, _P]),
-    "attn_bob_workspace_bytes": (ctypes.c_size_t, [_D]),
-    "attn_bob": (ctypes.c_int, [_D] + [_P] * 13 + [_P, ctypes.c_size_t, _P]),
+    "attn_bob_workspace_bytes": (ctypes.c_size_t, [_D, ctypes.c_int]),
+    "attn_bob": (ctypes.c_int, [_D] + [_P] * 13 + [ctypes.c_int, _P, ctypes.c_size_t, _P]),
     "attn_bwd_passes": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int, _P, ctypes.c_size_t,
                                         ctypes.c_int, _P]),
-    "attn_bob_passes": (ctypes.c_int, [_D] + [_P] * 13 + [_P, ctypes.c_size_t, ctypes.c_int, _P]),
+    "attn_bob_passes": (ctypes.c_int, [_D] + [_P] * 13 + [ctypes.c_int, _P, ctypes.c_size_t, ctypes.c_int, _P]),
     "attn_bob_static": (ctypes.c_int, [_D] + [_P] * 13 + [_P]),
     "attn_bwd_projected_dS": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, _P]),
     "attn_device_status": (ctypes.c_int, [_P]),

@@ -145,11 +145,20 @@ size_t attn_bwd_workspace_bytes(const attn_desc_t* desc, int gproj) {
   return static_cast<size_t>(desc->B) * desc->H * ((desc->N + 1) & ~static_cast<int64_t>(1)) * 16;
 }
 
-size_t attn_bob_workspace_bytes(const attn_desc_t* desc) {
+size_t attn_bob_workspace_bytes(const attn_desc_t* desc, int gproj) {
   if (desc == nullptr || desc->B < 0 || desc->H < 0 || desc->N < 0) return 0;
-  // 16 bytes per row, rows of each slice rounded up to an even count (the bf16
-  // column pass reads the row states two rows at a time).
-  return static_cast<size_t>(desc->B) * desc->H * ((desc->N + 1) & ~static_cast<int64_t>(1)) * 16;
+  // The row states: 16 bytes per row, rows of each slice rounded up to an even count
+  // (the bf16 column pass reads them two rows at a time).  GProj (bf16 only): as much
+  // again for the coefficients, and on the tensor-core path (d <= 128) the rows' P^ b
+  // in fp32 (64 or 128 per row).  The layout is fbd::bob_rho_region / bob_pb_region.
+  const size_t rows = static_cast<size_t>(desc->B) * desc->H * ((desc->N + 1) & ~static_cast<int64_t>(1));
+  size_t n = rows * 16;
+  if (gproj && desc->dtype == ATTN_BF16) {
+    n += rows * 16;
+    if (desc->d <= 128)
+      n += static_cast<size_t>(desc->B) * desc->H * desc->N * fbd::bob_pb_cols(desc->d) * sizeof(float);
+  }
+  return n;
 }
 
 attn_status_t attn_bwd_passes(const attn_desc_t* desc, const void* Q, const void* K, const void* V, const void* O,
@@ -186,14 +195,15 @@ attn_status_t attn_bwd(const attn_desc_t* desc, const void* Q, const void* K, co
 
 attn_status_t attn_bob_passes(const attn_desc_t* desc, const void* Q, const void* K, const void* V, const void* O,
                               const void* dO, const float* lse, const void* gdQ, const void* gdK, const void* gdV,
-                              void* gQ, void* gK, void* gV, void* gdO, void* workspace, size_t workspace_bytes,
-                              int passes, void* stream) {
+                              void* gQ, void* gK, void* gV, void* gdO, int gproj, void* workspace,
+                              size_t workspace_bytes, int passes, void* stream) {
   fbd::Problem p;
   attn_status_t s = check_desc(desc, p);
   if (s != ATTN_OK) return s;
   if (passes < 1 || passes > 3) return fail(ATTN_ERR_INVALID_ARG, "passes must be ATTN_ROW_PASS, ATTN_COL_PASS or both%s");
   if (p.BH * p.N == 0) return ATTN_OK;
-  const size_t need = attn_bob_workspace_bytes(desc);
+  const bool gp = gproj != 0 && p.dtype == ATTN_BF16;  // float32 dS is never rounded
+  const size_t need = attn_bob_workspace_bytes(desc, gproj);
   if (workspace == nullptr || workspace_bytes < need)
     return fail(ATTN_ERR_WORKSPACE, "workspace NULL or smaller than attn_bob_workspace_bytes()%s");
   const size_t tb = static_cast<size_t>(p.BH * p.N * p.d) * elem_size(p), sb = p.BH * p.N * sizeof(float);
@@ -207,18 +217,19 @@ attn_status_t attn_bob_passes(const attn_desc_t* desc, const void* Q, const void
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   float4* ws = static_cast<float4*>(workspace);
   if (!tc_path(p, 2))
-    return launch_status(fbd::simt_bob(p, Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ, gK, gV, gdO, ws, passes, st));
+    return launch_status(fbd::simt_bob(p, Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ, gK, gV, gdO, gp, ws, passes, st));
   if (p.d > 64)
-    return launch_status(fbd::tc_bob128(p, Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ, gK, gV, gdO, ws, passes, st));
-  return launch_status(fbd::tc_bob(p, Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ, gK, gV, gdO, ws, passes, st));
+    return launch_status(
+        fbd::tc_bob128(p, Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ, gK, gV, gdO, gp, ws, passes, st));
+  return launch_status(fbd::tc_bob(p, Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ, gK, gV, gdO, gp, ws, passes, st));
 }
 
 attn_status_t attn_bob(const attn_desc_t* desc, const void* Q, const void* K, const void* V, const void* O,
                        const void* dO, const float* lse, const void* gdQ, const void* gdK, const void* gdV,
-                       void* gQ, void* gK, void* gV, void* gdO, void* workspace, size_t workspace_bytes,
+                       void* gQ, void* gK, void* gV, void* gdO, int gproj, void* workspace, size_t workspace_bytes,
                        void* stream) {
-  return attn_bob_passes(desc, Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ, gK, gV, gdO, workspace, workspace_bytes,
-                         ATTN_ROW_PASS | ATTN_COL_PASS, stream);
+  return attn_bob_passes(desc, Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ, gK, gV, gdO, gproj, workspace,
+                         workspace_bytes, ATTN_ROW_PASS | ATTN_COL_PASS, stream);
 }
 
 attn_status_t attn_bwd_projected_dS(const attn_desc_t* desc, const void* Q, const void* K, const void* V,

@@ -63,7 +63,7 @@ extern "C" attn_status_t attn_bob_static(const attn_desc_t* desc, const void* Q,
                                          const void* gdK, const void* gdV, void* gQ, void* gK, void* gV,
                                          void* gdO, void* stream) {
   if (desc == nullptr) return fbd::set_last_error(ATTN_ERR_INVALID_ARG, "desc is NULL");
-  const size_t need = attn_bob_workspace_bytes(desc);
+  const size_t need = attn_bob_workspace_bytes(desc, 0);  // plain BoB (no GProj)
   if (need > kStaticBobScratchBytes) {
     char msg[200];
     std::snprintf(msg, sizeof(msg),
@@ -73,10 +73,10 @@ extern "C" attn_status_t attn_bob_static(const attn_desc_t* desc, const void* Q,
     return fbd::set_last_error(ATTN_ERR_WORKSPACE, msg);
   }
   if (need == 0)  // empty or malformed descriptor: attn_bob decides, touching no memory
-    return attn_bob(desc, Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ, gK, gV, gdO, nullptr, 0, stream);
+    return attn_bob(desc, Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ, gK, gV, gdO, 0, nullptr, 0, stream);
   void* scratch = nullptr;
   const attn_status_t s = scratch_address(&scratch);
   if (s != ATTN_OK) return s;
-  return attn_bob(desc, Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ, gK, gV, gdO, scratch, kStaticBobScratchBytes,
+  return attn_bob(desc, Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ, gK, gV, gdO, 0, scratch, kStaticBobScratchBytes,
                   stream);
 }

@@ -27,7 +27,7 @@ cudaError_t simt_bwd(const Problem& p, const void* Q, const void* K, const void*
                      int passes, cudaStream_t st);
 cudaError_t simt_bob(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
                      const void* dO, const float* lse, const void* a, const void* b, const void* c, void* gQ,
-                     void* gK, void* gV, void* gdO, float4* ws, int passes, cudaStream_t st);
+                     void* gK, void* gV, void* gdO, bool gproj, float4* ws, int passes, cudaStream_t st);
 cudaError_t simt_projected_dS(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
                               const void* dO, const float* lse, float* dS, cudaStream_t st);
 
@@ -45,12 +45,32 @@ cudaError_t tc_bwd_wide(const Problem& p, const void* Q, const void* K, const vo
                         cudaStream_t st, bool gproj = false);
 cudaError_t tc_bob(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
                    const void* dO, const float* lse, const void* a, const void* b, const void* c, void* gQ,
-                   void* gK, void* gV, void* gdO, float4* ws, int passes, cudaStream_t st);
+                   void* gK, void* gV, void* gdO, bool gproj, float4* ws, int passes, cudaStream_t st);
 // d = 128: the same passes with each block of rows (keys) split over two CTAs by
 // output half (tc_bob128.cu).
 cudaError_t tc_bob128(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
                       const void* dO, const float* lse, const void* a, const void* b, const void* c, void* gQ,
-                      void* gK, void* gV, void* gdO, float4* ws, int passes, cudaStream_t st);
+                      void* gK, void* gV, void* gdO, bool gproj, float4* ws, int passes, cudaStream_t st);
+// BoB with GProj, tensor-core path: Pb_i = sum_j P^_ij b_j (fp32, bob_pb_cols(d) per
+// row) for every row, P^ = bf16(2^(S s log2 e - L log2 e)) formed exactly as the BoB row
+// pass forms it (the forward kernel run with the stored L and b in place of V; tc_fwd.cu).
+cudaError_t tc_bob_pb(const Problem& p, const void* Q, const void* K, const void* b, const float* lse, float* pb,
+                      cudaStream_t st);
+
+// BoB workspace: the row states (16 bytes per row, the rows of a slice rounded up to
+// an even count); with GProj (bf16) a region of the same size for the GProj
+// coefficients (one float per row: at pitch bob_rho_pitch(N) on the tensor-core path,
+// at pitch N on the CUDA-core path), and on the tensor-core path the rows' P^ b (fp32,
+// bob_pb_cols(d) per row, B*H*N rows).
+inline int64_t bob_state_rows(const Problem& p) { return p.BH * ((p.N + 1) & ~static_cast<int64_t>(1)); }
+inline float4* bob_rho_region(float4* ws, const Problem& p) { return ws + bob_state_rows(p); }
+inline float* bob_pb_region(float4* ws, const Problem& p) {
+  return reinterpret_cast<float*>(ws + 2 * bob_state_rows(p));
+}
+inline int bob_pb_cols(int64_t d) { return d <= 64 ? 64 : 128; }
+// Tensor-core path: the coefficients are one float per row, -rho_i, the rows of a slice
+// rounded up to a multiple of 4 (read by TMA as float4 groups).
+__host__ __device__ inline int64_t bob_rho_pitch(int64_t N) { return (N + 3) & ~static_cast<int64_t>(3); }
 
 // passes: bit 0 = the row pass, bit 1 = the column pass (ATTN_ROW_PASS / ATTN_COL_PASS).
 

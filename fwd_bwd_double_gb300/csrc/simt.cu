@@ -309,12 +309,15 @@ __global__ void __launch_bounds__(kThreads) bwd_col_kernel(const T* __restrict__
 // Streams keys past each query row; accumulates E, F' and X, Y, Z, U, and at the
 // end applies the corrections that need the finished row:
 //   gdO = X - E O,  gQ = s (Y - E Z - F' U),  F = F' - E D.
-template <typename T, int D>
+// GP (GProj, bf16): the dS of gQ's dS b product is rounded to bf16 as the tensor-core
+// path rounds it and projected to zero row sum: Y gets bf16(dS) b, and rho_i (P^ b)_i is
+// subtracted with rho_i = sum_j bf16(dS_ij) / sum_j bf16(P_ij); rho goes to rho_ws.
+template <typename T, int D, bool GP>
 __global__ void __launch_bounds__(kThreads) bob_row_kernel(
     const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ Vt, const T* __restrict__ O,
     const T* __restrict__ dO, const float* __restrict__ lse, const T* __restrict__ A, const T* __restrict__ Bm,
-    const T* __restrict__ C, T* __restrict__ gQ, T* __restrict__ gdO, float4* __restrict__ ws, int64_t N,
-    int64_t BH, float scale, int causal, int64_t G) {
+    const T* __restrict__ C, T* __restrict__ gQ, T* __restrict__ gdO, float4* __restrict__ ws,
+    float* __restrict__ rho_ws, int64_t N, int64_t BH, float scale, int causal, int64_t G) {
   constexpr int V = D / 32;
   extern __shared__ float sm[];
   float* Ks = sm;
@@ -328,10 +331,12 @@ __global__ void __launch_bounds__(kThreads) bob_row_kernel(
   const bool live = i < N;
   const size_t base = static_cast<size_t>(tl.bh) * N * D;
   const size_t kvbase = static_cast<size_t>(tl.bh / G) * N * D;  // K, V, b, c of the shared head
-  float q[V], g[V], av[V], o[V], X[V], Y[V], Z[V], U[V];
-  float Di = 0.f, Li = 0.f, E = 0.f, Fp = 0.f;
+  float q[V], g[V], av[V], o[V], X[V], Y[V], Z[V], U[V], Pb[GP ? V : 1];
+  float Di = 0.f, Li = 0.f, E = 0.f, Fp = 0.f, r = 0.f, sp = 0.f;
 #pragma unroll
   for (int t = 0; t < V; ++t) X[t] = Y[t] = Z[t] = U[t] = 0.f;
+#pragma unroll
+  for (int t = 0; t < (GP ? V : 1); ++t) Pb[t] = 0.f;
   if (live) {
     load_vec(Q + base + i * D, lane, q);
     load_vec(dO + base + i * D, lane, g);
@@ -369,39 +374,55 @@ __global__ void __launch_bounds__(kThreads) bob_row_kernel(
       const float w = G * ds + p * Hh;
       E += pg;
       Fp += w;
+      const float dsb = GP ? bf16r(ds) : ds;  // the dS of the dS b product
+      if constexpr (GP) {
+        const float ph = bf16r(p);
+        r += dsb;
+        sp += ph;
+#pragma unroll
+        for (int t = 0; t < V; ++t) Pb[t] = fmaf(ph, bv[t], Pb[t]);
+      }
 #pragma unroll
       for (int t = 0; t < V; ++t) {
         X[t] = fmaf(p, cv[t], fmaf(pg, vv[t], X[t]));
-        Y[t] = fmaf(ds, bv[t], fmaf(w, kv[t], Y[t]));
+        Y[t] = fmaf(dsb, bv[t], fmaf(w, kv[t], Y[t]));
         Z[t] = fmaf(ds, kv[t], Z[t]);
         U[t] = fmaf(p, kv[t], U[t]);
       }
     }
   }
   if (!live) return;
+  const float rho = GP ? r / sp : 0.f;
   float go[V], gq[V];
 #pragma unroll
   for (int t = 0; t < V; ++t) {
     go[t] = X[t] - E * o[t];
     gq[t] = scale * (Y[t] - E * Z[t] - Fp * U[t]);
+    if constexpr (GP) gq[t] -= scale * rho * Pb[t];
   }
   store_vec(gdO + base + i * D, lane, go);
   store_vec(gQ + base + i * D, lane, gq);
-  if (lane == 0) ws[tl.bh * N + i] = make_float4(Li, Di, E, Fp - E * Di);
+  if (lane == 0) {
+    ws[tl.bh * N + i] = make_float4(Li, Di, E, Fp - E * Di);
+    if constexpr (GP) rho_ws[tl.bh * N + i] = rho;
+  }
 }
 
 // ---------------------------------------------------------- BoB, columns
-template <typename T, int D>
+// GP: gK's dS^T a product sees the projected bf16(dS) - rho_i bf16(P) (rho from rho_ws).
+template <typename T, int D, bool GP>
 __global__ void __launch_bounds__(kThreads) bob_col_kernel(
     const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ Vt, const T* __restrict__ dO,
     const T* __restrict__ A, const T* __restrict__ Bm, const T* __restrict__ C, const float4* __restrict__ ws,
-    T* __restrict__ gK, T* __restrict__ gV, int64_t N, int64_t BHkv, float scale, int causal, int64_t G) {
+    const float* __restrict__ rho_ws, T* __restrict__ gK, T* __restrict__ gV, int64_t N, int64_t BHkv,
+    float scale, int causal, int64_t G) {
   constexpr int V = D / 32;
   extern __shared__ float sm[];
   float* Qs = sm;
   float* Gs = sm + kTile * D;
   float* As = sm + 2 * kTile * D;
   float4* Ss = reinterpret_cast<float4*>(sm + 3 * kTile * D);
+  float* Rs = reinterpret_cast<float*>(Ss + kTile);  // GP: rho of the staged rows
   const int64_t nblk = (N + kWarps - 1) / kWarps;
   const Tile tl = decode(BHkv, nblk, false);  // tl.bh: a key/value head
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -425,8 +446,10 @@ __global__ void __launch_bounds__(kThreads) bob_col_kernel(
     stage<T, D>(Qs, Q + qbase, i0, N);
     stage<T, D>(Gs, dO + qbase, i0, N);
     stage<T, D>(As, A + qbase, i0, N);
-    if (threadIdx.x < kTile)
+    if (threadIdx.x < kTile) {
       Ss[threadIdx.x] = (i0 + threadIdx.x < N) ? ws[hq * N + i0 + threadIdx.x] : make_float4(0, 0, 0, 0);
+      if constexpr (GP) Rs[threadIdx.x] = (i0 + threadIdx.x < N) ? rho_ws[hq * N + i0 + threadIdx.x] : 0.f;
+    }
     __syncthreads();
     if (!live) continue;
     const int ib = causal ? static_cast<int>(lmax(0, j - i0)) : 0;
@@ -446,10 +469,11 @@ __global__ void __launch_bounds__(kThreads) bob_col_kernel(
       const float ds = p * (dp - st.y);
       const float dpbar = p * (G - st.z);
       const float sbar = p * (G * (dp - st.y) - st.z * dp + Hh - st.w);
+      const float dsa = GP ? bf16r(ds) - Rs[ii] * bf16r(p) : ds;  // the dS of the dS^T a product
 #pragma unroll
       for (int t = 0; t < V; ++t) {
         aV[t] = fmaf(dpbar, gv[t], aV[t]);
-        aK[t] = fmaf(ds, a2[t], fmaf(sbar, qv[t], aK[t]));
+        aK[t] = fmaf(dsa, a2[t], fmaf(sbar, qv[t], aK[t]));
       }
     }
   }
@@ -564,14 +588,14 @@ cudaError_t bwd_t(const Problem& p, const void* Q, const void* K, const void* V,
   return cudaGetLastError();
 }
 
-template <typename T, int D>
+template <typename T, int D, bool GP>
 cudaError_t bob_t(const Problem& p, const void* Q, const void* K, const void* V, const void* O, const void* dO,
                   const float* lse, const void* a, const void* b, const void* c, void* gQ, void* gK, void* gV,
-                  void* gdO, float4* ws, int passes, cudaStream_t st) {
+                  void* gdO, float4* ws, float* rho_ws, int passes, cudaStream_t st) {
   const size_t sm_row = 4 * kTile * D * sizeof(float);
-  const size_t sm_col = 3 * kTile * D * sizeof(float) + kTile * sizeof(float4);
-  auto kr = bob_row_kernel<T, D>;
-  auto kc = bob_col_kernel<T, D>;
+  const size_t sm_col = 3 * kTile * D * sizeof(float) + kTile * (sizeof(float4) + sizeof(float));
+  auto kr = bob_row_kernel<T, D, GP>;
+  auto kc = bob_col_kernel<T, D, GP>;
   cudaError_t e = allow_smem(kr, sm_row);
   if (e == cudaSuccess) e = allow_smem(kc, sm_col);
   if (e != cudaSuccess) return e;
@@ -580,15 +604,15 @@ cudaError_t bob_t(const Problem& p, const void* Q, const void* K, const void* V,
     kr<<<grid_for(p), kThreads, sm_row, st>>>(
         static_cast<CT>(Q), static_cast<CT>(K), static_cast<CT>(V), static_cast<CT>(O), static_cast<CT>(dO), lse,
         static_cast<CT>(a), static_cast<CT>(b), static_cast<CT>(c), static_cast<T*>(gQ), static_cast<T*>(gdO), ws,
-        p.N, p.BH, p.scale, p.causal, p.group);
+        rho_ws, p.N, p.BH, p.scale, p.causal, p.group);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   if (!(passes & 2)) return cudaSuccess;
   kc<<<grid_for_cols(p), kThreads, sm_col, st>>>(static_cast<CT>(Q), static_cast<CT>(K), static_cast<CT>(V),
                                                   static_cast<CT>(dO), static_cast<CT>(a), static_cast<CT>(b),
-                                                  static_cast<CT>(c), ws, static_cast<T*>(gK), static_cast<T*>(gV),
-                                                  p.N, p.BHkv, p.scale, p.causal, p.group);
+                                                  static_cast<CT>(c), ws, rho_ws, static_cast<T*>(gK),
+                                                  static_cast<T*>(gV), p.N, p.BHkv, p.scale, p.causal, p.group);
   return cudaGetLastError();
 }
 
@@ -642,11 +666,21 @@ cudaError_t simt_bwd(const Problem& p, const void* Q, const void* K, const void*
 
 cudaError_t simt_bob(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
                      const void* dO, const float* lse, const void* a, const void* b, const void* c, void* gQ,
-                     void* gK, void* gV, void* gdO, float4* ws, int passes, cudaStream_t st) {
+                     void* gK, void* gV, void* gdO, bool gproj, float4* ws, int passes, cudaStream_t st) {
+  // GProj applies to bf16 only (float32 dS is never rounded); its coefficients follow the
+  // row states in the workspace (internal.h; this path keeps one float per row there).
+  float* rho_ws = reinterpret_cast<float*>(bob_rho_region(ws, p));
   cudaError_t e = cudaErrorInvalidValue;
   with_type(p.dtype, [&](auto t) {
+    using T = decltype(t);
     with_head_dim(p.d, [&](auto dd) {
-      e = bob_t<decltype(t), dd()>(p, Q, K, V, O, dO, lse, a, b, c, gQ, gK, gV, gdO, ws, passes, st);
+      if constexpr (std::is_same_v<T, __nv_bfloat16>) {
+        if (gproj) {
+          e = bob_t<T, dd(), true>(p, Q, K, V, O, dO, lse, a, b, c, gQ, gK, gV, gdO, ws, rho_ws, passes, st);
+          return;
+        }
+      }
+      e = bob_t<T, dd(), false>(p, Q, K, V, O, dO, lse, a, b, c, gQ, gK, gV, gdO, ws, nullptr, passes, st);
     });
   });
   return e;

@@ -34,6 +34,14 @@
 // ("FlashAttention bf16 gradient and GProj", "How the zero sum turns into a false
 // gradient").  The stored state F'_i = sum_j W_ij uses the fp32 sums.
 //
+// Shift: every output is unchanged when a per-row constant g0_i is added to the row
+// of G (dPbar and Sbar hold G only through G - E, and E moves with it).  A large
+// mean of b (or of K) puts such a constant, s q_i.mean(b), into G, and the bf16
+// copies (PG)^ and W^ would round it before E removes it.  The row pass therefore
+// works with G - g0, g0_i = G_i0 (key 0, visible to every row): (PG)^, W^, E and F'
+// are those of the shifted G (F' = sum_j W_ij is shift-free since sum_j dS_ij = 0),
+// and the stored E is shifted back for the column pass, which forms G - E in fp32.
+//
 // Row-pass TMEM: one 128-column tile region holding first [G | S] and then
 // [H | dP] of the same key block, the four bf16 operands (32 columns each, the A
 // operand of the output products), X, U, Y, Z 64 each = 512.  Column-pass TMEM:
@@ -92,7 +100,7 @@ struct RowLay {
   static constexpr int kStage = 4 * kTile;
   static constexpr int oc = 0, oV = kTile, ob = 2 * kTile, oKs = 3 * kTile;
   static constexpr int oRed = oStage + NS * kStage;
-  static constexpr int oBar = oRed + 12 * BM * 4;
+  static constexpr int oBar = oRed + 13 * BM * 4;
   static constexpr int bytes = oBar + 256;
   // TMEM: tile region [G | S] (Q b^T + a K^T, then Q K^T), later [H | dP] of the same
   // block; bf16 operands P^, (PG)^, dS^, W^; accumulators [X | U], [Y | Z].
@@ -103,15 +111,18 @@ struct RowLay {
 
 // PAD: head dim hd < D (zero-padded in shared memory).  The unpadded instance sees
 // the constant D, so its code is that of a kernel without the option.
-template <bool PAD>
+// GP: GProj on the rounded dS of gQ's dS b product (the pre-pass left P^ b in `pb`);
+// the coefficient rho_i goes to `rho_ws` for the column pass.
+template <bool PAD, bool GP>
 __global__ void __launch_bounds__(kThreads, 1)
     bob_row_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                    const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __nv_bfloat16* __restrict__ O,
                    const __nv_bfloat16* __restrict__ dO, const float* __restrict__ lse,
-                   __nv_bfloat16* __restrict__ gQ, __nv_bfloat16* __restrict__ gdO, float4* __restrict__ ws, int N,
-                   int Np, int nrb, int BH, float scale, float c, int causal, int G, int hd_arg) {
+                   __nv_bfloat16* __restrict__ gQ, __nv_bfloat16* __restrict__ gdO, float4* __restrict__ ws,
+                   const float* __restrict__ pb, float* __restrict__ rho_ws, int N, int Np, int nrb, int BH,
+                   float scale, float c, int causal, int G, int hd_arg) {
   const int hd = PAD ? hd_arg : D;
   using Lay = RowLay;
   constexpr int NS = Lay::NS;
@@ -286,6 +297,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     float accW0 = 0.f, accW1 = 0.f, accdS0 = 0.f, accdS1 = 0.f, accP0 = 0.f, accP1 = 0.f;
     const uint64_t c2 = tc::pk2f(c, c), s2 = tc::pk2f(scale, scale);
     const uint64_t nL2 = tc::pk2f(-L2, -L2), nD2 = tc::pk2f(-Dr, -Dr);
+    // The row's shift g0 lives in shared memory (red) and is read where it is used, so it
+    // holds no register through the block's [H | dP] phase, where the registers run out.
+    volatile float* g0p = red + 12 * BM + r;
     const int c0 = hf * 32;
     const uint32_t tOp = tmem + static_cast<uint32_t>(hf * 16) + lo;  // this thread's keys in the operand columns
     for (int j = 0; j < nkv; ++j) {
@@ -302,6 +316,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tmem_wait_ld();
       ptx::tc_fence_before();
       ptx::mbar_arrive(consumed_a);  // the MMA warp may now write [H | dP] into the tile region
+      if (j == 0) {  // the row's shift g0 = G at key 0, which every row sees
+        if (hf == 0) red[12 * BM + r] = scale * f(gv[0]);
+        tc::named_sync(1, kCompute);
+      }
       const int krel = j * BN + c0 - rb * BM;
       // last visible key of this row, relative to the thread's first key of the block
       const int klim = causal ? r - krel : N - 1 - (j * BN + c0);
@@ -309,6 +327,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t pP[16], pG[16], pS[16], pW[16];
       // P, PG from the [G | S] tiles (while [H | dP] is being computed)
       auto first = [&](auto masked) {
+        const float g0 = *g0p;
+        const uint64_t ng0 = tc::pk2f(-g0, -g0);
 #pragma unroll
         for (int t = 0; t < 32; t += 2) {
           const float2 arg = tc::unpk2(tc::fma2(tc::pk2(sv[t], sv[t + 1]), c2, nL2));
@@ -319,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const int idx = t >> 1;
           P2[idx] = tc::pk2f(p0, p1);
-          G2[idx] = tc::mul2(tc::pk2(gv[t], gv[t + 1]), s2);
+          G2[idx] = tc::fma2(tc::pk2(gv[t], gv[t + 1]), s2, ng0);  // G - g0
           const uint64_t pg2 = tc::mul2(P2[idx], G2[idx]);
           accE = tc::add2(accE, pg2);
           const float2 pg = tc::unpk2(pg2);
@@ -406,16 +426,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = 0; t < 32; t += 2) {
         const float o0 = bf16_lo(ow[t >> 1]), o1 = bf16_hi(ow[t >> 1]);
         go[t >> 1] = ptx::pack_bf16(f(xv[t]) - E * o0, f(xv[t + 1]) - E * o1);
-        gq[t >> 1] = ptx::pack_bf16(scale * (f(yv[t]) - E * f(zv[t]) - Fq * f(uv[t])),
-                                    scale * (f(yv[t + 1]) - E * f(zv[t + 1]) - Fq * f(uv[t + 1])));
       }
       uint4* d0 = reinterpret_cast<uint4*>(gdO + rowoff + c0);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) d0[u] = make_uint4(go[4 * u], go[4 * u + 1], go[4 * u + 2], go[4 * u + 3]);
+      if constexpr (GP) {  // Y holds dS^ b: subtract rho_i (P^ b)_i, rho_i = sum_j dS^_ij / sum_j P^_ij
+        const float rho = sdS / sP;
+        const float4* pp = reinterpret_cast<const float4*>(pb + (static_cast<size_t>(bh) * N + row) * D + c0);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float4 q = pp[u];
+          const float qv[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) yv[4 * u + e] = __float_as_uint(fmaf(-rho, qv[e], f(yv[4 * u + e])));
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < 32; t += 2)
+        gq[t >> 1] = ptx::pack_bf16(scale * (f(yv[t]) - E * f(zv[t]) - Fq * f(uv[t])),
+                                    scale * (f(yv[t + 1]) - E * f(zv[t + 1]) - Fq * f(uv[t + 1])));
       uint4* d1 = reinterpret_cast<uint4*>(gQ + rowoff + c0);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        d0[u] = make_uint4(go[4 * u], go[4 * u + 1], go[4 * u + 2], go[4 * u + 3]);
-        d1[u] = make_uint4(gq[4 * u], gq[4 * u + 1], gq[4 * u + 2], gq[4 * u + 3]);
-      }
+      for (int u = 0; u < 4; ++u) d1[u] = make_uint4(gq[4 * u], gq[4 * u + 1], gq[4 * u + 2], gq[4 * u + 3]);
     }
     if (hf == 0 && row < Np) {  // row states, negated, pair-interleaved (see the column pass)
       // F' = F + E D = sum_j W_ij is what the column pass needs (its (G - E)(dP - D) form).
@@ -425,9 +457,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t k2 = row & ~static_cast<int64_t>(1);
       const int odd = static_cast<int>(row & 1);
       wf[k2 * 4 + odd] = live ? -L2 : 0.f;
-      wf[k2 * 4 + 2 + odd] = live ? -E : 0.f;
+      wf[k2 * 4 + 2 + odd] = live ? -(E + *g0p) : 0.f;  // the unshifted E
       wf[(k2 + 1) * 4 + odd] = live ? -Dr : 0.f;
       wf[(k2 + 1) * 4 + 2 + odd] = live ? -Fp : 0.f;
+    }
+    if constexpr (GP) {  // -rho_i, one float per row (rows up to the pitch written, as zeros past N)
+      const int64_t pitch = bob_rho_pitch(N);
+      if (hf == 0 && row < pitch) rho_ws[static_cast<size_t>(bh) * pitch + row] = live ? -(sdS / sP) : 0.f;
     }
   }
 
@@ -451,30 +487,36 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Per element the compute warps form
 //   P = 2^(S c - L log2 e),  dPbar = P (G - E),  dS = P (dP - D),
 //   Sbar = P ((G - E)(dP - D) + H - F')          (F' = F + E D, stored by the row pass)
-struct ColLay {
+// GP (GProj): the stage also holds the 64 queries' coefficients -rho (256 bytes behind
+// the states); the compute warps write bf16(-rho_i P_ij) into TMEM (cPT) and the output
+// warp adds that operand times a_i to gK, the key term of the projection.
+template <bool GP>
+struct ColLayT {
   static constexpr int NS = 8;
   static constexpr int kStat = BN * 16;
-  static constexpr int kStage = 3 * kTile + 2048;  // [Q_i; a_i], dO_i, row states (padded to a 1 KB multiple)
+  static constexpr int kRho = BN * 4;
+  static constexpr int kStage = 3 * kTile + 2048;  // [Q_i; a_i], dO_i, row states (+ GProj coefficients)
   static constexpr int oStage = 0;
   static constexpr int oBar = oStage + NS * kStage;
   static constexpr int bytes = oBar + 256;
   // TMEM: tile region, held bf16 A operands K, b, V, c (32 columns each), the bf16
-  // output operands dPbar, dS, Sbar (32 each), accumulators gV, gK.
-  static constexpr int cT = 0, cK = 128, cB = 160, cV = 192, cC = 224, cOp = 256, cgV = 352, cgK = 416;
+  // output operands dPbar, dS, Sbar (32 each), accumulators gV, gK; with GP P^ (32).
+  static constexpr int cT = 0, cK = 128, cB = 160, cV = 192, cC = 224, cOp = 256, cgV = 352, cgK = 416, cPT = 480;
 };
+static_assert(ColLayT<true>::bytes <= 232448, "column pass shared memory");
 
 // GR: grouped key/value heads (G > 1).  The G == 1 instance keeps the plain tile loop.
-// PAD as in the row pass.
-template <bool GR, bool PAD>
+// PAD as in the row pass.  GP as in ColLayT (tmRho: the coefficients, laid out as the states).
+template <bool GR, bool PAD, bool GP>
 __global__ void __launch_bounds__(kThreads, 1)
     bob_col_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmdO, const __grid_constant__ CUtensorMap tmSt,
-                   const __nv_bfloat16* __restrict__ Kp, const __nv_bfloat16* __restrict__ Bp,
+                   const __grid_constant__ CUtensorMap tmRho, const __nv_bfloat16* __restrict__ Kp, const __nv_bfloat16* __restrict__ Bp,
                    const __nv_bfloat16* __restrict__ Vp, const __nv_bfloat16* __restrict__ Cp,
                    __nv_bfloat16* __restrict__ gK, __nv_bfloat16* __restrict__ gV, int N, int BHkv, float scale,
                    float c, int causal, int G, int hd_arg) {
   const int hd = PAD ? hd_arg : D;
-  using Lay = ColLay;
+  using Lay = ColLayT<GP>;
   constexpr int NS = Lay::NS;
   extern __shared__ __align__(1024) uint8_t sm[];
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + Lay::oBar);
@@ -534,15 +576,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::prefetch_tmap(&tmA);
       ptx::prefetch_tmap(&tmdO);
       ptx::prefetch_tmap(&tmSt);
+      if constexpr (GP) ptx::prefetch_tmap(&tmRho);
       for (int t = 0; t < nt; ++t) {
         const int h = GR ? t / ntile : 0, s = t % NS, i = i0 + t - h * ntile, bh = GR ? kvh * G + h : kvh;
         if (t >= NS) wait(&empty[s], ((t / NS) - 1) & 1);
         uint8_t* st = sm + Lay::oStage + s * Lay::kStage;
-        ptx::mbar_expect_tx(&full[s], 3 * kTile + Lay::kStat);
+        ptx::mbar_expect_tx(&full[s], 3 * kTile + Lay::kStat + (GP ? Lay::kRho : 0));
         ptx::tma_load_3d(st, &tmQ, &full[s], 0, i * BN, bh);
         ptx::tma_load_3d(st + kTile, &tmA, &full[s], 0, i * BN, bh);
         ptx::tma_load_3d(st + 2 * kTile, &tmdO, &full[s], 0, i * BN, bh);
         ptx::tma_load_3d(st + 3 * kTile, &tmSt, &full[s], 0, i * BN, bh);
+        if constexpr (GP) ptx::tma_load_3d(st + 3 * kTile + Lay::kStat, &tmRho, &full[s], 0, i * (BN / 4), bh);
       }
       for (int t = (nt > NS ? nt - NS : 0); t < nt; ++t) wait(&empty[t % NS], (t / NS) & 1);
     }
@@ -593,6 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dAm = tc::mnmajor_desc(sSt + kTile, BN, 0);       // a_i, MN-major
       const uint64_t ddOm = tc::mnmajor_desc(sSt + 2 * kTile, BN, 0);  // dO_i, MN-major
       const uint32_t tOp = tmem + Lay::cOp, tgV = tmem + Lay::cgV, tgK = tmem + Lay::cgK;
+      const uint32_t tPT = tmem + Lay::cPT;
       for (int t = 0; t < nt; ++t) {
         const int s = t % NS;
         const uint32_t so = static_cast<uint32_t>(s * Lay::kStage);
@@ -607,6 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::mma_ts_e(tgV, tOp + k * 8, tc::desc_add(ddOm, kb2), idO, acc);
           ptx::mma_ts_e(tgK, tOp + 32 + k * 8, tc::desc_add(dAm, kb2), idO, acc);
           ptx::mma_ts_e(tgK, tOp + 64 + k * 8, tc::desc_add(dQm, kb2), idO, 1u);
+          if constexpr (GP) ptx::mma_ts_e(tgK, tPT + k * 8, tc::desc_add(dAm, kb2), idO, 1u);  // (-rho P)^T a_i
         }
         ptx::mma_commit_e(&empty[s]);
         ptx::mma_commit_e(out_done);
@@ -668,7 +714,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_before();
       ptx::mbar_arrive(consumed_a);  // the tile warp may now write [dP^T | H^T]
       uint64_t P2[16], GE2[16];
-      uint32_t pDP[16], pDS[16], pSB[16];
+      uint32_t pDP[16], pDS[16], pSB[16], pPT[GP ? 16 : 1];
+      // GP: -rho of this thread's 32 queries (the stage's coefficient tile)
+      const float4* nrho = reinterpret_cast<const float4*>(sm + Lay::oStage + s * Lay::kStage + 3 * kTile +
+                                                           Lay::kStat) + c0 / 4;
       auto first = [&](auto masked) {  // P and P (G - E) from [S^T | G^T]
 #pragma unroll
         for (int u = 0; u < 32; u += 2) {
@@ -712,7 +761,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         pDS[idx] = ptx::pack_bf16(vds.x, vds.y);
         pSB[idx] = ptx::pack_bf16(vsb.x, vsb.y);
       }
+      if constexpr (GP) {  // bf16(-rho_i P_ij), formed once dP and H are out of the registers
+#pragma unroll
+        for (int u = 0; u < 32; u += 4) {
+          const float4 r4 = nrho[u >> 2];
+          const float2 a0 = tc::unpk2(tc::mul2(P2[u >> 1], tc::pk2f(r4.x, r4.y)));
+          const float2 a1 = tc::unpk2(tc::mul2(P2[(u >> 1) + 1], tc::pk2f(r4.z, r4.w)));
+          pPT[u >> 1] = ptx::pack_bf16(a0.x, a0.y);
+          pPT[(u >> 1) + 1] = ptx::pack_bf16(a1.x, a1.y);
+        }
+      }
       if (t > 0) wait(out_done, (t - 1) & 1);  // block t-1's products have read the operand columns
+      if constexpr (GP) ptx::tmem_st16(tmem + Lay::cPT + static_cast<uint32_t>(hf * 16) + lo, pPT);
       ptx::tmem_st16(tOpT, pDP);
       ptx::tmem_st16(tOpT + 32, pDS);
       ptx::tmem_st16(tOpT + 64, pSB);  // completed (and `ready` arrived) at the next block's loads
@@ -756,10 +816,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 cudaError_t tc_bob(const Problem& p, const void* Q, const void* K, const void* V, const void* O, const void* dO,
                    const float* lse, const void* a, const void* b, const void* cc, void* gQ, void* gK, void* gV,
-                   void* gdO, float4* ws, int passes, cudaStream_t st) {
+                   void* gdO, bool gproj, float4* ws, int passes, cudaStream_t st) {
   if (p.d > D) return cudaErrorInvalidValue;
   alignas(64) CUtensorMap q128, do128, a128, k64, v64, b64, c64;
-  alignas(64) CUtensorMap q64, a64, do64, s64;
+  alignas(64) CUtensorMap q64, a64, do64, s64, r64;
+  // GProj: the coefficients follow the states, P^ b follows them (see internal.h).
+  float4* rho = gproj ? bob_rho_region(ws, p) : ws;
+  float* pbuf = gproj ? bob_pb_region(ws, p) : nullptr;
   const int64_t N = p.N, BH = p.BH, Np = (p.N + 1) & ~static_cast<int64_t>(1), d = p.d;
   // Tensor maps over the true head dim d <= D: TMA zero-fills the padding columns.
   if (!make_tmap_bf16(&q128, Q, N, d, BH, BM) || !make_tmap_bf16(&do128, dO, N, d, BH, BM) ||
@@ -767,29 +830,35 @@ cudaError_t tc_bob(const Problem& p, const void* Q, const void* K, const void* V
       !make_tmap_bf16(&v64, V, N, d, p.BHkv, BN) || !make_tmap_bf16(&b64, b, N, d, p.BHkv, BN) ||
       !make_tmap_bf16(&c64, cc, N, d, p.BHkv, BN) || !make_tmap_bf16(&q64, Q, N, d, BH, BN) ||
       !make_tmap_bf16(&a64, a, N, d, BH, BN) || !make_tmap_bf16(&do64, dO, N, d, BH, BN) ||
-      !make_tmap_stats(&s64, ws, Np, BH, BN))
+      !make_tmap_stats(&s64, ws, Np, BH, BN) ||
+      !make_tmap_stats(&r64, rho, bob_rho_pitch(N) / 4, BH, BN / 4))  // 64 floats = 16 float4 rows
     return cudaErrorInvalidValue;
   const float c = p.scale * kLog2e;
   const int nrb = static_cast<int>((N + BM - 1) / BM);
   cudaError_t e = cudaSuccess;
+  // The GProj instances take the general forms (runtime head dim, grouped tile loop),
+  // which also serve d = 64 and ungrouped heads.
   if (passes & 1) {
-  auto row = d < D ? bob_row_kernel<true> : bob_row_kernel<false>;
-  e = cudaFuncSetAttribute(row, cudaFuncAttributeMaxDynamicSharedMemorySize, RowLay::bytes);
-  if (e != cudaSuccess) return e;
-  row<<<static_cast<unsigned>(nrb * BH), kThreads, RowLay::bytes, st>>>(
-      q128, do128, a128, k64, v64, b64, c64, static_cast<const __nv_bfloat16*>(O),
-      static_cast<const __nv_bfloat16*>(dO), lse, static_cast<__nv_bfloat16*>(gQ), static_cast<__nv_bfloat16*>(gdO),
-      ws, static_cast<int>(N), static_cast<int>(Np), nrb, static_cast<int>(BH), p.scale, c, p.causal,
-      p.group, static_cast<int>(d));
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (gproj && (e = tc_bob_pb(p, Q, K, b, lse, pbuf, st)) != cudaSuccess) return e;
+    auto row = gproj ? bob_row_kernel<true, true> : d < D ? bob_row_kernel<true, false> : bob_row_kernel<false, false>;
+    e = cudaFuncSetAttribute(row, cudaFuncAttributeMaxDynamicSharedMemorySize, RowLay::bytes);
+    if (e != cudaSuccess) return e;
+    row<<<static_cast<unsigned>(nrb * BH), kThreads, RowLay::bytes, st>>>(
+        q128, do128, a128, k64, v64, b64, c64, static_cast<const __nv_bfloat16*>(O),
+        static_cast<const __nv_bfloat16*>(dO), lse, static_cast<__nv_bfloat16*>(gQ),
+        static_cast<__nv_bfloat16*>(gdO), ws, pbuf, reinterpret_cast<float*>(rho), static_cast<int>(N),
+        static_cast<int>(Np), nrb, static_cast<int>(BH), p.scale, c, p.causal, p.group, static_cast<int>(d));
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (!(passes & 2)) return cudaSuccess;
-  auto col = p.group > 1 ? (d < D ? bob_col_kernel<true, true> : bob_col_kernel<true, false>)
-                          : (d < D ? bob_col_kernel<false, true> : bob_col_kernel<false, false>);
-  e = cudaFuncSetAttribute(col, cudaFuncAttributeMaxDynamicSharedMemorySize, ColLay::bytes);
+  auto col = gproj ? bob_col_kernel<true, true, true>
+             : p.group > 1 ? (d < D ? bob_col_kernel<true, true, false> : bob_col_kernel<true, false, false>)
+                           : (d < D ? bob_col_kernel<false, true, false> : bob_col_kernel<false, false, false>);
+  const int cbytes = gproj ? ColLayT<true>::bytes : ColLayT<false>::bytes;
+  e = cudaFuncSetAttribute(col, cudaFuncAttributeMaxDynamicSharedMemorySize, cbytes);
   if (e != cudaSuccess) return e;
-  col<<<static_cast<unsigned>(nrb * p.BHkv), kThreads, ColLay::bytes, st>>>(
-      q64, a64, do64, s64, static_cast<const __nv_bfloat16*>(K), static_cast<const __nv_bfloat16*>(b),
+  col<<<static_cast<unsigned>(nrb * p.BHkv), kThreads, cbytes, st>>>(
+      q64, a64, do64, s64, r64, static_cast<const __nv_bfloat16*>(K), static_cast<const __nv_bfloat16*>(b),
       static_cast<const __nv_bfloat16*>(V), static_cast<const __nv_bfloat16*>(cc), static_cast<__nv_bfloat16*>(gK),
       static_cast<__nv_bfloat16*>(gV), static_cast<int>(N), static_cast<int>(p.BHkv), p.scale, c, p.causal,
       p.group, static_cast<int>(d));

@@ -4,7 +4,7 @@
 //
 // "FlashBoB: second-order attention", "Two scalar states replace quadratic
 // tensors".  The quantities, the two scalar states E and F', the consistent-rounding
-// state of the row pass and every hand-off between the warps are those of the d = 64
+// state and the per-row shift of G of the row pass, and every hand-off between the warps are those of the d = 64
 // kernels (see the header of tc_bob.cu); only the division of the work differs.
 //
 // Why split.  At d = 128 the row pass's four d-wide fp32 accumulators X, U, Y, Z
@@ -64,8 +64,8 @@ struct RowLay {
   static constexpr int kHalf = 4 * kSlab;  // c, V, b, K of one 64-column half
   static constexpr int kStage = 2 * kHalf;
   static constexpr int oc = 0, oV = kSlab, ob = 2 * kSlab, oKs = 3 * kSlab;
-  static constexpr int oRed = oStage + NS * kStage;  // D_i halves; the end-of-row sums reuse Q's slabs
-  static constexpr int oBar = oRed + 2 * BM * 4;
+  static constexpr int oRed = oStage + NS * kStage;  // D_i halves, the row shifts; the end-of-row sums reuse Q's slabs
+  static constexpr int oBar = oRed + 3 * BM * 4;
   static constexpr int bytes = oBar + 256;
   // TMEM as at d = 64: tile region [G | S] then [H | dP]; operands P^, (PG)^, dS^, W^;
   // accumulators [X | U], [Y | Z] of this CTA's 64 output columns.
@@ -75,6 +75,9 @@ struct RowLay {
 };
 static_assert(RowLay::bytes <= 232448, "row pass shared memory");
 
+// GP: GProj on the rounded dS of gQ's dS b product, as at d = 64 (P^ b from the pre-pass
+// in `pb`, 128 columns per row; the coefficient to `rho_ws`, by CTA h = 0).
+template <bool GP>
 __global__ void __launch_bounds__(kThreads, 1)
     bob128_row_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                       const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmK,
@@ -82,7 +85,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tmC, const __nv_bfloat16* __restrict__ O,
                       const __nv_bfloat16* __restrict__ dO, const float* __restrict__ lse,
                       __nv_bfloat16* __restrict__ gQ, __nv_bfloat16* __restrict__ gdO, float4* __restrict__ ws,
-                      int N, int Np, int nrb, int BH, float scale, float c, int causal, int G, int hd) {
+                      const float* __restrict__ pb, float* __restrict__ rho_ws, int N, int Np, int nrb, int BH,
+                      float scale, float c, int causal, int G, int hd) {
   using Lay = RowLay;
   constexpr int NS = Lay::NS;
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -262,6 +266,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     float accW0 = 0.f, accW1 = 0.f, accdS0 = 0.f, accdS1 = 0.f, accP0 = 0.f, accP1 = 0.f;
     const uint64_t c2 = tc::pk2f(c, c), s2 = tc::pk2f(scale, scale);
     const uint64_t nL2 = tc::pk2f(-L2, -L2), nD2 = tc::pk2f(-Dr, -Dr);
+    // The row's shift g0 lives in shared memory (red) and is read where it is used, so it
+    // holds no register through the block's [H | dP] phase, where the registers run out.
+    volatile float* g0p = red + 2 * BM + r;
     const int c0 = hf * 32;
     const uint32_t tOp = tmem + static_cast<uint32_t>(hf * 16) + lo;
     for (int j = 0; j < nkv; ++j) {
@@ -273,11 +280,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tmem_wait_ld();
       ptx::tc_fence_before();
       ptx::mbar_arrive(consumed_a);
+      if (j == 0) {  // the row's shift g0 = G at key 0 (the same in both CTAs of the pair)
+        if (hf == 0) red[2 * BM + r] = scale * f(gv[0]);
+        tc::named_sync(1, kCompute);
+      }
       const int krel = j * BN + c0 - rb * BM;
       const int klim = causal ? r - krel : N - 1 - (j * BN + c0);
       uint64_t P2[16], G2[16];
       uint32_t pP[16], pG[16], pS[16], pW[16];
       auto first = [&](auto masked) {
+        const float g0 = *g0p;
+        const uint64_t ng0 = tc::pk2f(-g0, -g0);
 #pragma unroll
         for (int t = 0; t < 32; t += 2) {
           const float2 arg = tc::unpk2(tc::fma2(tc::pk2(sv[t], sv[t + 1]), c2, nL2));
@@ -288,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const int idx = t >> 1;
           P2[idx] = tc::pk2f(p0, p1);
-          G2[idx] = tc::mul2(tc::pk2(gv[t], gv[t + 1]), s2);
+          G2[idx] = tc::fma2(tc::pk2(gv[t], gv[t + 1]), s2, ng0);  // G - g0
           const uint64_t pg2 = tc::mul2(P2[idx], G2[idx]);
           accE = tc::add2(accE, pg2);
           const float2 pg = tc::unpk2(pg2);
@@ -377,25 +390,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = 0; t < 32; t += 2) {
         const float o0 = bf16_lo(ow[t >> 1]), o1 = bf16_hi(ow[t >> 1]);
         go[t >> 1] = ptx::pack_bf16(f(xv[t]) - E * o0, f(xv[t + 1]) - E * o1);
-        gq[t >> 1] = ptx::pack_bf16(scale * (f(yv[t]) - E * f(zv[t]) - Fq * f(uv[t])),
-                                    scale * (f(yv[t + 1]) - E * f(zv[t + 1]) - Fq * f(uv[t + 1])));
       }
       uint4* d0 = reinterpret_cast<uint4*>(gdO + rowoff + gc0);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) d0[u] = make_uint4(go[4 * u], go[4 * u + 1], go[4 * u + 2], go[4 * u + 3]);
+      if constexpr (GP) {  // Y holds dS^ b: subtract rho_i (P^ b)_i
+        const float rho = sdS / sP;
+        const float4* pp = reinterpret_cast<const float4*>(pb + (static_cast<size_t>(bh) * N + row) * D + gc0);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float4 q = pp[u];
+          const float qv[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) yv[4 * u + e] = __float_as_uint(fmaf(-rho, qv[e], f(yv[4 * u + e])));
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < 32; t += 2)
+        gq[t >> 1] = ptx::pack_bf16(scale * (f(yv[t]) - E * f(zv[t]) - Fq * f(uv[t])),
+                                    scale * (f(yv[t + 1]) - E * f(zv[t + 1]) - Fq * f(uv[t + 1])));
       uint4* d1 = reinterpret_cast<uint4*>(gQ + rowoff + gc0);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        d0[u] = make_uint4(go[4 * u], go[4 * u + 1], go[4 * u + 2], go[4 * u + 3]);
-        d1[u] = make_uint4(gq[4 * u], gq[4 * u + 1], gq[4 * u + 2], gq[4 * u + 3]);
-      }
+      for (int u = 0; u < 4; ++u) d1[u] = make_uint4(gq[4 * u], gq[4 * u + 1], gq[4 * u + 2], gq[4 * u + 3]);
     }
     if (half == 0 && hf == 0 && row < Np) {  // row states, negated and pair-interleaved, once per row
       float* wf = reinterpret_cast<float*>(ws) + static_cast<size_t>(bh) * Np * 4;
       const int64_t k2 = row & ~static_cast<int64_t>(1);
       const int odd = static_cast<int>(row & 1);
       wf[k2 * 4 + odd] = live ? -L2 : 0.f;
-      wf[k2 * 4 + 2 + odd] = live ? -E : 0.f;
+      wf[k2 * 4 + 2 + odd] = live ? -(E + *g0p) : 0.f;  // the unshifted E
       wf[(k2 + 1) * 4 + odd] = live ? -Dr : 0.f;
       wf[(k2 + 1) * 4 + 2 + odd] = live ? -Fp : 0.f;
+    }
+    if constexpr (GP) {  // -rho_i, one float per row (rows up to the pitch written, as zeros past N)
+      const int64_t pitch = bob_rho_pitch(N);
+      if (half == 0 && hf == 0 && row < pitch)
+        rho_ws[static_cast<size_t>(bh) * pitch + row] = live ? -(sdS / sP) : 0.f;
     }
   }
 
@@ -408,31 +438,38 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ============================================================= column pass
-struct ColLay {
+// GP (GProj): the stage also holds the queries' coefficients -rho (256 bytes behind
+// the states); bf16(-rho_i P_ij) goes into TMEM (cPT) and the output warp adds that
+// operand times this CTA's half of a_i to gK, as at d = 64.
+template <bool GP>
+struct ColLayT {
   static constexpr int NS = 3;
   static constexpr int oV = 0, oC = 2 * kHeldSlab;  // held V, c: two slabs each
   static constexpr int oStage = 4 * kHeldSlab;
   static constexpr int kHalf = 3 * kSlab;  // Q, a, dO of one 64-column half
   static constexpr int kStat = BN * 16;
-  static constexpr int kStage = 2 * kHalf + kStat;  // a multiple of 1 KB
+  static constexpr int kRho = BN * 4;
+  static constexpr int kStage = 2 * kHalf + kStat + (GP ? 1024 : 0);  // a multiple of 1 KB
   static constexpr int oBar = oStage + NS * kStage;
   static constexpr int bytes = oBar + 256;
   // TMEM: tile region, held K and b (A operands, 64 columns each at d = 128), the bf16
-  // output operands dPbar, dS, Sbar (32 each), accumulators gV, gK of the 64 columns.
-  static constexpr int cT = 0, cK = 128, cB = 192, cOp = 256, cgV = 352, cgK = 416;
+  // output operands dPbar, dS, Sbar (32 each), accumulators gV, gK of the 64 columns;
+  // with GP P^ (32).
+  static constexpr int cT = 0, cK = 128, cB = 192, cOp = 256, cgV = 352, cgK = 416, cPT = 480;
 };
-static_assert(ColLay::bytes <= 232448, "column pass shared memory");
-static_assert(ColLay::kStage % 1024 == 0, "stages stay 1024-byte aligned");
+static_assert(ColLayT<true>::bytes <= 232448, "column pass shared memory");
+static_assert(ColLayT<false>::kStage % 1024 == 0 && ColLayT<true>::kStage % 1024 == 0,
+              "stages stay 1024-byte aligned");
 
-template <bool GR>
+template <bool GR, bool GP>
 __global__ void __launch_bounds__(kThreads, 1)
     bob128_col_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmdO, const __grid_constant__ CUtensorMap tmSt,
-                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmC,
+                      const __grid_constant__ CUtensorMap tmRho, const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmC,
                       const __nv_bfloat16* __restrict__ Kp, const __nv_bfloat16* __restrict__ Bp,
                       __nv_bfloat16* __restrict__ gK, __nv_bfloat16* __restrict__ gV, int N, int BHkv,
                       float scale, float c, int causal, int G, int hd) {
-  using Lay = ColLay;
+  using Lay = ColLayT<GP>;
   constexpr int NS = Lay::NS;
   extern __shared__ __align__(1024) uint8_t sm[];
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + Lay::oBar);
@@ -504,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int h = GR ? t / ntile : 0, s = t % NS, i = i0 + t - h * ntile, bh = GR ? kvh * G + h : kvh;
         if (t >= NS) wait(&empty[s], ((t / NS) - 1) & 1);
         uint8_t* st = sm + Lay::oStage + s * Lay::kStage;
-        ptx::mbar_expect_tx(&full[s], 6 * kSlab + Lay::kStat);
+        ptx::mbar_expect_tx(&full[s], 6 * kSlab + Lay::kStat + (GP ? Lay::kRho : 0));
         for (int cc = 0; cc < 2; ++cc) {
           uint8_t* hs = st + cc * Lay::kHalf;
           ptx::tma_load_3d(hs, &tmQ, &full[s], cc * 64, i * BN, bh);
@@ -512,6 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tma_load_3d(hs + 2 * kSlab, &tmdO, &full[s], cc * 64, i * BN, bh);
         }
         ptx::tma_load_3d(st + 2 * Lay::kHalf, &tmSt, &full[s], 0, i * BN, bh);
+        if constexpr (GP) ptx::tma_load_3d(st + 2 * Lay::kHalf + Lay::kStat, &tmRho, &full[s], 0, i * (BN / 4), bh);
       }
       for (int t = (nt > NS ? nt - NS : 0); t < nt; ++t) wait(&empty[t % NS], (t / NS) & 1);
     }
@@ -565,6 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dAm = tc::mnmajor_desc(sH + kSlab, BN, 0);         // ... of a_i
       const uint64_t ddOm = tc::mnmajor_desc(sH + 2 * kSlab, BN, 0);    // ... of dO_i
       const uint32_t tOp = tmem + Lay::cOp, tgV = tmem + Lay::cgV, tgK = tmem + Lay::cgK;
+      const uint32_t tPT = tmem + Lay::cPT;
       for (int t = 0; t < nt; ++t) {
         const int s = t % NS;
         const uint32_t so = static_cast<uint32_t>(s * Lay::kStage);
@@ -578,6 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::mma_ts_e(tgV, tOp + k * 8, tc::desc_add(ddOm, kb2), idO, acc);
           ptx::mma_ts_e(tgK, tOp + 32 + k * 8, tc::desc_add(dAm, kb2), idO, acc);
           ptx::mma_ts_e(tgK, tOp + 64 + k * 8, tc::desc_add(dQm, kb2), idO, 1u);
+          if constexpr (GP) ptx::mma_ts_e(tgK, tPT + k * 8, tc::desc_add(dAm, kb2), idO, 1u);  // (-rho P)^T a_i
         }
         ptx::mma_commit_e(&empty[s]);
         ptx::mma_commit_e(out_done);
@@ -636,7 +676,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_before();
       ptx::mbar_arrive(consumed_a);
       uint64_t P2[16], GE2[16];
-      uint32_t pDP[16], pDS[16], pSB[16];
+      uint32_t pDP[16], pDS[16], pSB[16], pPT[GP ? 16 : 1];
+      // GP: -rho of this thread's 32 queries (the stage's coefficient tile)
+      const float4* nrho = reinterpret_cast<const float4*>(sm + Lay::oStage + s * Lay::kStage + 2 * Lay::kHalf +
+                                                           Lay::kStat) + c0 / 4;
       auto first = [&](auto masked) {
 #pragma unroll
         for (int u = 0; u < 32; u += 2) {
@@ -678,7 +721,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         pDS[idx] = ptx::pack_bf16(vds.x, vds.y);
         pSB[idx] = ptx::pack_bf16(vsb.x, vsb.y);
       }
+      if constexpr (GP) {  // bf16(-rho_i P_ij), formed once dP and H are out of the registers
+#pragma unroll
+        for (int u = 0; u < 32; u += 4) {
+          const float4 r4 = nrho[u >> 2];
+          const float2 a0 = tc::unpk2(tc::mul2(P2[u >> 1], tc::pk2f(r4.x, r4.y)));
+          const float2 a1 = tc::unpk2(tc::mul2(P2[(u >> 1) + 1], tc::pk2f(r4.z, r4.w)));
+          pPT[u >> 1] = ptx::pack_bf16(a0.x, a0.y);
+          pPT[(u >> 1) + 1] = ptx::pack_bf16(a1.x, a1.y);
+        }
+      }
       if (t > 0) wait(out_done, (t - 1) & 1);
+      if constexpr (GP) ptx::tmem_st16(tmem + Lay::cPT + static_cast<uint32_t>(hf * 16) + lo, pPT);
       ptx::tmem_st16(tOpT, pDP);
       ptx::tmem_st16(tOpT + 32, pDS);
       ptx::tmem_st16(tOpT + 64, pSB);
@@ -722,10 +776,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 cudaError_t tc_bob128(const Problem& p, const void* Q, const void* K, const void* V, const void* O, const void* dO,
                       const float* lse, const void* a, const void* b, const void* cc, void* gQ, void* gK, void* gV,
-                      void* gdO, float4* ws, int passes, cudaStream_t st) {
+                      void* gdO, bool gproj, float4* ws, int passes, cudaStream_t st) {
   if (p.d > D || p.d <= DH) return cudaErrorInvalidValue;
   alignas(64) CUtensorMap q128, do128, a128, k64, v64, b64, c64;
-  alignas(64) CUtensorMap q64, a64, do64, s64, v128, c128;
+  alignas(64) CUtensorMap q64, a64, do64, s64, v128, c128, r64;
+  float4* rho = gproj ? bob_rho_region(ws, p) : ws;  // GProj coefficients, then P^ b (internal.h)
+  float* pbuf = gproj ? bob_pb_region(ws, p) : nullptr;
   const int64_t N = p.N, BH = p.BH, Np = (p.N + 1) & ~static_cast<int64_t>(1), d = p.d;
   // Tensor maps over the true head dim d (64 < d <= 128): TMA zero-fills the padding columns.
   if (!make_tmap_bf16(&q128, Q, N, d, BH, BM) || !make_tmap_bf16(&do128, dO, N, d, BH, BM) ||
@@ -734,27 +790,33 @@ cudaError_t tc_bob128(const Problem& p, const void* Q, const void* K, const void
       !make_tmap_bf16(&c64, cc, N, d, p.BHkv, BN) || !make_tmap_bf16(&q64, Q, N, d, BH, BN) ||
       !make_tmap_bf16(&a64, a, N, d, BH, BN) || !make_tmap_bf16(&do64, dO, N, d, BH, BN) ||
       !make_tmap_stats(&s64, ws, Np, BH, BN) || !make_tmap_bf16(&v128, V, N, d, p.BHkv, BM) ||
-      !make_tmap_bf16(&c128, cc, N, d, p.BHkv, BM))
+      !make_tmap_bf16(&c128, cc, N, d, p.BHkv, BM) ||
+      !make_tmap_stats(&r64, rho, bob_rho_pitch(N) / 4, BH, BN / 4))  // 64 floats = 16 float4 rows
     return cudaErrorInvalidValue;
   const float c = p.scale * kLog2e;
   const int nrb = static_cast<int>((N + BM - 1) / BM);
   cudaError_t e = cudaSuccess;
   if (passes & 1) {
-    e = cudaFuncSetAttribute(bob128_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, RowLay::bytes);
+    if (gproj && (e = tc_bob_pb(p, Q, K, b, lse, pbuf, st)) != cudaSuccess) return e;
+    auto row = gproj ? bob128_row_kernel<true> : bob128_row_kernel<false>;
+    e = cudaFuncSetAttribute(row, cudaFuncAttributeMaxDynamicSharedMemorySize, RowLay::bytes);
     if (e != cudaSuccess) return e;
-    bob128_row_kernel<<<static_cast<unsigned>(2 * nrb * BH), kThreads, RowLay::bytes, st>>>(
+    row<<<static_cast<unsigned>(2 * nrb * BH), kThreads, RowLay::bytes, st>>>(
         q128, do128, a128, k64, v64, b64, c64, static_cast<const __nv_bfloat16*>(O),
         static_cast<const __nv_bfloat16*>(dO), lse, static_cast<__nv_bfloat16*>(gQ),
-        static_cast<__nv_bfloat16*>(gdO), ws, static_cast<int>(N), static_cast<int>(Np), nrb,
-        static_cast<int>(BH), p.scale, c, p.causal, p.group, static_cast<int>(d));
+        static_cast<__nv_bfloat16*>(gdO), ws, pbuf, reinterpret_cast<float*>(rho), static_cast<int>(N),
+        static_cast<int>(Np), nrb, static_cast<int>(BH), p.scale, c, p.causal, p.group, static_cast<int>(d));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (!(passes & 2)) return cudaSuccess;
-  auto col = p.group > 1 ? bob128_col_kernel<true> : bob128_col_kernel<false>;
-  e = cudaFuncSetAttribute(col, cudaFuncAttributeMaxDynamicSharedMemorySize, ColLay::bytes);
+  // The GProj instance takes the grouped tile loop, which also serves ungrouped heads.
+  auto col = gproj ? bob128_col_kernel<true, true>
+                   : p.group > 1 ? bob128_col_kernel<true, false> : bob128_col_kernel<false, false>;
+  const int cbytes = gproj ? ColLayT<true>::bytes : ColLayT<false>::bytes;
+  e = cudaFuncSetAttribute(col, cudaFuncAttributeMaxDynamicSharedMemorySize, cbytes);
   if (e != cudaSuccess) return e;
-  col<<<static_cast<unsigned>(2 * nrb * p.BHkv), kThreads, ColLay::bytes, st>>>(
-      q64, a64, do64, s64, v128, c128, static_cast<const __nv_bfloat16*>(K), static_cast<const __nv_bfloat16*>(b),
+  col<<<static_cast<unsigned>(2 * nrb * p.BHkv), kThreads, cbytes, st>>>(
+      q64, a64, do64, s64, r64, v128, c128, static_cast<const __nv_bfloat16*>(K), static_cast<const __nv_bfloat16*>(b),
       static_cast<__nv_bfloat16*>(gK), static_cast<__nv_bfloat16*>(gV), static_cast<int>(N),
       static_cast<int>(p.BHkv), p.scale, c, p.causal, p.group, static_cast<int>(d));
   return cudaGetLastError();

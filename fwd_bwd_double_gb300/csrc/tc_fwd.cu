@@ -24,6 +24,13 @@
 // is written into its TMEM columns, and O rescaled, only after P_{j-1} V_{j-1}
 // has finished (`pv_done`).  With d = 64 two CTAs fit on an SM (256 TMEM columns
 // each), so one CTA's softmax also overlaps the other's MMAs.
+//
+// The PB instance serves the GProj form of the backward over backward: with the
+// stored log-sum-exp L and the cotangent b in place of V it accumulates
+// Pb_i = sum_j P^_ij b_j, P^_ij = bf16(2^(S_ij s log2 e - L_i log2 e)), which is the
+// probability row the BoB row pass rounds for its products, formed by the same
+// operations on the same S (Q K^T over the same K-steps).  No running max, no
+// rescaling, no normalisation; Pb is written in fp32.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -39,6 +46,7 @@ constexpr int BM = 128;
 constexpr int BN = 128;
 constexpr int NS = 3;  // K/V stages (2 CTAs per SM at d = 64 still fit)
 constexpr int kThreads = 192;
+constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
 struct Layout {
@@ -64,11 +72,12 @@ __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int rows, int k)
   return ptx::sdesc_sw128(base + k * 16 * 128, rows * 128, 1024);
 }
 
-template <int D>
+template <int D, bool PB>
 __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O, float* __restrict__ lse,
-               int N, int nrb, int BH, float scale, float scale_log2, int causal, int G, int dv) {
+               const float* __restrict__ lse_in, float* __restrict__ pb, int N, int nrb, int BH, float scale,
+               float scale_log2, int causal, int G, int dv) {
   using Lay = Layout<D>;
   extern __shared__ __align__(1024) uint8_t sm[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Lay::oBar);
@@ -177,6 +186,61 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
         ptx::mma_commit_e(pv_done);
       }
       ptx::mma_commit_e(o_full);
+    }
+  } else if constexpr (PB) {
+    // ------------------------------- P^ b: thread r owns query row r, L is known
+    const int r = threadIdx.x;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int64_t row = static_cast<int64_t>(rb) * BM + r;
+    const float L2 = row < N ? lse_in[static_cast<int64_t>(bh) * N + row] * kLog2e : 0.f;
+    const uint64_t c2 = tc::pk2f(scale_log2, scale_log2), nL2 = tc::pk2f(-L2, -L2);
+    for (int j = 0; j < nkv; ++j) {
+      wait(s_full, j & 1);
+      ptx::tc_fence_after();
+      const bool diag = causal ? (j == rb) : (j == nkv - 1 && (N % BN) != 0);
+      const int klim = causal ? r : N - 1 - j * BN;
+      uint32_t v[4][32];
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) ptx::tmem_ld32(tS + lane_off + ch * 32, v[ch]);
+      ptx::tmem_wait_ld();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(s_consumed);
+      uint32_t pk[4][16];
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+#pragma unroll
+        for (int t = 0; t < 32; t += 2) {
+          const float2 arg = tc::unpk2(tc::fma2(tc::pk2(v[ch][t], v[ch][t + 1]), c2, nL2));
+          float p0 = ptx::ex2(arg.x), p1 = ptx::ex2(arg.y);
+          if (diag) {
+            if (ch * 32 + t > klim) p0 = 0.f;
+            if (ch * 32 + t + 1 > klim) p1 = 0.f;
+          }
+          pk[ch][t >> 1] = ptx::pack_bf16(p0, p1);
+        }
+      }
+      if (j > 0) wait(pv_done, (j - 1) & 1);
+      ptx::tc_fence_after();
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) ptx::tmem_st16(tP + lane_off + ch * 16, pk[ch]);
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(p_ready);
+    }
+    wait(o_full, 0);
+    ptx::tc_fence_after();
+#pragma unroll
+    for (int ch = 0; ch < D / 32; ++ch) {
+      uint32_t v[32];
+      ptx::tmem_ld32(tO + lane_off + ch * 32, v);
+      ptx::tmem_wait_ld();
+      if (row < N) {
+        float4* dst = reinterpret_cast<float4*>(pb + (static_cast<int64_t>(bh) * N + row) * D + ch * 32);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          dst[u] = make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
+                               __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
+      }
     }
   } else {
     // ---------------------------------------- softmax: thread r owns query row r
@@ -288,9 +352,9 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
   }
 }
 
-template <int D>
+template <int D, bool PB>
 cudaError_t launch(const Problem& p, const void* Q, const void* K, const void* V, void* O, float* lse,
-                   cudaStream_t st) {
+                   const float* lse_in, float* pb, cudaStream_t st) {
   alignas(64) CUtensorMap mq, mk, mv;
   // Tensor maps over the true head dim p.d (<= D): TMA zero-fills columns p.d .. D-1,
   // which add nothing to any product.
@@ -299,13 +363,12 @@ cudaError_t launch(const Problem& p, const void* Q, const void* K, const void* V
     return cudaErrorInvalidValue;
   const int nrb = static_cast<int>((p.N + BM - 1) / BM);
   const size_t smem = Layout<D>::bytes;
-  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, PB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  const float log2e = 1.4426950408889634f;
-  fwd_kernel<D><<<static_cast<unsigned>(nrb * p.BH), kThreads, smem, st>>>(
-      mq, mk, mv, static_cast<__nv_bfloat16*>(O), lse, static_cast<int>(p.N), nrb, static_cast<int>(p.BH),
-      p.scale, p.scale * log2e, p.causal, p.group, static_cast<int>(p.d));
+  fwd_kernel<D, PB><<<static_cast<unsigned>(nrb * p.BH), kThreads, smem, st>>>(
+      mq, mk, mv, static_cast<__nv_bfloat16*>(O), lse, lse_in, pb, static_cast<int>(p.N), nrb,
+      static_cast<int>(p.BH), p.scale, p.scale * kLog2e, p.causal, p.group, static_cast<int>(p.d));
   return cudaGetLastError();
 }
 
@@ -314,7 +377,15 @@ cudaError_t launch(const Problem& p, const void* Q, const void* K, const void* V
 cudaError_t tc_fwd(const Problem& p, const void* Q, const void* K, const void* V, void* O, float* lse,
                    cudaStream_t st) {
   // d = 32 runs the d = 64 kernel and d = 96 the d = 128 one, zero-padded in shared memory.
-  return p.d <= 64 ? launch<64>(p, Q, K, V, O, lse, st) : launch<128>(p, Q, K, V, O, lse, st);
+  return p.d <= 64 ? launch<64, false>(p, Q, K, V, O, lse, nullptr, nullptr, st)
+                   : launch<128, false>(p, Q, K, V, O, lse, nullptr, nullptr, st);
+}
+
+cudaError_t tc_bob_pb(const Problem& p, const void* Q, const void* K, const void* b, const float* lse, float* pb,
+                      cudaStream_t st) {
+  // Rows of bob_pb_cols(d) floats: 64 for d <= 64, 128 for d <= 128 (padding columns 0).
+  return p.d <= 64 ? launch<64, true>(p, Q, K, b, nullptr, nullptr, lse, pb, st)
+                   : launch<128, true>(p, Q, K, b, nullptr, nullptr, lse, pb, st);
 }
 
 uint32_t tc_fwd_take_error() {

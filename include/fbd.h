@@ -142,8 +142,10 @@ attn_status_t attn_bwd(const attn_desc_t* desc, const void* Q, const void* K, co
 
 /* Workspace for attn_bob: 16 bytes per (b,h,row), the rows of each slice rounded
  * up to an even count: the per-row states (lse, D, E, F) written by the row pass
- * for the column pass (layout internal to the library). */
-size_t attn_bob_workspace_bytes(const attn_desc_t* desc);
+ * for the column pass.  With gproj != 0 and bf16: as much again for the GProj
+ * coefficients, plus, for d <= 128, 256 (d <= 64) or 512 bytes per (b,h,row) for the
+ * rows' P^ b (layout internal to the library). */
+size_t attn_bob_workspace_bytes(const attn_desc_t* desc, int gproj);
 
 /* Backward over backward.  [BoB] "Why go backward through an already computed
  * gradient": with Phi(Q,K,V,dO) = (dQ,dK,dV) the first backward and cotangents
@@ -158,12 +160,24 @@ size_t attn_bob_workspace_bytes(const attn_desc_t* desc);
  * Two launches: the row pass holds a block of query rows, streams keys, writes
  * gQ, gdO and (lse, D, E, F) per row; the column pass holds a block of keys,
  * streams rows, re-reads those states and writes gK, gV.
+ * gproj != 0 (bf16 only; ignored for ATTN_F32): [GP] "How the zero sum turns into
+ *   a false gradient", applied to the two products that contract dS, gQ's dS b and
+ *   gK's dS^T a.  They see the bf16-rounded row dS^ projected back to zero sum,
+ *   dS^ - rho_i P^, rho_i = sum_j dS^_ij / sum_k P^_ik (P^ the bf16 probability row
+ *   the products use), as attn_bwd's GProj treats dQ and dK.  On the bf16
+ *   tensor-core path a third launch precedes the row pass: it forms P^ b per row
+ *   (into the workspace), which the row pass scales by rho_i (in fp32, so the rows
+ *   gQ sees sum to zero); the column pass adds the key term with the correction
+ *   -rho_i P_ij as one more bf16 operand (its rows then sum to zero up to the bf16
+ *   rounding of that small correction).  Nothing else changes.
  *   O, lse: the forward's outputs for the same Q, K, V (attn_fwd).
- *   workspace: >= attn_bob_workspace_bytes(desc) bytes; holds (lse, D, E, F). */
+ *   workspace: >= attn_bob_workspace_bytes(desc, gproj) bytes of device memory,
+ *   16-byte aligned, contents ignored on entry; holds (lse, D, E, F) after (and
+ *   with GProj the coefficients and P^ b). */
 attn_status_t attn_bob(const attn_desc_t* desc, const void* Q, const void* K, const void* V,
                        const void* O, const void* dO, const float* lse,
                        const void* gdQ, const void* gdK, const void* gdV,
-                       void* gQ, void* gK, void* gV, void* gdO,
+                       void* gQ, void* gK, void* gV, void* gdO, int gproj,
                        void* workspace, size_t workspace_bytes, void* stream);
 
 /* attn_bob for callers that cannot allocate device memory.  The source pages have
@@ -174,7 +188,8 @@ attn_status_t attn_bob(const attn_desc_t* desc, const void* Q, const void* K, co
  * statistics live in a file-scope device array of 16 MiB, enough for
  * B*H*N <= 1,048,576 rows.  Larger problems return ATTN_ERR_WORKSPACE without
  * launching anything (use attn_bob with a caller workspace instead).
- *   Arguments, outputs and errors are those of attn_bob minus the workspace.
+ *   Arguments, outputs and errors are those of attn_bob with gproj = 0 and no
+ *   workspace (this entry point has no GProj form).
  *   The array is held by every GPU that loads the library until process exit.
  *   The first call on each device looks up the array's device address with
  *   cudaGetSymbolAddress (that device must be current) and caches it; make that
@@ -190,7 +205,8 @@ attn_status_t attn_bob_static(const attn_desc_t* desc, const void* Q, const void
 
 /* The two launches of attn_bwd / attn_bob, issued separately (for callers that
  * schedule or time the passes themselves).  passes = ATTN_ROW_PASS (backward: dQ
- * and the row statistics; BoB: gQ, gdO and the row states), ATTN_COL_PASS
+ * and the row statistics; BoB: gQ, gdO and the row states, after the P^ b launch
+ * when gproj is set on the bf16 tensor-core path), ATTN_COL_PASS
  * (backward: dK, dV; BoB: gK, gV, both from the statistics the row pass left in
  * `workspace`), or both, which is exactly attn_bwd / attn_bob.  A column pass
  * must follow, in stream order, a row pass over the same inputs and workspace.
@@ -207,7 +223,7 @@ attn_status_t attn_bwd_passes(const attn_desc_t* desc, const void* Q, const void
 attn_status_t attn_bob_passes(const attn_desc_t* desc, const void* Q, const void* K, const void* V,
                               const void* O, const void* dO, const float* lse,
                               const void* gdQ, const void* gdK, const void* gdV,
-                              void* gQ, void* gK, void* gV, void* gdO,
+                              void* gQ, void* gK, void* gV, void* gdO, int gproj,
                               void* workspace, size_t workspace_bytes, int passes, void* stream);
 
 /* Diagnostic export of the GProj-projected score gradient (bf16 only).

@@ -60,7 +60,7 @@ def oracle_full(w, op, causal=True):
 
 
 def run_ops(w, x_dev, ops=("fwd", "bwd", "bob"), gproj=0, causal=True):
-    """Run the requested ops through the binding; return host fp64 arrays."""
+    """Run the requested ops through the binding (gproj for the backward and the BoB)."""
     import fwd_bwd_double_gb300 as fbd
     out = {}
     O, lse = fbd.attn_fwd(x_dev["Q"], x_dev["K"], x_dev["V"], scale=w.scale, causal=causal)
@@ -71,7 +71,7 @@ def run_ops(w, x_dev, ops=("fwd", "bwd", "bob"), gproj=0, causal=True):
     if "bob" in ops:
         out["gQ"], out["gK"], out["gV"], out["gdO"] = fbd.attn_bob(
             x_dev["Q"], x_dev["K"], x_dev["V"], O, x_dev["dO"], lse, x_dev["gdQ"], x_dev["gdK"], x_dev["gdV"],
-            scale=w.scale, causal=causal)
+            scale=w.scale, causal=causal, gproj=gproj)
     fbd.attn_device_status()
     return out
 

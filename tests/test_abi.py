@@ -51,10 +51,10 @@ def bwd(dsc, p=None, gproj=0, ws_bytes=None):
     return lib.attn_bwd(ctypes.byref(dsc), *p[:9], gproj, p[9], wsb, None)
 
 
-def bob(dsc, p=None, ws_bytes=None):
+def bob(dsc, p=None, ws_bytes=None, gproj=0):
     p = p or ptrs(14)
-    wsb = lib.attn_bob_workspace_bytes(ctypes.byref(dsc)) if ws_bytes is None else ws_bytes
-    return lib.attn_bob(ctypes.byref(dsc), *p[:13], p[13], wsb, None)
+    wsb = lib.attn_bob_workspace_bytes(ctypes.byref(dsc), gproj) if ws_bytes is None else ws_bytes
+    return lib.attn_bob(ctypes.byref(dsc), *p[:13], gproj, p[13], wsb, None)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -104,12 +104,26 @@ def test_workspace_checks():
     d = desc(B=2, H=3, N=100)
     assert lib.attn_bwd_workspace_bytes(ctypes.byref(d), 0) == 2 * 3 * 100 * 16
     assert lib.attn_bwd_workspace_bytes(ctypes.byref(d), 1) == 2 * 3 * 100 * 16
-    assert lib.attn_bob_workspace_bytes(ctypes.byref(d)) == 2 * 3 * 100 * 16
+    assert lib.attn_bob_workspace_bytes(ctypes.byref(d), 0) == 2 * 3 * 100 * 16
     assert bwd(d, ws_bytes=2 * 3 * 100 * 16 - 1) == WS
     assert bob(d, ws_bytes=0) == WS
     p = ptrs(14)
     p[13] = ctypes.c_void_p(0)
     assert bob(d, p) == WS
+    # BoB with GProj (bf16): the coefficients (16 B per row) and, on the tensor-core
+    # path, P^ b in fp32 (64 per row at d <= 64, 128 at d <= 128); float32 ignores it.
+    rows = 2 * 3 * 100
+    assert lib.attn_bob_workspace_bytes(ctypes.byref(d), 1) == rows * 32 + rows * 64 * 4
+    d128 = desc(B=2, H=3, N=100, d=96)
+    assert lib.attn_bob_workspace_bytes(ctypes.byref(d128), 1) == rows * 32 + rows * 128 * 4
+    d256 = desc(B=2, H=3, N=100, d=256)
+    assert lib.attn_bob_workspace_bytes(ctypes.byref(d256), 1) == rows * 32
+    f32 = desc(B=2, H=3, N=100, dtype=0)
+    assert lib.attn_bob_workspace_bytes(ctypes.byref(f32), 1) == rows * 16
+    odd = desc(B=1, H=1, N=7)  # rows of a slice rounded up to an even count for the states only
+    assert lib.attn_bob_workspace_bytes(ctypes.byref(odd), 1) == 8 * 32 + 7 * 64 * 4
+    assert bob(d, gproj=1, ws_bytes=lib.attn_bob_workspace_bytes(ctypes.byref(d), 1) - 1) == WS
+    assert bob(f32, gproj=1, ws_bytes=rows * 16 - 1) == WS
 
 
 def test_empty_problems_are_ok_without_touching_memory():
@@ -143,9 +157,9 @@ def test_pass_masks_are_validated():
     for bad in (0, 4, -1):
         assert lib.attn_bwd_passes(ctypes.byref(d), *p[:9], 0, p[9], wsb, bad, None) == INVALID
     q = ptrs(14)
-    wsb = lib.attn_bob_workspace_bytes(ctypes.byref(d))
+    wsb = lib.attn_bob_workspace_bytes(ctypes.byref(d), 0)
     for bad in (0, 7):
-        assert lib.attn_bob_passes(ctypes.byref(d), *q[:13], q[13], wsb, bad, None) == INVALID
+        assert lib.attn_bob_passes(ctypes.byref(d), *q[:13], 0, q[13], wsb, bad, None) == INVALID
     assert fbd.ATTN_ROW_PASS == 1 and fbd.ATTN_COL_PASS == 2
 
 

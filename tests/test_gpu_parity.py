@@ -54,8 +54,8 @@ def test_tiny_f32_all_ops():
 @pytest.mark.parametrize("gproj", [0, 1])
 def test_gpt2_layer_bf16(gproj):
     w = W.GPT2_LAYER
-    got = run_ops(w, to_device(inputs(w), w), ops=("bwd", "bob") if gproj == 0 else ("bwd",), gproj=gproj)
-    errs = check_full(w, got, ("bwd", "bob") if gproj == 0 else ("bwd",))
+    got = run_ops(w, to_device(inputs(w), w), ops=("bwd", "bob"), gproj=gproj)
+    errs = check_full(w, got, ("bwd", "bob"))
     print(w.name, gproj, {k: f"{v:.2e}" for k, v in errs.items()})
 
 
@@ -125,7 +125,7 @@ def test_bench_workload_sampled(gproj):
     bench times), sampled rows and late columns of the first and the last batch entry."""
     w = W.GPT2_N8192
     x = to_device(W.inputs(w), w)
-    ops = ("bwd", "bob") if gproj == 0 else ("bwd",)
+    ops = ("bwd", "bob")
     got = run_ops(w, x, ops=ops, gproj=gproj)
     rows, cols = sample_rows_cols(w.N, np.random.default_rng(8192))
     for b in (0, w.B - 1):
@@ -183,6 +183,46 @@ def test_large_key_gproj_reduces_dQ_error():
     assert mc < m0
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_bob_gproj_large_mean_b(d):
+    """GProj page, "How the zero sum turns into a false gradient", carried to BoB.  A
+    cotangent b = gdK with a large common mean (norm 40 per head, the size of the
+    large-key workload's key mean) meets the bf16 row residual of dS in gQ's dS b
+    product, and puts the per-row constant s q_i.mean(b) into G.  The exact BoB sees
+    neither (every output is unchanged when one vector is added to every row of b).
+    Median per-row errors against the exact fp64 result, with and without GProj, next
+    to the same inputs without the mean."""
+    import fwd_bwd_double_gb300 as fbd
+    w = W.Workload(f"bob_meanb_B1H4N1024d{d}_bf16", 1, 4, 1024, d, "bf16")
+    x = dict(W.inputs(w))
+    g = np.random.default_rng(40).standard_normal((w.H, w.d))
+    m = 40.0 * g / np.linalg.norm(g, axis=1, keepdims=True)
+    bm = W.round_to_bf16((x["gdK"].astype(np.float64) + m[None, :, None, :]).astype(np.float32))
+    xd = to_device(x, w)
+    bmd = to_device({"gdK": bm}, w)["gdK"]
+    O, lse = fbd.attn_fwd(xd["Q"], xd["K"], xd["V"])
+    got = {}
+    for gp in (0, 1):
+        for name, bb in (("b", xd["gdK"]), ("b+m", bmd)):
+            got[gp, name] = [host(t) for t in fbd.attn_bob(xd["Q"], xd["K"], xd["V"], O, xd["dO"], lse,
+                                                           xd["gdQ"], bb, xd["gdV"], gproj=gp)]
+    fbd.attn_device_status()
+    ref = {"b": oracle.bob_all(x["Q"], x["K"], x["V"], x["dO"], x["gdQ"], x["gdK"], x["gdV"]),
+           "b+m": oracle.bob_all(x["Q"], x["K"], x["V"], x["dO"], x["gdQ"], bm, x["gdV"])}
+    med = {}
+    for (gp, name), outs in got.items():
+        for k, o in zip(("gQ", "gK", "gV", "gdO"), outs):
+            med[gp, name, k] = float(np.median(row_rel_errors(o, ref[name][k])))
+            assert rel_fro(o, ref[name][k]) <= TOL["bf16"], (gp, name, k)
+    print(w.name, {f"{k[2]} gproj={k[0]} {k[1]}": f"{v:.2e}" for k, v in sorted(med.items())})
+    # GProj removes most of what the mean adds to the gQ error ...
+    assert med[1, "b+m", "gQ"] < 0.8 * med[0, "b+m", "gQ"]
+    assert med[1, "b+m", "gQ"] < 1.5 * med[1, "b", "gQ"]
+    # ... and the row pass's per-row shift of G keeps gdO at its level without the mean.
+    for gp in (0, 1):
+        assert med[gp, "b+m", "gdO"] < 1.5 * med[gp, "b", "gdO"]
+
+
 def test_large_key_projected_rows_sum_to_zero():
     """The projected dS rows fed to the products sum to zero within 1e-6 of their L1 norm."""
     import fwd_bwd_double_gb300 as fbd
@@ -223,14 +263,15 @@ def test_other_head_dims(N, d, dtype, causal):
     got = run_ops(w, to_device(inputs(w), w), ops=("bwd", "bob"), causal=causal)
     check_full(w, got, ("bwd", "bob"), causal=causal)
     if dtype == "bf16":
-        got1 = run_ops(w, to_device(inputs(w), w), ops=("bwd",), gproj=1, causal=causal)
-        check_full(w, got1, ("bwd",), causal=causal)
+        got1 = run_ops(w, to_device(inputs(w), w), ops=("bwd", "bob"), gproj=1, causal=causal)
+        check_full(w, got1, ("bwd", "bob"), causal=causal)
 
 
+@pytest.mark.parametrize("gproj", [0, 1])
 @pytest.mark.parametrize("d", [32, 96, 128, 256])
-def test_other_head_dims_grouped_bf16(d):
+def test_other_head_dims_grouped_bf16(d, gproj):
     w = W.Workload(f"headdim_gqa_B2H4g2N200d{d}_bf16", 2, 4, 200, d, "bf16", group=2)
-    got = run_ops(w, to_device(inputs(w), w), ops=("bwd", "bob"))
+    got = run_ops(w, to_device(inputs(w), w), ops=("bwd", "bob"), gproj=gproj)
     check_full(w, got, ("bwd", "bob"))
 
 
@@ -268,25 +309,28 @@ def test_outputs_written_once_and_nothing_outside():
         assert not np.isnan(view.float().cpu().numpy()).any(), f"{k}: element not written"
 
 
+@pytest.mark.parametrize("gproj", [0, 1])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_separate_passes_equal_the_fused_call(dtype):
+def test_separate_passes_equal_the_fused_call(dtype, gproj):
     """attn_*_passes(ROW) then attn_*_passes(COL) is exactly attn_bwd / attn_bob."""
     import fwd_bwd_double_gb300 as fbd
     w = W.Workload(f"passes_B2H3N300d64_{dtype}", 2, 3, 300, 64, dtype)
     x = to_device(inputs(w), w)
     O, lse = fbd.attn_fwd(x["Q"], x["K"], x["V"])
     ref_b = fbd.attn_bwd(x["Q"], x["K"], x["V"], O, x["dO"], lse, gproj=1)
-    ref_g = fbd.attn_bob(x["Q"], x["K"], x["V"], O, x["dO"], lse, x["gdQ"], x["gdK"], x["gdV"])
+    ref_g = fbd.attn_bob(x["Q"], x["K"], x["V"], O, x["dO"], lse, x["gdQ"], x["gdK"], x["gdV"], gproj=gproj)
     import torch
     outs = [torch.empty_like(x["Q"]) for _ in range(3)]
-    ws = torch.empty(fbd.attn_bwd_workspace_bytes(fbd.make_desc(x["Q"]), 1), dtype=torch.uint8, device="cuda")
+    desc = fbd.make_desc(x["Q"])
+    nbytes = max(fbd.attn_bwd_workspace_bytes(desc, 1), fbd.attn_bob_workspace_bytes(desc, gproj))
+    ws = torch.full((nbytes // 4,), float("nan"), dtype=torch.float32, device="cuda")
     for ps in (fbd.ATTN_ROW_PASS, fbd.ATTN_COL_PASS):
         fbd.attn_bwd_passes(x["Q"], x["K"], x["V"], O, x["dO"], lse, ps, gproj=1, dQ=outs[0], dK=outs[1],
                             dV=outs[2], workspace=ws)
     gouts = [torch.empty_like(x["Q"]) for _ in range(4)]
     for ps in (fbd.ATTN_ROW_PASS, fbd.ATTN_COL_PASS):
         fbd.attn_bob_passes(x["Q"], x["K"], x["V"], O, x["dO"], lse, x["gdQ"], x["gdK"], x["gdV"], ps,
-                            gQ=gouts[0], gK=gouts[1], gV=gouts[2], gdO=gouts[3], workspace=ws)
+                            gQ=gouts[0], gK=gouts[1], gV=gouts[2], gdO=gouts[3], workspace=ws, gproj=gproj)
     fbd.attn_device_status()
     for a, b in zip(outs + gouts, list(ref_b) + list(ref_g)):
         assert torch.equal(a, b)
@@ -343,7 +387,7 @@ def test_noncausal_tiny_f32_all_ops():
 @pytest.mark.parametrize("gproj", [0, 1])
 def test_noncausal_gpt2_layer_bf16(gproj):
     w = W.Workload("noncausal_gpt2small_B4H12N1024d64", 4, 12, 1024, 64, "bf16")
-    ops = ("bwd", "bob") if gproj == 0 else ("bwd",)
+    ops = ("bwd", "bob")
     got = run_ops(w, to_device(inputs(w), w), ops=ops, gproj=gproj, causal=False)
     errs = check_full(w, got, ops, causal=False)
     print(w.name, gproj, {k: f"{v:.2e}" for k, v in errs.items()})
@@ -407,7 +451,7 @@ def test_gqa_tiny_f32_all_ops(causal):
 def test_gqa_gpt2_layer_bf16(group, gproj):
     """GPT-2 small layer shape with 4 key/value heads (g = 3) and multi-query (g = 12)."""
     w = W.Workload(f"gqa_gpt2small_B2H12g{group}N1024d64", 2, 12, 1024, 64, "bf16", group=group)
-    ops = ("bwd", "bob") if gproj == 0 else ("bwd",)
+    ops = ("bwd", "bob")
     got = run_ops(w, to_device(inputs(w), w), ops=ops, gproj=gproj)
     errs = check_full(w, got, ops)
     print(w.name, gproj, {k: f"{v:.2e}" for k, v in errs.items()})
@@ -422,8 +466,8 @@ def test_gqa_edge_sizes(N, d, dtype, causal):
     got = run_ops(w, to_device(inputs(w), w), ops=ops, causal=causal)
     check_full(w, got, ops, causal=causal)
     if dtype == "bf16":
-        got1 = run_ops(w, to_device(inputs(w), w), ops=("bwd",), gproj=1, causal=causal)
-        check_full(w, got1, ("bwd",), causal=causal)
+        got1 = run_ops(w, to_device(inputs(w), w), ops=("bwd", "bob"), gproj=1, causal=causal)
+        check_full(w, got1, ("bwd", "bob"), causal=causal)
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
@@ -460,26 +504,29 @@ def test_gqa_row_outputs_equal_repeated_heads_bitwise(dtype):
 # The tensor-core BoB at d = 128 runs each block of rows (keys) as two CTAs, one per
 # output half; both halves and the row states written by half 0 are checked here.
 
+@pytest.mark.parametrize("gproj", [0, 1])
 @pytest.mark.parametrize("causal", [True, False])
-def test_bob_head_dim_128_bf16(causal):
+def test_bob_head_dim_128_bf16(causal, gproj):
     w = W.Workload("bob_d128_B2H4N1000d128_bf16", 2, 4, 1000, 128, "bf16")
-    got = run_ops(w, to_device(inputs(w), w), ops=("bob",), causal=causal)
+    got = run_ops(w, to_device(inputs(w), w), ops=("bob",), causal=causal, gproj=gproj)
     errs = check_full(w, got, ("bob",), causal=causal)
-    print(w.name, causal, {k: f"{v:.2e}" for k, v in errs.items()})
+    print(w.name, causal, gproj, {k: f"{v:.2e}" for k, v in errs.items()})
 
 
-def test_bob_head_dim_128_passes_compose_on_nan_workspace():
+@pytest.mark.parametrize("gproj", [0, 1])
+def test_bob_head_dim_128_passes_compose_on_nan_workspace(gproj):
     import torch
     import fwd_bwd_double_gb300 as fbd
     w = W.Workload("bob_d128_passes_B1H3N300d128_bf16", 1, 3, 300, 128, "bf16")
     x = to_device(inputs(w), w)
     O, lse = fbd.attn_fwd(x["Q"], x["K"], x["V"])
-    ref = fbd.attn_bob(x["Q"], x["K"], x["V"], O, x["dO"], lse, x["gdQ"], x["gdK"], x["gdV"])
-    ws = torch.full((fbd.attn_bob_workspace_bytes(fbd.make_desc(x["Q"])) // 4,), float("nan"), device="cuda")
+    ref = fbd.attn_bob(x["Q"], x["K"], x["V"], O, x["dO"], lse, x["gdQ"], x["gdK"], x["gdV"], gproj=gproj)
+    nbytes = fbd.attn_bob_workspace_bytes(fbd.make_desc(x["Q"]), gproj)
+    ws = torch.full((nbytes // 4,), float("nan"), device="cuda")
     outs = [torch.full_like(x["Q"], float("nan")) for _ in range(4)]
     for ps in (fbd.ATTN_ROW_PASS, fbd.ATTN_COL_PASS):
         fbd.attn_bob_passes(x["Q"], x["K"], x["V"], O, x["dO"], lse, x["gdQ"], x["gdK"], x["gdV"], ps,
-                            gQ=outs[0], gK=outs[1], gV=outs[2], gdO=outs[3], workspace=ws)
+                            gQ=outs[0], gK=outs[1], gV=outs[2], gdO=outs[3], workspace=ws, gproj=gproj)
     fbd.attn_device_status()
     for a, b in zip(outs, ref):
         assert torch.equal(a, b)
@@ -493,6 +540,6 @@ def test_padded_head_dims_bf16(d, causal):
     w = W.Workload(f"padded_B2H4N1000d{d}_bf16", 2, 4, 1000, d, "bf16")
     got = run_ops(w, to_device(inputs(w), w), ops=("bwd", "bob"), causal=causal)
     errs = check_full(w, got, ("bwd", "bob"), causal=causal)
-    got1 = run_ops(w, to_device(inputs(w), w), ops=("bwd",), gproj=1, causal=causal)
-    errs1 = check_full(w, got1, ("bwd",), causal=causal)
-    print(w.name, causal, {k: f"{v:.2e}" for k, v in errs.items()}, "gproj dQ", f"{errs1['dQ']:.2e}")
+    got1 = run_ops(w, to_device(inputs(w), w), ops=("bwd", "bob"), gproj=1, causal=causal)
+    errs1 = check_full(w, got1, ("bwd", "bob"), causal=causal)
+    print(w.name, causal, {k: f"{v:.2e}" for k, v in errs.items()}, "gproj", {k: f"{v:.2e}" for k, v in errs1.items()})
