@@ -19,6 +19,8 @@ Sources:
     "Backward pass: recompute instead of store" (only O and the softmax statistics
     are kept; we keep their single-number form, the log-sum-exp);
   * causal masking: same page, section "Causal masking is where trading gets a discount";
+    the causal sliding window (``Window``), one of the flexible masks the FlashBoB page
+    names as a next extension, is accepted wherever `causal` is;
   * first backward: the vector-Jacobian product of O with respect to Q, K, V given dO.
     The pages describe it only as a recompute from Q, K and the statistics, so the
     oracle writes out the standard derivative (dP = dO V^T, D_i = sum_k dO_ik O_ik,
@@ -42,6 +44,37 @@ from __future__ import annotations
 import numpy as np
 
 NEG_INF = -np.inf
+
+
+class Window:
+    """Causal sliding-window mask: key j is visible to query i iff i - W < j <= i.
+
+    The FlashBoB page ("When FlashBoB changes the engineering plan") names flexible
+    masks among the next extensions without fixing one; this is the banded causal
+    mask.  Every function's `causal` argument accepts it in place of True (which is
+    the window without a lower limit); each row keeps its own key, so no row is empty.
+    """
+
+    def __init__(self, W: int):
+        if int(W) < 1:
+            raise ValueError("window must be >= 1")
+        self.W = int(W)
+
+    def __repr__(self):
+        return f"Window({self.W})"
+
+
+def hidden(rows, keys, causal):
+    """Boolean [len(rows), len(keys)]: True where the key is masked for the row
+    (causal: j > i; a Window also masks j <= i - W; causal=False masks nothing)."""
+    r = np.asarray(rows)[:, None]
+    k = np.asarray(keys)[None, :]
+    if not causal:
+        return np.zeros((r.shape[0], k.shape[1]), bool)
+    m = k > r
+    if isinstance(causal, Window):
+        m |= k <= r - causal.W
+    return m
 
 
 def _f64(x):
@@ -74,7 +107,7 @@ def scores(Q, K, rows, scale, causal=True):
         return scale * (Q[rows] @ K.T)
     kmax = int(rows.max()) + 1
     S = scale * (Q[rows] @ K[:kmax].T)
-    S[np.arange(kmax)[None, :] > rows[:, None]] = NEG_INF
+    S[hidden(rows, np.arange(kmax), causal)] = NEG_INF
     return S
 
 
@@ -149,7 +182,7 @@ def forward_online(Q, K, V, Br, Bc, scale=None, causal=True):
                 break  # the whole block is in the future of every query: never loaded
             Sij = scale * (Q[qi] @ K[kj].T)
             if causal:
-                Sij[kj[None, :] > qi[:, None]] = NEG_INF
+                Sij[hidden(qi, kj, causal)] = NEG_INF
             mij = Sij.max(axis=1)
             # a row whose keys in this block are all masked contributes nothing
             live = np.isfinite(mij)
@@ -157,10 +190,16 @@ def forward_online(Q, K, V, Br, Bc, scale=None, causal=True):
             Pij[live] = np.exp(Sij[live] - mij[live, None])
             lij = Pij.sum(axis=1)
             m_new = np.maximum(mi, mij)
-            a_old = np.where(np.isfinite(mi), np.exp(mi - m_new), 0.0)
-            a_new = np.where(live, np.exp(np.where(live, mij, 0.0) - m_new), 0.0)
+            fin = np.isfinite(m_new)  # (the others have seen nothing: both factors 0)
+            a_old = np.where(np.isfinite(mi), np.exp(np.where(np.isfinite(mi), mi, 0.0) - np.where(fin, m_new, 0.0)), 0.0)
+            a_new = np.where(live, np.exp(np.where(live, mij, 0.0) - np.where(fin, m_new, 0.0)), 0.0)
             l_new = li * a_old + lij * a_new
-            Oi = Oi * (li * a_old / l_new)[:, None] + (Pij @ V[kj]) * (a_new / l_new)[:, None]
+            # rows that have seen no visible key yet (possible under a window) keep
+            # their starting state (-inf, 0, 0)
+            seen = l_new > 0
+            l_div = np.where(seen, l_new, 1.0)
+            Oi = np.where(seen[:, None],
+                          Oi * (li * a_old / l_div)[:, None] + (Pij @ V[kj]) * (a_new / l_div)[:, None], Oi)
             mi, li = m_new, l_new
         O[qi] = Oi
         L[qi] = mi + np.log(li)
@@ -189,7 +228,7 @@ def _row_terms(Q, K, V, dO, rows, scale, a=None, b=None, c=None, causal=True):
         G = scale * (a[rows] @ K[:nk].T + Q[rows] @ b[:nk].T)
         Hm = dO[rows] @ c[:nk].T
         if causal:
-            mask = np.arange(nk)[None, :] > rows[:, None]
+            mask = hidden(rows, np.arange(nk), causal)
             G[mask] = 0.0
             Hm[mask] = 0.0
         E = (P * G).sum(axis=1)
@@ -458,7 +497,7 @@ def bob_row_pass(Q, K, V, dO, a, b, c, O, L, Bc, scale=None, causal=True):
         live = rows >= k0 if causal else rows >= 0  # rows that see at least one key here
         r = rows[live]
         S = scale * (Q[r] @ K[kj].T)
-        mask = kj[None, :] > r[:, None] if causal else np.zeros((len(r), len(kj)), bool)
+        mask = hidden(r, kj, causal)
         P = np.exp(np.where(mask, NEG_INF, S) - L[r, None])
         dP = dO[r] @ V[kj].T
         dS = P * (dP - D[r, None])
@@ -493,7 +532,7 @@ def bob_col_pass(Q, K, V, dO, a, b, c, L, D, E, F, Br, scale=None, causal=True):
     for q0 in range(0, N, Br):
         qi = np.arange(q0, min(q0 + Br, N))
         kj = np.arange(0, qi[-1] + 1) if causal else np.arange(N)
-        mask = kj[None, :] > qi[:, None] if causal else np.zeros((len(qi), len(kj)), bool)
+        mask = hidden(qi, kj, causal)
         S = scale * (Q[qi] @ K[kj].T)
         P = np.exp(np.where(mask, NEG_INF, S) - L[qi, None])
         dP = dO[qi] @ V[kj].T

@@ -655,3 +655,131 @@ def test_gqa_with_one_group_is_plain_attention():
     b = oracle.bob_all(*X)
     for k in ("gQ", "gK", "gV", "gdO"):
         assert np.array_equal(a[k], b[k])
+
+
+# ------------------------------------------------------ causal sliding window ----
+# A flexible mask (FlashBoB page, "When FlashBoB changes the engineering plan", names
+# flexible masks as a next extension): key j visible to query i iff i - W < j <= i.
+
+def brute_forward_window(Q, K, V, scale, W):
+    """Pure-Python loops over the definition with the banded mask."""
+    N, d = len(Q), len(Q[0])
+    O = [[0.0] * d for _ in range(N)]
+    L = [0.0] * N
+    for i in range(N):
+        js = [j for j in range(N) if i - W < j <= i]
+        s = [scale * sum(Q[i][t] * K[j][t] for t in range(d)) for j in js]
+        m = max(s)
+        e = [math.exp(x - m) for x in s]
+        tot = sum(e)
+        L[i] = m + math.log(tot)
+        for t in range(d):
+            O[i][t] = sum(e[n] / tot * V[js[n]][t] for n in range(len(js)))
+    return O, L
+
+
+@pytest.mark.parametrize("N,d,W", [(1, 3, 1), (7, 5, 2), (16, 8, 5), (16, 4, 40)])
+def test_window_forward_brute_force(N, d, W):
+    Q, K, V = (rnd(100 + k, N, d) for k in range(3))
+    O, L = oracle.forward(Q, K, V, scale=0.7, causal=oracle.Window(W))
+    Ob, Lb = brute_forward_window(Q.tolist(), K.tolist(), V.tolist(), 0.7, W)
+    assert rel(O, np.array(Ob)) <= 1e-13 and rel(L, np.array(Lb)) <= 1e-13
+
+
+@pytest.mark.parametrize("Br,Bc", [(1, 1), (16, 3), (5, 37), (37, 37)])
+def test_window_online_softmax_equals_two_pass(Br, Bc):
+    N, d = 37, 8
+    Q, K, V = rnd(103, N, d) * 2, rnd(104, N, d) * 2, rnd(105, N, d)
+    w = oracle.Window(9)
+    O2, L2 = oracle.forward(Q, K, V, causal=w)
+    O1, L1 = oracle.forward_online(Q, K, V, Br, Bc, causal=w)
+    assert rel(O1, O2) <= 1e-13 and rel(L1, L2) <= 1e-13
+
+
+def test_window_limits_reduce_to_causal_and_to_one_key():
+    """W >= N is the causal mask.  W = 1: every row sees only its own key, so P = I:
+    O = V, L_i = s q_i.k_i; dS = 0 (dQ = dK = 0), dV = dO; BoB: G - E = 0 and Sbar = 0,
+    so gQ = gK = gV = 0 and gdO = c."""
+    N, d = 12, 4
+    Q, K, V, dO, a, b, c = slice_set(N, d, 106)
+    s = 0.45
+    for fn in (oracle.forward, ):
+        assert all(np.array_equal(x, y) for x, y in zip(fn(Q, K, V, scale=s, causal=oracle.Window(N)),
+                                                        fn(Q, K, V, scale=s, causal=True)))
+    full = oracle.bob(Q, K, V, dO, a, b, c, scale=s, causal=oracle.Window(N + 5))
+    ref = oracle.bob(Q, K, V, dO, a, b, c, scale=s, causal=True)
+    for k in ("gQ", "gK", "gV", "gdO"):
+        assert np.array_equal(full[k], ref[k]), k
+    one = oracle.Window(1)
+    O, L = oracle.forward(Q, K, V, scale=s, causal=one)
+    assert rel(O, V) <= 1e-15 and np.allclose(L, s * (Q * K).sum(axis=1), rtol=0, atol=1e-14)
+    g = oracle.backward(Q, K, V, dO, scale=s, causal=one)
+    assert np.abs(g["dQ"]).max() <= 1e-14 and np.abs(g["dK"]).max() <= 1e-14 and rel(g["dV"], dO) <= 1e-15
+    bb = oracle.bob(Q, K, V, dO, a, b, c, scale=s, causal=one)
+    for k in ("gQ", "gK", "gV"):
+        assert np.abs(bb[k]).max() <= 1e-13, k
+    assert rel(bb["gdO"], c) <= 1e-15
+
+
+def loss_w(Q, K, V, dO, s, w):
+    O, _ = oracle.forward(Q, K, V, scale=s, causal=w)
+    return float((O * dO).sum())
+
+
+@pytest.mark.parametrize("N,d,W", [(6, 3, 2), (11, 4, 4)])
+def test_window_backward_matches_finite_differences(N, d, W):
+    Q, K, V, dO = (x * 0.8 for x in slice_set(N, d, 107)[:4])
+    s, w = 0.6, oracle.Window(W)
+    g = oracle.backward(Q, K, V, dO, scale=s, causal=w)
+    gQ = fd_grad(lambda X: loss_w(X, K, V, dO, s, w), Q)
+    gK = fd_grad(lambda X: loss_w(Q, X, V, dO, s, w), K)
+    gV = fd_grad(lambda X: loss_w(Q, K, X, dO, s, w), V)
+    top = max(np.abs(gQ).max(), np.abs(gK).max(), np.abs(gV).max(), 1e-3)
+    for got, want in ((g["dQ"], gQ), (g["dK"], gK), (g["dV"], gV)):
+        assert np.abs(got - want).max() <= 1e-8 * top
+
+
+@pytest.mark.parametrize("N,d,W", [(5, 3, 2), (12, 4, 5)])
+def test_window_bob_is_hessian_vector_product_and_jvp(N, d, W):
+    Q, K, V, dO, a, b, c = slice_set(N, d, 108)
+    s, h, w = 0.55, 1e-5, oracle.Window(W)
+    out = oracle.bob(Q, K, V, dO, a, b, c, scale=s, causal=w)
+
+    def grads_w(Q, K, V):
+        g = oracle.backward(Q, K, V, dO, scale=s, causal=w)
+        return g["dQ"], g["dK"], g["dV"]
+    gp = grads_w(Q + h * a, K + h * b, V + h * c)
+    gm = grads_w(Q - h * a, K - h * b, V - h * c)
+    fd = [(p - m) / (2 * h) for p, m in zip(gp, gm)]
+    top = max(np.abs(x).max() for x in fd)
+    for name, want in zip(("gQ", "gK", "gV"), fd):
+        assert np.abs(out[name] - want).max() <= 1e-8 * max(top, 1e-3), name
+    Op, _ = oracle.forward(Q + h * a, K + h * b, V + h * c, scale=s, causal=w)
+    Om, _ = oracle.forward(Q - h * a, K - h * b, V - h * c, scale=s, causal=w)
+    jvp = (Op - Om) / (2 * h)
+    assert np.abs(out["gdO"] - jvp).max() <= 1e-8 * max(np.abs(jvp).max(), 1e-3)
+
+
+@pytest.mark.parametrize("Bc,Br", [(1, 1), (4, 7), (16, 16)])
+def test_window_bob_streaming_passes_equal_closed_form(Bc, Br):
+    N, d = 33, 5
+    Q, K, V, dO, a, b, c = slice_set(N, d, 109)
+    w = oracle.Window(6)
+    ref = oracle.bob(Q, K, V, dO, a, b, c, causal=w)
+    O, L = oracle.forward(Q, K, V, causal=w)
+    row = oracle.bob_row_pass(Q, K, V, dO, a, b, c, O, L, Bc, causal=w)
+    gK, gV = oracle.bob_col_pass(Q, K, V, dO, a, b, c, L, row["D"], row["E"], row["F"], Br, causal=w)
+    for got, want in ((row["gQ"], ref["gQ"]), (row["gdO"], ref["gdO"]), (gK, ref["gK"]), (gV, ref["gV"])):
+        assert rel(got, want) <= 1e-12
+
+
+def test_window_sampling_agrees():
+    N, d = 45, 6
+    Q, K, V, dO, a, b, c = slice_set(N, d, 110)
+    w = oracle.Window(8)
+    ref = oracle.bob(Q, K, V, dO, a, b, c, block=7, causal=w)
+    rows, cols = np.array([0, 44, 13]), np.array([0, 30, 44])
+    r = oracle.bob_rows(Q, K, V, dO, a, b, c, rows, causal=w)
+    assert rel(r["gQ"], ref["gQ"][rows]) <= 1e-13 and rel(r["gdO"], ref["gdO"][rows]) <= 1e-13
+    gK, gV = oracle.bob_cols(Q, K, V, dO, a, b, c, cols, causal=w)
+    assert rel(gK, ref["gK"][cols]) <= 1e-13 and rel(gV, ref["gV"][cols]) <= 1e-13
