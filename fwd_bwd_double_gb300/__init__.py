@@ -38,16 +38,17 @@ def _dtype_code(t) -> int:
     raise FbdError(2, f"unsupported tensor dtype {t.dtype} (float32 or bfloat16)")
 
 
-def make_desc(Q, scale: float = 0.0, causal: int = 1, K=None) -> AttnDesc:
+def make_desc(Q, scale: float = 0.0, causal: int = 1, K=None, window: int = 0) -> AttnDesc:
     """Descriptor from a [B, H, N, d] query tensor and, for grouped key/value heads,
-    the [B, H / g, N, d] key tensor (g query heads per key/value head)."""
+    the [B, H / g, N, d] key tensor (g query heads per key/value head); window W > 0
+    (with causal) limits query i to the keys i - W < j <= i."""
     if Q.dim() != 4 or (K is not None and K.dim() != 4):
         raise FbdError(1, "tensors must be [B, H, N, d]")
     B, H, N, d = Q.shape
     Hkv = H if K is None else K.shape[1]
     if (Hkv == 0) != (H == 0) or (Hkv and H % Hkv):
         raise FbdError(1, f"key/value heads ({Hkv}) must divide query heads ({H})")
-    return AttnDesc(B, H, N, d, float(scale), int(causal), _dtype_code(Q), H // Hkv if Hkv else 1)
+    return AttnDesc(B, H, N, d, float(scale), int(causal), _dtype_code(Q), H // Hkv if Hkv else 1, int(window))
 
 
 def _ptr(t):
@@ -73,10 +74,10 @@ def _check(status: int):
         raise FbdError(status, lib.attn_last_error().decode())
 
 
-def attn_fwd(Q, K, V, O=None, lse=None, scale: float = 0.0, stream=None, desc=None, causal: bool = True):
+def attn_fwd(Q, K, V, O=None, lse=None, scale: float = 0.0, stream=None, desc=None, causal: bool = True, window: int = 0):
     """O, lse = attention forward (allocates O and lse with torch when not given)."""
     torch = _torch()
-    desc = desc or make_desc(Q, scale, int(causal), K)
+    desc = desc or make_desc(Q, scale, int(causal), K, window)
     if O is None:
         O = torch.empty_like(Q)
     if lse is None:
@@ -101,17 +102,17 @@ def _workspace(nbytes, like, workspace):
 
 
 def attn_bwd(Q, K, V, O, dO, lse, gproj: int = 0, dQ=None, dK=None, dV=None, workspace=None,
-             scale: float = 0.0, stream=None, desc=None, causal: bool = True):
+             scale: float = 0.0, stream=None, desc=None, causal: bool = True, window: int = 0):
     """dQ, dK, dV = recompute backward (GProj when gproj != 0, bf16 only)."""
     return attn_bwd_passes(Q, K, V, O, dO, lse, ATTN_ROW_PASS | ATTN_COL_PASS, gproj, dQ, dK, dV, workspace,
-                           scale, stream, desc, causal)
+                           scale, stream, desc, causal, window)
 
 
 def attn_bwd_passes(Q, K, V, O, dO, lse, passes, gproj: int = 0, dQ=None, dK=None, dV=None, workspace=None,
-                    scale: float = 0.0, stream=None, desc=None, causal: bool = True):
+                    scale: float = 0.0, stream=None, desc=None, causal: bool = True, window: int = 0):
     """The backward's row pass (dQ) and/or column pass (dK, dV); see attn_bwd_passes in fbd.h."""
     torch = _torch()
-    desc = desc or make_desc(Q, scale, int(causal), K)
+    desc = desc or make_desc(Q, scale, int(causal), K, window)
     dQ = torch.empty_like(Q) if dQ is None else dQ
     dK = torch.empty_like(K) if dK is None else dK
     dV = torch.empty_like(V) if dV is None else dV
@@ -125,19 +126,19 @@ def attn_bwd_passes(Q, K, V, O, dO, lse, passes, gproj: int = 0, dQ=None, dK=Non
 
 
 def attn_bob(Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ=None, gK=None, gV=None, gdO=None, workspace=None,
-             scale: float = 0.0, stream=None, desc=None, causal: bool = True, gproj: int = 0):
+             scale: float = 0.0, stream=None, desc=None, causal: bool = True, window: int = 0, gproj: int = 0):
     """gQ, gK, gV, gdO = backward over backward against cotangents (gdQ, gdK, gdV)
     (GProj on the rounded dS of its dS b and dS^T a products when gproj != 0, bf16 only)."""
     return attn_bob_passes(Q, K, V, O, dO, lse, gdQ, gdK, gdV, ATTN_ROW_PASS | ATTN_COL_PASS, gQ, gK, gV, gdO,
-                           workspace, scale, stream, desc, causal, gproj)
+                           workspace, scale, stream, desc, causal, window, gproj)
 
 
 def attn_bob_passes(Q, K, V, O, dO, lse, gdQ, gdK, gdV, passes, gQ=None, gK=None, gV=None, gdO=None,
-                    workspace=None, scale: float = 0.0, stream=None, desc=None, causal: bool = True,
+                    workspace=None, scale: float = 0.0, stream=None, desc=None, causal: bool = True, window: int = 0,
                     gproj: int = 0):
     """BoB's row pass (gQ, gdO, row states) and/or column pass (gK, gV); see fbd.h."""
     torch = _torch()
-    desc = desc or make_desc(Q, scale, int(causal), K)
+    desc = desc or make_desc(Q, scale, int(causal), K, window)
     gQ = torch.empty_like(Q) if gQ is None else gQ
     gK = torch.empty_like(K) if gK is None else gK
     gV = torch.empty_like(V) if gV is None else gV
@@ -151,11 +152,11 @@ def attn_bob_passes(Q, K, V, O, dO, lse, gdQ, gdK, gdV, passes, gQ=None, gK=None
 
 
 def attn_bob_static(Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ=None, gK=None, gV=None, gdO=None,
-                    scale: float = 0.0, stream=None, desc=None, causal: bool = True):
+                    scale: float = 0.0, stream=None, desc=None, causal: bool = True, window: int = 0):
     """attn_bob without a workspace argument: the library's static scratch array is used
     (for callers that cannot allocate device memory; B*H*N <= 1,048,576)."""
     torch = _torch()
-    desc = desc or make_desc(Q, scale, int(causal), K)
+    desc = desc or make_desc(Q, scale, int(causal), K, window)
     gQ = torch.empty_like(Q) if gQ is None else gQ
     gK = torch.empty_like(K) if gK is None else gK
     gV = torch.empty_like(V) if gV is None else gV
@@ -166,10 +167,10 @@ def attn_bob_static(Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ=None, gK=None, gV=Non
     return gQ, gK, gV, gdO
 
 
-def attn_bwd_projected_dS(Q, K, V, O, dO, lse, dS=None, scale: float = 0.0, stream=None, desc=None, causal: bool = True):
+def attn_bwd_projected_dS(Q, K, V, O, dO, lse, dS=None, scale: float = 0.0, stream=None, desc=None, causal: bool = True, window: int = 0):
     """Diagnostic: the GProj-projected dS [B, H, N, N] float32 (small N only)."""
     torch = _torch()
-    desc = desc or make_desc(Q, scale, int(causal), K)
+    desc = desc or make_desc(Q, scale, int(causal), K, window)
     B, H, N, _ = Q.shape
     dS = torch.empty((B, H, N, N), dtype=torch.float32, device=Q.device) if dS is None else dS
     _check(lib.attn_bwd_projected_dS(ctypes.byref(desc), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO),

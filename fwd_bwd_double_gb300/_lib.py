@@ -30,7 +30,7 @@ class FbdError(RuntimeError):
 class AttnDesc(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int64), ("H", ctypes.c_int64), ("N", ctypes.c_int64), ("d", ctypes.c_int64),
                 ("scale", ctypes.c_float), ("causal", ctypes.c_int32), ("dtype", ctypes.c_int32),
-                ("group", ctypes.c_int32)]
+                ("group", ctypes.c_int32), ("window", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p

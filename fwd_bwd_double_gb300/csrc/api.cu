@@ -38,6 +38,9 @@ attn_status_t check_desc(const attn_desc_t* desc, fbd::Problem& p) {
   if (desc->group < 0) return fail(ATTN_ERR_INVALID_ARG, "group must be >= 0%s");
   const int64_t g = desc->group == 0 ? 1 : desc->group;
   if (desc->H % g != 0) return fail(ATTN_ERR_INVALID_ARG, "group must divide H%s");
+  if (desc->window < 0) return fail(ATTN_ERR_INVALID_ARG, "window must be >= 0%s");
+  if (desc->window > 0 && desc->causal != 1)
+    return fail(ATTN_ERR_UNSUPPORTED, "a window needs the causal mask (causal = 1)%s");
   if (desc->d != 32 && desc->d != 64 && desc->d != 96 && desc->d != 128 && desc->d != 256)
     return fail(ATTN_ERR_UNSUPPORTED, "head dim must be 32, 64, 96, 128 or 256%s");
   if (desc->dtype != ATTN_F32 && desc->dtype != ATTN_BF16) return fail(ATTN_ERR_UNSUPPORTED, "unknown dtype%s");
@@ -60,6 +63,7 @@ attn_status_t check_desc(const attn_desc_t* desc, fbd::Problem& p) {
   p.causal = desc->causal;
   p.group = static_cast<int>(g);
   p.BHkv = p.BH / g;
+  p.window = desc->window > 0 && desc->window < desc->N ? desc->window : 0;  // W >= N: the causal mask
   if (p.BH >= lim) return fail(ATTN_ERR_INVALID_ARG, "B*H must be < 2^31%s");
   if (((p.N + 7) / 8) * p.BH >= lim) return fail(ATTN_ERR_INVALID_ARG, "B*H*N too large for one launch%s");
   return ATTN_OK;

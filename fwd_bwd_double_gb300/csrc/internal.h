@@ -17,7 +17,16 @@ struct Problem {
   int causal;     // 1: key j visible to query i iff j <= i; 0: every key visible
   int group;      // query heads per key/value head (1: multi-head attention)
   int64_t BHkv;   // B * H / group key/value slices; query slice bh reads slice bh / group
+  int64_t window; // causal sliding window W (key j visible to row i iff i - W < j <= i), 1 <= W < N;
+                  // 0: none (also when the caller's W >= N, which is the plain causal mask)
 };
+
+// The window as the kernels take it: W, or N + 1 when there is none (then i - W + 1 <= 0
+// and j + W > N for every row i and key j, so the window bounds never bind).
+inline int64_t eff_window(const Problem& p) { return p.window > 0 ? p.window : p.N + 1; }
+// The same for the tensor-core kernels (int): with no window, larger than N plus one
+// block of 256 rows, so that no block bound derived from it ever binds.
+inline int64_t eff_window_tc(const Problem& p) { return p.window > 0 ? p.window : p.N + 512; }
 
 // Float32 path: CUDA-core kernels with float32 inputs/outputs (exact fp32 arithmetic).
 cudaError_t simt_fwd(const Problem& p, const void* Q, const void* K, const void* V, void* O, float* lse,

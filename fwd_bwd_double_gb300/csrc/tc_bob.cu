@@ -38,7 +38,7 @@
 // of G (dPbar and Sbar hold G only through G - E, and E moves with it).  A large
 // mean of b (or of K) puts such a constant, s q_i.mean(b), into G, and the bf16
 // copies (PG)^ and W^ would round it before E removes it.  The row pass therefore
-// works with G - g0, g0_i = G_i0 (key 0, visible to every row): (PG)^, W^, E and F'
+// works with G - g0, g0_i = G at the first key of its first key block: (PG)^, W^, E and F'
 // are those of the shifted G (F' = sum_j W_ij is shift-free since sum_j dS_ij = 0),
 // and the stored E is shifted back for the column pass, which forms G - E in fp32.
 //
@@ -113,7 +113,8 @@ struct RowLay {
 // the constant D, so its code is that of a kernel without the option.
 // GP: GProj on the rounded dS of gQ's dS b product (the pre-pass left P^ b in `pb`);
 // the coefficient rho_i goes to `rho_ws` for the column pass.
-template <bool PAD, bool GP>
+// WIN: the causal sliding window is in force (win); the other instances carry none of it.
+template <bool PAD, bool GP, bool WIN = false>
 __global__ void __launch_bounds__(kThreads, 1)
     bob_row_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                    const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmK,
@@ -122,7 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __nv_bfloat16* __restrict__ dO, const float* __restrict__ lse,
                    __nv_bfloat16* __restrict__ gQ, __nv_bfloat16* __restrict__ gdO, float4* __restrict__ ws,
                    const float* __restrict__ pb, float* __restrict__ rho_ws, int N, int Np, int nrb, int BH,
-                   float scale, float c, int causal, int G, int hd_arg) {
+                   float scale, float c, int causal, int win, int G, int hd_arg) {
   const int hd = PAD ? hd_arg : D;
   using Lay = RowLay;
   constexpr int NS = Lay::NS;
@@ -147,7 +148,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kvh = bh / G;          // the slice of K, V, b, c this query slice reads
   const int rb = nrb - 1 - ord.k;  // heaviest row blocks first (within a group of slices)
   // 64-key blocks this row block sees: up to its last row, or all of them when not causal
-  const int nkv = causal ? ((rb + 1) * BM + BN - 1) / BN : (N + BN - 1) / BN;
+  const int j0 = (WIN && causal) ? max(0, rb * BM - win + 1) / BN : 0;  // first key block a row sees (window win)
+  const int nkv = (causal ? ((rb + 1) * BM + BN - 1) / BN : (N + BN - 1) / BN) - j0;  // blocks j0 + j, j < nkv
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(q_full, 1);
@@ -192,10 +194,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j >= NS) wait(&empty[s], ((j / NS) - 1) & 1);
         uint8_t* st = sm + Lay::oStage + s * Lay::kStage;
         ptx::mbar_expect_tx(&full[s], 4 * kTile);
-        ptx::tma_load_3d(st + Lay::oc, &tmC, &full[s], 0, j * BN, kvh);
-        ptx::tma_load_3d(st + Lay::oV, &tmV, &full[s], 0, j * BN, kvh);
-        ptx::tma_load_3d(st + Lay::ob, &tmB, &full[s], 0, j * BN, kvh);
-        ptx::tma_load_3d(st + Lay::oKs, &tmK, &full[s], 0, j * BN, kvh);
+        ptx::tma_load_3d(st + Lay::oc, &tmC, &full[s], 0, (j0 + j) * BN, kvh);
+        ptx::tma_load_3d(st + Lay::oV, &tmV, &full[s], 0, (j0 + j) * BN, kvh);
+        ptx::tma_load_3d(st + Lay::ob, &tmB, &full[s], 0, (j0 + j) * BN, kvh);
+        ptx::tma_load_3d(st + Lay::oKs, &tmK, &full[s], 0, (j0 + j) * BN, kvh);
       }
       for (int j = (nkv > NS ? nkv - NS : 0); j < nkv; ++j) wait(&empty[j % NS], (j / NS) & 1);
     }
@@ -316,13 +318,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tmem_wait_ld();
       ptx::tc_fence_before();
       ptx::mbar_arrive(consumed_a);  // the MMA warp may now write [H | dP] into the tile region
-      if (j == 0) {  // the row's shift g0 = G at key 0, which every row sees
+      if (j == 0) {  // the row's shift g0 = G at the first key of the first block (any key serves)
         if (hf == 0) red[12 * BM + r] = scale * f(gv[0]);
         tc::named_sync(1, kCompute);
       }
-      const int krel = j * BN + c0 - rb * BM;
+      const int kb = j0 + j;
+      const int krel = kb * BN + c0 - rb * BM;
       // last visible key of this row, relative to the thread's first key of the block
-      const int klim = causal ? r - krel : N - 1 - (j * BN + c0);
+      const int klim = causal ? r - krel : N - 1 - (kb * BN + c0);
+      const int klo = (WIN && causal) ? klim - win + 1 : 0;  // first visible key of the row, relative to column 0
       uint64_t P2[16], G2[16];
       uint32_t pP[16], pG[16], pS[16], pW[16];
       // P, PG from the [G | S] tiles (while [H | dP] is being computed)
@@ -334,8 +338,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float2 arg = tc::unpk2(tc::fma2(tc::pk2(sv[t], sv[t + 1]), c2, nL2));
           float p0 = ptx::ex2(arg.x), p1 = ptx::ex2(arg.y);
           if constexpr (decltype(masked)::value) {
-            if (t > klim) p0 = 0.f;
-            if (t + 1 > klim) p1 = 0.f;
+            if (t > klim || t < klo) p0 = 0.f;
+            if (t + 1 > klim || t + 1 < klo) p1 = 0.f;
           }
           const int idx = t >> 1;
           P2[idx] = tc::pk2f(p0, p1);
@@ -350,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       // Causal: a block reaching past the first row of this CTA.  Otherwise: a block reaching past N.
-      if (causal ? krel + 31 > 0 : j * BN + c0 + 32 > N)
+      if (causal ? (krel + 31 > 0 || (WIN && kb * BN + c0 < rb * BM + BM - win)) : kb * BN + c0 + 32 > N)
         first(std::true_type{});
       else
         first(std::false_type{});
@@ -507,14 +511,14 @@ static_assert(ColLayT<true>::bytes <= 232448, "column pass shared memory");
 
 // GR: grouped key/value heads (G > 1).  The G == 1 instance keeps the plain tile loop.
 // PAD as in the row pass.  GP as in ColLayT (tmRho: the coefficients, laid out as the states).
-template <bool GR, bool PAD, bool GP>
+template <bool GR, bool PAD, bool GP, bool WIN = false>
 __global__ void __launch_bounds__(kThreads, 1)
     bob_col_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmdO, const __grid_constant__ CUtensorMap tmSt,
                    const __grid_constant__ CUtensorMap tmRho, const __nv_bfloat16* __restrict__ Kp, const __nv_bfloat16* __restrict__ Bp,
                    const __nv_bfloat16* __restrict__ Vp, const __nv_bfloat16* __restrict__ Cp,
                    __nv_bfloat16* __restrict__ gK, __nv_bfloat16* __restrict__ gV, int N, int BHkv, float scale,
-                   float c, int causal, int G, int hd_arg) {
+                   float c, int causal, int win, int G, int hd_arg) {
   const int hd = PAD ? hd_arg : D;
   using Lay = ColLayT<GP>;
   constexpr int NS = Lay::NS;
@@ -539,7 +543,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kb = ord.k;  // first key blocks have the most rows: first
   const int nq = (N + BN - 1) / BN;
   const int i0 = causal ? (kb * BM) / BN : 0;  // first query block that sees this key block
-  const int ntile = nq - i0;                   // query blocks per query slice
+  // query blocks per query slice: up to the last query any key of the block sees (i < key + win)
+  const int ntile = ((WIN && causal) ? min(N - 1, kb * BM + BM - 2 + win) / BN + 1 : nq) - i0;
   const int nt = GR ? G * ntile : ntile;       // tiles t = h * ntile + (i - i0), one gK, gV
 
   if (threadIdx.x == 0) {
@@ -726,8 +731,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           float p0 = ptx::ex2(arg.x), p1 = ptx::ex2(arg.y);
           if constexpr (decltype(masked)::value) {
             const int q0 = qbase + u;
-            if ((causal && q0 < key) || q0 >= N) p0 = 0.f;
-            if ((causal && q0 + 1 < key) || q0 + 1 >= N) p1 = 0.f;
+            if ((causal && (q0 < key || (WIN && q0 >= key + win))) || q0 >= N) p0 = 0.f;
+            if ((causal && (q0 + 1 < key || (WIN && q0 + 1 >= key + win))) || q0 + 1 >= N) p1 = 0.f;
           }
           const int idx = u >> 1;
           P2[idx] = tc::pk2f(p0, p1);
@@ -736,9 +741,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           pDP[idx] = ptx::pack_bf16(vdp.x, vdp.y);
         }
       };
-      // Causal mask only in the first blocks (queries before this CTA's last key) and
-      // past N only in the last block.
-      if ((causal && qbase < kb * BM + BM) || qbase + 32 > N)
+      // Causal mask only in the first blocks (queries before this CTA's last key) and in
+      // those past the window of its first key; past N only in the last block.
+      if ((causal && (qbase < kb * BM + BM || (WIN && qbase + 31 >= kb * BM + win))) || qbase + 32 > N)
         first(std::true_type{});
       else
         first(std::false_type{});
@@ -840,18 +845,22 @@ cudaError_t tc_bob(const Problem& p, const void* Q, const void* K, const void* V
   // which also serve d = 64 and ungrouped heads.
   if (passes & 1) {
     if (gproj && (e = tc_bob_pb(p, Q, K, b, lse, pbuf, st)) != cudaSuccess) return e;
-    auto row = gproj ? bob_row_kernel<true, true> : d < D ? bob_row_kernel<true, false> : bob_row_kernel<false, false>;
+    // Windowed: the general forms (runtime head dim, grouped tile loop in the column pass).
+    auto row = p.window > 0 ? (gproj ? bob_row_kernel<true, true, true> : bob_row_kernel<true, false, true>)
+               : gproj ? bob_row_kernel<true, true> : d < D ? bob_row_kernel<true, false> : bob_row_kernel<false, false>;
     e = cudaFuncSetAttribute(row, cudaFuncAttributeMaxDynamicSharedMemorySize, RowLay::bytes);
     if (e != cudaSuccess) return e;
     row<<<static_cast<unsigned>(nrb * BH), kThreads, RowLay::bytes, st>>>(
         q128, do128, a128, k64, v64, b64, c64, static_cast<const __nv_bfloat16*>(O),
         static_cast<const __nv_bfloat16*>(dO), lse, static_cast<__nv_bfloat16*>(gQ),
         static_cast<__nv_bfloat16*>(gdO), ws, pbuf, reinterpret_cast<float*>(rho), static_cast<int>(N),
-        static_cast<int>(Np), nrb, static_cast<int>(BH), p.scale, c, p.causal, p.group, static_cast<int>(d));
+        static_cast<int>(Np), nrb, static_cast<int>(BH), p.scale, c, p.causal, static_cast<int>(eff_window_tc(p)),
+        p.group, static_cast<int>(d));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (!(passes & 2)) return cudaSuccess;
-  auto col = gproj ? bob_col_kernel<true, true, true>
+  auto col = p.window > 0 ? (gproj ? bob_col_kernel<true, true, true, true> : bob_col_kernel<true, true, false, true>)
+             : gproj ? bob_col_kernel<true, true, true>
              : p.group > 1 ? (d < D ? bob_col_kernel<true, true, false> : bob_col_kernel<true, false, false>)
                            : (d < D ? bob_col_kernel<false, true, false> : bob_col_kernel<false, false, false>);
   const int cbytes = gproj ? ColLayT<true>::bytes : ColLayT<false>::bytes;
@@ -861,7 +870,7 @@ cudaError_t tc_bob(const Problem& p, const void* Q, const void* K, const void* V
       q64, a64, do64, s64, r64, static_cast<const __nv_bfloat16*>(K), static_cast<const __nv_bfloat16*>(b),
       static_cast<const __nv_bfloat16*>(V), static_cast<const __nv_bfloat16*>(cc), static_cast<__nv_bfloat16*>(gK),
       static_cast<__nv_bfloat16*>(gV), static_cast<int>(N), static_cast<int>(p.BHkv), p.scale, c, p.causal,
-      p.group, static_cast<int>(d));
+      static_cast<int>(eff_window_tc(p)), p.group, static_cast<int>(d));
   return cudaGetLastError();
 }
 

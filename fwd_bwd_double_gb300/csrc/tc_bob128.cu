@@ -77,7 +77,8 @@ static_assert(RowLay::bytes <= 232448, "row pass shared memory");
 
 // GP: GProj on the rounded dS of gQ's dS b product, as at d = 64 (P^ b from the pre-pass
 // in `pb`, 128 columns per row; the coefficient to `rho_ws`, by CTA h = 0).
-template <bool GP>
+// WIN: the causal sliding window is in force (win); the other instances carry none of it.
+template <bool GP, bool WIN = false>
 __global__ void __launch_bounds__(kThreads, 1)
     bob128_row_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                       const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmK,
@@ -86,7 +87,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __nv_bfloat16* __restrict__ dO, const float* __restrict__ lse,
                       __nv_bfloat16* __restrict__ gQ, __nv_bfloat16* __restrict__ gdO, float4* __restrict__ ws,
                       const float* __restrict__ pb, float* __restrict__ rho_ws, int N, int Np, int nrb, int BH,
-                      float scale, float c, int causal, int G, int hd) {
+                      float scale, float c, int causal, int win, int G, int hd) {
   using Lay = RowLay;
   constexpr int NS = Lay::NS;
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -110,7 +111,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int bh = ord.bh;
   const int kvh = bh / G;
   const int rb = nrb - 1 - ord.k;
-  const int nkv = causal ? ((rb + 1) * BM + BN - 1) / BN : (N + BN - 1) / BN;
+  const int j0 = (WIN && causal) ? max(0, rb * BM - win + 1) / BN : 0;  // first key block a row sees (window win)
+  const int nkv = (causal ? ((rb + 1) * BM + BN - 1) / BN : (N + BN - 1) / BN) - j0;  // blocks j0 + j, j < nkv
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(q_full, 1);
@@ -159,10 +161,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_expect_tx(&full[s], 8 * kSlab);
         for (int cc = 0; cc < 2; ++cc) {
           uint8_t* hs = st + cc * Lay::kHalf;
-          ptx::tma_load_3d(hs + Lay::oc, &tmC, &full[s], cc * 64, j * BN, kvh);
-          ptx::tma_load_3d(hs + Lay::oV, &tmV, &full[s], cc * 64, j * BN, kvh);
-          ptx::tma_load_3d(hs + Lay::ob, &tmB, &full[s], cc * 64, j * BN, kvh);
-          ptx::tma_load_3d(hs + Lay::oKs, &tmK, &full[s], cc * 64, j * BN, kvh);
+          ptx::tma_load_3d(hs + Lay::oc, &tmC, &full[s], cc * 64, (j0 + j) * BN, kvh);
+          ptx::tma_load_3d(hs + Lay::oV, &tmV, &full[s], cc * 64, (j0 + j) * BN, kvh);
+          ptx::tma_load_3d(hs + Lay::ob, &tmB, &full[s], cc * 64, (j0 + j) * BN, kvh);
+          ptx::tma_load_3d(hs + Lay::oKs, &tmK, &full[s], cc * 64, (j0 + j) * BN, kvh);
         }
       }
       for (int j = (nkv > NS ? nkv - NS : 0); j < nkv; ++j) wait(&empty[j % NS], (j / NS) & 1);
@@ -280,12 +282,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tmem_wait_ld();
       ptx::tc_fence_before();
       ptx::mbar_arrive(consumed_a);
-      if (j == 0) {  // the row's shift g0 = G at key 0 (the same in both CTAs of the pair)
+      if (j == 0) {  // the row's shift g0 = G at the first key of the first block (the same in both CTAs)
         if (hf == 0) red[2 * BM + r] = scale * f(gv[0]);
         tc::named_sync(1, kCompute);
       }
-      const int krel = j * BN + c0 - rb * BM;
-      const int klim = causal ? r - krel : N - 1 - (j * BN + c0);
+      const int kb = j0 + j;
+      const int krel = kb * BN + c0 - rb * BM;
+      const int klim = causal ? r - krel : N - 1 - (kb * BN + c0);
+      const int klo = (WIN && causal) ? klim - win + 1 : 0;  // first visible key of the row, relative to column 0
       uint64_t P2[16], G2[16];
       uint32_t pP[16], pG[16], pS[16], pW[16];
       auto first = [&](auto masked) {
@@ -296,8 +300,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float2 arg = tc::unpk2(tc::fma2(tc::pk2(sv[t], sv[t + 1]), c2, nL2));
           float p0 = ptx::ex2(arg.x), p1 = ptx::ex2(arg.y);
           if constexpr (decltype(masked)::value) {
-            if (t > klim) p0 = 0.f;
-            if (t + 1 > klim) p1 = 0.f;
+            if (t > klim || t < klo) p0 = 0.f;
+            if (t + 1 > klim || t + 1 < klo) p1 = 0.f;
           }
           const int idx = t >> 1;
           P2[idx] = tc::pk2f(p0, p1);
@@ -311,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           accP1 = tc::add_bf16_hi(accP1, pP[idx]);
         }
       };
-      if (causal ? krel + 31 > 0 : j * BN + c0 + 32 > N)
+      if (causal ? (krel + 31 > 0 || (WIN && kb * BN + c0 < rb * BM + BM - win)) : kb * BN + c0 + 32 > N)
         first(std::true_type{});
       else
         first(std::false_type{});
@@ -461,14 +465,14 @@ static_assert(ColLayT<true>::bytes <= 232448, "column pass shared memory");
 static_assert(ColLayT<false>::kStage % 1024 == 0 && ColLayT<true>::kStage % 1024 == 0,
               "stages stay 1024-byte aligned");
 
-template <bool GR, bool GP>
+template <bool GR, bool GP, bool WIN = false>
 __global__ void __launch_bounds__(kThreads, 1)
     bob128_col_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmdO, const __grid_constant__ CUtensorMap tmSt,
                       const __grid_constant__ CUtensorMap tmRho, const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmC,
                       const __nv_bfloat16* __restrict__ Kp, const __nv_bfloat16* __restrict__ Bp,
                       __nv_bfloat16* __restrict__ gK, __nv_bfloat16* __restrict__ gV, int N, int BHkv,
-                      float scale, float c, int causal, int G, int hd) {
+                      float scale, float c, int causal, int win, int G, int hd) {
   using Lay = ColLayT<GP>;
   constexpr int NS = Lay::NS;
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -494,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kb = ord.k;
   const int nq = (N + BN - 1) / BN;
   const int i0 = causal ? (kb * BM) / BN : 0;
-  const int ntile = nq - i0;
+  const int ntile = ((WIN && causal) ? min(N - 1, kb * BM + BM - 2 + win) / BN + 1 : nq) - i0;  // i < key + win
   const int nt = GR ? G * ntile : ntile;
 
   if (threadIdx.x == 0) {
@@ -688,8 +692,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           float p0 = ptx::ex2(arg.x), p1 = ptx::ex2(arg.y);
           if constexpr (decltype(masked)::value) {
             const int q0 = qbase + u;
-            if ((causal && q0 < key) || q0 >= N) p0 = 0.f;
-            if ((causal && q0 + 1 < key) || q0 + 1 >= N) p1 = 0.f;
+            if ((causal && (q0 < key || (WIN && q0 >= key + win))) || q0 >= N) p0 = 0.f;
+            if ((causal && (q0 + 1 < key || (WIN && q0 + 1 >= key + win))) || q0 + 1 >= N) p1 = 0.f;
           }
           const int idx = u >> 1;
           P2[idx] = tc::pk2f(p0, p1);
@@ -698,7 +702,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           pDP[idx] = ptx::pack_bf16(vdp.x, vdp.y);
         }
       };
-      if ((causal && qbase < kb * BM + BM) || qbase + 32 > N)
+      if ((causal && (qbase < kb * BM + BM || (WIN && qbase + 31 >= kb * BM + win))) || qbase + 32 > N)
         first(std::true_type{});
       else
         first(std::false_type{});
@@ -798,19 +802,22 @@ cudaError_t tc_bob128(const Problem& p, const void* Q, const void* K, const void
   cudaError_t e = cudaSuccess;
   if (passes & 1) {
     if (gproj && (e = tc_bob_pb(p, Q, K, b, lse, pbuf, st)) != cudaSuccess) return e;
-    auto row = gproj ? bob128_row_kernel<true> : bob128_row_kernel<false>;
+    auto row = p.window > 0 ? (gproj ? bob128_row_kernel<true, true> : bob128_row_kernel<false, true>)
+                            : (gproj ? bob128_row_kernel<true> : bob128_row_kernel<false>);
     e = cudaFuncSetAttribute(row, cudaFuncAttributeMaxDynamicSharedMemorySize, RowLay::bytes);
     if (e != cudaSuccess) return e;
     row<<<static_cast<unsigned>(2 * nrb * BH), kThreads, RowLay::bytes, st>>>(
         q128, do128, a128, k64, v64, b64, c64, static_cast<const __nv_bfloat16*>(O),
         static_cast<const __nv_bfloat16*>(dO), lse, static_cast<__nv_bfloat16*>(gQ),
         static_cast<__nv_bfloat16*>(gdO), ws, pbuf, reinterpret_cast<float*>(rho), static_cast<int>(N),
-        static_cast<int>(Np), nrb, static_cast<int>(BH), p.scale, c, p.causal, p.group, static_cast<int>(d));
+        static_cast<int>(Np), nrb, static_cast<int>(BH), p.scale, c, p.causal, static_cast<int>(eff_window_tc(p)),
+        p.group, static_cast<int>(d));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (!(passes & 2)) return cudaSuccess;
   // The GProj instance takes the grouped tile loop, which also serves ungrouped heads.
-  auto col = gproj ? bob128_col_kernel<true, true>
+  auto col = p.window > 0 ? (gproj ? bob128_col_kernel<true, true, true> : bob128_col_kernel<true, false, true>)
+             : gproj ? bob128_col_kernel<true, true>
                    : p.group > 1 ? bob128_col_kernel<true, false> : bob128_col_kernel<false, false>;
   const int cbytes = gproj ? ColLayT<true>::bytes : ColLayT<false>::bytes;
   e = cudaFuncSetAttribute(col, cudaFuncAttributeMaxDynamicSharedMemorySize, cbytes);
@@ -818,7 +825,8 @@ cudaError_t tc_bob128(const Problem& p, const void* Q, const void* K, const void
   col<<<static_cast<unsigned>(2 * nrb * p.BHkv), kThreads, cbytes, st>>>(
       q64, a64, do64, s64, r64, v128, c128, static_cast<const __nv_bfloat16*>(K), static_cast<const __nv_bfloat16*>(b),
       static_cast<__nv_bfloat16*>(gK), static_cast<__nv_bfloat16*>(gV), static_cast<int>(N),
-      static_cast<int>(p.BHkv), p.scale, c, p.causal, p.group, static_cast<int>(d));
+      static_cast<int>(p.BHkv), p.scale, c, p.causal, static_cast<int>(eff_window_tc(p)), p.group,
+      static_cast<int>(d));
   return cudaGetLastError();
 }
 

@@ -74,13 +74,14 @@ struct RowLay {
   static_assert(cols == kCols && cols <= 512, "TMEM budget");
 };
 
-template <int D, int NB, bool GP>
+// WIN: the causal sliding window is in force (win); the other instances carry none of it.
+template <int D, int NB, bool GP, bool WIN = false>
 __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
     bwd_row_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                    const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const __nv_bfloat16* __restrict__ O, const __nv_bfloat16* __restrict__ dO,
                    const float* __restrict__ lse, __nv_bfloat16* __restrict__ dQ, float4* __restrict__ ws, int N,
-                   int Np, int nrb, int BH, float scale, float c, int causal, int G, int dv) {
+                   int Np, int nrb, int BH, float scale, float c, int causal, int win, int G, int dv) {
   using Lay = RowLay<D, NB, GP>;
   static_assert(NB == 1, "one score-tile buffer, released early");
   constexpr int NS = Lay::NS;
@@ -101,8 +102,10 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
   const tc::Order ord = tc::grid_order(BH, nrb);
   const int bh = ord.bh;
   const int rb = nrb - 1 - ord.k;  // heaviest row blocks first (within a group of slices)
-  // key blocks touching rows <= the last row (all key blocks when not causal)
-  const int nkv = causal ? ((rb + 1) * BM + BN - 1) / BN : (N + BN - 1) / BN;
+  // key blocks j0 + j, j < nkv: those touching rows <= the last row (all key blocks when
+  // not causal), from the first one a row sees under the window win (> N when none)
+  const int j0 = (WIN && causal) ? max(0, rb * BM - win + 1) / BN : 0;
+  const int nkv = (causal ? ((rb + 1) * BM + BN - 1) / BN : (N + BN - 1) / BN) - j0;
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(q_full, 1);
@@ -147,8 +150,10 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
         if (j >= NS) wait(&empty[s], ((j / NS) - 1) & 1);
         ptx::mbar_expect_tx(&full[s], 2 * Lay::kStream);
         for (int cc = 0; cc < D / 64; ++cc) {
-          ptx::tma_load_3d(sm + Lay::oK + s * Lay::kStream + cc * BN * 128, &tmK, &full[s], cc * 64, j * BN, bh / G);
-          ptx::tma_load_3d(sm + Lay::oV + s * Lay::kStream + cc * BN * 128, &tmV, &full[s], cc * 64, j * BN, bh / G);
+          ptx::tma_load_3d(sm + Lay::oK + s * Lay::kStream + cc * BN * 128, &tmK, &full[s], cc * 64, (j0 + j) * BN,
+                           bh / G);
+          ptx::tma_load_3d(sm + Lay::oV + s * Lay::kStream + cc * BN * 128, &tmV, &full[s], cc * 64, (j0 + j) * BN,
+                           bh / G);
         }
       }
       for (int j = (nkv > NS ? nkv - NS : 0); j < nkv; ++j) wait(&empty[j % NS], (j / NS) & 1);
@@ -235,9 +240,11 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
       ptx::tmem_wait_ld();
       ptx::tc_fence_before();
       ptx::mbar_arrive(consumed);  // the MMA warp may now compute the next block's tiles here
-      const int krel = j * BN + c0 - rb * BM;  // key of my column 0 minus the block's first row
-      // last visible key of this row, relative to my column 0
-      const int klim = causal ? r - krel : N - 1 - (j * BN + c0);
+      const int kb = j0 + j;
+      const int krel = kb * BN + c0 - rb * BM;  // key of my column 0 minus the block's first row
+      // last and first visible key of this row, relative to my column 0
+      const int klim = causal ? r - krel : N - 1 - (kb * BN + c0);
+      const int klo = (WIN && causal) ? klim - win + 1 : 0;
       uint32_t dsk[16], pk[16];
       auto block = [&](auto masked) {
 #pragma unroll
@@ -245,8 +252,8 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
           const float2 arg = tc::unpk2(tc::fma2(tc::pk2(sv[t], sv[t + 1]), c2, nL2));
           float p0 = ptx::ex2(arg.x), p1 = ptx::ex2(arg.y);
           if constexpr (decltype(masked)::value) {
-            if (t > klim) p0 = 0.f;
-            if (t + 1 > klim) p1 = 0.f;
+            if (t > klim || t < klo) p0 = 0.f;
+            if (t + 1 > klim || t + 1 < klo) p1 = 0.f;
           }
           const float2 ds = tc::unpk2(tc::mul2(tc::pk2f(p0, p1), tc::add2(tc::pk2(pv[t], pv[t + 1]), nD2)));
           dsk[t >> 1] = ptx::pack_bf16(ds.x, ds.y);
@@ -257,7 +264,9 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
           }
         }
       };
-      if (causal ? krel + 31 > 0 : j * BN + c0 + 32 > N)  // the mask reaches into this thread's columns
+      // the mask reaches into this thread's columns: past the row (causal), below the
+      // window of the block's last row, or past N
+      if (causal ? (krel + 31 > 0 || (WIN && kb * BN + c0 < rb * BM + BM - win)) : kb * BN + c0 + 32 > N)
         block(std::true_type{});
       else
         block(std::false_type{});
@@ -337,12 +346,13 @@ struct ColLay {
 };
 
 // GR: grouped key/value heads (G > 1).  The G == 1 instance keeps the plain tile loop.
-template <int D, int NB, bool GP, bool GR>
+template <int D, int NB, bool GP, bool GR, bool WIN = false>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_col_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                    const __grid_constant__ CUtensorMap tmSt, __nv_bfloat16* __restrict__ dK,
-                   __nv_bfloat16* __restrict__ dV, int N, int BHkv, float scale, float c, int causal, int G, int dv) {
+                   __nv_bfloat16* __restrict__ dV, int N, int BHkv, float scale, float c, int causal, int win, int G,
+                   int dv) {
   using Lay = ColLay<D, NB, GP>;
   static_assert(NB == 1, "one score-tile buffer, released early");
   constexpr int NS = Lay::NS;
@@ -365,7 +375,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kb = ord.k;  // first key blocks have the most rows: first
   const int nq = (N + BN - 1) / BN;
   const int i0 = causal ? (kb * BM) / BN : 0;         // first query block with a query >= first key
-  const int ntile = nq - i0;                          // query blocks per query slice
+  // query blocks per query slice: up to the last query any key of the block sees (i < key + win)
+  const int ntile = ((WIN && causal) ? min(N - 1, kb * BM + BM - 2 + win) / BN + 1 : nq) - i0;
   const int nt = GR ? G * ntile : ntile;              // tiles t = h * ntile + (i - i0), one dK, dV
 
   if (threadIdx.x == 0) {
@@ -492,8 +503,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           float p0 = ptx::ex2(arg.x), p1 = ptx::ex2(arg.y);
           if constexpr (decltype(masked)::value) {
             const int q0 = qbase + u;
-            if ((causal && q0 < key) || q0 >= N) p0 = 0.f;
-            if ((causal && q0 + 1 < key) || q0 + 1 >= N) p1 = 0.f;
+            if ((causal && (q0 < key || (WIN && q0 >= key + win))) || q0 >= N) p0 = 0.f;
+            if ((causal && (q0 + 1 < key || (WIN && q0 + 1 >= key + win))) || q0 + 1 >= N) p1 = 0.f;
           }
           const float2 ds =
               tc::unpk2(tc::mul2(tc::pk2f(p0, p1), tc::add2(tc::pk2(pv[u], pv[u + 1]), tc::pk2f(A.z, A.w))));
@@ -506,7 +517,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       };
-      if ((causal && qbase < kb * BM + BM) || qbase + 32 > N)  // causal mask (first blocks) or past N (last block)
+      // causal mask (first blocks), past the window of the block's first key, or past N (last block)
+      if ((causal && (qbase < kb * BM + BM || (WIN && qbase + 31 >= kb * BM + win))) || qbase + 32 > N)
         block(std::true_type{});
       else
         block(std::false_type{});
@@ -570,23 +582,26 @@ cudaError_t launch(const Problem& p, const void* Q, const void* K, const void* V
   const int nrb = static_cast<int>((N + BM - 1) / BM);
   if (passes & 1) {
     using Lay = RowLay<D, NBR, GP>;
-    auto kern = bwd_row_kernel<D, NBR, GP>;
+    auto kern = p.window > 0 ? bwd_row_kernel<D, NBR, GP, true> : bwd_row_kernel<D, NBR, GP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::bytes);
     if (e != cudaSuccess) return e;
     kern<<<static_cast<unsigned>(nrb * BH), kThreads, Lay::bytes, st>>>(
         q128, do128, k64, v64, static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), lse,
         static_cast<__nv_bfloat16*>(dQ), ws, static_cast<int>(N), static_cast<int>(Np), nrb, static_cast<int>(BH),
-        p.scale, c, p.causal, p.group, static_cast<int>(d));
+        p.scale, c, p.causal, static_cast<int>(eff_window_tc(p)), p.group, static_cast<int>(d));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (passes & 2) {
     using Lay = ColLay<D, NBC, GP>;
-    auto kern = p.group > 1 ? bwd_col_kernel<D, NBC, GP, true> : bwd_col_kernel<D, NBC, GP, false>;
+    // Windowed: the grouped tile loop (which also serves ungrouped heads).
+    auto kern = p.window > 0 ? bwd_col_kernel<D, NBC, GP, true, true>
+                : p.group > 1 ? bwd_col_kernel<D, NBC, GP, true> : bwd_col_kernel<D, NBC, GP, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::bytes);
     if (e != cudaSuccess) return e;
     kern<<<static_cast<unsigned>(nrb * p.BHkv), kThreads, Lay::bytes, st>>>(
         k128, v128, q64, do64, s64, static_cast<__nv_bfloat16*>(dK), static_cast<__nv_bfloat16*>(dV),
-        static_cast<int>(N), static_cast<int>(p.BHkv), p.scale, c, p.causal, p.group, static_cast<int>(d));
+        static_cast<int>(N), static_cast<int>(p.BHkv), p.scale, c, p.causal, static_cast<int>(eff_window_tc(p)),
+        p.group, static_cast<int>(d));
     return cudaGetLastError();
   }
   return cudaSuccess;

@@ -112,13 +112,14 @@ struct RowLay {
 };
 static_assert(RowLay<128>::bytes <= 232448, "row pass shared memory at d = 128");
 
-template <int DR, bool GP>
+// WIN: the causal sliding window is in force (win); the other instances carry none of it.
+template <int DR, bool GP, bool WIN = false>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_row_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                const __nv_bfloat16* __restrict__ O, const __nv_bfloat16* __restrict__ dO,
                const float* __restrict__ lse, __nv_bfloat16* __restrict__ dQ, float4* __restrict__ ws, int N, int Np,
-               int nrb, int BH, float scale, float c, int causal, int G, int dv) {
+               int nrb, int BH, float scale, float c, int causal, int win, int G, int dv) {
   using Lay = RowLay<DR, GP>;
   constexpr int NS = Lay::NSR, kTile = Lay::kTileR, DG = Lay::DGR, D = DR;
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -128,7 +129,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const tc::Order ord = tc::grid_order(BH, nrb);
   const int bh = ord.bh;
   const int rb = nrb - 1 - ord.k;  // heaviest first within a group of slices
-  const int nkv = causal ? rb + 1 : nrb;  // 128-key blocks j <= rb (all blocks when not causal)
+  // 128-key blocks j0 + j, j < nkv: up to rb (all blocks when not causal), from the first
+  // block a row of this block sees under the window win (larger than N when there is none)
+  const int j0 = (WIN && causal) ? max(0, rb * BW - win + 1) / BW : 0;
+  const int nkv = (causal ? rb + 1 : nrb) - j0;
 
   if (threadIdx.x == 0) sy.init(sm);
   if (warp == kCW + 1) {
@@ -156,8 +160,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j >= NS) wait(&sy.empty[s], ((j / NS) - 1) & 1);
         ptx::mbar_expect_tx(&sy.full[s], 2 * kTile);
         for (int cc = 0; cc < D / 64; ++cc) {
-          ptx::tma_load_3d(sm + Lay::oK + s * kTile + cc * BW * 128, &tmK, &sy.full[s], cc * 64, j * BW, bh / G);
-          ptx::tma_load_3d(sm + Lay::oV + s * kTile + cc * BW * 128, &tmV, &sy.full[s], cc * 64, j * BW, bh / G);
+          ptx::tma_load_3d(sm + Lay::oK + s * kTile + cc * BW * 128, &tmK, &sy.full[s], cc * 64, (j0 + j) * BW,
+                           bh / G);
+          ptx::tma_load_3d(sm + Lay::oV + s * kTile + cc * BW * 128, &tmV, &sy.full[s], cc * 64, (j0 + j) * BW,
+                           bh / G);
         }
       }
       for (int j = (nkv > NS ? nkv - NS : 0); j < nkv; ++j) wait(&sy.empty[j % NS], (j / NS) & 1);
@@ -248,17 +254,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_before();
       ptx::mbar_arrive(sy.consumed);
       uint32_t dsk[kC / 2], pkk[GP ? kC / 2 : 1];
-      const int klim = causal ? r : N - 1 - j * BW;  // last visible key of this row, relative to the block
+      const int kb = j0 + j;
+      const int klim = causal ? (WIN ? rb * BW + r - kb * BW : r) : N - 1 - kb * BW;  // last visible key, relative
+      const int klo = (WIN && causal) ? rb * BW + r - win + 1 - kb * BW : 0;        // first visible key, relative
       auto block = [&](auto masked) {
 #pragma unroll
         for (int t = 0; t < kC; t += 2) {
           const float2 arg = tc::unpk2(tc::fma2(tc::pk2(sv[t], sv[t + 1]), c2, nL2));
           float p0 = ptx::ex2(arg.x), p1 = ptx::ex2(arg.y);
           if constexpr (decltype(masked)::value) {
-            // Causal: the diagonal block, key - row = column - lane row.  Otherwise the
-            // last block: keys at or past N.
-            if (c0 + t > klim) p0 = 0.f;
-            if (c0 + t + 1 > klim) p1 = 0.f;
+            // Causal: the diagonal block (keys past the row) and the blocks below a
+            // row's window.  Otherwise the last block: keys at or past N.
+            if (c0 + t > klim || c0 + t < klo) p0 = 0.f;
+            if (c0 + t + 1 > klim || c0 + t + 1 < klo) p1 = 0.f;
           }
           const float2 ds = tc::unpk2(tc::mul2(tc::pk2f(p0, p1), tc::add2(tc::pk2(pv[t], pv[t + 1]), nD2)));
           dsk[t >> 1] = ptx::pack_bf16(ds.x, ds.y);
@@ -269,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       };
-      if (causal ? j == rb : (j == nkv - 1 && (N % BW) != 0))
+      if (causal ? (kb == rb || (WIN && kb * BW < rb * BW + BW - win)) : (j == nkv - 1 && (N % BW) != 0))
         block(std::true_type{});
       else
         block(std::false_type{});
@@ -354,13 +362,13 @@ using ColLay = ColLayT<false>;
 static_assert(ColLayT<true>::bytes <= 232448 && ColLayT<true>::oRQ % 1024 == 0, "GProj column layout");
 
 // GR: grouped key/value heads (G > 1).  The G == 1 instance keeps the plain tile loop.
-template <bool GR, bool GP>
+template <bool GR, bool GP, bool WIN = false>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_col_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                const __grid_constant__ CUtensorMap tmSt, __nv_bfloat16* __restrict__ dK,
-               __nv_bfloat16* __restrict__ dV, int N, int nb, int BHkv, float scale, float c, int causal, int G,
-               int dv) {
+               __nv_bfloat16* __restrict__ dV, int N, int nb, int BHkv, float scale, float c, int causal, int win,
+               int G, int dv) {
   using Lay = ColLayT<GP>;
   extern __shared__ __align__(1024) uint8_t sm[];
   Sync sy(sm + Lay::oBar);
@@ -369,7 +377,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kvh = ord.bh;        // key/value slice; its G query slices are kvh * G + h, h < G
   const int kb = ord.k;          // first key blocks have the most query blocks: first
   const int i0 = causal ? kb : 0;  // first query block that sees this key block
-  const int ntile = nb - i0;     // query blocks per query slice
+  // query blocks per query slice: up to the last query any key of the block sees
+  // (queries i < key + win under the window win; larger than N when there is none)
+  const int ntile = ((WIN && causal) ? min(N - 1, kb * BW + BW - 2 + win) / BW + 1 : nb) - i0;
   const int nt = GR ? G * ntile : ntile;  // tiles t = h * ntile + (i - i0), summed into one dK, dV
 
   if (threadIdx.x == 0) sy.init(sm);
@@ -503,8 +513,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               float p0 = ptx::ex2(arg.x), p1 = ptx::ex2(arg.y);
               if constexpr (decltype(masked)::value) {
                 const int q0 = qbase + 8 * k, kk = kbase + 16 * h + 8 * m;
-                if ((causal && q0 < kk) || q0 >= N) p0 = 0.f;
-                if ((causal && q0 + 1 < kk) || q0 + 1 >= N) p1 = 0.f;
+                if ((causal && (q0 < kk || (WIN && q0 >= kk + win))) || q0 >= N) p0 = 0.f;
+                if ((causal && (q0 + 1 < kk || (WIN && q0 + 1 >= kk + win))) || q0 + 1 >= N) p1 = 0.f;
               }
               const float2 ds = tc::unpk2(
                   tc::mul2(tc::pk2f(p0, p1), tc::add2(tc::pk2(pv[h][e], pv[h][e + 1]), tc::pk2f(A[k].z, A[k].w))));
@@ -512,7 +522,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               dk[h][2 * k + m] = ptx::pack_bf16(ds.x, ds.y);
             }
       };
-      if ((causal && (GR ? i == kb : t == 0)) || i * BW + c0 + kC > N)  // the diagonal block, or past N
+      // the diagonal block, a block reaching past the window of the block's first key, or past N
+      if ((causal && (GR ? i == kb : t == 0)) || (WIN && causal && i * BW + BW - 1 >= kb * BW + win) ||
+          i * BW + c0 + kC > N)
         block(std::true_type{});
       else
         block(std::false_type{});
@@ -592,13 +604,13 @@ cudaError_t tc_bwd_wide(const Problem& p, const void* Q, const void* K, const vo
         !make_tmap_bf16(&k, K, N, d, p.BHkv, BW) || !make_tmap_bf16(&v, V, N, d, p.BHkv, BW))
       return cudaErrorInvalidValue;
     const int nb = static_cast<int>((N + BW - 1) / BW);
-    cudaError_t e = cudaFuncSetAttribute(bwd_row_wide_kernel<128, false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, RowLay<128>::bytes);
+    auto row = p.window > 0 ? bwd_row_wide_kernel<128, false, true> : bwd_row_wide_kernel<128, false, false>;
+    cudaError_t e = cudaFuncSetAttribute(row, cudaFuncAttributeMaxDynamicSharedMemorySize, RowLay<128>::bytes);
     if (e != cudaSuccess) return e;
-    bwd_row_wide_kernel<128, false><<<static_cast<unsigned>(nb * BH), kThreads, RowLay<128>::bytes, st>>>(
+    row<<<static_cast<unsigned>(nb * BH), kThreads, RowLay<128>::bytes, st>>>(
         q, g, k, v, static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), lse,
         static_cast<__nv_bfloat16*>(dQ), ws, static_cast<int>(N), static_cast<int>(Np), nb, static_cast<int>(BH),
-        p.scale, p.scale * kLog2e, p.causal, p.group, static_cast<int>(d));
+        p.scale, p.scale * kLog2e, p.causal, static_cast<int>(eff_window_tc(p)), p.group, static_cast<int>(d));
     return cudaGetLastError();
   }
   alignas(64) CUtensorMap q, g, k, v, s;
@@ -612,25 +624,28 @@ cudaError_t tc_bwd_wide(const Problem& p, const void* Q, const void* K, const vo
   const int nb = static_cast<int>((N + BW - 1) / BW);
   cudaError_t e = cudaSuccess;
   if (passes & 1) {
-    auto row = gproj ? bwd_row_wide_kernel<64, true> : bwd_row_wide_kernel<64, false>;
+    auto row = p.window > 0 ? (gproj ? bwd_row_wide_kernel<64, true, true> : bwd_row_wide_kernel<64, false, true>)
+                            : (gproj ? bwd_row_wide_kernel<64, true> : bwd_row_wide_kernel<64, false>);
     const int bytes = gproj ? RowLay<64, true>::bytes : RowLay<64, false>::bytes;
     e = cudaFuncSetAttribute(row, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
     row<<<static_cast<unsigned>(nb * BH), kThreads, bytes, st>>>(
         q, g, k, v, static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), lse,
         static_cast<__nv_bfloat16*>(dQ), ws, static_cast<int>(N), static_cast<int>(Np), nb, static_cast<int>(BH),
-        p.scale, c, p.causal, p.group, static_cast<int>(d));
+        p.scale, c, p.causal, static_cast<int>(eff_window_tc(p)), p.group, static_cast<int>(d));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (passes & 2) {
-    auto kern = gproj ? (p.group > 1 ? bwd_col_wide_kernel<true, true> : bwd_col_wide_kernel<false, true>)
-                      : (p.group > 1 ? bwd_col_wide_kernel<true, false> : bwd_col_wide_kernel<false, false>);
+    // Windowed: the grouped tile loop (which also serves ungrouped heads).
+    auto kern = p.window > 0 ? (gproj ? bwd_col_wide_kernel<true, true, true> : bwd_col_wide_kernel<true, false, true>)
+                : gproj ? (p.group > 1 ? bwd_col_wide_kernel<true, true> : bwd_col_wide_kernel<false, true>)
+                        : (p.group > 1 ? bwd_col_wide_kernel<true, false> : bwd_col_wide_kernel<false, false>);
     const int bytes = gproj ? ColLayT<true>::bytes : ColLayT<false>::bytes;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
     kern<<<static_cast<unsigned>(nb * p.BHkv), kThreads, bytes, st>>>(
         k, v, q, g, s, static_cast<__nv_bfloat16*>(dK), static_cast<__nv_bfloat16*>(dV), static_cast<int>(N), nb,
-        static_cast<int>(p.BHkv), p.scale, c, p.causal, p.group, static_cast<int>(d));
+        static_cast<int>(p.BHkv), p.scale, c, p.causal, static_cast<int>(eff_window_tc(p)), p.group, static_cast<int>(d));
     e = cudaGetLastError();
   }
   return e;

@@ -72,12 +72,14 @@ __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int rows, int k)
   return ptx::sdesc_sw128(base + k * 16 * 128, rows * 128, 1024);
 }
 
-template <int D, bool PB>
+// WIN: the causal sliding window is in force (win); the instances without it carry none
+// of its arithmetic.
+template <int D, bool PB, bool WIN>
 __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O, float* __restrict__ lse,
                const float* __restrict__ lse_in, float* __restrict__ pb, int N, int nrb, int BH, float scale,
-               float scale_log2, int causal, int G, int dv) {
+               float scale_log2, int causal, int win, int G, int dv) {
   using Lay = Layout<D>;
   extern __shared__ __align__(1024) uint8_t sm[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Lay::oBar);
@@ -97,7 +99,10 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
   const int bh = ord.bh;
   const int kvh = bh / G;          // the key/value slice this query slice reads
   const int rb = nrb - 1 - ord.k;  // heaviest row blocks first (within a group of slices)
-  const int nkv = causal ? rb + 1 : nrb;  // key blocks this row block sees
+  // Key blocks this row block sees: j0 + j for j < nkv.  win: the causal window (key k
+  // visible to row i iff i - win < k <= i; larger than N when there is none).
+  const int j0 = (WIN && causal) ? max(0, rb * BM - win + 1) / BN : 0;
+  const int nkv = (causal ? rb + 1 : nrb) - j0;
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(q_full, 1);
@@ -142,8 +147,8 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
         if (j >= NS) wait(&empty[s], ((j / NS) - 1) & 1);
         ptx::mbar_expect_tx(&full[s], 2 * Lay::kKV);
         for (int c = 0; c < D / 64; ++c) {
-          ptx::tma_load_3d(sm + Lay::oK + s * Lay::kKV + c * BN * 128, &tmK, &full[s], c * 64, j * BN, kvh);
-          ptx::tma_load_3d(sm + Lay::oV + s * Lay::kKV + c * BN * 128, &tmV, &full[s], c * 64, j * BN, kvh);
+          ptx::tma_load_3d(sm + Lay::oK + s * Lay::kKV + c * BN * 128, &tmK, &full[s], c * 64, (j0 + j) * BN, kvh);
+          ptx::tma_load_3d(sm + Lay::oV + s * Lay::kKV + c * BN * 128, &tmV, &full[s], c * 64, (j0 + j) * BN, kvh);
         }
       }
       // Drain: the last NS stages must have been consumed before the CTA exits.
@@ -197,8 +202,12 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
     for (int j = 0; j < nkv; ++j) {
       wait(s_full, j & 1);
       ptx::tc_fence_after();
-      const bool diag = causal ? (j == rb) : (j == nkv - 1 && (N % BN) != 0);
-      const int klim = causal ? r : N - 1 - j * BN;
+      const int kb = j0 + j;
+      // Keys of this block past the row (causal), or past N, or below the row's window.
+      const bool diag = causal ? (kb == rb) : (j == nkv - 1 && (N % BN) != 0);
+      const bool low = WIN && causal && kb * BN < rb * BM + BM - win;
+      const int klim = causal ? (WIN ? rb * BM + r - kb * BN : r) : N - 1 - kb * BN;
+      const int klo = (WIN && causal) ? rb * BM + r - win + 1 - kb * BN : 0;
       uint32_t v[4][32];
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) ptx::tmem_ld32(tS + lane_off + ch * 32, v[ch]);
@@ -212,9 +221,9 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
         for (int t = 0; t < 32; t += 2) {
           const float2 arg = tc::unpk2(tc::fma2(tc::pk2(v[ch][t], v[ch][t + 1]), c2, nL2));
           float p0 = ptx::ex2(arg.x), p1 = ptx::ex2(arg.y);
-          if (diag) {
-            if (ch * 32 + t > klim) p0 = 0.f;
-            if (ch * 32 + t + 1 > klim) p1 = 0.f;
+          if (diag || low) {
+            if (ch * 32 + t > klim || ch * 32 + t < klo) p0 = 0.f;
+            if (ch * 32 + t + 1 > klim || ch * 32 + t + 1 < klo) p1 = 0.f;
           }
           pk[ch][t >> 1] = ptx::pack_bf16(p0, p1);
         }
@@ -251,10 +260,14 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
     for (int j = 0; j < nkv; ++j) {
       wait(s_full, j & 1);
       ptx::tc_fence_after();
-      // Causal: only the diagonal block holds keys after some rows.  Otherwise only
-      // the last block can hold keys past N (TMA reads them as zeros).
-      const bool diag = causal ? (j == rb) : (j == nkv - 1 && (N % BN) != 0);
-      const int klim = causal ? r : N - 1 - j * BN;  // last visible key of this row, relative to the block
+      // Causal: only the diagonal block holds keys after some rows, and only the first
+      // blocks keys below a row's window.  Otherwise only the last block can hold keys
+      // past N (TMA reads them as zeros).
+      const int kb = j0 + j;
+      const bool diag = causal ? (kb == rb) : (j == nkv - 1 && (N % BN) != 0);
+      const bool low = WIN && causal && kb * BN < rb * BM + BM - win;
+      const int klim = causal ? (WIN ? rb * BM + r - kb * BN : r) : N - 1 - kb * BN;  // last visible key, relative
+      const int klo = (WIN && causal) ? rb * BM + r - win + 1 - kb * BN : 0;        // first visible key, relative
       // The whole 128-column S row in registers: four loads, one wait.
       uint32_t v[4][32];
 #pragma unroll
@@ -262,12 +275,12 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
       ptx::tmem_wait_ld();
       ptx::tc_fence_before();
       ptx::mbar_arrive(s_consumed);  // the MMA warp may now compute S_{j+1} into these columns
-      if (diag) {
+      if (diag || low) {
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch)
 #pragma unroll
           for (int t = 0; t < 32; ++t)
-            if (ch * 32 + t > klim) v[ch][t] = __float_as_uint(-INFINITY);
+            if (ch * 32 + t > klim || ch * 32 + t < klo) v[ch][t] = __float_as_uint(-INFINITY);
       }
       // Row max over 8 independent partial maxima (short dependency chains).
       float mx8[8];
@@ -285,8 +298,10 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
       l *= alpha;
       m = m_new;
       // p = 2^((s - m) s log2 e): subtract first, then scale (masked entries are -inf -> 0).
-      // Packed f32x2: (s - m) then * s log2 e for two keys per instruction.
-      const uint64_t nm2 = tc::pk2f(-m, -m), c2 = tc::pk2f(scale_log2, scale_log2);
+      // Packed f32x2: (s - m) then * s log2 e for two keys per instruction.  A row with
+      // no visible key yet (its window starts in a later block) subtracts 0, not -inf.
+      const float msub = (WIN && m == -INFINITY) ? 0.f : m;
+      const uint64_t nm2 = tc::pk2f(-msub, -msub), c2 = tc::pk2f(scale_log2, scale_log2);
       uint64_t rs4[4] = {0, 0, 0, 0};
       uint32_t pk[4][16];  // P_j as bf16 pairs, written once P_{j-1} V_{j-1} is done
 #pragma unroll
@@ -363,12 +378,13 @@ cudaError_t launch(const Problem& p, const void* Q, const void* K, const void* V
     return cudaErrorInvalidValue;
   const int nrb = static_cast<int>((p.N + BM - 1) / BM);
   const size_t smem = Layout<D>::bytes;
-  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, PB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  auto kern = p.window > 0 ? fwd_kernel<D, PB, true> : fwd_kernel<D, PB, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  fwd_kernel<D, PB><<<static_cast<unsigned>(nrb * p.BH), kThreads, smem, st>>>(
+  kern<<<static_cast<unsigned>(nrb * p.BH), kThreads, smem, st>>>(
       mq, mk, mv, static_cast<__nv_bfloat16*>(O), lse, lse_in, pb, static_cast<int>(p.N), nrb,
-      static_cast<int>(p.BH), p.scale, p.scale * kLog2e, p.causal, p.group, static_cast<int>(p.d));
+      static_cast<int>(p.BH), p.scale, p.scale * kLog2e, p.causal, static_cast<int>(eff_window_tc(p)), p.group,
+      static_cast<int>(p.d));
   return cudaGetLastError();
 }
 

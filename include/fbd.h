@@ -79,8 +79,9 @@ extern "C" {
 typedef enum {
   ATTN_OK = 0,
   ATTN_ERR_INVALID_ARG = 1,  /* NULL/negative/overlapping arguments, non-finite scale,
-                                group < 0 or not dividing H */
-  ATTN_ERR_UNSUPPORTED = 2,  /* causal not 0 or 1, d not supported, unknown dtype */
+                                group < 0 or not dividing H, window < 0 */
+  ATTN_ERR_UNSUPPORTED = 2,  /* causal not 0 or 1, window > 0 without causal = 1,
+                                d not supported, unknown dtype */
   ATTN_ERR_ALIGNMENT = 3,    /* a pointer is not 16-byte aligned */
   ATTN_ERR_WORKSPACE = 4,    /* workspace NULL or smaller than the *_workspace_bytes query */
   ATTN_ERR_LAUNCH = 5,       /* CUDA rejected a launch or a tensor-map encode */
@@ -101,6 +102,11 @@ typedef struct {
                           multi-head attention; g must divide H; g == H is multi-query).
                           Query head h reads key/value head h / g (integer division);
                           see "Grouped key/value heads" above. */
+  int32_t window;      /* causal sliding window W: with W >= 1 (and causal = 1) key j
+                          is visible to query i iff i - W < j <= i; 0 means no window
+                          (W >= N is the same as none).  A flexible mask ([BoB] "When
+                          FlashBoB changes the engineering plan" lists flexible masks
+                          among the next extensions); every operation honours it. */
 } attn_desc_t;
 
 /* Forward.  [FA] "The Flash Attention algorithm", "Online softmax recurrence",

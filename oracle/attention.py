@@ -63,6 +63,12 @@ class Window:
     def __repr__(self):
         return f"Window({self.W})"
 
+    def __eq__(self, other):
+        return isinstance(other, Window) and other.W == self.W
+
+    def __hash__(self):
+        return hash(("Window", self.W))
+
 
 def hidden(rows, keys, causal):
     """Boolean [len(rows), len(keys)]: True where the key is masked for the row

@@ -59,19 +59,20 @@ def oracle_full(w, op, causal=True):
                           causal=causal, groups=g)
 
 
-def run_ops(w, x_dev, ops=("fwd", "bwd", "bob"), gproj=0, causal=True):
-    """Run the requested ops through the binding (gproj for the backward and the BoB)."""
+def run_ops(w, x_dev, ops=("fwd", "bwd", "bob"), gproj=0, causal=True, window=0):
+    """Run the requested ops through the binding (gproj for the backward and the BoB;
+    window: the causal sliding window, 0 for none)."""
     import fwd_bwd_double_gb300 as fbd
     out = {}
-    O, lse = fbd.attn_fwd(x_dev["Q"], x_dev["K"], x_dev["V"], scale=w.scale, causal=causal)
+    O, lse = fbd.attn_fwd(x_dev["Q"], x_dev["K"], x_dev["V"], scale=w.scale, causal=causal, window=window)
     out["O"], out["L"] = O, lse
     if "bwd" in ops:
         out["dQ"], out["dK"], out["dV"] = fbd.attn_bwd(x_dev["Q"], x_dev["K"], x_dev["V"], O, x_dev["dO"], lse,
-                                                       gproj=gproj, scale=w.scale, causal=causal)
+                                                       gproj=gproj, scale=w.scale, causal=causal, window=window)
     if "bob" in ops:
         out["gQ"], out["gK"], out["gV"], out["gdO"] = fbd.attn_bob(
             x_dev["Q"], x_dev["K"], x_dev["V"], O, x_dev["dO"], lse, x_dev["gdQ"], x_dev["gdK"], x_dev["gdV"],
-            scale=w.scale, causal=causal, gproj=gproj)
+            scale=w.scale, causal=causal, window=window, gproj=gproj)
     fbd.attn_device_status()
     return out
 

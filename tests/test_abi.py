@@ -32,8 +32,8 @@ def test_library_exports_every_declared_function():
         assert n in fbd._lib.PROTOTYPES, f"binding lacks a prototype for {n}"
 
 
-def desc(B=1, H=2, N=64, d=64, scale=0.0, causal=1, dtype=1, group=0):
-    return AttnDesc(B, H, N, d, scale, causal, dtype, group)
+def desc(B=1, H=2, N=64, d=64, scale=0.0, causal=1, dtype=1, group=0, window=0):
+    return AttnDesc(B, H, N, d, scale, causal, dtype, group, window)
 
 
 def ptrs(n, base=FAKE, stride=1 << 30):
@@ -63,6 +63,7 @@ def bob(dsc, p=None, ws_bytes=None, gproj=0):
     (dict(scale=float("nan")), INVALID), (dict(scale=float("inf")), INVALID), (dict(scale=-1.0), INVALID),
     (dict(N=1 << 31), INVALID),
     (dict(group=-1), INVALID), (dict(H=2, group=3), INVALID), (dict(H=6, group=4), INVALID),
+    (dict(window=-1), INVALID), (dict(window=8, causal=0), UNSUP),
 ])
 def test_rejects_bad_descriptors(kw, code):
     d = desc(**kw)

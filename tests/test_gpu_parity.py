@@ -26,8 +26,9 @@ def _lib():
     __graft_entry__.build()
 
 
-def check_full(w, got, ops, causal=True):
+def check_full(w, got, ops, causal=True, window=0):
     tol = TOL[w.dtype]
+    causal = oracle.Window(window) if window else causal
     errs = {}
     f = oracle_full(w, "fwd", causal)
     errs["O"], errs["L"] = rel_fro(host(got["O"]), f["O"]), rel_fro(host(got["L"]), f["L"])
@@ -543,3 +544,73 @@ def test_padded_head_dims_bf16(d, causal):
     got1 = run_ops(w, to_device(inputs(w), w), ops=("bwd", "bob"), gproj=1, causal=causal)
     errs1 = check_full(w, got1, ("bwd", "bob"), causal=causal)
     print(w.name, causal, {k: f"{v:.2e}" for k, v in errs.items()}, "gproj", {k: f"{v:.2e}" for k, v in errs1.items()})
+
+
+# --------------------------------------------------------- causal sliding window ----
+# Key j visible to query i iff i - win < j <= i (desc->window).  The windows cover less
+# than one 64-key block (1, 17), one block (64, 128), between blocks (100, 200) and past
+# N (the causal mask); N = 1000 spans several row and key blocks and a ragged tail.
+
+@pytest.mark.parametrize("win", [1, 17, 64, 100, 128, 200, 5000])
+@pytest.mark.parametrize("d,dtype", [(64, "bf16"), (128, "bf16"), (64, "f32")])
+def test_window_all_ops(win, d, dtype):
+    w = W.Workload(f"window_B1H3N1000d{d}_{dtype}", 1, 3, 1000, d, dtype)
+    got = run_ops(w, to_device(inputs(w), w), ops=("bwd", "bob"), window=win)
+    if win == 1:
+        # Each row sees only its own key: P = I, so dQ, dK, gQ, gK, gV are exactly 0 and
+        # O = V, dV = dO, gdO = gdV (the oracle's pinned closed forms).  The zeros are
+        # checked against the scale of the outputs that are not zero.
+        x = inputs(w)
+        for k, want in (("O", x["V"]), ("dV", x["dO"]), ("gdO", x["gdV"])):
+            assert rel_fro(host(got[k]), want) <= TOL[w.dtype], k
+        scale = float(np.abs(x["dO"]).max())
+        for k in ("dQ", "dK", "gQ", "gK", "gV"):
+            assert float(np.abs(host(got[k])).max()) <= TOL[w.dtype] * scale, k
+        return
+    errs = check_full(w, got, ("bwd", "bob"), window=win)
+    print(w.name, win, {k: f"{v:.2e}" for k, v in errs.items()})
+
+
+@pytest.mark.parametrize("win", [33, 130])
+@pytest.mark.parametrize("d", [32, 96, 256])
+def test_window_other_head_dims_bf16(d, win):
+    w = W.Workload(f"window_B1H2N600d{d}_bf16", 1, 2, 600, d, "bf16")
+    for gp in (0, 1):
+        got = run_ops(w, to_device(inputs(w), w), ops=("bwd", "bob"), gproj=gp, window=win)
+        check_full(w, got, ("bwd", "bob"), window=win)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_window_gproj_and_grouped_heads(d):
+    w = W.Workload(f"window_gqa_B2H6g3N700d{d}_bf16", 2, 6, 700, d, "bf16", group=3)
+    for gp in (0, 1):
+        got = run_ops(w, to_device(inputs(w), w), ops=("bwd", "bob"), gproj=gp, window=150)
+        errs = check_full(w, got, ("bwd", "bob"), window=150)
+        print(w.name, gp, {k: f"{v:.2e}" for k, v in errs.items()})
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_window_passes_compose_on_nan_workspace(d):
+    import torch
+    import fwd_bwd_double_gb300 as fbd
+    w = W.Workload(f"window_passes_B1H3N300d{d}_bf16", 1, 3, 300, d, "bf16")
+    x = to_device(inputs(w), w)
+    O, lse = fbd.attn_fwd(x["Q"], x["K"], x["V"], window=70)
+    for gp in (0, 1):
+        ref_b = fbd.attn_bwd(x["Q"], x["K"], x["V"], O, x["dO"], lse, gproj=gp, window=70)
+        ref_g = fbd.attn_bob(x["Q"], x["K"], x["V"], O, x["dO"], lse, x["gdQ"], x["gdK"], x["gdV"], window=70,
+                             gproj=gp)
+        desc = fbd.make_desc(x["Q"], window=70)
+        nbytes = max(fbd.attn_bwd_workspace_bytes(desc, gp), fbd.attn_bob_workspace_bytes(desc, gp))
+        ws = torch.full((nbytes // 4,), float("nan"), device="cuda")
+        b = [torch.full_like(x["Q"], float("nan")) for _ in range(3)]
+        g = [torch.full_like(x["Q"], float("nan")) for _ in range(4)]
+        for ps in (fbd.ATTN_ROW_PASS, fbd.ATTN_COL_PASS):
+            fbd.attn_bwd_passes(x["Q"], x["K"], x["V"], O, x["dO"], lse, ps, gproj=gp, dQ=b[0], dK=b[1], dV=b[2],
+                                workspace=ws, desc=desc)
+        for ps in (fbd.ATTN_ROW_PASS, fbd.ATTN_COL_PASS):
+            fbd.attn_bob_passes(x["Q"], x["K"], x["V"], O, x["dO"], lse, x["gdQ"], x["gdK"], x["gdV"], ps,
+                                gQ=g[0], gK=g[1], gV=g[2], gdO=g[3], workspace=ws, desc=desc, gproj=gp)
+        fbd.attn_device_status()
+        for a, r in zip(b + g, list(ref_b) + list(ref_g)):
+            assert torch.equal(a, r)
