@@ -53,7 +53,7 @@ def executed_flops(w, kn):
         return None
     pad = 64 if w.d <= 64 else 128
     table = EXECUTED_CONTRACTIONS if pad == 64 else EXECUTED_CONTRACTIONS_D128
-    return 2 * table[kn] * w.B * w.H * w.N * w.N * pad / (2.0 if CAUSAL else 1.0)
+    return 2 * table[kn] * w.B * w.H * pairs(w.N) * pad
 
 
 def dist_init(world, backend="nccl"):
@@ -90,15 +90,24 @@ def job_tflops(flops_per_rank_step, world, ms_max):
 # Causal attention by default; --causal 0 measures the same step with every key
 # visible (its flop counts are not halved).
 CAUSAL = True
+WINDOW = 0  # causal sliding window (key j visible to query i iff i - W < j <= i); 0: none
+
+
+def pairs(N):
+    """(query, key) pairs of one slice the dense definition counts: N^2 / 2 under the
+    causal mask (N^2 without it); with a window W < N, the visible pairs N W - W (W - 1) / 2."""
+    if CAUSAL and 0 < WINDOW < N:
+        return N * WINDOW - WINDOW * (WINDOW - 1) / 2.0
+    return N * N / (2.0 if CAUSAL else 1.0)
 
 
 def dense_flops(w, op):
-    unit = w.B * w.H * w.N * w.N * w.d / (2.0 if CAUSAL else 1.0)
+    unit = w.B * w.H * pairs(w.N) * w.d
     return {"fwd": 4, "bwd": 10, "bob": 24}[op] * unit
 
 
 def kernel_flops(w, kn, table):
-    return 2 * table[kn] * w.B * w.H * w.N * w.N * w.d / (2.0 if CAUSAL else 1.0)
+    return 2 * table[kn] * w.B * w.H * pairs(w.N) * w.d
 
 
 def traffic_for(kernel, w):
@@ -196,7 +205,7 @@ def run_ours(args, w, rank, world):
     stream = torch.cuda.Stream(device=dev)
     pinned, x = make_inputs(w, dev)
     torch.cuda.synchronize()
-    desc = fbd.make_desc(x["Q"], w.scale, int(CAUSAL), x["K"])
+    desc = fbd.make_desc(x["Q"], w.scale, int(CAUSAL), x["K"], WINDOW)
     bf = torch.bfloat16
     shp = x["Q"].shape
     # Outputs with the shape of their input: dK, dV, gK, gV follow K (H / group heads).
@@ -357,9 +366,10 @@ def cpu_baseline(w, budget_s=20.0):
     t0 = time.perf_counter()
     reps = 0
     while True:
-        oracle.forward(x["Q"], x["K"], x["V"], scale=w.scale, causal=CAUSAL)
-        oracle.backward(x["Q"], x["K"], x["V"], x["dO"], scale=w.scale, causal=CAUSAL)
-        oracle.bob(x["Q"], x["K"], x["V"], x["dO"], x["gdQ"], x["gdK"], x["gdV"], scale=w.scale, causal=CAUSAL)
+        mask = oracle.Window(WINDOW) if (CAUSAL and WINDOW) else CAUSAL
+        oracle.forward(x["Q"], x["K"], x["V"], scale=w.scale, causal=mask)
+        oracle.backward(x["Q"], x["K"], x["V"], x["dO"], scale=w.scale, causal=mask)
+        oracle.bob(x["Q"], x["K"], x["V"], x["dO"], x["gdQ"], x["gdK"], x["gdV"], scale=w.scale, causal=mask)
         reps += 1
         if time.perf_counter() - t0 > budget_s or reps >= 50:
             break
@@ -534,6 +544,8 @@ def main():
     ap.add_argument("--gproj", type=int, default=0)
     ap.add_argument("--causal", type=int, default=1, choices=[0, 1],
                     help="1: causal attention (the headline workload); 0: every key visible")
+    ap.add_argument("--window", type=int, default=0,
+                    help="causal sliding window W (key j visible to query i iff i - W < j <= i); 0: none")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--max-n", action="store_true", help="report the largest N that fits in HBM instead")
     ap.add_argument("--sweep", action="store_true",
@@ -546,14 +558,17 @@ def main():
         (max_n if args.max_n else sweep)(args)
         return
     args.warmup = max(args.warmup, 3)
-    global CAUSAL
+    global CAUSAL, WINDOW
     CAUSAL = bool(args.causal)
+    WINDOW = args.window if CAUSAL else 0
     w = W.Workload(f"gpt2small_B{args.batch}H{args.heads}N{args.n_seq}d{args.head_dim}"
-                   + ("" if CAUSAL else "_noncausal") + (f"_g{args.group}" if args.group > 1 else ""),
+                   + ("" if CAUSAL else "_noncausal") + (f"_g{args.group}" if args.group > 1 else "")
+                   + (f"_w{WINDOW}" if WINDOW else ""),
                    args.batch, args.heads, args.n_seq, args.head_dim, "bf16", group=args.group)
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     config = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": CAUSAL, "group": w.group,
+              "window": WINDOW,
               "ops": "fwd + bwd(gproj=%d) + BoB(gproj=%d)" % (args.gproj, args.gproj),
               "l2": "inputs larger than L2 (7 input tensors, %.0f MB in total)"
                     % (w.rows * w.d * 2 * (3 + 4 / w.group) / 1e6),
@@ -573,7 +588,7 @@ def main():
         flops = sum(dense_flops(w, op) for op in ("fwd", "bwd", "bob"))
         print(json.dumps({"impl": "reference",
                           "metric": "fwd+bwd+BoB attention TFLOP/s (dense definition%s)"
-                          % (", causal-halved" if CAUSAL else ""),
+                          % ((", visible pairs of the window" if WINDOW else ", causal-halved") if CAUSAL else ""),
                           "value": v, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
                           "warmup": args.warmup, "ms_per_step": flops / (v * 1e12) * 1e3,
                           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -596,7 +611,7 @@ def main():
         return flops / (ms * 1e-3) / 1e12
 
     line = {
-        "metric": "fwd+bwd+BoB attention TFLOP/s (dense definition%s)" % (", causal-halved" if CAUSAL else ""),
+        "metric": "fwd+bwd+BoB attention TFLOP/s (dense definition%s)" % ((", visible pairs of the window" if WINDOW else ", causal-halved") if CAUSAL else ""),
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": r["ms_max"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic", "config": config,
