@@ -126,11 +126,11 @@ def traffic_for(kernel, w):
 # the bench command; see profiles/), keyed by (kernel, workload), with the source
 # hash of the kernel file the counters were taken on.
 MEASURED_TRAFFIC = {
-    ("fwd", "gpt2small_B4H12N8192d64"): {"bytes": 185316608, "source": "tc_fwd.cu", "sha": "316a1b3f69c940c5"},
-    ("bwd_row", "gpt2small_B4H12N8192d64"): {"bytes": 293595136, "source": "tc_bwd_wide.cu", "sha": "bad96f59c9420ca6"},
-    ("bwd_col", "gpt2small_B4H12N8192d64"): {"bytes": 276578816, "source": "tc_bwd_wide.cu", "sha": "bad96f59c9420ca6"},
-    ("bob_row", "gpt2small_B4H12N8192d64"): {"bytes": 502659840, "source": "tc_bob.cu", "sha": "588d8906743f3253"},
-    ("bob_col", "gpt2small_B4H12N8192d64"): {"bytes": 438088448, "source": "tc_bob.cu", "sha": "588d8906743f3253"},
+    ("fwd", "gpt2small_B4H12N8192d64"): {"bytes": 184821504, "source": "tc_fwd.cu", "sha": "9dfeebe0db5d4d08"},
+    ("bwd_row", "gpt2small_B4H12N8192d64"): {"bytes": 293671424, "source": "tc_bwd_wide.cu", "sha": "d42757ea38eeed42"},
+    ("bwd_col", "gpt2small_B4H12N8192d64"): {"bytes": 276380672, "source": "tc_bwd_wide.cu", "sha": "d42757ea38eeed42"},
+    ("bob_row", "gpt2small_B4H12N8192d64"): {"bytes": 502399488, "source": "tc_bob.cu", "sha": "0ff6073741142524"},
+    ("bob_col", "gpt2small_B4H12N8192d64"): {"bytes": 438908928, "source": "tc_bob.cu", "sha": "0ff6073741142524"},
 }
 
 
