@@ -378,7 +378,44 @@ def cpu_baseline(w, budget_s=20.0):
     cores = len(os.sched_getaffinity(0))
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "sample": f"fwd+bwd+BoB of one (b,h) slice at N={N}, d={w.d}, fp64 NumPy, {reps} reps, "
-                      f"{dt:.2f} s each"}
+                      f"{dt:.2f} s each",
+            "single_core": oracle_one_core(w, min(N, 1024))}
+
+
+def oracle_one_core(w, N, budget_s=8.0):
+    """The same oracle sample on one host core: a child process pinned to one CPU with
+    every BLAS thread pool set to one thread before NumPy loads."""
+    import subprocess
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    mask = f"oracle.Window({WINDOW})" if (CAUSAL and WINDOW) else repr(CAUSAL)
+    code = f'''
+import os, sys, time, json
+os.sched_setaffinity(0, {{min(os.sched_getaffinity(0))}})
+sys.path.insert(0, {ROOT!r})
+import numpy as np, oracle, workloads as W
+ws = W.Workload("one_core", 1, 1, {N}, {w.d}, "{w.dtype}")
+x = {{k: v[0, 0].astype(np.float64) for k, v in W.inputs(ws).items()}}
+mask = {mask}
+t0, reps = time.perf_counter(), 0
+while True:
+    oracle.forward(x["Q"], x["K"], x["V"], scale={w.scale!r}, causal=mask)
+    oracle.backward(x["Q"], x["K"], x["V"], x["dO"], scale={w.scale!r}, causal=mask)
+    oracle.bob(x["Q"], x["K"], x["V"], x["dO"], x["gdQ"], x["gdK"], x["gdV"], scale={w.scale!r}, causal=mask)
+    reps += 1
+    if time.perf_counter() - t0 > {budget_s} or reps >= 20:
+        break
+print(json.dumps({{"dt": (time.perf_counter() - t0) / reps, "reps": reps}}))
+'''
+    try:
+        r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=120)
+        out = json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception as e:  # reported, not fatal: the multi-core figure above stands
+        return {"error": f"{type(e).__name__}: {e}"[:200]}
+    ws = W.Workload("one_core", 1, 1, N, w.d, w.dtype)
+    flops = sum(dense_flops(ws, op) for op in ("fwd", "bwd", "bob"))
+    return {"value": flops / out["dt"] / 1e12, "unit": "TFLOP/s", "cores": 1,
+            "sample": f"fwd+bwd+BoB of one (b,h) slice at N={N}, d={w.d}, {out['reps']} reps, "
+                      f"{out['dt']:.2f} s each, one CPU, one BLAS thread"}
 
 
 def max_n(args):
