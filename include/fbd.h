@@ -1,7 +1,7 @@
 /*
- * fbd.h -- C ABI of libfbd: exact softmax attention (causal or not) on GB300
- * (sm_103a): forward, recompute backward (optional GProj), and
- * backward-over-backward.
+ * fbd.h -- C ABI of libfbd: exact softmax attention (causal, causal with a sliding
+ * window, or full) on GB300 (sm_103a): forward, recompute backward (optional
+ * GProj), and backward-over-backward (optional GProj).
  *
  * The N x N score matrix is never written to device memory.  All entry points
  * take plain device pointers owned by the caller; the library allocates and
@@ -30,9 +30,10 @@
  *               (inputs and outputs alike): ATTN_F32 = float, ATTN_BF16 =
  *               bfloat16.  Arithmetic is float32 throughout (bf16 tensor-core
  *               products accumulate in float32).
- *   Supported:  causal in {0, 1}; any group dividing H; d in {32, 64, 96, 128,
- *               256}; dtype in {ATTN_F32, ATTN_BF16}.  Anything else returns
- *               ATTN_ERR_UNSUPPORTED before any launch.
+ *   Supported:  causal in {0, 1}; window >= 0 (> 0 only with causal = 1); any
+ *               group dividing H; d in {32, 64, 96, 128, 256}; dtype in
+ *               {ATTN_F32, ATTN_BF16}.  Anything else returns ATTN_ERR_UNSUPPORTED
+ *               (or ATTN_ERR_INVALID_ARG) before any launch.
  *   Kernels:    the shape decides, never a failure: bf16 attn_fwd, attn_bwd and
  *               attn_bob at d in {32, 64, 96, 128} run on the tcgen05/TMA
  *               tensor-core kernels (d = 32 and 96 on those of d = 64 and 128, the
@@ -56,6 +57,13 @@
  *               synchronised.  Each output element is written exactly once.
  *   Ragged N:   any N >= 1 is accepted; tiles past N are zero-filled on load and
  *               never stored.
+ *   Sliding window ([BoB] "When FlashBoB changes the engineering plan" lists
+ *               flexible masks among the next extensions; the reading here is the
+ *               banded causal mask): with W = desc->window > 0, query i sees the
+ *               keys i - W < j <= i, and every operation (forward, backward with or
+ *               without GProj, BoB) is that of attention under this mask; row
+ *               blocks skip the key blocks wholly outside every row's window and
+ *               column blocks the query blocks that see none of their keys.
  *   Grouped key/value heads ([BoB] "When FlashBoB changes the engineering plan"
  *               lists shared keys and values among the next extensions; the reading
  *               here is the usual grouped-query one): with g = desc->group > 1 the tensors on the key
