@@ -241,6 +241,21 @@ def test_large_key_projected_rows_sum_to_zero():
     assert np.all(np.triu(dS[0, 0], 1) == 0)
 
 
+def test_projected_dS_with_window():
+    """The diagnostic under a sliding window: keys outside i - W < j <= i are 0 and the
+    projected rows still sum to zero."""
+    import fwd_bwd_double_gb300 as fbd
+    w = W.Workload("projected_window_B1H2N300d64", 1, 2, 300, 64, "bf16")
+    xd = to_device(inputs(w), w)
+    O, lse = fbd.attn_fwd(xd["Q"], xd["K"], xd["V"], window=40)
+    dS = host(fbd.attn_bwd_projected_dS(xd["Q"], xd["K"], xd["V"], O, xd["dO"], lse, window=40))
+    i, j = np.meshgrid(np.arange(300), np.arange(300), indexing="ij")
+    assert np.all(dS[:, :, (j > i) | (j <= i - 40)] == 0)
+    l1 = np.abs(dS).sum(axis=-1)
+    keep = l1 > 0
+    assert float(np.max(np.abs(dS.sum(axis=-1))[keep] / l1[keep])) <= 1e-6
+
+
 EDGE_N = [1, 2, 15, 17, 127, 128, 129, 255, 300]
 
 
@@ -276,13 +291,14 @@ def test_other_head_dims_grouped_bf16(d, gproj):
     check_full(w, got, ("bwd", "bob"))
 
 
-def test_outputs_written_once_and_nothing_outside():
+@pytest.mark.parametrize("d,win", [(64, 0), (64, 70), (128, 0), (128, 70)])
+def test_outputs_written_once_and_nothing_outside(d, win):
     """Outputs live inside NaN-filled guard buffers: every output element is written
-    (no NaN left) and no guard element is touched."""
+    (no NaN left) and no guard element is touched (with and without a window)."""
     import torch
 
     import fwd_bwd_double_gb300 as fbd
-    w = W.Workload("guard_B1H3N200d64", 1, 3, 200, 64, "bf16")
+    w = W.Workload(f"guard_B1H3N200d{d}", 1, 3, 200, d, "bf16")
     xd = to_device(inputs(w), w)
     n = xd["Q"].numel()
     pad = 4096
@@ -298,11 +314,11 @@ def test_outputs_written_once_and_nothing_outside():
     bufs = {k: guarded() for k in ("O", "dQ", "dK", "dV", "gQ", "gK", "gV", "gdO")}
     lb, lse = lse_guarded()
     O = bufs["O"][1]
-    fbd.attn_fwd(xd["Q"], xd["K"], xd["V"], O=O, lse=lse)
+    fbd.attn_fwd(xd["Q"], xd["K"], xd["V"], O=O, lse=lse, window=win)
     fbd.attn_bwd(xd["Q"], xd["K"], xd["V"], O, xd["dO"], lse, gproj=1, dQ=bufs["dQ"][1], dK=bufs["dK"][1],
-                 dV=bufs["dV"][1])
+                 dV=bufs["dV"][1], window=win)
     fbd.attn_bob(xd["Q"], xd["K"], xd["V"], O, xd["dO"], lse, xd["gdQ"], xd["gdK"], xd["gdV"], gQ=bufs["gQ"][1],
-                 gK=bufs["gK"][1], gV=bufs["gV"][1], gdO=bufs["gdO"][1])
+                 gK=bufs["gK"][1], gV=bufs["gV"][1], gdO=bufs["gdO"][1], window=win, gproj=1)
     fbd.attn_device_status()
     for k, (buf, view) in list(bufs.items()) + [("lse", (lb, lse))]:
         b = buf.float().cpu().numpy()
