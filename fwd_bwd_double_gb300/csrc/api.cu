@@ -111,10 +111,11 @@ namespace fbd {
 // zero-padded to 64 and 128 in shared memory (TMA fills the columns past d with
 // zeros, which add nothing to any product; nothing past d is stored).  BoB at
 // d > 64 splits each block over two CTAs by output half: its row pass's four d-wide
-// accumulators would otherwise fill the 512 TMEM columns.  d = 256 runs on the
-// CUDA-core kernels (simt.cu).
+// accumulators would otherwise fill the 512 TMEM columns.  At d = 256 the forward
+// runs on tensor cores (64-key blocks, O in 256 TMEM columns); the backward and BoB
+// run on the CUDA-core kernels (simt.cu): their d-wide accumulators do not fit TMEM.
 bool tc_supports(int op, int64_t d) {
-  (void)op;
+  if (d == 256) return op == 0;
   return d == 32 || d == 64 || d == 96 || d == 128;
 }
 }  // namespace fbd

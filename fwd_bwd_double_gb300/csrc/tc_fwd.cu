@@ -43,13 +43,15 @@ namespace {
 __device__ unsigned int g_err = 0;
 
 constexpr int BM = 128;
-constexpr int BN = 128;
-constexpr int NS = 3;  // K/V stages (2 CTAs per SM at d = 64 still fit)
 constexpr int kThreads = 192;
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
 struct Layout {
+  // Key blocks of BN keys through an NS-stage ring: 128 keys, 3 stages up to d = 128
+  // (2 CTAs per SM at d = 64 still fit); 64 keys, 2 stages at d = 256 (Q alone is 64 KB).
+  static constexpr int BN = D <= 128 ? 128 : 64;
+  static constexpr int NS = D <= 128 ? 3 : 2;
   static constexpr int kQ = BM * D * 2;   // bytes of the Q tile
   static constexpr int kKV = BN * D * 2;  // bytes of one K (or V) tile
   static constexpr int oQ = 0;
@@ -57,8 +59,8 @@ struct Layout {
   static constexpr int oV = oK + NS * kKV;
   static constexpr int oBar = oV + NS * kKV;
   static constexpr int bytes = oBar + 128;
-  // TMEM columns: S fp32 [0, 128), P bf16 pairs [128, 192), O fp32 [192, 192 + D).
-  static constexpr int kTmemCols = (192 + D <= 256) ? 256 : 512;
+  // TMEM columns: S fp32 [0, BN), P bf16 pairs [BN, BN + BN/2), O fp32 after them (D).
+  static constexpr int kTmemCols = (BN + BN / 2 + D <= 256) ? 256 : 512;
 };
 
 // Shared-memory descriptor of a K-major operand tile stored as 64-element
@@ -81,6 +83,7 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
                const float* __restrict__ lse_in, float* __restrict__ pb, int N, int nrb, int BH, float scale,
                float scale_log2, int causal, int win, int G, int dv) {
   using Lay = Layout<D>;
+  constexpr int BN = Lay::BN, NS = Lay::NS;
   extern __shared__ __align__(1024) uint8_t sm[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Lay::oBar);
   uint64_t* q_full = bars + 0;
@@ -102,7 +105,7 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
   // Key blocks this row block sees: j0 + j for j < nkv.  win: the causal window (key k
   // visible to row i iff i - win < k <= i; larger than N when there is none).
   const int j0 = (WIN && causal) ? max(0, rb * BM - win + 1) / BN : 0;
-  const int nkv = (causal ? rb + 1 : nrb) - j0;
+  const int nkv = (BN == BM ? (causal ? rb + 1 : nrb) : (causal ? ((rb + 1) * BM + BN - 1) / BN : (N + BN - 1) / BN)) - j0;
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(q_full, 1);
@@ -204,19 +207,19 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
       ptx::tc_fence_after();
       const int kb = j0 + j;
       // Keys of this block past the row (causal), or past N, or below the row's window.
-      const bool diag = causal ? (kb == rb) : (j == nkv - 1 && (N % BN) != 0);
+      const bool diag = causal ? (BN == BM ? kb == rb : kb * BN + BN - 1 > rb * BM) : (j == nkv - 1 && (N % BN) != 0);
       const bool low = WIN && causal && kb * BN < rb * BM + BM - win;
-      const int klim = causal ? (WIN ? rb * BM + r - kb * BN : r) : N - 1 - kb * BN;
+      const int klim = causal ? ((WIN || BN != BM) ? rb * BM + r - kb * BN : r) : N - 1 - kb * BN;
       const int klo = (WIN && causal) ? rb * BM + r - win + 1 - kb * BN : 0;
-      uint32_t v[4][32];
+      uint32_t v[BN / 32][32];
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) ptx::tmem_ld32(tS + lane_off + ch * 32, v[ch]);
+      for (int ch = 0; ch < BN / 32; ++ch) ptx::tmem_ld32(tS + lane_off + ch * 32, v[ch]);
       ptx::tmem_wait_ld();
       ptx::tc_fence_before();
       ptx::mbar_arrive(s_consumed);
-      uint32_t pk[4][16];
+      uint32_t pk[BN / 32][16];
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
+      for (int ch = 0; ch < BN / 32; ++ch) {
 #pragma unroll
         for (int t = 0; t < 32; t += 2) {
           const float2 arg = tc::unpk2(tc::fma2(tc::pk2(v[ch][t], v[ch][t + 1]), c2, nL2));
@@ -231,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
       if (j > 0) wait(pv_done, (j - 1) & 1);
       ptx::tc_fence_after();
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) ptx::tmem_st16(tP + lane_off + ch * 16, pk[ch]);
+      for (int ch = 0; ch < BN / 32; ++ch) ptx::tmem_st16(tP + lane_off + ch * 16, pk[ch]);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(p_ready);
@@ -264,20 +267,20 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
       // blocks keys below a row's window.  Otherwise only the last block can hold keys
       // past N (TMA reads them as zeros).
       const int kb = j0 + j;
-      const bool diag = causal ? (kb == rb) : (j == nkv - 1 && (N % BN) != 0);
+      const bool diag = causal ? (BN == BM ? kb == rb : kb * BN + BN - 1 > rb * BM) : (j == nkv - 1 && (N % BN) != 0);
       const bool low = WIN && causal && kb * BN < rb * BM + BM - win;
-      const int klim = causal ? (WIN ? rb * BM + r - kb * BN : r) : N - 1 - kb * BN;  // last visible key, relative
+      const int klim = causal ? ((WIN || BN != BM) ? rb * BM + r - kb * BN : r) : N - 1 - kb * BN;  // last visible
       const int klo = (WIN && causal) ? rb * BM + r - win + 1 - kb * BN : 0;        // first visible key, relative
-      // The whole 128-column S row in registers: four loads, one wait.
-      uint32_t v[4][32];
+      // The whole BN-column S row in registers: BN / 32 loads, one wait.
+      uint32_t v[BN / 32][32];
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) ptx::tmem_ld32(tS + lane_off + ch * 32, v[ch]);
+      for (int ch = 0; ch < BN / 32; ++ch) ptx::tmem_ld32(tS + lane_off + ch * 32, v[ch]);
       ptx::tmem_wait_ld();
       ptx::tc_fence_before();
       ptx::mbar_arrive(s_consumed);  // the MMA warp may now compute S_{j+1} into these columns
       if (diag || low) {
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch)
+        for (int ch = 0; ch < BN / 32; ++ch)
 #pragma unroll
           for (int t = 0; t < 32; ++t)
             if (ch * 32 + t > klim || ch * 32 + t < klo) v[ch][t] = __float_as_uint(-INFINITY);
@@ -287,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
 #pragma unroll
       for (int u = 0; u < 8; ++u) mx8[u] = -INFINITY;
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch)
+      for (int ch = 0; ch < BN / 32; ++ch)
 #pragma unroll
         for (int t = 0; t < 32; ++t) mx8[t & 7] = fmaxf(mx8[t & 7], __uint_as_float(v[ch][t]));
 #pragma unroll
@@ -303,9 +306,9 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
       const float msub = (WIN && m == -INFINITY) ? 0.f : m;
       const uint64_t nm2 = tc::pk2f(-msub, -msub), c2 = tc::pk2f(scale_log2, scale_log2);
       uint64_t rs4[4] = {0, 0, 0, 0};
-      uint32_t pk[4][16];  // P_j as bf16 pairs, written once P_{j-1} V_{j-1} is done
+      uint32_t pk[BN / 32][16];  // P_j as bf16 pairs, written once P_{j-1} V_{j-1} is done
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
+      for (int ch = 0; ch < BN / 32; ++ch) {
 #pragma unroll
         for (int t = 0; t < 32; t += 2) {
           const float2 arg = tc::unpk2(tc::mul2(tc::add2(tc::pk2(v[ch][t], v[ch][t + 1]), nm2), c2));
@@ -318,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
       if (j > 0) wait(pv_done, (j - 1) & 1);  // P_{j-1} V_{j-1} has read the P columns and updated O
       ptx::tc_fence_after();
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) ptx::tmem_st16(tP + lane_off + ch * 16, pk[ch]);  // keys ch*32 .. ch*32+31
+      for (int ch = 0; ch < BN / 32; ++ch) ptx::tmem_st16(tP + lane_off + ch * 16, pk[ch]);  // keys ch*32 .. ch*32+31
       const float2 rsa = tc::unpk2(tc::add2(tc::add2(rs4[0], rs4[1]), tc::add2(rs4[2], rs4[3])));
       const float rs = rsa.x + rsa.y;
       if (__any_sync(0xffffffffu, moved)) {  // rescale O for rows whose max moved
@@ -373,6 +376,7 @@ cudaError_t launch(const Problem& p, const void* Q, const void* K, const void* V
   alignas(64) CUtensorMap mq, mk, mv;
   // Tensor maps over the true head dim p.d (<= D): TMA zero-fills columns p.d .. D-1,
   // which add nothing to any product.
+  constexpr int BN = Layout<D>::BN;
   if (!make_tmap_bf16(&mq, Q, p.N, p.d, p.BH, BM) || !make_tmap_bf16(&mk, K, p.N, p.d, p.BHkv, BN) ||
       !make_tmap_bf16(&mv, V, p.N, p.d, p.BHkv, BN))
     return cudaErrorInvalidValue;
@@ -393,8 +397,10 @@ cudaError_t launch(const Problem& p, const void* Q, const void* K, const void* V
 cudaError_t tc_fwd(const Problem& p, const void* Q, const void* K, const void* V, void* O, float* lse,
                    cudaStream_t st) {
   // d = 32 runs the d = 64 kernel and d = 96 the d = 128 one, zero-padded in shared memory.
-  return p.d <= 64 ? launch<64, false>(p, Q, K, V, O, lse, nullptr, nullptr, st)
-                   : launch<128, false>(p, Q, K, V, O, lse, nullptr, nullptr, st);
+  // d = 256: 64-key blocks (the Q tile alone takes 64 KB of shared memory).
+  return p.d <= 64    ? launch<64, false>(p, Q, K, V, O, lse, nullptr, nullptr, st)
+         : p.d <= 128 ? launch<128, false>(p, Q, K, V, O, lse, nullptr, nullptr, st)
+                      : launch<256, false>(p, Q, K, V, O, lse, nullptr, nullptr, st);
 }
 
 cudaError_t tc_bob_pb(const Problem& p, const void* Q, const void* K, const void* b, const float* lse, float* pb,

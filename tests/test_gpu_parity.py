@@ -630,3 +630,19 @@ def test_window_passes_compose_on_nan_workspace(d):
         fbd.attn_device_status()
         for a, r in zip(b + g, list(ref_b) + list(ref_g)):
             assert torch.equal(a, r)
+
+
+# The forward at d = 256 runs on tensor cores with 64-key blocks (the backward and BoB
+# at d = 256 on the CUDA-core kernels): several row blocks, the two-block diagonal of a
+# 128-row block, ragged tails, causal and not, a window.
+@pytest.mark.parametrize("N,causal,win", [(1000, True, 0), (2500, True, 0), (1000, False, 0), (1000, True, 200)])
+def test_forward_head_dim_256_bf16(N, causal, win):
+    import fwd_bwd_double_gb300 as fbd
+    w = W.Workload(f"fwd256_B1H3N{N}d256_bf16", 1, 3, N, 256, "bf16")
+    xd = to_device(inputs(w), w)
+    O, lse = fbd.attn_fwd(xd["Q"], xd["K"], xd["V"], causal=causal, window=win)
+    fbd.attn_device_status()
+    mask = oracle.Window(win) if win else causal
+    x = inputs(w)
+    ref = oracle.forward_all(x["Q"], x["K"], x["V"], causal=mask)
+    assert rel_fro(host(O), ref["O"]) <= TOL["bf16"] and rel_fro(host(lse), ref["L"]) <= 1e-5
