@@ -67,9 +67,9 @@ def test_long_sweep_n4096_all_heads():
     print(w.name, {k: f"{v:.2e}" for k, v in errs.items()})
 
 
-def sampled_check(w, got, ops, heads, rows, cols, batch=0):
+def sampled_check(w, got, ops, heads, rows, cols, batch=0, causal=True):
     """Oracle on sampled rows (row outputs) and columns (column outputs) of given heads
-    of one batch entry."""
+    of one batch entry (causal: True, False or an oracle.Window)."""
     tol = TOL[w.dtype]
     errs = {}
     x = W.inputs(w, heads=heads, batches=[batch])
@@ -77,21 +77,21 @@ def sampled_check(w, got, ops, heads, rows, cols, batch=0):
     b = batch
     for hi, h in enumerate(heads):
         s = {k: v[0, hi].astype(np.float64) for k, v in x.items()}
-        O, L = oracle.forward_rows(s["Q"], s["K"], s["V"], rows, scale=w.scale)
+        O, L = oracle.forward_rows(s["Q"], s["K"], s["V"], rows, scale=w.scale, causal=causal)
         acc["O"][0].append(host(got["O"][b, h])[rows]); acc["O"][1].append(O)
         acc["L"][0].append(host(got["L"][b, h])[rows]); acc["L"][1].append(L)
         if "bwd" in ops:
             acc["dQ"][0].append(host(got["dQ"][b, h])[rows])
-            acc["dQ"][1].append(oracle.backward_rows(s["Q"], s["K"], s["V"], s["dO"], rows, scale=w.scale))
-            dK, dV = oracle.backward_cols(s["Q"], s["K"], s["V"], s["dO"], cols, scale=w.scale)
+            acc["dQ"][1].append(oracle.backward_rows(s["Q"], s["K"], s["V"], s["dO"], rows, scale=w.scale, causal=causal))
+            dK, dV = oracle.backward_cols(s["Q"], s["K"], s["V"], s["dO"], cols, scale=w.scale, causal=causal)
             acc["dK"][0].append(host(got["dK"][b, h])[cols]); acc["dK"][1].append(dK)
             acc["dV"][0].append(host(got["dV"][b, h])[cols]); acc["dV"][1].append(dV)
         if "bob" in ops:
-            r = oracle.bob_rows(s["Q"], s["K"], s["V"], s["dO"], s["gdQ"], s["gdK"], s["gdV"], rows, scale=w.scale)
+            r = oracle.bob_rows(s["Q"], s["K"], s["V"], s["dO"], s["gdQ"], s["gdK"], s["gdV"], rows, scale=w.scale, causal=causal)
             acc["gQ"][0].append(host(got["gQ"][b, h])[rows]); acc["gQ"][1].append(r["gQ"])
             acc["gdO"][0].append(host(got["gdO"][b, h])[rows]); acc["gdO"][1].append(r["gdO"])
             gK, gV = oracle.bob_cols(s["Q"], s["K"], s["V"], s["dO"], s["gdQ"], s["gdK"], s["gdV"], cols,
-                                     scale=w.scale)
+                                     scale=w.scale, causal=causal)
             acc["gK"][0].append(host(got["gK"][b, h])[cols]); acc["gK"][1].append(gK)
             acc["gV"][0].append(host(got["gV"][b, h])[cols]); acc["gV"][1].append(gV)
     for k, (g, r) in acc.items():
@@ -646,3 +646,14 @@ def test_forward_head_dim_256_bf16(N, causal, win):
     x = inputs(w)
     ref = oracle.forward_all(x["Q"], x["K"], x["V"], causal=mask)
     assert rel_fro(host(O), ref["O"]) <= TOL["bf16"] and rel_fro(host(lse), ref["L"]) <= 1e-5
+
+
+@pytest.mark.parametrize("win", [1024, 4000])
+def test_window_long_sampled(win):
+    """A window at the bench's sequence length (B1 H2 N8192 d64 bf16), sampled rows and
+    late columns of every output against the oracle under the same window."""
+    w = W.Workload(f"window_long_B1H2N8192d64_bf16", 1, 2, 8192, 64, "bf16")
+    got = run_ops(w, to_device(W.inputs(w), w), ops=("bwd", "bob"), window=win)
+    rows, cols = sample_rows_cols(w.N, np.random.default_rng(win))
+    errs = sampled_check(w, got, ("bwd", "bob"), heads=[0, 1], rows=rows, cols=cols, causal=oracle.Window(win))
+    print(w.name, win, {k: f"{v:.2e}" for k, v in errs.items()})
