@@ -783,3 +783,19 @@ def test_window_sampling_agrees():
     assert rel(r["gQ"], ref["gQ"][rows]) <= 1e-13 and rel(r["gdO"], ref["gdO"][rows]) <= 1e-13
     gK, gV = oracle.bob_cols(Q, K, V, dO, a, b, c, cols, causal=w)
     assert rel(gK, ref["gK"][cols]) <= 1e-13 and rel(gV, ref["gV"][cols]) <= 1e-13
+
+
+def test_window_bob_gproj_projection():
+    """GProj inside BoB under a sliding window: the projected rows (over each row's
+    visible keys) sum to zero, and a common shift of b leaves the projected gQ alone."""
+    N, d = 80, 8
+    Q, K, V, dO, a, b, c = slice_set(N, d, 111)
+    w = oracle.Window(13)
+    proj = oracle.bob_bf16_dS(Q, K, V, dO, a, b + 7.0, c, True, causal=w)
+    assert proj["dS_rowsum_rel"] <= 1e-13
+    v = rnd(112, d) * 3
+    proj_v = oracle.bob_bf16_dS(Q, K, V, dO, a, b + 7.0 + v[None, :], c, True, causal=w)
+    assert rel(proj_v["gQ"], proj["gQ"]) <= 1e-11
+    exact = oracle.bob(Q, K, V, dO, a, b + 7.0, c, causal=w)
+    plain = oracle.bob_bf16_dS(Q, K, V, dO, a, b + 7.0, c, False, causal=w)
+    assert rel(proj["gQ"], exact["gQ"]) < rel(plain["gQ"], exact["gQ"])
