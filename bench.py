@@ -382,6 +382,25 @@ def cpu_baseline(w, budget_s=20.0):
             "single_core": oracle_one_core(w, min(N, 1024))}
 
 
+def oracle_sample_step(w):
+    """The reference arm's step: the oracle's forward, backward and BoB on one (b, h)
+    slice of the workload at N = min(N, 2048).  Returns (step, its dense-definition
+    flops, a description of the sample)."""
+    import oracle
+    N = min(w.N, 2048)
+    ws = W.Workload(w.name + "@cpu_sample", 1, 1, N, w.d, w.dtype)
+    x = {k: v[0, 0].astype(np.float64) for k, v in W.inputs(ws).items()}
+    mask = oracle.Window(WINDOW) if (CAUSAL and WINDOW) else CAUSAL
+
+    def step():
+        oracle.forward(x["Q"], x["K"], x["V"], scale=w.scale, causal=mask)
+        oracle.backward(x["Q"], x["K"], x["V"], x["dO"], scale=w.scale, causal=mask)
+        oracle.bob(x["Q"], x["K"], x["V"], x["dO"], x["gdQ"], x["gdK"], x["gdV"], scale=w.scale, causal=mask)
+
+    flops = sum(dense_flops(ws, op) for op in ("fwd", "bwd", "bob"))
+    return step, flops, f"fwd+bwd+BoB of one (b,h) slice at N={N}, d={w.d}, fp64 NumPy on the host cores"
+
+
 def oracle_one_core(w, N, budget_s=8.0):
     """The same oracle sample on one host core: a child process pinned to one CPU with
     every BLAS thread pool set to one thread before NumPy loads."""
@@ -418,20 +437,25 @@ print(json.dumps({{"dt": (time.perf_counter() - t0) / reps, "reps": reps}}))
                       f"{out['dt']:.2f} s each, one CPU, one BLAS thread"}
 
 
-def max_n(args):
+def max_n_report(exec_n=1 << 20, check=True):
     """Largest N (multiple of 2^16) whose full buffer set for BoB / backward allocates at
-    B=1, H=12, d=64, bf16; then one timed run of each op at N = 2^20 on device-drawn inputs."""
+    B=1, H=12, d=64, bf16 (allocation-only: the op is not run at that N), next to the
+    linear-memory bound; then one timed run of the forward, backward and BoB at
+    N = exec_n with a sampled parity check of head 0 against the oracle."""
     import torch
 
     import fwd_bwd_double_gb300 as fbd
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
+    torch.cuda.empty_cache()
     H, d = 12, 64
     row = H * d * 2  # bytes of one token of one [B,H,N,d] bf16 tensor
     per_token = {"bob": 12 * row + 4 * H + 16 * H, "bwd": 8 * row + 4 * H + 16 * H}
     ntensor = {"bob": 12, "bwd": 8}
     free, total = torch.cuda.mem_get_info(dev)
-    out = {"metric": "max N in HBM (B=1, H=12, d=64, bf16)", "hbm_total_bytes": total, "hbm_free_bytes": free}
+    out = {"metric": "max N in HBM (B=1, H=12, d=64, bf16)", "hbm_total_bytes": total, "hbm_free_bytes": free,
+           "basis": "allocation-only: the largest N whose whole buffer set (inputs, outputs, lse, workspace) "
+                    "allocates; the ops are executed at executed_n"}
 
     def fits(op, N):
         bufs = []
@@ -448,6 +472,7 @@ def max_n(args):
             torch.cuda.empty_cache()
 
     step = 1 << 16
+    t0 = time.perf_counter()
     for op in ("bob", "bwd"):
         lo, hi = 0, (free // per_token[op]) // step + 2  # in units of step
         while hi - lo > 1:
@@ -460,29 +485,60 @@ def max_n(args):
         bound = free / per_token[op]
         out[op] = {"max_n_alloc": nmax, "bytes_per_token": per_token[op], "linear_bound_tokens": int(bound),
                    "fraction_of_bound": nmax / bound}
-    # one execution per op at N = 2^20 (device-drawn N(0,1) inputs: a timing run, not parity)
-    N = 1 << 20
+    out["bisect_s"] = time.perf_counter() - t0
+    # One execution per op at N = exec_n.  Head 0 comes from the seeded workload (so the
+    # oracle can check it); heads 1..11 are device-drawn N(0,1) values (timing filler).
+    N = exec_n
+    w = W.Workload(f"maxn_B1H12N{N}d64", 1, H, N, d, "bf16")
+    x0 = W.inputs(w, heads=[0])
     g = torch.Generator(device=dev)
     g.manual_seed(0)
-    x = {k: torch.randn((1, H, N, d), generator=g, device=dev).to(torch.bfloat16)
-         for k in ("Q", "K", "V", "dO", "gdQ", "gdK", "gdV")}
+    x = {}
+    for k in W.TENSORS:
+        t = torch.randn((1, H, N, d), generator=g, device=dev).to(torch.bfloat16)
+        t[0, 0] = torch.from_numpy(x0[k][0, 0]).to(dev).to(torch.bfloat16)
+        x[k] = t
     O, lse = fbd.attn_fwd(x["Q"], x["K"], x["V"])
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
     torch.cuda.synchronize()
     ev[0].record()
-    fbd.attn_bwd(x["Q"], x["K"], x["V"], O, x["dO"], lse)
+    dQ, dK, dV = fbd.attn_bwd(x["Q"], x["K"], x["V"], O, x["dO"], lse)
     ev[1].record()
-    fbd.attn_bob(x["Q"], x["K"], x["V"], O, x["dO"], lse, x["gdQ"], x["gdK"], x["gdV"])
+    gQ, gK, gV, gdO = fbd.attn_bob(x["Q"], x["K"], x["V"], O, x["dO"], lse, x["gdQ"], x["gdK"], x["gdV"])
     ev[2].record()
     torch.cuda.synchronize()
     fbd.attn_device_status()
-    w = W.Workload("maxn", 1, H, N, d, "bf16")
+    ex = {"executed_n": N, "peak_hbm_bytes": torch.cuda.max_memory_allocated(dev)}
     for i, op in enumerate(("bwd", "bob")):
         ms = ev[i].elapsed_time(ev[i + 1])
-        out[op]["executed_n"] = N
-        out[op]["executed_ms"] = ms
-        out[op]["executed_tflops_dense"] = dense_flops(w, op) / (ms * 1e-3) / 1e12
-    print(json.dumps(out))
+        ex[op + "_ms"] = ms
+        ex[op + "_tflops_dense"] = dense_flops(w, op) / (ms * 1e-3) / 1e12
+    if check:
+        import oracle
+        rows = np.array([0, 1, 4097, N // 2 + 3, N - 130, N - 2, N - 1])
+        cols = np.arange(N - 48, N)
+        s0 = {k: x0[k][0, 0].astype(np.float64) for k in W.TENSORS}
+        hst = lambda t: t[0, 0].float().cpu().numpy().astype(np.float64)
+        Oo, Lo = oracle.forward_rows(s0["Q"], s0["K"], s0["V"], rows)
+        dQo = oracle.backward_rows(s0["Q"], s0["K"], s0["V"], s0["dO"], rows)
+        dKo, dVo = oracle.backward_cols(s0["Q"], s0["K"], s0["V"], s0["dO"], cols)
+        bo = oracle.bob_rows(s0["Q"], s0["K"], s0["V"], s0["dO"], s0["gdQ"], s0["gdK"], s0["gdV"], rows)
+        gKo, gVo = oracle.bob_cols(s0["Q"], s0["K"], s0["V"], s0["dO"], s0["gdQ"], s0["gdK"], s0["gdV"], cols)
+        relf = lambda a, b: float(np.linalg.norm(a - b) / np.linalg.norm(b))
+        errs = {"O": relf(hst(O)[rows], Oo), "L": relf(lse[0, 0].cpu().numpy()[rows], Lo),
+                "dQ": relf(hst(dQ)[rows], dQo), "dK": relf(hst(dK)[cols], dKo), "dV": relf(hst(dV)[cols], dVo),
+                "gQ": relf(hst(gQ)[rows], bo["gQ"]), "gdO": relf(hst(gdO)[rows], bo["gdO"]),
+                "gK": relf(hst(gK)[cols], gKo), "gV": relf(hst(gV)[cols], gVo)}
+        ex["parity_sampled"] = {"rows": rows.tolist(), "cols": f"{N - 48}..{N - 1}", "head": 0,
+                                "rel_fro": errs, "tol": 2e-2, "ok": all(v <= 2e-2 for v in errs.values())}
+    out["executed"] = ex
+    del x, O, lse, dQ, dK, dV, gQ, gK, gV, gdO
+    torch.cuda.empty_cache()
+    return out
+
+
+def max_n(args):
+    print(json.dumps(max_n_report(args.exec_n)))
 
 
 def sweep(args):
@@ -586,6 +642,10 @@ def main():
                     help="causal sliding window W (key j visible to query i iff i - W < j <= i); 0: none")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--max-n", action="store_true", help="report the largest N that fits in HBM instead")
+    ap.add_argument("--exec-n", type=int, default=1 << 20,
+                    help="with --max-n: the N at which the ops are executed and checked (default 2^20)")
+    ap.add_argument("--no-max-n", action="store_true",
+                    help="leave the max-N report (allocation bisection + one run at N = 2^20) out of the line")
     ap.add_argument("--sweep", action="store_true",
                     help="time the ops on the long sweep, the target shape at B = 1 and 4, the full day and "
                          "the large-key shape instead (one JSON line per config)")
@@ -615,22 +675,31 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        times = []
+        # One reference step = the oracle's fwd + bwd + BoB on a bounded sample of the
+        # workload (one (b, h) slice at N <= 2048); W untimed steps, then K timed ones.
+        step, flops, sample = oracle_sample_step(w)
         for _ in range(args.warmup):
-            pass
-        base = None
+            step()
+        times = []
         for _ in range(args.steps):
-            base = cpu_baseline(w, budget_s=max(2.0, 60.0 / max(args.steps, 1)))
-            times.append(base["value"])
-        v = statistics.mean(times)
-        flops = sum(dense_flops(w, op) for op in ("fwd", "bwd", "bob"))
+            t0 = time.perf_counter()
+            step()
+            times.append(time.perf_counter() - t0)
+        dt = statistics.mean(times)
+        v = flops / dt / 1e12
+        cores = len(os.sched_getaffinity(0))
+        full = sum(dense_flops(w, op) for op in ("fwd", "bwd", "bob"))
         print(json.dumps({"impl": "reference",
                           "metric": "fwd+bwd+BoB attention TFLOP/s (dense definition%s)"
                           % ((", visible pairs of the window" if WINDOW else ", causal-halved") if CAUSAL else ""),
                           "value": v, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
-                          "warmup": args.warmup, "ms_per_step": flops / (v * 1e12) * 1e3,
+                          "warmup": args.warmup, "ms_per_step": dt * 1e3,
+                          "step": "one timed step = the bounded sample below (not the whole workload)",
+                          "ms_per_step_full_workload_extrapolated": full / (v * 1e12) * 1e3,
                           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                          "data": "synthetic", "config": config, "cpu_baseline": base,
+                          "data": "synthetic", "config": config,
+                          "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                                           "sample": sample},
                           "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                                   "d2h_bytes_per_step": 0}}))
         return
@@ -678,6 +747,8 @@ def main():
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
+    if world == 1 and not args.no_max_n:
+        line["max_n"] = max_n_report()
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

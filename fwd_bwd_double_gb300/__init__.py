@@ -154,7 +154,8 @@ def attn_bob_passes(Q, K, V, O, dO, lse, gdQ, gdK, gdV, passes, gQ=None, gK=None
 def attn_bob_static(Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ=None, gK=None, gV=None, gdO=None,
                     scale: float = 0.0, stream=None, desc=None, causal: bool = True, window: int = 0):
     """attn_bob without a workspace argument: the library's static scratch array is used
-    (for callers that cannot allocate device memory; B*H*N <= 1,048,576)."""
+    (for callers that cannot allocate device memory; B*H*Np <= 1,048,576 with Np = N
+    rounded up to an even count)."""
     torch = _torch()
     desc = desc or make_desc(Q, scale, int(causal), K, window)
     gQ = torch.empty_like(Q) if gQ is None else gQ

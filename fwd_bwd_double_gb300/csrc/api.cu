@@ -122,6 +122,10 @@ bool tc_supports(int op, int64_t d) {
 
 namespace fbd {
 attn_status_t set_last_error(attn_status_t s, const char* msg) { return fail(s, "%s", msg); }
+attn_status_t validate_desc(const attn_desc_t* desc) {
+  Problem p;
+  return check_desc(desc, p);
+}
 }  // namespace fbd
 
 extern "C" {

@@ -101,8 +101,8 @@ cudaError_t selftest_wait_timeout(cudaStream_t st);
 // Record `msg` as the calling thread's attn_last_error() detail; returns s.
 attn_status_t set_last_error(attn_status_t s, const char* msg);
 
-// Size of the file-scope scratch array behind attn_bob_static.
-size_t static_bob_scratch_bytes();
+// The descriptor checks every entry point makes (ATTN_OK or the status attn_bob would return).
+attn_status_t validate_desc(const attn_desc_t* desc);
 
 // Tensor maps: 3-D bf16 view (d, N, B*H) of a [B,H,N,d] tensor, box (64, rows, 1),
 // 128-byte swizzle.  Returns false if the driver entry point is missing or the

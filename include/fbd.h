@@ -200,15 +200,24 @@ attn_status_t attn_bob(const attn_desc_t* desc, const void* Q, const void* K, co
  * of their own (for example a plugin inside a host application whose memory
  * manager owns the device, or a deployment with a fixed memory plan that forbids
  * allocation after start-up), so this variant takes no workspace: the row
- * statistics live in a file-scope device array of 16 MiB, enough for
- * B*H*N <= 1,048,576 rows.  Larger problems return ATTN_ERR_WORKSPACE without
- * launching anything (use attn_bob with a caller workspace instead).
+ * statistics live in a file-scope device array of 16 MiB, 1,048,576 rows of 16
+ * bytes, which holds problems with B*H*Np <= 1,048,576, Np = N rounded up to an
+ * even count (the row statistics are stored in row pairs).  Larger problems return
+ * ATTN_ERR_WORKSPACE without launching anything (use attn_bob with a caller
+ * workspace instead).
  *   Arguments, outputs and errors are those of attn_bob with gproj = 0 and no
- *   workspace (this entry point has no GProj form).
+ *   workspace (this entry point has no GProj form); the descriptor is checked
+ *   first, as attn_bob checks it.
  *   The array is held by every GPU that loads the library until process exit.
- *   The first call on each device looks up the array's device address with
- *   cudaGetSymbolAddress (that device must be current) and caches it; make that
- *   first call before any stream capture.  No call allocates or frees memory.
+ *   Under CUDA's lazy module loading (the default) the 16 MiB are committed on a
+ *   device when the array is first looked up there, which the first call on that
+ *   device does: it looks up the array's device address with cudaGetSymbolAddress
+ *   (that device must be current) and caches it.  Callers with a fixed memory
+ *   plan should therefore make one call per device at start-up -- an empty
+ *   problem (B*H*N == 0, NULL pointers) does the look-up and launches nothing --
+ *   or run with CUDA_MODULE_LOADING=EAGER; make that first call before any stream
+ *   capture.  The cached address assumes the device is not reset (cudaDeviceReset)
+ *   while the library is in use.  No call allocates or frees memory itself.
  *   All calls share the one array, which keeps the last call's contents; nothing
  *   in it needs clearing (the row pass writes every entry the column pass reads).
  *   Calls whose executions overlap on the GPU (other streams, or other host

@@ -319,14 +319,16 @@ def backward_bf16_dS(Q, K, V, dO, gproj, scale=None, block=None, causal=True):
     product, P^_ij / sum_k P^_ik with P^ = bf16(P), so that the projected row sums to
     zero exactly.  Everything except the two roundings is fp64.  Used only to show
     what the rounding does; the reference for errors is always ``backward``.
-    Returns dict(dQ, dK, r, dS_proj_rowsum_rel) where the last item is
-    max_i |sum_j dS~_ij| / sum_j |dS~_ij| over rows with nonzero L1.
+    Returns dict(dQ, dK, r, rho, l1, dS_proj_rowsum_rel): r_i and rho_i = r_i / sum_k P^_ik
+    per row (both 0 without GProj), l1_i = sum_j |dS~_ij| (the L1 norm of the row the
+    products see: dS~ with GProj, dS^ without), and the worst row's
+    |sum_j dS~_ij| / sum_j |dS~_ij| over rows with nonzero L1.
     """
     Q, K, V, dO = map(_f64, (Q, K, V, dO))
     N, d = Q.shape
     scale = default_scale(d) if scale is None else scale
     dQ, dK = np.zeros((N, d)), np.zeros((N, d))
-    r_all = np.zeros(N)
+    r_all, rho_all, l1_all = np.zeros(N), np.zeros(N), np.zeros(N)
     worst = 0.0
     for r in _blocks(np.arange(N), block or _panel_budget(N, 4)):
         t = _row_terms(Q, K, V, dO, r, scale, causal=causal)
@@ -335,17 +337,19 @@ def backward_bf16_dS(Q, K, V, dO, gproj, scale=None, block=None, causal=True):
         if gproj:
             res = dSh.sum(axis=1)
             Ph = bf16_round(t["P"])
-            dSt = dSh - (res / Ph.sum(axis=1))[:, None] * Ph
-            r_all[r] = res
+            rho = res / Ph.sum(axis=1)
+            dSt = dSh - rho[:, None] * Ph
+            r_all[r], rho_all[r] = res, rho
         else:
             dSt = dSh
         l1 = np.abs(dSt).sum(axis=1)
+        l1_all[r] = l1
         nz = l1 > 0
         if nz.any():
             worst = max(worst, float(np.max(np.abs(dSt.sum(axis=1))[nz] / l1[nz])))
         dQ[r] = scale * (dSt @ K[:nk])
         dK[:nk] += scale * (dSt.T @ Q[r])
-    return dict(dQ=dQ, dK=dK, r=r_all, dS_proj_rowsum_rel=worst)
+    return dict(dQ=dQ, dK=dK, r=r_all, rho=rho_all, l1=l1_all, dS_proj_rowsum_rel=worst)
 
 
 # ---------------------------------------------------------------------------
@@ -404,15 +408,17 @@ def bob_bf16_dS(Q, K, V, dO, a, b, c, gproj, scale=None, block=None, causal=True
         gQ = s (dS~ b + Sbar K),   gK = s (dS~^T a + Sbar^T Q);
     gV, gdO and everything else are the exact fp64 values.  Used only to show what
     the rounding and the projection do; the reference for errors is always ``bob``.
-    Returns dict(gQ, gK, gV, gdO, r, rho, dS_rowsum_rel) where the last item is
-    max_i |sum_j dS~_ij| / sum_j |dS~_ij| over rows with nonzero L1.
+    Returns dict(gQ, gK, gV, gdO, r, rho, l1_dS, l1_Sbar, dS_rowsum_rel): per row the
+    residual r_i, the coefficient rho_i (0 without GProj), the L1 norms of the row of
+    dS~ (dS^ without GProj) and of Sbar, and the worst row's
+    |sum_j dS~_ij| / sum_j |dS~_ij| over rows with nonzero L1.
     """
     rnd = bf16_round if rnd is None else rnd
     Q, K, V, dO, a, b, c = map(_f64, (Q, K, V, dO, a, b, c))
     N, d = Q.shape
     scale = default_scale(d) if scale is None else scale
     gQ, gK, gV, gdO = (np.zeros((N, d)) for _ in range(4))
-    r_all, rho_all = np.zeros(N), np.zeros(N)
+    r_all, rho_all, l1_all, l1s_all = np.zeros(N), np.zeros(N), np.zeros(N), np.zeros(N)
     worst = 0.0
     for r in _blocks(np.arange(N), block or _panel_budget(N, 12)):
         t = _row_terms(Q, K, V, dO, r, scale, a, b, c, causal=causal)
@@ -428,6 +434,7 @@ def bob_bf16_dS(Q, K, V, dO, a, b, c, gproj, scale=None, block=None, causal=True
             dSt = dSh
             r_all[r] = dSh.sum(axis=1)
         l1 = np.abs(dSt).sum(axis=1)
+        l1_all[r], l1s_all[r] = l1, np.abs(t["Sbar"]).sum(axis=1)
         nz = l1 > 0
         if nz.any():
             worst = max(worst, float(np.max(np.abs(dSt.sum(axis=1))[nz] / l1[nz])))
@@ -435,7 +442,8 @@ def bob_bf16_dS(Q, K, V, dO, a, b, c, gproj, scale=None, block=None, causal=True
         gK[:nk] += scale * (dSt.T @ a[r] + t["Sbar"].T @ Q[r])
         gV[:nk] += t["dPbar"].T @ dO[r]
         gdO[r] = t["P"] @ c[:nk] + t["dPbar"] @ V[:nk]
-    return dict(gQ=gQ, gK=gK, gV=gV, gdO=gdO, r=r_all, rho=rho_all, dS_rowsum_rel=worst)
+    return dict(gQ=gQ, gK=gK, gV=gV, gdO=gdO, r=r_all, rho=rho_all, l1_dS=l1_all, l1_Sbar=l1s_all,
+                dS_rowsum_rel=worst)
 
 
 def bob_rows(Q, K, V, dO, a, b, c, rows, scale=None, causal=True):

@@ -1,0 +1,170 @@
+"""GProj on the tensor-core hot path ("FlashAttention bf16 gradient and GProj", section
+"How the zero sum turns into a false gradient").
+
+The exact score gradient dS has rows that sum to zero; its bf16 copy dS^ does not, and
+the leftover mass r_i = sum_j dS^_ij multiplies the mean key in dQ = s dS^ K.  GProj
+feeds the products the projected row dS~ = dS^ - rho_i P^ (rho_i = r_i / sum_j P^_ij),
+which sums to zero.  These tests read that row sum off the kernels themselves.
+
+Reading the row sum off dQ.  If every key has the same first coordinate c (a power of
+two, so each product dS~_ij c is exact in fp32), then column 0 of
+dQ_i = s sum_j dS~_ij K_j is s c sum_j dS~_ij: the sum of the very row the tensor-core
+products consumed.  The exact dQ[..., 0] is 0 (exact rows sum to zero, and a common
+key coordinate only shifts each row of S by a constant).  Without GProj the same column
+carries s c r_i.  In the backward over backward, setting the first coordinate of both K
+and the cotangent b = gdK to c makes gQ_i[0] = s c (sum_j dS~_ij + sum_j Sbar_ij), the
+row sums of the two operands gQ's products consume.
+
+Inputs: the large-key construction (keys with a shared mean of norm 40, queries near
+copies of earlier keys), B1 H4 N2048 at d = 64 and 128, then K[..., 0] = c = 16."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from gpu_util import host, rel_fro, row_rel_errors, to_device
+
+pytestmark = pytest.mark.gpu
+
+C = 16.0           # the shared first key coordinate (bf16-exact)
+ROWSUM_TOL = 1e-6  # projected row sums, relative to the row's L1 norm
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _inputs(d, cotangent_b=False):
+    w = W.Workload(f"gproj_hot_B1H4N2048d{d}_bf16", 1, 4, 2048, d, "bf16", kind="large_key")
+    x = dict(W.inputs(w))
+    x["K"] = x["K"].copy()
+    x["K"][..., 0] = C
+    if cotangent_b:
+        x["gdK"] = x["gdK"].copy()
+        x["gdK"][..., 0] = C
+    return w, x
+
+
+def _flip_aware_rho_dev(rho_gpu, rho_o, r_o, l1_o):
+    """|rho_gpu - rho_o| sum_j P^_ij relative to the row's L1 norm (sum P^ = r / rho).
+    A row where the kernel's fp32 dS rounds one element to the other bf16 neighbour than
+    the fp64 oracle's (the two dS differ in the last fp32 bits) moves r_i by one bf16
+    step of that element: at most 2^-8 max_j |dS_ij| <= 2^-8 of the L1 norm."""
+    keep = (l1_o > 0) & (rho_o != 0)
+    return np.abs(rho_gpu[keep] / rho_o[keep] - 1.0) * np.abs(r_o[keep]) / l1_o[keep]
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_backward_projected_rows_sum_to_zero_on_the_hot_path(d):
+    import torch
+
+    import fwd_bwd_double_gb300 as fbd
+    w, x = _inputs(d)
+    xd = to_device(x, w)
+    s = w.scale
+    O, lse = fbd.attn_fwd(xd["Q"], xd["K"], xd["V"])
+    desc = fbd.make_desc(xd["Q"])
+    got, wsrow = {}, {}
+    for gp in (0, 1):
+        ws = torch.full((fbd.attn_bwd_workspace_bytes(desc, gp) // 4,), float("nan"), dtype=torch.float32,
+                        device="cuda")
+        outs = [torch.empty_like(xd["Q"]) for _ in range(3)]
+        fbd.attn_bwd_passes(xd["Q"], xd["K"], xd["V"], O, xd["dO"], lse, fbd.ATTN_ROW_PASS, gp, *outs,
+                            workspace=ws)
+        fbd.attn_device_status()
+        wsrow[gp] = host(ws)
+        fbd.attn_bwd_passes(xd["Q"], xd["K"], xd["V"], O, xd["dO"], lse, fbd.ATTN_COL_PASS, gp, *outs,
+                            workspace=ws)
+        fbd.attn_device_status()
+        got[gp] = [host(t) for t in outs]
+    N, Np = w.N, (w.N + 1) // 2 * 2
+    worst, resid, rho_dev = [], [], []
+    for h in range(w.H):
+        sl = {k: x[k][0, h].astype(np.float64) for k in ("Q", "K", "V", "dO")}
+        ref = oracle.backward(sl["Q"], sl["K"], sl["V"], sl["dO"])
+        for gp in (0, 1):
+            for k, o in zip(("dQ", "dK", "dV"), got[gp]):
+                assert rel_fro(o[0, h], ref[k]) <= 2e-2, (gp, k, h)
+        em1 = oracle.backward_bf16_dS(sl["Q"], sl["K"], sl["V"], sl["dO"], gproj=True)
+        em0 = oracle.backward_bf16_dS(sl["Q"], sl["K"], sl["V"], sl["dO"], gproj=False)
+        keep = em1["l1"] > 0
+        rs1 = got[1][0][0, h, :, 0] / (s * C)   # row sums of dS~ as the products saw them
+        rs0 = got[0][0][0, h, :, 0] / (s * C)   # without GProj: the residual r_i
+        worst.append(np.abs(rs1[keep]) / em1["l1"][keep])
+        resid.append(np.abs(rs0[keep]) / em0["l1"][keep])
+        # -rho_i in the row statistics: float4 (k2 + 1) of the row pair k2 = i & ~1, slot i & 1.
+        wf = wsrow[1][h * Np * 4:(h + 1) * Np * 4]
+        i = np.arange(N)
+        rho_gpu = -wf[((i & ~1) + 1) * 4 + (i & 1)]
+        rho_dev.append(_flip_aware_rho_dev(rho_gpu, em1["rho"], em1["r"], em1["l1"]))
+        assert np.all(wf[((i & ~1) + 1) * 4 + 2 + (i & 1)] == 0)
+    worst, resid, rho_dev = (np.concatenate(v) for v in (worst, resid, rho_dev))
+    print(f"d={d}: projected row sum / L1 on the hot path: max {worst.max():.2e}, median {np.median(worst):.2e}; "
+          f"without GProj median {np.median(resid):.2e}; rho vs oracle (flip-aware, / L1): median "
+          f"{np.median(rho_dev):.2e}, max {rho_dev.max():.2e}")
+    assert worst.max() <= ROWSUM_TOL
+    assert np.median(resid) > 100 * ROWSUM_TOL   # the check sees the residual GProj removes
+    assert np.median(rho_dev) <= 1e-5
+    assert rho_dev.max() <= 2 ** -7
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_bob_projected_rows_sum_to_zero_on_the_hot_path(d):
+    import torch
+
+    import fwd_bwd_double_gb300 as fbd
+    w, x = _inputs(d, cotangent_b=True)
+    xd = to_device(x, w)
+    s = w.scale
+    O, lse = fbd.attn_fwd(xd["Q"], xd["K"], xd["V"])
+    desc = fbd.make_desc(xd["Q"])
+    got, wsrow = {}, {}
+    for gp in (0, 1):
+        ws = torch.full((fbd.attn_bob_workspace_bytes(desc, gp) // 4,), float("nan"), dtype=torch.float32,
+                        device="cuda")
+        outs = [torch.empty_like(xd["Q"]) for _ in range(4)]
+        fbd.attn_bob_passes(xd["Q"], xd["K"], xd["V"], O, xd["dO"], lse, xd["gdQ"], xd["gdK"], xd["gdV"],
+                            fbd.ATTN_ROW_PASS, *outs, workspace=ws, gproj=gp)
+        fbd.attn_device_status()
+        wsrow[gp] = host(ws)
+        fbd.attn_bob_passes(xd["Q"], xd["K"], xd["V"], O, xd["dO"], lse, xd["gdQ"], xd["gdK"], xd["gdV"],
+                            fbd.ATTN_COL_PASS, *outs, workspace=ws, gproj=gp)
+        fbd.attn_device_status()
+        got[gp] = [host(t) for t in outs]
+    N, Np, pitch = w.N, (w.N + 1) // 2 * 2, (w.N + 3) // 4 * 4
+    worst, resid, rho_dev, med = [], [], [], {0: [], 1: []}
+    for h in range(w.H):
+        sl = {k: x[k][0, h].astype(np.float64) for k in W.TENSORS}
+        args = (sl["Q"], sl["K"], sl["V"], sl["dO"], sl["gdQ"], sl["gdK"], sl["gdV"])
+        ref = oracle.bob(*args)
+        for gp in (0, 1):
+            for k, o in zip(("gQ", "gK", "gV", "gdO"), got[gp]):
+                assert rel_fro(o[0, h], ref[k]) <= 2e-2, (gp, k, h)
+            med[gp].append(row_rel_errors(got[gp][0][0, h], ref["gQ"]))
+        em1 = oracle.bob_bf16_dS(*args, True)
+        em0 = oracle.bob_bf16_dS(*args, False)
+        l1 = em1["l1_dS"] + em1["l1_Sbar"]
+        keep = em1["l1_dS"] > 0
+        rs1 = got[1][0][0, h, :, 0] / (s * C)
+        rs0 = got[0][0][0, h, :, 0] / (s * C)
+        worst.append(np.abs(rs1[keep]) / l1[keep])
+        resid.append(np.abs(rs0[keep]) / (em0["l1_dS"] + em0["l1_Sbar"])[keep])
+        # -rho_i: behind the row states (B*H*Np float4), one float per row at pitch N rounded up to 4.
+        base = w.H * Np * 4 + h * pitch
+        rho_gpu = -wsrow[1][base:base + N]
+        rho_dev.append(_flip_aware_rho_dev(rho_gpu, em1["rho"], em1["r"], em1["l1_dS"]))
+    worst, resid, rho_dev = (np.concatenate(v) for v in (worst, resid, rho_dev))
+    m0, m1 = (float(np.median(np.concatenate(med[g]))) for g in (0, 1))
+    print(f"d={d}: BoB gQ row sums of [dS~ | Sbar] / L1 on the hot path: max {worst.max():.2e}, median "
+          f"{np.median(worst):.2e}; without GProj median {np.median(resid):.2e}; rho vs oracle (flip-aware): "
+          f"median {np.median(rho_dev):.2e}, max {rho_dev.max():.2e}; median row gQ error {m0:.2e} -> {m1:.2e}")
+    assert worst.max() <= ROWSUM_TOL
+    assert np.median(resid) > 100 * ROWSUM_TOL
+    assert np.median(rho_dev) <= 1e-5
+    assert rho_dev.max() <= 2 ** -7
+    assert m1 < m0

@@ -135,15 +135,17 @@ def test_bench_workload_sampled(gproj):
 
 
 def test_full_day_ragged_tail():
+    """B2 H12 N23400 (N = 182 * 128 + 104): sampled rows (the whole ragged last tile of 104
+    rows among them) and late columns of four heads in each batch entry (every slice has
+    its own offset in the tensor maps)."""
     w = W.FULL_DAY
     x = to_device(W.inputs(w), w)
     got = run_ops(w, x, ops=("bwd",))
-    # The batch-0 heads checked; rows include the whole ragged last tile (104 rows).
     rows, cols = sample_rows_cols(w.N, np.random.default_rng(3))
     rows = np.unique(np.concatenate([rows, np.arange(w.N - 104, w.N)]))
-    errs = sampled_check(w, got, ("bwd",), heads=[0, 7], rows=rows, cols=cols)
-    print(w.name, {k: f"{v:.2e}" for k, v in errs.items()})
-    # batch 1 (a different slice offset) and no NaN anywhere
+    for b, heads in ((0, [0, 3, 7, 11]), (1, [1, 5, 8, 11])):
+        errs = sampled_check(w, got, ("bwd",), heads=heads, rows=rows, cols=cols, batch=b)
+        print(w.name, b, heads, {k: f"{v:.2e}" for k, v in errs.items()})
     for k in ("O", "dQ", "dK", "dV"):
         assert not np.isnan(host(got[k])).any(), k
 
@@ -160,26 +162,40 @@ def test_large_key_gproj_reduces_dQ_error():
     x = W.inputs(w)
     xd = to_device(x, w)
     O, lse = fbd.attn_fwd(xd["Q"], xd["K"], xd["V"], scale=w.scale)
-    dQ0, dK0, _ = fbd.attn_bwd(xd["Q"], xd["K"], xd["V"], O, xd["dO"], lse, gproj=0, scale=w.scale)
+    dQ0, dK0, dV0 = fbd.attn_bwd(xd["Q"], xd["K"], xd["V"], O, xd["dO"], lse, gproj=0, scale=w.scale)
     dQ1, dK1, dV1 = fbd.attn_bwd(xd["Q"], xd["K"], xd["V"], O, xd["dO"], lse, gproj=1, scale=w.scale)
+    outs = {0: [host(t) for t in (dQ0, dK0, dV0)], 1: [host(t) for t in (dQ1, dK1, dV1)]}
     Kc = W.round_to_bf16((x["K"] - x["K"].astype(np.float64).mean(axis=2, keepdims=True)).astype(np.float32))
     xc = to_device({"K": Kc}, w)
     Oc, lsec = fbd.attn_fwd(xd["Q"], xc["K"], xd["V"], scale=w.scale)
     dQc, _, _ = fbd.attn_bwd(xd["Q"], xc["K"], xd["V"], Oc, xd["dO"], lsec, gproj=0, scale=w.scale)
     fbd.attn_device_status()
-    e0, e1, ec, maxp = [], [], [], []
+    dQc = host(dQc)
+    e0, e1, ec, k0, k1, maxp = [], [], [], [], [], []
+    acc = {(gp, k): ([], []) for gp in (0, 1) for k in ("dQ", "dK", "dV")}
     for b in range(2):
         for h in range(w.H):
             s = {k: x[k][b, h].astype(np.float64) for k in ("Q", "K", "V", "dO")}
             ref = oracle.backward(s["Q"], s["K"], s["V"], s["dO"], scale=w.scale)
-            e0.append(row_rel_errors(host(dQ0[b, h]), ref["dQ"]))
-            e1.append(row_rel_errors(host(dQ1[b, h]), ref["dQ"]))
-            ec.append(row_rel_errors(host(dQc[b, h]), ref["dQ"]))
+            for gp in (0, 1):
+                for k, o in zip(("dQ", "dK", "dV"), outs[gp]):
+                    acc[gp, k][0].append(o[b, h])
+                    acc[gp, k][1].append(ref[k])
+            e0.append(row_rel_errors(outs[0][0][b, h], ref["dQ"]))
+            e1.append(row_rel_errors(outs[1][0][b, h], ref["dQ"]))
+            ec.append(row_rel_errors(dQc[b, h], ref["dQ"]))
+            k0.append(row_rel_errors(outs[0][1][b, h], ref["dK"]))
+            k1.append(row_rel_errors(outs[1][1][b, h], ref["dK"]))
             P, _ = oracle.softmax_rows(oracle.scores(s["Q"], s["K"], np.arange(256, 2048, 64), w.scale))
             maxp.append(P.max(axis=1))
-    m0, m1, mc = (float(np.median(np.concatenate(e))) for e in (e0, e1, ec))
+    # Parity of every output, with and without GProj, against the exact fp64 backward.
+    fro = {f"{k} gproj={gp}": rel_fro(np.stack(g), np.stack(r)) for (gp, k), (g, r) in acc.items()}
+    m0, m1, mc, mk0, mk1 = (float(np.median(np.concatenate(e))) for e in (e0, e1, ec, k0, k1))
     print(f"{w.name}: median row dQ rel err no-GProj {m0:.4e}, GProj {m1:.4e}, mean-key subtraction {mc:.4e}; "
-          f"median row max P {float(np.median(np.concatenate(maxp))):.3f}")
+          f"median row dK rel err no-GProj {mk0:.4e}, GProj {mk1:.4e}; "
+          f"median row max P {float(np.median(np.concatenate(maxp))):.3f}; rel-Frobenius "
+          + ", ".join(f"{k} {v:.2e}" for k, v in fro.items()))
+    assert all(v <= TOL["bf16"] for v in fro.values()), fro
     assert m1 < m0
     assert mc < m0
 

@@ -221,6 +221,36 @@ def test_gproj_projected_rows_sum_to_zero_and_rounding_leaves_residual():
     assert rel(proj["dQ"], exact["dQ"]) < rel(plain["dQ"], exact["dQ"])
 
 
+def test_gproj_row_coefficients_brute_force():
+    """The per-row quantities the emulation reports (r_i, rho_i = r_i / sum P^_i and the
+    L1 norm of the projected row) against pure-Python loops over the definitions of P,
+    dP, D and dS, rounded with the pinned bf16 rounding."""
+    N, d = 12, 4
+    Q, K, V, dO = slice_set(N, d, 41)[:4]
+    K = K + 3.0
+    s = 1.0 / math.sqrt(d)
+    proj = oracle.backward_bf16_dS(Q, K, V, dO, gproj=True)
+    plain = oracle.backward_bf16_dS(Q, K, V, dO, gproj=False)
+    for i in range(N):
+        sc = [s * sum(Q[i][t] * K[j][t] for t in range(d)) for j in range(i + 1)]
+        m = max(sc)
+        e = [math.exp(x - m) for x in sc]
+        P = [x / sum(e) for x in e]
+        dP = [sum(dO[i][t] * V[j][t] for t in range(d)) for j in range(i + 1)]
+        D = sum(P[j] * dP[j] for j in range(i + 1))
+        dS = [P[j] * (dP[j] - D) for j in range(i + 1)]
+        dSh = [float(x) for x in A.bf16_round(np.array(dS))]
+        Ph = [float(x) for x in A.bf16_round(np.array(P))]
+        r = sum(dSh)
+        rho = r / sum(Ph)
+        l1 = sum(abs(dSh[j] - rho * Ph[j]) for j in range(i + 1))
+        assert abs(proj["r"][i] - r) <= 1e-12 * sum(abs(x) for x in dSh)
+        assert abs(proj["rho"][i] - rho) <= 1e-12 * (abs(rho) + 1e-300) + 1e-15
+        assert abs(proj["l1"][i] - l1) <= 1e-12 * l1
+        assert abs(plain["l1"][i] - sum(abs(x) for x in dSh)) <= 1e-12 * l1
+        assert plain["rho"][i] == 0.0
+
+
 def test_bf16_round_is_round_to_nearest_even():
     # 1 + 2^-8 is halfway between 1 and 1 + 2^-7: ties to even gives 1.
     x = np.array([1.0, 1 + 2 ** -8, 1 + 3 * 2 ** -8, -2.5 + 2 ** -9, 3.0e-39])
