@@ -488,6 +488,7 @@ def max_n_report(exec_n=1 << 20, check=True):
     out["bisect_s"] = time.perf_counter() - t0
     # One execution per op at N = exec_n.  Head 0 comes from the seeded workload (so the
     # oracle can check it); heads 1..11 are device-drawn N(0,1) values (timing filler).
+    torch.cuda.reset_peak_memory_stats(dev)
     N = exec_n
     w = W.Workload(f"maxn_B1H12N{N}d64", 1, H, N, d, "bf16")
     x0 = W.inputs(w, heads=[0])
