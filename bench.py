@@ -34,26 +34,41 @@ sys.path.insert(0, ROOT)
 import workloads as W  # noqa: E402
 
 L2_BYTES = 129 * 2 ** 20
-LAUNCHES_PER_STEP = {"fwd": 1, "bwd": 2, "bob": 2}  # BoB with GProj: + 1 (the P^ b launch)
-KERNELS = ("fwd", "bwd_row", "bwd_col", "bob_row", "bob_col")
-# Contractions (N^2 d products) per kernel: the dense definition's share (each of
+# Timed intervals of a step: the forward, the whole backward (bf16 at d <= 64 without
+# GProj: the single-pass form, three launches -- statistics, the key-block pass, the dQ
+# write; otherwise the row and the column pass), the BoB row pass and column pass.
+KERNELS = ("fwd", "bwd", "bob_row", "bob_col")
+# Contractions (N^2 d products) per interval: the dense definition's share (each of
 # the pages' contractions counted once; tiles recomputed by a column pass are not
-# counted) and what the kernel executes.  Flops = 2 x count x B H N^2 d / 2.
-DENSE_CONTRACTIONS = {"fwd": 2, "bwd_row": 3, "bwd_col": 2, "bob_row": 9, "bob_col": 3}
-EXECUTED_CONTRACTIONS = {"fwd": 2, "bwd_row": 3, "bwd_col": 4, "bob_row": 11, "bob_col": 8}
+# counted) and what the kernels execute.  Flops = 2 x count x B H N^2 d / 2.
+DENSE_CONTRACTIONS = {"fwd": 2, "bwd": 5, "bob_row": 9, "bob_col": 3}
+EXECUTED_CONTRACTIONS = {"fwd": 2, "bwd": 5, "bob_row": 11, "bob_col": 8}
 # At 64 < d <= 128 the BoB passes run two CTAs per block (one per output half), both
-# computing the five tile products: 2 x 5 + 6 and 2 x 5 + 3 full-width contractions.
-EXECUTED_CONTRACTIONS_D128 = dict(EXECUTED_CONTRACTIONS, bob_row=16, bob_col=13)
+# computing the five tile products: 2 x 5 + 6 and 2 x 5 + 3 full-width contractions;
+# the backward runs its two passes (3 + 4 contractions: the tiles recomputed).
+EXECUTED_CONTRACTIONS_D128 = dict(EXECUTED_CONTRACTIONS, bwd=7, bob_row=16, bob_col=13)
 
 
-def executed_flops(w, kn):
-    """Flops the tensor-core kernel executes: head dims 32 and 96 run zero-padded to
-    64 and 128; None for d = 256 (CUDA-core kernels)."""
+def bwd_single_pass(w, gproj):
+    return w.d <= 64 and not gproj
+
+
+def launches_per_step(w, gproj):
+    return 1 + (3 if bwd_single_pass(w, gproj) else 2) + 2 + (1 if gproj else 0)
+
+
+def executed_flops(w, kn, gproj=0):
+    """Flops the tensor-core kernels execute: head dims 32 and 96 run zero-padded to
+    64 and 128; the two-pass backward (GProj, or d > 64) 7 contractions, 9 with GProj;
+    None for d = 256 (CUDA-core kernels)."""
     if w.d > 128:
         return None
     pad = 64 if w.d <= 64 else 128
     table = EXECUTED_CONTRACTIONS if pad == 64 else EXECUTED_CONTRACTIONS_D128
-    return 2 * table[kn] * w.B * w.H * pairs(w.N) * pad
+    n = table[kn]
+    if kn == "bwd" and not bwd_single_pass(w, gproj):
+        n = 9 if gproj else 7
+    return 2 * n * w.B * w.H * pairs(w.N) * pad
 
 
 def dist_init(world, backend="nccl"):
@@ -212,28 +227,28 @@ def run_ours(args, w, rank, world):
     like = {"O": "Q", "dQ": "Q", "dK": "K", "dV": "V", "gQ": "Q", "gK": "K", "gV": "V", "gdO": "Q"}
     out = {k: torch.empty(x[src].shape, dtype=bf, device=dev) for k, src in like.items()}
     lse = torch.empty(shp[:3], dtype=torch.float32, device=dev)
-    ws = torch.empty(fbd.attn_bwd_workspace_bytes(desc, 1), dtype=torch.uint8, device=dev)
+    ws = torch.empty(max(fbd.attn_bwd_workspace_bytes(desc, g) for g in (0, 1)), dtype=torch.uint8, device=dev)
     ws2 = torch.empty(fbd.attn_bob_workspace_bytes(desc, 1), dtype=torch.uint8, device=dev)  # fits both forms
 
     R, C = fbd.ATTN_ROW_PASS, fbd.ATTN_COL_PASS
 
     def step(xx, gproj=args.gproj, ev=None):
-        """fwd, bwd row pass, bwd column pass, BoB row pass, BoB column pass: one launch each."""
+        """fwd, the backward (one call: its single-pass or two-pass launches), the BoB row
+        pass and the BoB column pass, each between two events."""
         def mark(i):
             if ev:
                 ev[i].record(stream)
         mark(0)
         fbd.attn_fwd(xx["Q"], xx["K"], xx["V"], O=out["O"], lse=lse, stream=stream, desc=desc)
         mark(1)
-        for i, ps in enumerate((R, C)):
-            fbd.attn_bwd_passes(xx["Q"], xx["K"], xx["V"], out["O"], xx["dO"], lse, ps, gproj=gproj, dQ=out["dQ"],
-                                dK=out["dK"], dV=out["dV"], workspace=ws, stream=stream, desc=desc)
-            mark(2 + i)
+        fbd.attn_bwd(xx["Q"], xx["K"], xx["V"], out["O"], xx["dO"], lse, gproj=gproj, dQ=out["dQ"], dK=out["dK"],
+                     dV=out["dV"], workspace=ws, stream=stream, desc=desc)
+        mark(2)
         for i, ps in enumerate((R, C)):
             fbd.attn_bob_passes(xx["Q"], xx["K"], xx["V"], out["O"], xx["dO"], lse, xx["gdQ"], xx["gdK"], xx["gdV"],
                                 ps, gQ=out["gQ"], gK=out["gK"], gV=out["gV"], gdO=out["gdO"], workspace=ws2,
                                 stream=stream, desc=desc, gproj=gproj)
-            mark(4 + i)
+            mark(3 + i)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -241,7 +256,7 @@ def run_ours(args, w, rank, world):
     torch.cuda.synchronize()
     fbd.attn_device_status(stream)
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(KERNELS) + 1)] for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(dev.index) as clk:
@@ -255,8 +270,7 @@ def run_ours(args, w, rank, world):
     fbd.attn_device_status(stream)
     per_kernel = {kn: [evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps)]
                   for i, kn in enumerate(KERNELS)}
-    per_op = {"fwd": per_kernel["fwd"],
-              "bwd": [x + y for x, y in zip(per_kernel["bwd_row"], per_kernel["bwd_col"])],
+    per_op = {"fwd": per_kernel["fwd"], "bwd": per_kernel["bwd"],
               "bob": [x + y for x, y in zip(per_kernel["bob_row"], per_kernel["bob_col"])]}
     step_ms = [sum(per_op[op][k] for op in per_op) for k in range(args.steps)]
     ms = statistics.mean(step_ms)
@@ -450,7 +464,8 @@ def max_n_report(exec_n=1 << 20, check=True):
     torch.cuda.empty_cache()
     H, d = 12, 64
     row = H * d * 2  # bytes of one token of one [B,H,N,d] bf16 tensor
-    per_token = {"bob": 12 * row + 4 * H + 16 * H, "bwd": 8 * row + 4 * H + 16 * H}
+    # The backward's single-pass form adds its fp32 dQ accumulator (64 floats per row).
+    per_token = {"bob": 12 * row + 4 * H + 16 * H, "bwd": 8 * row + 4 * H + 16 * H + 256 * H}
     ntensor = {"bob": 12, "bwd": 8}
     free, total = torch.cuda.mem_get_info(dev)
     out = {"metric": "max N in HBM (B=1, H=12, d=64, bf16)", "hbm_total_bytes": total, "hbm_free_bytes": free,
@@ -464,6 +479,8 @@ def max_n_report(exec_n=1 << 20, check=True):
                 bufs.append(torch.empty((1, H, N, d), dtype=torch.bfloat16, device=dev))
             bufs.append(torch.empty((1, H, N), dtype=torch.float32, device=dev))
             bufs.append(torch.empty((1, H, N, 4), dtype=torch.float32, device=dev))
+            if op == "bwd":
+                bufs.append(torch.empty((1, H, N, 64), dtype=torch.float32, device=dev))
             return True
         except torch.OutOfMemoryError:
             return False
@@ -728,8 +745,8 @@ def main():
                 for op in r["per_op"]},
         "kernels": {kn: {"ms": r["per_kernel"][kn],
                          "tflops_dense_share": tf(kernel_flops(w, kn, DENSE_CONTRACTIONS), r["per_kernel"][kn]),
-                         "tflops_executed": (tf(executed_flops(w, kn), r["per_kernel"][kn])
-                                             if executed_flops(w, kn) else None)}
+                         "tflops_executed": (tf(executed_flops(w, kn, args.gproj), r["per_kernel"][kn])
+                                             if executed_flops(w, kn, args.gproj) else None)}
                     for kn in KERNELS},
         "gproj_bwd_ms": {"off": r["bwd_gproj_ms"][0], "on": r["bwd_gproj_ms"][1],
                          "overhead_pct": 100.0 * (r["bwd_gproj_ms"][1] / r["bwd_gproj_ms"][0] - 1.0)},
@@ -739,11 +756,11 @@ def main():
                      "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops"], "traffic": traffic_for(dom, w),
                      "peak_source": pk["source"] + " burst bf16",
                      "achieved_basis": "dense-definition contractions of this kernel / its CUDA-event time",
-                     "executed_frac": (tf(executed_flops(w, dom), r["per_kernel"][dom]) / pk["bf16_tflops"]
-                                       if executed_flops(w, dom) else None)},
+                     "executed_frac": (tf(executed_flops(w, dom, args.gproj), r["per_kernel"][dom]) / pk["bf16_tflops"]
+                                       if executed_flops(w, dom, args.gproj) else None)},
         "e2e": {"value": r["flops_step"] / (r["e2e_ms"] * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["e2e_ms"]},
-        "gpu_launches": (sum(LAUNCHES_PER_STEP.values()) + (1 if args.gproj else 0)) * args.steps,
+        "gpu_launches": launches_per_step(w, args.gproj) * args.steps,
         "clocks": r["clocks"],
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -147,11 +147,14 @@ attn_status_t attn_fwd(const attn_desc_t* desc, const void* Q, const void* K, co
 }
 
 size_t attn_bwd_workspace_bytes(const attn_desc_t* desc, int gproj) {
-  (void)gproj;
   if (desc == nullptr || desc->B < 0 || desc->H < 0 || desc->N < 0) return 0;
   // 16 bytes per row, the rows of each slice rounded up to an even count (the bf16
-  // column pass reads the row statistics two rows at a time).
-  return static_cast<size_t>(desc->B) * desc->H * ((desc->N + 1) & ~static_cast<int64_t>(1)) * 16;
+  // column pass reads the row statistics two rows at a time); for the single-pass bf16
+  // backward (d <= 64, no GProj) then the fp32 dQ accumulator, 256 bytes per row.
+  size_t n = static_cast<size_t>(desc->B) * desc->H * ((desc->N + 1) & ~static_cast<int64_t>(1)) * 16;
+  if (desc->dtype == ATTN_BF16 && desc->d > 0 && desc->d <= 64 && !gproj)
+    n += fbd::bwd_fused_acc_bytes(desc->B * desc->H, desc->N);
+  return n;
 }
 
 size_t attn_bob_workspace_bytes(const attn_desc_t* desc, int gproj) {
@@ -178,7 +181,10 @@ attn_status_t attn_bwd_passes(const attn_desc_t* desc, const void* Q, const void
   if (s != ATTN_OK) return s;
   if (passes < 1 || passes > 3) return fail(ATTN_ERR_INVALID_ARG, "passes must be ATTN_ROW_PASS, ATTN_COL_PASS or both%s");
   if (p.BH * p.N == 0) return ATTN_OK;
-  const size_t need = attn_bwd_workspace_bytes(desc, gproj);
+  // One pass alone reads or writes only the row statistics (the first 16 bytes per row of
+  // the workspace); both passes in one call may take the single-pass form's accumulator.
+  const size_t stats_bytes = static_cast<size_t>(p.BH) * ((p.N + 1) & ~static_cast<int64_t>(1)) * 16;
+  const size_t need = passes == (ATTN_ROW_PASS | ATTN_COL_PASS) ? attn_bwd_workspace_bytes(desc, gproj) : stats_bytes;
   if (workspace == nullptr || workspace_bytes < need)
     return fail(ATTN_ERR_WORKSPACE, "workspace NULL or smaller than attn_bwd_workspace_bytes()%s");
   const size_t tb = static_cast<size_t>(p.BH * p.N * p.d) * elem_size(p), sb = p.BH * p.N * sizeof(float);
@@ -192,6 +198,9 @@ attn_status_t attn_bwd_passes(const attn_desc_t* desc, const void* Q, const void
   float4* ws = static_cast<float4*>(workspace);
   if (!tc_path(p, 1))
     return launch_status(fbd::simt_bwd(p, Q, K, V, O, dO, lse, dQ, dK, dV, gproj, ws, passes, st));
+  // Both passes in one call: the single-pass form where it exists (bf16, d <= 64, no GProj).
+  if (passes == (ATTN_ROW_PASS | ATTN_COL_PASS) && fbd::bwd_fused_applies(p, gproj != 0))
+    return launch_status(fbd::tc_bwd_fused(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, st));
   return launch_status(fbd::tc_bwd(p, Q, K, V, O, dO, lse, dQ, dK, dV, gproj != 0, ws, passes, st));
 }
 
@@ -262,7 +271,7 @@ attn_status_t attn_bwd_projected_dS(const attn_desc_t* desc, const void* Q, cons
 attn_status_t attn_device_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "CUDA: %s", cudaGetErrorString(e));
-  const uint32_t flags = fbd::tc_fwd_take_error() | fbd::tc_bwd_take_error() | fbd::tc_bwd_wide_take_error() |
+  const uint32_t flags = fbd::tc_fwd_take_error() | fbd::tc_bwd_take_error() | fbd::tc_bwd_wide_take_error() | fbd::tc_bwd_fused_take_error() |
                          fbd::tc_bob_take_error() | fbd::tc_bob128_take_error() | fbd::selftest_take_error();
   if (flags != 0) return fail(ATTN_ERR_TIMEOUT, "a device-side bounded wait gave up%s");
   return ATTN_OK;
@@ -324,6 +333,19 @@ bool make_tmap_bf16(void* map_out, const void* base, int64_t N, int64_t d, int64
   const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows), 1u};
   const cuuint32_t estr[3] = {1u, 1u, 1u};
   CUresult r = fn(static_cast<CUtensorMap*>(map_out), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
+                  dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool make_tmap_f32_rows(void* map_out, const void* base, int64_t N, int64_t BH, int box_rows) {
+  EncodeFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {64u, static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {256u, static_cast<cuuint64_t>(N) * 256u};
+  const cuuint32_t box[3] = {32u, static_cast<cuuint32_t>(box_rows), 1u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = fn(static_cast<CUtensorMap*>(map_out), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base),
                   dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;

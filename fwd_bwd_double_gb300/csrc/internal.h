@@ -52,6 +52,17 @@ cudaError_t tc_bwd(const Problem& p, const void* Q, const void* K, const void* V
 cudaError_t tc_bwd_wide(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
                         const void* dO, const float* lse, void* dQ, void* dK, void* dV, float4* ws, int passes,
                         cudaStream_t st, bool gproj = false);
+// Single-pass backward (tc_bwd_fused.cu), bf16 at d <= 64 without GProj: a prep launch
+// (D_i, the row statistics, a zeroed fp32 dQ accumulator), one launch per key block that
+// writes dK, dV once and reduce-adds each query block's dS K into the accumulator, and a
+// launch that scales and rounds dQ.  `ws` holds the statistics (16 bytes per row, rows of
+// a slice rounded up to even) and then the accumulator (bwd_fused_acc_bytes).
+bool bwd_fused_applies(const Problem& p, bool gproj);
+inline size_t bwd_fused_acc_bytes(int64_t BH, int64_t N) { return static_cast<size_t>(BH) * N * 64 * sizeof(float); }
+cudaError_t tc_bwd_fused(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
+                         const void* dO, const float* lse, void* dQ, void* dK, void* dV, float4* ws, cudaStream_t st);
+uint32_t tc_bwd_fused_take_error();
+
 cudaError_t tc_bob(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
                    const void* dO, const float* lse, const void* a, const void* b, const void* c, void* gQ,
                    void* gK, void* gV, void* gdO, bool gproj, float4* ws, int passes, cudaStream_t st);
@@ -109,6 +120,10 @@ attn_status_t validate_desc(const attn_desc_t* desc);
 // encode fails.
 bool make_tmap_bf16(void* map_out /* CUtensorMap* */, const void* base, int64_t N, int64_t d, int64_t BH,
                     int box_rows);
+
+// Tensor map of an fp32 [B*H, N, 64] row buffer: 3-D view (64, N, B*H), box (32, rows, 1)
+// (128 bytes of a row), 128-byte swizzle; rows past N are never written by a store or reduce.
+bool make_tmap_f32_rows(void* map_out, const void* base, int64_t N, int64_t BH, int box_rows);
 
 // Tensor map of the float4 row-statistics workspace [B*H, N]: 3-D fp32 view
 // (4, N, B*H), box (4, rows, 1), no swizzle; rows past N read as zero.

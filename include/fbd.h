@@ -130,8 +130,10 @@ attn_status_t attn_fwd(const attn_desc_t* desc, const void* Q, const void* K, co
                        void* O, float* lse, void* stream);
 
 /* Workspace for attn_bwd: 16 bytes per (b,h,row), the rows of each slice rounded
- * up to an even count: the row statistics (lse, D, GProj coefficient) written by
- * the row pass and read by the column pass (layout internal to the library). */
+ * up to an even count: the row statistics (lse, D, GProj coefficient) read by the
+ * column pass (layout internal to the library); for bf16 at d <= 64 without GProj
+ * (the single-pass form of attn_bwd) 256 bytes more per (b,h,row) for an fp32 dQ
+ * accumulator. */
 size_t attn_bwd_workspace_bytes(const attn_desc_t* desc, int gproj);
 
 /* Recompute backward.  [FA] "Backward pass: recompute instead of store": P is
@@ -139,7 +141,15 @@ size_t attn_bwd_workspace_bytes(const attn_desc_t* desc, int gproj);
  *   dP = dO V^T, D_i = sum_k dO_ik O_ik, dS = P * (dP - D):
  *   dQ = s dS K,  dK = s dS^T Q,  dV = P^T dO          (all [B,H,N,d]).
  * Two launches on `stream`: a row pass (dQ and the row statistics) and a column
- * pass (dK, dV).
+ * pass (dK, dV).  For bf16 at d <= 64 without GProj, the single-pass form instead
+ * ([FA] "FA2: parallelism": the work split over key blocks, the query gradient summed
+ * across them): a launch forming D and the row statistics, one launch over key blocks
+ * that writes dK, dV once and adds each key block's dS K share of dQ into an fp32
+ * accumulator in the workspace (tensor reduce-adds in L2), and a launch that writes
+ * dQ = s * accumulator once, rounded to bf16.  Every contraction then runs once.  The
+ * shares are added in the order the key blocks reach a query block, so dQ may differ
+ * between calls in its last bits (two bf16 steps at most); dK and dV, and every output
+ * of the two-pass forms, are the same bits on every call.
  * gproj != 0 (bf16 only; ignored for ATTN_F32, whose dS is never rounded):
  *   [GP] "How the zero sum turns into a false gradient".  The row of dS is rounded
  *   to bf16 (dS^) before the dS K and dS^T Q products; its remaining mass
@@ -232,7 +242,10 @@ attn_status_t attn_bob_static(const attn_desc_t* desc, const void* Q, const void
  * and the row statistics; BoB: gQ, gdO and the row states, after the P^ b launch
  * when gproj is set on the bf16 tensor-core path), ATTN_COL_PASS
  * (backward: dK, dV; BoB: gK, gV, both from the statistics the row pass left in
- * `workspace`), or both, which is exactly attn_bwd / attn_bob.  A column pass
+ * `workspace`), or both, which is exactly attn_bwd / attn_bob (for the backward the
+ * single-pass form where attn_bwd uses it, so dQ then equals the two separate passes'
+ * dQ up to the summation order).  A single pass needs only the statistics part of the
+ * workspace: 16 bytes per (b,h,row), the rows of each slice rounded up to even.  A column pass
  * must follow, in stream order, a row pass over the same inputs and workspace.
  * Arguments and checks are those of attn_bwd / attn_bob (all pointers are
  * validated whichever pass runs); any other `passes` is ATTN_ERR_INVALID_ARG.

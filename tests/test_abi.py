@@ -103,10 +103,16 @@ def test_null_misaligned_and_overlapping_pointers():
 
 def test_workspace_checks():
     d = desc(B=2, H=3, N=100)
-    assert lib.attn_bwd_workspace_bytes(ctypes.byref(d), 0) == 2 * 3 * 100 * 16
+    # The single-pass bf16 backward (d <= 64, no GProj): the statistics and then the fp32
+    # dQ accumulator (64 floats per row); with GProj, at d > 64 or in float32 the
+    # statistics alone.
+    assert lib.attn_bwd_workspace_bytes(ctypes.byref(d), 0) == 2 * 3 * 100 * (16 + 256)
     assert lib.attn_bwd_workspace_bytes(ctypes.byref(d), 1) == 2 * 3 * 100 * 16
+    assert lib.attn_bwd_workspace_bytes(ctypes.byref(desc(B=2, H=3, N=100, d=128)), 0) == 2 * 3 * 100 * 16
+    assert lib.attn_bwd_workspace_bytes(ctypes.byref(desc(B=2, H=3, N=100, dtype=0)), 0) == 2 * 3 * 100 * 16
+    assert lib.attn_bwd_workspace_bytes(ctypes.byref(desc(B=1, H=1, N=7, d=32)), 0) == 8 * 16 + 7 * 256
     assert lib.attn_bob_workspace_bytes(ctypes.byref(d), 0) == 2 * 3 * 100 * 16
-    assert bwd(d, ws_bytes=2 * 3 * 100 * 16 - 1) == WS
+    assert bwd(d, ws_bytes=2 * 3 * 100 * (16 + 256) - 1) == WS
     assert bob(d, ws_bytes=0) == WS
     p = ptrs(14)
     p[13] = ctypes.c_void_p(0)

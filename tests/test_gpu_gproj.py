@@ -29,8 +29,11 @@ In that regime the kernels' fp32 scores differ from the fp64 oracle's by far mor
 than the spacing of bf16 values, so dS rounds to the other neighbour on a few percent
 of the elements and the residual r_i differs from the oracle's row by row; the
 coefficient rho the row pass stores is therefore checked against the residual its own
-products carried (the GProj-free run's readout), and against the oracle on i.i.d.
-inputs, where such flips are rare."""
+products carried (the GProj-free run's readout).  (On any inputs the kernels form
+D_i = dO_i . O_i from the bf16-rounded O the forward stored, where the oracle's D is
+exact; the two dS then differ at about 1e-3 relative and round to different bf16
+neighbours on many elements, so r_i and rho_i are not comparable row by row with the
+oracle's emulation.)"""
 import numpy as np
 import pytest
 
@@ -191,33 +194,3 @@ def test_bob_projected_rows_sum_to_zero_on_the_hot_path(d):
     assert np.median(rho_dev) <= 2e-2
     assert m1 < m0
 
-
-def test_projected_rho_matches_oracle_on_iid_inputs():
-    """The coefficient rho_i = sum_j dS^_ij / sum_j P^_ij that the tensor-core row pass
-    stores for the column pass, against the oracle's emulation on the i.i.d. GPT-2 layer
-    inputs (B1 H4 N1024 d64), where the kernel's fp32 dS and the fp64 one rarely round
-    to different bf16 neighbours: most rows agree to the fp32 summation error of r_i."""
-    import torch
-
-    import fwd_bwd_double_gb300 as fbd
-    w = W.Workload("gproj_rho_B1H4N1024d64_bf16", 1, 4, 1024, 64, "bf16")
-    x = W.inputs(w)
-    xd = to_device(x, w)
-    O, lse = fbd.attn_fwd(xd["Q"], xd["K"], xd["V"])
-    desc = fbd.make_desc(xd["Q"])
-    ws = torch.full((fbd.attn_bwd_workspace_bytes(desc, 1) // 4,), float("nan"), dtype=torch.float32, device="cuda")
-    fbd.attn_bwd_passes(xd["Q"], xd["K"], xd["V"], O, xd["dO"], lse, fbd.ATTN_ROW_PASS, 1, workspace=ws)
-    fbd.attn_device_status()
-    wf = host(ws)
-    N, Np = w.N, w.N
-    i = np.arange(N)
-    dev = []
-    for h in range(w.H):
-        sl = {k: x[k][0, h].astype(np.float64) for k in ("Q", "K", "V", "dO")}
-        em = oracle.backward_bf16_dS(sl["Q"], sl["K"], sl["V"], sl["dO"], gproj=True)
-        rho_gpu = -wf[h * Np * 4:(h + 1) * Np * 4][((i & ~1) + 1) * 4 + (i & 1)]
-        keep = em["l1"] > 0
-        dev.append(np.abs(rho_gpu[keep] - em["rho"][keep]) / np.abs(em["rho"][keep]))
-    dev = np.concatenate(dev)
-    print(f"rho vs oracle on i.i.d. inputs: median rel {np.median(dev):.2e}, 90th pct {np.percentile(dev, 90):.2e}")
-    assert np.median(dev) <= 1e-2 and np.percentile(dev, 90) <= 1e-1

@@ -10,7 +10,8 @@ import pytest
 
 import oracle
 import workloads as W
-from gpu_util import host, inputs, oracle_full, rel_fro, row_rel_errors, run_ops, to_device
+from gpu_util import (assert_same_up_to_sum_order, host, inputs, oracle_full, rel_fro, row_rel_errors, run_ops,
+                      to_device)
 
 pytestmark = pytest.mark.gpu
 
@@ -370,12 +371,23 @@ def test_separate_passes_equal_the_fused_call(dtype, gproj):
 
 
 def test_deterministic():
+    """Every output is the same bits on every run, except the dQ of the single-pass bf16
+    backward (d <= 64, no GProj), whose fp32 accumulator adds the key blocks' partial
+    sums in the order they arrive: that one is the same up to that order.  With GProj
+    (two passes) dQ is the same bits too."""
     w = W.GPT2_LAYER.with_n(512)
     xd = to_device(inputs(w), w)
     a = run_ops(w, xd)
     b = run_ops(w, xd)
     for k in a:
-        assert np.array_equal(host(a[k]), host(b[k])), k
+        if k == "dQ":
+            assert_same_up_to_sum_order(a[k], b[k], k)
+        else:
+            assert np.array_equal(host(a[k]), host(b[k])), k
+    a1 = run_ops(w, xd, ops=("bwd",), gproj=1)
+    b1 = run_ops(w, xd, ops=("bwd",), gproj=1)
+    for k in ("dQ", "dK", "dV"):
+        assert np.array_equal(host(a1[k]), host(b1[k])), k
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -390,7 +402,8 @@ def test_result_does_not_depend_on_workspace_content(N, dtype):
     w = W.Workload(f"wsfill_B2H3N{N}d64_{dtype}", 2, 3, N, 64, dtype)
     x = to_device(inputs(w), w)
     O, lse = fbd.attn_fwd(x["Q"], x["K"], x["V"])
-    nbytes = max(fbd.attn_bwd_workspace_bytes(fbd.make_desc(x["Q"]), 1), fbd.attn_bob_workspace_bytes(fbd.make_desc(x["Q"])))
+    nbytes = max(fbd.attn_bwd_workspace_bytes(fbd.make_desc(x["Q"]), 0), fbd.attn_bwd_workspace_bytes(fbd.make_desc(x["Q"]), 1),
+                 fbd.attn_bob_workspace_bytes(fbd.make_desc(x["Q"])))
 
     def run(fill):
         ws = torch.full((nbytes // 4,), fill, dtype=torch.float32, device="cuda").view(torch.uint8)
@@ -400,9 +413,12 @@ def test_result_does_not_depend_on_workspace_content(N, dtype):
         fbd.attn_device_status()
         return outs
 
-    for a, b in zip(run(0.0), run(float("nan"))):
+    for n, (a, b) in enumerate(zip(run(0.0), run(float("nan")))):
         assert not torch.isnan(b).any()
-        assert torch.equal(a, b)
+        if n == 0 and dtype == "bf16":  # single-pass dQ: the same up to its summation order
+            assert_same_up_to_sum_order(a, b, "dQ")
+        else:
+            assert torch.equal(a, b)
 
 
 
@@ -441,7 +457,8 @@ def test_noncausal_edge_sizes(N, d, dtype):
 
 def test_noncausal_differs_from_causal_and_passes_compose():
     """The mask flag reaches the kernels (the outputs differ), and the separate row and
-    column passes give the fused call's bits without the causal mask too."""
+    column passes give the one-call results without the causal mask too (dQ up to the
+    summation order of the single-pass backward)."""
     import torch
 
     import fwd_bwd_double_gb300 as fbd
@@ -453,7 +470,7 @@ def test_noncausal_differs_from_causal_and_passes_compose():
     ref_b = fbd.attn_bwd(x["Q"], x["K"], x["V"], O, x["dO"], lse, causal=False)
     ref_g = fbd.attn_bob(x["Q"], x["K"], x["V"], O, x["dO"], lse, x["gdQ"], x["gdK"], x["gdV"], causal=False)
     outs = [torch.empty_like(x["Q"]) for _ in range(3)]
-    ws = torch.full((fbd.attn_bwd_workspace_bytes(fbd.make_desc(x["Q"]), 1) // 4,), float("nan"),
+    ws = torch.full((fbd.attn_bwd_workspace_bytes(fbd.make_desc(x["Q"]), 0) // 4,), float("nan"),
                     dtype=torch.float32, device="cuda").view(torch.uint8)
     for ps in (fbd.ATTN_ROW_PASS, fbd.ATTN_COL_PASS):
         fbd.attn_bwd_passes(x["Q"], x["K"], x["V"], O, x["dO"], lse, ps, dQ=outs[0], dK=outs[1], dV=outs[2],
@@ -463,7 +480,12 @@ def test_noncausal_differs_from_causal_and_passes_compose():
         fbd.attn_bob_passes(x["Q"], x["K"], x["V"], O, x["dO"], lse, x["gdQ"], x["gdK"], x["gdV"], ps,
                             gQ=gouts[0], gK=gouts[1], gV=gouts[2], gdO=gouts[3], workspace=ws, causal=False)
     fbd.attn_device_status()
-    for a, b in zip(outs + gouts, list(ref_b) + list(ref_g)):
+    # The backward's two separate passes against the single-pass form of attn_bwd: dQ is
+    # summed in another order and dK's product reads dS from shared memory instead of TMEM,
+    # so they agree up to the order of the fp32 roundings; the BoB outputs are the same bits.
+    for n, k in enumerate(("dQ", "dK", "dV")):
+        assert_same_up_to_sum_order(outs[n], ref_b[n], k)
+    for a, b in zip(gouts, list(ref_g)):
         assert torch.equal(a, b)
 
 
@@ -519,7 +541,10 @@ def test_gqa_row_outputs_equal_repeated_heads_bitwise(dtype):
         assert torch.equal(O, Or) and torch.equal(lse, lser)
         dQ, dK, dV = fbd.attn_bwd(x["Q"], x["K"], x["V"], O, x["dO"], lse, causal=causal)
         dQr, dKr, dVr = fbd.attn_bwd(rep["Q"], rep["K"], rep["V"], O, x["dO"], lse, causal=causal)
-        assert torch.equal(dQ, dQr)
+        if dtype == "bf16":  # the single-pass accumulator: the same up to its summation order
+            assert_same_up_to_sum_order(dQ, dQr, "dQ")
+        else:
+            assert torch.equal(dQ, dQr)
         assert dK.shape == x["K"].shape
         g = fbd.attn_bob(x["Q"], x["K"], x["V"], O, x["dO"], lse, x["gdQ"], x["gdK"], x["gdV"], causal=causal)
         gr = fbd.attn_bob(rep["Q"], rep["K"], rep["V"], O, x["dO"], lse, x["gdQ"], rep["gdK"], rep["gdV"],
@@ -644,8 +669,11 @@ def test_window_passes_compose_on_nan_workspace(d):
             fbd.attn_bob_passes(x["Q"], x["K"], x["V"], O, x["dO"], lse, x["gdQ"], x["gdK"], x["gdV"], ps,
                                 gQ=g[0], gK=g[1], gV=g[2], gdO=g[3], workspace=ws, desc=desc, gproj=gp)
         fbd.attn_device_status()
-        for a, r in zip(b + g, list(ref_b) + list(ref_g)):
-            assert torch.equal(a, r)
+        for n, (a, r) in enumerate(zip(b + g, list(ref_b) + list(ref_g))):
+            if n < 3 and gp == 0 and d <= 64:  # the separate passes vs the single-pass form
+                assert_same_up_to_sum_order(a, r, ("dQ", "dK", "dV")[n])
+            else:
+                assert torch.equal(a, r)
 
 
 # The forward at d = 256 runs on tensor cores with 64-key blocks (the backward and BoB
