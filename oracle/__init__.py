@@ -14,5 +14,5 @@ closed-form special cases and invariants); see ``tests/test_oracle_pins.py``.
 from .attention import (  # noqa: F401
     backward, backward_all, backward_bf16_dS, backward_cols, backward_rows, bf16_round, bob,
     bob_all, bob_bf16_dS, bob_bf16_dS_all, bob_col_pass, bob_cols, bob_row_pass, bob_rows, default_scale, forward, forward_all,
-    forward_online, forward_rows, hidden, scores, softmax_rows, Window,
+    forward_online, forward_rows, hidden, scores, Segments, SegmentsBatch, softmax_rows, Window,
 )

@@ -70,9 +70,44 @@ class Window:
         return hash(("Window", self.W))
 
 
+class Segments:
+    """Document (segment) mask over one sequence: key j is visible to query i iff j <= i
+    and the two tokens carry the same segment id, seg[j] == seg[i] (packed documents
+    attend only within their own document); with W > 0 the causal window i - W < j
+    applies as well.
+
+    A second flexible mask beside the window (the FlashBoB page, "When FlashBoB changes
+    the engineering plan", names flexible masks among the next extensions): the ids of
+    a packed batch row are non-decreasing, each document one run, so every row keeps
+    its own key and its visible keys form one contiguous range.  Accepted wherever
+    `causal` is, for one (batch, head) slice; ``SegmentsBatch`` carries the ids of
+    every batch row for the batched helpers."""
+
+    def __init__(self, seg, W: int = 0):
+        self.seg = np.asarray(seg, dtype=np.int64).reshape(-1)
+        if int(W) < 0:
+            raise ValueError("window must be >= 0")
+        self.W = int(W)
+
+    def __repr__(self):
+        return f"Segments(n={len(self.seg)}, W={self.W})"
+
+
+class SegmentsBatch:
+    """Segment ids [B, N] of a batch: slice (b, h) uses ``Segments(seg[b], W)``."""
+
+    def __init__(self, seg, W: int = 0):
+        self.seg = np.asarray(seg, dtype=np.int64)
+        self.W = int(W)
+
+    def for_batch(self, b):
+        return Segments(self.seg[b], self.W)
+
+
 def hidden(rows, keys, causal):
     """Boolean [len(rows), len(keys)]: True where the key is masked for the row
-    (causal: j > i; a Window also masks j <= i - W; causal=False masks nothing)."""
+    (causal: j > i; a Window also masks j <= i - W; Segments also masks keys of another
+    segment; causal=False masks nothing)."""
     r = np.asarray(rows)[:, None]
     k = np.asarray(keys)[None, :]
     if not causal:
@@ -80,6 +115,10 @@ def hidden(rows, keys, causal):
     m = k > r
     if isinstance(causal, Window):
         m |= k <= r - causal.W
+    if isinstance(causal, Segments):
+        m |= causal.seg[k] != causal.seg[r]
+        if causal.W:
+            m |= k <= r - causal.W
     return m
 
 
@@ -568,8 +607,11 @@ def _each_slice(fn, *tensors, **kw):
     B, H = tensors[0].shape[:2]
     outs = None
     for bb in range(B):
+        kb = dict(kw)
+        if hasattr(kw.get("causal"), "for_batch"):  # per-batch segment ids
+            kb["causal"] = kw["causal"].for_batch(bb)
         for hh in range(H):
-            r = fn(*(t[bb, hh] for t in tensors), **kw)
+            r = fn(*(t[bb, hh] for t in tensors), **kb)
             if outs is None:
                 outs = {k: np.empty((B, H) + np.shape(v)) for k, v in r.items()
                         if isinstance(v, np.ndarray)}

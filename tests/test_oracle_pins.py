@@ -829,3 +829,176 @@ def test_window_bob_gproj_projection():
     exact = oracle.bob(Q, K, V, dO, a, b + 7.0, c, causal=w)
     plain = oracle.bob_bf16_dS(Q, K, V, dO, a, b + 7.0, c, False, causal=w)
     assert rel(proj["gQ"], exact["gQ"]) < rel(plain["gQ"], exact["gQ"])
+
+
+# ------------------------------------------------------ document (segment) mask ----
+# Query i sees key j iff j <= i and seg[j] == seg[i] (packed documents), optionally also
+# inside a window.  The strongest pin: the mask is block diagonal over the documents, so
+# every output restricted to one document equals plain causal attention run on that
+# document alone -- a different code path (sub-arrays, no segment logic at all).
+
+def brute_forward_segments(Q, K, V, scale, seg, W=0):
+    """Pure-Python loops over the definition with the document mask."""
+    N, d = len(Q), len(Q[0])
+    O = [[0.0] * d for _ in range(N)]
+    L = [0.0] * N
+    for i in range(N):
+        js = [j for j in range(N) if j <= i and seg[j] == seg[i] and (W == 0 or j > i - W)]
+        s = [scale * sum(Q[i][t] * K[j][t] for t in range(d)) for j in js]
+        m = max(s)
+        e = [math.exp(x - m) for x in s]
+        tot = sum(e)
+        L[i] = m + math.log(tot)
+        for t in range(d):
+            O[i][t] = sum(e[u] / tot * V[js[u]][t] for u in range(len(js)))
+    return O, L
+
+
+SEGS = [np.array([0, 0, 0, 1, 1, 2, 2, 2, 2, 3, 4, 4, 4, 4, 4, 4, 5]),
+        np.array([7] * 5 + [9] * 11 + [12])]
+
+
+@pytest.mark.parametrize("seg", SEGS)
+@pytest.mark.parametrize("W", [0, 3])
+def test_segments_forward_brute_force(seg, W):
+    N, d = len(seg), 5
+    Q, K, V = rnd(201, N, d), rnd(202, N, d), rnd(203, N, d)
+    Ob, Lb = brute_forward_segments(Q.tolist(), K.tolist(), V.tolist(), 0.41, seg.tolist(), W)
+    O, L = oracle.forward(Q, K, V, scale=0.41, causal=oracle.Segments(seg, W))
+    assert rel(O, Ob) <= 1e-13 and rel(L, Lb) <= 1e-13
+
+
+def _runs(seg):
+    cut = np.flatnonzero(np.diff(seg)) + 1
+    return np.split(np.arange(len(seg)), cut)
+
+
+@pytest.mark.parametrize("W", [0, 4])
+def test_segments_are_block_diagonal(W):
+    seg = np.repeat(np.arange(6), [1, 9, 4, 13, 2, 8])  # 37 tokens, runs of 1 .. 13
+    N, d = len(seg), 6
+    Q, K, V, dO, a, b, c = slice_set(N, d, 204)
+    m = oracle.Segments(seg, W)
+    f = oracle.forward(Q, K, V, causal=m)
+    g = oracle.backward(Q, K, V, dO, causal=m)
+    h = oracle.bob(Q, K, V, dO, a, b, c, causal=m)
+    for r in _runs(seg):
+        sub = lambda X: X[r]
+        cm = oracle.Window(W) if W else True
+        fr = oracle.forward(sub(Q), sub(K), sub(V), causal=cm)
+        gr = oracle.backward(sub(Q), sub(K), sub(V), sub(dO), causal=cm)
+        hr = oracle.bob(sub(Q), sub(K), sub(V), sub(dO), sub(a), sub(b), sub(c), causal=cm)
+        assert rel(f[0][r], fr[0]) <= 1e-13 and rel(f[1][r], fr[1]) <= 1e-13
+        for k in ("dQ", "dK", "dV"):
+            assert rel(g[k][r], gr[k]) <= 1e-12, k
+        for k in ("gQ", "gK", "gV", "gdO"):
+            assert rel(h[k][r], hr[k]) <= 1e-12, k
+
+
+def test_segments_limits():
+    """One segment is the causal mask (bit for bit); one token per segment leaves each row
+    its own key only: O = V, lse = s q.k, dQ = dK = 0, dV = dO, gQ = gK = gV = 0, gdO = c."""
+    N, d = 21, 4
+    Q, K, V, dO, a, b, c = slice_set(N, d, 205)
+    one = oracle.Segments(np.zeros(N, int))
+    for f in (lambda m: oracle.forward(Q, K, V, causal=m)[0], lambda m: oracle.backward(Q, K, V, dO, causal=m)["dK"],
+              lambda m: oracle.bob(Q, K, V, dO, a, b, c, causal=m)["gK"]):
+        assert np.array_equal(f(one), f(True))
+    each = oracle.Segments(np.arange(N))
+    O, L = oracle.forward(Q, K, V, scale=0.5, causal=each)
+    assert rel(O, V) <= 1e-15 and rel(L, 0.5 * (Q * K).sum(axis=1)) <= 1e-15
+    g = oracle.backward(Q, K, V, dO, causal=each)
+    assert np.abs(g["dQ"]).max() == 0 and np.abs(g["dK"]).max() == 0 and rel(g["dV"], dO) <= 1e-15
+    h = oracle.bob(Q, K, V, dO, a, b, c, causal=each)
+    assert max(np.abs(h[k]).max() for k in ("gQ", "gK", "gV")) <= 1e-14 and rel(h["gdO"], c) <= 1e-15
+
+
+@pytest.mark.parametrize("Br,Bc", [(1, 1), (3, 5), (16, 16), (7, 33)])
+def test_segments_online_softmax_equals_two_pass(Br, Bc):
+    seg = np.repeat(np.arange(5), [6, 1, 12, 3, 11])
+    N, d = len(seg), 5
+    Q, K, V = rnd(206, N, d), rnd(207, N, d), rnd(208, N, d)
+    m = oracle.Segments(seg, 5)
+    O1, L1 = oracle.forward_online(Q, K, V, Br, Bc, causal=m)
+    O2, L2 = oracle.forward(Q, K, V, causal=m)
+    assert rel(O1, O2) <= 1e-13 and rel(L1, L2) <= 1e-13
+
+
+def test_segments_backward_fd_and_bob_hvp_jvp():
+    seg = np.array([0, 0, 0, 1, 1, 1, 1, 2, 3, 3, 3])
+    N, d = len(seg), 4
+    Q, K, V, dO, a, b, c = (x * 0.8 for x in slice_set(N, d, 209))
+    s, h, m = 0.6, 1e-5, oracle.Segments(seg)
+    g = oracle.backward(Q, K, V, dO, scale=s, causal=m)
+    top = 0.0
+    fds = []
+    for k, X in (("dQ", 0), ("dK", 1), ("dV", 2)):
+        def f(Y, X=X):
+            args = [Q, K, V]
+            args[X] = Y
+            O, _ = oracle.forward(*args, scale=s, causal=m)
+            return float((O * dO).sum())
+        fd = fd_grad(f, (Q, K, V)[X])
+        fds.append((k, fd))
+        top = max(top, np.abs(fd).max())
+    for k, fd in fds:
+        assert np.abs(g[k] - fd).max() <= 1e-8 * max(top, 1e-3), k
+    out = oracle.bob(Q, K, V, dO, a, b, c, scale=s, causal=m)
+
+    def gr(Q, K, V):
+        x = oracle.backward(Q, K, V, dO, scale=s, causal=m)
+        return x["dQ"], x["dK"], x["dV"]
+    gp, gm = gr(Q + h * a, K + h * b, V + h * c), gr(Q - h * a, K - h * b, V - h * c)
+    fd = [(p_ - m_) / (2 * h) for p_, m_ in zip(gp, gm)]
+    top = max(np.abs(x).max() for x in fd)
+    for name, want in zip(("gQ", "gK", "gV"), fd):
+        assert np.abs(out[name] - want).max() <= 1e-8 * max(top, 1e-3), name
+    Op, _ = oracle.forward(Q + h * a, K + h * b, V + h * c, scale=s, causal=m)
+    Om, _ = oracle.forward(Q - h * a, K - h * b, V - h * c, scale=s, causal=m)
+    jvp = (Op - Om) / (2 * h)
+    assert np.abs(out["gdO"] - jvp).max() <= 1e-8 * max(np.abs(jvp).max(), 1e-3)
+
+
+def test_segments_streaming_passes_and_sampling():
+    seg = np.repeat(np.arange(4), [10, 3, 15, 7])
+    N, d = len(seg), 5
+    Q, K, V, dO, a, b, c = slice_set(N, d, 210)
+    m = oracle.Segments(seg, 9)
+    ref = oracle.bob(Q, K, V, dO, a, b, c, causal=m)
+    O, L = oracle.forward(Q, K, V, causal=m)
+    row = oracle.bob_row_pass(Q, K, V, dO, a, b, c, O, L, 6, causal=m)
+    gK, gV = oracle.bob_col_pass(Q, K, V, dO, a, b, c, L, row["D"], row["E"], row["F"], 5, causal=m)
+    for got, want in ((row["gQ"], ref["gQ"]), (row["gdO"], ref["gdO"]), (gK, ref["gK"]), (gV, ref["gV"])):
+        assert rel(got, want) <= 1e-12
+    rows, cols = np.array([0, 34, 12, 13]), np.array([0, 20, 34])
+    r = oracle.bob_rows(Q, K, V, dO, a, b, c, rows, causal=m)
+    assert rel(r["gQ"], ref["gQ"][rows]) <= 1e-13 and rel(r["gdO"], ref["gdO"][rows]) <= 1e-13
+    gKc, gVc = oracle.bob_cols(Q, K, V, dO, a, b, c, cols, causal=m)
+    assert rel(gKc, ref["gK"][cols]) <= 1e-13 and rel(gVc, ref["gV"][cols]) <= 1e-13
+
+
+def test_segments_batched_helpers_use_each_rows_ids():
+    seg = np.array([np.repeat([0, 1], [5, 9]), np.repeat([3, 4, 5], [2, 2, 10])])
+    B, H, N, d = 2, 2, 14, 4
+    r = np.random.default_rng(211)
+    X = [r.standard_normal((B, H, N, d)) for _ in range(4)]
+    out = oracle.backward_all(*X, causal=oracle.SegmentsBatch(seg))
+    for bb in range(B):
+        for hh in range(H):
+            g = oracle.backward(*(x[bb, hh] for x in X), causal=oracle.Segments(seg[bb]))
+            assert np.array_equal(out["dQ"][bb, hh], g["dQ"]) and np.array_equal(out["dK"][bb, hh], g["dK"])
+
+
+def test_planted_mistake_segments_ignored_in_backward_is_caught(monkeypatch):
+    """A backward that drops the segment test (but keeps it in the forward) breaks the
+    block-diagonal pin."""
+    seg = np.repeat(np.arange(3), [4, 6, 5])
+    N, d = len(seg), 4
+    Q, K, V, dO = slice_set(N, d, 212)[:4]
+    real = A.hidden
+    monkeypatch.setattr(A, "hidden", lambda rows, keys, causal: real(rows, keys, True if isinstance(causal, A.Segments) else causal))
+    g = oracle.backward(Q, K, V, dO, causal=oracle.Segments(seg))
+    monkeypatch.setattr(A, "hidden", real)
+    r = _runs(seg)[1]
+    gr = oracle.backward(Q[r], K[r], V[r], dO[r])
+    assert rel(g["dQ"][r], gr["dQ"]) > 1e-3

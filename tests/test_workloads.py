@@ -70,3 +70,14 @@ def test_grouped_heads_draw_key_side_tensors_per_key_value_head():
     import pytest
     with pytest.raises(ValueError):
         W.inputs(w, heads=[0])
+
+
+def test_segment_ids_are_runs_of_the_stated_lengths():
+    s = W.segment_ids(3, 5000, 64, seed=1)
+    assert s.shape == (3, 5000) and s.dtype == np.int32
+    assert np.all(np.diff(s, axis=1) >= 0) and np.all(s[:, 0] == 0)
+    for b in range(3):
+        lens = np.bincount(s[b])
+        assert np.all(lens[:-1] >= 1) and np.all(lens[:-1] <= 127) and 40 < lens[:-1].mean() < 90
+    assert np.array_equal(s, W.segment_ids(3, 5000, 64, seed=1))
+    assert not np.array_equal(s[0], s[1])

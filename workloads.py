@@ -32,6 +32,7 @@ _TID = {name: i for i, name in enumerate(TENSORS)}
 _TID_SHARED_MEAN = 100  # per-head shared key mean of the large-key workload
 _TID_PERM = 101         # per-slice earlier-position draw of the large-key workload
 _TID_QNOISE = 102       # per-slice query noise of the large-key workload
+_TID_SEGMENTS = 103     # per-batch-row document lengths of the document-mask workloads
 
 
 @dataclasses.dataclass(frozen=True)
@@ -143,4 +144,21 @@ def inputs(w: Workload, names=TENSORS, heads=None, batches=None) -> dict:
             s = slice_inputs(w, b, h, here)
             for n in here:
                 out[n][bi, hi] = s[n]
+    return out
+
+
+def segment_ids(B: int, N: int, mean_len: int, seed: int = 0) -> np.ndarray:
+    """Document ids [B, N] int32 of a packed batch: each row is cut into documents of
+    random lengths drawn uniformly from 1 .. 2 mean_len - 1 (the last one clipped at N),
+    numbered 0, 1, 2, ... along the row, so the ids are non-decreasing and each document
+    is one run.  Only random draws: no attention arithmetic."""
+    out = np.empty((B, N), dtype=np.int32)
+    for b in range(B):
+        r = _rng(seed, (_TID_SEGMENTS, b, 0))
+        pos, doc = 0, 0
+        while pos < N:
+            n = int(r.integers(1, 2 * mean_len))
+            out[b, pos:pos + n] = doc
+            pos += n
+            doc += 1
     return out
