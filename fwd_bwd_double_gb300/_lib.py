@@ -30,7 +30,8 @@ class FbdError(RuntimeError):
 class AttnDesc(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int64), ("H", ctypes.c_int64), ("N", ctypes.c_int64), ("d", ctypes.c_int64),
                 ("scale", ctypes.c_float), ("causal", ctypes.c_int32), ("dtype", ctypes.c_int32),
-                ("group", ctypes.c_int32), ("window", ctypes.c_int32)]
+                ("group", ctypes.c_int32), ("window", ctypes.c_int32), ("seg_lo", ctypes.c_void_p),
+                ("seg_hi", ctypes.c_void_p)]
 
 
 _P = ctypes.c_void_p
@@ -46,6 +47,7 @@ PROTOTYPES = {
     "attn_bob_passes": (ctypes.c_int, [_D] + [_P] * 13 + [ctypes.c_int, _P, ctypes.c_size_t, ctypes.c_int, _P]),
     "attn_bob_static": (ctypes.c_int, [_D] + [_P] * 13 + [_P]),
     "attn_bwd_projected_dS": (ctypes.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "attn_segment_bounds": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, _P, _P, _P, _P]),
     "attn_device_status": (ctypes.c_int, [_P]),
     "attn_check_wait_timeout": (ctypes.c_int, [_P]),
     "attn_status_string": (ctypes.c_char_p, [ctypes.c_int]),

@@ -8,6 +8,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
 
 #include "fbd.h"
@@ -41,6 +42,10 @@ attn_status_t check_desc(const attn_desc_t* desc, fbd::Problem& p) {
   if (desc->window < 0) return fail(ATTN_ERR_INVALID_ARG, "window must be >= 0%s");
   if (desc->window > 0 && desc->causal != 1)
     return fail(ATTN_ERR_UNSUPPORTED, "a window needs the causal mask (causal = 1)%s");
+  if ((desc->seg_lo == nullptr) != (desc->seg_hi == nullptr))
+    return fail(ATTN_ERR_INVALID_ARG, "seg_lo and seg_hi must both be set or both be NULL%s");
+  if (desc->seg_lo != nullptr && desc->causal != 1)
+    return fail(ATTN_ERR_UNSUPPORTED, "a document mask needs the causal mask (causal = 1)%s");
   if (desc->d != 32 && desc->d != 64 && desc->d != 96 && desc->d != 128 && desc->d != 256)
     return fail(ATTN_ERR_UNSUPPORTED, "head dim must be 32, 64, 96, 128 or 256%s");
   if (desc->dtype != ATTN_F32 && desc->dtype != ATTN_BF16) return fail(ATTN_ERR_UNSUPPORTED, "unknown dtype%s");
@@ -64,6 +69,8 @@ attn_status_t check_desc(const attn_desc_t* desc, fbd::Problem& p) {
   p.group = static_cast<int>(g);
   p.BHkv = p.BH / g;
   p.window = desc->window > 0 && desc->window < desc->N ? desc->window : 0;  // W >= N: the causal mask
+  p.seg_lo = desc->seg_lo;
+  p.seg_hi = desc->seg_hi;
   if (p.BH >= lim) return fail(ATTN_ERR_INVALID_ARG, "B*H must be < 2^31%s");
   if (((p.N + 7) / 8) * p.BH >= lim) return fail(ATTN_ERR_INVALID_ARG, "B*H*N too large for one launch%s");
   return ATTN_OK;
@@ -94,6 +101,20 @@ Span span(const char* name, const void* ptr, size_t bytes) {
   const uintptr_t lo = reinterpret_cast<uintptr_t>(ptr);
   return Span{name, lo, lo + bytes};
 }
+
+// The inputs of an entry point, with the document bounds appended when they are given.
+struct Inputs {
+  Span s[13];
+  int n = 0;
+  Inputs(std::initializer_list<Span> l, const fbd::Problem& p) {
+    for (const Span& x : l) s[n++] = x;
+    if (p.seg_lo != nullptr) {
+      const size_t b = static_cast<size_t>(p.B * p.N) * sizeof(int);
+      s[n++] = span("seg_lo", p.seg_lo, b);
+      s[n++] = span("seg_hi", p.seg_hi, b);
+    }
+  }
+};
 
 attn_status_t launch_status(cudaError_t e) {
   if (e == cudaSuccess) return ATTN_OK;
@@ -138,9 +159,9 @@ attn_status_t attn_fwd(const attn_desc_t* desc, const void* Q, const void* K, co
   if (p.BH * p.N == 0) return ATTN_OK;
   const size_t tb = static_cast<size_t>(p.BH * p.N * p.d) * elem_size(p), sb = p.BH * p.N * sizeof(float);
   const size_t kb = kv_bytes(p);
-  const Span in[] = {span("Q", Q, tb), span("K", K, kb), span("V", V, kb)};
+  const Inputs in({span("Q", Q, tb), span("K", K, kb), span("V", V, kb)}, p);
   const Span out[] = {span("O", O, tb), span("lse", lse, sb)};
-  if ((s = check_ptrs(in, 3, out, 2)) != ATTN_OK) return s;
+  if ((s = check_ptrs(in.s, in.n, out, 2)) != ATTN_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (!tc_path(p, 0)) return launch_status(fbd::simt_fwd(p, Q, K, V, O, lse, st));
   return launch_status(fbd::tc_fwd(p, Q, K, V, O, lse, st));
@@ -189,11 +210,11 @@ attn_status_t attn_bwd_passes(const attn_desc_t* desc, const void* Q, const void
     return fail(ATTN_ERR_WORKSPACE, "workspace NULL or smaller than attn_bwd_workspace_bytes()%s");
   const size_t tb = static_cast<size_t>(p.BH * p.N * p.d) * elem_size(p), sb = p.BH * p.N * sizeof(float);
   const size_t kb = kv_bytes(p);
-  const Span in[] = {span("Q", Q, tb), span("K", K, kb), span("V", V, kb),
-                     span("O", O, tb), span("dO", dO, tb), span("lse", lse, sb)};
+  const Inputs in({span("Q", Q, tb), span("K", K, kb), span("V", V, kb), span("O", O, tb), span("dO", dO, tb),
+                   span("lse", lse, sb)}, p);
   const Span out[] = {span("dQ", dQ, tb), span("dK", dK, kb), span("dV", dV, kb),
                       span("workspace", workspace, need)};
-  if ((s = check_ptrs(in, 6, out, 4)) != ATTN_OK) return s;
+  if ((s = check_ptrs(in.s, in.n, out, 4)) != ATTN_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   float4* ws = static_cast<float4*>(workspace);
   if (!tc_path(p, 1))
@@ -226,12 +247,11 @@ attn_status_t attn_bob_passes(const attn_desc_t* desc, const void* Q, const void
     return fail(ATTN_ERR_WORKSPACE, "workspace NULL or smaller than attn_bob_workspace_bytes()%s");
   const size_t tb = static_cast<size_t>(p.BH * p.N * p.d) * elem_size(p), sb = p.BH * p.N * sizeof(float);
   const size_t kb = kv_bytes(p);
-  const Span in[] = {span("Q", Q, tb),     span("K", K, kb),     span("V", V, kb),
-                     span("O", O, tb),     span("dO", dO, tb),   span("lse", lse, sb),
-                     span("gdQ", gdQ, tb), span("gdK", gdK, kb), span("gdV", gdV, kb)};
+  const Inputs in({span("Q", Q, tb), span("K", K, kb), span("V", V, kb), span("O", O, tb), span("dO", dO, tb),
+                   span("lse", lse, sb), span("gdQ", gdQ, tb), span("gdK", gdK, kb), span("gdV", gdV, kb)}, p);
   const Span out[] = {span("gQ", gQ, tb), span("gK", gK, kb), span("gV", gV, kb), span("gdO", gdO, tb),
                       span("workspace", workspace, need)};
-  if ((s = check_ptrs(in, 9, out, 5)) != ATTN_OK) return s;
+  if ((s = check_ptrs(in.s, in.n, out, 5)) != ATTN_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   float4* ws = static_cast<float4*>(workspace);
   if (!tc_path(p, 2))
@@ -261,11 +281,25 @@ attn_status_t attn_bwd_projected_dS(const attn_desc_t* desc, const void* Q, cons
   const size_t tb = static_cast<size_t>(p.BH * p.N * p.d) * 2, sb = p.BH * p.N * sizeof(float);
   const size_t ob = static_cast<size_t>(p.BH) * p.N * p.N * sizeof(float);
   const size_t kb = static_cast<size_t>(p.BHkv * p.N * p.d) * 2;
-  const Span in[] = {span("Q", Q, tb), span("K", K, kb), span("V", V, kb),
-                     span("O", O, tb), span("dO", dO, tb), span("lse", lse, sb)};
+  const Inputs in({span("Q", Q, tb), span("K", K, kb), span("V", V, kb), span("O", O, tb), span("dO", dO, tb),
+                   span("lse", lse, sb)}, p);
   const Span out[] = {span("dS_out", dS_out, ob)};
-  if ((s = check_ptrs(in, 6, out, 1)) != ATTN_OK) return s;
+  if ((s = check_ptrs(in.s, in.n, out, 1)) != ATTN_OK) return s;
   return launch_status(fbd::simt_projected_dS(p, Q, K, V, O, dO, lse, dS_out, static_cast<cudaStream_t>(stream)));
+}
+
+attn_status_t attn_segment_bounds(int64_t B, int64_t N, const int32_t* seg, int32_t* seg_lo, int32_t* seg_hi,
+                                  void* stream) {
+  if (B < 0 || N < 0) return fail(ATTN_ERR_INVALID_ARG, "negative B or N%s");
+  if (N >= (int64_t(1) << 31) || B >= (int64_t(1) << 31) || (B > 0 && N > (int64_t(1) << 40) / B))
+    return fail(ATTN_ERR_INVALID_ARG, "B and N must each be < 2^31 and B*N < 2^40%s");
+  if (B * N == 0) return ATTN_OK;
+  const size_t b = static_cast<size_t>(B * N) * sizeof(int32_t);
+  const Span in[] = {span("seg", seg, b)};
+  const Span out[] = {span("seg_lo", seg_lo, b), span("seg_hi", seg_hi, b)};
+  attn_status_t s = check_ptrs(in, 1, out, 2);
+  if (s != ATTN_OK) return s;
+  return launch_status(fbd::segment_bounds(B, N, seg, seg_lo, seg_hi, static_cast<cudaStream_t>(stream)));
 }
 
 attn_status_t attn_device_status(void* stream) {

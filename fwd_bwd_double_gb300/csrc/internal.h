@@ -19,7 +19,44 @@ struct Problem {
   int64_t BHkv;   // B * H / group key/value slices; query slice bh reads slice bh / group
   int64_t window; // causal sliding window W (key j visible to row i iff i - W < j <= i), 1 <= W < N;
                   // 0: none (also when the caller's W >= N, which is the plain causal mask)
+  const int* seg_lo;  // document mask: first key of each row's document, [B][N] (nullptr: none)
+  const int* seg_hi;  // ... last row of each key's document, [B][N]
 };
+
+// A banded causal mask is in force: the window, the document bounds, or both.
+inline bool banded(const Problem& p) { return p.window > 0 || p.seg_lo != nullptr; }
+
+// The banded causal mask as the kernels take it (by value): row i sees the keys
+// lo(i) <= j <= i and key j is seen by the rows j <= i <= hi(j), with
+// lo(i) = max(i - W + 1, seg_lo[i], 0) and hi(j) = min(j + W - 1, seg_hi[j], N - 1), each
+// term only where given.  A slice index s (query slice in row passes, key/value slice in
+// column passes) belongs to batch row s / hpb.  Positions past N are looked up at N - 1.
+struct Band {
+  int64_t N;
+  int64_t win;   // W, or larger than N plus a block when there is no window
+  int64_t hpb;   // slices per batch row of the slice index the kernel holds
+  const int* lo;
+  const int* hi;
+  __device__ __forceinline__ int row_lo(int64_t slice, int64_t i) const {
+    int64_t l = i - win + 1;
+    if (lo != nullptr) {
+      const int64_t v = lo[(slice / hpb) * N + (i < N ? i : N - 1)];
+      l = l > v ? l : v;
+    }
+    return static_cast<int>(l > 0 ? l : 0);
+  }
+  __device__ __forceinline__ int key_hi(int64_t slice, int64_t j) const {
+    int64_t h = j + win - 1;
+    if (hi != nullptr) {
+      const int64_t v = hi[(slice / hpb) * N + (j < N ? j : N - 1)];
+      h = h < v ? h : v;
+    }
+    return static_cast<int>(h < N - 1 ? h : N - 1);
+  }
+};
+inline Band make_band(const Problem& p, int64_t win, bool kv_slices) {
+  return Band{p.N, win, kv_slices ? p.BHkv / p.B : p.H, p.seg_lo, p.seg_hi};
+}
 
 // The window as the kernels take it: W, or N + 1 when there is none (then i - W + 1 <= 0
 // and j + W > N for every row i and key j, so the window bounds never bind).
@@ -39,6 +76,10 @@ cudaError_t simt_bob(const Problem& p, const void* Q, const void* K, const void*
                      void* gK, void* gV, void* gdO, bool gproj, float4* ws, int passes, cudaStream_t st);
 cudaError_t simt_projected_dS(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
                               const void* dO, const float* lse, float* dS, cudaStream_t st);
+
+// Document bounds from segment ids (mask.cu): lo[b][i] = first index of i's run of equal
+// ids, hi[b][j] = last index of j's run (binary searches; ids non-decreasing along N).
+cudaError_t segment_bounds(int64_t B, int64_t N, const int* seg, int* lo, int* hi, cudaStream_t st);
 
 // bf16 tensor-core path (tcgen05 + TMA).  Return cudaErrorInvalidValue if a
 // tensor map could not be encoded.

@@ -110,7 +110,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) fwd_kernel(const T* __restrict__ Q, const T* __restrict__ K,
                                                        const T* __restrict__ Vt, T* __restrict__ O,
                                                        float* __restrict__ lse, int64_t N, int64_t BH,
-                                                       float scale, int causal, int64_t W, int64_t G) {
+                                                       float scale, int causal, Band bd, int64_t G) {
   constexpr int V = D / 32;
   extern __shared__ float sm[];
   float* Ks = sm;
@@ -128,8 +128,9 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(const T* __restrict__ Q, 
   if (live) load_vec(Q + base + i * D, lane, q);
   float m = -CUDART_INF_F, l = 0.f;  // running max of raw dot products, running sum
   const int64_t last = causal ? min(row0 + kWarps, N) - 1 : N - 1;  // last key any row of the block sees
-  // W: the causal window (key j visible to row i iff i - W < j <= i; N + 1 when there is none)
-  const int64_t first = causal ? (lmax(0, row0 - W + 1) / kTile) * kTile : 0;  // first key tile any row sees
+  // bd: the banded causal mask (row i sees the keys bd.row_lo(i) <= j <= i)
+  const int64_t first = causal ? (bd.row_lo(tl.bh, row0) / kTile) * kTile : 0;  // first key tile any row sees
+  const int64_t lo_i = causal ? bd.row_lo(tl.bh, i) : 0;  // this row's first visible key
   for (int64_t k0 = first; k0 <= last; k0 += kTile) {
     __syncthreads();
     stage<T, D>(Ks, K + kvbase, k0, N);
@@ -137,7 +138,7 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(const T* __restrict__ Q, 
     __syncthreads();
     if (!live) continue;
     const int jn = static_cast<int>(lmin(kTile, (causal ? i + 1 : N) - k0));
-    const int jb = causal ? static_cast<int>(lmin(kTile, lmax(0, i - W + 1 - k0))) : 0;  // below the window
+    const int jb = causal ? static_cast<int>(lmin(kTile, lmax(0, lo_i - k0))) : 0;  // below the row's band
     for (int jj = jb; jj < jn; ++jj) {
       float kv[V], vv[V];
       load_smem(Ks + jj * D, lane, kv);
@@ -173,7 +174,7 @@ __global__ void __launch_bounds__(kThreads) bwd_row_kernel(const T* __restrict__
                                                            const T* __restrict__ Vt, const T* __restrict__ O,
                                                            const T* __restrict__ dO, const float* __restrict__ lse,
                                                            T* __restrict__ dQ, float4* __restrict__ ws, int64_t N,
-                                                           int64_t BH, float scale, int causal, int64_t W, int64_t G) {
+                                                           int64_t BH, float scale, int causal, Band bd, int64_t G) {
   constexpr int V = D / 32;
   extern __shared__ float sm[];
   float* Ks = sm;
@@ -200,8 +201,9 @@ __global__ void __launch_bounds__(kThreads) bwd_row_kernel(const T* __restrict__
     Li = lse[tl.bh * N + i];
   }
   const int64_t last = causal ? min(row0 + kWarps, N) - 1 : N - 1;  // last key any row of the block sees
-  // W: the causal window (key j visible to row i iff i - W < j <= i; N + 1 when there is none)
-  const int64_t first = causal ? (lmax(0, row0 - W + 1) / kTile) * kTile : 0;  // first key tile any row sees
+  // bd: the banded causal mask (row i sees the keys bd.row_lo(i) <= j <= i)
+  const int64_t first = causal ? (bd.row_lo(tl.bh, row0) / kTile) * kTile : 0;  // first key tile any row sees
+  const int64_t lo_i = causal ? bd.row_lo(tl.bh, i) : 0;  // this row's first visible key
   for (int64_t k0 = first; k0 <= last; k0 += kTile) {
     __syncthreads();
     stage<T, D>(Ks, K + kvbase, k0, N);
@@ -209,7 +211,7 @@ __global__ void __launch_bounds__(kThreads) bwd_row_kernel(const T* __restrict__
     __syncthreads();
     if (!live) continue;
     const int jn = static_cast<int>(lmin(kTile, (causal ? i + 1 : N) - k0));
-    const int jb = causal ? static_cast<int>(lmin(kTile, lmax(0, i - W + 1 - k0))) : 0;  // below the window
+    const int jb = causal ? static_cast<int>(lmin(kTile, lmax(0, lo_i - k0))) : 0;  // below the row's band
     for (int jj = jb; jj < jn; ++jj) {
       float kv[V], vv[V];
       load_smem(Ks + jj * D, lane, kv);
@@ -247,7 +249,7 @@ __global__ void __launch_bounds__(kThreads) bwd_col_kernel(const T* __restrict__
                                                            const T* __restrict__ Vt, const T* __restrict__ dO,
                                                            const float4* __restrict__ ws, T* __restrict__ dK,
                                                            T* __restrict__ dV, int64_t N, int64_t BHkv,
-                                                           float scale, int causal, int64_t W, int64_t G) {
+                                                           float scale, int causal, Band bd, int64_t G) {
   constexpr int V = D / 32;
   extern __shared__ float sm[];
   float* Qs = sm;
@@ -257,6 +259,9 @@ __global__ void __launch_bounds__(kThreads) bwd_col_kernel(const T* __restrict__
   const Tile tl = decode(BHkv, nblk, false);  // tl.bh: a key/value head; smallest key index = most rows: first
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int64_t col0 = tl.blk * kWarps, j = col0 + warp;
+  // bd: the banded causal mask (key j is seen by the rows j <= i <= bd.key_hi(j))
+  const int64_t hi_blk = causal ? bd.key_hi(tl.bh, lmin(col0 + kWarps - 1, N - 1)) : N - 1;  // last row any key sees
+  const int64_t hi_j = causal ? bd.key_hi(tl.bh, j) : N - 1;
   const bool live = j < N;
   const size_t base = static_cast<size_t>(tl.bh) * N * D;
   float kv[V], vv[V], ak[V], av[V];
@@ -268,7 +273,7 @@ __global__ void __launch_bounds__(kThreads) bwd_col_kernel(const T* __restrict__
   }
   // dK and dV of a shared head sum over the G query heads that read it.
   for (int64_t hq = tl.bh * G; hq < (tl.bh + 1) * G; ++hq)
-  for (int64_t i0 = causal ? col0 : 0; i0 < (causal ? lmin(N, col0 + kWarps - 1 + W) : N); i0 += kTile) {
+  for (int64_t i0 = causal ? col0 : 0; i0 < (causal ? hi_blk + 1 : N); i0 += kTile) {
     const size_t qbase = static_cast<size_t>(hq) * N * D;
     __syncthreads();
     stage<T, D>(Qs, Q + qbase, i0, N);
@@ -278,7 +283,7 @@ __global__ void __launch_bounds__(kThreads) bwd_col_kernel(const T* __restrict__
     __syncthreads();
     if (!live) continue;
     const int ib = causal ? static_cast<int>(lmax(0, j - i0)) : 0;  // causal: rows i >= j only
-    const int ie = static_cast<int>(lmin(kTile, (causal ? lmin(N, j + W) : N) - i0));  // rows i < j + W
+    const int ie = static_cast<int>(lmin(kTile, (causal ? hi_j + 1 : N) - i0));  // rows i <= bd.key_hi(j)
     for (int ii = ib; ii < ie; ++ii) {
       float qv[V], gv[V];
       load_smem(Qs + ii * D, lane, qv);
@@ -323,7 +328,7 @@ __global__ void __launch_bounds__(kThreads) bob_row_kernel(
     const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ Vt, const T* __restrict__ O,
     const T* __restrict__ dO, const float* __restrict__ lse, const T* __restrict__ A, const T* __restrict__ Bm,
     const T* __restrict__ C, T* __restrict__ gQ, T* __restrict__ gdO, float4* __restrict__ ws,
-    float* __restrict__ rho_ws, int64_t N, int64_t BH, float scale, int causal, int64_t W, int64_t G) {
+    float* __restrict__ rho_ws, int64_t N, int64_t BH, float scale, int causal, Band bd, int64_t G) {
   constexpr int V = D / 32;
   extern __shared__ float sm[];
   float* Ks = sm;
@@ -354,8 +359,9 @@ __global__ void __launch_bounds__(kThreads) bob_row_kernel(
     Li = lse[tl.bh * N + i];
   }
   const int64_t last = causal ? min(row0 + kWarps, N) - 1 : N - 1;  // last key any row of the block sees
-  // W: the causal window (key j visible to row i iff i - W < j <= i; N + 1 when there is none)
-  const int64_t first = causal ? (lmax(0, row0 - W + 1) / kTile) * kTile : 0;  // first key tile any row sees
+  // bd: the banded causal mask (row i sees the keys bd.row_lo(i) <= j <= i)
+  const int64_t first = causal ? (bd.row_lo(tl.bh, row0) / kTile) * kTile : 0;  // first key tile any row sees
+  const int64_t lo_i = causal ? bd.row_lo(tl.bh, i) : 0;  // this row's first visible key
   for (int64_t k0 = first; k0 <= last; k0 += kTile) {
     __syncthreads();
     stage<T, D>(Ks, K + kvbase, k0, N);
@@ -365,7 +371,7 @@ __global__ void __launch_bounds__(kThreads) bob_row_kernel(
     __syncthreads();
     if (!live) continue;
     const int jn = static_cast<int>(lmin(kTile, (causal ? i + 1 : N) - k0));
-    const int jb = causal ? static_cast<int>(lmin(kTile, lmax(0, i - W + 1 - k0))) : 0;  // below the window
+    const int jb = causal ? static_cast<int>(lmin(kTile, lmax(0, lo_i - k0))) : 0;  // below the row's band
     for (int jj = jb; jj < jn; ++jj) {
       float kv[V], vv[V], bv[V], cv[V];
       load_smem(Ks + jj * D, lane, kv);
@@ -424,7 +430,7 @@ __global__ void __launch_bounds__(kThreads) bob_col_kernel(
     const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ Vt, const T* __restrict__ dO,
     const T* __restrict__ A, const T* __restrict__ Bm, const T* __restrict__ C, const float4* __restrict__ ws,
     const float* __restrict__ rho_ws, T* __restrict__ gK, T* __restrict__ gV, int64_t N, int64_t BHkv,
-    float scale, int causal, int64_t W, int64_t G) {
+    float scale, int causal, Band bd, int64_t G) {
   constexpr int V = D / 32;
   extern __shared__ float sm[];
   float* Qs = sm;
@@ -436,6 +442,9 @@ __global__ void __launch_bounds__(kThreads) bob_col_kernel(
   const Tile tl = decode(BHkv, nblk, false);  // tl.bh: a key/value head
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int64_t col0 = tl.blk * kWarps, j = col0 + warp;
+  // bd: the banded causal mask (key j is seen by the rows j <= i <= bd.key_hi(j))
+  const int64_t hi_blk = causal ? bd.key_hi(tl.bh, lmin(col0 + kWarps - 1, N - 1)) : N - 1;  // last row any key sees
+  const int64_t hi_j = causal ? bd.key_hi(tl.bh, j) : N - 1;
   const bool live = j < N;
   const size_t base = static_cast<size_t>(tl.bh) * N * D;
   float kv[V], vv[V], bv[V], cv[V], aK[V], aV[V];
@@ -449,7 +458,7 @@ __global__ void __launch_bounds__(kThreads) bob_col_kernel(
   }
   // gK and gV of a shared head sum over the G query heads that read it.
   for (int64_t hq = tl.bh * G; hq < (tl.bh + 1) * G; ++hq)
-  for (int64_t i0 = causal ? col0 : 0; i0 < (causal ? lmin(N, col0 + kWarps - 1 + W) : N); i0 += kTile) {
+  for (int64_t i0 = causal ? col0 : 0; i0 < (causal ? hi_blk + 1 : N); i0 += kTile) {
     const size_t qbase = static_cast<size_t>(hq) * N * D;
     __syncthreads();
     stage<T, D>(Qs, Q + qbase, i0, N);
@@ -462,7 +471,7 @@ __global__ void __launch_bounds__(kThreads) bob_col_kernel(
     __syncthreads();
     if (!live) continue;
     const int ib = causal ? static_cast<int>(lmax(0, j - i0)) : 0;
-    const int ie = static_cast<int>(lmin(kTile, (causal ? lmin(N, j + W) : N) - i0));  // rows i < j + W
+    const int ie = static_cast<int>(lmin(kTile, (causal ? hi_j + 1 : N) - i0));  // rows i <= bd.key_hi(j)
     for (int ii = ib; ii < ie; ++ii) {
       float qv[V], gv[V], a2[V];
       load_smem(Qs + ii * D, lane, qv);
@@ -503,7 +512,7 @@ __global__ void __launch_bounds__(kThreads) projected_dS_kernel(const T* __restr
                                                                 const T* __restrict__ dO,
                                                                 const float* __restrict__ lse,
                                                                 float* __restrict__ out, int64_t N, int64_t BH,
-                                                                float scale, int causal, int64_t W, int64_t G) {
+                                                                float scale, int causal, Band bd, int64_t G) {
   constexpr int V = D / 32;
   const int64_t nblk = (N + kWarps - 1) / kWarps;
   const Tile tl = decode(BH, nblk, true);
@@ -519,12 +528,13 @@ __global__ void __launch_bounds__(kThreads) projected_dS_kernel(const T* __restr
   float x0[1] = {dot(g, o)};
   warp_sum(x0);
   const float Di = x0[0], Li = lse[tl.bh * N + i];
+  const int64_t lo_i = causal ? bd.row_lo(tl.bh, i) : 0;  // this row's first visible key
   float r = 0.f, sp = 0.f;
   for (int pass = 0; pass < 2; ++pass) {
     const float rho = r / sp;
     for (int64_t j = 0; j < N; ++j) {
       float* dst = out + (static_cast<size_t>(tl.bh) * N + i) * N + j;
-      if (causal && (j > i || j <= i - W)) {
+      if (causal && (j > i || j < lo_i)) {
         if (pass == 1 && lane == 0) *dst = 0.f;
         continue;
       }
@@ -567,7 +577,7 @@ cudaError_t fwd_t(const Problem& p, const void* Q, const void* K, const void* V,
   cudaError_t e = allow_smem(k, sm);
   if (e != cudaSuccess) return e;
   k<<<grid_for(p), kThreads, sm, st>>>(static_cast<const T*>(Q), static_cast<const T*>(K),
-                                        static_cast<const T*>(V), static_cast<T*>(O), lse, p.N, p.BH, p.scale, p.causal, eff_window(p), p.group);
+                                        static_cast<const T*>(V), static_cast<T*>(O), lse, p.N, p.BH, p.scale, p.causal, make_band(p, eff_window(p), false), p.group);
   return cudaGetLastError();
 }
 
@@ -585,7 +595,7 @@ cudaError_t bwd_t(const Problem& p, const void* Q, const void* K, const void* V,
     kr<<<grid_for(p), kThreads, sm_row, st>>>(static_cast<const T*>(Q), static_cast<const T*>(K),
                                                static_cast<const T*>(V), static_cast<const T*>(O),
                                                static_cast<const T*>(dO), lse, static_cast<T*>(dQ), ws, p.N, p.BH,
-                                               p.scale, p.causal, eff_window(p), p.group);
+                                               p.scale, p.causal, make_band(p, eff_window(p), false), p.group);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -593,7 +603,7 @@ cudaError_t bwd_t(const Problem& p, const void* Q, const void* K, const void* V,
   kc<<<grid_for_cols(p), kThreads, sm_col, st>>>(static_cast<const T*>(Q), static_cast<const T*>(K),
                                                   static_cast<const T*>(V), static_cast<const T*>(dO), ws,
                                                   static_cast<T*>(dK), static_cast<T*>(dV), p.N, p.BHkv, p.scale,
-                                                  p.causal, eff_window(p), p.group);
+                                                  p.causal, make_band(p, eff_window(p), true), p.group);
   return cudaGetLastError();
 }
 
@@ -613,7 +623,7 @@ cudaError_t bob_t(const Problem& p, const void* Q, const void* K, const void* V,
     kr<<<grid_for(p), kThreads, sm_row, st>>>(
         static_cast<CT>(Q), static_cast<CT>(K), static_cast<CT>(V), static_cast<CT>(O), static_cast<CT>(dO), lse,
         static_cast<CT>(a), static_cast<CT>(b), static_cast<CT>(c), static_cast<T*>(gQ), static_cast<T*>(gdO), ws,
-        rho_ws, p.N, p.BH, p.scale, p.causal, eff_window(p), p.group);
+        rho_ws, p.N, p.BH, p.scale, p.causal, make_band(p, eff_window(p), false), p.group);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -621,7 +631,7 @@ cudaError_t bob_t(const Problem& p, const void* Q, const void* K, const void* V,
   kc<<<grid_for_cols(p), kThreads, sm_col, st>>>(static_cast<CT>(Q), static_cast<CT>(K), static_cast<CT>(V),
                                                   static_cast<CT>(dO), static_cast<CT>(a), static_cast<CT>(b),
                                                   static_cast<CT>(c), ws, rho_ws, static_cast<T*>(gK),
-                                                  static_cast<T*>(gV), p.N, p.BHkv, p.scale, p.causal, eff_window(p), p.group);
+                                                  static_cast<T*>(gV), p.N, p.BHkv, p.scale, p.causal, make_band(p, eff_window(p), true), p.group);
   return cudaGetLastError();
 }
 
@@ -702,7 +712,7 @@ cudaError_t simt_projected_dS(const Problem& p, const void* Q, const void* K, co
   with_head_dim(p.d, [&](auto dd) {
     projected_dS_kernel<T, dd()><<<grid_for(p), kThreads, 0, st>>>(
         static_cast<const T*>(Q), static_cast<const T*>(K), static_cast<const T*>(V), static_cast<const T*>(O),
-        static_cast<const T*>(dO), lse, dS, p.N, p.BH, p.scale, p.causal, eff_window(p), p.group);
+        static_cast<const T*>(dO), lse, dS, p.N, p.BH, p.scale, p.causal, make_band(p, eff_window(p), false), p.group);
     e = cudaGetLastError();
   });
   return e;

@@ -113,7 +113,8 @@ struct RowLay {
 // the constant D, so its code is that of a kernel without the option.
 // GP: GProj on the rounded dS of gQ's dS b product (the pre-pass left P^ b in `pb`);
 // the coefficient rho_i goes to `rho_ws` for the column pass.
-// WIN: the causal sliding window is in force (win); the other instances carry none of it.
+// WIN: a banded causal mask is in force (bd: the sliding window and/or the document
+// bounds); the other instances carry none of it.
 template <bool PAD, bool GP, bool WIN = false>
 __global__ void __launch_bounds__(kThreads, 1)
     bob_row_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
@@ -123,7 +124,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __nv_bfloat16* __restrict__ dO, const float* __restrict__ lse,
                    __nv_bfloat16* __restrict__ gQ, __nv_bfloat16* __restrict__ gdO, float4* __restrict__ ws,
                    const float* __restrict__ pb, float* __restrict__ rho_ws, int N, int Np, int nrb, int BH,
-                   float scale, float c, int causal, int win, int G, int hd_arg) {
+                   float scale, float c, int causal, Band bd, int G, int hd_arg) {
   const int hd = PAD ? hd_arg : D;
   using Lay = RowLay;
   constexpr int NS = Lay::NS;
@@ -148,7 +149,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kvh = bh / G;          // the slice of K, V, b, c this query slice reads
   const int rb = nrb - 1 - ord.k;  // heaviest row blocks first (within a group of slices)
   // 64-key blocks this row block sees: up to its last row, or all of them when not causal
-  const int j0 = (WIN && causal) ? max(0, rb * BM - win + 1) / BN : 0;  // first key block a row sees (window win)
+  const int j0 = (WIN && causal) ? bd.row_lo(bh, rb * BM) / BN : 0;  // first key block a row sees (banded mask bd)
+  const int lo_last = (WIN && causal) ? bd.row_lo(bh, min(rb * BM + BM - 1, N - 1)) : 0;
   const int nkv = (causal ? ((rb + 1) * BM + BN - 1) / BN : (N + BN - 1) / BN) - j0;  // blocks j0 + j, j < nkv
 
   if (threadIdx.x == 0) {
@@ -276,6 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lo = static_cast<uint32_t>(qd * 32) << 16;
     const int64_t row = static_cast<int64_t>(rb) * BM + r;
     const bool live = row < N;
+    const int lo_row = (WIN && causal) ? bd.row_lo(bh, row) : 0;
     const size_t rowoff = (static_cast<size_t>(bh) * N + row) * hd;  // rows of hd <= D columns
     float part = 0.f;
     if (live && hf * 32 < hd) {  // columns past hd are padding
@@ -326,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int krel = kb * BN + c0 - rb * BM;
       // last visible key of this row, relative to the thread's first key of the block
       const int klim = causal ? r - krel : N - 1 - (kb * BN + c0);
-      const int klo = (WIN && causal) ? klim - win + 1 : 0;  // first visible key of the row, relative to column 0
+      const int klo = (WIN && causal) ? lo_row - (kb * BN + c0) : 0;  // first visible key of the row, relative to column 0
       uint64_t P2[16], G2[16];
       uint32_t pP[16], pG[16], pS[16], pW[16];
       // P, PG from the [G | S] tiles (while [H | dP] is being computed)
@@ -354,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       // Causal: a block reaching past the first row of this CTA.  Otherwise: a block reaching past N.
-      if (causal ? (krel + 31 > 0 || (WIN && kb * BN + c0 < rb * BM + BM - win)) : kb * BN + c0 + 32 > N)
+      if (causal ? (krel + 31 > 0 || (WIN && kb * BN + c0 < lo_last)) : kb * BN + c0 + 32 > N)
         first(std::true_type{});
       else
         first(std::false_type{});
@@ -518,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tmRho, const __nv_bfloat16* __restrict__ Kp, const __nv_bfloat16* __restrict__ Bp,
                    const __nv_bfloat16* __restrict__ Vp, const __nv_bfloat16* __restrict__ Cp,
                    __nv_bfloat16* __restrict__ gK, __nv_bfloat16* __restrict__ gV, int N, int BHkv, float scale,
-                   float c, int causal, int win, int G, int hd_arg) {
+                   float c, int causal, Band bd, int G, int hd_arg) {
   const int hd = PAD ? hd_arg : D;
   using Lay = ColLayT<GP>;
   constexpr int NS = Lay::NS;
@@ -543,8 +546,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kb = ord.k;  // first key blocks have the most rows: first
   const int nq = (N + BN - 1) / BN;
   const int i0 = causal ? (kb * BM) / BN : 0;  // first query block that sees this key block
-  // query blocks per query slice: up to the last query any key of the block sees (i < key + win)
-  const int ntile = ((WIN && causal) ? min(N - 1, kb * BM + BM - 2 + win) / BN + 1 : nq) - i0;
+  // query blocks per query slice: up to the last query any key of the block sees (bd.key_hi)
+  const int ntile = ((WIN && causal) ? bd.key_hi(kvh, min(kb * BM + BM - 1, N - 1)) / BN + 1 : nq) - i0;
+  const int hi_first = (WIN && causal) ? bd.key_hi(kvh, kb * BM) : 0;  // the block's first key's last query
   const int nt = GR ? G * ntile : ntile;       // tiles t = h * ntile + (i - i0), one gK, gV
 
   if (threadIdx.x == 0) {
@@ -670,6 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lo = static_cast<uint32_t>(qd * 32) << 16;
     const int key = kb * BM + r;
     const int c0 = hf * 32;
+    const int khi = (WIN && causal) ? bd.key_hi(kvh, key) : 0;  // the last query this key is seen by
     {  // K, b, V, c rows of this key, elements 32 hf .. 32 hf + 31, into TMEM (A operands)
       const __nv_bfloat16* src[4] = {Kp, Bp, Vp, Cp};
       const uint32_t col[4] = {Lay::cK, Lay::cB, Lay::cV, Lay::cC};
@@ -731,8 +736,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           float p0 = ptx::ex2(arg.x), p1 = ptx::ex2(arg.y);
           if constexpr (decltype(masked)::value) {
             const int q0 = qbase + u;
-            if ((causal && (q0 < key || (WIN && q0 >= key + win))) || q0 >= N) p0 = 0.f;
-            if ((causal && (q0 + 1 < key || (WIN && q0 + 1 >= key + win))) || q0 + 1 >= N) p1 = 0.f;
+            if ((causal && (q0 < key || (WIN && q0 > khi))) || q0 >= N) p0 = 0.f;
+            if ((causal && (q0 + 1 < key || (WIN && q0 + 1 > khi))) || q0 + 1 >= N) p1 = 0.f;
           }
           const int idx = u >> 1;
           P2[idx] = tc::pk2f(p0, p1);
@@ -743,7 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       // Causal mask only in the first blocks (queries before this CTA's last key) and in
       // those past the window of its first key; past N only in the last block.
-      if ((causal && (qbase < kb * BM + BM || (WIN && qbase + 31 >= kb * BM + win))) || qbase + 32 > N)
+      if ((causal && (qbase < kb * BM + BM || (WIN && qbase + 31 > hi_first))) || qbase + 32 > N)
         first(std::true_type{});
       else
         first(std::false_type{});
@@ -846,7 +851,7 @@ cudaError_t tc_bob(const Problem& p, const void* Q, const void* K, const void* V
   if (passes & 1) {
     if (gproj && (e = tc_bob_pb(p, Q, K, b, lse, pbuf, st)) != cudaSuccess) return e;
     // Windowed: the general forms (runtime head dim, grouped tile loop in the column pass).
-    auto row = p.window > 0 ? (gproj ? bob_row_kernel<true, true, true> : bob_row_kernel<true, false, true>)
+    auto row = banded(p) ? (gproj ? bob_row_kernel<true, true, true> : bob_row_kernel<true, false, true>)
                : gproj ? bob_row_kernel<true, true> : d < D ? bob_row_kernel<true, false> : bob_row_kernel<false, false>;
     e = cudaFuncSetAttribute(row, cudaFuncAttributeMaxDynamicSharedMemorySize, RowLay::bytes);
     if (e != cudaSuccess) return e;
@@ -854,12 +859,12 @@ cudaError_t tc_bob(const Problem& p, const void* Q, const void* K, const void* V
         q128, do128, a128, k64, v64, b64, c64, static_cast<const __nv_bfloat16*>(O),
         static_cast<const __nv_bfloat16*>(dO), lse, static_cast<__nv_bfloat16*>(gQ),
         static_cast<__nv_bfloat16*>(gdO), ws, pbuf, reinterpret_cast<float*>(rho), static_cast<int>(N),
-        static_cast<int>(Np), nrb, static_cast<int>(BH), p.scale, c, p.causal, static_cast<int>(eff_window_tc(p)),
+        static_cast<int>(Np), nrb, static_cast<int>(BH), p.scale, c, p.causal, make_band(p, eff_window_tc(p), false),
         p.group, static_cast<int>(d));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (!(passes & 2)) return cudaSuccess;
-  auto col = p.window > 0 ? (gproj ? bob_col_kernel<true, true, true, true> : bob_col_kernel<true, true, false, true>)
+  auto col = banded(p) ? (gproj ? bob_col_kernel<true, true, true, true> : bob_col_kernel<true, true, false, true>)
              : gproj ? bob_col_kernel<true, true, true>
              : p.group > 1 ? (d < D ? bob_col_kernel<true, true, false> : bob_col_kernel<true, false, false>)
                            : (d < D ? bob_col_kernel<false, true, false> : bob_col_kernel<false, false, false>);
@@ -870,7 +875,7 @@ cudaError_t tc_bob(const Problem& p, const void* Q, const void* K, const void* V
       q64, a64, do64, s64, r64, static_cast<const __nv_bfloat16*>(K), static_cast<const __nv_bfloat16*>(b),
       static_cast<const __nv_bfloat16*>(V), static_cast<const __nv_bfloat16*>(cc), static_cast<__nv_bfloat16*>(gK),
       static_cast<__nv_bfloat16*>(gV), static_cast<int>(N), static_cast<int>(p.BHkv), p.scale, c, p.causal,
-      static_cast<int>(eff_window_tc(p)), p.group, static_cast<int>(d));
+      make_band(p, eff_window_tc(p), true), p.group, static_cast<int>(d));
   return cudaGetLastError();
 }
 

@@ -77,7 +77,8 @@ static_assert(RowLay::bytes <= 232448, "row pass shared memory");
 
 // GP: GProj on the rounded dS of gQ's dS b product, as at d = 64 (P^ b from the pre-pass
 // in `pb`, 128 columns per row; the coefficient to `rho_ws`, by CTA h = 0).
-// WIN: the causal sliding window is in force (win); the other instances carry none of it.
+// WIN: a banded causal mask is in force (bd: the sliding window and/or the document
+// bounds); the other instances carry none of it.
 template <bool GP, bool WIN = false>
 __global__ void __launch_bounds__(kThreads, 1)
     bob128_row_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
@@ -87,7 +88,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __nv_bfloat16* __restrict__ dO, const float* __restrict__ lse,
                       __nv_bfloat16* __restrict__ gQ, __nv_bfloat16* __restrict__ gdO, float4* __restrict__ ws,
                       const float* __restrict__ pb, float* __restrict__ rho_ws, int N, int Np, int nrb, int BH,
-                      float scale, float c, int causal, int win, int G, int hd) {
+                      float scale, float c, int causal, Band bd, int G, int hd) {
   using Lay = RowLay;
   constexpr int NS = Lay::NS;
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -111,7 +112,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int bh = ord.bh;
   const int kvh = bh / G;
   const int rb = nrb - 1 - ord.k;
-  const int j0 = (WIN && causal) ? max(0, rb * BM - win + 1) / BN : 0;  // first key block a row sees (window win)
+  const int j0 = (WIN && causal) ? bd.row_lo(bh, rb * BM) / BN : 0;  // first key block a row sees (banded mask bd)
+  const int lo_last = (WIN && causal) ? bd.row_lo(bh, min(rb * BM + BM - 1, N - 1)) : 0;
   const int nkv = (causal ? ((rb + 1) * BM + BN - 1) / BN : (N + BN - 1) / BN) - j0;  // blocks j0 + j, j < nkv
 
   if (threadIdx.x == 0) {
@@ -246,6 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lo = static_cast<uint32_t>(qd * 32) << 16;
     const int64_t row = static_cast<int64_t>(rb) * BM + r;
     const bool live = row < N;
+    const int lo_row = (WIN && causal) ? bd.row_lo(bh, row) : 0;
     const size_t rowoff = (static_cast<size_t>(bh) * N + row) * hd;  // rows of hd <= D columns
     float part = 0.f;  // D_i over columns [64 hf, 64 hf + 64)
     if (live) {
@@ -289,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int kb = j0 + j;
       const int krel = kb * BN + c0 - rb * BM;
       const int klim = causal ? r - krel : N - 1 - (kb * BN + c0);
-      const int klo = (WIN && causal) ? klim - win + 1 : 0;  // first visible key of the row, relative to column 0
+      const int klo = (WIN && causal) ? lo_row - (kb * BN + c0) : 0;  // first visible key of the row, relative to column 0
       uint64_t P2[16], G2[16];
       uint32_t pP[16], pG[16], pS[16], pW[16];
       auto first = [&](auto masked) {
@@ -315,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           accP1 = tc::add_bf16_hi(accP1, pP[idx]);
         }
       };
-      if (causal ? (krel + 31 > 0 || (WIN && kb * BN + c0 < rb * BM + BM - win)) : kb * BN + c0 + 32 > N)
+      if (causal ? (krel + 31 > 0 || (WIN && kb * BN + c0 < lo_last)) : kb * BN + c0 + 32 > N)
         first(std::true_type{});
       else
         first(std::false_type{});
@@ -472,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tmRho, const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmC,
                       const __nv_bfloat16* __restrict__ Kp, const __nv_bfloat16* __restrict__ Bp,
                       __nv_bfloat16* __restrict__ gK, __nv_bfloat16* __restrict__ gV, int N, int BHkv,
-                      float scale, float c, int causal, int win, int G, int hd) {
+                      float scale, float c, int causal, Band bd, int G, int hd) {
   using Lay = ColLayT<GP>;
   constexpr int NS = Lay::NS;
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -498,7 +501,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kb = ord.k;
   const int nq = (N + BN - 1) / BN;
   const int i0 = causal ? (kb * BM) / BN : 0;
-  const int ntile = ((WIN && causal) ? min(N - 1, kb * BM + BM - 2 + win) / BN + 1 : nq) - i0;  // i < key + win
+  const int ntile = ((WIN && causal) ? bd.key_hi(kvh, min(kb * BM + BM - 1, N - 1)) / BN + 1 : nq) - i0;  // i <= key_hi
+  const int hi_first = (WIN && causal) ? bd.key_hi(kvh, kb * BM) : 0;  // the block's first key's last query
   const int nt = GR ? G * ntile : ntile;
 
   if (threadIdx.x == 0) {
@@ -634,6 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lo = static_cast<uint32_t>(qd * 32) << 16;
     const int key = kb * BM + r;
     const int c0 = hf * 32;
+    const int khi = (WIN && causal) ? bd.key_hi(kvh, key) : 0;  // the last query this key is seen by
     {  // K and b rows of this key, elements 64 hf .. 64 hf + 63, into TMEM (A operands)
       const __nv_bfloat16* src[2] = {Kp, Bp};
       const uint32_t col[2] = {Lay::cK, Lay::cB};
@@ -692,8 +697,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           float p0 = ptx::ex2(arg.x), p1 = ptx::ex2(arg.y);
           if constexpr (decltype(masked)::value) {
             const int q0 = qbase + u;
-            if ((causal && (q0 < key || (WIN && q0 >= key + win))) || q0 >= N) p0 = 0.f;
-            if ((causal && (q0 + 1 < key || (WIN && q0 + 1 >= key + win))) || q0 + 1 >= N) p1 = 0.f;
+            if ((causal && (q0 < key || (WIN && q0 > khi))) || q0 >= N) p0 = 0.f;
+            if ((causal && (q0 + 1 < key || (WIN && q0 + 1 > khi))) || q0 + 1 >= N) p1 = 0.f;
           }
           const int idx = u >> 1;
           P2[idx] = tc::pk2f(p0, p1);
@@ -702,7 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           pDP[idx] = ptx::pack_bf16(vdp.x, vdp.y);
         }
       };
-      if ((causal && (qbase < kb * BM + BM || (WIN && qbase + 31 >= kb * BM + win))) || qbase + 32 > N)
+      if ((causal && (qbase < kb * BM + BM || (WIN && qbase + 31 > hi_first))) || qbase + 32 > N)
         first(std::true_type{});
       else
         first(std::false_type{});
@@ -802,7 +807,7 @@ cudaError_t tc_bob128(const Problem& p, const void* Q, const void* K, const void
   cudaError_t e = cudaSuccess;
   if (passes & 1) {
     if (gproj && (e = tc_bob_pb(p, Q, K, b, lse, pbuf, st)) != cudaSuccess) return e;
-    auto row = p.window > 0 ? (gproj ? bob128_row_kernel<true, true> : bob128_row_kernel<false, true>)
+    auto row = banded(p) ? (gproj ? bob128_row_kernel<true, true> : bob128_row_kernel<false, true>)
                             : (gproj ? bob128_row_kernel<true> : bob128_row_kernel<false>);
     e = cudaFuncSetAttribute(row, cudaFuncAttributeMaxDynamicSharedMemorySize, RowLay::bytes);
     if (e != cudaSuccess) return e;
@@ -810,13 +815,13 @@ cudaError_t tc_bob128(const Problem& p, const void* Q, const void* K, const void
         q128, do128, a128, k64, v64, b64, c64, static_cast<const __nv_bfloat16*>(O),
         static_cast<const __nv_bfloat16*>(dO), lse, static_cast<__nv_bfloat16*>(gQ),
         static_cast<__nv_bfloat16*>(gdO), ws, pbuf, reinterpret_cast<float*>(rho), static_cast<int>(N),
-        static_cast<int>(Np), nrb, static_cast<int>(BH), p.scale, c, p.causal, static_cast<int>(eff_window_tc(p)),
+        static_cast<int>(Np), nrb, static_cast<int>(BH), p.scale, c, p.causal, make_band(p, eff_window_tc(p), false),
         p.group, static_cast<int>(d));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (!(passes & 2)) return cudaSuccess;
   // The GProj instance takes the grouped tile loop, which also serves ungrouped heads.
-  auto col = p.window > 0 ? (gproj ? bob128_col_kernel<true, true, true> : bob128_col_kernel<true, false, true>)
+  auto col = banded(p) ? (gproj ? bob128_col_kernel<true, true, true> : bob128_col_kernel<true, false, true>)
              : gproj ? bob128_col_kernel<true, true>
                    : p.group > 1 ? bob128_col_kernel<true, false> : bob128_col_kernel<false, false>;
   const int cbytes = gproj ? ColLayT<true>::bytes : ColLayT<false>::bytes;
@@ -825,7 +830,7 @@ cudaError_t tc_bob128(const Problem& p, const void* Q, const void* K, const void
   col<<<static_cast<unsigned>(2 * nrb * p.BHkv), kThreads, cbytes, st>>>(
       q64, a64, do64, s64, r64, v128, c128, static_cast<const __nv_bfloat16*>(K), static_cast<const __nv_bfloat16*>(b),
       static_cast<__nv_bfloat16*>(gK), static_cast<__nv_bfloat16*>(gV), static_cast<int>(N),
-      static_cast<int>(p.BHkv), p.scale, c, p.causal, static_cast<int>(eff_window_tc(p)), p.group,
+      static_cast<int>(p.BHkv), p.scale, c, p.causal, make_band(p, eff_window_tc(p), true), p.group,
       static_cast<int>(d));
   return cudaGetLastError();
 }

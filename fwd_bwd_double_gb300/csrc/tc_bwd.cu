@@ -74,14 +74,15 @@ struct RowLay {
   static_assert(cols == kCols && cols <= 512, "TMEM budget");
 };
 
-// WIN: the causal sliding window is in force (win); the other instances carry none of it.
+// WIN: a banded causal mask is in force (bd: the sliding window and/or the document
+// bounds); the other instances carry none of it.
 template <int D, int NB, bool GP, bool WIN = false>
 __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
     bwd_row_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                    const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const __nv_bfloat16* __restrict__ O, const __nv_bfloat16* __restrict__ dO,
                    const float* __restrict__ lse, __nv_bfloat16* __restrict__ dQ, float4* __restrict__ ws, int N,
-                   int Np, int nrb, int BH, float scale, float c, int causal, int win, int G, int dv) {
+                   int Np, int nrb, int BH, float scale, float c, int causal, Band bd, int G, int dv) {
   using Lay = RowLay<D, NB, GP>;
   static_assert(NB == 1, "one score-tile buffer, released early");
   constexpr int NS = Lay::NS;
@@ -103,8 +104,9 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
   const int bh = ord.bh;
   const int rb = nrb - 1 - ord.k;  // heaviest row blocks first (within a group of slices)
   // key blocks j0 + j, j < nkv: those touching rows <= the last row (all key blocks when
-  // not causal), from the first one a row sees under the window win (> N when none)
-  const int j0 = (WIN && causal) ? max(0, rb * BM - win + 1) / BN : 0;
+  // not causal), from the first one a row sees under the banded mask bd
+  const int j0 = (WIN && causal) ? bd.row_lo(bh, rb * BM) / BN : 0;
+  const int lo_last = (WIN && causal) ? bd.row_lo(bh, min(rb * BM + BM - 1, N - 1)) : 0;
   const int nkv = (causal ? ((rb + 1) * BM + BN - 1) / BN : (N + BN - 1) / BN) - j0;
 
   if (threadIdx.x == 0) {
@@ -230,6 +232,7 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
     uint64_t accR = 0, accP = 0;  // GProj: sums of the bf16 dS and P fed to the products
     const uint64_t c2 = tc::pk2f(c, c), nL2 = tc::pk2f(-L2, -L2), nD2 = tc::pk2f(-Dr, -Dr);
     const int c0 = hf * (BN / 2);
+    const int lo_row = (WIN && causal) ? bd.row_lo(bh, row) : 0;
     for (int j = 0; j < nkv; ++j) {
       const int b = j % NB;
       wait(&s_full[b], (j / NB) & 1);
@@ -244,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
       const int krel = kb * BN + c0 - rb * BM;  // key of my column 0 minus the block's first row
       // last and first visible key of this row, relative to my column 0
       const int klim = causal ? r - krel : N - 1 - (kb * BN + c0);
-      const int klo = (WIN && causal) ? klim - win + 1 : 0;
+      const int klo = (WIN && causal) ? lo_row - (kb * BN + c0) : 0;
       uint32_t dsk[16], pk[16];
       auto block = [&](auto masked) {
 #pragma unroll
@@ -266,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
       };
       // the mask reaches into this thread's columns: past the row (causal), below the
       // window of the block's last row, or past N
-      if (causal ? (krel + 31 > 0 || (WIN && kb * BN + c0 < rb * BM + BM - win)) : kb * BN + c0 + 32 > N)
+      if (causal ? (krel + 31 > 0 || (WIN && kb * BN + c0 < lo_last)) : kb * BN + c0 + 32 > N)
         block(std::true_type{});
       else
         block(std::false_type{});
@@ -351,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bwd_col_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                    const __grid_constant__ CUtensorMap tmSt, __nv_bfloat16* __restrict__ dK,
-                   __nv_bfloat16* __restrict__ dV, int N, int BHkv, float scale, float c, int causal, int win, int G,
+                   __nv_bfloat16* __restrict__ dV, int N, int BHkv, float scale, float c, int causal, Band bd, int G,
                    int dv) {
   using Lay = ColLay<D, NB, GP>;
   static_assert(NB == 1, "one score-tile buffer, released early");
@@ -375,8 +378,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kb = ord.k;  // first key blocks have the most rows: first
   const int nq = (N + BN - 1) / BN;
   const int i0 = causal ? (kb * BM) / BN : 0;         // first query block with a query >= first key
-  // query blocks per query slice: up to the last query any key of the block sees (i < key + win)
-  const int ntile = ((WIN && causal) ? min(N - 1, kb * BM + BM - 2 + win) / BN + 1 : nq) - i0;
+  // query blocks per query slice: up to the last query any key of the block sees (bd.key_hi)
+  const int ntile = ((WIN && causal) ? bd.key_hi(kvh, min(kb * BM + BM - 1, N - 1)) / BN + 1 : nq) - i0;
+  const int hi_first = (WIN && causal) ? bd.key_hi(kvh, kb * BM) : 0;  // the block's first key's last query
   const int nt = GR ? G * ntile : ntile;              // tiles t = h * ntile + (i - i0), one dK, dV
 
   if (threadIdx.x == 0) {
@@ -480,6 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int key = kb * BM + r;
     const int c0 = hf * (BN / 2);
     const uint64_t c2 = tc::pk2f(c, c);
+    const int khi = (WIN && causal) ? bd.key_hi(kvh, key) : 0;  // the last query this key is seen by
     for (int t = 0; t < nt; ++t) {
       const int s = t % NS, b = t % NB, i = GR ? i0 + t % ntile : i0 + t;
       wait(&s_full[b], (t / NB) & 1);
@@ -503,8 +508,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           float p0 = ptx::ex2(arg.x), p1 = ptx::ex2(arg.y);
           if constexpr (decltype(masked)::value) {
             const int q0 = qbase + u;
-            if ((causal && (q0 < key || (WIN && q0 >= key + win))) || q0 >= N) p0 = 0.f;
-            if ((causal && (q0 + 1 < key || (WIN && q0 + 1 >= key + win))) || q0 + 1 >= N) p1 = 0.f;
+            if ((causal && (q0 < key || (WIN && q0 > khi))) || q0 >= N) p0 = 0.f;
+            if ((causal && (q0 + 1 < key || (WIN && q0 + 1 > khi))) || q0 + 1 >= N) p1 = 0.f;
           }
           const float2 ds =
               tc::unpk2(tc::mul2(tc::pk2f(p0, p1), tc::add2(tc::pk2(pv[u], pv[u + 1]), tc::pk2f(A.z, A.w))));
@@ -518,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       // causal mask (first blocks), past the window of the block's first key, or past N (last block)
-      if ((causal && (qbase < kb * BM + BM || (WIN && qbase + 31 >= kb * BM + win))) || qbase + 32 > N)
+      if ((causal && (qbase < kb * BM + BM || (WIN && qbase + 31 > hi_first))) || qbase + 32 > N)
         block(std::true_type{});
       else
         block(std::false_type{});
@@ -582,25 +587,25 @@ cudaError_t launch(const Problem& p, const void* Q, const void* K, const void* V
   const int nrb = static_cast<int>((N + BM - 1) / BM);
   if (passes & 1) {
     using Lay = RowLay<D, NBR, GP>;
-    auto kern = p.window > 0 ? bwd_row_kernel<D, NBR, GP, true> : bwd_row_kernel<D, NBR, GP>;
+    auto kern = banded(p) ? bwd_row_kernel<D, NBR, GP, true> : bwd_row_kernel<D, NBR, GP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::bytes);
     if (e != cudaSuccess) return e;
     kern<<<static_cast<unsigned>(nrb * BH), kThreads, Lay::bytes, st>>>(
         q128, do128, k64, v64, static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), lse,
         static_cast<__nv_bfloat16*>(dQ), ws, static_cast<int>(N), static_cast<int>(Np), nrb, static_cast<int>(BH),
-        p.scale, c, p.causal, static_cast<int>(eff_window_tc(p)), p.group, static_cast<int>(d));
+        p.scale, c, p.causal, make_band(p, eff_window_tc(p), false), p.group, static_cast<int>(d));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (passes & 2) {
     using Lay = ColLay<D, NBC, GP>;
     // Windowed: the grouped tile loop (which also serves ungrouped heads).
-    auto kern = p.window > 0 ? bwd_col_kernel<D, NBC, GP, true, true>
+    auto kern = banded(p) ? bwd_col_kernel<D, NBC, GP, true, true>
                 : p.group > 1 ? bwd_col_kernel<D, NBC, GP, true> : bwd_col_kernel<D, NBC, GP, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::bytes);
     if (e != cudaSuccess) return e;
     kern<<<static_cast<unsigned>(nrb * p.BHkv), kThreads, Lay::bytes, st>>>(
         k128, v128, q64, do64, s64, static_cast<__nv_bfloat16*>(dK), static_cast<__nv_bfloat16*>(dV),
-        static_cast<int>(N), static_cast<int>(p.BHkv), p.scale, c, p.causal, static_cast<int>(eff_window_tc(p)),
+        static_cast<int>(N), static_cast<int>(p.BHkv), p.scale, c, p.causal, make_band(p, eff_window_tc(p), true),
         p.group, static_cast<int>(d));
     return cudaGetLastError();
   }

@@ -73,7 +73,9 @@ struct Bars {
   uint64_t* ready;     // P^T in TMEM and dS in shared memory
   uint64_t* dq_full;   // the block's three output products finished (dQ_i in TMEM, P^T, dS read)
   uint64_t* dq_empty;  // dQ_i copied out of TMEM (the next block's dQ product may start)
-  uint64_t* stg_full;  // dQ_i staged in its stage
+  uint64_t* stg_full;  // [NS] dQ_i staged in its stage (one barrier per stage: the compute
+                       // warps cannot run a full ring ahead of the reduces, so no phase of
+                       // it completes twice before its wait)
   uint64_t* acc_full;
   uint32_t* tmem_slot;
   volatile int* abort_flag;
@@ -86,7 +88,7 @@ struct Bars {
     dq_full = ready + 1;
     dq_empty = dq_full + 1;
     stg_full = dq_empty + 1;
-    acc_full = stg_full + 1;
+    acc_full = stg_full + NS;
     tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
     abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   }
@@ -98,14 +100,15 @@ __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
   return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
-// GR: grouped key/value heads (G > 1); WIN: the causal sliding window win is in force.
+// GR: grouped key/value heads (G > 1); WIN: a banded causal mask is in force (bd: the
+// sliding window and/or the document bounds).
 template <bool GR, bool WIN>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_fused_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                      const __grid_constant__ CUtensorMap tmSt, const __grid_constant__ CUtensorMap tmAcc,
                      __nv_bfloat16* __restrict__ dK, __nv_bfloat16* __restrict__ dV, int N, int nb, int BHkv,
-                     float scale, float c, int causal, int win, int G, int dv) {
+                     float scale, float c, int causal, Band bd, int G, int dv) {
   extern __shared__ __align__(1024) uint8_t sm[];
   Bars br(sm + Lay::oBar);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -113,9 +116,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kvh = ord.bh;          // key/value slice; its G query slices are kvh * G + h, h < G
   const int kb = ord.k;            // first key blocks have the most query blocks: first
   const int i0 = causal ? kb : 0;  // first query block that sees this key block
-  // query blocks per query slice: up to the last query any key of the block sees
-  // (queries i < key + win under the window win; larger than N when there is none)
-  const int ntile = ((WIN && causal) ? min(N - 1, kb * BW + BW - 2 + win) / BW + 1 : nb) - i0;
+  // query blocks per query slice: up to the last query any key of the block sees (the
+  // banded mask bd: queries i <= bd.key_hi(key))
+  const int ntile = ((WIN && causal) ? bd.key_hi(kvh, min(kb * BW + BW - 1, N - 1)) / BW + 1 : nb) - i0;
+  const int hi_first = (WIN && causal) ? bd.key_hi(kvh, kb * BW) : 0;  // the block's first key's last query
   const int nt = GR ? G * ntile : ntile;  // tiles t = h * ntile + (i - i0)
 
   if (threadIdx.x == 0) {
@@ -126,7 +130,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(br.ready, kCompute);
     ptx::mbar_init(br.dq_full, 1);
     ptx::mbar_init(br.dq_empty, kCompute);
-    ptx::mbar_init(br.stg_full, kCompute);
+    for (int s = 0; s < NS; ++s) ptx::mbar_init(&br.stg_full[s], kCompute);
     ptx::mbar_init(br.acc_full, 1);
     *br.abort_flag = (ptx::smem_u32(sm) & 1023u) ? 1 : 0;
     if (*br.abort_flag) atomicOr(&g_err, FBD_ERR_TIMEOUT);
@@ -171,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = 0; t < nt && t < NS; ++t) load(t);
       for (int t = 0; t < nt; ++t) {
         // dQ_t staged in its stage: reduce-add the two 32-column boxes, then refill the stage.
-        if (!wait(br.stg_full, t & 1)) break;
+        if (!wait(&br.stg_full[t % NS], (t / NS) & 1)) break;
         int bh, i;
         tile_at(t, bh, i);
         const uint8_t* st = sm + Lay::oStage + (t % NS) * Lay::kStage;
@@ -258,6 +262,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // statistics of its 4 query pairs are loaded once per block.
     const int g4 = lane >> 2, q4 = lane & 3;
     const uint64_t c2 = tc::pk2f(c, c);
+    // last query each of this thread's four keys (rows g4 + 16 h + 8 m of its quarter) sees
+    int khi[2][2] = {{0, 0}, {0, 0}};
+    if constexpr (WIN) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int m = 0; m < 2; ++m) khi[h][m] = bd.key_hi(kvh, kb * BW + qd * 32 + g4 + 16 * h + 8 * m);
+    }
     // dQ_t out of TMEM (this thread: query 32 qd + lane, columns 16 cg ..) into the stage of
     // block t as two 128-byte-swizzled fp32 boxes of 32 columns (the TMA reduce's layout).
     // Called once dq_full of block t has been waited for (its products read nothing more).
@@ -274,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<uint4*>(box + sw128(q, (cg & 1) * 4 + u)) =
             make_uint4(qv[4 * u], qv[4 * u + 1], qv[4 * u + 2], qv[4 * u + 3]);
       ptx::fence_proxy_async_smem();
-      ptx::mbar_arrive(br.stg_full);
+      ptx::mbar_arrive(&br.stg_full[t % NS]);
     };
     for (int t = 0; t < nt; ++t) {
       const int s = t % NS;
@@ -315,8 +327,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               float p0 = ptx::ex2(arg.x), p1 = ptx::ex2(arg.y);
               if constexpr (decltype(masked)::value) {
                 const int q0 = qbase + 8 * k, kk = kbase + 16 * h + 8 * m;
-                if ((causal && (q0 < kk || (WIN && q0 >= kk + win))) || q0 >= N) p0 = 0.f;
-                if ((causal && (q0 + 1 < kk || (WIN && q0 + 1 >= kk + win))) || q0 + 1 >= N) p1 = 0.f;
+                if ((causal && (q0 < kk || (WIN && q0 > khi[h][m]))) || q0 >= N) p0 = 0.f;
+                if ((causal && (q0 + 1 < kk || (WIN && q0 + 1 > khi[h][m]))) || q0 + 1 >= N) p1 = 0.f;
               }
               const float2 ds = tc::unpk2(
                   tc::mul2(tc::pk2f(p0, p1), tc::add2(tc::pk2(pv[h][e], pv[h][e + 1]), tc::pk2f(A[k].z, A[k].w))));
@@ -325,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
       };
       // the diagonal block, a block reaching past the window of the block's first key, or past N
-      if ((causal && i == kb) || (WIN && causal && i * BW + BW - 1 >= kb * BW + win) || i * BW + c0 + kC > N)
+      if ((causal && i == kb) || (WIN && causal && i * BW + BW - 1 > hi_first) || i * BW + c0 + kC > N)
         block(std::true_type{});
       else
         block(std::false_type{});
@@ -478,14 +490,14 @@ cudaError_t tc_bwd_fused(const Problem& p, const void* Q, const void* K, const v
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int nb = static_cast<int>((N + BW - 1) / BW);
-  auto kern = p.window > 0 ? bwd_fused_kernel<true, true>
+  auto kern = banded(p) ? bwd_fused_kernel<true, true>
               : p.group > 1 ? bwd_fused_kernel<true, false>
                             : bwd_fused_kernel<false, false>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::bytes);
   if (e != cudaSuccess) return e;
   kern<<<static_cast<unsigned>(nb * p.BHkv), kThreads, Lay::bytes, st>>>(
       k, v, q, g, s, a, static_cast<__nv_bfloat16*>(dK), static_cast<__nv_bfloat16*>(dV), static_cast<int>(N), nb,
-      static_cast<int>(p.BHkv), p.scale, p.scale * kLog2e, p.causal, static_cast<int>(eff_window_tc(p)), p.group,
+      static_cast<int>(p.BHkv), p.scale, p.scale * kLog2e, p.causal, make_band(p, eff_window_tc(p), true), p.group,
       static_cast<int>(d));
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int64_t cv_threads = BH * N * 8;

@@ -112,14 +112,15 @@ struct RowLay {
 };
 static_assert(RowLay<128>::bytes <= 232448, "row pass shared memory at d = 128");
 
-// WIN: the causal sliding window is in force (win); the other instances carry none of it.
+// WIN: a banded causal mask is in force (bd: the sliding window and/or the document
+// bounds); the other instances carry none of it.
 template <int DR, bool GP, bool WIN = false>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_row_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                const __nv_bfloat16* __restrict__ O, const __nv_bfloat16* __restrict__ dO,
                const float* __restrict__ lse, __nv_bfloat16* __restrict__ dQ, float4* __restrict__ ws, int N, int Np,
-               int nrb, int BH, float scale, float c, int causal, int win, int G, int dv) {
+               int nrb, int BH, float scale, float c, int causal, Band bd, int G, int dv) {
   using Lay = RowLay<DR, GP>;
   constexpr int NS = Lay::NSR, kTile = Lay::kTileR, DG = Lay::DGR, D = DR;
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -130,8 +131,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int bh = ord.bh;
   const int rb = nrb - 1 - ord.k;  // heaviest first within a group of slices
   // 128-key blocks j0 + j, j < nkv: up to rb (all blocks when not causal), from the first
-  // block a row of this block sees under the window win (larger than N when there is none)
-  const int j0 = (WIN && causal) ? max(0, rb * BW - win + 1) / BW : 0;
+  // block a row of this block sees under the banded mask bd (window and/or documents)
+  const int j0 = (WIN && causal) ? bd.row_lo(bh, rb * BW) / BW : 0;
+  const int lo_last = (WIN && causal) ? bd.row_lo(bh, min(rb * BW + BW - 1, N - 1)) : 0;
   const int nkv = (causal ? rb + 1 : nrb) - j0;
 
   if (threadIdx.x == 0) sy.init(sm);
@@ -243,6 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float L2 = live ? lse[static_cast<size_t>(bh) * N + row] * kLog2e : 0.f;
     const uint64_t c2 = tc::pk2f(c, c), nL2 = tc::pk2f(-L2, -L2), nD2 = tc::pk2f(-Dr, -Dr);
     const int c0 = cg * kC;
+    const int lo_row = (WIN && causal) ? bd.row_lo(bh, row) : 0;
     uint64_t accR = 0, accP = 0;  // GProj: sums of the bf16 dS and P fed to the products
     for (int j = 0; j < nkv; ++j) {
       wait(sy.s_full, j & 1);
@@ -256,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t dsk[kC / 2], pkk[GP ? kC / 2 : 1];
       const int kb = j0 + j;
       const int klim = causal ? (WIN ? rb * BW + r - kb * BW : r) : N - 1 - kb * BW;  // last visible key, relative
-      const int klo = (WIN && causal) ? rb * BW + r - win + 1 - kb * BW : 0;        // first visible key, relative
+      const int klo = (WIN && causal) ? lo_row - kb * BW : 0;  // first visible key, relative
       auto block = [&](auto masked) {
 #pragma unroll
         for (int t = 0; t < kC; t += 2) {
@@ -277,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       };
-      if (causal ? (kb == rb || (WIN && kb * BW < rb * BW + BW - win)) : (j == nkv - 1 && (N % BW) != 0))
+      if (causal ? (kb == rb || (WIN && kb * BW < lo_last)) : (j == nkv - 1 && (N % BW) != 0))
         block(std::true_type{});
       else
         block(std::false_type{});
@@ -367,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bwd_col_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                const __grid_constant__ CUtensorMap tmSt, __nv_bfloat16* __restrict__ dK,
-               __nv_bfloat16* __restrict__ dV, int N, int nb, int BHkv, float scale, float c, int causal, int win,
+               __nv_bfloat16* __restrict__ dV, int N, int nb, int BHkv, float scale, float c, int causal, Band bd,
                int G, int dv) {
   using Lay = ColLayT<GP>;
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -377,9 +380,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kvh = ord.bh;        // key/value slice; its G query slices are kvh * G + h, h < G
   const int kb = ord.k;          // first key blocks have the most query blocks: first
   const int i0 = causal ? kb : 0;  // first query block that sees this key block
-  // query blocks per query slice: up to the last query any key of the block sees
-  // (queries i < key + win under the window win; larger than N when there is none)
-  const int ntile = ((WIN && causal) ? min(N - 1, kb * BW + BW - 2 + win) / BW + 1 : nb) - i0;
+  // query blocks per query slice: up to the last query any key of the block sees (the
+  // banded mask bd: queries i <= bd.key_hi(key))
+  const int ntile = ((WIN && causal) ? bd.key_hi(kvh, min(kb * BW + BW - 1, N - 1)) / BW + 1 : nb) - i0;
+  const int hi_first = (WIN && causal) ? bd.key_hi(kvh, kb * BW) : 0;  // the block's first key's last query
   const int nt = GR ? G * ntile : ntile;  // tiles t = h * ntile + (i - i0), summed into one dK, dV
 
   if (threadIdx.x == 0) sy.init(sm);
@@ -476,6 +480,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // of its 32 (pairs 2(t%4) + 8k, k < 4) for 4 keys (quarter rows t/4 + 8m, m < 4):
     // the row statistics of 4 query pairs stay in registers for the whole block.
     const int g4 = lane >> 2, q4 = lane & 3;
+    // last query each of this thread's four keys (rows g4 + 16 h + 8 m of its quarter) sees
+    int khi[2][2] = {{0, 0}, {0, 0}};
+    if constexpr (WIN) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int m = 0; m < 2; ++m) khi[h][m] = bd.key_hi(kvh, kb * BW + qd * 32 + g4 + 16 * h + 8 * m);
+    }
     const uint64_t c2 = tc::pk2f(c, c);
     for (int t = 0; t < nt; ++t) {
       const int s = t % NS, i = GR ? i0 + t % ntile : i0 + t;
@@ -513,8 +525,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               float p0 = ptx::ex2(arg.x), p1 = ptx::ex2(arg.y);
               if constexpr (decltype(masked)::value) {
                 const int q0 = qbase + 8 * k, kk = kbase + 16 * h + 8 * m;
-                if ((causal && (q0 < kk || (WIN && q0 >= kk + win))) || q0 >= N) p0 = 0.f;
-                if ((causal && (q0 + 1 < kk || (WIN && q0 + 1 >= kk + win))) || q0 + 1 >= N) p1 = 0.f;
+                if ((causal && (q0 < kk || (WIN && q0 > khi[h][m]))) || q0 >= N) p0 = 0.f;
+                if ((causal && (q0 + 1 < kk || (WIN && q0 + 1 > khi[h][m]))) || q0 + 1 >= N) p1 = 0.f;
               }
               const float2 ds = tc::unpk2(
                   tc::mul2(tc::pk2f(p0, p1), tc::add2(tc::pk2(pv[h][e], pv[h][e + 1]), tc::pk2f(A[k].z, A[k].w))));
@@ -523,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
       };
       // the diagonal block, a block reaching past the window of the block's first key, or past N
-      if ((causal && (GR ? i == kb : t == 0)) || (WIN && causal && i * BW + BW - 1 >= kb * BW + win) ||
+      if ((causal && (GR ? i == kb : t == 0)) || (WIN && causal && i * BW + BW - 1 > hi_first) ||
           i * BW + c0 + kC > N)
         block(std::true_type{});
       else
@@ -604,13 +616,13 @@ cudaError_t tc_bwd_wide(const Problem& p, const void* Q, const void* K, const vo
         !make_tmap_bf16(&k, K, N, d, p.BHkv, BW) || !make_tmap_bf16(&v, V, N, d, p.BHkv, BW))
       return cudaErrorInvalidValue;
     const int nb = static_cast<int>((N + BW - 1) / BW);
-    auto row = p.window > 0 ? bwd_row_wide_kernel<128, false, true> : bwd_row_wide_kernel<128, false, false>;
+    auto row = banded(p) ? bwd_row_wide_kernel<128, false, true> : bwd_row_wide_kernel<128, false, false>;
     cudaError_t e = cudaFuncSetAttribute(row, cudaFuncAttributeMaxDynamicSharedMemorySize, RowLay<128>::bytes);
     if (e != cudaSuccess) return e;
     row<<<static_cast<unsigned>(nb * BH), kThreads, RowLay<128>::bytes, st>>>(
         q, g, k, v, static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), lse,
         static_cast<__nv_bfloat16*>(dQ), ws, static_cast<int>(N), static_cast<int>(Np), nb, static_cast<int>(BH),
-        p.scale, p.scale * kLog2e, p.causal, static_cast<int>(eff_window_tc(p)), p.group, static_cast<int>(d));
+        p.scale, p.scale * kLog2e, p.causal, make_band(p, eff_window_tc(p), false), p.group, static_cast<int>(d));
     return cudaGetLastError();
   }
   alignas(64) CUtensorMap q, g, k, v, s;
@@ -624,7 +636,7 @@ cudaError_t tc_bwd_wide(const Problem& p, const void* Q, const void* K, const vo
   const int nb = static_cast<int>((N + BW - 1) / BW);
   cudaError_t e = cudaSuccess;
   if (passes & 1) {
-    auto row = p.window > 0 ? (gproj ? bwd_row_wide_kernel<64, true, true> : bwd_row_wide_kernel<64, false, true>)
+    auto row = banded(p) ? (gproj ? bwd_row_wide_kernel<64, true, true> : bwd_row_wide_kernel<64, false, true>)
                             : (gproj ? bwd_row_wide_kernel<64, true> : bwd_row_wide_kernel<64, false>);
     const int bytes = gproj ? RowLay<64, true>::bytes : RowLay<64, false>::bytes;
     e = cudaFuncSetAttribute(row, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
@@ -632,12 +644,12 @@ cudaError_t tc_bwd_wide(const Problem& p, const void* Q, const void* K, const vo
     row<<<static_cast<unsigned>(nb * BH), kThreads, bytes, st>>>(
         q, g, k, v, static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), lse,
         static_cast<__nv_bfloat16*>(dQ), ws, static_cast<int>(N), static_cast<int>(Np), nb, static_cast<int>(BH),
-        p.scale, c, p.causal, static_cast<int>(eff_window_tc(p)), p.group, static_cast<int>(d));
+        p.scale, c, p.causal, make_band(p, eff_window_tc(p), false), p.group, static_cast<int>(d));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (passes & 2) {
     // Windowed: the grouped tile loop (which also serves ungrouped heads).
-    auto kern = p.window > 0 ? (gproj ? bwd_col_wide_kernel<true, true, true> : bwd_col_wide_kernel<true, false, true>)
+    auto kern = banded(p) ? (gproj ? bwd_col_wide_kernel<true, true, true> : bwd_col_wide_kernel<true, false, true>)
                 : gproj ? (p.group > 1 ? bwd_col_wide_kernel<true, true> : bwd_col_wide_kernel<false, true>)
                         : (p.group > 1 ? bwd_col_wide_kernel<true, false> : bwd_col_wide_kernel<false, false>);
     const int bytes = gproj ? ColLayT<true>::bytes : ColLayT<false>::bytes;
@@ -645,7 +657,7 @@ cudaError_t tc_bwd_wide(const Problem& p, const void* Q, const void* K, const vo
     if (e != cudaSuccess) return e;
     kern<<<static_cast<unsigned>(nb * p.BHkv), kThreads, bytes, st>>>(
         k, v, q, g, s, static_cast<__nv_bfloat16*>(dK), static_cast<__nv_bfloat16*>(dV), static_cast<int>(N), nb,
-        static_cast<int>(p.BHkv), p.scale, c, p.causal, static_cast<int>(eff_window_tc(p)), p.group, static_cast<int>(d));
+        static_cast<int>(p.BHkv), p.scale, c, p.causal, make_band(p, eff_window_tc(p), true), p.group, static_cast<int>(d));
     e = cudaGetLastError();
   }
   return e;

@@ -74,14 +74,14 @@ __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int rows, int k)
   return ptx::sdesc_sw128(base + k * 16 * 128, rows * 128, 1024);
 }
 
-// WIN: the causal sliding window is in force (win); the instances without it carry none
-// of its arithmetic.
+// WIN: a banded causal mask is in force (bd: the sliding window and/or the document
+// bounds); the instances without it carry none of its arithmetic.
 template <int D, bool PB, bool WIN>
 __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O, float* __restrict__ lse,
                const float* __restrict__ lse_in, float* __restrict__ pb, int N, int nrb, int BH, float scale,
-               float scale_log2, int causal, int win, int G, int dv) {
+               float scale_log2, int causal, Band bd, int G, int dv) {
   using Lay = Layout<D>;
   constexpr int BN = Lay::BN, NS = Lay::NS;
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -102,9 +102,12 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
   const int bh = ord.bh;
   const int kvh = bh / G;          // the key/value slice this query slice reads
   const int rb = nrb - 1 - ord.k;  // heaviest row blocks first (within a group of slices)
-  // Key blocks this row block sees: j0 + j for j < nkv.  win: the causal window (key k
-  // visible to row i iff i - win < k <= i; larger than N when there is none).
-  const int j0 = (WIN && causal) ? max(0, rb * BM - win + 1) / BN : 0;
+  // Key blocks this row block sees: j0 + j for j < nkv.  bd: the banded causal mask (row i
+  // sees the keys bd.row_lo(i) <= k <= i: the window and/or the document bounds).
+  const int j0 = (WIN && causal) ? bd.row_lo(bh, rb * BM) / BN : 0;
+  // the lowest key a row of the block sees at the block's last row (rows at or past N
+  // looked up at N - 1): blocks starting below it hold keys some row does not see
+  const int lo_last = (WIN && causal) ? bd.row_lo(bh, min(rb * BM + BM - 1, N - 1)) : 0;
   const int nkv = (BN == BM ? (causal ? rb + 1 : nrb) : (causal ? ((rb + 1) * BM + BN - 1) / BN : (N + BN - 1) / BN)) - j0;
 
   if (threadIdx.x == 0) {
@@ -201,6 +204,7 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     const int64_t row = static_cast<int64_t>(rb) * BM + r;
     const float L2 = row < N ? lse_in[static_cast<int64_t>(bh) * N + row] * kLog2e : 0.f;
+    const int lo_row = (WIN && causal) ? bd.row_lo(bh, row) : 0;
     const uint64_t c2 = tc::pk2f(scale_log2, scale_log2), nL2 = tc::pk2f(-L2, -L2);
     for (int j = 0; j < nkv; ++j) {
       wait(s_full, j & 1);
@@ -208,9 +212,9 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
       const int kb = j0 + j;
       // Keys of this block past the row (causal), or past N, or below the row's window.
       const bool diag = causal ? (BN == BM ? kb == rb : kb * BN + BN - 1 > rb * BM) : (j == nkv - 1 && (N % BN) != 0);
-      const bool low = WIN && causal && kb * BN < rb * BM + BM - win;
+      const bool low = WIN && causal && kb * BN < lo_last;
       const int klim = causal ? ((WIN || BN != BM) ? rb * BM + r - kb * BN : r) : N - 1 - kb * BN;
-      const int klo = (WIN && causal) ? rb * BM + r - win + 1 - kb * BN : 0;
+      const int klo = (WIN && causal) ? lo_row - kb * BN : 0;
       uint32_t v[BN / 32][32];
 #pragma unroll
       for (int ch = 0; ch < BN / 32; ++ch) ptx::tmem_ld32(tS + lane_off + ch * 32, v[ch]);
@@ -259,6 +263,7 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
     const int r = threadIdx.x;                       // TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     const int64_t row = static_cast<int64_t>(rb) * BM + r;
+    const int lo_row = (WIN && causal) ? bd.row_lo(bh, row) : 0;
     float m = -INFINITY, l = 0.f;
     for (int j = 0; j < nkv; ++j) {
       wait(s_full, j & 1);
@@ -268,9 +273,9 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
       // past N (TMA reads them as zeros).
       const int kb = j0 + j;
       const bool diag = causal ? (BN == BM ? kb == rb : kb * BN + BN - 1 > rb * BM) : (j == nkv - 1 && (N % BN) != 0);
-      const bool low = WIN && causal && kb * BN < rb * BM + BM - win;
+      const bool low = WIN && causal && kb * BN < lo_last;
       const int klim = causal ? ((WIN || BN != BM) ? rb * BM + r - kb * BN : r) : N - 1 - kb * BN;  // last visible
-      const int klo = (WIN && causal) ? rb * BM + r - win + 1 - kb * BN : 0;        // first visible key, relative
+      const int klo = (WIN && causal) ? lo_row - kb * BN : 0;  // first visible key, relative
       // The whole BN-column S row in registers: BN / 32 loads, one wait.
       uint32_t v[BN / 32][32];
 #pragma unroll
@@ -382,12 +387,12 @@ cudaError_t launch(const Problem& p, const void* Q, const void* K, const void* V
     return cudaErrorInvalidValue;
   const int nrb = static_cast<int>((p.N + BM - 1) / BM);
   const size_t smem = Layout<D>::bytes;
-  auto kern = p.window > 0 ? fwd_kernel<D, PB, true> : fwd_kernel<D, PB, false>;
+  auto kern = banded(p) ? fwd_kernel<D, PB, true> : fwd_kernel<D, PB, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   kern<<<static_cast<unsigned>(nrb * p.BH), kThreads, smem, st>>>(
       mq, mk, mv, static_cast<__nv_bfloat16*>(O), lse, lse_in, pb, static_cast<int>(p.N), nrb,
-      static_cast<int>(p.BH), p.scale, p.scale * kLog2e, p.causal, static_cast<int>(eff_window_tc(p)), p.group,
+      static_cast<int>(p.BH), p.scale, p.scale * kLog2e, p.causal, make_band(p, eff_window_tc(p), false), p.group,
       static_cast<int>(p.d));
   return cudaGetLastError();
 }

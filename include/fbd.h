@@ -65,6 +65,12 @@
  *               without GProj, BoB) is that of attention under this mask; row
  *               blocks skip the key blocks wholly outside every row's window and
  *               column blocks the query blocks that see none of their keys.
+ *   Document mask ([BoB] "When FlashBoB changes the engineering plan" lists flexible
+ *               masks among the next extensions; the reading here is the mask of packed
+ *               batches): with desc->seg_lo / seg_hi set (attn_segment_bounds), query i
+ *               sees the keys j <= i of its own document, every operation is that of
+ *               attention under this mask, and the passes skip the blocks no row of
+ *               theirs can see, as for the window.
  *   Grouped key/value heads ([BoB] "When FlashBoB changes the engineering plan"
  *               lists shared keys and values among the next extensions; the reading
  *               here is the usual grouped-query one): with g = desc->group > 1 the tensors on the key
@@ -88,9 +94,10 @@ extern "C" {
 typedef enum {
   ATTN_OK = 0,
   ATTN_ERR_INVALID_ARG = 1,  /* NULL/negative/overlapping arguments, non-finite scale,
-                                group < 0 or not dividing H, window < 0 */
-  ATTN_ERR_UNSUPPORTED = 2,  /* causal not 0 or 1, window > 0 without causal = 1,
-                                d not supported, unknown dtype */
+                                group < 0 or not dividing H, window < 0, only one of
+                                seg_lo / seg_hi set */
+  ATTN_ERR_UNSUPPORTED = 2,  /* causal not 0 or 1, window > 0 or a document mask without
+                                causal = 1, d not supported, unknown dtype */
   ATTN_ERR_ALIGNMENT = 3,    /* a pointer is not 16-byte aligned */
   ATTN_ERR_WORKSPACE = 4,    /* workspace NULL or smaller than the *_workspace_bytes query */
   ATTN_ERR_LAUNCH = 5,       /* CUDA rejected a launch or a tensor-map encode */
@@ -116,7 +123,32 @@ typedef struct {
                           (W >= N is the same as none).  A flexible mask ([BoB] "When
                           FlashBoB changes the engineering plan" lists flexible masks
                           among the next extensions); every operation honours it. */
+  /* Document (segment) mask, the second flexible mask: device arrays [B, N] written by
+     attn_segment_bounds from per-token segment ids (both NULL: no document mask; both
+     set: causal must be 1).  Query i of batch row b sees key j iff
+     seg_lo[b][i] <= j <= i, i.e. j <= i and seg[b][j] == seg[b][i]; combined with a
+     window when both are given.  16-byte aligned, B*N int32 each, read only.  See
+     "Document mask" above. */
+  const int32_t* seg_lo;
+  const int32_t* seg_hi;
 } attn_desc_t;
+
+/* Bounds of the document (segment) mask.  [BoB] "When FlashBoB changes the engineering
+ * plan" lists flexible masks among the next extensions; this is the mask of packed
+ * batches: documents laid back to back along N, each attending only within itself.
+ *   In:  seg [B, N] int32 device array, the segment (document) id of every token, non-
+ *        decreasing along each batch row (each document one run of equal ids).
+ *   Out: seg_lo [B, N]: for token i, the first index of its run (its document's first key);
+ *        seg_hi [B, N]: for token j, the last index of its run (its document's last query).
+ *   One launch on `stream` (binary searches; the ids are read, nothing else).  Pass both
+ *   outputs in attn_desc_t.seg_lo / seg_hi to every call of the same batch: query i then
+ *   sees exactly the keys j <= i with seg[j] == seg[i].  For ids that are not non-
+ *   decreasing the bounds are those of the searches (still lo <= i <= hi, every row keeps
+ *   its own key), not that mask.  Errors: B or N negative, or B*N >= 2^40
+ *   (ATTN_ERR_INVALID_ARG); NULL, unaligned (16 bytes) or overlapping arrays; B*N == 0 is
+ *   ATTN_OK with no launch. */
+attn_status_t attn_segment_bounds(int64_t B, int64_t N, const int32_t* seg, int32_t* seg_lo, int32_t* seg_hi,
+                                  void* stream);
 
 /* Forward.  [FA] "The Flash Attention algorithm", "Online softmax recurrence",
  * causal masking; [GP] "Why the error appears late" (max subtracted before the

@@ -189,3 +189,35 @@ def test_binding_derives_the_group_from_the_key_heads():
     assert fbd.make_desc(q).group == 1
     with pytest.raises(fbd.FbdError):
         fbd.make_desc(q, K=torch.zeros(2, 4, 8, 64))  # 4 key/value heads do not divide 6
+
+
+def test_document_mask_descriptor_checks():
+    """seg_lo / seg_hi: both or neither, only with the causal mask, 16-byte aligned, and
+    never overlapping an output."""
+    lo, hi = ctypes.c_void_p(FAKE + (9 << 30)), ctypes.c_void_p(FAKE + (10 << 30))
+    d = desc()
+    d.seg_lo = lo
+    assert fwd(d) == INVALID                    # only one of the two
+    d.seg_hi = hi
+    d.causal = 0
+    assert fwd(d) == UNSUP                      # a document mask needs causal = 1
+    d.causal = 1
+    d.seg_hi = ctypes.c_void_p(FAKE + (10 << 30) + 4)
+    assert fwd(d) == ALIGN
+    d.seg_hi = hi
+    p = ptrs(5)
+    p[3] = ctypes.c_void_p(lo.value)              # O placed on seg_lo
+    assert fwd(d, p) == INVALID
+    assert "seg_lo" in lib.attn_last_error().decode() or "overlaps" in lib.attn_last_error().decode()
+
+
+def test_segment_bounds_argument_checks():
+    f = lib.attn_segment_bounds
+    a, b, c = ptrs(3)
+    assert f(-1, 4, a, b, c, None) == INVALID
+    assert f(2, -4, a, b, c, None) == INVALID
+    assert f(0, 5, None, None, None, None) == OK       # empty: nothing launched
+    assert f(2, 8, None, b, c, None) == INVALID
+    assert f(2, 8, a, b, b, None) == INVALID           # the two outputs overlap
+    assert f(2, 8, a, a, c, None) == INVALID           # an output overlaps the ids
+    assert f(2, 8, ctypes.c_void_p(FAKE + 8), b, c, None) == ALIGN
