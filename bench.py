@@ -581,7 +581,7 @@ def sweep(args):
                 ("fullday_B2H12N23400d64", 2, 12, 23400, 64, ("fwd", "bwd")),
                 ("largekey_B8H8N2048d128", 8, 8, 2048, 128, ("bwd", "bwd_gproj")),
                 ("headdim128_B4H12N8192d128", 4, 12, 8192, 128, ("fwd", "bwd", "bwd_gproj", "bob", "bob_gproj")),
-                ("headdim256_B4H12N8192d256", 4, 12, 8192, 256, ("fwd",))]
+                ("headdim256_B4H12N8192d256", 4, 12, 8192, 256, ("fwd", "bwd"))]
     reps, warm = max(args.steps, 1), max(args.warmup, 1)
     for name, B, H, N, d, ops in configs:
         torch.cuda.empty_cache()

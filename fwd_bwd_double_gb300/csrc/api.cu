@@ -133,12 +133,15 @@ namespace fbd {
 // zeros, which add nothing to any product; nothing past d is stored).  BoB at
 // d > 64 splits each block over two CTAs by output half: its row pass's four d-wide
 // accumulators would otherwise fill the 512 TMEM columns.  At d = 256 the forward
-// runs on tensor cores (64-key blocks, O in 256 TMEM columns); the backward and BoB
-// run on the CUDA-core kernels (simt.cu): their d-wide accumulators do not fit TMEM.
+// runs on tensor cores (64-key blocks, O in 256 TMEM columns), and so does the backward
+// without GProj (one stage of streamed tiles; the column pass split over two CTAs by
+// output half); the GProj backward and BoB at d = 256 run on the CUDA-core kernels
+// (simt.cu): their d-wide accumulators do not fit TMEM.
 bool tc_supports(int op, int64_t d) {
-  if (d == 256) return op == 0;
+  if (d == 256) return op == 0 || op == 1;  // the backward without GProj (bwd_gproj_on_tc)
   return d == 32 || d == 64 || d == 96 || d == 128;
 }
+bool bwd_gproj_on_tc(int64_t d) { return d <= 128; }
 }  // namespace fbd
 
 namespace fbd {
@@ -217,7 +220,7 @@ attn_status_t attn_bwd_passes(const attn_desc_t* desc, const void* Q, const void
   if ((s = check_ptrs(in.s, in.n, out, 4)) != ATTN_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   float4* ws = static_cast<float4*>(workspace);
-  if (!tc_path(p, 1))
+  if (!tc_path(p, 1) || (gproj && !fbd::bwd_gproj_on_tc(p.d)))
     return launch_status(fbd::simt_bwd(p, Q, K, V, O, dO, lse, dQ, dK, dV, gproj, ws, passes, st));
   // Both passes in one call: the single-pass form where it exists (bf16, d <= 64, no GProj).
   if (passes == (ATTN_ROW_PASS | ATTN_COL_PASS) && fbd::bwd_fused_applies(p, gproj != 0))

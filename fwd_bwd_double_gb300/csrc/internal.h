@@ -137,6 +137,7 @@ __host__ __device__ inline int64_t bob_rho_pitch(int64_t N) { return (N + 3) & ~
 
 // Which kernels exist for a given (op, dtype, d): false means ATTN_ERR_UNSUPPORTED.
 bool tc_supports(int op, int64_t d);  // op: 0 fwd, 1 bwd, 2 bob
+bool bwd_gproj_on_tc(int64_t d);       // the GProj backward has tensor-core kernels at this d
 
 // Device status words (bit FBD_ERR_TIMEOUT), read-and-cleared per translation unit.
 uint32_t tc_fwd_take_error();

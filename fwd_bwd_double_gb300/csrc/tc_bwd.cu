@@ -43,8 +43,10 @@ constexpr int BM = 128;        // rows held by a CTA (queries, or keys in the co
 constexpr int BN = 64;         // rows of a streamed block
 // Shared-memory stages of streamed tiles: deep enough that a tile is requested
 // several tile-times before its MMA needs it (L2/HBM latency under load).
+// At d = 256 one stage is all that fits beside the held block (64 KB a tile); the MMA
+// warp then finishes each block's products before the next block's tiles (see below).
 template <int D>
-constexpr int stages() { return D == 64 ? 6 : 4; }
+constexpr int stages() { return D == 64 ? 6 : D == 256 ? 1 : 4; }
 constexpr int kCompute = 256;  // 8 compute warps
 constexpr int kThreads = kCompute + 64;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -184,6 +186,8 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
       };
       // Block j's tiles go into the columns block j-1's tiles left as soon as the
       // compute warps have copied those out (`consumed`), ahead of block j-1's products.
+      // With a single stage the block's own products come first (they read K_j, which
+      // the next block's load replaces).
       wait(q_full, 0);
       for (int j = 0; j < nkv; ++j) {
         const int s = j % NS, b = j % NB;
@@ -199,9 +203,13 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
           ptx::mma_ss_e(tmem + Lay::cdP + b * BN, tc::kmajor_desc(sdO, BM, kk), tc::kmajor_desc(vt, BN, kk), idS,
                       kk > 0);
         ptx::mma_commit_e(&s_full[b]);
-        if (j > 0) products(j - 1);
+        if constexpr (NS == 1) {
+          products(j);
+        } else if (j > 0) {
+          products(j - 1);
+        }
       }
-      if (nkv > 0) products(nkv - 1);
+      if (NS > 1 && nkv > 0) products(nkv - 1);
       ptx::mma_commit_e(acc_full);
     }
   } else {
@@ -333,8 +341,12 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
 }
 
 // ============================================================= column pass
+// At d = 256 the accumulators dV, dK of the whole head dim would take 512 TMEM columns
+// beside the tiles: each key block runs as two CTAs, CTA h accumulating and writing output
+// columns [DO h, DO h + DO) (DO = 128); both compute the full score tiles.
 template <int D, int NB, bool GP>
 struct ColLay {
+  static constexpr int DO = D == 256 ? 128 : D;  // output columns a CTA accumulates
   static constexpr int NS = stages<D>();
   static constexpr int kHeld = BM * D * 2;
   static constexpr int kStream = BN * D * 2;
@@ -343,8 +355,8 @@ struct ColLay {
   static constexpr int oBar = oSt + NS * kStat;
   static constexpr int bytes = oBar + 256;
   static constexpr int cS = 0, cdP = NB * BN, cP = 2 * NB * BN, cdS = cP + NB * BN / 2, cG = cdS + NB * BN / 2;
-  static constexpr int cdV = cG + (GP ? NB * BN / 2 : 0), cdK = cdV + D;
-  static constexpr int cols = cdK + D;
+  static constexpr int cdV = cG + (GP ? NB * BN / 2 : 0), cdK = cdV + DO;
+  static constexpr int cols = cdK + DO;
   static_assert(cols <= 512, "TMEM budget");
 };
 
@@ -358,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    int dv) {
   using Lay = ColLay<D, NB, GP>;
   static_assert(NB == 1, "one score-tile buffer, released early");
-  constexpr int NS = Lay::NS;
+  constexpr int NS = Lay::NS, DO = Lay::DO, HV = D / DO;  // HV CTAs per key block, one per output part
   extern __shared__ __align__(1024) uint8_t sm[];
   uint64_t* k_full = reinterpret_cast<uint64_t*>(sm + Lay::oBar);
   uint64_t* full = k_full + 1;
@@ -373,7 +385,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkb = (N + BM - 1) / BM;
-  const tc::Order ord = tc::grid_order(BHkv, nkb);
+  const int part = HV > 1 ? static_cast<int>(blockIdx.x) % HV : 0;  // output columns [DO part, DO part + DO)
+  const tc::Order ord = tc::grid_order_at(static_cast<int>(blockIdx.x) / HV, BHkv, nkb);
   const int kvh = ord.bh;  // key/value slice; its G query slices are kvh * G + h, h < G
   const int kb = ord.k;  // first key blocks have the most rows: first
   const int nq = (N + BN - 1) / BN;
@@ -436,14 +449,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 9) {
     if (ok) {  // all 32 lanes; one elected lane issues each MMA and commit
       constexpr uint32_t idS = ptx::idesc_bf16(BM, BN, 0, 0);
-      constexpr uint32_t idKV = ptx::idesc_bf16(BM, D, 0, 1);
+      constexpr uint32_t idKV = ptx::idesc_bf16(BM, DO, 0, 1);
       const uint32_t sK = ptx::smem_u32(sm + Lay::oK), sV = ptx::smem_u32(sm + Lay::oV);
       const uint32_t sQ = ptx::smem_u32(sm + Lay::oQ), sdO = ptx::smem_u32(sm + Lay::odO);
+      const uint32_t po = static_cast<uint32_t>(part * (DO / 64) * BN * 128);  // this CTA's column slabs
       auto products = [&](int t) {
         const int b = t % NB, s = t % NS;
         wait(&ds_ready[b], (t / NB) & 1);
         ptx::tc_fence_after();
-        const uint32_t qt = sQ + s * Lay::kStream, gt = sdO + s * Lay::kStream;
+        const uint32_t qt = sQ + s * Lay::kStream + po, gt = sdO + s * Lay::kStream + po;
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k) {
           ptx::mma_ts_e(tmem + Lay::cdV, tmem + Lay::cP + b * (BN / 2) + k * 8, tc::mnmajor_desc(gt, BN, k), idKV,
@@ -472,9 +486,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::mma_ss_e(tmem + Lay::cdP + b * BN, tc::kmajor_desc(sV, BM, kk), tc::kmajor_desc(gt, BN, kk), idS,
                       kk > 0);
         ptx::mma_commit_e(&s_full[b]);
-        if (t > 0) products(t - 1);
+        if constexpr (NS == 1) {  // one stage: the block's products before the next block's load
+          products(t);
+        } else if (t > 0) {
+          products(t - 1);
+        }
       }
-      if (nt > 0) products(nt - 1);
+      if (NS > 1 && nt > 0) products(nt - 1);
       ptx::mma_commit_e(acc_full);
     }
   } else {
@@ -540,20 +558,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool live = key < N;
     const size_t rowoff = (static_cast<size_t>(kvh) * N + key) * dv;
 #pragma unroll
-    for (int cc = 0; cc < D / 2; cc += 32) {
+    for (int cc = 0; cc < DO / 2; cc += 32) {
       uint32_t a[32], g[32];
-      ptx::tmem_ld32(tmem + Lay::cdV + hf * (D / 2) + cc + lo, a);
-      ptx::tmem_ld32(tmem + Lay::cdK + hf * (D / 2) + cc + lo, g);
+      ptx::tmem_ld32(tmem + Lay::cdV + hf * (DO / 2) + cc + lo, a);
+      ptx::tmem_ld32(tmem + Lay::cdK + hf * (DO / 2) + cc + lo, g);
       ptx::tmem_wait_ld();
-      if (live && hf * (D / 2) + cc < dv) {
+      const int col = part * DO + hf * (DO / 2) + cc;  // first of the 32 output columns
+      if (live && col < dv) {
         uint32_t ov[16], ok2[16];
 #pragma unroll
         for (int u = 0; u < 32; u += 2) {
           ov[u >> 1] = ptx::pack_bf16(f(a[u]), f(a[u + 1]));
           ok2[u >> 1] = ptx::pack_bf16(scale * f(g[u]), scale * f(g[u + 1]));
         }
-        uint4* dvp = reinterpret_cast<uint4*>(dV + rowoff + hf * (D / 2) + cc);
-        uint4* dk2 = reinterpret_cast<uint4*>(dK + rowoff + hf * (D / 2) + cc);
+        uint4* dvp = reinterpret_cast<uint4*>(dV + rowoff + col);
+        uint4* dk2 = reinterpret_cast<uint4*>(dK + rowoff + col);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           dvp[u] = make_uint4(ov[4 * u], ov[4 * u + 1], ov[4 * u + 2], ov[4 * u + 3]);
@@ -603,7 +622,7 @@ cudaError_t launch(const Problem& p, const void* Q, const void* K, const void* V
                 : p.group > 1 ? bwd_col_kernel<D, NBC, GP, true> : bwd_col_kernel<D, NBC, GP, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::bytes);
     if (e != cudaSuccess) return e;
-    kern<<<static_cast<unsigned>(nrb * p.BHkv), kThreads, Lay::bytes, st>>>(
+    kern<<<static_cast<unsigned>(nrb * p.BHkv * (D / Lay::DO)), kThreads, Lay::bytes, st>>>(
         k128, v128, q64, do64, s64, static_cast<__nv_bfloat16*>(dK), static_cast<__nv_bfloat16*>(dV),
         static_cast<int>(N), static_cast<int>(p.BHkv), p.scale, c, p.causal, make_band(p, eff_window_tc(p), true),
         p.group, static_cast<int>(d));
@@ -621,6 +640,12 @@ cudaError_t tc_bwd(const Problem& p, const void* Q, const void* K, const void* V
   // d <= 64, with or without GProj: the 128-wide kernels.
   if (p.d <= 64) return tc_bwd_wide(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st, gproj != 0);
   if (gproj) return launch<128, 1, 1, true>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st);
+  // d = 256 without GProj: both passes here (one stage; the column pass in two output
+  // halves).  GProj at d = 256 would need 704 TMEM columns in the row pass.
+  if (p.d > 128) {
+    if (gproj) return cudaErrorInvalidValue;
+    return launch<256, 1, 1, false>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st);
+  }
   // d = 96, 128 without GProj: the 128-wide row pass, then this file's column pass
   // (both use the same pair-interleaved row statistics).
   if (passes & 1) {

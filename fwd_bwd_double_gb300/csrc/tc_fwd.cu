@@ -330,14 +330,25 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
       const float2 rsa = tc::unpk2(tc::add2(tc::add2(rs4[0], rs4[1]), tc::add2(rs4[2], rs4[3])));
       const float rs = rsa.x + rsa.y;
       if (__any_sync(0xffffffffu, moved)) {  // rescale O for rows whose max moved
+        // up to 64 columns per round trip: both loads in flight, one wait, packed multiplies
+        constexpr int R = D < 64 ? D / 32 : 2;
+        const uint64_t a2 = tc::pk2f(alpha, alpha);
 #pragma unroll
-        for (int ch = 0; ch < D / 32; ++ch) {
-          uint32_t o[32];
-          ptx::tmem_ld32(tO + lane_off + ch * 32, o);
+        for (int c0 = 0; c0 < D / 32; c0 += R) {
+          uint32_t o[R][32];
+#pragma unroll
+          for (int u = 0; u < R; ++u) ptx::tmem_ld32(tO + lane_off + (c0 + u) * 32, o[u]);
           ptx::tmem_wait_ld();
 #pragma unroll
-          for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
-          ptx::tmem_st32(tO + lane_off + ch * 32, o);
+          for (int u = 0; u < R; ++u) {
+#pragma unroll
+            for (int t = 0; t < 32; t += 2) {
+              const float2 v = tc::unpk2(tc::mul2(tc::pk2(o[u][t], o[u][t + 1]), a2));
+              o[u][t] = __float_as_uint(v.x);
+              o[u][t + 1] = __float_as_uint(v.y);
+            }
+            ptx::tmem_st32(tO + lane_off + (c0 + u) * 32, o[u]);
+          }
         }
       }
       ptx::tmem_wait_st();

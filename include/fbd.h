@@ -35,11 +35,11 @@
  *               {ATTN_F32, ATTN_BF16}.  Anything else returns ATTN_ERR_UNSUPPORTED
  *               (or ATTN_ERR_INVALID_ARG) before any launch.
  *   Kernels:    the shape decides, never a failure: bf16 attn_fwd, attn_bwd and
- *               attn_bob at d in {32, 64, 96, 128}, and bf16 attn_fwd at d = 256,
- *               run on the tcgen05/TMA tensor-core kernels (d = 32 and 96 on those
- *               of d = 64 and 128, the head dim zero-padded in shared memory);
- *               float32 inputs at every d and the bf16 backward and BoB at d = 256
- *               run on the CUDA-core kernels (fp32 arithmetic;
+ *               attn_bob at d in {32, 64, 96, 128}, and bf16 attn_fwd and attn_bwd
+ *               (without GProj) at d = 256, run on the tcgen05/TMA tensor-core kernels
+ *               (d = 32 and 96 on those of d = 64 and 128, the head dim zero-padded in
+ *               shared memory); float32 inputs at every d, and the bf16 GProj backward
+ *               and BoB at d = 256, run on the CUDA-core kernels (fp32 arithmetic;
  *               bf16 inputs widened on load, outputs rounded once on store), which
  *               are exact to fp32 rounding but one to two orders of magnitude
  *               slower.

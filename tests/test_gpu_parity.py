@@ -701,3 +701,14 @@ def test_window_long_sampled(win):
     rows, cols = sample_rows_cols(w.N, np.random.default_rng(win))
     errs = sampled_check(w, got, ("bwd", "bob"), heads=[0, 1], rows=rows, cols=cols, causal=oracle.Window(win))
     print(w.name, win, {k: f"{v:.2e}" for k, v in errs.items()})
+
+
+# The backward at d = 256 on tensor cores (without GProj): a row pass with one stage of
+# 64-key tiles, a column pass split over two CTAs by output half.  Several row and key
+# blocks, a ragged tail, causal and not, grouped heads, a window.
+@pytest.mark.parametrize("causal,win,group", [(True, 0, 1), (False, 0, 1), (True, 300, 1), (True, 0, 3)])
+def test_backward_head_dim_256_tensor_cores(causal, win, group):
+    w = W.Workload(f"bwd256_B1H3N1000d256_g{group}_bf16", 1, 3, 1000, 256, "bf16", group=group)
+    got = run_ops(w, to_device(inputs(w), w), ops=("bwd",), causal=causal, window=win)
+    errs = check_full(w, got, ("bwd",), causal=causal, window=win)
+    print(w.name, causal, win, {k: f"{v:.2e}" for k, v in errs.items()})
