@@ -141,11 +141,11 @@ def traffic_for(kernel, w):
 # the bench command; see profiles/), keyed by (kernel, workload), with the source
 # hash of the kernel file the counters were taken on.
 MEASURED_TRAFFIC = {
-    ("fwd", "gpt2small_B4H12N8192d64"): {"bytes": 184851200, "source": "tc_fwd.cu", "sha": "5d3b6cedd24a4cdc"},
-    ("bwd_row", "gpt2small_B4H12N8192d64"): {"bytes": 293592576, "source": "tc_bwd_wide.cu", "sha": "d42757ea38eeed42"},
-    ("bwd_col", "gpt2small_B4H12N8192d64"): {"bytes": 276359936, "source": "tc_bwd_wide.cu", "sha": "d42757ea38eeed42"},
-    ("bob_row", "gpt2small_B4H12N8192d64"): {"bytes": 502947328, "source": "tc_bob.cu", "sha": "0ff6073741142524"},
-    ("bob_col", "gpt2small_B4H12N8192d64"): {"bytes": 438278656, "source": "tc_bob.cu", "sha": "0ff6073741142524"},
+    ("fwd", "gpt2small_B4H12N8192d64"): {"bytes": 185246720, "source": "tc_fwd.cu", "sha": "b3dd2dc992a7c400"},
+    # the backward interval: its three launches (statistics, key-block pass, dQ write) summed
+    ("bwd", "gpt2small_B4H12N8192d64"): {"bytes": 732555264, "source": "tc_bwd_fused.cu", "sha": "31685e0ef3cd0787"},
+    ("bob_row", "gpt2small_B4H12N8192d64"): {"bytes": 502313984, "source": "tc_bob.cu", "sha": "e49e09428023f3d1"},
+    ("bob_col", "gpt2small_B4H12N8192d64"): {"bytes": 438223872, "source": "tc_bob.cu", "sha": "e49e09428023f3d1"},
 }
 
 
