@@ -123,6 +123,8 @@ attn_status_t launch_status(cudaError_t e) {
 }
 
 bool tc_path(const fbd::Problem& p, int op) { return p.dtype == ATTN_BF16 && fbd::tc_supports(op, p.d); }
+// float32 inputs on the tensor cores (three tf32 products per product) where tc_f32.cu has kernels.
+bool tc32_path(const fbd::Problem& p) { return p.dtype == ATTN_F32 && fbd::tc32_supports(p.d); }
 
 }  // namespace
 
@@ -166,6 +168,7 @@ attn_status_t attn_fwd(const attn_desc_t* desc, const void* Q, const void* K, co
   const Span out[] = {span("O", O, tb), span("lse", lse, sb)};
   if ((s = check_ptrs(in.s, in.n, out, 2)) != ATTN_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (tc32_path(p)) return launch_status(fbd::tc32_fwd(p, Q, K, V, O, lse, st));
   if (!tc_path(p, 0)) return launch_status(fbd::simt_fwd(p, Q, K, V, O, lse, st));
   return launch_status(fbd::tc_fwd(p, Q, K, V, O, lse, st));
 }
@@ -220,6 +223,7 @@ attn_status_t attn_bwd_passes(const attn_desc_t* desc, const void* Q, const void
   if ((s = check_ptrs(in.s, in.n, out, 4)) != ATTN_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   float4* ws = static_cast<float4*>(workspace);
+  if (tc32_path(p)) return launch_status(fbd::tc32_bwd(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st));
   if (!tc_path(p, 1) || (gproj && !fbd::bwd_gproj_on_tc(p.d)))
     return launch_status(fbd::simt_bwd(p, Q, K, V, O, dO, lse, dQ, dK, dV, gproj, ws, passes, st));
   // Both passes in one call: the single-pass form where it exists (bf16, d <= 64, no GProj).
@@ -257,6 +261,8 @@ attn_status_t attn_bob_passes(const attn_desc_t* desc, const void* Q, const void
   if ((s = check_ptrs(in.s, in.n, out, 5)) != ATTN_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   float4* ws = static_cast<float4*>(workspace);
+  if (tc32_path(p))
+    return launch_status(fbd::tc32_bob(p, Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ, gK, gV, gdO, ws, passes, st));
   if (!tc_path(p, 2))
     return launch_status(fbd::simt_bob(p, Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ, gK, gV, gdO, gp, ws, passes, st));
   if (p.d > 64)
@@ -309,7 +315,8 @@ attn_status_t attn_device_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "CUDA: %s", cudaGetErrorString(e));
   const uint32_t flags = fbd::tc_fwd_take_error() | fbd::tc_bwd_take_error() | fbd::tc_bwd_wide_take_error() | fbd::tc_bwd_fused_take_error() |
-                         fbd::tc_bob_take_error() | fbd::tc_bob128_take_error() | fbd::selftest_take_error();
+                         fbd::tc_bob_take_error() | fbd::tc_bob128_take_error() | fbd::tc32_take_error() |
+                         fbd::selftest_take_error();
   if (flags != 0) return fail(ATTN_ERR_TIMEOUT, "a device-side bounded wait gave up%s");
   return ATTN_OK;
 }
@@ -337,7 +344,7 @@ const char* attn_status_string(attn_status_t status) {
 
 const char* attn_last_error(void) { return g_last_error; }
 
-const char* attn_version(void) { return "libfbd 0.1 (sm_103a: tcgen05/TMA bf16 path, CUDA-core fp32 path)"; }
+const char* attn_version(void) { return "libfbd 0.2 (sm_103a: tcgen05/TMA bf16 path, tcgen05 tf32x3 fp32 path at d <= 64, CUDA-core kernels elsewhere)"; }
 
 }  // extern "C"
 

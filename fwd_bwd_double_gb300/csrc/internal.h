@@ -81,6 +81,20 @@ cudaError_t simt_projected_dS(const Problem& p, const void* Q, const void* K, co
 // ids, hi[b][j] = last index of j's run (binary searches; ids non-decreasing along N).
 cudaError_t segment_bounds(int64_t B, int64_t N, const int* seg, int* lo, int* hi, cudaStream_t st);
 
+// float32 tensor-core path (tc_f32.cu): kind::tf32 MMAs, each product as three tf32
+// products of the operands' high and low parts, at d = 32 and 64 (tc32_supports); the
+// workspace layout is the CUDA-core kernels' (one float4 of row statistics or states per
+// row at slice pitch N).  GProj does not apply to float32 inputs.
+bool tc32_supports(int64_t d);
+cudaError_t tc32_fwd(const Problem& p, const void* Q, const void* K, const void* V, void* O, float* lse,
+                     cudaStream_t st);
+cudaError_t tc32_bwd(const Problem& p, const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                     const float* lse, void* dQ, void* dK, void* dV, float4* ws, int passes, cudaStream_t st);
+cudaError_t tc32_bob(const Problem& p, const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                     const float* lse, const void* a, const void* b, const void* c, void* gQ, void* gK, void* gV,
+                     void* gdO, float4* ws, int passes, cudaStream_t st);
+uint32_t tc32_take_error();
+
 // bf16 tensor-core path (tcgen05 + TMA).  Return cudaErrorInvalidValue if a
 // tensor map could not be encoded.
 cudaError_t tc_fwd(const Problem& p, const void* Q, const void* K, const void* V, void* O, float* lse,

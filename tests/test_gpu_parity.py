@@ -27,20 +27,34 @@ def _lib():
     __graft_entry__.build()
 
 
+def err_vs(got, ref, scale):
+    """Relative Frobenius error; for a reference that is exactly zero, the error norm over
+    `scale`.  Such outputs vanish by cancellation (at N = 1, P = 1 makes dS = dP - D = 0,
+    and with it dQ, dK, gQ, gK, gV), and an fp32 computation that does not evaluate the
+    two cancelling dot products dP = dO.V and D = dO.O in the same order leaves about
+    2^-24 sqrt(d) |dO| |V| of each: relative to zero that is no error measure, so those
+    outputs are held to the tolerance times the scale of the terms that cancel (the norm
+    of dO), as the closed forms of the one-key window are held to the scale of dO."""
+    if not np.any(np.asarray(ref)):
+        return float(np.linalg.norm(np.asarray(got, np.float64)) / scale)
+    return rel_fro(got, ref)
+
+
 def check_full(w, got, ops, causal=True, window=0):
     tol = TOL[w.dtype]
     causal = oracle.Window(window) if window else causal
+    scale = float(np.linalg.norm(inputs(w)["dO"].astype(np.float64))) or 1.0
     errs = {}
     f = oracle_full(w, "fwd", causal)
     errs["O"], errs["L"] = rel_fro(host(got["O"]), f["O"]), rel_fro(host(got["L"]), f["L"])
     if "bwd" in ops:
         b = oracle_full(w, "bwd", causal)
         for k in ("dQ", "dK", "dV"):
-            errs[k] = rel_fro(host(got[k]), b[k])
+            errs[k] = err_vs(host(got[k]), b[k], scale)
     if "bob" in ops:
         b = oracle_full(w, "bob", causal)
         for k in ("gQ", "gK", "gV", "gdO"):
-            errs[k] = rel_fro(host(got[k]), b[k])
+            errs[k] = err_vs(host(got[k]), b[k], scale)
     bad = {k: v for k, v in errs.items() if not v <= tol}
     assert not bad, f"{w.name}: errors above {tol}: {bad} (all: {errs})"
     return errs
