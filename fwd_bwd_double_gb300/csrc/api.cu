@@ -123,7 +123,7 @@ attn_status_t launch_status(cudaError_t e) {
 }
 
 bool tc_path(const fbd::Problem& p, int op) { return p.dtype == ATTN_BF16 && fbd::tc_supports(op, p.d); }
-// float32 inputs on the tensor cores (three tf32 products per product) where tc_f32.cu has kernels.
+// float32 inputs on the tensor cores (three tf32 products per product), every supported d.
 bool tc32_path(const fbd::Problem& p) { return p.dtype == ATTN_F32 && fbd::tc32_supports(p.d); }
 
 }  // namespace
@@ -169,8 +169,7 @@ attn_status_t attn_fwd(const attn_desc_t* desc, const void* Q, const void* K, co
   if ((s = check_ptrs(in.s, in.n, out, 2)) != ATTN_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (tc32_path(p)) return launch_status(fbd::tc32_fwd(p, Q, K, V, O, lse, st));
-  if (!tc_path(p, 0)) return launch_status(fbd::simt_fwd(p, Q, K, V, O, lse, st));
-  return launch_status(fbd::tc_fwd(p, Q, K, V, O, lse, st));
+  return launch_status(fbd::tc_fwd(p, Q, K, V, O, lse, st));  // bf16: tensor cores at every d
 }
 
 size_t attn_bwd_workspace_bytes(const attn_desc_t* desc, int gproj) {
@@ -344,7 +343,7 @@ const char* attn_status_string(attn_status_t status) {
 
 const char* attn_last_error(void) { return g_last_error; }
 
-const char* attn_version(void) { return "libfbd 0.2 (sm_103a: tcgen05/TMA bf16 path, tcgen05 tf32x3 fp32 path at d <= 64, CUDA-core kernels elsewhere)"; }
+const char* attn_version(void) { return "libfbd 0.2 (sm_103a: tcgen05/TMA bf16 path, tcgen05 tf32x3 fp32 path, CUDA-core kernels for bf16 GProj and BoB at d = 256)"; }
 
 }  // extern "C"
 

@@ -65,9 +65,9 @@ inline int64_t eff_window(const Problem& p) { return p.window > 0 ? p.window : p
 // block of 256 rows, so that no block bound derived from it ever binds.
 inline int64_t eff_window_tc(const Problem& p) { return p.window > 0 ? p.window : p.N + 512; }
 
-// Float32 path: CUDA-core kernels with float32 inputs/outputs (exact fp32 arithmetic).
-cudaError_t simt_fwd(const Problem& p, const void* Q, const void* K, const void* V, void* O, float* lse,
-                     cudaStream_t st);
+// CUDA-core kernels (simt.cu), bf16 inputs in fp32 arithmetic: the GProj backward and
+// BoB at d = 256, and the GProj diagnostic.  They return cudaErrorInvalidValue for
+// float32 inputs (those have tensor-core kernels at every head dim).
 cudaError_t simt_bwd(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
                      const void* dO, const float* lse, void* dQ, void* dK, void* dV, int gproj, float4* ws,
                      int passes, cudaStream_t st);

@@ -1,8 +1,8 @@
-// CUDA-core path: forward, backward and BoB in fp32 arithmetic, for float32
-// inputs at every supported head dim and for bf16 inputs at the head dims that
-// have no tensor-core kernel (bf16 is widened on load and rounded once on store;
-// with GProj the bf16 rounding of dS and P is emulated); plus the GProj
-// projected-dS diagnostic export (bf16 inputs).
+// CUDA-core path: the backward and BoB in fp32 arithmetic for the bf16 cases that
+// have no tensor-core kernel (GProj at d = 256: bf16 is widened on load and rounded
+// once on store; the bf16 rounding of dS and P is emulated), and the GProj
+// projected-dS diagnostic export.  float32 inputs run on the tf32 tensor-core kernels
+// (tc_f32.cu) at every head dim.
 //
 // Work split: one warp per query row (row passes) or per key (column passes);
 // a warp's 32 lanes each hold d/32 consecutive elements of the row's vectors, so
@@ -13,9 +13,6 @@
 // bookkeeping is warp-uniform.
 //
 // These kernels follow the same decomposition as the tensor-core path:
-//   forward: online softmax ("Flash attention for trading models", "Online
-//            softmax recurrence"), max subtracted before scaling ("FlashAttention
-//            bf16 gradient and GProj", "Why the error appears late");
 //   backward: recompute P from lse ("Backward pass: recompute instead of store");
 //   BoB: row pass with the two scalar states, column pass re-reading them
 //        ("FlashBoB: second-order attention", "Two scalar states replace
@@ -103,67 +100,6 @@ __device__ __forceinline__ Tile decode(int64_t BH, int64_t nblk, bool heavy_last
   const int64_t k = x / BH;
   t.blk = heavy_last_rows ? (nblk - 1 - k) : k;
   return t;
-}
-
-// ---------------------------------------------------------------- forward
-template <typename T, int D>
-__global__ void __launch_bounds__(kThreads) fwd_kernel(const T* __restrict__ Q, const T* __restrict__ K,
-                                                       const T* __restrict__ Vt, T* __restrict__ O,
-                                                       float* __restrict__ lse, int64_t N, int64_t BH,
-                                                       float scale, int causal, Band bd, int64_t G) {
-  constexpr int V = D / 32;
-  extern __shared__ float sm[];
-  float* Ks = sm;
-  float* Vs = sm + kTile * D;
-  const int64_t nblk = (N + kWarps - 1) / kWarps;
-  const Tile tl = decode(BH, nblk, true);
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int64_t row0 = tl.blk * kWarps, i = row0 + warp;
-  const bool live = i < N;
-  const size_t base = static_cast<size_t>(tl.bh) * N * D;
-  const size_t kvbase = static_cast<size_t>(tl.bh / G) * N * D;  // the key/value head this query head reads
-  float q[V], o[V];
-#pragma unroll
-  for (int t = 0; t < V; ++t) o[t] = 0.f;
-  if (live) load_vec(Q + base + i * D, lane, q);
-  float m = -CUDART_INF_F, l = 0.f;  // running max of raw dot products, running sum
-  const int64_t last = causal ? min(row0 + kWarps, N) - 1 : N - 1;  // last key any row of the block sees
-  // bd: the banded causal mask (row i sees the keys bd.row_lo(i) <= j <= i)
-  const int64_t first = causal ? (bd.row_lo(tl.bh, row0) / kTile) * kTile : 0;  // first key tile any row sees
-  const int64_t lo_i = causal ? bd.row_lo(tl.bh, i) : 0;  // this row's first visible key
-  for (int64_t k0 = first; k0 <= last; k0 += kTile) {
-    __syncthreads();
-    stage<T, D>(Ks, K + kvbase, k0, N);
-    stage<T, D>(Vs, Vt + kvbase, k0, N);
-    __syncthreads();
-    if (!live) continue;
-    const int jn = static_cast<int>(lmin(kTile, (causal ? i + 1 : N) - k0));
-    const int jb = causal ? static_cast<int>(lmin(kTile, lmax(0, lo_i - k0))) : 0;  // below the row's band
-    for (int jj = jb; jj < jn; ++jj) {
-      float kv[V], vv[V];
-      load_smem(Ks + jj * D, lane, kv);
-      load_smem(Vs + jj * D, lane, vv);
-      float s[1] = {dot(q, kv)};
-      warp_sum(s);
-      if (s[0] > m) {  // the running max moves: rescale what was accumulated
-        const float al = expf((m - s[0]) * scale);
-        l *= al;
-#pragma unroll
-        for (int t = 0; t < V; ++t) o[t] *= al;
-        m = s[0];
-      }
-      const float p = expf((s[0] - m) * scale);  // subtract the max, then scale
-      l += p;
-#pragma unroll
-      for (int t = 0; t < V; ++t) o[t] = fmaf(p, vv[t], o[t]);
-    }
-  }
-  if (!live) return;
-  const float inv = 1.f / l;
-#pragma unroll
-  for (int t = 0; t < V; ++t) o[t] *= inv;
-  store_vec(O + base + i * D, lane, o);
-  if (lane == 0) lse[tl.bh * N + i] = m * scale + logf(l);
 }
 
 // --------------------------------------------------------- backward, rows
@@ -569,18 +505,6 @@ inline unsigned grid_for_cols(const Problem& p) {
   return static_cast<unsigned>(((p.N + kWarps - 1) / kWarps) * p.BHkv);
 }
 
-template <typename T, int D>
-cudaError_t fwd_t(const Problem& p, const void* Q, const void* K, const void* V, void* O, float* lse,
-                  cudaStream_t st) {
-  const size_t sm = 2 * kTile * D * sizeof(float);
-  auto k = fwd_kernel<T, D>;
-  cudaError_t e = allow_smem(k, sm);
-  if (e != cudaSuccess) return e;
-  k<<<grid_for(p), kThreads, sm, st>>>(static_cast<const T*>(Q), static_cast<const T*>(K),
-                                        static_cast<const T*>(V), static_cast<T*>(O), lse, p.N, p.BH, p.scale, p.causal, make_band(p, eff_window(p), false), p.group);
-  return cudaGetLastError();
-}
-
 template <typename T, int D, bool GP>
 cudaError_t bwd_t(const Problem& p, const void* Q, const void* K, const void* V, const void* O, const void* dO,
                   const float* lse, void* dQ, void* dK, void* dV, float4* ws, int passes, cudaStream_t st) {
@@ -651,20 +575,11 @@ bool with_head_dim(int64_t d, F&& f) {
   return false;
 }
 
-// Element type of the [B,H,N,d] tensors: float (ATTN_F32) or bf16 (ATTN_BF16).
+// Element type of the [B,H,N,d] tensors this path serves: bf16 (float32 inputs have
+// tensor-core kernels at every head dim; for them the launchers return an error).
 template <typename F>
 void with_type(int dtype, F&& f) {
-  if (dtype == ATTN_F32) f(float{});
-  else f(__nv_bfloat16{});
-}
-
-cudaError_t simt_fwd(const Problem& p, const void* Q, const void* K, const void* V, void* O, float* lse,
-                     cudaStream_t st) {
-  cudaError_t e = cudaErrorInvalidValue;
-  with_type(p.dtype, [&](auto t) {
-    with_head_dim(p.d, [&](auto dd) { e = fwd_t<decltype(t), dd()>(p, Q, K, V, O, lse, st); });
-  });
-  return e;
+  if (dtype == ATTN_BF16) f(__nv_bfloat16{});
 }
 
 cudaError_t simt_bwd(const Problem& p, const void* Q, const void* K, const void* V, const void* O,

@@ -36,6 +36,7 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <type_traits>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -120,37 +121,40 @@ __device__ __forceinline__ void put1(uint8_t* hi, uint8_t* lo, int off, float v)
   *reinterpret_cast<float*>(lo + off) = ptx::to_tf32(v - h);
 }
 
-// R rows (row0 ...) of a row-major [rows][KD] fp32 array as a K-major tile (K = KD);
-// rows at or past `nrows` are zero.  `a`: the A tile (else the B tile).
-template <int KD>
-__device__ __forceinline__ void stage_rows(const Ctx& c, bool a, const float* src, int64_t row0, int64_t nrows,
-                                           int R) {
-  constexpr int C4 = KD / 4;
+// KW columns [col0, col0 + KW) of R rows (row0 ...) of a row-major array with row
+// stride ld, as a K-major tile (K = KW); rows at or past `nrows` are zero.  `a`: the A
+// tile (else the B tile).
+template <int KW>
+__device__ __forceinline__ void stage_rows(const Ctx& c, bool a, const float* src, int ld, int col0, int64_t row0,
+                                           int64_t nrows, int R) {
+  constexpr int C4 = KW / 4;
   uint8_t* hi = c.sm + (a ? oAh : oBh);
   uint8_t* lo = c.sm + (a ? oAl : oBl);
   for (int idx = threadIdx.x; idx < R * C4; idx += kThreads) {
     const int row = idx / C4, k = (idx % C4) * 4;
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (row0 + row < nrows) v = *reinterpret_cast<const float4*>(src + (row0 + row) * KD + k);
+    if (row0 + row < nrows) v = *reinterpret_cast<const float4*>(src + (row0 + row) * ld + col0 + k);
     put4(hi, lo, swz(row, k, R), v);
   }
 }
 
-// 64 rows (row0 ...) of a row-major [rows][KD] array, transposed: the B tile of KD rows
-// whose K index is the source row (for the products with K = the streamed rows).
-template <int KD>
-__device__ __forceinline__ void stage_rows_t(const Ctx& c, const float* src, int64_t row0, int64_t nrows) {
-  constexpr int C4 = KD / 4;
+// Columns [col0, col0 + KW) of 64 rows (row0 ...) of a row-major array with row stride
+// ld, transposed: the B tile of KW rows whose K index is the source row (the products
+// whose K is the streamed rows).
+template <int KW>
+__device__ __forceinline__ void stage_rows_t(const Ctx& c, const float* src, int ld, int col0, int64_t row0,
+                                             int64_t nrows) {
+  constexpr int C4 = KW / 4;
   uint8_t* hi = c.sm + oBh;
   uint8_t* lo = c.sm + oBl;
   for (int idx = threadIdx.x; idx < BN * C4; idx += kThreads) {
     const int srow = idx / C4, col = (idx % C4) * 4;
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (row0 + srow < nrows) v = *reinterpret_cast<const float4*>(src + (row0 + srow) * KD + col);
-    put1(hi, lo, swz(col, srow, KD), v.x);
-    put1(hi, lo, swz(col + 1, srow, KD), v.y);
-    put1(hi, lo, swz(col + 2, srow, KD), v.z);
-    put1(hi, lo, swz(col + 3, srow, KD), v.w);
+    if (row0 + srow < nrows) v = *reinterpret_cast<const float4*>(src + (row0 + srow) * ld + col0 + col);
+    put1(hi, lo, swz(col, srow, KW), v.x);
+    put1(hi, lo, swz(col + 1, srow, KW), v.y);
+    put1(hi, lo, swz(col + 2, srow, KW), v.z);
+    put1(hi, lo, swz(col + 3, srow, KW), v.w);
   }
 }
 
@@ -215,14 +219,34 @@ __device__ __forceinline__ void mma3(Ctx& c, uint32_t col, int n, int nk, bool a
   ptx::tc_fence_after();
 }
 
-// Running accumulator (TMEM columns acc .. acc + D) += the block product in the scratch
+// A score-type tile: TMEM columns [col, col + 64) (+)= A B^T with A = 128 rows (a0 ...)
+// of `a` and B = 64 rows (b0 ...) of `b`, both of row length D, K = D in chunks of 64
+// (the last one 32 wide when D = 96), each chunk staged and multiplied in turn.
+template <int D>
+__device__ __forceinline__ void tile_product(Ctx& c, uint32_t col, const float* a, int64_t a0, const float* b,
+                                             int64_t b0, int N, bool accumulate) {
+#pragma unroll 1
+  for (int ch = 0; ch < (D + 63) / 64; ++ch) {
+    const int k0 = 64 * ch;
+    if (D - k0 >= 64) {
+      stage_rows<64>(c, true, a, D, k0, a0, N, BM);
+      stage_rows<64>(c, false, b, D, k0, b0, N, BN);
+      mma3(c, col, BN, 8, accumulate || ch > 0);
+    } else {
+      stage_rows<32>(c, true, a, D, k0, a0, N, BM);
+      stage_rows<32>(c, false, b, D, k0, b0, N, BN);
+      mma3(c, col, BN, 4, accumulate || ch > 0);
+    }
+  }
+}
+
+// Running accumulator (TMEM columns acc .. acc + np) += the block product in the scratch
 // columns, in IEEE fp32 on the CUDA cores (first: the accumulator takes the product).
 // The tensor core's own accumulation rounds differently from fp32 addition, and its
 // error grows with the length of the chain; across blocks the sums are kept here.
-template <int D>
-__device__ __forceinline__ void add_into(const Ctx& c, uint32_t acc, uint32_t scr, bool first) {
+__device__ __forceinline__ void add_into(const Ctx& c, uint32_t acc, uint32_t scr, int np, bool first) {
 #pragma unroll 1
-  for (int h = 0; h < D / 32; ++h) {
+  for (int h = 0; h < np / 32; ++h) {
     float t[32];
     tld(c, scr + 32 * h, t);
     if (!first) {
@@ -234,39 +258,37 @@ __device__ __forceinline__ void add_into(const Ctx& c, uint32_t acc, uint32_t sc
     tst(c, acc + 32 * h, t);
   }
 }
-// One block's output product into the scratch columns, then into the accumulator.
-template <int D>
-__device__ __forceinline__ void mma_acc(Ctx& c, uint32_t acc, uint32_t scr, bool first) {
-  mma3(c, scr, D, BN / 8, false);
-  add_into<D>(c, acc, scr, first);
+// An output-type product for this CTA's output columns [p0, p0 + np): the A tile (K =
+// the 64 streamed rows) times columns p0 .. p0 + np of the streamed rows (b0 ...) of `b`
+// (row length ld), into the scratch columns, then added to the accumulator.
+__device__ __forceinline__ void out_product(Ctx& c, uint32_t acc, uint32_t scr, const float* b, int ld, int p0, int np,
+                                            int64_t b0, int N, bool first) {
+  if (np == 64) {
+    stage_rows_t<64>(c, b, ld, p0, b0, N);
+  } else {
+    stage_rows_t<32>(c, b, ld, p0, b0, N);
+  }
+  mma3(c, scr, np, BN / 8, false);
+  add_into(c, acc, scr, np, first);
 }
 
+// dot(x_i, y_i) over a row of D floats.
 template <int D>
-__device__ __forceinline__ void load_row(const float* src, float (&v)[D]) {
-#pragma unroll
+__device__ __forceinline__ float row_dot(const float* x, const float* y) {
+  float acc = 0.f;
+#pragma unroll 4
   for (int k = 0; k < D; k += 4) {
-    const float4 x = *reinterpret_cast<const float4*>(src + k);
-    v[k] = x.x;
-    v[k + 1] = x.y;
-    v[k + 2] = x.z;
-    v[k + 3] = x.w;
+    const float4 a = *reinterpret_cast<const float4*>(x + k), b = *reinterpret_cast<const float4*>(y + k);
+    acc = fmaf(a.x, b.x, acc);
+    acc = fmaf(a.y, b.y, acc);
+    acc = fmaf(a.z, b.z, acc);
+    acc = fmaf(a.w, b.w, acc);
   }
+  return acc;
 }
-template <int D>
-__device__ __forceinline__ void store_row(float* dst, const float (&v)[D]) {
+__device__ __forceinline__ void store32(float* dst, const float (&v)[32]) {
 #pragma unroll
-  for (int k = 0; k < D; k += 4) *reinterpret_cast<float4*>(dst + k) = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
-}
-// D accumulator columns of this thread's lane (D = 32 or 64), times `mul`.
-template <int D>
-__device__ __forceinline__ void tld_acc(const Ctx& c, uint32_t col, float mul, float (&v)[D]) {
-  float t[32];
-#pragma unroll
-  for (int h = 0; h < D / 32; ++h) {
-    tld(c, col + 32 * h, t);
-#pragma unroll
-    for (int u = 0; u < 32; ++u) v[32 * h + u] = mul * t[u];
-  }
+  for (int k = 0; k < 32; k += 4) *reinterpret_cast<float4*>(dst + k) = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
 }
 
 // Key blocks of a row block (row passes) and query blocks of a key block (column
@@ -283,6 +305,21 @@ __device__ __forceinline__ RowRange query_blocks(int kb, int N, int causal, cons
   return {kb * BM / BN, bd.key_hi(kvh, min(kb * BM + BM - 1, N - 1)) / BN + 1};
 }
 
+// Output columns are split over parts of 64 (CTAs of one block of rows differ only in
+// the part they accumulate and write; each computes the whole score-type tiles).
+constexpr int parts_of(int D) { return (D + 63) / 64; }
+struct Where {
+  int slice, blk, p0, np;  // slice, block of rows (heaviest first where it matters), output columns
+};
+template <int D>
+__device__ __forceinline__ Where where(int nslices, int nblk, bool reverse) {
+  const int x = static_cast<int>(blockIdx.x);
+  const int part = x % parts_of(D);
+  const tc::Order o = tc::grid_order_at(x / parts_of(D), nslices, nblk);
+  const int p0 = 64 * part;
+  return Where{o.bh, reverse ? nblk - 1 - o.k : o.k, p0, min(64, D - p0)};
+}
+
 // ------------------------------------------------------------------ forward
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -291,21 +328,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                    Band bd, int G) {
   extern __shared__ __align__(1024) uint8_t sm[];
   Ctx c = setup(sm, 128);  // S / P 0-63, P V 64-127
-  const tc::Order ord = tc::grid_order(BH, nrb);
-  const int bh = ord.bh, rb = nrb - 1 - ord.k, kvh = bh / G;
+  const Where w = where<D>(BH, nrb, true);
+  const int bh = w.slice, rb = w.blk, kvh = bh / G;
   const int64_t i = static_cast<int64_t>(rb) * BM + threadIdx.x;
   const float* q = Q + static_cast<size_t>(bh) * N * D;
   const float* k = K + static_cast<size_t>(kvh) * N * D;
   const float* v = V + static_cast<size_t>(kvh) * N * D;
   const int lo_i = causal ? bd.row_lo(bh, i) : 0;
   const RowRange rr = key_blocks(rb, N, causal, bd, bh);
-  float m = -INFINITY, l = 0.f, o[D];
+  float m = -INFINITY, l = 0.f, o[64];  // this part's np <= 64 output columns
 #pragma unroll
-  for (int t = 0; t < D; ++t) o[t] = 0.f;
+  for (int t = 0; t < 64; ++t) o[t] = 0.f;
   for (int kb = rr.k0; kb < rr.k1; ++kb) {
-    stage_rows<D>(c, true, q, static_cast<int64_t>(rb) * BM, N, BM);
-    stage_rows<D>(c, false, k, static_cast<int64_t>(kb) * BN, N, BN);
-    mma3(c, 0, BN, D / 8, false);  // S = Q K^T
+    tile_product<D>(c, 0, q, static_cast<int64_t>(rb) * BM, k, static_cast<int64_t>(kb) * BN, N, false);  // S = Q K^T
     float s[2][32];
     tld(c, 0, s[0]);
     tld(c, 32, s[1]);
@@ -334,22 +369,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     m = m_new;
     l = l * alpha + rs;
-    stage_rows_t<D>(c, v, static_cast<int64_t>(kb) * BN, N);
-    mma3(c, 64, D, BN / 8, false);  // P V
+    if (w.np == 64) {
+      stage_rows_t<64>(c, v, D, w.p0, static_cast<int64_t>(kb) * BN, N);
+    } else {
+      stage_rows_t<32>(c, v, D, w.p0, static_cast<int64_t>(kb) * BN, N);
+    }
+    mma3(c, 64, w.np, BN / 8, false);  // P V, this part's columns
 #pragma unroll
-    for (int h = 0; h < D / 32; ++h) {
-      float pv[32];
-      tld(c, 64 + 32 * h, pv);
+    for (int h = 0; h < 2; ++h) {
+      if (32 * h < w.np) {
+        float pv[32];
+        tld(c, 64 + 32 * h, pv);
 #pragma unroll
-      for (int t = 0; t < 32; ++t) o[32 * h + t] = o[32 * h + t] * alpha + pv[t];
+        for (int t = 0; t < 32; ++t) o[32 * h + t] = o[32 * h + t] * alpha + pv[t];
+      }
     }
   }
   if (i < N) {
     const float inv = 1.f / l;
 #pragma unroll
-    for (int t = 0; t < D; ++t) o[t] *= inv;
-    store_row<D>(O + (static_cast<size_t>(bh) * N + i) * D, o);
-    lse[static_cast<size_t>(bh) * N + i] = m + logf(l);
+    for (int h = 0; h < 2; ++h) {
+      if (32 * h < w.np) {
+        float out[32];
+#pragma unroll
+        for (int t = 0; t < 32; ++t) out[t] = o[32 * h + t] * inv;
+        store32(O + (static_cast<size_t>(bh) * N + i) * D + w.p0 + 32 * h, out);
+      }
+    }
+    if (w.p0 == 0) lse[static_cast<size_t>(bh) * N + i] = m + logf(l);
   }
   teardown(c, 128);
 }
@@ -362,30 +409,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                        float* __restrict__ dQ, float4* __restrict__ ws, int N, int nrb, int BH, float scale,
                        int causal, Band bd, int G) {
   extern __shared__ __align__(1024) uint8_t sm[];
-  Ctx c = setup(sm, 256);  // S 0-63, dP 64-127, dQ 128-191
-  const tc::Order ord = tc::grid_order(BH, nrb);
-  const int bh = ord.bh, rb = nrb - 1 - ord.k, kvh = bh / G;
-  const int64_t i = static_cast<int64_t>(rb) * BM + threadIdx.x;
+  Ctx c = setup(sm, 256);  // S 0-63, dP 64-127, dQ 128-191 (this part's columns)
+  const Where w = where<D>(BH, nrb, true);
+  const int bh = w.slice, rb = w.blk, kvh = bh / G;
+  const int64_t i = static_cast<int64_t>(rb) * BM + threadIdx.x, r0 = static_cast<int64_t>(rb) * BM;
   const size_t qo = static_cast<size_t>(bh) * N * D, ko = static_cast<size_t>(kvh) * N * D;
   const int lo_i = causal ? bd.row_lo(bh, i) : 0;
   float Di = 0.f, Li = 0.f;
   if (i < N) {
-    float a[D], b[D];
-    load_row<D>(dO + qo + i * D, a);
-    load_row<D>(O + qo + i * D, b);
-#pragma unroll
-    for (int t = 0; t < D; ++t) Di = fmaf(a[t], b[t], Di);
+    Di = row_dot<D>(dO + qo + i * D, O + qo + i * D);
     Li = lse[static_cast<size_t>(bh) * N + i];
   }
   const RowRange rr = key_blocks(rb, N, causal, bd, bh);
   for (int kb = rr.k0; kb < rr.k1; ++kb) {
     const int64_t k0 = static_cast<int64_t>(kb) * BN;
-    stage_rows<D>(c, true, Q + qo, static_cast<int64_t>(rb) * BM, N, BM);
-    stage_rows<D>(c, false, K + ko, k0, N, BN);
-    mma3(c, 0, BN, D / 8, false);  // S = Q K^T
-    stage_rows<D>(c, true, dO + qo, static_cast<int64_t>(rb) * BM, N, BM);
-    stage_rows<D>(c, false, V + ko, k0, N, BN);
-    mma3(c, 64, BN, D / 8, false);  // dP = dO V^T
+    tile_product<D>(c, 0, Q + qo, r0, K + ko, k0, N, false);    // S = Q K^T
+    tile_product<D>(c, 64, dO + qo, r0, V + ko, k0, N, false);  // dP = dO V^T
 #pragma unroll 1
     for (int h = 0; h < 2; ++h) {
       float s[32], dp[32];
@@ -399,15 +438,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       stage_own(c, 32 * h, s);
     }
-    stage_rows_t<D>(c, K + ko, k0, N);
-    mma_acc<D>(c, 128, 0, kb == rr.k0);  // dQ += dS K (S and dP are read: scratch at 0)
+    out_product(c, 128, 0, K + ko, D, w.p0, w.np, k0, N, kb == rr.k0);  // dQ += dS K (scratch: the read S)
   }
-  float g[D];
-  tld_acc<D>(c, 128, scale, g);
-  if (i < N) {
-    store_row<D>(dQ + qo + i * D, g);
-    ws[static_cast<size_t>(bh) * N + i] = make_float4(Li, Di, 0.f, 0.f);
+#pragma unroll 1
+  for (int h = 0; h < w.np / 32; ++h) {
+    float g[32];
+    tld(c, 128 + 32 * h, g);
+#pragma unroll
+    for (int t = 0; t < 32; ++t) g[t] *= scale;
+    if (i < N) store32(dQ + qo + i * D + w.p0 + 32 * h, g);
   }
+  if (i < N && w.p0 == 0) ws[static_cast<size_t>(bh) * N + i] = make_float4(Li, Di, 0.f, 0.f);
   teardown(c, 256);
 }
 
@@ -419,9 +460,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                        float* __restrict__ dV, int N, int nkb, int BHkv, float scale, int causal, Band bd, int G) {
   extern __shared__ __align__(1024) uint8_t sm[];
   Ctx c = setup(sm, 256);  // S^T / P^T 0-63, dP^T / dS^T 64-127, dV 128-191, dK 192-255
-  const tc::Order ord = tc::grid_order(BHkv, nkb);
-  const int kvh = ord.bh, kb = ord.k;
-  const int64_t key = static_cast<int64_t>(kb) * BM + threadIdx.x;
+  const Where w = where<D>(BHkv, nkb, false);
+  const int kvh = w.slice, kb = w.blk;
+  const int64_t key = static_cast<int64_t>(kb) * BM + threadIdx.x, c0 = static_cast<int64_t>(kb) * BM;
   const size_t ko = static_cast<size_t>(kvh) * N * D;
   const int hi_k = causal ? bd.key_hi(kvh, key) : N - 1;
   const RowRange qr = query_blocks(kb, N, causal, bd, kvh);
@@ -436,12 +477,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         reinterpret_cast<float4*>(sm + oSt)[threadIdx.x] =
             qi < N ? ws[static_cast<size_t>(hq) * N + qi] : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      stage_rows<D>(c, true, K + ko, static_cast<int64_t>(kb) * BM, N, BM);
-      stage_rows<D>(c, false, Q + qo, q0, N, BN);
-      mma3(c, 0, BN, D / 8, false);  // S^T = K Q^T (the barrier in mma3 also publishes the states)
-      stage_rows<D>(c, true, V + ko, static_cast<int64_t>(kb) * BM, N, BM);
-      stage_rows<D>(c, false, dO + qo, q0, N, BN);
-      mma3(c, 64, BN, D / 8, false);  // dP^T = V dO^T
+      tile_product<D>(c, 0, K + ko, c0, Q + qo, q0, N, false);    // S^T = K Q^T (mma3's barrier publishes the states)
+      tile_product<D>(c, 64, V + ko, c0, dO + qo, q0, N, false);  // dP^T = V dO^T
 #pragma unroll 1
       for (int h = 0; h < 2; ++h) {
         float s[32], dp[32];
@@ -459,20 +496,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         stage_own(c, 32 * h, s);  // P^T
         tst(c, 64 + 32 * h, dp);
       }
-      stage_rows_t<D>(c, dO + qo, q0, N);
-      mma_acc<D>(c, 128, 0, first);  // dV += P^T dO (P^T is in the A tile: scratch at 0)
+      out_product(c, 128, 0, dO + qo, D, w.p0, w.np, q0, N, first);  // dV += P^T dO (scratch: the read S^T)
       stage_tmem(c, 64);
-      stage_rows_t<D>(c, Q + qo, q0, N);
-      mma_acc<D>(c, 192, 0, first);  // dK += dS^T Q
+      out_product(c, 192, 0, Q + qo, D, w.p0, w.np, q0, N, first);   // dK += dS^T Q
       first = false;
     }
   }
-  float gv[D], gk[D];
-  tld_acc<D>(c, 128, 1.f, gv);
-  tld_acc<D>(c, 192, scale, gk);
-  if (key < N) {
-    store_row<D>(dV + ko + key * D, gv);
-    store_row<D>(dK + ko + key * D, gk);
+#pragma unroll 1
+  for (int h = 0; h < w.np / 32; ++h) {
+    float gv[32], gk[32];
+    tld(c, 128 + 32 * h, gv);
+    tld(c, 192 + 32 * h, gk);
+#pragma unroll
+    for (int t = 0; t < 32; ++t) gk[t] *= scale;
+    if (key < N) {
+      store32(dV + ko + key * D + w.p0 + 32 * h, gv);
+      store32(dK + ko + key * D + w.p0 + 32 * h, gk);
+    }
   }
   teardown(c, 256);
 }
@@ -486,40 +526,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                        float* __restrict__ gQ, float* __restrict__ gdO, float4* __restrict__ ws, int N, int nrb,
                        int BH, float scale, int causal, Band bd, int G) {
   extern __shared__ __align__(1024) uint8_t sm[];
-  // TMEM: S / P 0, dP / dS 64, G / PG 128, H / W 192, X 256, Y 320, Z 384, U 448.
+  // TMEM: S / P 0, dP / dS 64, G / PG 128, H / W 192, and this part's X 256, Y 320, Z 384, U 448.
   Ctx c = setup(sm, 512);
-  const tc::Order ord = tc::grid_order(BH, nrb);
-  const int bh = ord.bh, rb = nrb - 1 - ord.k, kvh = bh / G;
-  const int64_t i = static_cast<int64_t>(rb) * BM + threadIdx.x;
-  const int64_t r0 = static_cast<int64_t>(rb) * BM;
+  const Where w = where<D>(BH, nrb, true);
+  const int bh = w.slice, rb = w.blk, kvh = bh / G;
+  const int64_t i = static_cast<int64_t>(rb) * BM + threadIdx.x, r0 = static_cast<int64_t>(rb) * BM;
   const size_t qo = static_cast<size_t>(bh) * N * D, ko = static_cast<size_t>(kvh) * N * D;
   const int lo_i = causal ? bd.row_lo(bh, i) : 0;
   float Di = 0.f, Li = 0.f, E = 0.f, Fp = 0.f;
   if (i < N) {
-    float a[D], b[D];
-    load_row<D>(dO + qo + i * D, a);
-    load_row<D>(O + qo + i * D, b);
-#pragma unroll
-    for (int t = 0; t < D; ++t) Di = fmaf(a[t], b[t], Di);
+    Di = row_dot<D>(dO + qo + i * D, O + qo + i * D);
     Li = lse[static_cast<size_t>(bh) * N + i];
   }
   const RowRange rr = key_blocks(rb, N, causal, bd, bh);
   for (int kb = rr.k0; kb < rr.k1; ++kb) {
     const int64_t k0 = static_cast<int64_t>(kb) * BN;
     const bool acc = kb > rr.k0;
-    stage_rows<D>(c, true, Q + qo, r0, N, BM);
-    stage_rows<D>(c, false, K + ko, k0, N, BN);
-    mma3(c, 0, BN, D / 8, false);  // S = Q K^T
-    stage_rows<D>(c, false, Bm + ko, k0, N, BN);
-    mma3(c, 128, BN, D / 8, false);  // G = Q b^T ...
-    stage_rows<D>(c, true, A + qo, r0, N, BM);
-    stage_rows<D>(c, false, K + ko, k0, N, BN);
-    mma3(c, 128, BN, D / 8, true);  // ... + a K^T
-    stage_rows<D>(c, true, dO + qo, r0, N, BM);
-    stage_rows<D>(c, false, V + ko, k0, N, BN);
-    mma3(c, 64, BN, D / 8, false);  // dP = dO V^T
-    stage_rows<D>(c, false, C + ko, k0, N, BN);
-    mma3(c, 192, BN, D / 8, false);  // H = dO c^T
+    tile_product<D>(c, 0, Q + qo, r0, K + ko, k0, N, false);    // S = Q K^T
+    tile_product<D>(c, 128, Q + qo, r0, Bm + ko, k0, N, false); // G = Q b^T ...
+    tile_product<D>(c, 128, A + qo, r0, K + ko, k0, N, true);   // ... + a K^T
+    tile_product<D>(c, 64, dO + qo, r0, V + ko, k0, N, false);  // dP = dO V^T
+    tile_product<D>(c, 192, dO + qo, r0, C + ko, k0, N, false); // H = dO c^T
 #pragma unroll 1
     for (int h = 0; h < 2; ++h) {
       float s[32], dp[32], g[32], hh[32];
@@ -535,13 +562,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float gg = scale * g[t];
         const float ds = p * (dp[t] - Di);
         const float pg = p * gg;
-        const float w = gg * ds + p * hh[t];
+        const float wv = gg * ds + p * hh[t];
         E += pg;
-        Fp += w;
+        Fp += wv;
         s[t] = p;
         dp[t] = ds;
         g[t] = pg;
-        hh[t] = w;
+        hh[t] = wv;
       }
       tst(c, 32 * h, s);
       tst(c, 64 + 32 * h, dp);
@@ -551,42 +578,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Block products into the scratch columns 0-63 (P, once in the A tile, is not read
     // from TMEM again), each added to its accumulator.
     stage_tmem(c, 0);  // P
-    stage_rows_t<D>(c, C + ko, k0, N);
-    mma_acc<D>(c, 256, 0, !acc);  // X += P c
-    stage_rows_t<D>(c, K + ko, k0, N);
-    mma_acc<D>(c, 448, 0, !acc);  // U += P K
+    out_product(c, 256, 0, C + ko, D, w.p0, w.np, k0, N, !acc);   // X += P c
+    out_product(c, 448, 0, K + ko, D, w.p0, w.np, k0, N, !acc);   // U += P K
     stage_tmem(c, 128);  // P G
-    stage_rows_t<D>(c, V + ko, k0, N);
-    mma_acc<D>(c, 256, 0, false);  // X += (P G) V
+    out_product(c, 256, 0, V + ko, D, w.p0, w.np, k0, N, false);  // X += (P G) V
     stage_tmem(c, 64);  // dS
-    stage_rows_t<D>(c, K + ko, k0, N);
-    mma_acc<D>(c, 384, 0, !acc);  // Z += dS K
-    stage_rows_t<D>(c, Bm + ko, k0, N);
-    mma_acc<D>(c, 320, 0, !acc);  // Y += dS b
+    out_product(c, 384, 0, K + ko, D, w.p0, w.np, k0, N, !acc);   // Z += dS K
+    out_product(c, 320, 0, Bm + ko, D, w.p0, w.np, k0, N, !acc);  // Y += dS b
     stage_tmem(c, 192);  // W
-    stage_rows_t<D>(c, K + ko, k0, N);
-    mma_acc<D>(c, 320, 0, false);  // Y += W K
+    out_product(c, 320, 0, K + ko, D, w.p0, w.np, k0, N, false);  // Y += W K
   }
 #pragma unroll 1
-  for (int h = 0; h < D / 32; ++h) {  // 32 output columns at a time
+  for (int h = 0; h < w.np / 32; ++h) {  // 32 output columns at a time
     float x[32], y[32], z[32], u[32];
     tld(c, 256 + 32 * h, x);
     tld(c, 320 + 32 * h, y);
     tld(c, 384 + 32 * h, z);
     tld(c, 448 + 32 * h, u);
     if (i < N) {
-      float o[32];
-      load_row<32>(O + qo + i * D + 32 * h, o);
+      const float* orow = O + qo + i * D + w.p0 + 32 * h;
 #pragma unroll
-      for (int t = 0; t < 32; ++t) {
-        x[t] = x[t] - E * o[t];                        // gdO
-        y[t] = scale * (y[t] - E * z[t] - Fp * u[t]);  // gQ
+      for (int t = 0; t < 32; t += 4) {
+        const float4 o4 = *reinterpret_cast<const float4*>(orow + t);
+        const float ov[4] = {o4.x, o4.y, o4.z, o4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          x[t + e] = x[t + e] - E * ov[e];                                      // gdO
+          y[t + e] = scale * (y[t + e] - E * z[t + e] - Fp * u[t + e]);         // gQ
+        }
       }
-      store_row<32>(gdO + qo + i * D + 32 * h, x);
-      store_row<32>(gQ + qo + i * D + 32 * h, y);
+      store32(gdO + qo + i * D + w.p0 + 32 * h, x);
+      store32(gQ + qo + i * D + w.p0 + 32 * h, y);
     }
   }
-  if (i < N) ws[static_cast<size_t>(bh) * N + i] = make_float4(Li, Di, E, Fp - E * Di);
+  if (i < N && w.p0 == 0) ws[static_cast<size_t>(bh) * N + i] = make_float4(Li, Di, E, Fp - E * Di);
   teardown(c, 512);
 }
 
@@ -598,12 +623,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const float* __restrict__ C, const float4* __restrict__ ws, float* __restrict__ gK,
                        float* __restrict__ gV, int N, int nkb, int BHkv, float scale, int causal, Band bd, int G) {
   extern __shared__ __align__(1024) uint8_t sm[];
-  // TMEM: S^T / dPbar 0, dP^T / dS 64, G^T / Sbar 128, H^T 192, gV 256, gK 320, scratch 384.
+  // TMEM: S^T / dPbar 0, dP^T / dS 64, G^T / Sbar 128, H^T 192, this part's gV 256 and
+  // gK 320, scratch 384.
   Ctx c = setup(sm, 512);
-  const tc::Order ord = tc::grid_order(BHkv, nkb);
-  const int kvh = ord.bh, kb = ord.k;
-  const int64_t key = static_cast<int64_t>(kb) * BM + threadIdx.x;
-  const int64_t c0 = static_cast<int64_t>(kb) * BM;
+  const Where w = where<D>(BHkv, nkb, false);
+  const int kvh = w.slice, kb = w.blk;
+  const int64_t key = static_cast<int64_t>(kb) * BM + threadIdx.x, c0 = static_cast<int64_t>(kb) * BM;
   const size_t ko = static_cast<size_t>(kvh) * N * D;
   const int hi_k = causal ? bd.key_hi(kvh, key) : N - 1;
   const RowRange qr = query_blocks(kb, N, causal, bd, kvh);
@@ -618,19 +643,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         reinterpret_cast<float4*>(sm + oSt)[threadIdx.x] =
             qi < N ? ws[static_cast<size_t>(hq) * N + qi] : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      stage_rows<D>(c, true, K + ko, c0, N, BM);
-      stage_rows<D>(c, false, Q + qo, q0, N, BN);
-      mma3(c, 0, BN, D / 8, false);  // S^T = K Q^T (the barrier in mma3 also publishes the states)
-      stage_rows<D>(c, false, A + qo, q0, N, BN);
-      mma3(c, 128, BN, D / 8, false);  // G^T = K a^T ...
-      stage_rows<D>(c, true, Bm + ko, c0, N, BM);
-      stage_rows<D>(c, false, Q + qo, q0, N, BN);
-      mma3(c, 128, BN, D / 8, true);  // ... + b Q^T
-      stage_rows<D>(c, true, V + ko, c0, N, BM);
-      stage_rows<D>(c, false, dO + qo, q0, N, BN);
-      mma3(c, 64, BN, D / 8, false);  // dP^T = V dO^T
-      stage_rows<D>(c, true, C + ko, c0, N, BM);
-      mma3(c, 192, BN, D / 8, false);  // H^T = c dO^T
+      tile_product<D>(c, 0, K + ko, c0, Q + qo, q0, N, false);     // S^T = K Q^T (mma3's barrier publishes the states)
+      tile_product<D>(c, 128, K + ko, c0, A + qo, q0, N, false);   // G^T = K a^T ...
+      tile_product<D>(c, 128, Bm + ko, c0, Q + qo, q0, N, true);   // ... + b Q^T
+      tile_product<D>(c, 64, V + ko, c0, dO + qo, q0, N, false);   // dP^T = V dO^T
+      tile_product<D>(c, 192, C + ko, c0, dO + qo, q0, N, false);  // H^T = c dO^T
 #pragma unroll 1
       for (int h = 0; h < 2; ++h) {
         float s[32], dp[32], g[32], hh[32];
@@ -645,9 +662,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool vis = key < N && qi < N && (!causal || (qi >= key && qi <= hi_k));
           const float p = vis ? expf(s[t] * scale - sv.x) : 0.f;
           const float gg = scale * g[t];
-          s[t] = p * (gg - sv.z);                                            // dPbar
-          g[t] = p * (gg * (dp[t] - sv.y) - sv.z * dp[t] + hh[t] - sv.w);    // Sbar
-          dp[t] = p * (dp[t] - sv.y);                                        // dS
+          s[t] = p * (gg - sv.z);                                          // dPbar
+          g[t] = p * (gg * (dp[t] - sv.y) - sv.z * dp[t] + hh[t] - sv.w);  // Sbar
+          dp[t] = p * (dp[t] - sv.y);                                      // dS
         }
         tst(c, 32 * h, s);
         tst(c, 64 + 32 * h, dp);
@@ -655,23 +672,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // Block products into the scratch columns 384-447, each added to its accumulator.
       stage_tmem(c, 0);  // dPbar
-      stage_rows_t<D>(c, dO + qo, q0, N);
-      mma_acc<D>(c, 256, 384, first);  // gV += dPbar^T dO
+      out_product(c, 256, 384, dO + qo, D, w.p0, w.np, q0, N, first);  // gV += dPbar^T dO
       stage_tmem(c, 64);  // dS
-      stage_rows_t<D>(c, A + qo, q0, N);
-      mma_acc<D>(c, 320, 384, first);  // gK += dS^T a
+      out_product(c, 320, 384, A + qo, D, w.p0, w.np, q0, N, first);   // gK += dS^T a
       stage_tmem(c, 128);  // Sbar
-      stage_rows_t<D>(c, Q + qo, q0, N);
-      mma_acc<D>(c, 320, 384, false);  // gK += Sbar^T Q
+      out_product(c, 320, 384, Q + qo, D, w.p0, w.np, q0, N, false);   // gK += Sbar^T Q
       first = false;
     }
   }
-  float gv[D], gk[D];
-  tld_acc<D>(c, 256, 1.f, gv);
-  tld_acc<D>(c, 320, scale, gk);
-  if (key < N) {
-    store_row<D>(gV + ko + key * D, gv);
-    store_row<D>(gK + ko + key * D, gk);
+#pragma unroll 1
+  for (int h = 0; h < w.np / 32; ++h) {
+    float gv[32], gk[32];
+    tld(c, 256 + 32 * h, gv);
+    tld(c, 320 + 32 * h, gk);
+#pragma unroll
+    for (int t = 0; t < 32; ++t) gk[t] *= scale;
+    if (key < N) {
+      store32(gV + ko + key * D + w.p0 + 32 * h, gv);
+      store32(gK + ko + key * D + w.p0 + 32 * h, gk);
+    }
   }
   teardown(c, 512);
 }
@@ -682,6 +701,9 @@ cudaError_t launch_prep(Kern k, int smem) {
 }
 
 inline int blocks_of(int64_t N, int rows) { return static_cast<int>((N + rows - 1) / rows); }
+inline unsigned grid_of(int nblk, int64_t slices, int D) {
+  return static_cast<unsigned>(static_cast<int64_t>(nblk) * slices * parts_of(D));
+}
 
 template <int D>
 cudaError_t fwd_t(const Problem& p, const void* Q, const void* K, const void* V, void* O, float* lse, cudaStream_t st) {
@@ -689,7 +711,7 @@ cudaError_t fwd_t(const Problem& p, const void* Q, const void* K, const void* V,
   cudaError_t e = launch_prep(k, kSmem);
   if (e != cudaSuccess) return e;
   const int nrb = blocks_of(p.N, BM);
-  k<<<static_cast<unsigned>(nrb * p.BH), kThreads, kSmem, st>>>(
+  k<<<grid_of(nrb, p.BH, D), kThreads, kSmem, st>>>(
       static_cast<const float*>(Q), static_cast<const float*>(K), static_cast<const float*>(V),
       static_cast<float*>(O), lse, static_cast<int>(p.N), nrb, static_cast<int>(p.BH), p.scale, p.causal,
       make_band(p, eff_window(p), false), p.group);
@@ -705,7 +727,7 @@ cudaError_t bwd_t(const Problem& p, const void* Q, const void* K, const void* V,
     auto k = f32_bwd_row_kernel<D>;
     cudaError_t e = launch_prep(k, kSmem);
     if (e != cudaSuccess) return e;
-    k<<<static_cast<unsigned>(nb * p.BH), kThreads, kSmem, st>>>(
+    k<<<grid_of(nb, p.BH, D), kThreads, kSmem, st>>>(
         static_cast<CF>(Q), static_cast<CF>(K), static_cast<CF>(V), static_cast<CF>(O), static_cast<CF>(dO), lse,
         static_cast<float*>(dQ), ws, static_cast<int>(p.N), nb, static_cast<int>(p.BH), p.scale, p.causal,
         make_band(p, eff_window(p), false), p.group);
@@ -715,7 +737,7 @@ cudaError_t bwd_t(const Problem& p, const void* Q, const void* K, const void* V,
     auto k = f32_bwd_col_kernel<D>;
     cudaError_t e = launch_prep(k, kSmem);
     if (e != cudaSuccess) return e;
-    k<<<static_cast<unsigned>(nb * p.BHkv), kThreads, kSmem, st>>>(
+    k<<<grid_of(nb, p.BHkv, D), kThreads, kSmem, st>>>(
         static_cast<CF>(Q), static_cast<CF>(K), static_cast<CF>(V), static_cast<CF>(dO), ws,
         static_cast<float*>(dK), static_cast<float*>(dV), static_cast<int>(p.N), nb, static_cast<int>(p.BHkv),
         p.scale, p.causal, make_band(p, eff_window(p), true), p.group);
@@ -734,7 +756,7 @@ cudaError_t bob_t(const Problem& p, const void* Q, const void* K, const void* V,
     auto k = f32_bob_row_kernel<D>;
     cudaError_t e = launch_prep(k, kSmemBob);
     if (e != cudaSuccess) return e;
-    k<<<static_cast<unsigned>(nb * p.BH), kThreads, kSmemBob, st>>>(
+    k<<<grid_of(nb, p.BH, D), kThreads, kSmemBob, st>>>(
         static_cast<CF>(Q), static_cast<CF>(K), static_cast<CF>(V), static_cast<CF>(O), static_cast<CF>(dO), lse,
         static_cast<CF>(a), static_cast<CF>(b), static_cast<CF>(cc), static_cast<float*>(gQ),
         static_cast<float*>(gdO), ws, static_cast<int>(p.N), nb, static_cast<int>(p.BH), p.scale, p.causal,
@@ -745,7 +767,7 @@ cudaError_t bob_t(const Problem& p, const void* Q, const void* K, const void* V,
     auto k = f32_bob_col_kernel<D>;
     cudaError_t e = launch_prep(k, kSmemBob);
     if (e != cudaSuccess) return e;
-    k<<<static_cast<unsigned>(nb * p.BHkv), kThreads, kSmemBob, st>>>(
+    k<<<grid_of(nb, p.BHkv, D), kThreads, kSmemBob, st>>>(
         static_cast<CF>(Q), static_cast<CF>(K), static_cast<CF>(V), static_cast<CF>(dO), static_cast<CF>(a),
         static_cast<CF>(b), static_cast<CF>(cc), ws, static_cast<float*>(gK), static_cast<float*>(gV),
         static_cast<int>(p.N), nb, static_cast<int>(p.BHkv), p.scale, p.causal, make_band(p, eff_window(p), true),
@@ -755,30 +777,39 @@ cudaError_t bob_t(const Problem& p, const void* Q, const void* K, const void* V,
   return cudaSuccess;
 }
 
+// The head dims with kernels: 32, 64, 96, 128, 256.
+template <typename F>
+cudaError_t with_d(int64_t d, F&& f) {
+  switch (d) {
+    case 32: return f(std::integral_constant<int, 32>{});
+    case 64: return f(std::integral_constant<int, 64>{});
+    case 96: return f(std::integral_constant<int, 96>{});
+    case 128: return f(std::integral_constant<int, 128>{});
+    case 256: return f(std::integral_constant<int, 256>{});
+  }
+  return cudaErrorInvalidValue;
+}
+
 }  // namespace
 
-bool tc32_supports(int64_t d) { return d == 32 || d == 64; }
+bool tc32_supports(int64_t d) { return d == 32 || d == 64 || d == 96 || d == 128 || d == 256; }
 
 cudaError_t tc32_fwd(const Problem& p, const void* Q, const void* K, const void* V, void* O, float* lse,
                      cudaStream_t st) {
-  if (p.d == 32) return fwd_t<32>(p, Q, K, V, O, lse, st);
-  if (p.d == 64) return fwd_t<64>(p, Q, K, V, O, lse, st);
-  return cudaErrorInvalidValue;
+  return with_d(p.d, [&](auto dd) { return fwd_t<dd()>(p, Q, K, V, O, lse, st); });
 }
 
 cudaError_t tc32_bwd(const Problem& p, const void* Q, const void* K, const void* V, const void* O, const void* dO,
                      const float* lse, void* dQ, void* dK, void* dV, float4* ws, int passes, cudaStream_t st) {
-  if (p.d == 32) return bwd_t<32>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st);
-  if (p.d == 64) return bwd_t<64>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st);
-  return cudaErrorInvalidValue;
+  return with_d(p.d, [&](auto dd) { return bwd_t<dd()>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st); });
 }
 
 cudaError_t tc32_bob(const Problem& p, const void* Q, const void* K, const void* V, const void* O, const void* dO,
                      const float* lse, const void* a, const void* b, const void* c, void* gQ, void* gK, void* gV,
                      void* gdO, float4* ws, int passes, cudaStream_t st) {
-  if (p.d == 32) return bob_t<32>(p, Q, K, V, O, dO, lse, a, b, c, gQ, gK, gV, gdO, ws, passes, st);
-  if (p.d == 64) return bob_t<64>(p, Q, K, V, O, dO, lse, a, b, c, gQ, gK, gV, gdO, ws, passes, st);
-  return cudaErrorInvalidValue;
+  return with_d(p.d, [&](auto dd) {
+    return bob_t<dd()>(p, Q, K, V, O, dO, lse, a, b, c, gQ, gK, gV, gdO, ws, passes, st);
+  });
 }
 
 uint32_t tc32_take_error() {

@@ -38,15 +38,16 @@
  *               attn_bob at d in {32, 64, 96, 128}, and bf16 attn_fwd and attn_bwd
  *               (without GProj) at d = 256, run on the tcgen05/TMA tensor-core kernels
  *               (d = 32 and 96 on those of d = 64 and 128, the head dim zero-padded in
- *               shared memory); float32 inputs at d in {32, 64} run on tcgen05
+ *               shared memory); float32 inputs at every d run on tcgen05
  *               kind::tf32 kernels that form each product from the operands' tf32
  *               high and low parts (A_lo B_hi + A_hi B_lo + A_hi B_hi: about 2^-21
  *               relative per element product, fp32 accumulation; across blocks the
- *               sums are fp32 additions on the CUDA cores); float32 inputs at
- *               d in {96, 128, 256}, and the bf16 GProj backward and BoB at d = 256,
- *               run on the CUDA-core kernels (fp32 arithmetic; bf16 inputs widened
- *               on load, outputs rounded once on store).  GProj does not apply to
- *               float32 inputs (gproj is ignored: nothing is rounded to bf16).
+ *               sums are fp32 additions on the CUDA cores; past d = 64 the head dim
+ *               is taken in chunks of 64 and the output columns are split over CTAs
+ *               in parts of 64); the bf16 GProj backward and BoB at d = 256 run on
+ *               the CUDA-core kernels (fp32 arithmetic; bf16 inputs widened on load,
+ *               outputs rounded once on store).  GProj does not apply to float32
+ *               inputs (gproj is ignored: nothing is rounded to bf16).
  *   Scale:      desc->scale == 0 means 1/sqrt(d); otherwise it must be finite and
  *               positive (the row max is subtracted before scaling).
  *   Pointers:   device pointers, 16-byte aligned (ATTN_ERR_ALIGNMENT otherwise),

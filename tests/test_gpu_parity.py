@@ -314,6 +314,19 @@ def test_other_head_dims(N, d, dtype, causal):
         check_full(w, got1, ("bwd", "bob"), causal=causal)
 
 
+@pytest.mark.parametrize("d", [96, 128, 256])
+def test_f32_wide_heads(d):
+    """float32 past d = 64 on the tf32 tensor-core kernels: the head dim in chunks of 64
+    (the last 32 wide at d = 96), the output columns split over CTAs in parts of 64;
+    several row blocks, a ragged tail, grouped heads, causal and not, and a window."""
+    w = W.Workload(f"f32wide_B1H4g2N700d{d}_f32", 1, 4, 700, d, "f32", group=2)
+    x = to_device(inputs(w), w)
+    for causal, win in ((True, 0), (False, 0), (True, 90)):
+        got = run_ops(w, x, ops=("bwd", "bob"), causal=causal, window=win)
+        errs = check_full(w, got, ("bwd", "bob"), causal=causal, window=win)
+        print(w.name, causal, win, {k: f"{v:.2e}" for k, v in errs.items()})
+
+
 @pytest.mark.parametrize("gproj", [0, 1])
 @pytest.mark.parametrize("d", [32, 96, 128, 256])
 def test_other_head_dims_grouped_bf16(d, gproj):
