@@ -564,8 +564,9 @@ def sweep(args):
     the long sweep (B1 H12 d64 at N = 4096 ... 262144: bwd and BoB, with the forward
     that produces O and L), the target shape at B = 1 and B = 4 (fwd, bwd, BoB), the
     full trading day (B2 H12 N23400: fwd, bwd), the large-key shape (B8 H8 N2048
-    d128: bwd with and without GProj) and the target shape at d = 128 (fwd, bwd with
-    and without GProj, BoB).  Median of `--steps` runs after `--warmup`,
+    d128: bwd with and without GProj), the target shape at d = 128 (fwd, bwd with
+    and without GProj, BoB) and at d = 256 (fwd, bwd; and at B = 1 the GProj backward
+    and BoB, on the tf32 engine).  Median of `--steps` runs after `--warmup`,
     CUDA events on the launching stream, min and max beside; peak device memory
     of the op's buffers (nothing else is allocated: the library allocates nothing).
     Inputs are device-drawn N(0,1) values rounded to bf16 (a timing run, not parity)."""
@@ -581,9 +582,12 @@ def sweep(args):
                 ("fullday_B2H12N23400d64", 2, 12, 23400, 64, ("fwd", "bwd")),
                 ("largekey_B8H8N2048d128", 8, 8, 2048, 128, ("bwd", "bwd_gproj")),
                 ("headdim128_B4H12N8192d128", 4, 12, 8192, 128, ("fwd", "bwd", "bwd_gproj", "bob", "bob_gproj")),
-                ("headdim256_B4H12N8192d256", 4, 12, 8192, 256, ("fwd", "bwd"))]
+                ("headdim256_B4H12N8192d256", 4, 12, 8192, 256, ("fwd", "bwd")),
+                ("headdim256_B1H12N8192d256", 1, 12, 8192, 256, ("bwd", "bwd_gproj", "bob", "bob_gproj"))]
     reps, warm = max(args.steps, 1), max(args.warmup, 1)
     for name, B, H, N, d, ops in configs:
+        if args.sweep_only and args.sweep_only not in name:
+            continue
         torch.cuda.empty_cache()
         torch.cuda.reset_peak_memory_stats(dev)
         g = torch.Generator(device=dev)
@@ -664,6 +668,8 @@ def main():
                     help="with --max-n: the N at which the ops are executed and checked (default 2^20)")
     ap.add_argument("--no-max-n", action="store_true",
                     help="leave the max-N report (allocation bisection + one run at N = 2^20) out of the line")
+    ap.add_argument("--sweep-only", default="",
+                    help="with --sweep: only the configs whose name contains this text")
     ap.add_argument("--sweep", action="store_true",
                     help="time the ops on the long sweep, the target shape at B = 1 and 4, the full day and "
                          "the large-key shape instead (one JSON line per config)")

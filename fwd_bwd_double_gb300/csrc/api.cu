@@ -137,8 +137,9 @@ namespace fbd {
 // accumulators would otherwise fill the 512 TMEM columns.  At d = 256 the forward
 // runs on tensor cores (64-key blocks, O in 256 TMEM columns), and so does the backward
 // without GProj (one stage of streamed tiles; the column pass split over two CTAs by
-// output half); the GProj backward and BoB at d = 256 run on the CUDA-core kernels
-// (simt.cu): their d-wide accumulators do not fit TMEM.
+// output half); the GProj backward and BoB at d = 256 run on the tf32 tensor-core engine
+// (tc_f32.cu, output columns in parts of 64 or 32): their d-wide accumulators do not fit
+// beside the pipelined kernels' tiles.
 bool tc_supports(int op, int64_t d) {
   if (d == 256) return op == 0 || op == 1;  // the backward without GProj (bwd_gproj_on_tc)
   return d == 32 || d == 64 || d == 96 || d == 128;
@@ -222,9 +223,11 @@ attn_status_t attn_bwd_passes(const attn_desc_t* desc, const void* Q, const void
   if ((s = check_ptrs(in.s, in.n, out, 4)) != ATTN_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   float4* ws = static_cast<float4*>(workspace);
-  if (tc32_path(p)) return launch_status(fbd::tc32_bwd(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st));
-  if (!tc_path(p, 1) || (gproj && !fbd::bwd_gproj_on_tc(p.d)))
-    return launch_status(fbd::simt_bwd(p, Q, K, V, O, dO, lse, dQ, dK, dV, gproj, ws, passes, st));
+  // float32 at every d, and the bf16 GProj backward past the bf16 GProj kernels (d = 256):
+  // the tf32 engine.
+  if (tc32_path(p) || (gproj && !fbd::bwd_gproj_on_tc(p.d)))
+    return launch_status(
+        fbd::tc32_bwd(p, Q, K, V, O, dO, lse, dQ, dK, dV, gproj != 0 && p.dtype == ATTN_BF16, ws, passes, st));
   // Both passes in one call: the single-pass form where it exists (bf16, d <= 64, no GProj).
   if (passes == (ATTN_ROW_PASS | ATTN_COL_PASS) && fbd::bwd_fused_applies(p, gproj != 0))
     return launch_status(fbd::tc_bwd_fused(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, st));
@@ -260,10 +263,9 @@ attn_status_t attn_bob_passes(const attn_desc_t* desc, const void* Q, const void
   if ((s = check_ptrs(in.s, in.n, out, 5)) != ATTN_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   float4* ws = static_cast<float4*>(workspace);
-  if (tc32_path(p))
-    return launch_status(fbd::tc32_bob(p, Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ, gK, gV, gdO, ws, passes, st));
-  if (!tc_path(p, 2))
-    return launch_status(fbd::simt_bob(p, Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ, gK, gV, gdO, gp, ws, passes, st));
+  // float32 at every d, and bf16 BoB past the bf16 BoB kernels (d = 256): the tf32 engine.
+  if (tc32_path(p) || !tc_path(p, 2))
+    return launch_status(fbd::tc32_bob(p, Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ, gK, gV, gdO, gp, ws, passes, st));
   if (p.d > 64)
     return launch_status(
         fbd::tc_bob128(p, Q, K, V, O, dO, lse, gdQ, gdK, gdV, gQ, gK, gV, gdO, gp, ws, passes, st));
@@ -343,7 +345,7 @@ const char* attn_status_string(attn_status_t status) {
 
 const char* attn_last_error(void) { return g_last_error; }
 
-const char* attn_version(void) { return "libfbd 0.2 (sm_103a: tcgen05/TMA bf16 path, tcgen05 tf32x3 fp32 path, CUDA-core kernels for bf16 GProj and BoB at d = 256)"; }
+const char* attn_version(void) { return "libfbd 0.2 (sm_103a: tcgen05/TMA bf16 kernels, tcgen05 tf32x3 engine for float32 and the bf16 GProj backward and BoB at d = 256)"; }
 
 }  // extern "C"
 

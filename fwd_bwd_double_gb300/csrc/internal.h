@@ -65,15 +65,7 @@ inline int64_t eff_window(const Problem& p) { return p.window > 0 ? p.window : p
 // block of 256 rows, so that no block bound derived from it ever binds.
 inline int64_t eff_window_tc(const Problem& p) { return p.window > 0 ? p.window : p.N + 512; }
 
-// CUDA-core kernels (simt.cu), bf16 inputs in fp32 arithmetic: the GProj backward and
-// BoB at d = 256, and the GProj diagnostic.  They return cudaErrorInvalidValue for
-// float32 inputs (those have tensor-core kernels at every head dim).
-cudaError_t simt_bwd(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
-                     const void* dO, const float* lse, void* dQ, void* dK, void* dV, int gproj, float4* ws,
-                     int passes, cudaStream_t st);
-cudaError_t simt_bob(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
-                     const void* dO, const float* lse, const void* a, const void* b, const void* c, void* gQ,
-                     void* gK, void* gV, void* gdO, bool gproj, float4* ws, int passes, cudaStream_t st);
+// CUDA-core kernel (simt.cu): the GProj projected-dS diagnostic export (bf16 inputs).
 cudaError_t simt_projected_dS(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
                               const void* dO, const float* lse, float* dS, cudaStream_t st);
 
@@ -81,18 +73,22 @@ cudaError_t simt_projected_dS(const Problem& p, const void* Q, const void* K, co
 // ids, hi[b][j] = last index of j's run (binary searches; ids non-decreasing along N).
 cudaError_t segment_bounds(int64_t B, int64_t N, const int* seg, int* lo, int* hi, cudaStream_t st);
 
-// float32 tensor-core path (tc_f32.cu): kind::tf32 MMAs, each product as three tf32
-// products of the operands' high and low parts, at d = 32 and 64 (tc32_supports); the
-// workspace layout is the CUDA-core kernels' (one float4 of row statistics or states per
-// row at slice pitch N).  GProj does not apply to float32 inputs.
+// The tf32 tensor-core engine (tc_f32.cu): kind::tf32 MMAs, each product as three tf32
+// products of the operands' high and low parts, synchronous steps.  It serves float32
+// inputs at every head dim (tc32_supports; GProj does not apply to float32) and the bf16
+// cases that have no bf16 kernel: the GProj backward and BoB (with or without GProj) at
+// d = 256, with the GProj rounding of dS and P applied in fp32.  Workspace layout: one
+// float4 of row statistics or states per row at slice pitch N; GProj BoB coefficients
+// one float per row at pitch N in bob_rho_region.
 bool tc32_supports(int64_t d);
 cudaError_t tc32_fwd(const Problem& p, const void* Q, const void* K, const void* V, void* O, float* lse,
                      cudaStream_t st);
 cudaError_t tc32_bwd(const Problem& p, const void* Q, const void* K, const void* V, const void* O, const void* dO,
-                     const float* lse, void* dQ, void* dK, void* dV, float4* ws, int passes, cudaStream_t st);
+                     const float* lse, void* dQ, void* dK, void* dV, bool gproj, float4* ws, int passes,
+                     cudaStream_t st);
 cudaError_t tc32_bob(const Problem& p, const void* Q, const void* K, const void* V, const void* O, const void* dO,
                      const float* lse, const void* a, const void* b, const void* c, void* gQ, void* gK, void* gV,
-                     void* gdO, float4* ws, int passes, cudaStream_t st);
+                     void* gdO, bool gproj, float4* ws, int passes, cudaStream_t st);
 uint32_t tc32_take_error();
 
 // bf16 tensor-core path (tcgen05 + TMA).  Return cudaErrorInvalidValue if a

@@ -45,9 +45,11 @@
  *               sums are fp32 additions on the CUDA cores; past d = 64 the head dim
  *               is taken in chunks of 64 and the output columns are split over CTAs
  *               in parts of 64); the bf16 GProj backward and BoB at d = 256 run on
- *               the CUDA-core kernels (fp32 arithmetic; bf16 inputs widened on load,
- *               outputs rounded once on store).  GProj does not apply to float32
- *               inputs (gproj is ignored: nothing is rounded to bf16).
+ *               the same tf32 engine (bf16 inputs widened on load, dS and P rounded
+ *               to bf16 where GProj reads them, outputs rounded once on store).
+ *               GProj does not apply to float32 inputs (gproj is ignored: nothing is
+ *               rounded to bf16).  The GProj diagnostic attn_bwd_projected_dS runs on
+ *               CUDA cores.
  *   Scale:      desc->scale == 0 means 1/sqrt(d); otherwise it must be finite and
  *               positive (the row max is subtracted before scaling).
  *   Pointers:   device pointers, 16-byte aligned (ATTN_ERR_ALIGNMENT otherwise),
