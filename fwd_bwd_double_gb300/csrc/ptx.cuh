@@ -287,6 +287,14 @@ __device__ __forceinline__ void tmem_st16x128_x4(uint32_t taddr, const uint32_t 
                "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
                : "memory");
 }
+// Four 8x8 b16 matrices to shared memory: thread t holds elements (t/4, 2(t%4)) and
+// (t/4, 2(t%4)+1) of each (register i: matrix i, low half the even column) and gives the
+// address of row t%8 of matrix t/8 (rows are 16 contiguous bytes).
+__device__ __forceinline__ void stmatrix_x4(uint32_t saddr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(r0), "r"(r1),
+               "r"(r2), "r"(r3)
+               : "memory");
+}
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 

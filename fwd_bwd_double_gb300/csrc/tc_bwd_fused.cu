@@ -350,19 +350,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t la = lo + (static_cast<uint32_t>(16 * h) << 16);
         ptx::tmem_st16x128_x4(tmem + Lay::cP + c0 / 2 + la, pk[h]);
       }
-      // dS into shared memory: key row kr, queries (q, q+1) of the 16-byte chunk of column q.
-      uint8_t* sdS = sm + Lay::odS;
+      // dS into shared memory (key rows, 128-byte lines of queries): the thread's values
+      // are the fragments of 8x8 matrices (rows: keys 8m + g4 of half h, columns: the 8
+      // queries of chunk k), so one stmatrix writes the four chunks k of a (h, m); the
+      // thread gives the address of row lane % 8 of chunk lane / 8.
+      {
+        const uint32_t sdS = ptx::smem_u32(sm + Lay::odS);
+        const int qcol = c0 + 8 * (lane >> 3);  // first query of the chunk this lane addresses
+        const uint32_t cbase = sdS + static_cast<uint32_t>((qcol >> 6) * kTile);
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
+        for (int h = 0; h < 2; ++h)
 #pragma unroll
           for (int m = 0; m < 2; ++m) {
-            const int kr = qd * 32 + 16 * h + 8 * m + g4;
-            const int qc = c0 + 8 * k + 2 * q4;  // even query column of the block
-            *reinterpret_cast<uint32_t*>(sdS + (qc >> 6) * kTile + sw128(kr, (qc & 63) >> 3) + 4 * q4) =
-                dk[h][2 * k + m];
+            const int kr = qd * 32 + 16 * h + 8 * m + (lane & 7);
+            ptx::stmatrix_x4(cbase + sw128(kr, (qcol & 63) >> 3), dk[h][m], dk[h][2 + m], dk[h][4 + m], dk[h][6 + m]);
           }
+      }
       ptx::fence_proxy_async_smem();
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
