@@ -156,48 +156,61 @@ __device__ __forceinline__ float bf16r(float x) { return __bfloat162float(__floa
 
 // KW columns [col0, col0 + KW) of R rows (row0 ...) of a row-major array with row
 // stride ld, as a K-major tile (K = KW); rows at or past `nrows` are zero.  `a`: the A
-// tile (else the B tile).
-template <int KW, typename T>
+// tile (else the B tile).  Every load of the thread is issued before the first store, so
+// the L2 round trips overlap.
+template <int KW, int R, typename T>
 __device__ __forceinline__ void stage_rows(const Ctx& c, bool a, const T* src, int ld, int col0, int64_t row0,
-                                           int64_t nrows, int R) {
-  constexpr int C4 = KW / 4;
+                                           int64_t nrows) {
+  constexpr int C4 = KW / 4, IT = R * C4 / kThreads;
+  static_assert(R * C4 % kThreads == 0, "staging split");
   uint8_t* hi = c.sm + (a ? oAh : oBh);
   uint8_t* lo = c.sm + (a ? oAl : oBl);
-  for (int idx = threadIdx.x; idx < R * C4; idx += kThreads) {
-    const int row = idx / C4, k = (idx % C4) * 4;
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (row0 + row < nrows) v = ld4(src + (row0 + row) * ld + col0 + k);
+  float4 v[IT];
+#pragma unroll
+  for (int u = 0; u < IT; ++u) {
+    const int idx = threadIdx.x + u * kThreads, row = idx / C4, k = (idx % C4) * 4;
+    v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (row0 + row < nrows) v[u] = ld4(src + (row0 + row) * ld + col0 + k);
+  }
+#pragma unroll
+  for (int u = 0; u < IT; ++u) {
+    const int idx = threadIdx.x + u * kThreads, row = idx / C4, k = (idx % C4) * 4;
     if constexpr (kExact<T>) {
-      *reinterpret_cast<float4*>(hi + swz(row, k, R)) = v;  // bf16 values are tf32 values
+      *reinterpret_cast<float4*>(hi + swz(row, k, R)) = v[u];  // bf16 values are tf32 values
     } else {
-      put4(hi, lo, swz(row, k, R), v);
+      put4(hi, lo, swz(row, k, R), v[u]);
     }
   }
 }
 
 // Columns [col0, col0 + KW) of 64 rows (row0 ...) of a row-major array with row stride
 // ld, transposed: the B tile of KW rows whose K index is the source row (the products
-// whose K is the streamed rows).
+// whose K is the streamed rows).  Loads first, as above.
 template <int KW, typename T>
 __device__ __forceinline__ void stage_rows_t(const Ctx& c, const T* src, int ld, int col0, int64_t row0,
                                              int64_t nrows) {
-  constexpr int C4 = KW / 4;
+  constexpr int C4 = KW / 4, IT = BN * C4 / kThreads;
+  static_assert(BN * C4 % kThreads == 0, "staging split");
   uint8_t* hi = c.sm + oBh;
   uint8_t* lo = c.sm + oBl;
-  for (int idx = threadIdx.x; idx < BN * C4; idx += kThreads) {
-    const int srow = idx / C4, col = (idx % C4) * 4;
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (row0 + srow < nrows) v = ld4(src + (row0 + srow) * ld + col0 + col);
-    if constexpr (kExact<T>) {
-      *reinterpret_cast<float*>(hi + swz(col, srow, KW)) = v.x;
-      *reinterpret_cast<float*>(hi + swz(col + 1, srow, KW)) = v.y;
-      *reinterpret_cast<float*>(hi + swz(col + 2, srow, KW)) = v.z;
-      *reinterpret_cast<float*>(hi + swz(col + 3, srow, KW)) = v.w;
-    } else {
-      put1(hi, lo, swz(col, srow, KW), v.x);
-      put1(hi, lo, swz(col + 1, srow, KW), v.y);
-      put1(hi, lo, swz(col + 2, srow, KW), v.z);
-      put1(hi, lo, swz(col + 3, srow, KW), v.w);
+  float4 v[IT];
+#pragma unroll
+  for (int u = 0; u < IT; ++u) {
+    const int idx = threadIdx.x + u * kThreads, srow = idx / C4, col = (idx % C4) * 4;
+    v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (row0 + srow < nrows) v[u] = ld4(src + (row0 + srow) * ld + col0 + col);
+  }
+#pragma unroll
+  for (int u = 0; u < IT; ++u) {
+    const int idx = threadIdx.x + u * kThreads, srow = idx / C4, col = (idx % C4) * 4;
+    const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if constexpr (kExact<T>) {
+        *reinterpret_cast<float*>(hi + swz(col + q, srow, KW)) = e[q];
+      } else {
+        put1(hi, lo, swz(col + q, srow, KW), e[q]);
+      }
     }
   }
 }
@@ -290,12 +303,12 @@ __device__ __forceinline__ void tile_product(Ctx& c, uint32_t col, const T* a, i
   for (int ch = 0; ch < (D + 63) / 64; ++ch) {
     const int k0 = 64 * ch;
     if (D - k0 >= 64) {
-      stage_rows<64>(c, true, a, D, k0, a0, N, BM);
-      stage_rows<64>(c, false, b, D, k0, b0, N, BN);
+      stage_rows<64, BM>(c, true, a, D, k0, a0, N);
+      stage_rows<64, BN>(c, false, b, D, k0, b0, N);
       mma3(c, col, BN, 8, accumulate || ch > 0, kExact<T>, kExact<T>);
     } else {
-      stage_rows<32>(c, true, a, D, k0, a0, N, BM);
-      stage_rows<32>(c, false, b, D, k0, b0, N, BN);
+      stage_rows<32, BM>(c, true, a, D, k0, a0, N);
+      stage_rows<32, BN>(c, false, b, D, k0, b0, N);
       mma3(c, col, BN, 4, accumulate || ch > 0, kExact<T>, kExact<T>);
     }
   }
