@@ -135,6 +135,17 @@ def test_long_sweep_sampled(N):
     print(w.name, {k: f"{v:.2e}" for k, v in errs.items()})
 
 
+@pytest.mark.parametrize("d", [64, 256])
+def test_f32_long_sampled(d):
+    """float32 on the tf32 engine over many key blocks with a ragged tail (N = 5000:
+    39 blocks of 128 rows, 79 of 64 keys), sampled rows and late columns of two heads."""
+    w = W.Workload(f"f32long_B1H2N5000d{d}_f32", 1, 2, 5000, d, "f32")
+    got = run_ops(w, to_device(W.inputs(w), w))
+    rows, cols = sample_rows_cols(w.N, np.random.default_rng(d))
+    errs = sampled_check(w, got, ("bwd", "bob"), heads=[0, 1], rows=rows, cols=cols)
+    print(w.name, {k: f"{v:.2e}" for k, v in errs.items()})
+
+
 @pytest.mark.parametrize("gproj", [0, 1])
 def test_bench_workload_sampled(gproj):
     """The throughput workload itself (B4 H12 N8192 d64 bf16, the kernels and grids the
