@@ -60,7 +60,8 @@ def launches_per_step(w, gproj):
 def executed_flops(w, kn, gproj=0):
     """Flops the tensor-core kernels execute: head dims 32 and 96 run zero-padded to
     64 and 128; the two-pass backward (GProj, or d > 64) 7 contractions, 9 with GProj;
-    None for d = 256 (CUDA-core kernels)."""
+    None for d = 256 (the backward without GProj runs the 64-wide kernels; GProj and
+    BoB the tf32 engine, whose executed work is not counted here)."""
     if w.d > 128:
         return None
     pad = 64 if w.d <= 64 else 128

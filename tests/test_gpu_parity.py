@@ -714,9 +714,8 @@ def test_window_passes_compose_on_nan_workspace(d):
                 assert torch.equal(a, r)
 
 
-# The forward at d = 256 runs on tensor cores with 64-key blocks (the backward and BoB
-# at d = 256 on the CUDA-core kernels): several row blocks, the two-block diagonal of a
-# 128-row block, ragged tails, causal and not, a window.
+# The forward at d = 256 runs on tensor cores with 64-key blocks: several row blocks, the
+# two-block diagonal of a 128-row block, ragged tails, causal and not, a window.
 @pytest.mark.parametrize("N,causal,win", [(1000, True, 0), (2500, True, 0), (1000, False, 0), (1000, True, 200)])
 def test_forward_head_dim_256_bf16(N, causal, win):
     import fwd_bwd_double_gb300 as fbd

@@ -5,7 +5,7 @@ library's file-scope scratch array instead of a caller workspace.
 
 The GPU test calls it through the C ABI several times in a row -- a larger problem
 first, then smaller ones with an odd N (a padding row in the statistics), head dim
-128 (the two-CTA BoB kernels) and 256 (the CUDA-core kernels), and again the first
+128 (the two-CTA BoB kernels) and 256 (the tf32 tensor-core engine), and again the first
 one -- and checks each result against attn_bob run with a caller workspace that
 is filled with NaN beforehand.  The bf16 parity tolerance of the other tests is the
 bound the task sets; since the two entry points run the same kernels on the same
@@ -80,7 +80,7 @@ def test_static_scratch_matches_attn_bob_on_calls_in_a_row():
     stream = torch.cuda.current_stream().cuda_stream
     cases = [("noalloc_B2H3N300d64", 2, 3, 300, 64, 0),     # the largest first
              ("noalloc_B1H2N301d128", 1, 2, 301, 128, 1),   # odd N: a padding row per slice
-             ("noalloc_B1H2N129d256", 1, 2, 129, 256, 2),   # CUDA-core kernels
+             ("noalloc_B1H2N129d256", 1, 2, 129, 256, 2),   # the tf32 engine
              ("noalloc_B2H3N300d64", 2, 3, 300, 64, 0)]     # the first one again
     for call, (name, B, H, N, d, seed) in enumerate(cases):
         t = _problem(name, B, H, N, d, seed)
