@@ -60,8 +60,8 @@ def launches_per_step(w, gproj):
 def executed_flops(w, kn, gproj=0):
     """Flops the tensor-core kernels execute: head dims 32 and 96 run zero-padded to
     64 and 128; the two-pass backward (GProj, or d > 64) 7 contractions, 9 with GProj;
-    None for d = 256 (the backward without GProj runs the 64-wide kernels; GProj and
-    BoB the tf32 engine, whose executed work is not counted here)."""
+    None for d = 256 (the backward runs the 64-wide kernels, with GProj the row pass in
+    two output halves; BoB the tf32 engine, whose executed work is not counted here)."""
     if w.d > 128:
         return None
     pad = 64 if w.d <= 64 else 128
@@ -568,8 +568,8 @@ def sweep(args):
     that produces O and L), the target shape at B = 1 and B = 4 (fwd, bwd, BoB), the
     full trading day (B2 H12 N23400: fwd, bwd), the large-key shape (B8 H8 N2048
     d128: bwd with and without GProj), the target shape at d = 128 (fwd, bwd with
-    and without GProj, BoB) and at d = 256 (fwd, bwd; and at B = 1 the GProj backward
-    and BoB, on the tf32 engine).  Median of `--steps` runs after `--warmup`,
+    and without GProj, BoB) and at d = 256 (fwd, bwd with and without GProj; and at B = 1
+    the BoB, on the tf32 engine).  Median of `--steps` runs after `--warmup`,
     CUDA events on the launching stream, min and max beside; peak device memory
     of the op's buffers (nothing else is allocated: the library allocates nothing).
     Inputs are device-drawn N(0,1) values rounded to bf16 (a timing run, not parity)."""
@@ -585,8 +585,8 @@ def sweep(args):
                 ("fullday_B2H12N23400d64", 2, 12, 23400, 64, ("fwd", "bwd")),
                 ("largekey_B8H8N2048d128", 8, 8, 2048, 128, ("bwd", "bwd_gproj")),
                 ("headdim128_B4H12N8192d128", 4, 12, 8192, 128, ("fwd", "bwd", "bwd_gproj", "bob", "bob_gproj")),
-                ("headdim256_B4H12N8192d256", 4, 12, 8192, 256, ("fwd", "bwd")),
-                ("headdim256_B1H12N8192d256", 1, 12, 8192, 256, ("bwd", "bwd_gproj", "bob", "bob_gproj"))]
+                ("headdim256_B4H12N8192d256", 4, 12, 8192, 256, ("fwd", "bwd", "bwd_gproj")),
+                ("headdim256_B1H12N8192d256", 1, 12, 8192, 256, ("bob", "bob_gproj"))]
     reps, warm = max(args.steps, 1), max(args.warmup, 1)
     for name, B, H, N, d, ops in configs:
         if args.sweep_only and args.sweep_only not in name:

@@ -136,15 +136,14 @@ namespace fbd {
 // d > 64 splits each block over two CTAs by output half: its row pass's four d-wide
 // accumulators would otherwise fill the 512 TMEM columns.  At d = 256 the forward
 // runs on tensor cores (64-key blocks, O in 256 TMEM columns), and so does the backward
-// without GProj (one stage of streamed tiles; the column pass split over two CTAs by
-// output half); the GProj backward and BoB at d = 256 run on the tf32 tensor-core engine
-// (tc_f32.cu, output columns in parts of 64 or 32): their d-wide accumulators do not fit
-// beside the pipelined kernels' tiles.
+// with and without GProj (one stage of streamed tiles; the column pass, and with GProj the
+// row pass, split over two CTAs by output half); the BoB at d = 256 runs on the tf32
+// tensor-core engine (tc_f32.cu, output columns in parts of 64 or 32): its d-wide
+// accumulators and held operands do not fit beside the pipelined kernels' tiles.
 bool tc_supports(int op, int64_t d) {
-  if (d == 256) return op == 0 || op == 1;  // the backward without GProj (bwd_gproj_on_tc)
+  if (d == 256) return op == 0 || op == 1;
   return d == 32 || d == 64 || d == 96 || d == 128;
 }
-bool bwd_gproj_on_tc(int64_t d) { return d <= 128; }
 }  // namespace fbd
 
 namespace fbd {
@@ -223,11 +222,8 @@ attn_status_t attn_bwd_passes(const attn_desc_t* desc, const void* Q, const void
   if ((s = check_ptrs(in.s, in.n, out, 4)) != ATTN_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   float4* ws = static_cast<float4*>(workspace);
-  // float32 at every d, and the bf16 GProj backward past the bf16 GProj kernels (d = 256):
-  // the tf32 engine.
-  if (tc32_path(p) || (gproj && !fbd::bwd_gproj_on_tc(p.d)))
-    return launch_status(
-        fbd::tc32_bwd(p, Q, K, V, O, dO, lse, dQ, dK, dV, gproj != 0 && p.dtype == ATTN_BF16, ws, passes, st));
+  // float32 at every d: the tf32 engine (GProj does not apply).
+  if (tc32_path(p)) return launch_status(fbd::tc32_bwd(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st));
   // Both passes in one call: the single-pass form where it exists (bf16, d <= 64, no GProj).
   if (passes == (ATTN_ROW_PASS | ATTN_COL_PASS) && fbd::bwd_fused_applies(p, gproj != 0))
     return launch_status(fbd::tc_bwd_fused(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, st));

@@ -76,16 +76,15 @@ cudaError_t segment_bounds(int64_t B, int64_t N, const int* seg, int* lo, int* h
 // The tf32 tensor-core engine (tc_f32.cu): kind::tf32 MMAs, each product as three tf32
 // products of the operands' high and low parts, synchronous steps.  It serves float32
 // inputs at every head dim (tc32_supports; GProj does not apply to float32) and the bf16
-// cases that have no bf16 kernel: the GProj backward and BoB (with or without GProj) at
-// d = 256, with the GProj rounding of dS and P applied in fp32.  Workspace layout: one
+// case that has no bf16 kernel: the BoB (with or without GProj) at d = 256, with the GProj
+// rounding of dS and P applied in fp32.  Workspace layout: one
 // float4 of row statistics or states per row at slice pitch N; GProj BoB coefficients
 // one float per row at pitch N in bob_rho_region.
 bool tc32_supports(int64_t d);
 cudaError_t tc32_fwd(const Problem& p, const void* Q, const void* K, const void* V, void* O, float* lse,
                      cudaStream_t st);
 cudaError_t tc32_bwd(const Problem& p, const void* Q, const void* K, const void* V, const void* O, const void* dO,
-                     const float* lse, void* dQ, void* dK, void* dV, bool gproj, float4* ws, int passes,
-                     cudaStream_t st);
+                     const float* lse, void* dQ, void* dK, void* dV, float4* ws, int passes, cudaStream_t st);
 cudaError_t tc32_bob(const Problem& p, const void* Q, const void* K, const void* V, const void* O, const void* dO,
                      const float* lse, const void* a, const void* b, const void* c, void* gQ, void* gK, void* gV,
                      void* gdO, bool gproj, float4* ws, int passes, cudaStream_t st);
@@ -147,7 +146,6 @@ __host__ __device__ inline int64_t bob_rho_pitch(int64_t N) { return (N + 3) & ~
 
 // Which kernels exist for a given (op, dtype, d): false means ATTN_ERR_UNSUPPORTED.
 bool tc_supports(int op, int64_t d);  // op: 0 fwd, 1 bwd, 2 bob
-bool bwd_gproj_on_tc(int64_t d);       // the GProj backward has tensor-core kernels at this d
 
 // Device status words (bit FBD_ERR_TIMEOUT), read-and-cleared per translation unit.
 uint32_t tc_fwd_take_error();

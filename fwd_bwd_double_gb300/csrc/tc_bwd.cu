@@ -56,11 +56,16 @@ using tc::bf16_lo;
 using tc::f;
 
 // ================================================================ row pass
+// With GProj at d = 256 the accumulators dQ and P^ K of the whole head dim would take
+// 512 TMEM columns beside the tiles: each row block then runs as two CTAs, CTA h
+// accumulating and writing output columns [DO h, DO h + DO) (DO = 128); both compute the
+// full score tiles and the coefficient rho.
 template <int D, int NB, bool GP>
 struct RowLay {
+  static constexpr int DO = (GP && D == 256) ? 128 : D;  // output columns a CTA accumulates
   // TMEM columns used (see below); at most 256 lets two CTAs share an SM, in which
   // case the ring is shortened so that both fit in shared memory.
-  static constexpr int kCols = 2 * NB * BN + NB * BN / 2 + (GP ? NB * BN / 2 : 0) + D + (GP ? D : 0);
+  static constexpr int kCols = 2 * NB * BN + NB * BN / 2 + (GP ? NB * BN / 2 : 0) + DO + (GP ? DO : 0);
   static constexpr int kTmem = kCols <= 256 ? 256 : 512;
   static constexpr int kMinBlocks = kTmem == 256 ? 2 : 1;
   static constexpr int NS = kTmem == 256 ? 4 : stages<D>();
@@ -71,8 +76,8 @@ struct RowLay {
   static constexpr int oBar = oRed + 6 * BM * 4;
   static constexpr int bytes = oBar + 256;
   static constexpr int cS = 0, cdP = NB * BN, cdS = 2 * NB * BN, cP = cdS + NB * BN / 2;
-  static constexpr int cdQ = cP + (GP ? NB * BN / 2 : 0), cPK = cdQ + D;
-  static constexpr int cols = cPK + (GP ? D : 0);
+  static constexpr int cdQ = cP + (GP ? NB * BN / 2 : 0), cPK = cdQ + DO;
+  static constexpr int cols = cPK + (GP ? DO : 0);
   static_assert(cols == kCols && cols <= 512, "TMEM budget");
 };
 
@@ -87,7 +92,7 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
                    int Np, int nrb, int BH, float scale, float c, int causal, Band bd, int G, int dv) {
   using Lay = RowLay<D, NB, GP>;
   static_assert(NB == 1, "one score-tile buffer, released early");
-  constexpr int NS = Lay::NS;
+  constexpr int NS = Lay::NS, DO = Lay::DO, HV = D / DO;  // HV CTAs per row block, one per output part
   extern __shared__ __align__(1024) uint8_t sm[];
   uint64_t* q_full = reinterpret_cast<uint64_t*>(sm + Lay::oBar);
   uint64_t* full = q_full + 1;
@@ -102,7 +107,8 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
   float* red = reinterpret_cast<float*>(sm + Lay::oRed);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const tc::Order ord = tc::grid_order(BH, nrb);
+  const int opart = HV > 1 ? static_cast<int>(blockIdx.x) % HV : 0;  // output columns [DO opart, DO opart + DO)
+  const tc::Order ord = tc::grid_order_at(static_cast<int>(blockIdx.x) / HV, BH, nrb);
   const int bh = ord.bh;
   const int rb = nrb - 1 - ord.k;  // heaviest row blocks first (within a group of slices)
   // key blocks j0 + j, j < nkv: those touching rows <= the last row (all key blocks when
@@ -166,14 +172,15 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
     // ---------------------------------------------------------------- MMA
     if (ok) {  // all 32 lanes; one elected lane issues each MMA and commit
       constexpr uint32_t idS = ptx::idesc_bf16(BM, BN, 0, 0);
-      constexpr uint32_t idQ = ptx::idesc_bf16(BM, D, 0, 1);
+      constexpr uint32_t idQ = ptx::idesc_bf16(BM, DO, 0, 1);
       const uint32_t sQ = ptx::smem_u32(sm + Lay::oQ), sdO = ptx::smem_u32(sm + Lay::odO);
       const uint32_t sK = ptx::smem_u32(sm + Lay::oK), sV = ptx::smem_u32(sm + Lay::oV);
+      const uint32_t po = static_cast<uint32_t>(opart * (DO / 64) * BN * 128);  // this CTA's column slabs
       auto products = [&](int t) {  // dQ (+ P^ K) of tile t, then release its stage
         const int b = t % NB, s = t % NS;
         wait(&ds_ready[b], (t / NB) & 1);
         ptx::tc_fence_after();
-        const uint32_t kt = sK + s * Lay::kStream;
+        const uint32_t kt = sK + s * Lay::kStream + po;
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k) {
           const uint64_t bd = tc::mnmajor_desc(kt, BN, k);
@@ -299,12 +306,13 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
     wait(acc_full, 0);
     ptx::tc_fence_after();
 #pragma unroll
-    for (int cc = 0; cc < D / 2; cc += 32) {
+    for (int cc = 0; cc < DO / 2; cc += 32) {
       uint32_t a[32], pkv[32];
-      ptx::tmem_ld32(tmem + Lay::cdQ + hf * (D / 2) + cc + lo, a);
-      if constexpr (GP) ptx::tmem_ld32(tmem + Lay::cPK + hf * (D / 2) + cc + lo, pkv);
+      ptx::tmem_ld32(tmem + Lay::cdQ + hf * (DO / 2) + cc + lo, a);
+      if constexpr (GP) ptx::tmem_ld32(tmem + Lay::cPK + hf * (DO / 2) + cc + lo, pkv);
       ptx::tmem_wait_ld();
-      if (live && hf * (D / 2) + cc < dv) {
+      const int col = opart * DO + hf * (DO / 2) + cc;  // first of the 32 output columns
+      if (live && col < dv) {
         uint32_t o[16];
 #pragma unroll
         for (int t = 0; t < 32; t += 2) {
@@ -315,12 +323,12 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
           }
           o[t >> 1] = ptx::pack_bf16(scale * v0, scale * v1);
         }
-        uint4* dst = reinterpret_cast<uint4*>(dQ + rowoff + hf * (D / 2) + cc);
+        uint4* dst = reinterpret_cast<uint4*>(dQ + rowoff + col);
 #pragma unroll
         for (int u = 0; u < 4; ++u) dst[u] = make_uint4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
       }
     }
-    if (hf == 0 && row < Np) {  // row statistics, negated, pair-interleaved (see the column pass)
+    if (hf == 0 && opart == 0 && row < Np) {  // row statistics, negated, pair-interleaved (see the column pass)
       // The row past N of an odd-length slice gets zeros: the column pass reads it (with P = 0).
       float* wf = reinterpret_cast<float*>(ws) + static_cast<size_t>(bh) * Np * 4;
       const int64_t k2 = row & ~static_cast<int64_t>(1);
@@ -609,7 +617,7 @@ cudaError_t launch(const Problem& p, const void* Q, const void* K, const void* V
     auto kern = banded(p) ? bwd_row_kernel<D, NBR, GP, true> : bwd_row_kernel<D, NBR, GP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::bytes);
     if (e != cudaSuccess) return e;
-    kern<<<static_cast<unsigned>(nrb * BH), kThreads, Lay::bytes, st>>>(
+    kern<<<static_cast<unsigned>(nrb * BH * (D / Lay::DO)), kThreads, Lay::bytes, st>>>(
         q128, do128, k64, v64, static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), lse,
         static_cast<__nv_bfloat16*>(dQ), ws, static_cast<int>(N), static_cast<int>(Np), nrb, static_cast<int>(BH),
         p.scale, c, p.causal, make_band(p, eff_window_tc(p), false), p.group, static_cast<int>(d));
@@ -639,13 +647,13 @@ cudaError_t tc_bwd(const Problem& p, const void* Q, const void* K, const void* V
   // d = 32 runs the d = 64 kernels and d = 96 the d = 128 ones, zero-padded in shared memory.
   // d <= 64, with or without GProj: the 128-wide kernels.
   if (p.d <= 64) return tc_bwd_wide(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st, gproj != 0);
-  if (gproj) return launch<128, 1, 1, true>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st);
-  // d = 256 without GProj: both passes here (one stage; the column pass in two output
-  // halves).  GProj at d = 256 would need 704 TMEM columns in the row pass.
+  // d = 256: both passes here (one stage; the column pass in two output halves, and with
+  // GProj the row pass too).
   if (p.d > 128) {
-    if (gproj) return cudaErrorInvalidValue;
+    if (gproj) return launch<256, 1, 1, true>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st);
     return launch<256, 1, 1, false>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st);
   }
+  if (gproj) return launch<128, 1, 1, true>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st);
   // d = 96, 128 without GProj: the 128-wide row pass, then this file's column pass
   // (both use the same pair-interleaved row statistics).
   if (passes & 1) {

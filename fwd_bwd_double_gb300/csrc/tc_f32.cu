@@ -1,6 +1,6 @@
 // The tf32 tensor-core engine (tcgen05, kind::tf32): float32 attention at every head dim
 // (forward, backward row and column passes, BoB row and column passes), and the bf16
-// cases the pipelined bf16 kernels do not cover (the GProj backward and BoB at d = 256).
+// case the pipelined bf16 kernels do not cover (the BoB at d = 256, with or without GProj).
 // The decomposition is the one of the bf16 kernels:
 //   forward   online softmax ("Flash attention for trading models", "Online softmax
 //             recurrence"), O and the natural-log lse written once;
@@ -15,8 +15,8 @@
 //             gV = dPbar^T dO, gK = s (dS^T a + Sbar^T Q), with G = s (a K^T + Q b^T),
 //             H = dO c^T, W = G dS + P H, dPbar = P (G - E),
 //             Sbar = P (G (dP - D) - E dP + H - F);
-//   GProj     (bf16, "FlashAttention bf16 gradient and GProj", "How the zero sum turns
-//             into a false gradient"): the products that contract dS see bf16(dS)
+//   GProj     (bf16 BoB, "FlashAttention bf16 gradient and GProj", "How the zero sum
+//             turns into a false gradient"): the products that contract dS see bf16(dS)
 //             projected to zero row sum with bf16(P), rho_i = sum_j bf16(dS_ij) /
 //             sum_j bf16(P_ij).
 //
@@ -472,24 +472,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // --------------------------------------------------------- backward, rows
-// GP (GProj, bf16 inputs): the dS K product sees bf16(dS) and P^ K = sum_j bf16(P_ij) k_j
-// is accumulated beside it; dQ = s (bf16(dS) K - rho P^ K), rho_i = sum_j bf16(dS_ij) /
-// sum_j bf16(P_ij) (the projection of the rounded dS row to zero sum), and rho goes to
-// the row statistics for the column pass.
-template <typename T, int D, bool GP>
+// dQ = s dS K with dS in fp32 (GProj, a bf16 rounding remedy, does not apply).
+template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     f32_bwd_row_kernel(const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V,
                        const T* __restrict__ O, const T* __restrict__ dO, const float* __restrict__ lse,
                        T* __restrict__ dQ, float4* __restrict__ ws, int N, int nrb, int BH, float scale, int causal,
                        Band bd, int G) {
   extern __shared__ __align__(1024) uint8_t sm[];
-  Ctx c = setup(sm, 256);  // S 0-63, dP / P^ 64-127, dQ 128-191, P^ K 192-255 (this part's columns)
+  Ctx c = setup(sm, 256);  // S 0-63, dP 64-127, dQ 128-191 (this part's columns)
   const Where w = where<D, 64>(BH, nrb, true);
   const int bh = w.slice, rb = w.blk, kvh = bh / G;
   const int64_t i = static_cast<int64_t>(rb) * BM + threadIdx.x, r0 = static_cast<int64_t>(rb) * BM;
   const size_t qo = static_cast<size_t>(bh) * N * D, ko = static_cast<size_t>(kvh) * N * D;
   const int lo_i = causal ? bd.row_lo(bh, i) : 0;
-  float Di = 0.f, Li = 0.f, r = 0.f, sp = 0.f;
+  float Di = 0.f, Li = 0.f;
   if (i < N) {
     Di = row_dot<D>(dO + qo + i * D, O + qo + i * D);
     Li = lse[static_cast<size_t>(bh) * N + i];
@@ -509,46 +506,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t key = k0 + 32 * h + t;
         const bool vis = i < N && key < N && (!causal || (key <= i && key >= lo_i));
         const float p = vis ? expf(s[t] * scale - Li) : 0.f;
-        float ds = p * (dp[t] - Di);
-        if constexpr (GP) {
-          ds = bf16r(ds);
-          dp[t] = bf16r(p);  // P^, kept in the dP columns for the P^ K product
-          r += ds;
-          sp += dp[t];
-        }
-        s[t] = ds;
+        s[t] = p * (dp[t] - Di);
       }
       stage_own(c, 32 * h, s);
-      if constexpr (GP) tst(c, 64 + 32 * h, dp);
     }
     out_product(c, 128, 0, K + ko, D, w.p0, w.np, k0, N, kb == rr.k0);  // dQ += dS K (scratch: the read S)
-    if constexpr (GP) {
-      stage_tmem(c, 64);
-      out_product(c, 192, 0, K + ko, D, w.p0, w.np, k0, N, kb == rr.k0);  // P^ K
-    }
   }
-  const float rho = GP ? r / sp : 0.f;
 #pragma unroll 1
   for (int h = 0; h < w.np / 32; ++h) {
     float g[32];
     tld(c, 128 + 32 * h, g);
-    if constexpr (GP) {
-      float pk[32];
-      tld(c, 192 + 32 * h, pk);
-#pragma unroll
-      for (int t = 0; t < 32; ++t) g[t] -= rho * pk[t];
-    }
 #pragma unroll
     for (int t = 0; t < 32; ++t) g[t] *= scale;
     if (i < N) store32(dQ + qo + i * D + w.p0 + 32 * h, g);
   }
-  if (i < N && w.p0 == 0) ws[static_cast<size_t>(bh) * N + i] = make_float4(Li, Di, rho, 0.f);
+  if (i < N && w.p0 == 0) ws[static_cast<size_t>(bh) * N + i] = make_float4(Li, Di, 0.f, 0.f);
   teardown(c, 256);
 }
 
 // ------------------------------------------------------- backward, columns
-// GP: dV takes bf16(P) and dK the projected bf16(dS) - rho_i bf16(P).
-template <typename T, int D, bool GP>
+template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     f32_bwd_col_kernel(const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V,
                        const T* __restrict__ dO, const float4* __restrict__ ws, T* __restrict__ dK, T* __restrict__ dV,
@@ -582,17 +559,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int t = 0; t < 32; ++t) {
           const int64_t qi = q0 + 32 * h + t;
-          const float4 sv = st[32 * h + t];  // (lse, D, rho) of query qi
+          const float4 sv = st[32 * h + t];  // (lse, D) of query qi
           const bool vis = key < N && qi < N && (!causal || (qi >= key && qi <= hi_k));
           const float p = vis ? expf(s[t] * scale - sv.x) : 0.f;
-          const float ds = p * (dp[t] - sv.y);
-          if constexpr (GP) {
-            s[t] = bf16r(p);
-            dp[t] = bf16r(ds) - sv.z * s[t];
-          } else {
-            s[t] = p;
-            dp[t] = ds;
-          }
+          dp[t] = p * (dp[t] - sv.y);
+          s[t] = p;
         }
         stage_own(c, 32 * h, s);  // P^T
         tst(c, 64 + 32 * h, dp);
@@ -862,13 +833,13 @@ cudaError_t fwd_t(const Problem& p, const void* Q, const void* K, const void* V,
   return cudaGetLastError();
 }
 
-template <typename T, int D, bool GP>
+template <typename T, int D>
 cudaError_t bwd_t(const Problem& p, const void* Q, const void* K, const void* V, const void* O, const void* dO,
                   const float* lse, void* dQ, void* dK, void* dV, float4* ws, int passes, cudaStream_t st) {
   using CT = const T*;
   const int nb = blocks_of(p.N, BM);
   if (passes & 1) {
-    auto k = f32_bwd_row_kernel<T, D, GP>;
+    auto k = f32_bwd_row_kernel<T, D>;
     cudaError_t e = launch_prep(k, kSmem);
     if (e != cudaSuccess) return e;
     k<<<grid_of(nb, p.BH, parts_of(D, 64)), kThreads, kSmem, st>>>(
@@ -878,7 +849,7 @@ cudaError_t bwd_t(const Problem& p, const void* Q, const void* K, const void* V,
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (passes & 2) {
-    auto k = f32_bwd_col_kernel<T, D, GP>;
+    auto k = f32_bwd_col_kernel<T, D>;
     cudaError_t e = launch_prep(k, kSmem);
     if (e != cudaSuccess) return e;
     k<<<grid_of(nb, p.BHkv, parts_of(D, 64)), kThreads, kSmem, st>>>(
@@ -921,7 +892,7 @@ cudaError_t bob_t(const Problem& p, const void* Q, const void* K, const void* V,
   return cudaSuccess;
 }
 
-// float32 at every head dim; bf16 only at d = 256 (the cases without a bf16 kernel).
+// float32 at every head dim; bf16 only at d = 256 (the BoB, which has no bf16 kernel there).
 template <typename F>
 cudaError_t with_case(const Problem& p, F&& f) {
   if (p.dtype == ATTN_BF16) {
@@ -952,16 +923,11 @@ cudaError_t tc32_fwd(const Problem& p, const void* Q, const void* K, const void*
 }
 
 cudaError_t tc32_bwd(const Problem& p, const void* Q, const void* K, const void* V, const void* O, const void* dO,
-                     const float* lse, void* dQ, void* dK, void* dV, bool gproj, float4* ws, int passes,
-                     cudaStream_t st) {
+                     const float* lse, void* dQ, void* dK, void* dV, float4* ws, int passes, cudaStream_t st) {
   return with_case(p, [&](auto t, auto dd) {
     using T = decltype(t);
-    if constexpr (std::is_same_v<T, __nv_bfloat16>) {
-      if (gproj) return bwd_t<T, dd(), true>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st);
-      return cudaErrorInvalidValue;  // the bf16 backward without GProj has its own kernels at every d
-    } else {
-      return bwd_t<T, dd(), false>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st);
-    }
+    if constexpr (std::is_same_v<T, float>) return bwd_t<T, dd()>(p, Q, K, V, O, dO, lse, dQ, dK, dV, ws, passes, st);
+    return cudaErrorInvalidValue;  // the bf16 backward has its own kernels at every d
   });
 }
 

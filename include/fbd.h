@@ -36,7 +36,7 @@
  *               (or ATTN_ERR_INVALID_ARG) before any launch.
  *   Kernels:    the shape decides, never a failure: bf16 attn_fwd, attn_bwd and
  *               attn_bob at d in {32, 64, 96, 128}, and bf16 attn_fwd and attn_bwd
- *               (without GProj) at d = 256, run on the tcgen05/TMA tensor-core kernels
+ *               (with or without GProj) at d = 256, run on the tcgen05/TMA tensor-core kernels
  *               (d = 32 and 96 on those of d = 64 and 128, the head dim zero-padded in
  *               shared memory); float32 inputs at every d run on tcgen05
  *               kind::tf32 kernels that form each product from the operands' tf32
@@ -44,9 +44,9 @@
  *               relative per element product, fp32 accumulation; across blocks the
  *               sums are fp32 additions on the CUDA cores; past d = 64 the head dim
  *               is taken in chunks of 64 and the output columns are split over CTAs
- *               in parts of 64); the bf16 GProj backward and BoB at d = 256 run on
- *               the same tf32 engine (bf16 inputs widened on load, dS and P rounded
- *               to bf16 where GProj reads them, outputs rounded once on store).
+ *               in parts of 64); the bf16 BoB at d = 256 runs on the same tf32 engine
+ *               (bf16 inputs widened on load, dS and P rounded to bf16 where GProj
+ *               reads them, outputs rounded once on store).
  *               GProj does not apply to float32 inputs (gproj is ignored: nothing is
  *               rounded to bf16).  The GProj diagnostic attn_bwd_projected_dS runs on
  *               CUDA cores.

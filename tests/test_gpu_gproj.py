@@ -82,7 +82,7 @@ def _rho_vs_own_residual(rho_ws, r_readout, l1, abs_tol):
     return np.abs(rho_ws[keep] - r_readout[keep]) / (np.abs(r_readout[keep]) + abs_tol * l1[keep])
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_backward_projected_rows_sum_to_zero_on_the_hot_path(d):
     import torch
 
@@ -196,17 +196,15 @@ def test_bob_projected_rows_sum_to_zero_on_the_hot_path(d):
 
 
 
-def test_gproj_head_dim_256_on_the_tf32_engine():
-    """bf16 at d = 256: the GProj backward and BoB run on the tf32 tensor-core engine,
-    which forms dS and P in fp32 and rounds them to bf16 where the projection reads them.
-    Every output is checked against the oracle with and without GProj; the projected rows
-    are read off the outputs' constant-key column; the coefficients rho it leaves in the
-    workspace (backward: the third float of each row's statistics, slice pitch N; BoB: one
-    float per row at pitch N behind the states) are checked against the residual the
-    GProj-free products carried (read off their constant-key column), as on the d <= 128
-    kernels: that residual includes the one from the bf16 O in D_i = dO_i . O_i, which the
-    oracle's emulation (exact O) does not have.  The BoB coefficients also reach gK through
-    the column pass, whose output is checked against the oracle."""
+def test_bob_gproj_head_dim_256_on_the_tf32_engine():
+    """bf16 BoB at d = 256: it runs on the tf32 tensor-core engine, which forms dS and P in
+    fp32 and rounds them to bf16 where the projection reads them.  Every output is checked
+    against the oracle with and without GProj; the projected rows are read off gQ's
+    constant-key column; the coefficients rho it leaves in the workspace (one float per row
+    at pitch N behind the states) are checked against the residual the GProj-free products
+    carried (read off their constant-key column).  The coefficients also reach gK through
+    the column pass, whose output is checked against the oracle.  (The d = 256 GProj
+    backward runs on the pipelined kernels and is checked by the backward test above.)"""
     import torch
 
     import fwd_bwd_double_gb300 as fbd
@@ -217,56 +215,40 @@ def test_gproj_head_dim_256_on_the_tf32_engine():
     Np = (N + 1) // 2 * 2
     O, lse = fbd.attn_fwd(xd["Q"], xd["K"], xd["V"])
     desc = fbd.make_desc(xd["Q"])
-    wsb = torch.full((fbd.attn_bwd_workspace_bytes(desc, 1) // 4,), float("nan"), dtype=torch.float32, device="cuda")
     wsg = torch.full((fbd.attn_bob_workspace_bytes(desc, 1) // 4,), float("nan"), dtype=torch.float32, device="cuda")
-    bo = [torch.empty_like(xd["Q"]) for _ in range(3)]
     go = [torch.empty_like(xd["Q"]) for _ in range(4)]
     for ps in (fbd.ATTN_ROW_PASS, fbd.ATTN_COL_PASS):
-        fbd.attn_bwd_passes(xd["Q"], xd["K"], xd["V"], O, xd["dO"], lse, ps, 1, *bo, workspace=wsb)
         fbd.attn_bob_passes(xd["Q"], xd["K"], xd["V"], O, xd["dO"], lse, xd["gdQ"], xd["gdK"], xd["gdV"], ps, *go,
                             workspace=wsg, gproj=1)
     fbd.attn_device_status()
-    bo, go, wsb, wsg = [host(t) for t in bo], [host(t) for t in go], host(wsb), host(wsg)
-    plain_b = [host(t) for t in fbd.attn_bwd(xd["Q"], xd["K"], xd["V"], O, xd["dO"], lse, gproj=0)]
+    go, wsg = [host(t) for t in go], host(wsg)
     plain_g = [host(t) for t in fbd.attn_bob(xd["Q"], xd["K"], xd["V"], O, xd["dO"], lse, xd["gdQ"], xd["gdK"],
                                              xd["gdV"], gproj=0)]
-    rows_b, rows_g, rho_b, rho_g, errs = [], [], [], [], {}
+    rows_g, rho_g, errs = [], [], {}
     for h in range(H):
         sl = {k: x[k][0, h].astype(np.float64) for k in W.TENSORS}
         args = (sl["Q"], sl["K"], sl["V"], sl["dO"], sl["gdQ"], sl["gdK"], sl["gdV"])
-        rb, rg = oracle.backward(*args[:4]), oracle.bob(*args)
-        for gp, outs in ((1, bo), (0, plain_b)):
-            for k, o in zip(("dQ", "dK", "dV"), outs):
-                errs[(gp, k, h)] = rel_fro(o[0, h], rb[k])
+        rg = oracle.bob(*args)
         for gp, outs in ((1, go), (0, plain_g)):
             for k, o in zip(("gQ", "gK", "gV", "gdO"), outs):
                 errs[(gp, k, h)] = rel_fro(o[0, h], rg[k])
-        eb = oracle.backward_bf16_dS(*args[:4], gproj=True)
         eg = oracle.bob_bf16_dS(*args, True)
-        keep = eb["l1"] > 0
-        rows_b.append(np.abs(bo[0][0, h, :, 0] / (s * C))[keep] / eb["l1"][keep])
         l1g = eg["l1_dS"] + eg["l1_Sbar"]
         keepg = eg["l1_dS"] > 0
         rows_g.append(np.abs(go[0][0, h, :, 0] / (s * C))[keepg] / l1g[keepg])
-        i = np.arange(N)
-        rb_gpu = wsb[(h * N + i) * 4 + 2]
-        rg_gpu = wsg[H * Np * 4 + h * N + i]
-        rho_b.append(_rho_vs_own_residual(rb_gpu[keep], (plain_b[0][0, h, :, 0] / (s * C))[keep], eb["l1"][keep],
-                                          ROWSUM_MAX))
+        rg_gpu = wsg[H * Np * 4 + h * N + np.arange(N)]
         # The GProj-free BoB on this engine keeps dS in fp32, so its residual lacks the bf16
         # rounding residual that rho also carries; their difference is measured against the
         # size of that rounding residual as the oracle's emulation gives it.
         rs0g = (plain_g[0][0, h, :, 0] / (s * C))[keepg]
         rho_g.append(np.abs(rg_gpu[keepg] - rs0g) / (np.abs(rs0g) + np.abs(eg["r"][keepg]) + BOB_READOUT * l1g[keepg]))
-    rows_b, rows_g, rho_b, rho_g = (np.concatenate(v) for v in (rows_b, rows_g, rho_b, rho_g))
+    rows_g, rho_g = (np.concatenate(v) for v in (rows_g, rho_g))
     worst = {f"{k[1]}{'+GP' if k[0] else ''}": max(v for kk, v in errs.items() if kk[:2] == k[:2]) for k in errs}
     pg = np.percentile(rows_g, [50, 99.9, 100])
-    print("d=256 engine: rel-Fro errors (worst head)", {k: f"{v:.2e}" for k, v in worst.items()})
-    print(f"d=256 engine: projected row sums / L1, backward median {np.median(rows_b):.2e} max {rows_b.max():.2e}; "
-          f"BoB percentiles 50/99.9/100 {pg[0]:.2e} {pg[1]:.2e} {pg[2]:.2e}; rho vs the GProj-free residual: "
-          f"backward median {np.median(rho_b):.2e}, BoB median {np.median(rho_g):.2e}")
+    print("d=256 BoB engine: rel-Fro errors (worst head)", {k: f"{v:.2e}" for k, v in worst.items()})
+    print(f"d=256 BoB engine: projected row sums / L1 percentiles 50/99.9/100 {pg[0]:.2e} {pg[1]:.2e} {pg[2]:.2e}; "
+          f"rho vs the GProj-free residual: median {np.median(rho_g):.2e}")
     bad = {k: v for k, v in errs.items() if not v <= 2e-2}
     assert not bad, bad
-    assert np.median(rows_b) <= ROWSUM_TOL and rows_b.max() <= ROWSUM_MAX
     assert pg[0] <= ROWSUM_TOL and pg[1] <= BOB_READOUT and pg[2] <= 10 * BOB_READOUT
-    assert np.median(rho_b) <= 1e-2 and np.median(rho_g) <= 1.0
+    assert np.median(rho_g) <= 1.0
