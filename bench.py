@@ -314,9 +314,11 @@ def run_ours(args, w, rank, world):
 
     # End to end: every step copies its 7 inputs from pinned host memory to the device,
     # runs the five launches and copies O, lse and the 7 outputs back to pinned host
-    # memory.  The copies of step i+1's inputs and of step i-1's outputs run on their
-    # own streams (the GPU's copy engines) while step i computes; input and output
-    # device buffers are double-buffered, and events order reuse.
+    # memory.  The copies run on their own streams (the GPU's copy engines) while other
+    # steps compute; input and output device buffers are double-buffered, and events order
+    # reuse.  Each op waits only for the inputs it reads (the forward for Q, K, V, the
+    # backward for dO, the BoB for the cotangents), and each op's outputs leave as soon as
+    # it has finished, so the pipeline's fill and drain are one op's copies, not a step's.
     host_out = {k: torch.empty(out[k].shape, dtype=bf).pin_memory() for k in out}
     host_lse = torch.empty(shp[:3], dtype=torch.float32).pin_memory()
     # The pipeline's fill (the first inputs) and drain (the last outputs) are inside the
@@ -326,18 +328,24 @@ def run_ours(args, w, rank, world):
     xin = [{k: torch.empty_like(v) for k, v in x.items()} for _ in range(2)]
     outs = [{k: torch.empty_like(out[k]) for k in out} for _ in range(2)]
     lses = [torch.empty(shp[:3], dtype=torch.float32, device=dev) for _ in range(2)]
+    # per op: the inputs it is the first to read, and the outputs it writes
+    op_in = (("Q", "K", "V"), ("dO",), ("gdQ", "gdK", "gdV"))
+    op_out = (("O",), ("dQ", "dK", "dV"), ("gQ", "gK", "gV", "gdO"))
 
-    def e2e_step(xx, oo, ll):
-        fbd.attn_fwd(xx["Q"], xx["K"], xx["V"], O=oo["O"], lse=ll, stream=stream, desc=desc)
-        fbd.attn_bwd(xx["Q"], xx["K"], xx["V"], oo["O"], xx["dO"], ll, gproj=args.gproj, dQ=oo["dQ"], dK=oo["dK"],
-                     dV=oo["dV"], workspace=ws, stream=stream, desc=desc)
-        fbd.attn_bob(xx["Q"], xx["K"], xx["V"], oo["O"], xx["dO"], ll, xx["gdQ"], xx["gdK"], xx["gdV"], gQ=oo["gQ"],
-                     gK=oo["gK"], gV=oo["gV"], gdO=oo["gdO"], workspace=ws2, stream=stream, desc=desc,
-                     gproj=args.gproj)
+    def e2e_op(j, xx, oo, ll):
+        if j == 0:
+            fbd.attn_fwd(xx["Q"], xx["K"], xx["V"], O=oo["O"], lse=ll, stream=stream, desc=desc)
+        elif j == 1:
+            fbd.attn_bwd(xx["Q"], xx["K"], xx["V"], oo["O"], xx["dO"], ll, gproj=args.gproj, dQ=oo["dQ"],
+                         dK=oo["dK"], dV=oo["dV"], workspace=ws, stream=stream, desc=desc)
+        else:
+            fbd.attn_bob(xx["Q"], xx["K"], xx["V"], oo["O"], xx["dO"], ll, xx["gdQ"], xx["gdK"], xx["gdV"],
+                         gQ=oo["gQ"], gK=oo["gK"], gV=oo["gV"], gdO=oo["gdO"], workspace=ws2, stream=stream,
+                         desc=desc, gproj=args.gproj)
 
     ev = lambda: torch.cuda.Event(enable_timing=False)
-    in_done = [ev() for _ in range(e2e_steps)]
-    comp_done = [ev() for _ in range(e2e_steps)]
+    in_done = [[ev() for _ in range(3)] for _ in range(e2e_steps)]
+    op_done = [[ev() for _ in range(3)] for _ in range(e2e_steps)]
     out_done = [ev() for _ in range(e2e_steps)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -345,22 +353,25 @@ def run_ours(args, w, rank, world):
     for i in range(e2e_steps):
         b = i % 2
         if i >= 2:
-            s_in.wait_event(comp_done[i - 2])  # step i-2 has read this input buffer
-        with torch.cuda.stream(s_in):
-            for k in xin[b]:
-                xin[b][k].copy_(pinned[k], non_blocking=True)
-        in_done[i].record(s_in)
-        stream.wait_event(in_done[i])
+            s_in.wait_event(op_done[i - 2][2])  # step i-2 has read this input buffer
+        for j in range(3):
+            with torch.cuda.stream(s_in):
+                for k in op_in[j]:
+                    xin[b][k].copy_(pinned[k], non_blocking=True)
+            in_done[i][j].record(s_in)
         if i >= 2:
             stream.wait_event(out_done[i - 2])  # step i-2's outputs have left this buffer
-        with torch.cuda.stream(stream):
-            e2e_step(xin[b], outs[b], lses[b])
-        comp_done[i].record(stream)
-        s_out.wait_event(comp_done[i])
-        with torch.cuda.stream(s_out):
-            for k in out:
-                host_out[k].copy_(outs[b][k], non_blocking=True)
-            host_lse.copy_(lses[b], non_blocking=True)
+        for j in range(3):
+            stream.wait_event(in_done[i][j])
+            with torch.cuda.stream(stream):
+                e2e_op(j, xin[b], outs[b], lses[b])
+            op_done[i][j].record(stream)
+            s_out.wait_event(op_done[i][j])
+            with torch.cuda.stream(s_out):
+                for k in op_out[j]:
+                    host_out[k].copy_(outs[b][k], non_blocking=True)
+                if j == 0:
+                    host_lse.copy_(lses[b], non_blocking=True)
         out_done[i].record(s_out)
     e1.record(s_out)
     torch.cuda.synchronize()
