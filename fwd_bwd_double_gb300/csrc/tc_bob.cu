@@ -512,10 +512,15 @@ struct ColLayT {
 };
 static_assert(ColLayT<true>::bytes <= 232448, "column pass shared memory");
 
+// The column pass runs 16 compute warps (warp w: TMEM lanes 32 (w % 4) .., queries
+// 16 (w / 4) .. of each 64-query block), then the TMA, tile-MMA and output-MMA warps.
+constexpr int kColCompute = 512;
+constexpr int kColThreads = kColCompute + 96;
+constexpr int wTma = kColCompute / 32, wTile = wTma + 1, wOut = wTma + 2;
 // GR: grouped key/value heads (G > 1).  The G == 1 instance keeps the plain tile loop.
 // PAD as in the row pass.  GP as in ColLayT (tmRho: the coefficients, laid out as the states).
 template <bool GR, bool PAD, bool GP, bool WIN = false>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kColThreads, 1)
     bob_col_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmdO, const __grid_constant__ CUtensorMap tmSt,
                    const __grid_constant__ CUtensorMap tmRho, const __nv_bfloat16* __restrict__ Kp, const __nv_bfloat16* __restrict__ Bp,
@@ -556,19 +561,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&full[s], 1);
       ptx::mbar_init(&empty[s], 2);  // released by the tile warp and by the output warp
     }
-    ptx::mbar_init(held_ready, kCompute);
+    ptx::mbar_init(held_ready, kColCompute);
     ptx::mbar_init(sa_full, 1);
     ptx::mbar_init(sb_full, 1);
-    ptx::mbar_init(consumed_a, kCompute);
-    ptx::mbar_init(consumed_b, kCompute);
-    ptx::mbar_init(ready, kCompute);
+    ptx::mbar_init(consumed_a, kColCompute);
+    ptx::mbar_init(consumed_b, kColCompute);
+    ptx::mbar_init(ready, kColCompute);
     ptx::mbar_init(out_done, 1);
     ptx::mbar_init(acc_full, 1);
     *abort_flag = (ptx::smem_u32(sm) & 1023u) ? 1 : 0;
     if (*abort_flag) atomicOr(&g_err, FBD_ERR_TIMEOUT);
     ptx::fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == wTile) {
     ptx::tmem_alloc(tmem_slot, 512);
     ptx::tmem_relinquish();
   }
@@ -579,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const ptx::BoundedWait wait{abort_flag, &g_err};
   const bool ok = *abort_flag == 0;
 
-  if (warp == 8) {
+  if (warp == wTma) {
     if (lane == 0 && ok) {
       ptx::prefetch_tmap(&tmQ);
       ptx::prefetch_tmap(&tmA);
@@ -599,7 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int t = (nt > NS ? nt - NS : 0); t < nt; ++t) wait(&empty[t % NS], (t / NS) & 1);
     }
-  } else if (warp == 9) {
+  } else if (warp == wTile) {
     if (ok) {  // all 32 lanes; one elected lane issues each MMA and commit
       constexpr uint32_t id128 = ptx::idesc_bf16(BM, 2 * BN, 0, 0);
       constexpr uint32_t id64 = ptx::idesc_bf16(BM, BN, 0, 0);
@@ -638,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mma_commit_e(&empty[s]);
       }
     }
-  } else if (warp == 10) {
+  } else if (warp == wOut) {
     if (ok) {  // all 32 lanes; one elected lane issues each MMA and commit
       constexpr uint32_t idO = ptx::idesc_bf16(BM, D, 0, 1);
       const uint32_t sSt = ptx::smem_u32(sm + Lay::oStage);
@@ -673,18 +678,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = qd * 32 + lane;
     const uint32_t lo = static_cast<uint32_t>(qd * 32) << 16;
     const int key = kb * BM + r;
-    const int c0 = hf * 32;
+    const int c0 = hf * 16;  // this thread's 16 queries of each block (and 16 of the head dim)
     const int khi = (WIN && causal) ? bd.key_hi(kvh, key) : 0;  // the last query this key is seen by
-    {  // K, b, V, c rows of this key, elements 32 hf .. 32 hf + 31, into TMEM (A operands)
+    {  // K, b, V, c rows of this key, elements 16 hf .. 16 hf + 15, into TMEM (A operands)
       const __nv_bfloat16* src[4] = {Kp, Bp, Vp, Cp};
       const uint32_t col[4] = {Lay::cK, Lay::cB, Lay::cV, Lay::cC};
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
-        uint32_t w[16];
+        uint32_t w[8];
         if (key < N && c0 < hd) {
           const uint4* g = reinterpret_cast<const uint4*>(src[m] + (static_cast<size_t>(kvh) * N + key) * hd + c0);
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
+          for (int u = 0; u < 2; ++u) {
             const uint4 v = g[u];
             w[4 * u] = v.x;
             w[4 * u + 1] = v.y;
@@ -693,16 +698,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         } else {
 #pragma unroll
-          for (int u = 0; u < 16; ++u) w[u] = 0u;
+          for (int u = 0; u < 8; ++u) w[u] = 0u;
         }
-        ptx::tmem_st16(tmem + col[m] + static_cast<uint32_t>(hf * 16) + lo, w);
+        ptx::tmem_st8(tmem + col[m] + static_cast<uint32_t>(hf * 8) + lo, w);
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(held_ready);
     }
     const uint64_t c2 = tc::pk2f(c, c), s2 = tc::pk2f(scale, scale);
-    const uint32_t tOpT = tmem + Lay::cOp + static_cast<uint32_t>(hf * 16) + lo;
+    const uint32_t tOpT = tmem + Lay::cOp + static_cast<uint32_t>(hf * 8) + lo;
     for (int t = 0; t < nt; ++t) {
       const int s = t % NS, i = GR ? i0 + t % ntile : i0 + t;
       // Row states of the 64 queries, pair-interleaved: float4 2m = (-L2, -L2', -E, -E'),
@@ -712,9 +717,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int qbase = i * BN + c0;
       wait(sa_full, t & 1);
       ptx::tc_fence_after();
-      uint32_t sv[32], gv[32];
-      ptx::tmem_ld32(tmem + Lay::cT + c0 + lo, sv);
-      ptx::tmem_ld32(tmem + Lay::cT + BN + c0 + lo, gv);
+      uint32_t sv[16], gv[16];
+      ptx::tmem_ld16(tmem + Lay::cT + c0 + lo, sv);
+      ptx::tmem_ld16(tmem + Lay::cT + BN + c0 + lo, gv);
       if (t > 0) {  // block t-1's operand stores complete while this block's tiles load
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
@@ -723,14 +728,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tmem_wait_ld();
       ptx::tc_fence_before();
       ptx::mbar_arrive(consumed_a);  // the tile warp may now write [dP^T | H^T]
-      uint64_t P2[16], GE2[16];
-      uint32_t pDP[16], pDS[16], pSB[16], pPT[GP ? 16 : 1];
-      // GP: -rho of this thread's 32 queries (the stage's coefficient tile)
+      uint64_t P2[8], GE2[8];
+      uint32_t pDP[8], pDS[8], pSB[8], pPT[GP ? 8 : 1];
+      // GP: -rho of this thread's 16 queries (the stage's coefficient tile)
       const float4* nrho = reinterpret_cast<const float4*>(sm + Lay::oStage + s * Lay::kStage + 3 * kTile +
                                                            Lay::kStat) + c0 / 4;
       auto first = [&](auto masked) {  // P and P (G - E) from [S^T | G^T]
 #pragma unroll
-        for (int u = 0; u < 32; u += 2) {
+        for (int u = 0; u < 16; u += 2) {
           const float4 A = stat[u];
           const float2 arg = tc::unpk2(tc::fma2(tc::pk2(sv[u], sv[u + 1]), c2, tc::pk2f(A.x, A.y)));
           float p0 = ptx::ex2(arg.x), p1 = ptx::ex2(arg.y);
@@ -748,20 +753,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       // Causal mask only in the first blocks (queries before this CTA's last key) and in
       // those past the window of its first key; past N only in the last block.
-      if ((causal && (qbase < kb * BM + BM || (WIN && qbase + 31 > hi_first))) || qbase + 32 > N)
+      if ((causal && (qbase < kb * BM + BM || (WIN && qbase + 15 > hi_first))) || qbase + 16 > N)
         first(std::true_type{});
       else
         first(std::false_type{});
       wait(sb_full, t & 1);
       ptx::tc_fence_after();
-      uint32_t dv[32], hv[32];
-      ptx::tmem_ld32(tmem + Lay::cT + c0 + lo, dv);
-      ptx::tmem_ld32(tmem + Lay::cT + BN + c0 + lo, hv);
+      uint32_t dv[16], hv[16];
+      ptx::tmem_ld16(tmem + Lay::cT + c0 + lo, dv);
+      ptx::tmem_ld16(tmem + Lay::cT + BN + c0 + lo, hv);
       ptx::tmem_wait_ld();
       ptx::tc_fence_before();
       ptx::mbar_arrive(consumed_b);  // the tile warp may now write the next block's [S^T | G^T]
 #pragma unroll
-      for (int u = 0; u < 32; u += 2) {  // dS and Sbar from [dP^T | H^T]
+      for (int u = 0; u < 16; u += 2) {  // dS and Sbar from [dP^T | H^T]
         const float4 Bs = stat[u + 1];
         const int idx = u >> 1;
         const uint64_t dmd = tc::add2(tc::pk2(dv[u], dv[u + 1]), tc::pk2f(Bs.x, Bs.y));  // dP - D
@@ -773,7 +778,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if constexpr (GP) {  // bf16(-rho_i P_ij), formed once dP and H are out of the registers
 #pragma unroll
-        for (int u = 0; u < 32; u += 4) {
+        for (int u = 0; u < 16; u += 4) {
           const float4 r4 = nrho[u >> 2];
           const float2 a0 = tc::unpk2(tc::mul2(P2[u >> 1], tc::pk2f(r4.x, r4.y)));
           const float2 a1 = tc::unpk2(tc::mul2(P2[(u >> 1) + 1], tc::pk2f(r4.z, r4.w)));
@@ -782,32 +787,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (t > 0) wait(out_done, (t - 1) & 1);  // block t-1's products have read the operand columns
-      if constexpr (GP) ptx::tmem_st16(tmem + Lay::cPT + static_cast<uint32_t>(hf * 16) + lo, pPT);
-      ptx::tmem_st16(tOpT, pDP);
-      ptx::tmem_st16(tOpT + 32, pDS);
-      ptx::tmem_st16(tOpT + 64, pSB);  // completed (and `ready` arrived) at the next block's loads
+      if constexpr (GP) ptx::tmem_st8(tmem + Lay::cPT + static_cast<uint32_t>(hf * 8) + lo, pPT);
+      ptx::tmem_st8(tOpT, pDP);
+      ptx::tmem_st8(tOpT + 32, pDS);
+      ptx::tmem_st8(tOpT + 64, pSB);  // completed (and `ready` arrived) at the next block's loads
     }
     ptx::tmem_wait_st();
     ptx::tc_fence_before();
     ptx::mbar_arrive(ready);  // the last block's operands
     wait(acc_full, 0);
     ptx::tc_fence_after();
-    uint32_t av[32], bv[32];
-    ptx::tmem_ld32(tmem + Lay::cgV + c0 + lo, av);
-    ptx::tmem_ld32(tmem + Lay::cgK + c0 + lo, bv);
+    uint32_t av[16], bv[16];
+    ptx::tmem_ld16(tmem + Lay::cgV + c0 + lo, av);
+    ptx::tmem_ld16(tmem + Lay::cgK + c0 + lo, bv);
     ptx::tmem_wait_ld();
     if (key < N && c0 < hd) {
       const size_t rowoff = (static_cast<size_t>(kvh) * N + key) * hd;
-      uint32_t ov[16], ok2[16];
+      uint32_t ov[8], ok2[8];
 #pragma unroll
-      for (int u = 0; u < 32; u += 2) {
+      for (int u = 0; u < 16; u += 2) {
         ov[u >> 1] = ptx::pack_bf16(f(av[u]), f(av[u + 1]));
         ok2[u >> 1] = ptx::pack_bf16(scale * f(bv[u]), scale * f(bv[u + 1]));
       }
       uint4* dvp = reinterpret_cast<uint4*>(gV + rowoff + c0);
       uint4* dkp = reinterpret_cast<uint4*>(gK + rowoff + c0);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < 2; ++u) {
         dvp[u] = make_uint4(ov[4 * u], ov[4 * u + 1], ov[4 * u + 2], ov[4 * u + 3]);
         dkp[u] = make_uint4(ok2[4 * u], ok2[4 * u + 1], ok2[4 * u + 2], ok2[4 * u + 3]);
       }
@@ -816,7 +821,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == wTile) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, 512);
   }
@@ -871,7 +876,7 @@ cudaError_t tc_bob(const Problem& p, const void* Q, const void* K, const void* V
   const int cbytes = gproj ? ColLayT<true>::bytes : ColLayT<false>::bytes;
   e = cudaFuncSetAttribute(col, cudaFuncAttributeMaxDynamicSharedMemorySize, cbytes);
   if (e != cudaSuccess) return e;
-  col<<<static_cast<unsigned>(nrb * p.BHkv), kThreads, cbytes, st>>>(
+  col<<<static_cast<unsigned>(nrb * p.BHkv), kColThreads, cbytes, st>>>(
       q64, a64, do64, s64, r64, static_cast<const __nv_bfloat16*>(K), static_cast<const __nv_bfloat16*>(b),
       static_cast<const __nv_bfloat16*>(V), static_cast<const __nv_bfloat16*>(cc), static_cast<__nv_bfloat16*>(gK),
       static_cast<__nv_bfloat16*>(gV), static_cast<int>(N), static_cast<int>(p.BHkv), p.scale, c, p.causal,
