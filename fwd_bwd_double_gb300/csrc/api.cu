@@ -341,7 +341,7 @@ const char* attn_status_string(attn_status_t status) {
 
 const char* attn_last_error(void) { return g_last_error; }
 
-const char* attn_version(void) { return "libfbd 0.2 (sm_103a: tcgen05/TMA bf16 kernels, tcgen05 tf32x3 engine for float32 and the bf16 GProj backward and BoB at d = 256)"; }
+const char* attn_version(void) { return "libfbd 0.2 (sm_103a: tcgen05/TMA bf16 kernels, tcgen05 tf32x3 engine for float32 and the bf16 BoB at d = 256)"; }
 
 }  // extern "C"
 
