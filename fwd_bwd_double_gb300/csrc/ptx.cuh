@@ -154,29 +154,12 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-// D(tmem) (+)= A(smem desc) * B(smem desc), kind::f16 (bf16 inputs, f32 accumulate).
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// D(tmem) (+)= A(tmem) * B(smem desc).  A is M x K with two 16-bit values per column.
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// The same two MMAs and the commit below, executed by a whole converged warp: an
-// elect.sync inside the instruction sequence picks the one lane that issues.  The
-// MMA warps run their loops on all 32 lanes with warp-uniform operands, which
-// keeps the issue in uniform control flow; issuing from a one-lane branch costs
-// the issuing warp markedly more time per MMA and per commit.
+// tcgen05 MMAs of kind::f16 (bf16 inputs, f32 accumulate), issued by a whole converged
+// warp: an elect.sync inside the instruction sequence picks the one lane that issues.
+// The MMA warps run their loops on all 32 lanes with warp-uniform operands, which keeps
+// the issue in uniform control flow; issuing from a one-lane branch costs the issuing
+// warp markedly more time per MMA and per commit.
+// D(tmem) (+)= A(smem desc) * B(smem desc):
 __device__ __forceinline__ void mma_ss_e(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                          uint32_t accumulate) {
   asm volatile(
@@ -187,6 +170,7 @@ __device__ __forceinline__ void mma_ss_e(uint32_t d_tmem, uint64_t a_desc, uint6
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// D(tmem) (+)= A(tmem) * B(smem desc); A is M x K with two 16-bit values per column:
 __device__ __forceinline__ void mma_ts_e(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                          uint32_t accumulate) {
   asm volatile(
@@ -209,12 +193,8 @@ __device__ __forceinline__ void mma_ss_tf32_e(uint32_t d_tmem, uint64_t a_desc, 
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-// Arrive (once) on `bar` when all previously issued tcgen05 async ops of this thread complete.
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   smem_u32(bar))
-               : "memory");
-}
+// Arrive (once) on `bar` when all previously issued tcgen05 async ops of the electing
+// thread complete.
 __device__ __forceinline__ void mma_commit_e(uint64_t* bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\t.reg .b32 r;\n\t"
