@@ -176,9 +176,9 @@ size_t attn_bwd_workspace_bytes(const attn_desc_t* desc, int gproj) {
   if (desc == nullptr || desc->B < 0 || desc->H < 0 || desc->N < 0) return 0;
   // 16 bytes per row, the rows of each slice rounded up to an even count (the bf16
   // column pass reads the row statistics two rows at a time); for the single-pass bf16
-  // backward (d <= 64, no GProj) then the fp32 dQ accumulator, 256 bytes per row.
+  // backward (d <= 64, no GProj, N < 2^21) then the fp32 dQ accumulator, 256 bytes per row.
   size_t n = static_cast<size_t>(desc->B) * desc->H * ((desc->N + 1) & ~static_cast<int64_t>(1)) * 16;
-  if (desc->dtype == ATTN_BF16 && desc->d > 0 && desc->d <= 64 && !gproj)
+  if (fbd::bwd_single_pass(desc->dtype, desc->d, desc->N, gproj != 0))
     n += fbd::bwd_fused_acc_bytes(desc->B * desc->H, desc->N);
   return n;
 }

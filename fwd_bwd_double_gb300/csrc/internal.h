@@ -107,6 +107,15 @@ cudaError_t tc_bwd_wide(const Problem& p, const void* Q, const void* K, const vo
 // writes dK, dV once and reduce-adds each query block's dS K into the accumulator, and a
 // launch that scales and rounds dQ.  `ws` holds the statistics (16 bytes per row, rows of
 // a slice rounded up to even) and then the accumulator (bwd_fused_acc_bytes).
+//
+// From N = 2^21 on the two-pass form is used instead: its reduce-adds of dQ shares, one
+// per (key block, query block) pair, then run at ~2.5 TB/s instead of ~3.6, and the
+// two passes (no reduction) are as fast at 2^21 and faster beyond (B1 H12 d64: 1165 vs
+// 946 TFLOP/s at 2^20, 878 vs 888 at 2^21, 795 vs 876 at 2^22).
+constexpr int64_t kBwdSinglePassMaxN = (int64_t{1} << 21) - 1;
+inline bool bwd_single_pass(int dtype, int64_t d, int64_t N, bool gproj) {
+  return dtype == ATTN_BF16 && d > 0 && d <= 64 && !gproj && N <= kBwdSinglePassMaxN;
+}
 bool bwd_fused_applies(const Problem& p, bool gproj);
 inline size_t bwd_fused_acc_bytes(int64_t BH, int64_t N) { return static_cast<size_t>(BH) * N * 64 * sizeof(float); }
 cudaError_t tc_bwd_fused(const Problem& p, const void* Q, const void* K, const void* V, const void* O,

@@ -471,7 +471,7 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ a
 
 }  // namespace
 
-bool bwd_fused_applies(const Problem& p, bool gproj) { return p.dtype == ATTN_BF16 && p.d <= 64 && !gproj; }
+bool bwd_fused_applies(const Problem& p, bool gproj) { return bwd_single_pass(p.dtype, p.d, p.N, gproj); }
 
 cudaError_t tc_bwd_fused(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
                          const void* dO, const float* lse, void* dQ, void* dK, void* dV, float4* ws,

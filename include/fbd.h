@@ -171,8 +171,8 @@ attn_status_t attn_fwd(const attn_desc_t* desc, const void* Q, const void* K, co
 /* Workspace for attn_bwd: 16 bytes per (b,h,row), the rows of each slice rounded
  * up to an even count: the row statistics (lse, D, GProj coefficient) read by the
  * column pass (layout internal to the library); for bf16 at d <= 64 without GProj
- * (the single-pass form of attn_bwd) 256 bytes more per (b,h,row) for an fp32 dQ
- * accumulator. */
+ * and N < 2^21 (the single-pass form of attn_bwd) 256 bytes more per (b,h,row) for an
+ * fp32 dQ accumulator. */
 size_t attn_bwd_workspace_bytes(const attn_desc_t* desc, int gproj);
 
 /* Recompute backward.  [FA] "Backward pass: recompute instead of store": P is
@@ -180,12 +180,14 @@ size_t attn_bwd_workspace_bytes(const attn_desc_t* desc, int gproj);
  *   dP = dO V^T, D_i = sum_k dO_ik O_ik, dS = P * (dP - D):
  *   dQ = s dS K,  dK = s dS^T Q,  dV = P^T dO          (all [B,H,N,d]).
  * Two launches on `stream`: a row pass (dQ and the row statistics) and a column
- * pass (dK, dV).  For bf16 at d <= 64 without GProj, the single-pass form instead
+ * pass (dK, dV).  For bf16 at d <= 64 without GProj and N < 2^21, the single-pass form instead
  * ([FA] "FA2: parallelism": the work split over key blocks, the query gradient summed
  * across them): a launch forming D and the row statistics, one launch over key blocks
  * that writes dK, dV once and adds each key block's dS K share of dQ into an fp32
  * accumulator in the workspace (tensor reduce-adds in L2), and a launch that writes
- * dQ = s * accumulator once, rounded to bf16.  Every contraction then runs once.  The
+ * dQ = s * accumulator once, rounded to bf16.  Every contraction then runs once.  (From
+ * N = 2^21 on its reduce-adds of dQ shares slow down and the two passes are as fast or
+ * faster, so those lengths take the two passes.)  The
  * shares are added in the order the key blocks reach a query block, so dQ may differ
  * between calls in its last bits (two bf16 steps at most); dK and dV, and every output
  * of the two-pass forms, are the same bits on every call.

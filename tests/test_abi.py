@@ -111,6 +111,10 @@ def test_workspace_checks():
     assert lib.attn_bwd_workspace_bytes(ctypes.byref(desc(B=2, H=3, N=100, d=128)), 0) == 2 * 3 * 100 * 16
     assert lib.attn_bwd_workspace_bytes(ctypes.byref(desc(B=2, H=3, N=100, dtype=0)), 0) == 2 * 3 * 100 * 16
     assert lib.attn_bwd_workspace_bytes(ctypes.byref(desc(B=1, H=1, N=7, d=32)), 0) == 8 * 16 + 7 * 256
+    # From N = 2^21 on the backward takes its two passes: the statistics alone.
+    n1 = (1 << 21) - 1
+    assert lib.attn_bwd_workspace_bytes(ctypes.byref(desc(B=1, H=2, N=n1)), 0) == 2 * (n1 + 1) * 16 + 2 * n1 * 256
+    assert lib.attn_bwd_workspace_bytes(ctypes.byref(desc(B=1, H=2, N=1 << 21)), 0) == 2 * (1 << 21) * 16
     assert lib.attn_bob_workspace_bytes(ctypes.byref(d), 0) == 2 * 3 * 100 * 16
     assert bwd(d, ws_bytes=2 * 3 * 100 * (16 + 256) - 1) == WS
     assert bob(d, ws_bytes=0) == WS
