@@ -489,7 +489,7 @@ def max_n_report(exec_n=1 << 20, check=True):
     # workspace is the 16-byte row statistics alone; the bisection allocates what the
     # library asks for at each N.
     big = 1 << 24
-    per_token = {op: ntensor[op] * row + 4 * H + ws_bytes(op, big) / big for op in ("bob", "bwd")}
+    per_token = {op: ntensor[op] * row + 4 * H + ws_bytes(op, big) // big for op in ("bob", "bwd")}
     free, total = torch.cuda.mem_get_info(dev)
     out = {"metric": "max N in HBM (B=1, H=12, d=64, bf16)", "hbm_total_bytes": total, "hbm_free_bytes": free,
            "basis": "allocation-only: the largest N whose whole buffer set (inputs, outputs, lse, workspace) "

@@ -135,6 +135,23 @@ def test_long_sweep_sampled(N):
     print(w.name, {k: f"{v:.2e}" for k, v in errs.items()})
 
 
+def test_backward_two_passes_from_n_2_21():
+    """At N = 2^21 the bf16 backward at d = 64 takes its two passes (the single-pass form
+    only runs below that length): sampled rows of dQ and late columns of dK, dV of both
+    heads against the oracle, and the workspace it asks for is the statistics alone."""
+    import fwd_bwd_double_gb300 as fbd
+    N = 1 << 21
+    w = W.Workload(f"longbwd_B1H2N{N}d64_bf16", 1, 2, N, 64, "bf16")
+    x = to_device(W.inputs(w, names=("Q", "K", "V", "dO")), w)
+    assert fbd.attn_bwd_workspace_bytes(fbd.make_desc(x["Q"]), 0) == 2 * N * 16
+    got = run_ops(w, x, ops=("fwd", "bwd"))
+    rng = np.random.default_rng(21)
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, N // 2, N - 2, N - 1], rng.integers(0, N, 16)]))
+    cols = np.arange(N - 48, N)  # the last keys: each needs only the queries after it
+    errs = sampled_check(w, got, ("bwd",), heads=[0, 1], rows=rows, cols=cols)
+    print(w.name, {k: f"{v:.2e}" for k, v in errs.items()})
+
+
 @pytest.mark.parametrize("d", [64, 256])
 def test_f32_long_sampled(d):
     """float32 on the tf32 engine over many key blocks with a ragged tail (N = 5000:
