@@ -161,18 +161,18 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    """nvidia-smi clocks / throttle reasons sampled every `ms` milliseconds while running."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index=0):
-        self.index, self.rows, self.proc = index, [], None
+    def __init__(self, index=0, ms=200):
+        self.index, self.ms, self.rows, self.proc = index, ms, [], None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.ms)],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -201,8 +201,10 @@ class ClockSampler:
         mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in self.rows for i in range(4) if r[5 + i].lower() == "active"})
+        pw = [float(r[3]) for r in self.rows if r[3].replace(".", "").isdigit()]
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(self.rows)}
+                "reasons": reasons, "samples": len(self.rows),
+                "sm_mhz_min": min(sm) if sm else None, "power_w_max": max(pw) if pw else None}
 
 
 def make_inputs(w, device):
@@ -350,7 +352,10 @@ def run_ours(args, w, rank, world):
     out_done = [ev() for _ in range(e2e_steps)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
+    clk_e2e = ClockSampler(dev.index, ms=50).__enter__()
+    time.sleep(0.25)  # the sampler's first readings come a little after it starts
     e0.record(s_in)
+    t_issue = time.perf_counter()
     for i in range(e2e_steps):
         b = i % 2
         if i >= 2:
@@ -375,7 +380,9 @@ def run_ours(args, w, rank, world):
                     host_lse.copy_(lses[b], non_blocking=True)
         out_done[i].record(s_out)
     e1.record(s_out)
+    host_issue_ms = (time.perf_counter() - t_issue) * 1e3 / e2e_steps  # the host's time to enqueue a step
     torch.cuda.synchronize()
+    clk_e2e.__exit__(None, None, None)
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     h2d = sum(v.numel() * v.element_size() for v in pinned.values())
     d2h = sum(v.numel() * v.element_size() for v in host_out.values()) + host_lse.numel() * 4
@@ -383,7 +390,7 @@ def run_ours(args, w, rank, world):
                 per_kernel={kn: statistics.mean(v) for kn, v in per_kernel.items()},
                 flops_step=flops_step, wall=wall, clocks=clk.summary(), bwd_gproj_ms=(bwd0, bwd1),
                 bob_gproj_ms=(bob0, bob1),
-                e2e_ms=e2e_ms, h2d=h2d, d2h=d2h)
+                e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, host_issue_ms=host_issue_ms, e2e_clocks=clk_e2e.summary())
 
 
 def cpu_baseline(w, budget_s=20.0):
@@ -786,7 +793,9 @@ def main():
                      "executed_frac": (tf(executed_flops(w, dom, args.gproj), r["per_kernel"][dom]) / pk["bf16_tflops"]
                                        if executed_flops(w, dom, args.gproj) else None)},
         "e2e": {"value": r["flops_step"] / (r["e2e_ms"] * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
-                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["e2e_ms"]},
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["e2e_ms"],
+                "host_issue_ms_per_step": r["host_issue_ms"],
+                "clocks": r["e2e_clocks"]},
         "gpu_launches": launches_per_step(w, args.gproj) * args.steps,
         "clocks": r["clocks"],
     }
