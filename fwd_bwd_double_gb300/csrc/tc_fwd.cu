@@ -23,7 +23,10 @@
 // S_{j+1} = Q K_{j+1}^T runs on the tensor pipe while they exponentiate S_j; P_j
 // is written into its TMEM columns, and O rescaled, only after P_{j-1} V_{j-1}
 // has finished (`pv_done`).  With d = 64 two CTAs fit on an SM (256 TMEM columns
-// each), so one CTA's softmax also overlaps the other's MMAs.
+// each), so one CTA's softmax also overlaps the other's MMAs.  At d = 256 (224 threads)
+// K and V have a 128-key buffer each and their own TMA warps (4: K, 6: V): K_{j+1} loads
+// as soon as S_j is done (`k_empty`), V_{j+1} as soon as P_j V_j is (`empty`), so the
+// 128-key blocks fit beside the 64 KB Q tile.
 //
 // The PB instance serves the GProj form of the backward over backward: with the
 // stored log-sum-exp L and the cotangent b in place of V it accumulates
@@ -43,15 +46,18 @@ namespace {
 __device__ unsigned int g_err = 0;
 
 constexpr int BM = 128;
-constexpr int kThreads = 192;
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
 struct Layout {
-  // Key blocks of BN keys through an NS-stage ring: 128 keys, 3 stages up to d = 128
-  // (2 CTAs per SM at d = 64 still fit); 64 keys, 2 stages at d = 256 (Q alone is 64 KB).
-  static constexpr int BN = D <= 128 ? 128 : 64;
-  static constexpr int NS = D <= 128 ? 3 : 2;
+  // Key blocks of BN = 128 keys.  Up to d = 128 they come through a ring of NS = 3 stages
+  // of K and V (2 CTAs per SM at d = 64 still fit).  At d = 256 (SPLIT) the Q tile alone is
+  // 64 KB: K and V have one 128-key buffer each, reloaded independently as soon as the
+  // product reading it is done (K after S_j, V after P_j V_j), by a TMA warp each.
+  static constexpr bool SPLIT = D > 128;
+  static constexpr int BN = 128;
+  static constexpr int NS = SPLIT ? 1 : 3;
+  static constexpr int kThreads = SPLIT ? 224 : 192;  // 4 softmax warps, TMA, MMA (+ the V loader)
   static constexpr int kQ = BM * D * 2;   // bytes of the Q tile
   static constexpr int kKV = BN * D * 2;  // bytes of one K (or V) tile
   static constexpr int oQ = 0;
@@ -77,7 +83,7 @@ __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int rows, int k)
 // WIN: a banded causal mask is in force (bd: the sliding window and/or the document
 // bounds); the instances without it carry none of its arithmetic.
 template <int D, bool PB, bool WIN>
-__global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
+__global__ void __launch_bounds__(Layout<D>::kThreads, (D == 64 ? 2 : 1))
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O, float* __restrict__ lse,
                const float* __restrict__ lse_in, float* __restrict__ pb, int N, int nrb, int BH, float scale,
@@ -94,7 +100,10 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
   uint64_t* o_full = s_full + 2;
   uint64_t* s_consumed = s_full + 3;  // S_j copied into the softmax registers
   uint64_t* pv_done = s_full + 4;     // P_j V_j finished: P columns and O free
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 5);
+  // SPLIT: full[0] = K_j loaded, empty[0] = P_j V_j done (the V buffer free), and
+  uint64_t* v_full = s_full + 5;      // V_j loaded
+  uint64_t* k_empty = s_full + 6;     // S_j done (the K buffer free)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + (Lay::SPLIT ? 7 : 5));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -121,6 +130,10 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
     ptx::mbar_init(o_full, 1);
     ptx::mbar_init(s_consumed, 128);
     ptx::mbar_init(pv_done, 1);
+    if constexpr (Lay::SPLIT) {
+      ptx::mbar_init(v_full, 1);
+      ptx::mbar_init(k_empty, 1);
+    }
     // The swizzled operand layout needs 1024-byte aligned tiles.
     *abort_flag = (ptx::smem_u32(sm) & 1023u) ? 1 : 0;
     if (*abort_flag) atomicOr(&g_err, FBD_ERR_TIMEOUT);
@@ -148,17 +161,27 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
       ptx::prefetch_tmap(&tmV);
       ptx::mbar_expect_tx(q_full, Lay::kQ);
       for (int c = 0; c < D / 64; ++c) ptx::tma_load_3d(sm + Lay::oQ + c * BM * 128, &tmQ, q_full, c * 64, rb * BM, bh);
-      for (int j = 0; j < nkv; ++j) {
-        const int s = j % NS;
-        if (j >= NS) wait(&empty[s], ((j / NS) - 1) & 1);
-        ptx::mbar_expect_tx(&full[s], 2 * Lay::kKV);
-        for (int c = 0; c < D / 64; ++c) {
-          ptx::tma_load_3d(sm + Lay::oK + s * Lay::kKV + c * BN * 128, &tmK, &full[s], c * 64, (j0 + j) * BN, kvh);
-          ptx::tma_load_3d(sm + Lay::oV + s * Lay::kKV + c * BN * 128, &tmV, &full[s], c * 64, (j0 + j) * BN, kvh);
+      if constexpr (Lay::SPLIT) {  // K only (the V loader is warp 6)
+        for (int j = 0; j < nkv; ++j) {
+          if (j >= 1) wait(k_empty, (j - 1) & 1);
+          ptx::mbar_expect_tx(&full[0], Lay::kKV);
+          for (int c = 0; c < D / 64; ++c)
+            ptx::tma_load_3d(sm + Lay::oK + c * BN * 128, &tmK, &full[0], c * 64, (j0 + j) * BN, kvh);
         }
+        if (nkv > 0) wait(k_empty, (nkv - 1) & 1);
+      } else {
+        for (int j = 0; j < nkv; ++j) {
+          const int s = j % NS;
+          if (j >= NS) wait(&empty[s], ((j / NS) - 1) & 1);
+          ptx::mbar_expect_tx(&full[s], 2 * Lay::kKV);
+          for (int c = 0; c < D / 64; ++c) {
+            ptx::tma_load_3d(sm + Lay::oK + s * Lay::kKV + c * BN * 128, &tmK, &full[s], c * 64, (j0 + j) * BN, kvh);
+            ptx::tma_load_3d(sm + Lay::oV + s * Lay::kKV + c * BN * 128, &tmV, &full[s], c * 64, (j0 + j) * BN, kvh);
+          }
+        }
+        // Drain: the last NS stages must have been consumed before the CTA exits.
+        for (int j = (nkv > NS ? nkv - NS : 0); j < nkv; ++j) wait(&empty[j % NS], (j / NS) & 1);
       }
-      // Drain: the last NS stages must have been consumed before the CTA exits.
-      for (int j = (nkv > NS ? nkv - NS : 0); j < nkv; ++j) wait(&empty[j % NS], (j / NS) & 1);
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------- MMA issuer
@@ -179,6 +202,7 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
           ptx::mma_ss_e(tS, tc::desc_add(dQ, tc::kmajor_off(BM, kk)), tc::desc_add(dK, so + tc::kmajor_off(BN, kk)), idS,
                       kk > 0 ? 1u : 0u);
         ptx::mma_commit_e(s_full);
+        if constexpr (Lay::SPLIT) ptx::mma_commit_e(k_empty);  // the K buffer may be refilled
       };
       wait(q_full, 0);
       issue_s(0);
@@ -188,6 +212,7 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
           issue_s(j + 1);
         }
         wait(p_ready, j & 1);  // P_j written, O rescaled
+        if constexpr (Lay::SPLIT) wait(v_full, j & 1);
         ptx::tc_fence_after();
         const uint32_t so = static_cast<uint32_t>((j % NS) * Lay::kKV);
 #pragma unroll
@@ -197,6 +222,17 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
         ptx::mma_commit_e(pv_done);
       }
       ptx::mma_commit_e(o_full);
+    }
+  } else if (Lay::SPLIT && warp == 6) {
+    // ----------------------------------------------- V loader (d = 256)
+    if (lane == 0 && ok) {
+      for (int j = 0; j < nkv; ++j) {
+        if (j >= 1) wait(&empty[0], (j - 1) & 1);  // P_{j-1} V_{j-1} has read the V buffer
+        ptx::mbar_expect_tx(v_full, Lay::kKV);
+        for (int c = 0; c < D / 64; ++c)
+          ptx::tma_load_3d(sm + Lay::oV + c * BN * 128, &tmV, v_full, c * 64, (j0 + j) * BN, kvh);
+      }
+      if (nkv > 0) wait(&empty[0], (nkv - 1) & 1);
     }
   } else if constexpr (PB) {
     // ------------------------------- P^ b: thread r owns query row r, L is known
@@ -401,7 +437,7 @@ cudaError_t launch(const Problem& p, const void* Q, const void* K, const void* V
   auto kern = banded(p) ? fwd_kernel<D, PB, true> : fwd_kernel<D, PB, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<static_cast<unsigned>(nrb * p.BH), kThreads, smem, st>>>(
+  kern<<<static_cast<unsigned>(nrb * p.BH), Layout<D>::kThreads, smem, st>>>(
       mq, mk, mv, static_cast<__nv_bfloat16*>(O), lse, lse_in, pb, static_cast<int>(p.N), nrb,
       static_cast<int>(p.BH), p.scale, p.scale * kLog2e, p.causal, make_band(p, eff_window_tc(p), false), p.group,
       static_cast<int>(p.d));
@@ -413,7 +449,7 @@ cudaError_t launch(const Problem& p, const void* Q, const void* K, const void* V
 cudaError_t tc_fwd(const Problem& p, const void* Q, const void* K, const void* V, void* O, float* lse,
                    cudaStream_t st) {
   // d = 32 runs the d = 64 kernel and d = 96 the d = 128 one, zero-padded in shared memory.
-  // d = 256: 64-key blocks (the Q tile alone takes 64 KB of shared memory).
+  // d = 256: one K and one V buffer, each reloaded on its own (the Q tile alone takes 64 KB).
   return p.d <= 64    ? launch<64, false>(p, Q, K, V, O, lse, nullptr, nullptr, st)
          : p.d <= 128 ? launch<128, false>(p, Q, K, V, O, lse, nullptr, nullptr, st)
                       : launch<256, false>(p, Q, K, V, O, lse, nullptr, nullptr, st);
