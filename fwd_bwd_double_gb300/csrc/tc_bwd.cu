@@ -44,7 +44,8 @@ constexpr int BN = 64;         // rows of a streamed block
 // Shared-memory stages of streamed tiles: deep enough that a tile is requested
 // several tile-times before its MMA needs it (L2/HBM latency under load).
 // At d = 256 one stage is all that fits beside the held block (64 KB a tile); the MMA
-// warp then finishes each block's products before the next block's tiles (see below).
+// warp then finishes each block's products before the next block's tiles (see below),
+// and the row pass keeps K and V in buffers reloaded on their own (RowLay::SPLIT).
 template <int D>
 constexpr int stages() { return D == 64 ? 6 : D == 256 ? 1 : 4; }
 constexpr int kCompute = 256;  // 8 compute warps
@@ -69,6 +70,11 @@ struct RowLay {
   static constexpr int kTmem = kCols <= 256 ? 256 : 512;
   static constexpr int kMinBlocks = kTmem == 256 ? 2 : 1;
   static constexpr int NS = kTmem == 256 ? 4 : stages<D>();
+  // One stage (d = 256): K and V in buffers of their own, each reloaded as soon as the
+  // products reading it are done (V after dP_j, K after S_j and the dQ product), V by a
+  // second TMA warp, so that dP_{j+1} runs while K_{j+1} loads.
+  static constexpr bool SPLIT = NS == 1;
+  static constexpr int kThreadsRow = kThreads + (SPLIT ? 32 : 0);
   static constexpr int kHeld = BM * D * 2;
   static constexpr int kStream = BN * D * 2;
   static constexpr int oQ = 0, odO = kHeld, oK = 2 * kHeld, oV = oK + NS * kStream;
@@ -84,7 +90,7 @@ struct RowLay {
 // WIN: a banded causal mask is in force (bd: the sliding window and/or the document
 // bounds); the other instances carry none of it.
 template <int D, int NB, bool GP, bool WIN = false>
-__global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
+__global__ void __launch_bounds__(RowLay<D, NB, GP>::kThreadsRow, RowLay<D, NB, GP>::kMinBlocks)
     bwd_row_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                    const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const __nv_bfloat16* __restrict__ O, const __nv_bfloat16* __restrict__ dO,
@@ -102,7 +108,10 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
   uint64_t* consumed = ds_ready + NB;   // the block's S, dP copied out: the tile columns are free
   uint64_t* out_done = consumed + 1;    // the block's dQ (and P^ K) products have read the operands
   uint64_t* acc_full = out_done + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+  // SPLIT: full[0] / empty[0] are K's (loaded / read by S_j and the dQ product), and
+  uint64_t* v_full = acc_full + 1;   // V_j loaded
+  uint64_t* v_empty = acc_full + 2;  // dP_j done: the V buffer free
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + (Lay::SPLIT ? 3 : 1));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* red = reinterpret_cast<float*>(sm + Lay::oRed);
 
@@ -130,6 +139,10 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
     ptx::mbar_init(consumed, kCompute);
     ptx::mbar_init(out_done, 1);
     ptx::mbar_init(acc_full, 1);
+    if constexpr (Lay::SPLIT) {
+      ptx::mbar_init(v_full, 1);
+      ptx::mbar_init(v_empty, 1);
+    }
     *abort_flag = (ptx::smem_u32(sm) & 1023u) ? 1 : 0;
     if (*abort_flag) atomicOr(&g_err, FBD_ERR_TIMEOUT);
     ptx::fence_mbar_init();
@@ -158,15 +171,27 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
       for (int j = 0; j < nkv; ++j) {
         const int s = j % NS;
         if (j >= NS) wait(&empty[s], ((j / NS) - 1) & 1);
-        ptx::mbar_expect_tx(&full[s], 2 * Lay::kStream);
+        ptx::mbar_expect_tx(&full[s], (Lay::SPLIT ? 1 : 2) * Lay::kStream);
         for (int cc = 0; cc < D / 64; ++cc) {
           ptx::tma_load_3d(sm + Lay::oK + s * Lay::kStream + cc * BN * 128, &tmK, &full[s], cc * 64, (j0 + j) * BN,
                            bh / G);
-          ptx::tma_load_3d(sm + Lay::oV + s * Lay::kStream + cc * BN * 128, &tmV, &full[s], cc * 64, (j0 + j) * BN,
-                           bh / G);
+          if constexpr (!Lay::SPLIT)
+            ptx::tma_load_3d(sm + Lay::oV + s * Lay::kStream + cc * BN * 128, &tmV, &full[s], cc * 64,
+                             (j0 + j) * BN, bh / G);
         }
       }
       for (int j = (nkv > NS ? nkv - NS : 0); j < nkv; ++j) wait(&empty[j % NS], (j / NS) & 1);
+    }
+  } else if (Lay::SPLIT && warp == kThreads / 32) {
+    // ------------------------------------------------- V loader (one stage)
+    if (lane == 0 && ok) {
+      for (int j = 0; j < nkv; ++j) {
+        if (j >= 1) wait(v_empty, (j - 1) & 1);  // dP_{j-1} has read the V buffer
+        ptx::mbar_expect_tx(v_full, Lay::kStream);
+        for (int cc = 0; cc < D / 64; ++cc)
+          ptx::tma_load_3d(sm + Lay::oV + cc * BN * 128, &tmV, v_full, cc * 64, (j0 + j) * BN, bh / G);
+      }
+      if (nkv > 0) wait(v_empty, (nkv - 1) & 1);
     }
   } else if (warp == 9) {
     // ---------------------------------------------------------------- MMA
@@ -194,21 +219,42 @@ __global__ void __launch_bounds__(kThreads, RowLay<D, NB, GP>::kMinBlocks)
       // Block j's tiles go into the columns block j-1's tiles left as soon as the
       // compute warps have copied those out (`consumed`), ahead of block j-1's products.
       // With a single stage the block's own products come first (they read K_j, which
-      // the next block's load replaces).
+      // the next block's load replaces); V_{j+1} is loaded as soon as dP_j is done, so
+      // dP_{j+1} runs on the pipe while K_{j+1} comes in.
       wait(q_full, 0);
       for (int j = 0; j < nkv; ++j) {
         const int s = j % NS, b = j % NB;
-        wait(&full[s], (j / NS) & 1);
-        if (j > 0) wait(consumed, (j - 1) & 1);
-        ptx::tc_fence_after();
         const uint32_t kt = sK + s * Lay::kStream, vt = sV + s * Lay::kStream;
+        if constexpr (Lay::SPLIT) {
+          // dP_j first (V_j came in while the previous block's products ran), then S_j once
+          // K_j has replaced K_{j-1}.
+          if (j > 0) wait(consumed, (j - 1) & 1);
+          wait(v_full, j & 1);
+          ptx::tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          ptx::mma_ss_e(tmem + Lay::cS + b * BN, tc::kmajor_desc(sQ, BM, kk), tc::kmajor_desc(kt, BN, kk), idS, kk > 0);
+          for (int kk = 0; kk < D / 16; ++kk)
+            ptx::mma_ss_e(tmem + Lay::cdP + b * BN, tc::kmajor_desc(sdO, BM, kk), tc::kmajor_desc(vt, BN, kk), idS,
+                          kk > 0);
+          ptx::mma_commit_e(v_empty);
+          wait(&full[s], (j / NS) & 1);
+          ptx::tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          ptx::mma_ss_e(tmem + Lay::cdP + b * BN, tc::kmajor_desc(sdO, BM, kk), tc::kmajor_desc(vt, BN, kk), idS,
-                      kk > 0);
+          for (int kk = 0; kk < D / 16; ++kk)
+            ptx::mma_ss_e(tmem + Lay::cS + b * BN, tc::kmajor_desc(sQ, BM, kk), tc::kmajor_desc(kt, BN, kk), idS,
+                          kk > 0);
+        } else {
+          wait(&full[s], (j / NS) & 1);
+          if (j > 0) wait(consumed, (j - 1) & 1);
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            ptx::mma_ss_e(tmem + Lay::cS + b * BN, tc::kmajor_desc(sQ, BM, kk), tc::kmajor_desc(kt, BN, kk), idS,
+                          kk > 0);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            ptx::mma_ss_e(tmem + Lay::cdP + b * BN, tc::kmajor_desc(sdO, BM, kk), tc::kmajor_desc(vt, BN, kk), idS,
+                          kk > 0);
+        }
         ptx::mma_commit_e(&s_full[b]);
         if constexpr (NS == 1) {
           products(j);
@@ -617,7 +663,7 @@ cudaError_t launch(const Problem& p, const void* Q, const void* K, const void* V
     auto kern = banded(p) ? bwd_row_kernel<D, NBR, GP, true> : bwd_row_kernel<D, NBR, GP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::bytes);
     if (e != cudaSuccess) return e;
-    kern<<<static_cast<unsigned>(nrb * BH * (D / Lay::DO)), kThreads, Lay::bytes, st>>>(
+    kern<<<static_cast<unsigned>(nrb * BH * (D / Lay::DO)), Lay::kThreadsRow, Lay::bytes, st>>>(
         q128, do128, k64, v64, static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), lse,
         static_cast<__nv_bfloat16*>(dQ), ws, static_cast<int>(N), static_cast<int>(Np), nrb, static_cast<int>(BH),
         p.scale, c, p.causal, make_band(p, eff_window_tc(p), false), p.group, static_cast<int>(d));
